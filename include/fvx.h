@@ -1,0 +1,209 @@
+/*
+ * fvx — sparse-voxel IndexGrid build, 3x3x3 kernel map and sparse convolution
+ * on one GB300 (sm_103a).  Plain C ABI: opaque handles, plain pointers and
+ * sizes; no C++ or torch types cross this boundary.
+ *
+ * Sources (page title, section):
+ *   [fVDB-notes]  "fVDB: A Deep-Learning Framework for Sparse, Large Scale, and
+ *                 High Performance Spatial Intelligence" (reading notes):
+ *                 "Core method", "IndexGrid", "GPU-accelerated IndexGrid
+ *                 build", "Sparse-convolution operators".
+ *   [fVDB-ONNX]   "Proposal: ONNX Runtime support for fVDB operations",
+ *                 §1.1 Tensor Representations, §1.2 Custom Operator Schemas.
+ *   [DriveRT]     "DriveRT": "Shared neighbour maps", "Counts kept on the GPU",
+ *                 "Kernels selected per GPU", "Compilation and deployment"
+ *                 (C ABI; dynamic sizes are never truncated), "Inspection and
+ *                 debugging" (errors name what failed).
+ *
+ * Conventions shared by every call
+ *   - Device pointers are CUDA global-memory addresses on the current device;
+ *     host pointers are ordinary process memory.  Every argument says which.
+ *   - Every call is asynchronous on the given stream unless it says it
+ *     synchronises.  fvx_stream is a cudaStream_t (NULL = legacy default).
+ *   - The library owns grids and kernel maps (their sizes depend on the data)
+ *     and frees them in *_destroy.  The caller owns coordinates, features,
+ *     weights and outputs.
+ *   - Every call returns an fvx_status; nothing throws across the ABI.
+ *     fvx_last_error() gives a message naming the call, argument or kernel.
+ *   - Coordinates are signed int32 voxel indices (i, j, k).  Active indices are
+ *     0-based ranks in the canonical tree order: batch, then root tile
+ *     (floor(c/4096), signed), then upper-node child, lower-node child and
+ *     voxel-in-leaf, each child position in x-major order.  Absent -> -1.
+ */
+#ifndef FVX_H
+#define FVX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct fvx_grid_s* fvx_grid;
+typedef struct fvx_kmap_s* fvx_kmap;
+typedef void* fvx_stream; /* cudaStream_t */
+
+typedef enum {
+  FVX_OK = 0,
+  FVX_ERR_INVALID_ARG = 1,    /* malformed argument (sizes, offsets, dtype) */
+  FVX_ERR_RANGE = 2,          /* data outside the supported range (see call) */
+  FVX_ERR_CAPACITY = 3,       /* a caller buffer is too small; required size reported */
+  FVX_ERR_ALLOC = 4,          /* the allocator returned NULL */
+  FVX_ERR_CUDA = 5,           /* a CUDA runtime call or kernel launch failed */
+  FVX_ERR_DEVICE_TIMEOUT = 6, /* a bounded device-side wait gave up */
+  FVX_ERR_CHECK = 7           /* a device-side check failed (see fvx_last_error) */
+} fvx_status;
+
+typedef enum { FVX_F32 = 0, FVX_BF16 = 1 } fvx_dtype;
+
+/* Device memory the library allocates for grids, kernel maps and temporary
+ * buffers goes through these callbacks (stream-ordered).  Default (or after
+ * passing NULLs): cudaMallocAsync / cudaFreeAsync on the call's stream.
+ * alloc returns NULL on failure; the call then returns FVX_ERR_ALLOC. */
+typedef void* (*fvx_alloc_fn)(size_t bytes, fvx_stream stream, void* ctx);
+typedef void (*fvx_free_fn)(void* ptr, fvx_stream stream, void* ctx);
+fvx_status fvx_set_allocator(fvx_alloc_fn alloc, fvx_free_fn free_fn, void* ctx);
+
+/* ---------------------------------------------------------------------------
+ * IndexGrid build  [fVDB-notes, "GPU-accelerated IndexGrid build", steps 1-12;
+ * "IndexGrid"; fVDB-ONNX §1.2 GridFromIJK]
+ *
+ * coords        device int32 [n_rows, 3], row-major; rows need not be sorted or
+ *               unique (duplicates collapse to one active voxel).
+ * n_rows        >= 0; at most 2^31 - 2.  n_rows == 0 gives an empty grid.
+ * batch_offsets HOST int64 [B + 1], CSR over rows: batch b owns rows
+ *               [batch_offsets[b], batch_offsets[b+1]); monotone, starts at 0,
+ *               ends at n_rows.  [fVDB-ONNX §1.1: joffsets]
+ * B             >= 1.
+ * out           receives the new grid handle (library-owned).
+ *
+ * Topology: the root is the sorted list of (batch, tile) upper nodes; an upper
+ * node holds a 32^3-bit child mask, a lower node 16^3 bits, a leaf 8^3 bits in
+ * an 80-byte record: 8 mask words, the index of its first active voxel and the
+ * popcounts of words 0..w-1 (w = 1..7) in 9-bit fields.  [fVDB-notes, "Core
+ * method": fanout 32/16/8; "IndexGrid": 80 bytes per leaf]
+ *
+ * Synchronises the stream twice (to size the sort keys and to size the
+ * topology).  Errors: FVX_ERR_INVALID_ARG (NULL pointers, bad offsets),
+ * FVX_ERR_RANGE (the packed sort keys would need more than 64 bits: only
+ * possible with very many batches spread over the full int32 range),
+ * FVX_ERR_ALLOC, FVX_ERR_CUDA. */
+fvx_status fvx_build_grid(const int32_t* coords, int64_t n_rows, const int64_t* batch_offsets, int32_t B,
+                          fvx_stream stream, fvx_grid* out);
+
+/* Counts of a built grid (host values, no device work). */
+fvx_status fvx_grid_counts(fvx_grid g, int64_t* n_upper, int64_t* n_lower, int64_t* n_leaf, int64_t* n_active);
+
+/* Device pointers into the grid's topology, owned by the grid (valid until
+ * fvx_grid_destroy).  All arrays are in canonical order.  32-byte aligned. */
+typedef struct {
+  int32_t batch_size;
+  int64_t n_rows, n_upper, n_lower, n_leaf, n_active;
+  const int32_t* ijk;                 /* [n_active, 3]  coordinate of each index (sidecar order) */
+  const int32_t* row_to_index;        /* [n_rows]       active index of each input row */
+  const int64_t* voxel_batch_offsets; /* [B + 1]        CSR of active indices per batch */
+  const int32_t* leaf_origin;         /* [n_leaf, 3] */
+  const int32_t* leaf_batch;          /* [n_leaf] */
+  const uint64_t* leaf_records;       /* [n_leaf, 10]: mask[8], first index, packed 9-bit prefix */
+  const int32_t* lower_origin;        /* [n_lower, 3] */
+  const int32_t* lower_batch;         /* [n_lower] */
+  const uint64_t* lower_mask;         /* [n_lower, 64]  child leaves, bit n = (x*16+y)*16+z */
+  const uint32_t* lower_prefix;       /* [n_lower, 64]  popcount of mask words before w */
+  const uint32_t* lower_first;        /* [n_lower]      index of the first child leaf */
+  const int32_t* upper_origin;        /* [n_upper, 3] */
+  const int32_t* upper_batch;         /* [n_upper] */
+  const uint64_t* upper_mask;         /* [n_upper, 512] child lower nodes, bit n = (x*32+y)*32+z */
+  const uint32_t* upper_prefix;       /* [n_upper, 512] */
+  const uint32_t* upper_first;        /* [n_upper]      index of the first child lower node */
+} fvx_grid_view_t;
+fvx_status fvx_grid_view(fvx_grid g, fvx_grid_view_t* view);
+
+/* Host copy of the per-batch voxel offsets [B + 1] (synchronises the grid's
+ * last stream on first call). */
+fvx_status fvx_grid_batch_offsets(fvx_grid g, int64_t* host_out);
+
+/* Coordinate -> active index or -1, by tree walk: root search, then upper and
+ * lower child masks with prefix counts, then the leaf's packed prefix plus the
+ * popcount of the mask word below the voxel (two branches).
+ * [fVDB-notes, "IndexGrid"; fVDB-ONNX §1.2 IJKToIndex / CoordsInGrid]
+ * coords device int32 [n, 3]; batch_idx device int32 [n] or NULL (all batch 0);
+ * out_idx device int32 [n]. */
+fvx_status fvx_lookup(fvx_grid g, const int32_t* coords, const int32_t* batch_idx, int64_t n, int32_t* out_idx,
+                      fvx_stream stream);
+
+/* Output grid of a strided conv: the unique floor(ijk / stride) per batch,
+ * built by the same GPU build.  stride >= 1.  [fVDB-ONNX §1.2 CoarsenedGrid /
+ * ConvGrid]  Synchronises like fvx_build_grid. */
+fvx_status fvx_coarsen(fvx_grid g, int32_t stride, fvx_stream stream, fvx_grid* out);
+
+/* ---------------------------------------------------------------------------
+ * Kernel map  [DriveRT, "Shared neighbour maps"; "Kernels selected per GPU"]
+ *
+ * For every output voxel q of gout and offset slot s = (di+1)*9 + (dj+1)*3 +
+ * (dk+1), d in {-1,0,1}^3, the input voxel p of gin at stride*ijk(q) + d in
+ * the same batch.  Pairs are grouped by s, and inside a group ordered by q.
+ * ksize must be 3; stride 1 (submanifold: pass gout == gin) or 2 (gout is
+ * usually fvx_coarsen(gin, 2)).  gin and gout must have the same batch size.
+ * Synchronises the stream once (to size the pair lists; never truncated).
+ * [DriveRT, "Compilation and deployment": dynamic sizes, no truncation] */
+fvx_status fvx_kernel_map(fvx_grid gin, fvx_grid gout, int32_t ksize, int32_t stride, fvx_stream stream,
+                          fvx_kmap* out);
+
+/* offsets_host: HOST int64 [28] (list s is [offsets[s], offsets[s+1]));
+ * in_idx / out_idx: device int32 [n_pairs]; out_mask: device uint32 [n_out],
+ * bit s set when output q has a neighbour at slot s.  All owned by the map. */
+fvx_status fvx_kmap_view(fvx_kmap m, const int64_t** offsets_host, const int32_t** in_idx, const int32_t** out_idx,
+                         const uint32_t** out_mask, int64_t* n_pairs, int64_t* n_out);
+
+/* ---------------------------------------------------------------------------
+ * Sparse convolution (gather - GEMM - scatter)  [fVDB-notes, "Sparse-
+ * convolution operators"; effective-TFLOPS definition there]
+ *
+ *   out[q, co] = sum_s sum_{(p,q) in list s} sum_ci feats[p, ci] * W[s, ci, co]
+ *
+ * Cross-correlation, no bias; outputs without pairs are 0.
+ * feats  device [gin.n_active, cin], row-major, dtype dt.
+ * W      device [27, cin, cout], row-major, dtype dt.
+ * out    device [gout.n_active, cout], row-major, dtype dt, caller-allocated;
+ *        fully overwritten.
+ * FVX_BF16: bf16 inputs, fp32 accumulation on the tensor cores, bf16 output
+ *           (round to nearest even).  cin and cout multiples of 8 and 16,
+ *           cin <= 512, cout <= 256.
+ * FVX_F32:  fp32 FFMA throughout (no TF32).  cin, cout >= 1.
+ * m must have been built for (gin, gout).  Errors: FVX_ERR_INVALID_ARG. */
+fvx_status fvx_sparse_conv(fvx_grid gin, fvx_grid gout, fvx_kmap m, fvx_dtype dt, const void* feats, int64_t cin,
+                           const void* W, int64_t cout, void* out, fvx_stream stream);
+
+fvx_status fvx_grid_destroy(fvx_grid g);
+fvx_status fvx_kmap_destroy(fvx_kmap m);
+
+/* ---------------------------------------------------------------------------
+ * Status, diagnostics, accounting
+ */
+const char* fvx_status_string(fvx_status st);
+/* Message of the last failing call on this host thread ("" if none). */
+const char* fvx_last_error(void);
+
+/* Synchronises `stream` and returns the device status word that bounded waits
+ * and device-side checks write (FVX_OK, FVX_ERR_DEVICE_TIMEOUT or
+ * FVX_ERR_CHECK), then clears it. */
+fvx_status fvx_device_status(fvx_stream stream);
+
+/* Number of kernels this library has launched since it was loaded (host
+ * counter, all threads). */
+uint64_t fvx_launch_count(void);
+
+/* Kernel timing for roofline measurement: while enabled, every launch of a
+ * kernel whose name equals `kernel_name` is bracketed with CUDA events on its
+ * own stream.  fvx_profile_read synchronises those events and returns the
+ * total milliseconds and the number of timed launches since the last enable.
+ * Pass NULL to disable. */
+fvx_status fvx_profile_enable(const char* kernel_name);
+fvx_status fvx_profile_read(double* total_ms, int64_t* launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FVX_H */

@@ -1,0 +1,818 @@
+// GPU IndexGrid build, lookup and coarsening.
+//
+// Follows the build of "fVDB: A Deep-Learning Framework for Sparse, Large
+// Scale, and High Performance Spatial Intelligence" (reading notes, section
+// "GPU-accelerated IndexGrid build"):
+//   1  N signed voxel coordinates i, j, k
+//   2  a 64-bit key per coordinate from i, j, k shifted right by 12 bits
+//      (the root tile), packed side by side
+//   3  radix sort of the N keys
+//   4  run-length encoding of the sorted keys (one run per root tile)
+//   5  a unique 64-bit key per coordinate: run id + the offsets inside the
+//      upper, lower and leaf node
+//   6  radix sort of those keys
+//   7-9  upper / lower / leaf / voxel counts from runs and unique keys
+//   10-12  allocation from the counts, then top-down registration of nodes
+//      and active-voxel bitmasks (80-byte leaves: "IndexGrid" section).
+// Differences from the printed recipe (same result): the tile fields of the
+// step-2 key use only as many bits as the data's tile range needs (so the batch
+// index fits in the same key), and the step-5 key keeps only the offset bits
+// that vary across the input (order-preserving bit compaction), so that the
+// sorts run only over significant 8-bit digits.
+#include <cuda_runtime.h>
+#include <limits.h>
+#include <string.h>
+
+#include <algorithm>
+
+#include "block_scan.cuh"
+#include "fvx_internal.cuh"
+
+namespace fvx {
+
+namespace {
+
+constexpr int kThreads = 256;
+
+// 36-bit in-tile offset key, x-major inside each level:
+//   [35:21] upper child (5+5+5)  [20:9] lower child (4+4+4)  [8:0] voxel (3+3+3)
+__device__ __forceinline__ uint64_t offset_key(int i, int j, int k) {
+  const uint64_t ui = (i >> 7) & 31, uj = (j >> 7) & 31, uk = (k >> 7) & 31;
+  const uint64_t li = (i >> 3) & 15, lj = (j >> 3) & 15, lk = (k >> 3) & 15;
+  const uint64_t vi = i & 7, vj = j & 7, vk = k & 7;
+  return (ui << 31) | (uj << 26) | (uk << 21) | (li << 17) | (lj << 13) | (lk << 9) | (vi << 6) | (vj << 3) | vk;
+}
+
+struct BitRuns {  // contiguous runs of set bits of the varying-offset mask
+  int n;
+  uint8_t src[36], len[36], dst[36];
+};
+
+__device__ __forceinline__ uint64_t compact_bits(uint64_t x, const BitRuns& r) {
+  uint64_t y = 0;
+  for (int t = 0; t < r.n; ++t) y |= ((x >> r.src[t]) & ((1ull << r.len[t]) - 1ull)) << r.dst[t];
+  return y;
+}
+__device__ __forceinline__ uint64_t expand_bits(uint64_t y, const BitRuns& r) {
+  uint64_t x = 0;
+  for (int t = 0; t < r.n; ++t) x |= ((y >> r.dst[t]) & ((1ull << r.len[t]) - 1ull)) << r.src[t];
+  return x;
+}
+
+struct PlanDev {
+  int32_t tmin[3];
+  int32_t tmax[3];
+  unsigned long long off_or, off_and;
+};
+
+struct Key1Layout {
+  int w[3];  // bits per tile axis
+  int32_t tmin[3];
+  int tile_bits;  // w0 + w1 + w2
+};
+
+__device__ __forceinline__ int batch_of_row(const int64_t* __restrict__ offs, int B, int64_t r) {
+  int lo = 0, hi = B;  // largest b with offs[b] <= r
+  while (hi - lo > 1) {
+    int mid = (lo + hi) >> 1;
+    if (__ldg((const long long*)offs + mid) <= r) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// ---------------------------------------------------------------- step 2 planning
+__global__ void k_plan_init(PlanDev* plan) {
+  for (int a = 0; a < 3; ++a) {
+    plan->tmin[a] = INT_MAX;
+    plan->tmax[a] = INT_MIN;
+  }
+  plan->off_or = 0ull;
+  plan->off_and = ~0ull;
+}
+
+__global__ void __launch_bounds__(kThreads) k_plan_reduce(const int32_t* __restrict__ coords, int64_t n,
+                                                          PlanDev* __restrict__ plan) {
+  int tmin[3] = {INT_MAX, INT_MAX, INT_MAX}, tmax[3] = {INT_MIN, INT_MIN, INT_MIN};
+  unsigned long long o_or = 0ull, o_and = ~0ull;
+  for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < n; r += (int64_t)gridDim.x * blockDim.x) {
+    const int i = coords[3 * r], j = coords[3 * r + 1], k = coords[3 * r + 2];
+    const int t[3] = {i >> 12, j >> 12, k >> 12};
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+      tmin[a] = min(tmin[a], t[a]);
+      tmax[a] = max(tmax[a], t[a]);
+    }
+    const uint64_t o = offset_key(i, j, k);
+    o_or |= o;
+    o_and &= o;
+  }
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) {
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+      tmin[a] = min(tmin[a], __shfl_xor_sync(0xffffffffu, tmin[a], d));
+      tmax[a] = max(tmax[a], __shfl_xor_sync(0xffffffffu, tmax[a], d));
+    }
+    o_or |= __shfl_xor_sync(0xffffffffu, o_or, d);
+    o_and &= __shfl_xor_sync(0xffffffffu, o_and, d);
+  }
+  if ((threadIdx.x & 31) == 0) {
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+      atomicMin(&plan->tmin[a], tmin[a]);
+      atomicMax(&plan->tmax[a], tmax[a]);
+    }
+    atomicOr(&plan->off_or, o_or);
+    atomicAnd(&plan->off_and, o_and);
+  }
+}
+
+// ---------------------------------------------------------------- step 2 key
+__global__ void __launch_bounds__(kThreads) k_key1(const int32_t* __restrict__ coords, int64_t n,
+                                                   const int64_t* __restrict__ offs, int B, Key1Layout L,
+                                                   uint64_t* __restrict__ key, uint32_t* __restrict__ val) {
+  const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= n) return;
+  const int b = batch_of_row(offs, B, r);
+  const uint64_t ti = (uint64_t)(uint32_t)((coords[3 * r] >> 12) - L.tmin[0]);
+  const uint64_t tj = (uint64_t)(uint32_t)((coords[3 * r + 1] >> 12) - L.tmin[1]);
+  const uint64_t tk = (uint64_t)(uint32_t)((coords[3 * r + 2] >> 12) - L.tmin[2]);
+  key[r] = ((uint64_t)b << L.tile_bits) | (ti << (L.w[1] + L.w[2])) | (tj << L.w[2]) | tk;
+  val[r] = (uint32_t)r;
+}
+
+// step 5 key when every row lies in one root tile of one batch (no step 2-4)
+__global__ void __launch_bounds__(kThreads) k_key2_direct(const int32_t* __restrict__ coords, int64_t n,
+                                                          const __grid_constant__ BitRuns runs, int4 tile0,
+                                                          uint64_t* __restrict__ key, uint32_t* __restrict__ val,
+                                                          int4* __restrict__ run_tile) {
+  const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (r == 0) run_tile[0] = tile0;
+  if (r >= n) return;
+  key[r] = compact_bits(offset_key(coords[3 * r], coords[3 * r + 1], coords[3 * r + 2]), runs);
+  val[r] = (uint32_t)r;
+}
+
+// ---------------------------------------------------------------- step 4 RLE + step 5 key
+constexpr int kFlagItems = 8;
+constexpr int kFlagTile = kThreads * kFlagItems;  // 2048
+
+__global__ void __launch_bounds__(kThreads) k_rle_count(const uint64_t* __restrict__ key, int64_t n,
+                                                        uint32_t* __restrict__ partial) {
+  __shared__ uint32_t tmp[33];
+  const int64_t base = (int64_t)blockIdx.x * kFlagTile + (int64_t)threadIdx.x * kFlagItems;
+  uint32_t c = 0;
+  for (int q = 0; q < kFlagItems; ++q) {
+    const int64_t j = base + q;
+    if (j < n) c += (j == 0 || key[j] != key[j - 1]) ? 1u : 0u;
+  }
+  uint32_t tot;
+  block_exclusive_scan<uint32_t>(c, tmp, &tot);
+  if (threadIdx.x == 0) partial[blockIdx.x] = tot;
+}
+
+__global__ void __launch_bounds__(kThreads) k_rle_key2(const uint64_t* __restrict__ key1, int64_t n,
+                                                       const uint32_t* __restrict__ val,
+                                                       const int32_t* __restrict__ coords,
+                                                       const uint32_t* __restrict__ partial, Key1Layout L,
+                                                       int vbits, const __grid_constant__ BitRuns runs,
+                                                       uint64_t* __restrict__ key2, int4* __restrict__ run_tile) {
+  __shared__ uint32_t tmp[33];
+  const int64_t base = (int64_t)blockIdx.x * kFlagTile + (int64_t)threadIdx.x * kFlagItems;
+  uint32_t c = 0;
+  for (int q = 0; q < kFlagItems; ++q) {
+    const int64_t j = base + q;
+    if (j < n) c += (j == 0 || key1[j] != key1[j - 1]) ? 1u : 0u;
+  }
+  uint32_t run = block_exclusive_scan<uint32_t>(c, tmp, (uint32_t*)nullptr) + partial[blockIdx.x];
+  for (int q = 0; q < kFlagItems; ++q) {
+    const int64_t j = base + q;
+    if (j >= n) break;
+    const uint64_t k1 = key1[j];
+    const bool head = (j == 0 || k1 != key1[j - 1]);
+    run += head ? 1u : 0u;
+    const uint32_t r = val[j];
+    const uint64_t o = offset_key(coords[3 * (int64_t)r], coords[3 * (int64_t)r + 1], coords[3 * (int64_t)r + 2]);
+    key2[j] = ((uint64_t)(run - 1) << vbits) | compact_bits(o, runs);
+    if (head) {
+      const int w12 = L.w[1] + L.w[2];
+      int4 t;
+      t.x = (int)(k1 >> L.tile_bits);
+      t.y = (int)((k1 >> w12) & ((1ull << L.w[0]) - 1ull)) + L.tmin[0];
+      t.z = (int)((k1 >> L.w[2]) & ((1ull << L.w[1]) - 1ull)) + L.tmin[1];
+      t.w = (int)(k1 & ((1ull << L.w[2]) - 1ull)) + L.tmin[2];
+      run_tile[run - 1] = t;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- steps 7-9 counts
+struct Shifts {
+  int leaf, lower, upper;  // key2 >> shift identifies leaf / lower / upper node
+};
+
+__device__ __forceinline__ uint32_t head_flags(const uint64_t* __restrict__ key, int64_t j, Shifts sh) {
+  if (j == 0) return 0xFu;
+  const uint64_t a = key[j], b = key[j - 1];
+  return (a != b ? 1u : 0u) | (((a >> sh.leaf) != (b >> sh.leaf)) ? 2u : 0u) |
+         (((a >> sh.lower) != (b >> sh.lower)) ? 4u : 0u) | (((a >> sh.upper) != (b >> sh.upper)) ? 8u : 0u);
+}
+
+__device__ __forceinline__ uint64_t pack_flags(uint32_t f) {
+  return (uint64_t)(f & 1u) | ((uint64_t)((f >> 1) & 1u) << 16) | ((uint64_t)((f >> 2) & 1u) << 32) |
+         ((uint64_t)((f >> 3) & 1u) << 48);
+}
+
+__global__ void __launch_bounds__(kThreads) k_count_tiles(const uint64_t* __restrict__ key, int64_t n, Shifts sh,
+                                                          uint32_t* __restrict__ partial, int64_t ntiles) {
+  __shared__ uint64_t tmp[33];
+  const int64_t base = (int64_t)blockIdx.x * kFlagTile + (int64_t)threadIdx.x * kFlagItems;
+  uint64_t c = 0;
+  for (int q = 0; q < kFlagItems; ++q) {
+    const int64_t j = base + q;
+    if (j < n) c += pack_flags(head_flags(key, j, sh));
+  }
+  uint64_t tot;
+  block_exclusive_scan<uint64_t>(c, tmp, &tot);
+  if (threadIdx.x < 4) partial[threadIdx.x * ntiles + blockIdx.x] = (uint32_t)((tot >> (16 * threadIdx.x)) & 0xFFFFu);
+}
+
+__global__ void k_gather_counts(const uint32_t* __restrict__ scanned, int64_t ntiles, const uint32_t* total,
+                                uint32_t* __restrict__ out) {
+  // out[f] = count of head flag f = (row f+1 base) - (row f base); last row to the total
+  if (threadIdx.x < 4) {
+    const uint32_t lo = scanned[threadIdx.x * ntiles];
+    const uint32_t hi = threadIdx.x < 3 ? scanned[(threadIdx.x + 1) * ntiles] : *total;
+    out[threadIdx.x] = hi - lo;
+  }
+}
+
+struct DecodeInfo {
+  int vbits;
+  uint64_t const_bits;  // offset bits that do not vary (their common value)
+};
+
+struct BuildOut {
+  int32_t* ijk;
+  int32_t* row_to_index;
+  uint32_t* leaf_first_voxel;
+  int32_t* leaf_origin;
+  int32_t* leaf_batch;
+  uint32_t* lower_first;
+  int32_t* lower_origin;
+  int32_t* lower_batch;
+  uint32_t* upper_first;
+  uint32_t* upper_first_voxel;
+  int32_t* upper_origin;
+  int32_t* upper_batch;
+  int4* upper_tile;
+};
+
+__global__ void __launch_bounds__(kThreads) k_count_down(const uint64_t* __restrict__ key,
+                                                         const uint32_t* __restrict__ val, int64_t n, Shifts sh,
+                                                         const uint32_t* __restrict__ scanned, int64_t ntiles,
+                                                         const __grid_constant__ BitRuns runs, DecodeInfo dec,
+                                                         const int4* __restrict__ run_tile, BuildOut o) {
+  __shared__ uint64_t tmp[33];
+  const int64_t base = (int64_t)blockIdx.x * kFlagTile + (int64_t)threadIdx.x * kFlagItems;
+  uint32_t fl[kFlagItems];
+  uint64_t c = 0;
+#pragma unroll
+  for (int q = 0; q < kFlagItems; ++q) {
+    const int64_t j = base + q;
+    fl[q] = (j < n) ? head_flags(key, j, sh) : 0u;
+    c += pack_flags(fl[q]);
+  }
+  const uint64_t ex = block_exclusive_scan<uint64_t>(c, tmp, (uint64_t*)nullptr);
+  uint32_t cnt[4];
+#pragma unroll
+  for (int f = 0; f < 4; ++f)
+    cnt[f] = (uint32_t)((ex >> (16 * f)) & 0xFFFFu) + scanned[f * ntiles + blockIdx.x] - scanned[f * ntiles];
+#pragma unroll
+  for (int q = 0; q < kFlagItems; ++q) {
+    const int64_t j = base + q;
+    if (j >= n) break;
+    const uint32_t f = fl[q];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) cnt[a] += (f >> a) & 1u;
+    const uint32_t vox = cnt[0] - 1, leaf = cnt[1] - 1, lower = cnt[2] - 1, upper = cnt[3] - 1;
+    o.row_to_index[val[j]] = (int32_t)vox;
+    if (!(f & 1u)) continue;
+    const uint64_t k2 = key[j];
+    const uint64_t off = expand_bits(k2 & ((1ull << dec.vbits) - 1ull), runs) | dec.const_bits;
+    const int4 t = run_tile[(uint32_t)(k2 >> dec.vbits)];
+    const int ci = t.y * 4096 + (int)(((off >> 31) & 31) << 7 | ((off >> 17) & 15) << 3 | ((off >> 6) & 7));
+    const int cj = t.z * 4096 + (int)(((off >> 26) & 31) << 7 | ((off >> 13) & 15) << 3 | ((off >> 3) & 7));
+    const int ck = t.w * 4096 + (int)(((off >> 21) & 31) << 7 | ((off >> 9) & 15) << 3 | (off & 7));
+    o.ijk[3 * (int64_t)vox] = ci;
+    o.ijk[3 * (int64_t)vox + 1] = cj;
+    o.ijk[3 * (int64_t)vox + 2] = ck;
+    if (f & 2u) {
+      o.leaf_first_voxel[leaf] = vox;
+      o.leaf_origin[3 * (int64_t)leaf] = ci & ~7;
+      o.leaf_origin[3 * (int64_t)leaf + 1] = cj & ~7;
+      o.leaf_origin[3 * (int64_t)leaf + 2] = ck & ~7;
+      o.leaf_batch[leaf] = t.x;
+    }
+    if (f & 4u) {
+      o.lower_first[lower] = leaf;
+      o.lower_origin[3 * (int64_t)lower] = ci & ~127;
+      o.lower_origin[3 * (int64_t)lower + 1] = cj & ~127;
+      o.lower_origin[3 * (int64_t)lower + 2] = ck & ~127;
+      o.lower_batch[lower] = t.x;
+    }
+    if (f & 8u) {
+      o.upper_first[upper] = lower;
+      o.upper_first_voxel[upper] = vox;
+      o.upper_origin[3 * (int64_t)upper] = t.y * 4096;
+      o.upper_origin[3 * (int64_t)upper + 1] = t.z * 4096;
+      o.upper_origin[3 * (int64_t)upper + 2] = t.w * 4096;
+      o.upper_batch[upper] = t.x;
+      o.upper_tile[upper] = t;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- steps 10-12 registration
+// One warp per leaf: 8 mask words from its voxels, first index, packed prefix.
+__global__ void __launch_bounds__(kThreads) k_leaf_register(const int32_t* __restrict__ ijk,
+                                                            const uint32_t* __restrict__ leaf_first_voxel,
+                                                            int64_t n_leaf, int64_t n_active,
+                                                            uint64_t* __restrict__ rec) {
+  const int64_t l = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (l >= n_leaf) return;
+  const uint32_t first = leaf_first_voxel[l];
+  const uint32_t end = (l + 1 < n_leaf) ? leaf_first_voxel[l + 1] : (uint32_t)n_active;
+  uint64_t m[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  for (uint32_t t = first + lane; t < end; t += 32) {
+    const int i = ijk[3 * (int64_t)t], j = ijk[3 * (int64_t)t + 1], k = ijk[3 * (int64_t)t + 2];
+    const int w = i & 7;
+    const uint64_t bit = 1ull << (((j & 7) << 3) | (k & 7));
+#pragma unroll
+    for (int q = 0; q < 8; ++q) m[q] |= (q == w) ? bit : 0ull;
+  }
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) m[q] |= __shfl_xor_sync(0xffffffffu, m[q], d);
+  }
+  uint64_t packed = 0, acc = 0;
+#pragma unroll
+  for (int w = 1; w < 8; ++w) {
+    acc += (uint64_t)__popcll(m[w - 1]);
+    packed |= acc << (9 * (w - 1));
+  }
+  uint64_t v = 0;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) v = (lane == q) ? m[q] : v;
+  if (lane == 8) v = first;
+  if (lane == 9) v = packed;
+  if (lane < 10) rec[l * 10 + lane] = v;
+}
+
+// One warp per lower node: 4096-bit child mask (64 words) and prefix counts.
+__global__ void __launch_bounds__(kThreads) k_lower_register(const int32_t* __restrict__ leaf_origin,
+                                                             const uint32_t* __restrict__ lower_first,
+                                                             int64_t n_lower, int64_t n_leaf,
+                                                             uint64_t* __restrict__ mask,
+                                                             uint32_t* __restrict__ prefix) {
+  __shared__ unsigned long long sm[kThreads / 32][64];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t w = (int64_t)blockIdx.x * (kThreads / 32) + warp;
+  sm[warp][lane] = 0ull;
+  sm[warp][lane + 32] = 0ull;
+  __syncwarp();
+  if (w < n_lower) {
+    const uint32_t first = lower_first[w];
+    const uint32_t end = (w + 1 < n_lower) ? lower_first[w + 1] : (uint32_t)n_leaf;
+    for (uint32_t t = first + lane; t < end; t += 32) {
+      const int i = leaf_origin[3 * (int64_t)t], j = leaf_origin[3 * (int64_t)t + 1], k = leaf_origin[3 * (int64_t)t + 2];
+      const int nb = (((i >> 3) & 15) << 8) | (((j >> 3) & 15) << 4) | ((k >> 3) & 15);
+      atomicOr(&sm[warp][nb >> 6], 1ull << (nb & 63));
+    }
+  }
+  __syncwarp();
+  if (w >= n_lower) return;
+  const uint64_t a = sm[warp][2 * lane], b = sm[warp][2 * lane + 1];
+  const uint32_t pa = __popcll(a), pb = __popcll(b);
+  const uint32_t ex = warp_inclusive_scan<uint32_t>(pa + pb) - (pa + pb);
+  mask[w * 64 + 2 * lane] = a;
+  mask[w * 64 + 2 * lane + 1] = b;
+  prefix[w * 64 + 2 * lane] = ex;
+  prefix[w * 64 + 2 * lane + 1] = ex + pa;
+}
+
+// One block per upper node: 32768-bit child mask (512 words) and prefix counts.
+__global__ void __launch_bounds__(kThreads) k_upper_register(const int32_t* __restrict__ lower_origin,
+                                                             const uint32_t* __restrict__ upper_first,
+                                                             int64_t n_upper, int64_t n_lower,
+                                                             uint64_t* __restrict__ mask,
+                                                             uint32_t* __restrict__ prefix) {
+  __shared__ unsigned long long sm[512];
+  __shared__ uint32_t tmp[33];
+  const int64_t u = blockIdx.x;
+  sm[threadIdx.x] = 0ull;
+  sm[threadIdx.x + 256] = 0ull;
+  __syncthreads();
+  const uint32_t first = upper_first[u];
+  const uint32_t end = (u + 1 < n_upper) ? upper_first[u + 1] : (uint32_t)n_lower;
+  for (uint32_t t = first + threadIdx.x; t < end; t += blockDim.x) {
+    const int i = lower_origin[3 * (int64_t)t], j = lower_origin[3 * (int64_t)t + 1], k = lower_origin[3 * (int64_t)t + 2];
+    const int nb = (((i >> 7) & 31) << 10) | (((j >> 7) & 31) << 5) | ((k >> 7) & 31);
+    atomicOr(&sm[nb >> 6], 1ull << (nb & 63));
+  }
+  __syncthreads();
+  const uint64_t a = sm[2 * threadIdx.x], b = sm[2 * threadIdx.x + 1];
+  const uint32_t pa = __popcll(a), pb = __popcll(b);
+  const uint32_t ex = block_exclusive_scan<uint32_t>(pa + pb, tmp, (uint32_t*)nullptr);
+  mask[u * 512 + 2 * threadIdx.x] = a;
+  mask[u * 512 + 2 * threadIdx.x + 1] = b;
+  prefix[u * 512 + 2 * threadIdx.x] = ex;
+  prefix[u * 512 + 2 * threadIdx.x + 1] = ex + pa;
+}
+
+__global__ void k_batch_offsets(const int4* __restrict__ upper_tile, const uint32_t* __restrict__ upper_first_voxel,
+                                int64_t n_upper, int64_t n_active, int B, int64_t* __restrict__ vbo) {
+  for (int b = threadIdx.x; b <= B; b += blockDim.x) {
+    int lo = 0, hi = (int)n_upper;  // first upper node with batch >= b
+    while (lo < hi) {
+      int mid = (lo + hi) >> 1;
+      if (upper_tile[mid].x < b) lo = mid + 1; else hi = mid;
+    }
+    vbo[b] = (lo < n_upper) ? (int64_t)upper_first_voxel[lo] : n_active;
+  }
+}
+
+__global__ void k_lookup(GridDev g, const int32_t* __restrict__ coords, const int32_t* __restrict__ batch, int64_t n,
+                         int32_t* __restrict__ out) {
+  const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= n) return;
+  const int b = batch ? batch[r] : 0;
+  out[r] = lookup_index(g, b, coords[3 * r], coords[3 * r + 1], coords[3 * r + 2]);
+}
+
+__global__ void k_coarsen_coords(const int32_t* __restrict__ ijk, int64_t n, int stride, int shift,
+                                 int32_t* __restrict__ out) {
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= 3 * n) return;
+  const int c = ijk[t];
+  if (shift >= 0) {
+    out[t] = c >> shift;  // floor division by a power of two
+  } else {
+    int q = c / stride;
+    if ((c % stride) != 0 && c < 0) q -= 1;
+    out[t] = q;
+  }
+}
+
+int bits_for(uint64_t maxval) {  // bits needed to represent 0..maxval
+  int b = 0;
+  while (b < 64 && (maxval >> b) != 0) ++b;
+  return b;
+}
+
+size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
+
+unsigned grid_for(int64_t n, int threads) { return (unsigned)((n + threads - 1) / threads); }
+
+}  // namespace
+
+fvx_status build_grid_device(const int32_t* coords, int64_t n, const int64_t* offs_dev, int32_t B, cudaStream_t s,
+                             fvx_grid_s** out) {
+  Scratch scr(s);
+  fvx_grid_s* g = new fvx_grid_s();
+  g->B = B;
+  g->n_rows = n;
+  g->stream = s;
+  struct Guard {
+    fvx_grid_s** g;
+    ~Guard() {
+      if (*g) fvx_grid_destroy(*g);
+    }
+  } guard{&g};
+
+  int64_t counts[4] = {0, 0, 0, 0};  // voxels, leaves, lower, upper
+  uint64_t* ka = nullptr;
+  uint32_t* va = nullptr;
+  Shifts sh{0, 0, 0};
+  BitRuns runs{};
+  DecodeInfo dec{0, 0};
+  int4* run_tile = nullptr;
+  uint32_t* scanned = nullptr;
+  int64_t ntiles = 0;
+
+  if (n > 0) {
+    // ---- step 2 planning: tile range per axis and the varying offset bits
+    PlanDev* plan = scr.get<PlanDev>(1);
+    if (!plan) return FVX_ERR_ALLOC;
+    PlanDev* hp = (PlanDev*)pinned_staging(sizeof(PlanDev));
+    if (!hp) {
+      set_error("fvx_build_grid: pinned staging allocation failed");
+      return FVX_ERR_ALLOC;
+    }
+    {
+      LaunchScope ls("build_plan_init", s);
+      k_plan_init<<<1, 1, 0, s>>>(plan);
+    }
+    FVX_TRY(check_launch("build_plan_init"));
+    {
+      LaunchScope ls("build_plan_reduce", s);
+      unsigned nb = std::min<unsigned>(grid_for(n, kThreads), 152u * 8u);
+      k_plan_reduce<<<nb, kThreads, 0, s>>>(coords, n, plan);
+    }
+    FVX_TRY(check_launch("build_plan_reduce"));
+    FVX_CUDA(cudaMemcpyAsync(hp, plan, sizeof(PlanDev), cudaMemcpyDeviceToHost, s));
+    FVX_CUDA(cudaStreamSynchronize(s));
+    const PlanDev P = *hp;
+
+    Key1Layout L{};
+    for (int a = 0; a < 3; ++a) {
+      L.tmin[a] = P.tmin[a];
+      L.w[a] = bits_for((uint64_t)((int64_t)P.tmax[a] - (int64_t)P.tmin[a]));
+    }
+    L.tile_bits = L.w[0] + L.w[1] + L.w[2];
+    const int width1 = L.tile_bits + bits_for((uint64_t)(B - 1));
+    if (width1 > 64) {
+      set_error("fvx_build_grid: batch size %d with tile range needs a %d-bit key (max 64)", B, width1);
+      return FVX_ERR_RANGE;
+    }
+    const uint64_t vm = P.off_or & ~P.off_and;
+    runs.n = 0;
+    int dst = 0;
+    for (int b = 0; b < 36;) {
+      if (!((vm >> b) & 1ull)) {
+        ++b;
+        continue;
+      }
+      int e = b;
+      while (e < 36 && ((vm >> e) & 1ull)) ++e;
+      runs.src[runs.n] = (uint8_t)b;
+      runs.len[runs.n] = (uint8_t)(e - b);
+      runs.dst[runs.n] = (uint8_t)dst;
+      ++runs.n;
+      dst += e - b;
+      b = e;
+    }
+    const int vbits = dst;
+    dec.vbits = vbits;
+    dec.const_bits = P.off_and & ~vm;
+    sh.leaf = __builtin_popcountll(vm & 0x1FFull);
+    sh.lower = __builtin_popcountll(vm & 0x1FFFFFull);
+    sh.upper = vbits;
+    const uint64_t max_runs = (width1 >= 63) ? (uint64_t)n : std::min<uint64_t>((uint64_t)n, 1ull << width1);
+    const int runbits = bits_for(max_runs - 1);
+    if (runbits + vbits > 64) {
+      set_error("fvx_build_grid: %d rows spread over too many root tiles for a 64-bit key", (int)n);
+      return FVX_ERR_RANGE;
+    }
+
+    ka = scr.get<uint64_t>((size_t)n);
+    va = scr.get<uint32_t>((size_t)n);
+    uint64_t* kb = scr.get<uint64_t>((size_t)n);
+    uint32_t* vb = scr.get<uint32_t>((size_t)n);
+    run_tile = scr.get<int4>((size_t)max_runs);
+    if (!ka || !va || !kb || !vb || !run_tile) return FVX_ERR_ALLOC;
+
+    if (width1 == 0) {
+      // one batch, one root tile: steps 2-4 are empty; run 0 is that tile
+      const int4 tile0 = make_int4(0, P.tmin[0], P.tmin[1], P.tmin[2]);
+      {
+        LaunchScope ls("build_key2_direct", s);
+        k_key2_direct<<<grid_for(n, kThreads), kThreads, 0, s>>>(coords, n, runs, tile0, ka, va, run_tile);
+      }
+      FVX_TRY(check_launch("build_key2_direct"));
+    } else {
+      {
+        LaunchScope ls("build_key1", s);
+        k_key1<<<grid_for(n, kThreads), kThreads, 0, s>>>(coords, n, offs_dev, B, L, ka, va);
+      }
+      FVX_TRY(check_launch("build_key1"));
+      bool in1 = false;
+      FVX_TRY(radix_sort_pairs(ka, va, kb, vb, n, 0, width1, s, &in1));
+      uint64_t* k1 = in1 ? kb : ka;
+      uint32_t* v1 = in1 ? vb : va;
+      uint64_t* k2 = in1 ? ka : kb;  // the other key buffer receives key2
+      const int64_t nt = (n + kFlagTile - 1) / kFlagTile;
+      uint32_t* partial = scr.get<uint32_t>((size_t)nt);
+      if (!partial) return FVX_ERR_ALLOC;
+      {
+        LaunchScope ls("build_rle_count", s);
+        k_rle_count<<<(unsigned)nt, kThreads, 0, s>>>(k1, n, partial);
+      }
+      FVX_TRY(check_launch("build_rle_count"));
+      FVX_TRY(scan_exclusive_u32(partial, partial, nt, nullptr, s));
+      {
+        LaunchScope ls("build_rle_key2", s);
+        k_rle_key2<<<(unsigned)nt, kThreads, 0, s>>>(k1, n, v1, coords, partial, L, vbits, runs, k2, run_tile);
+      }
+      FVX_TRY(check_launch("build_rle_key2"));
+      // arrange so that (ka, va) hold key2 and the row ids
+      if (in1) {
+        // key2 in ka, rows in vb
+        std::swap(va, vb);
+      } else {
+        // key2 in kb, rows in va
+        std::swap(ka, kb);
+      }
+    }
+    // ---- step 6: sort by key2 (run id above the compacted offsets)
+    {
+      bool in1 = false;
+      FVX_TRY(radix_sort_pairs(ka, va, kb, vb, n, 0, runbits + vbits, s, &in1));
+      if (in1) {
+        ka = kb;
+        va = vb;
+      }
+    }
+    // ---- steps 7-9: node counts
+    ntiles = (n + kFlagTile - 1) / kFlagTile;
+    scanned = scr.get<uint32_t>((size_t)(4 * ntiles));
+    uint32_t* dcounts = scr.get<uint32_t>(8);
+    if (!scanned || !dcounts) return FVX_ERR_ALLOC;
+    {
+      LaunchScope ls("build_count_tiles", s);
+      k_count_tiles<<<(unsigned)ntiles, kThreads, 0, s>>>(ka, n, sh, scanned, ntiles);
+    }
+    FVX_TRY(check_launch("build_count_tiles"));
+    FVX_TRY(scan_exclusive_u32(scanned, scanned, 4 * ntiles, dcounts + 4, s));
+    {
+      LaunchScope ls("build_gather_counts", s);
+      k_gather_counts<<<1, 32, 0, s>>>(scanned, ntiles, dcounts + 4, dcounts);
+    }
+    FVX_TRY(check_launch("build_gather_counts"));
+    uint32_t* hc = (uint32_t*)pinned_staging(16);
+    FVX_CUDA(cudaMemcpyAsync(hc, dcounts, 16, cudaMemcpyDeviceToHost, s));
+    FVX_CUDA(cudaStreamSynchronize(s));
+    for (int f = 0; f < 4; ++f) counts[f] = hc[f];
+  }
+
+  // ---- step 10: allocate the topology from the counts
+  g->n_active = counts[0];
+  g->n_leaf = counts[1];
+  g->n_lower = counts[2];
+  g->n_upper = counts[3];
+  const int64_t U = g->n_active, Lf = g->n_leaf, NL = g->n_lower, NU = g->n_upper;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off += align_up(bytes);
+    return o;
+  };
+  const size_t o_ijk = take(12 * U), o_r2i = take(4 * n), o_vbo = take(8 * (B + 1));
+  const size_t o_lfo = take(12 * Lf), o_lfb = take(4 * Lf), o_lfr = take(80 * Lf);
+  const size_t o_lwo = take(12 * NL), o_lwb = take(4 * NL), o_lwm = take(512 * NL), o_lwp = take(256 * NL),
+               o_lwf = take(4 * NL);
+  const size_t o_upo = take(12 * NU), o_upb = take(4 * NU), o_upm = take(4096 * NU), o_upp = take(2048 * NU),
+               o_upf = take(4 * NU), o_upt = take(16 * NU);
+  g->block = dalloc(off, s);
+  if (!g->block) return FVX_ERR_ALLOC;
+  char* base = (char*)g->block;
+  g->ijk = (int32_t*)(base + o_ijk);
+  g->row_to_index = (int32_t*)(base + o_r2i);
+  g->voxel_batch_offsets = (int64_t*)(base + o_vbo);
+  g->leaf_origin = (int32_t*)(base + o_lfo);
+  g->leaf_batch = (int32_t*)(base + o_lfb);
+  g->leaf_rec = (uint64_t*)(base + o_lfr);
+  g->lower_origin = (int32_t*)(base + o_lwo);
+  g->lower_batch = (int32_t*)(base + o_lwb);
+  g->lower_mask = (uint64_t*)(base + o_lwm);
+  g->lower_prefix = (uint32_t*)(base + o_lwp);
+  g->lower_first = (uint32_t*)(base + o_lwf);
+  g->upper_origin = (int32_t*)(base + o_upo);
+  g->upper_batch = (int32_t*)(base + o_upb);
+  g->upper_mask = (uint64_t*)(base + o_upm);
+  g->upper_prefix = (uint32_t*)(base + o_upp);
+  g->upper_first = (uint32_t*)(base + o_upf);
+  g->upper_tile = (int32_t*)(base + o_upt);
+
+  if (n == 0) {
+    FVX_CUDA(cudaMemsetAsync(g->voxel_batch_offsets, 0, 8 * (B + 1), s));
+  } else {
+    uint32_t* leaf_first_voxel = scr.get<uint32_t>((size_t)Lf);
+    uint32_t* upper_first_voxel = scr.get<uint32_t>((size_t)NU);
+    if (!leaf_first_voxel || !upper_first_voxel) return FVX_ERR_ALLOC;
+    BuildOut o{g->ijk,        g->row_to_index,   leaf_first_voxel, g->leaf_origin,  g->leaf_batch,
+               g->lower_first, g->lower_origin,  g->lower_batch,   g->upper_first,  upper_first_voxel,
+               g->upper_origin, g->upper_batch, (int4*)g->upper_tile};
+    {
+      LaunchScope ls("build_count_down", s);
+      k_count_down<<<(unsigned)ntiles, kThreads, 0, s>>>(ka, va, n, sh, scanned, ntiles, runs, dec, run_tile, o);
+    }
+    FVX_TRY(check_launch("build_count_down"));
+    // ---- steps 11-12: masks and prefix counts, leaves up to the root
+    {
+      LaunchScope ls("build_leaf_register", s);
+      k_leaf_register<<<grid_for(Lf * 32, kThreads), kThreads, 0, s>>>(g->ijk, leaf_first_voxel, Lf, U, g->leaf_rec);
+    }
+    FVX_TRY(check_launch("build_leaf_register"));
+    {
+      LaunchScope ls("build_lower_register", s);
+      k_lower_register<<<grid_for(NL * 32, kThreads), kThreads, 0, s>>>(g->leaf_origin, g->lower_first, NL, Lf,
+                                                                         g->lower_mask, g->lower_prefix);
+    }
+    FVX_TRY(check_launch("build_lower_register"));
+    {
+      LaunchScope ls("build_upper_register", s);
+      k_upper_register<<<(unsigned)NU, kThreads, 0, s>>>(g->lower_origin, g->upper_first, NU, NL, g->upper_mask,
+                                                         g->upper_prefix);
+    }
+    FVX_TRY(check_launch("build_upper_register"));
+    {
+      LaunchScope ls("build_batch_offsets", s);
+      k_batch_offsets<<<1, 256, 0, s>>>((const int4*)g->upper_tile, upper_first_voxel, NU, U, B,
+                                        g->voxel_batch_offsets);
+    }
+    FVX_TRY(check_launch("build_batch_offsets"));
+  }
+  *out = g;
+  g = nullptr;  // release the guard
+  return FVX_OK;
+}
+
+}  // namespace fvx
+
+using namespace fvx;
+
+extern "C" {
+
+fvx_status fvx_build_grid(const int32_t* coords, int64_t n_rows, const int64_t* batch_offsets, int32_t B,
+                          fvx_stream stream, fvx_grid* out) {
+  if (!out || !batch_offsets || (n_rows > 0 && !coords)) {
+    set_error("fvx_build_grid: NULL argument");
+    return FVX_ERR_INVALID_ARG;
+  }
+  *out = nullptr;
+  if (B < 1 || n_rows < 0 || n_rows > (int64_t)INT32_MAX - 1) {
+    set_error("fvx_build_grid: need B >= 1 and 0 <= n_rows < 2^31 - 1 (got B=%d, n_rows=%lld)", B,
+              (long long)n_rows);
+    return FVX_ERR_INVALID_ARG;
+  }
+  if (batch_offsets[0] != 0 || batch_offsets[B] != n_rows) {
+    set_error("fvx_build_grid: batch_offsets must start at 0 and end at n_rows (%lld, %lld vs %lld)",
+              (long long)batch_offsets[0], (long long)batch_offsets[B], (long long)n_rows);
+    return FVX_ERR_INVALID_ARG;
+  }
+  for (int32_t b = 0; b < B; ++b) {
+    if (batch_offsets[b + 1] < batch_offsets[b]) {
+      set_error("fvx_build_grid: batch_offsets not monotone at batch %d", b);
+      return FVX_ERR_INVALID_ARG;
+    }
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  Scratch scr(s);
+  int64_t* offs = scr.get<int64_t>((size_t)B + 1);
+  if (!offs) return FVX_ERR_ALLOC;
+  int64_t* ho = (int64_t*)pinned_staging(sizeof(int64_t) * (B + 1));
+  if (!ho) return FVX_ERR_ALLOC;
+  memcpy(ho, batch_offsets, sizeof(int64_t) * (B + 1));
+  FVX_CUDA(cudaMemcpyAsync(offs, ho, sizeof(int64_t) * (B + 1), cudaMemcpyHostToDevice, s));
+  fvx_grid_s* g = nullptr;
+  FVX_TRY(build_grid_device(coords, n_rows, offs, B, s, &g));
+  *out = g;
+  return FVX_OK;
+}
+
+fvx_status fvx_lookup(fvx_grid g, const int32_t* coords, const int32_t* batch_idx, int64_t n, int32_t* out_idx,
+                      fvx_stream stream) {
+  if (!g || n < 0 || (n > 0 && (!coords || !out_idx))) {
+    set_error("fvx_lookup: bad argument");
+    return FVX_ERR_INVALID_ARG;
+  }
+  if (n == 0) return FVX_OK;
+  cudaStream_t s = (cudaStream_t)stream;
+  {
+    LaunchScope ls("lookup", s);
+    k_lookup<<<grid_for(n, kThreads), kThreads, 0, s>>>(grid_dev(g), coords, batch_idx, n, out_idx);
+  }
+  return check_launch("lookup");
+}
+
+fvx_status fvx_coarsen(fvx_grid g, int32_t stride, fvx_stream stream, fvx_grid* out) {
+  if (!g || !out || stride < 1) {
+    set_error("fvx_coarsen: bad argument (stride must be >= 1)");
+    return FVX_ERR_INVALID_ARG;
+  }
+  *out = nullptr;
+  cudaStream_t s = (cudaStream_t)stream;
+  Scratch scr(s);
+  const int64_t U = g->n_active;
+  int32_t* c = scr.get<int32_t>((size_t)(3 * U + 3));
+  if (!c) return FVX_ERR_ALLOC;
+  int shift = -1;
+  for (int b = 0; b < 31; ++b)
+    if ((1 << b) == stride) shift = b;
+  if (U > 0) {
+    {
+      LaunchScope ls("coarsen_coords", s);
+      k_coarsen_coords<<<grid_for(3 * U, kThreads), kThreads, 0, s>>>(g->ijk, U, stride, shift, c);
+    }
+    FVX_TRY(check_launch("coarsen_coords"));
+  }
+  fvx_grid_s* r = nullptr;
+  FVX_TRY(build_grid_device(c, U, g->voxel_batch_offsets, g->B, s, &r));
+  *out = r;
+  return FVX_OK;
+}
+
+}  // extern "C"

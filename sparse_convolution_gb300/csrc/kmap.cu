@@ -1,0 +1,265 @@
+// 3x3x3 kernel map (neighbour pair lists) over two IndexGrids.
+//
+// [DriveRT, "Shared neighbour maps"]: a map is identified by the coordinate
+// domain (the grids), the kernel geometry (3x3x3, stride) and the row order
+// (the grids' index order); building it can cost more than the convolution.
+// [DriveRT, "Kernels selected per GPU"]: the 27 neighbours of a voxel form a
+// bit mask, kept here per output voxel.
+// [fVDB notes, "IndexGrid"]: coordinate -> index through the leaf bitmask and
+// its prefix popcounts.
+//
+// One CTA per OUTPUT leaf.  The 27 input leaves that can hold a neighbour of
+// the leaf's voxels (stride 1: origin-8 .. origin+8; stride 2: 2*origin-8 ..
+// 2*origin+8, per axis) are found once by tree walks and staged in shared
+// memory; every voxel-offset lookup is then a shared-memory mask test plus a
+// popcount.  Pass A counts pairs per (offset, output leaf) and writes the
+// 27-bit masks; a device-wide exclusive scan over the offset-major counts gives
+// every (offset, leaf) its position; pass B writes the pairs, ordered by output
+// inside each offset list, without atomics (deterministic).
+#include <cuda_runtime.h>
+#include <string.h>
+
+#include "block_scan.cuh"
+#include "fvx_internal.cuh"
+
+namespace fvx {
+namespace {
+
+constexpr int kKmThreads = 256;
+constexpr int kKmWarps = kKmThreads / 32;
+
+struct KmSmem {
+  unsigned long long mask[27][8];
+  unsigned long long pre9[27];
+  uint32_t first[27];
+  int nleaf[27];
+  uint16_t vox[512];
+  uint32_t omask[512];
+  int nvox;
+  uint32_t qfirst;
+};
+
+__device__ __forceinline__ void km_prologue(KmSmem& sm, const GridDev& gin, const int32_t* __restrict__ out_origin,
+                                            const int32_t* __restrict__ out_batch,
+                                            const uint64_t* __restrict__ out_rec, int stride, int lo) {
+  const int tid = threadIdx.x;
+  if (tid < 27) {
+    const int a = tid / 9, b = (tid / 3) % 3, c = tid % 3;
+    const int bt = out_batch[lo];
+    const int oi = stride * out_origin[3 * lo] - 8 + 8 * a;
+    const int oj = stride * out_origin[3 * lo + 1] - 8 + 8 * b;
+    const int ok = stride * out_origin[3 * lo + 2] - 8 + 8 * c;
+    const int l = find_leaf(gin, bt, oi, oj, ok);
+    sm.nleaf[tid] = l;
+    if (l >= 0) {
+      const unsigned long long* r = reinterpret_cast<const unsigned long long*>(gin.leaf_rec) + (size_t)l * 10;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) sm.mask[tid][w] = __ldg(r + w);
+      sm.first[tid] = (uint32_t)__ldg(r + 8);
+      sm.pre9[tid] = __ldg(r + 9);
+    }
+  }
+  // active voxels of the output leaf, ascending bit number = ascending index
+  const unsigned long long* orec = reinterpret_cast<const unsigned long long*>(out_rec) + (size_t)lo * 10;
+  const unsigned long long pre9 = __ldg(orec + 9);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int n = tid + h * 256;
+    const int w = n >> 6, bit = n & 63;
+    const unsigned long long m = __ldg(orec + w);
+    if ((m >> bit) & 1ull) {
+      const uint32_t pre = w ? (uint32_t)((pre9 >> (9 * (w - 1))) & 511ull) : 0u;
+      const uint32_t rank = pre + (uint32_t)__popcll(m & ((1ull << bit) - 1ull));
+      sm.vox[rank] = (uint16_t)n;
+      sm.omask[rank] = 0u;
+    }
+  }
+  if (tid == 0) {
+    sm.nvox = (int)(((pre9 >> 54) & 511ull) + (unsigned long long)__popcll(__ldg(orec + 7)));
+    sm.qfirst = (uint32_t)__ldg(orec + 8);
+  }
+  __syncthreads();
+}
+
+// input index of the neighbour of output voxel n at offset (di, dj, dk), or -1
+__device__ __forceinline__ int km_neighbour(const KmSmem& sm, int n, int stride, int di, int dj, int dk) {
+  const int ri = stride * (n >> 6) + 8 + di;
+  const int rj = stride * ((n >> 3) & 7) + 8 + dj;
+  const int rk = stride * (n & 7) + 8 + dk;
+  const int slot = (ri >> 3) * 9 + (rj >> 3) * 3 + (rk >> 3);
+  if (sm.nleaf[slot] < 0) return -1;
+  const int nn = ((ri & 7) << 6) | ((rj & 7) << 3) | (rk & 7);
+  const int w = nn >> 6, bit = nn & 63;
+  const unsigned long long m = sm.mask[slot][w];
+  if (!((m >> bit) & 1ull)) return -1;
+  const uint32_t pre = w ? (uint32_t)((sm.pre9[slot] >> (9 * (w - 1))) & 511ull) : 0u;
+  return (int)(sm.first[slot] + pre + (uint32_t)__popcll(m & ((1ull << bit) - 1ull)));
+}
+
+__global__ void __launch_bounds__(kKmThreads) k_kmap_count(GridDev gin, const int32_t* __restrict__ out_origin,
+                                                           const int32_t* __restrict__ out_batch,
+                                                           const uint64_t* __restrict__ out_rec, int64_t n_out_leaf,
+                                                           int stride, uint32_t* __restrict__ counts,
+                                                           uint32_t* __restrict__ out_mask) {
+  __shared__ KmSmem sm;
+  const int lo = blockIdx.x;
+  km_prologue(sm, gin, out_origin, out_batch, out_rec, stride, lo);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int s = warp; s < 27; s += kKmWarps) {
+    const int di = s / 9 - 1, dj = (s / 3) % 3 - 1, dk = s % 3 - 1;
+    uint32_t cnt = 0;
+    for (int c0 = 0; c0 < sm.nvox; c0 += 32) {
+      const int idx = c0 + lane;
+      const int p = (idx < sm.nvox) ? km_neighbour(sm, sm.vox[idx], stride, di, dj, dk) : -1;
+      cnt += __popc(__ballot_sync(0xffffffffu, p >= 0));
+      if (p >= 0) atomicOr(&sm.omask[idx], 1u << s);
+    }
+    if (lane == 0) counts[(int64_t)s * n_out_leaf + lo] = cnt;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < sm.nvox; idx += kKmThreads) out_mask[sm.qfirst + idx] = sm.omask[idx];
+}
+
+__global__ void __launch_bounds__(kKmThreads) k_kmap_write(GridDev gin, const int32_t* __restrict__ out_origin,
+                                                           const int32_t* __restrict__ out_batch,
+                                                           const uint64_t* __restrict__ out_rec, int64_t n_out_leaf,
+                                                           int stride, const uint32_t* __restrict__ starts,
+                                                           int32_t* __restrict__ in_idx,
+                                                           int32_t* __restrict__ out_idx) {
+  __shared__ KmSmem sm;
+  const int lo = blockIdx.x;
+  km_prologue(sm, gin, out_origin, out_batch, out_rec, stride, lo);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t lt = lanemask_lt();
+  for (int s = warp; s < 27; s += kKmWarps) {
+    const int di = s / 9 - 1, dj = (s / 3) % 3 - 1, dk = s % 3 - 1;
+    uint32_t pos = starts[(int64_t)s * n_out_leaf + lo];
+    for (int c0 = 0; c0 < sm.nvox; c0 += 32) {
+      const int idx = c0 + lane;
+      const int p = (idx < sm.nvox) ? km_neighbour(sm, sm.vox[idx], stride, di, dj, dk) : -1;
+      const uint32_t bal = __ballot_sync(0xffffffffu, p >= 0);
+      if (p >= 0) {
+        const uint32_t e = pos + __popc(bal & lt);
+        in_idx[e] = p;
+        out_idx[e] = (int32_t)(sm.qfirst + idx);
+      }
+      pos += __popc(bal);
+    }
+  }
+}
+
+__global__ void k_list_offsets(const uint32_t* __restrict__ starts, int64_t n_out_leaf, const uint32_t* total,
+                               uint32_t* __restrict__ out) {
+  const int s = threadIdx.x;
+  if (s < 27) out[s] = (n_out_leaf > 0) ? starts[(int64_t)s * n_out_leaf] : 0u;
+  if (s == 27) out[27] = *total;
+}
+
+// per conv tile of kTileRows outputs: number of outputs with mask bit s
+__global__ void __launch_bounds__(kTileRows) k_tile_counts(const uint32_t* __restrict__ mask, int64_t n_out,
+                                                           int64_t ntiles, uint32_t* __restrict__ cnt) {
+  const int64_t q = (int64_t)blockIdx.x * kTileRows + threadIdx.x;
+  const uint32_t m = (q < n_out) ? mask[q] : 0u;
+  for (int s = 0; s < 27; ++s) {
+    const int c = __syncthreads_count((m >> s) & 1u);
+    if (threadIdx.x == 0) cnt[(int64_t)s * ntiles + blockIdx.x] = (uint32_t)c;
+  }
+}
+
+size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace
+}  // namespace fvx
+
+using namespace fvx;
+
+extern "C" fvx_status fvx_kernel_map(fvx_grid gin, fvx_grid gout, int32_t ksize, int32_t stride, fvx_stream stream,
+                                     fvx_kmap* out) {
+  if (!gin || !gout || !out) {
+    set_error("fvx_kernel_map: NULL argument");
+    return FVX_ERR_INVALID_ARG;
+  }
+  *out = nullptr;
+  if (ksize != 3 || (stride != 1 && stride != 2)) {
+    set_error("fvx_kernel_map: need ksize == 3 and stride 1 or 2 (got %d, %d)", ksize, stride);
+    return FVX_ERR_INVALID_ARG;
+  }
+  if (gin->B != gout->B) {
+    set_error("fvx_kernel_map: batch sizes differ (%d vs %d)", gin->B, gout->B);
+    return FVX_ERR_INVALID_ARG;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  Scratch scr(s);
+  fvx_kmap_s* m = new fvx_kmap_s();
+  struct Guard {
+    fvx_kmap_s** m;
+    ~Guard() {
+      if (*m) fvx_kmap_destroy(*m);
+    }
+  } guard{&m};
+  m->stride = stride;
+  m->n_out = gout->n_active;
+  m->stream = s;
+  m->gin = gin;
+  m->gout = gout;
+  const int64_t Lo = gout->n_leaf, Nout = gout->n_active;
+  m->n_tiles = (Nout + kTileRows - 1) / kTileRows;
+
+  uint32_t* counts = scr.get<uint32_t>((size_t)(27 * Lo + 1));
+  uint32_t* dtot = scr.get<uint32_t>(32);
+  if (!counts || !dtot) return FVX_ERR_ALLOC;
+  // mask + conv tiling live in the first block, pairs in the second
+  const size_t o_mask = 0, o_tile = align_up(4 * (size_t)Nout);
+  const size_t bytes1 = o_tile + align_up(4 * (size_t)(27 * m->n_tiles + 1));
+  m->block = dalloc(bytes1, s);
+  if (!m->block) return FVX_ERR_ALLOC;
+  m->out_mask = (uint32_t*)((char*)m->block + o_mask);
+  m->tile_start = (uint32_t*)((char*)m->block + o_tile);
+
+  const GridDev gd = grid_dev(gin);
+  if (Lo > 0) {
+    LaunchScope ls("kmap_count", s);
+    k_kmap_count<<<(unsigned)Lo, kKmThreads, 0, s>>>(gd, gout->leaf_origin, gout->leaf_batch, gout->leaf_rec, Lo,
+                                                     stride, counts, m->out_mask);
+  }
+  FVX_TRY(check_launch("kmap_count"));
+  FVX_TRY(scan_exclusive_u32(counts, counts, 27 * Lo, dtot + 28, s));
+  {
+    LaunchScope ls("kmap_list_offsets", s);
+    k_list_offsets<<<1, 32, 0, s>>>(counts, Lo, dtot + 28, dtot);
+  }
+  FVX_TRY(check_launch("kmap_list_offsets"));
+  uint32_t* h = (uint32_t*)pinned_staging(28 * 4);
+  if (!h) return FVX_ERR_ALLOC;
+  FVX_CUDA(cudaMemcpyAsync(h, dtot, 28 * 4, cudaMemcpyDeviceToHost, s));
+  FVX_CUDA(cudaStreamSynchronize(s));
+  for (int t = 0; t < 28; ++t) m->offsets_host[t] = h[t];
+  const int64_t P = m->offsets_host[27];
+  if (P >= (int64_t)INT32_MAX) {
+    set_error("fvx_kernel_map: %lld pairs exceed the int32 pair index range", (long long)P);
+    return FVX_ERR_RANGE;
+  }
+  m->n_pairs = P;
+  m->block2 = dalloc(2 * align_up(4 * (size_t)P), s);
+  if (!m->block2) return FVX_ERR_ALLOC;
+  m->in_idx = (int32_t*)m->block2;
+  m->out_idx = (int32_t*)((char*)m->block2 + align_up(4 * (size_t)P));
+  if (Lo > 0 && P > 0) {
+    LaunchScope ls("kmap_write", s);
+    k_kmap_write<<<(unsigned)Lo, kKmThreads, 0, s>>>(gd, gout->leaf_origin, gout->leaf_batch, gout->leaf_rec, Lo,
+                                                     stride, counts, m->in_idx, m->out_idx);
+  }
+  FVX_TRY(check_launch("kmap_write"));
+  // conv tiling: where each tile's pairs start in every list
+  if (m->n_tiles > 0) {
+    {
+      LaunchScope ls("kmap_tile_counts", s);
+      k_tile_counts<<<(unsigned)m->n_tiles, kTileRows, 0, s>>>(m->out_mask, Nout, m->n_tiles, m->tile_start);
+    }
+    FVX_TRY(check_launch("kmap_tile_counts"));
+  }
+  FVX_TRY(scan_exclusive_u32(m->tile_start, m->tile_start, 27 * m->n_tiles, m->tile_start + 27 * m->n_tiles, s));
+  *out = m;
+  m = nullptr;
+  return FVX_OK;
+}

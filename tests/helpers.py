@@ -65,12 +65,21 @@ def tree_lookup(upper, lower, leaves, batch, ijk):
     batch = np.asarray(batch, dtype=np.int64).reshape(-1)
     n = ijk.shape[0]
     out = np.full(n, -1, np.int64)
-    root = {}
-    for u in range(upper["origin"].shape[0]):
-        root[(int(upper["batch"][u]),) + tuple(int(v) for v in upper["origin"][u])] = u
-    uorg = ijk - np.mod(ijk, UPPER)
-    uidx = np.array([root.get((int(batch[r]),) + tuple(int(v) for v in uorg[r]), -1) for r in range(n)],
-                    dtype=np.int64)
+    # root: sorted (batch, origin) keys of the upper nodes, searched per query
+    ukeys = np.concatenate([np.asarray(upper["batch"], np.int64)[:, None],
+                            np.asarray(upper["origin"], np.int64)], axis=1)
+    qkeys = np.concatenate([batch[:, None], ijk - np.mod(ijk, UPPER)], axis=1)
+    uidx = np.full(n, -1, np.int64)
+    if 0 < ukeys.shape[0] <= 64:
+        for u in range(ukeys.shape[0]):
+            uidx[np.all(qkeys == ukeys[u], axis=1)] = u
+    elif ukeys.shape[0] > 64:
+        allk = np.concatenate([ukeys, qkeys], axis=0)
+        _, inv = np.unique(allk, axis=0, return_inverse=True)
+        inv = inv.reshape(-1)
+        pos = np.full(inv.max() + 1, -1, np.int64)
+        pos[inv[:ukeys.shape[0]]] = np.arange(ukeys.shape[0])
+        uidx = pos[inv[ukeys.shape[0]:]]
     ok = uidx >= 0
 
     def child(mask, prefix, first, node, nbit, words):
@@ -152,3 +161,20 @@ def dense_conv_active(ijk_in, x, W, ijk_out, stride):
     # dense output index o corresponds to coordinate lo/stride + o
     orel = ijk_out - lo // stride
     return y[0, :, orel[:, 0], orel[:, 1], orel[:, 2]].T.numpy()
+
+
+def key64(batch, ijk):
+    """Order-preserving int64 packing of the canonical tuple for data whose
+    batch < 16 and root tiles lie in [-8, 8): batch | 3 tiles | 36 offset bits."""
+    ijk = np.asarray(ijk, dtype=np.int64).reshape(-1, 3)
+    b = np.asarray(batch, dtype=np.int64).reshape(-1)
+    tile = np.floor_divide(ijk, UPPER)
+    assert b.size == 0 or (b.min() >= 0 and b.max() < 16 and tile.min() >= -8 and tile.max() < 8)
+    o = np.mod(ijk, UPPER)
+    u, l, v = o // LOWER, (o % LOWER) // LEAF, o % LEAF
+    off = ((u[:, 0] * 32 + u[:, 1]) * 32 + u[:, 2])
+    off = (off * 16 + l[:, 0]) * 16 + l[:, 1]
+    off = (off * 16 + l[:, 2]) * 8 + v[:, 0]
+    off = (off * 8 + v[:, 1]) * 8 + v[:, 2]
+    t = ((b * 16 + tile[:, 0] + 8) * 16 + tile[:, 1] + 8) * 16 + tile[:, 2] + 8
+    return (t << 36) | off

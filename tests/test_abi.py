@@ -1,0 +1,95 @@
+"""The C-ABI library builds for sm_103a, loads, exports every entry point that
+include/fvx.h declares, and validates arguments on the host (no GPU needed:
+every call below returns before any CUDA work)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sparse_convolution_gb300 import build_lib
+
+    build_lib.build()
+    import sparse_convolution_gb300 as fvx
+
+    return fvx.load()
+
+
+def _declared():
+    txt = open(os.path.join(ROOT, "include", "fvx.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(fvx_[a-z_0-9]+)\s*\(", txt)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ("fvx_build_grid", "fvx_kernel_map", "fvx_sparse_conv", "fvx_lookup", "fvx_coarsen",
+              "fvx_grid_view", "fvx_kmap_view", "fvx_grid_destroy", "fvx_kmap_destroy", "fvx_set_allocator",
+              "fvx_status_string", "fvx_last_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(lib):
+    assert lib.fvx_status_string(0) == b"FVX_OK"
+    assert lib.fvx_status_string(2) == b"FVX_ERR_RANGE"
+    assert lib.fvx_status_string(6) == b"FVX_ERR_DEVICE_TIMEOUT"
+
+
+def _build(lib, coords_ptr, n, offs, B):
+    out = ctypes.c_void_p()
+    o = np.asarray(offs, np.int64)
+    st = lib.fvx_build_grid(coords_ptr, n, o.ctypes.data_as(ctypes.c_void_p), B, None, ctypes.byref(out))
+    return st, lib.fvx_last_error().decode()
+
+
+def test_build_validates_on_host(lib):
+    fake = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails first
+    st, msg = _build(lib, fake, 10, [0, 10], 0)
+    assert st == 1 and "B >= 1" in msg
+    st, msg = _build(lib, fake, 10, [0, 4, 3, 10], 3)
+    assert st == 1 and "monotone" in msg
+    st, msg = _build(lib, fake, 10, [0, 9], 1)
+    assert st == 1 and "end at n_rows" in msg
+    st, msg = _build(lib, fake, -1, [0, -1], 1)
+    assert st == 1
+    st, msg = _build(lib, None, 10, [0, 10], 1)
+    assert st == 1 and "NULL" in msg
+
+
+def test_kmap_and_conv_validate_on_host(lib):
+    out = ctypes.c_void_p()
+    assert lib.fvx_kernel_map(None, None, 3, 1, None, ctypes.byref(out)) == 1
+    assert lib.fvx_sparse_conv(None, None, None, 1, None, 8, None, 16, None, None) == 1
+    assert lib.fvx_coarsen(None, 2, None, ctypes.byref(out)) == 1
+    assert lib.fvx_set_allocator(ctypes.c_void_p(1), None, None) == 1
+    assert lib.fvx_set_allocator(None, None, None) == 0
+
+
+def test_launch_counter_and_profiler_idle(lib):
+    import sparse_convolution_gb300 as fvx
+
+    n0 = fvx.launch_count()
+    fvx.profile_enable("conv_bf16_tc")
+    assert fvx.profile_read() == (0.0, 0)
+    fvx.profile_enable(None)
+    assert fvx.launch_count() == n0
+
+
+def test_package_fails_loudly_without_library(tmp_path, monkeypatch):
+    import sparse_convolution_gb300 as fvx
+
+    monkeypatch.setattr(fvx, "_lib", None)
+    monkeypatch.setattr(fvx, "LIB_PATH", str(tmp_path / "libfvx.so"))
+    with pytest.raises(fvx.FvxError, match="missing"):
+        fvx.load()

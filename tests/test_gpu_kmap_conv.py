@@ -1,0 +1,147 @@
+"""GPU kernel map and sparse conv vs the CPU oracle.
+
+Kernel map: bit-exact ("DriveRT", Shared neighbour maps).  Conv: within
+2e-3 * sum|w*x| per output element for bf16 (bf16-rounded inputs, fp32
+accumulation, bf16 output) and 1e-5 * sum|w*x| for fp32 ("fVDB: A Deep-Learning
+Framework for Sparse, Large Scale, and High Performance Spatial Intelligence"
+notes, Sparse-convolution operators)."""
+import numpy as np
+import pytest
+
+import oracle
+from tests import gpu_common as G
+
+pytestmark = pytest.mark.gpu
+
+
+def _random(seed, n, lo, span, B, dup=0.1):
+    rng = np.random.default_rng(seed)
+    rows, offs = [], [0]
+    for _ in range(B):
+        c = rng.integers(lo, lo + span, size=(n, 3)).astype(np.int32)
+        c = np.concatenate([c, c[rng.integers(0, n, size=int(dup * n))]])
+        rows.append(c[rng.permutation(len(c))])
+        offs.append(offs[-1] + len(c))
+    return np.concatenate(rows), np.array(offs, np.int64)
+
+
+@pytest.fixture(scope="module")
+def grids():
+    c, offs = _random(3, 9000, -25, 50, 2)
+    import sparse_convolution_gb300 as fvx  # noqa: F401
+
+    g = G.gpu_grid(c, offs)
+    og = oracle.Grid.build(c, offs)
+    gc = g.coarsen(2)
+    ogc = og.coarsen(2)
+    return dict(g=g, og=og, gc=gc, ogc=ogc)
+
+
+def _maps(grids, stride):
+    import sparse_convolution_gb300 as fvx
+
+    if stride == 1:
+        return grids["g"], grids["g"], fvx.KernelMap(grids["g"], grids["g"], 1), oracle.KernelMap(
+            grids["og"], grids["og"], 1)
+    return grids["g"], grids["gc"], fvx.KernelMap(grids["g"], grids["gc"], 2), oracle.KernelMap(
+        grids["og"], grids["ogc"], 2)
+
+
+@pytest.mark.parametrize("stride", [1, 2])
+def test_kmap_matches_oracle(cuda_device, grids, stride):
+    _, _, km, okm = _maps(grids, stride)
+    G.assert_kmap_equal(km, okm)
+
+
+def test_kmap_between_unrelated_grids(cuda_device):
+    """Stride-1 map from one grid to a different output grid: outputs far from
+    every input get no pairs (and a zero conv output)."""
+    import sparse_convolution_gb300 as fvx
+
+    a, oa = _random(41, 3000, 0, 30, 1)
+    b, ob = _random(42, 3000, 20, 40, 1)
+    ga, gb = G.gpu_grid(a, oa), G.gpu_grid(b, ob)
+    oga, ogb = oracle.Grid.build(a, oa), oracle.Grid.build(b, ob)
+    km = fvx.KernelMap(ga, gb, 1)
+    okm = oracle.KernelMap(oga, ogb, 1)
+    G.assert_kmap_equal(km, okm)
+    x, W = G.bf16_inputs(5, ga.n_active, 16, 32)
+    y = fvx.sparse_conv(ga, gb, km, x, W)
+    yo, ao = oracle.conv(okm, G.as_f64(x), G.as_f64(W))
+    assert (okm.mask == 0).any()
+    G.assert_conv_close(G.np_(y.float()), yo, ao, G.BF16_TOL)
+    assert np.all(G.np_(y.float())[okm.mask == 0] == 0)
+
+
+@pytest.mark.parametrize("cin,cout", [(16, 16), (5, 7), (3, 33), (32, 8)])
+@pytest.mark.parametrize("stride", [1, 2])
+def test_conv_f32_matches_oracle(cuda_device, grids, stride, cin, cout):
+    import torch
+
+    import sparse_convolution_gb300 as fvx
+    from sparse_convolution_gb300 import synth
+
+    gin, gout, km, okm = _maps(grids, stride)
+    x = torch.from_numpy(synth.features(7, gin.n_active, cin, "uniform")).cuda()
+    W = torch.from_numpy(synth.weights(8, cin, cout)).cuda()
+    y = fvx.sparse_conv(gin, gout, km, x, W)
+    yo, ao = oracle.conv(okm, G.as_f64(x), G.as_f64(W))
+    G.assert_conv_close(G.np_(y), yo, ao, G.F32_TOL)
+
+
+@pytest.mark.parametrize("cin,cout", [(8, 16), (16, 32), (32, 64), (64, 64), (128, 128), (128, 256), (24, 48),
+                                      (256, 16)])
+@pytest.mark.parametrize("stride", [1, 2])
+def test_conv_bf16_matches_oracle(cuda_device, grids, stride, cin, cout):
+    import sparse_convolution_gb300 as fvx
+
+    gin, gout, km, okm = _maps(grids, stride)
+    x, W = G.bf16_inputs(11, gin.n_active, cin, cout)
+    y = fvx.sparse_conv(gin, gout, km, x, W)
+    fvx.device_status()
+    yo, ao = oracle.conv(okm, G.as_f64(x), G.as_f64(W))
+    G.assert_conv_close(G.np_(y.float()), yo, ao, G.BF16_TOL)
+
+
+def test_conv_bf16_identity_is_exact(cuda_device, grids):
+    """W[13] = I, other offsets 0: out == feats bit for bit."""
+    import torch
+
+    import sparse_convolution_gb300 as fvx
+
+    g = grids["g"]
+    km = fvx.KernelMap(g, g, 1)
+    x, _ = G.bf16_inputs(13, g.n_active, 64, 64)
+    W = torch.zeros((27, 64, 64), dtype=torch.bfloat16, device="cuda")
+    W[13] = torch.eye(64, dtype=torch.bfloat16, device="cuda")
+    y = fvx.sparse_conv(g, g, km, x, W)
+    assert torch.equal(y, x)
+
+
+def test_conv_bf16_repeatable(cuda_device, grids):
+    import torch
+
+    import sparse_convolution_gb300 as fvx
+
+    gin, gout, km, _ = _maps(grids, 1)
+    x, W = G.bf16_inputs(17, gin.n_active, 64, 128)
+    y1 = fvx.sparse_conv(gin, gout, km, x, W)
+    y2 = fvx.sparse_conv(gin, gout, km, x, W)
+    assert torch.equal(y1, y2)
+
+
+def test_conv_rejects_bad_shapes(cuda_device, grids):
+    import torch
+
+    import sparse_convolution_gb300 as fvx
+
+    gin, gout, km, _ = _maps(grids, 1)
+    x = torch.zeros((gin.n_active, 12), dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros((27, 12, 16), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(fvx.FvxError, match="FVX_ERR_INVALID_ARG"):
+        fvx.sparse_conv(gin, gout, km, x, W)
+    x2 = torch.zeros((gin.n_active, 16), dtype=torch.bfloat16, device="cuda")
+    W2 = torch.zeros((27, 16, 16), dtype=torch.bfloat16, device="cuda")
+    km2 = fvx.KernelMap(grids["g"], grids["gc"], 2)
+    with pytest.raises(fvx.FvxError, match="other grids"):
+        fvx.sparse_conv(gin, gout, km2, x2, W2)
