@@ -55,7 +55,12 @@ typedef enum {
   FVX_ERR_CHECK = 7           /* a device-side check failed (see fvx_last_error) */
 } fvx_status;
 
-typedef enum { FVX_F32 = 0, FVX_BF16 = 1 } fvx_dtype;
+/* Conv arithmetic / storage types.
+ *   FVX_F32            fp32 feats, weights and output; exact fp32 FFMA.
+ *   FVX_BF16           bf16 feats and weights, fp32 accumulation, fp32 output.
+ *   FVX_BF16_OUT_BF16  bf16 feats and weights, fp32 accumulation, output rounded
+ *                      to bf16 (nearest even): adds up to 2^-8 |y| of error. */
+typedef enum { FVX_F32 = 0, FVX_BF16 = 1, FVX_BF16_OUT_BF16 = 2 } fvx_dtype;
 
 /* Device memory the library allocates for grids, kernel maps and temporary
  * buffers goes through these callbacks (stream-ordered).  Default (or after
@@ -163,13 +168,13 @@ fvx_status fvx_kmap_view(fvx_kmap m, const int64_t** offsets_host, const int32_t
  *   out[q, co] = sum_s sum_{(p,q) in list s} sum_ci feats[p, ci] * W[s, ci, co]
  *
  * Cross-correlation, no bias; outputs without pairs are 0.
- * feats  device [gin.n_active, cin], row-major, dtype dt.
- * W      device [27, cin, cout], row-major, dtype dt.
- * out    device [gout.n_active, cout], row-major, dtype dt, caller-allocated;
- *        fully overwritten.
- * FVX_BF16: bf16 inputs, fp32 accumulation on the tensor cores, bf16 output
- *           (round to nearest even).  cin and cout multiples of 8 and 16,
- *           cin <= 512, cout <= 256.
+ * feats  device [gin.n_active, cin], row-major (fp32 for FVX_F32, else bf16).
+ * W      device [27, cin, cout], row-major (same type as feats).
+ * out    device [gout.n_active, cout], row-major, caller-allocated, fully
+ *        overwritten; bf16 for FVX_BF16_OUT_BF16, else fp32.
+ * FVX_BF16 / FVX_BF16_OUT_BF16: tcgen05 tensor cores, fp32 accumulation in
+ *           TMEM.  cin a multiple of 8 (<= 512), cout a multiple of 16
+ *           (<= 256); feats and out 16-byte aligned.
  * FVX_F32:  fp32 FFMA throughout (no TF32).  cin, cout >= 1.
  * m must have been built for (gin, gout).  Errors: FVX_ERR_INVALID_ARG. */
 fvx_status fvx_sparse_conv(fvx_grid gin, fvx_grid gout, fvx_kmap m, fvx_dtype dt, const void* feats, int64_t cin,

@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(_HERE, "libfvx.so")
 
 _lib = None
 
-FVX_F32, FVX_BF16 = 0, 1
+FVX_F32, FVX_BF16, FVX_BF16_OUT_BF16 = 0, 1, 2
 
 
 class FvxError(RuntimeError):
@@ -102,7 +102,7 @@ class _DevArray:
 
     def __init__(self, ptr, shape, typestr, owner):
         self.__cuda_array_interface__ = dict(shape=tuple(int(s) for s in shape), typestr=typestr,
-                                             data=(int(ptr or 0), True), version=3, strides=None)
+                                             data=(int(ptr or 0), False), version=3, strides=None)
         self._owner = owner
 
 
@@ -233,20 +233,28 @@ class KernelMap:
                 _view(mm, (self.n_out,), "u4", self))
 
 
-def sparse_conv(gin: Grid, gout: Grid, kmap: KernelMap, feats, W, out=None, stream=None):
+def sparse_conv(gin: Grid, gout: Grid, kmap: KernelMap, feats, W, out=None, out_dtype=None, stream=None):
     """out[q] = sum over pairs (p, q) of list s of feats[p] @ W[s].
-    feats [gin.n_active, cin] and W [27, cin, cout]: both float32 or both
-    bfloat16 CUDA tensors; returns [gout.n_active, cout] of the same dtype."""
+
+    feats [gin.n_active, cin] and W [27, cin, cout]: both float32 (exact fp32
+    FFMA, float32 out) or both bfloat16 (tensor cores, fp32 accumulation;
+    out_dtype float32 by default, or bfloat16 for a rounded bf16 output)."""
     import torch
 
     assert feats.dtype == W.dtype and feats.is_cuda and W.is_cuda
-    dt = {torch.float32: FVX_F32, torch.bfloat16: FVX_BF16}[feats.dtype]
+    if feats.dtype == torch.float32:
+        dt, odt = FVX_F32, torch.float32
+    else:
+        assert feats.dtype == torch.bfloat16
+        odt = out_dtype or (out.dtype if out is not None else torch.float32)
+        dt = {torch.float32: FVX_BF16, torch.bfloat16: FVX_BF16_OUT_BF16}[odt]
     feats = feats.contiguous()
     W = W.contiguous()
     cin, cout = W.shape[1], W.shape[2]
     assert W.shape[0] == 27 and feats.shape[1] == cin
     if out is None:
-        out = torch.empty((gout.n_active, cout), dtype=feats.dtype, device=feats.device)
+        out = torch.empty((gout.n_active, cout), dtype=odt, device=feats.device)
+    assert out.dtype == odt and out.is_contiguous() and tuple(out.shape) == (gout.n_active, cout)
     _check(load().fvx_sparse_conv(gin._h, gout._h, kmap._h, dt, _ptr(feats), cin, _ptr(W), cout, _ptr(out),
                                   _stream(stream)))
     return out

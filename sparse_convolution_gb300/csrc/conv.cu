@@ -16,13 +16,19 @@
 // among the tile's rows with bit s, added to the tile's start in list s.
 //
 // Two kernels, one per dtype (no dispatch between backends):
-//   * bf16: cp.async gathers into 128B-swizzled K-major shared tiles,
-//     tcgen05.mma kind::f16 (bf16 x bf16 -> fp32 in TMEM) issued by one
-//     thread, tcgen05.ld epilogue, bf16 round-to-nearest-even output.
+//   * bf16: persistent and warp-specialized.  Producers build each tile's row
+//     table (software-pipelined one tile ahead) and gather A (feature rows)
+//     and B (weight rows) with cp.async into 128B-swizzled K-major stages;
+//     one thread issues tcgen05.mma kind::f16 (bf16 x bf16 -> fp32 in TMEM);
+//     epilogue warps drain a double-buffered TMEM accumulator with tcgen05.ld
+//     while the next tile accumulates.  Output fp32, or bf16 rounded to nearest
+//     even.
 //   * fp32: exact FFMA on CUDA cores (no TF32).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <string.h>
+
+#include <algorithm>
 
 #include "block_scan.cuh"
 #include "fvx_internal.cuh"
@@ -32,7 +38,7 @@ namespace {
 
 constexpr int kRows = kTileRows;  // 128
 
-// ============================================================== shared prologue
+// ============================================================== tile row tables
 // Per tile: for each offset s, the ballot of the tile's rows having bit s, per
 // warp (4 warps x 32 rows).  rank of row m in list s = popcount of the bits
 // before it.
@@ -41,7 +47,7 @@ struct TileMasks {
 };
 
 __device__ __forceinline__ void tile_ballots(TileMasks& tm, uint32_t mk) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
 #pragma unroll 1
   for (int s = 0; s < 27; ++s) {
     const uint32_t b = __ballot_sync(0xffffffffu, (mk >> s) & 1u);
@@ -71,22 +77,26 @@ __global__ void __launch_bounds__(kRows) k_conv_f32(const float* __restrict__ x,
                                                     const uint32_t* __restrict__ tile_start, int64_t ntiles,
                                                     int64_t n_out, int cin, int cout, float* __restrict__ y) {
   __shared__ TileMasks tm;
+  __shared__ uint32_t tstart[27];
+  __shared__ int ps[27][kRows];  // gathered input row per (offset, tile row), -1 = none
   const int m = threadIdx.x, warp = m >> 5;
   const int64_t t = blockIdx.x;
   const int64_t q = t * kRows + m;
   const uint32_t mk = (q < n_out) ? mask[q] : 0u;
+  if (m < 27) tstart[m] = tile_start[(int64_t)m * ntiles + t];
   tile_ballots(tm, mk);
   __syncthreads();
   const uint32_t lt = lanemask_lt();
-  const uint32_t tor = tile_or(tm);
+#pragma unroll
+  for (int s = 0; s < 27; ++s)
+    ps[s][m] = ((mk >> s) & 1u) ? __ldg(in_idx + tstart[s] + tile_rank(tm, s, warp, lt)) : -1;
   for (int c0 = 0; c0 < cout; c0 += kF32Cols) {
     float acc[kF32Cols];
 #pragma unroll
     for (int c = 0; c < kF32Cols; ++c) acc[c] = 0.f;
     for (int s = 0; s < 27; ++s) {
-      if (!((tor >> s) & 1u)) continue;
-      if (!((mk >> s) & 1u)) continue;
-      const int p = in_idx[tile_start[(int64_t)s * ntiles + t] + tile_rank(tm, s, warp, lt)];
+      const int p = ps[s][m];
+      if (p < 0) continue;
       const float* xp = x + (int64_t)p * cin;
       const float* ws = W + (int64_t)s * cin * cout + c0;
       if (c0 + kF32Cols <= cout) {
@@ -116,15 +126,17 @@ __global__ void __launch_bounds__(kRows) k_conv_f32(const float* __restrict__ x,
 }
 
 // ============================================================== bf16 tcgen05
+// Warp roles of the persistent bf16 kernel: warps 0-3 build each tile's row
+// table and gather A/B into the stage ring, warp 4 issues the MMAs (and owns
+// TMEM), warps 5-8 drain the double-buffered TMEM accumulator to global.
 constexpr int kProducerWarps = 4;
-constexpr int kConvThreads = (kProducerWarps + 1) * 32;  // + one MMA-issue warp
-constexpr int kLag = 2;                                   // cp.async groups kept in flight per producer
-constexpr int kATileBytes = kRows * 128;                  // 128 rows x 64 bf16 (one 128B swizzle atom wide)
-constexpr unsigned long long kWaitNs = 2000000000ull;     // bounded mbarrier waits: 2 s
+constexpr int kMmaWarp = kProducerWarps;
+constexpr int kConvThreads = (kProducerWarps + 1 + 4) * 32;
+constexpr int kLag = 2;                                // cp.async groups kept in flight per producer
+constexpr int kATileBytes = kRows * 128;               // 128 rows x 64 bf16 (one 128B swizzle atom wide)
+constexpr unsigned long long kWaitNs = 2000000000ull;  // bounded mbarrier waits: 2 s
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
 __device__ __forceinline__ unsigned long long globaltimer() {
   unsigned long long t;
@@ -140,25 +152,24 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-// Waits for the phase with the given parity to complete; gives up after
-// kWaitNs (or when another CTA has already reported a failure), recording
-// DEV_TIMEOUT in the status word.  Returns false on give-up.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* status) {
-  uint32_t ok = 0;
+__device__ __forceinline__ uint32_t mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
   asm volatile(
       "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
       : "memory");
-  if (ok) return true;
+  return ok;
+}
+
+// Waits for the phase with the given parity to complete; gives up after
+// kWaitNs (or as soon as another CTA has reported a failure), recording
+// DEV_TIMEOUT in the status word.  Returns false on give-up.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* status) {
+  if (mbar_try(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   while (true) {
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    if (ok) return true;
+    if (mbar_try(bar, parity)) return true;
     if (globaltimer() - t0 > kWaitNs || *(volatile uint32_t*)status != 0u) {
       report_device_error(status, DEV_TIMEOUT);
       return false;
@@ -174,9 +185,8 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void producer_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 // UMMA shared-memory descriptor: K-major, 128-byte swizzle, 8-row groups
 // 1024 bytes apart (SBO), leading offset unused for this layout.
@@ -221,13 +231,22 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-struct ConvSmemHead {
+// Row table of one tile (double-buffered: producers fill tile i+1's while
+// gathering tile i's).
+struct TileTable {
   TileMasks tm;
   int32_t rowp[27][kRows];  // gathered input row for (offset slot, tile row), -1 = zeros
-  int32_t slot_s[27];       // offset of each slot (only offsets present in the tile)
-  unsigned long long full[8], empty[8], done;
+  int32_t slot_s[27];       // offset of each slot (offsets present in the tile, ascending)
+  uint32_t tstart[27];      // the tile's first pair in each list
+};
+
+struct ConvSmemHead {
+  TileTable tab[2];
+  unsigned long long full[8], empty[8];              // stage ring: producers <-> MMA
+  unsigned long long tinfo_full[2], tinfo_empty[2];  // per-tile stage count: producers -> MMA, epilogue
+  unsigned long long acc_full[2], acc_empty[2];      // TMEM accumulators: MMA <-> epilogue
+  int tinfo_nst[2];
   uint32_t tmem_base;
-  int nslots;
 };
 
 struct ConvArgs {
@@ -236,11 +255,43 @@ struct ConvArgs {
   const uint32_t* mask;
   const int32_t* in_idx;
   const uint32_t* tile_start;
-  __nv_bfloat16* y;
+  void* y;                  // fp32 or bf16 [n_out][cout]
   uint32_t* status;
   int64_t ntiles, n_out;
-  int cin, cout, stages, stage_bytes, b_bytes, tmem_cols;
+  int cin, cout, stages, stage_bytes, tmem_cols, out_bf16;
 };
+
+// Producer helpers ----------------------------------------------------------
+__device__ __forceinline__ uint32_t load_mask(const ConvArgs& a, int64_t t, int m) {
+  const int64_t q = t * kRows + m;
+  return (t < a.ntiles && q < a.n_out) ? __ldg(a.mask + q) : 0u;
+}
+__device__ __forceinline__ uint32_t load_tstart(const ConvArgs& a, int64_t t, int m) {
+  return (t < a.ntiles && m < 27) ? __ldg(a.tile_start + (int64_t)m * a.ntiles + t) : 0u;
+}
+
+// Issues the 27 independent input-index loads of this thread's row (results
+// land in ps while the caller goes on).  Requires tab.tm / tab.tstart set.
+__device__ __forceinline__ void issue_row_loads(const TileTable& tab, const int32_t* __restrict__ in_idx, uint32_t mk,
+                                                int (&ps)[27]) {
+  const int warp = threadIdx.x >> 5;
+  const uint32_t lt = lanemask_lt();
+#pragma unroll
+  for (int s = 0; s < 27; ++s) ps[s] = ((mk >> s) & 1u) ? __ldg(in_idx + tab.tstart[s] + tile_rank(tab.tm, s, warp, lt)) : -1;
+}
+
+__device__ __forceinline__ void store_rows(TileTable& tab, uint32_t tor, const int (&ps)[27]) {
+  const int m = threadIdx.x;
+  int slot = 0;
+#pragma unroll
+  for (int s = 0; s < 27; ++s) {
+    if ((tor >> s) & 1u) {
+      tab.rowp[slot][m] = ps[s];
+      if (m == 0) tab.slot_s[slot] = s;
+      ++slot;
+    }
+  }
+}
 
 __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tc(const __grid_constant__ ConvArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -248,161 +299,229 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tc(const __grid_c
   unsigned char* sbase = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   ConvSmemHead& h = *reinterpret_cast<ConvSmemHead*>(sbase + (size_t)a.stages * a.stage_bytes);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t t = blockIdx.x;
   const int S = a.stages;
+  const int ppo = a.cin >> 3;  // 16-byte pieces per (row, offset)
+  const uint32_t acc_cols = (uint32_t)a.tmem_cols;
+  const int64_t G = gridDim.x;
 
-  // ---- setup: barriers (thread 0), TMEM allocation (MMA warp)
+  // ---- setup: barriers (thread 0), TMEM for two accumulators (MMA warp)
   if (tid == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(smem_u32(&h.full[i]), kProducerWarps * 32);
       mbar_init(smem_u32(&h.empty[i]), 1);
     }
-    mbar_init(smem_u32(&h.done), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&h.tinfo_full[b]), 1);
+      mbar_init(smem_u32(&h.tinfo_empty[b]), 4);  // one arrival per epilogue warp
+      mbar_init(smem_u32(&h.acc_full[b]), 1);
+      mbar_init(smem_u32(&h.acc_empty[b]), 128);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == kProducerWarps) {
+  if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&h.tmem_base)),
-                 "r"(a.tmem_cols)
+                 "r"(2 * acc_cols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
-  // ---- tile prologue (producer warps): masks, ranks, gathered row per slot
-  uint32_t mk = 0;
-  if (warp < kProducerWarps) {
-    const int64_t q = t * kRows + tid;
-    mk = (q < a.n_out) ? a.mask[q] : 0u;
-    tile_ballots(h.tm, mk);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tor = tile_or(h.tm);
-  const int nslots = __popc(tor);
-  if (warp < kProducerWarps) {
-    const uint32_t lt = lanemask_lt();
-    int slot = 0;
-    for (int s = 0; s < 27; ++s) {
-      if (!((tor >> s) & 1u)) continue;
-      int p = -1;
-      if ((mk >> s) & 1u) p = a.in_idx[a.tile_start[(int64_t)s * a.ntiles + t] + tile_rank(h.tm, s, warp, lt)];
-      h.rowp[slot][tid] = p;
-      if (tid == 0) h.slot_s[slot] = s;
-      ++slot;
-    }
-  }
-  __syncthreads();
   const uint32_t tmem = h.tmem_base;
-  const int ppo = a.cin >> 3;  // 16-byte pieces per (row, offset)
-  const int total = nslots * ppo;
-  const int nst = (total + 7) >> 3;  // pipeline stages of 8 pieces (K = 64)
 
   if (warp < kProducerWarps) {
-    // ---------------- producers: gather A rows and B (weights) rows
+    // ---------------- producers
     const int m = tid;
-    int signaled = 0;
-    for (int k = 0; k < nst; ++k) {
-      const int sb = k % S;
-      if (k >= S) mbar_wait(smem_u32(&h.empty[sb]), (uint32_t)((k / S - 1) & 1), a.status);
-      const uint32_t sA = smem_u32(sbase + (size_t)sb * a.stage_bytes);
-      const uint32_t sB = sA + kATileBytes;
-#pragma unroll
-      for (int pc = 0; pc < 8; ++pc) {
-        const int g = 8 * k + pc;
-        const void* src = a.x;
-        uint32_t bytes = 0;
-        if (g < total) {
-          const int slot = g / ppo, cb = g - slot * ppo;
-          const int p = h.rowp[slot][m];
-          if (p >= 0) {
-            src = a.x + (int64_t)p * a.cin + cb * 8;
-            bytes = 16;
-          }
-        }
-        cp_async16(sA + (m >> 3) * 1024 + (m & 7) * 128 + ((pc ^ (m & 7)) << 4), src, bytes);
+    int64_t kg = 0, signaled = 0;  // stage counters, continuing across tiles
+    int ps[27];
+    // tables of the first tile (exposed once), masks of the second prefetched
+    int64_t t = blockIdx.x;
+    uint32_t mk_cur = load_mask(a, t, m), ts_cur = load_tstart(a, t, m);
+    uint32_t mk_nxt = load_mask(a, t + G, m), ts_nxt = load_tstart(a, t + G, m);
+    if (m < 27) h.tab[0].tstart[m] = ts_cur;
+    tile_ballots(h.tab[0].tm, mk_cur);
+    producer_bar();
+    uint32_t tor = tile_or(h.tab[0].tm);
+    issue_row_loads(h.tab[0], a.in_idx, mk_cur, ps);
+    store_rows(h.tab[0], tor, ps);
+    int total = __popc(tor) * ppo;
+    if (m == 0 && t < a.ntiles) {
+      h.tinfo_nst[0] = (total + 7) >> 3;
+      mbar_arrive(smem_u32(&h.tinfo_full[0]));
+    }
+    producer_bar();
+    for (int i = 0; t < a.ntiles; t += G, ++i) {
+      const int b = i & 1, nb = b ^ 1;
+      const bool has_next = (t + G) < a.ntiles;
+      const TileTable& cur = h.tab[b];
+      TileTable& nxt = h.tab[nb];
+      // (a) next tile: ballots and the 27 index loads (left in flight)
+      uint32_t tor_n = 0;
+      if (has_next) {
+        if (m < 27) nxt.tstart[m] = ts_nxt;
+        tile_ballots(nxt.tm, mk_nxt);
+        producer_bar();
+        tor_n = tile_or(nxt.tm);
+        issue_row_loads(nxt, a.in_idx, mk_nxt, ps);
       }
-      for (int n = m; n < a.cout; n += kProducerWarps * 32) {
+      const uint32_t mk_n = mk_nxt;
+      // (b) prefetch the masks of the tile after next
+      mk_nxt = load_mask(a, t + 2 * G, m);
+      ts_nxt = load_tstart(a, t + 2 * G, m);
+      // (c) gathers of this tile
+      const int64_t kg_tile0 = kg;       // first stage of this tile
+      const int nst = (total + 7) >> 3;  // stages of 8 pieces (K = 64)
+      for (int k = 0; k < nst; ++k, ++kg) {
+        const int sb = (int)(kg % S);
+        if (kg >= S) mbar_wait(smem_u32(&h.empty[sb]), (uint32_t)((kg / S - 1) & 1), a.status);
+        const uint32_t sA = smem_u32(sbase + (size_t)sb * a.stage_bytes);
+        const uint32_t sB = sA + kATileBytes;
 #pragma unroll
         for (int pc = 0; pc < 8; ++pc) {
           const int g = 8 * k + pc;
-          const void* src = a.wt;
+          const void* src = a.x;
           uint32_t bytes = 0;
           if (g < total) {
             const int slot = g / ppo, cb = g - slot * ppo;
-            src = a.wt + ((int64_t)h.slot_s[slot] * a.cout + n) * a.cin + cb * 8;
-            bytes = 16;
+            const int p = cur.rowp[slot][m];
+            if (p >= 0) {
+              src = a.x + (int64_t)p * a.cin + cb * 8;
+              bytes = 16;
+            }
           }
-          cp_async16(sB + (n >> 3) * 1024 + (n & 7) * 128 + ((pc ^ (n & 7)) << 4), src, bytes);
+          cp_async16(sA + (m >> 3) * 1024 + (m & 7) * 128 + ((pc ^ (m & 7)) << 4), src, bytes);
+        }
+        for (int n = m; n < a.cout; n += kProducerWarps * 32) {
+#pragma unroll
+          for (int pc = 0; pc < 8; ++pc) {
+            const int g = 8 * k + pc;
+            const void* src = a.wt;
+            uint32_t bytes = 0;
+            if (g < total) {
+              const int slot = g / ppo, cb = g - slot * ppo;
+              src = a.wt + ((int64_t)cur.slot_s[slot] * a.cout + n) * a.cin + cb * 8;
+              bytes = 16;
+            }
+            cp_async16(sB + (n >> 3) * 1024 + (n & 7) * 128 + ((pc ^ (n & 7)) << 4), src, bytes);
+          }
+        }
+        cp_async_commit();
+        if (kg - signaled >= kLag) {
+          cp_async_wait<kLag>();
+          fence_proxy_async();
+          mbar_arrive(smem_u32(&h.full[signaled % S]));
+          ++signaled;
         }
       }
-      cp_async_commit();
-      if (k - signaled >= kLag) {
-        cp_async_wait<kLag>();
+      // (d) next tile: row table and its stage count for the MMA and epilogue.
+      // Its count slot is freed by the epilogue of the previous tile, which
+      // needs every stage of that tile signaled: flush any still held back by
+      // the lag (a short tile may not have pushed them out).
+      if (signaled < kg_tile0) {
+        cp_async_wait<0>();
         fence_proxy_async();
-        mbar_arrive(smem_u32(&h.full[signaled % S]));
-        ++signaled;
+        while (signaled < kg) {
+          mbar_arrive(smem_u32(&h.full[signaled % S]));
+          ++signaled;
+        }
       }
+      if (has_next) {
+        store_rows(nxt, tor_n, ps);
+        total = __popc(tor_n) * ppo;
+        if (m == 0) {
+          if (i + 1 >= 2) mbar_wait(smem_u32(&h.tinfo_empty[nb]), (uint32_t)((((i + 1) >> 1) - 1) & 1), a.status);
+          h.tinfo_nst[nb] = (total + 7) >> 3;
+          mbar_arrive(smem_u32(&h.tinfo_full[nb]));
+        }
+      }
+      (void)mk_n;
+      producer_bar();  // tables of the next tile complete; this tile's no longer read
     }
     cp_async_wait<0>();
     fence_proxy_async();
-    while (signaled < nst) {
+    while (signaled < kg) {
       mbar_arrive(smem_u32(&h.full[signaled % S]));
       ++signaled;
     }
-  } else if (lane == 0) {
+  } else if (warp == kMmaWarp) {
     // ---------------- MMA issue (one thread)
-    const uint32_t idesc = idesc_bf16(kRows, a.cout);
-    for (int k = 0; k < nst; ++k) {
-      const int sb = k % S;
-      mbar_wait(smem_u32(&h.full[sb]), (uint32_t)((k / S) & 1), a.status);
-      tc_fence_after();
-      const uint32_t sA = smem_u32(sbase + (size_t)sb * a.stage_bytes);
-      const uint32_t sB = sA + kATileBytes;
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(kRows, a.cout);
+      int64_t kg = 0;
+      int i = 0;
+      for (int64_t t = blockIdx.x; t < a.ntiles; t += G, ++i) {
+        const int b = i & 1;
+        mbar_wait(smem_u32(&h.tinfo_full[b]), (uint32_t)((i >> 1) & 1), a.status);
+        const int nst = *(volatile int*)&h.tinfo_nst[b];
+        if (i >= 2) mbar_wait(smem_u32(&h.acc_empty[b]), (uint32_t)(((i >> 1) - 1) & 1), a.status);
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)b * acc_cols;
+        for (int k = 0; k < nst; ++k, ++kg) {
+          const int sb = (int)(kg % S);
+          mbar_wait(smem_u32(&h.full[sb]), (uint32_t)((kg / S) & 1), a.status);
+          tc_fence_after();
+          const uint32_t sA = smem_u32(sbase + (size_t)sb * a.stage_bytes);
+          const uint32_t sB = sA + kATileBytes;
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        umma_bf16(tmem, sdesc_sw128(sA + kk * 32), sdesc_sw128(sB + kk * 32), idesc, (k | kk) ? 1u : 0u);
-      umma_commit(smem_u32(&h.empty[sb]));
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(d, sdesc_sw128(sA + kk * 32), sdesc_sw128(sB + kk * 32), idesc, (k | kk) ? 1u : 0u);
+          umma_commit(smem_u32(&h.empty[sb]));
+        }
+        if (nst > 0) umma_commit(smem_u32(&h.acc_full[b]));
+        else mbar_arrive(smem_u32(&h.acc_full[b]));
+      }
     }
-    if (nst > 0) umma_commit(smem_u32(&h.done));
-  }
-  if (warp == kProducerWarps) __syncwarp();
-
-  // ---------------- epilogue: TMEM -> registers -> bf16 -> global
-  if (warp < kProducerWarps) {
-    const int64_t q = t * kRows + tid;
-    if (nst > 0) {
-      mbar_wait(smem_u32(&h.done), 0u, a.status);
+    __syncwarp();
+  } else {
+    // ---------------- epilogue: TMEM -> registers -> global (row per thread)
+    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+    const int m = quarter * 32 + lane;
+    int i = 0;
+    for (int64_t t = blockIdx.x; t < a.ntiles; t += G, ++i) {
+      const int b = i & 1;
+      mbar_wait(smem_u32(&h.acc_full[b]), (uint32_t)((i >> 1) & 1), a.status);
       tc_fence_after();
-    }
-    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-    for (int c = 0; c < a.cout; c += 16) {
-      uint32_t r[16];
-      if (nst > 0) {
-        tmem_ld16(trow + (uint32_t)c, r);
-      } else {
+      const int nst = *(volatile int*)&h.tinfo_nst[b];
+      const int64_t q = t * kRows + m;
+      const uint32_t trow = tmem + (uint32_t)b * acc_cols + ((uint32_t)(quarter * 32) << 16);
+      for (int c = 0; c < a.cout; c += 16) {
+        uint32_t r[16];
+        if (nst > 0) {
+          tmem_ld16(trow + (uint32_t)c, r);
+        } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) r[i] = 0u;
+          for (int v = 0; v < 16; ++v) r[v] = 0u;
+        }
+        if (q < a.n_out && a.out_bf16) {
+          uint4 v0, v1;
+          v0.x = pack_bf16x2(__uint_as_float(r[0]), __uint_as_float(r[1]));
+          v0.y = pack_bf16x2(__uint_as_float(r[2]), __uint_as_float(r[3]));
+          v0.z = pack_bf16x2(__uint_as_float(r[4]), __uint_as_float(r[5]));
+          v0.w = pack_bf16x2(__uint_as_float(r[6]), __uint_as_float(r[7]));
+          v1.x = pack_bf16x2(__uint_as_float(r[8]), __uint_as_float(r[9]));
+          v1.y = pack_bf16x2(__uint_as_float(r[10]), __uint_as_float(r[11]));
+          v1.z = pack_bf16x2(__uint_as_float(r[12]), __uint_as_float(r[13]));
+          v1.w = pack_bf16x2(__uint_as_float(r[14]), __uint_as_float(r[15]));
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.y) + q * a.cout + c);
+          dst[0] = v0;
+          dst[1] = v1;
+        } else if (q < a.n_out) {
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<float*>(a.y) + q * a.cout + c);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) dst[v] = make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+        }
       }
-      if (q < a.n_out) {
-        uint4 v0, v1;
-        v0.x = pack_bf16x2(__uint_as_float(r[0]), __uint_as_float(r[1]));
-        v0.y = pack_bf16x2(__uint_as_float(r[2]), __uint_as_float(r[3]));
-        v0.z = pack_bf16x2(__uint_as_float(r[4]), __uint_as_float(r[5]));
-        v0.w = pack_bf16x2(__uint_as_float(r[6]), __uint_as_float(r[7]));
-        v1.x = pack_bf16x2(__uint_as_float(r[8]), __uint_as_float(r[9]));
-        v1.y = pack_bf16x2(__uint_as_float(r[10]), __uint_as_float(r[11]));
-        v1.z = pack_bf16x2(__uint_as_float(r[12]), __uint_as_float(r[13]));
-        v1.w = pack_bf16x2(__uint_as_float(r[14]), __uint_as_float(r[15]));
-        uint4* dst = reinterpret_cast<uint4*>(a.y + q * a.cout + c);
-        dst[0] = v0;
-        dst[1] = v1;
-      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&h.acc_empty[b]));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&h.tinfo_empty[b]));
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == kProducerWarps) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(a.tmem_cols) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * acc_cols) : "memory");
   }
 }
 
@@ -447,7 +566,7 @@ extern "C" fvx_status fvx_sparse_conv(fvx_grid gin, fvx_grid gout, fvx_kmap m, f
     }
     return check_launch("conv_f32");
   }
-  if (dt != FVX_BF16) {
+  if (dt != FVX_BF16 && dt != FVX_BF16_OUT_BF16) {
     set_error("fvx_sparse_conv: unknown dtype %d", (int)dt);
     return FVX_ERR_INVALID_ARG;
   }
@@ -481,29 +600,35 @@ extern "C" fvx_status fvx_sparse_conv(fvx_grid gin, fvx_grid gout, fvx_kmap m, f
   a.mask = m->out_mask;
   a.in_idx = m->in_idx;
   a.tile_start = m->tile_start;
-  a.y = (__nv_bfloat16*)out;
+  a.y = out;
+  a.out_bf16 = (dt == FVX_BF16_OUT_BF16) ? 1 : 0;
   a.status = status;
   a.ntiles = nt;
   a.n_out = m->n_out;
   a.cin = (int)cin;
   a.cout = (int)cout;
-  a.b_bytes = (int)cout * 128;
-  a.stage_bytes = kATileBytes + a.b_bytes;  // multiple of 1024 since cout % 8 == 0
-  const int budget = 200 * 1024 - (int)sizeof(ConvSmemHead);
-  a.stages = budget / a.stage_bytes;
+  a.stage_bytes = kATileBytes + (int)cout * 128;  // multiple of 1024 since cout % 8 == 0
+  // Stage ring (persistent across the CTA's tiles): as deep as shared memory
+  // allows, up to 8; one CTA per SM.
+  const int head = (int)sizeof(ConvSmemHead) + 1024;
+  a.stages = (224 * 1024 - head) / a.stage_bytes;
   if (a.stages > 8) a.stages = 8;
   if (a.stages < kLag + 1) {
-    set_error("fvx_sparse_conv: cout %lld leaves too few pipeline stages", (long long)cout);
+    set_error("fvx_sparse_conv: cout %lld leaves fewer than %d pipeline stages", (long long)cout, kLag + 1);
     return FVX_ERR_INVALID_ARG;
   }
   int cols = 32;
   while (cols < cout) cols <<= 1;
-  a.tmem_cols = cols;
+  a.tmem_cols = cols;  // per accumulator; two accumulators per CTA (<= 512 columns)
   const size_t smem = 1024 + (size_t)a.stages * a.stage_bytes + sizeof(ConvSmemHead);
   FVX_CUDA(cudaFuncSetAttribute(k_conv_bf16_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  int dev = 0, sms = 0;
+  FVX_CUDA(cudaGetDevice(&dev));
+  FVX_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  const int64_t grid = std::min<int64_t>(nt, (int64_t)sms);
   {
     LaunchScope ls("conv_bf16_tc", s);
-    k_conv_bf16_tc<<<(unsigned)nt, kConvThreads, smem, s>>>(a);
+    k_conv_bf16_tc<<<(unsigned)grid, kConvThreads, smem, s>>>(a);
   }
   return check_launch("conv_bf16_tc");
 }

@@ -2,9 +2,10 @@
 
 Kernel map: bit-exact ("DriveRT", Shared neighbour maps).  Conv: within
 2e-3 * sum|w*x| per output element for bf16 (bf16-rounded inputs, fp32
-accumulation, bf16 output) and 1e-5 * sum|w*x| for fp32 ("fVDB: A Deep-Learning
-Framework for Sparse, Large Scale, and High Performance Spatial Intelligence"
-notes, Sparse-convolution operators)."""
+accumulation, fp32 output; a bf16 output adds one 2^-8 |y| rounding) and
+1e-5 * sum|w*x| for fp32 ("fVDB: A Deep-Learning Framework for Sparse, Large
+Scale, and High Performance Spatial Intelligence" notes, Sparse-convolution
+operators)."""
 import numpy as np
 import pytest
 
@@ -103,6 +104,25 @@ def test_conv_bf16_matches_oracle(cuda_device, grids, stride, cin, cout):
     G.assert_conv_close(G.np_(y.float()), yo, ao, G.BF16_TOL)
 
 
+@pytest.mark.parametrize("cin,cout", [(8, 16), (64, 64), (128, 256)])
+@pytest.mark.parametrize("stride", [1, 2])
+def test_conv_bf16_out_bf16_matches_oracle(cuda_device, grids, stride, cin, cout):
+    """bf16-rounded output: the stated bound plus one bf16 rounding of y."""
+    import torch
+
+    import sparse_convolution_gb300 as fvx
+
+    gin, gout, km, okm = _maps(grids, stride)
+    x, W = G.bf16_inputs(19, gin.n_active, cin, cout)
+    y = fvx.sparse_conv(gin, gout, km, x, W, out_dtype=torch.bfloat16)
+    assert y.dtype == torch.bfloat16
+    yo, ao = oracle.conv(okm, G.as_f64(x), G.as_f64(W))
+    G.assert_conv_close(G.np_(y.float()), yo, ao, G.BF16_TOL, rel_y=G.BF16_OUT_REL)
+    # and it is the fp32-output result rounded to nearest bf16
+    y32 = fvx.sparse_conv(gin, gout, km, x, W)
+    assert torch.equal(y, y32.bfloat16())
+
+
 def test_conv_bf16_identity_is_exact(cuda_device, grids):
     """W[13] = I, other offsets 0: out == feats bit for bit."""
     import torch
@@ -115,7 +135,8 @@ def test_conv_bf16_identity_is_exact(cuda_device, grids):
     W = torch.zeros((27, 64, 64), dtype=torch.bfloat16, device="cuda")
     W[13] = torch.eye(64, dtype=torch.bfloat16, device="cuda")
     y = fvx.sparse_conv(g, g, km, x, W)
-    assert torch.equal(y, x)
+    assert torch.equal(y, x.float())
+    assert torch.equal(fvx.sparse_conv(g, g, km, x, W, out_dtype=torch.bfloat16), x)
 
 
 def test_conv_bf16_repeatable(cuda_device, grids):

@@ -56,7 +56,12 @@ def _oracle_parity(w, conv_rows=None):
             rows = np.random.default_rng(i).choice(gout.n_active, size=min(conv_rows, gout.n_active), replace=False)
             yo, ao = oracle.conv_rows(og, ogout, stride, rows, G.as_f64(x), G.as_f64(W))
             G.assert_conv_close(G.np_(y.float())[rows], yo, ao, tol)
-        x = y  # the next conv reads this one's output (LiDAR: subm 128 -> stride-2 128->256)
+        if w["dtype"] != "f32":
+            # the next conv reads this one's bf16-rounded output (LiDAR: subm 128 -> stride-2 128->256)
+            yb = fvx.sparse_conv(g, gout, km, x, W, out_dtype=torch.bfloat16)
+            assert torch.equal(yb, y.bfloat16())
+            y = yb
+        x = y
         if stride != 1:
             break
 
@@ -121,6 +126,8 @@ def _full_size(w, n_kmap_rows=100_000, n_conv_rows=3000):
         yr, ar = G.conv_rows_independent(nbr, G.as_f64(x), G.as_f64(W))
         tol = G.F32_TOL if w["dtype"] == "f32" else G.BF16_TOL
         G.assert_conv_close(G.np_(y.float())[crow], yr, ar, tol)
+        if w["dtype"] != "f32":
+            y = fvx.sparse_conv(g, gout, km, x, W, out_dtype=torch.bfloat16)
         x = y
         if stride != 1:
             break
