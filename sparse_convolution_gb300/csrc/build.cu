@@ -116,7 +116,30 @@ __global__ void __launch_bounds__(kThreads) k_plan_reduce(const int32_t* __restr
     o_or |= __shfl_xor_sync(0xffffffffu, o_or, d);
     o_and &= __shfl_xor_sync(0xffffffffu, o_and, d);
   }
-  if ((threadIdx.x & 31) == 0) {
+  // block reduction, then one set of atomics per block
+  __shared__ int s_min[3][kThreads / 32], s_max[3][kThreads / 32];
+  __shared__ unsigned long long s_or[kThreads / 32], s_and[kThreads / 32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+      s_min[a][warp] = tmin[a];
+      s_max[a][warp] = tmax[a];
+    }
+    s_or[warp] = o_or;
+    s_and[warp] = o_and;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kThreads / 32; ++w) {
+#pragma unroll
+      for (int a = 0; a < 3; ++a) {
+        tmin[a] = min(tmin[a], s_min[a][w]);
+        tmax[a] = max(tmax[a], s_max[a][w]);
+      }
+      o_or |= s_or[w];
+      o_and &= s_and[w];
+    }
 #pragma unroll
     for (int a = 0; a < 3; ++a) {
       atomicMin(&plan->tmin[a], tmin[a]);
@@ -266,6 +289,8 @@ struct BuildOut {
   int32_t* upper_origin;
   int32_t* upper_batch;
   int4* upper_tile;
+  uint64_t* lower_mask;
+  uint64_t* upper_mask;
 };
 
 __global__ void __launch_bounds__(kThreads) k_count_down(const uint64_t* __restrict__ key,
@@ -314,12 +339,18 @@ __global__ void __launch_bounds__(kThreads) k_count_down(const uint64_t* __restr
       o.leaf_origin[3 * (int64_t)leaf + 2] = ck & ~7;
       o.leaf_batch[leaf] = t.x;
     }
+    if (f & 2u) {  // the new leaf is a child of its lower node (masks zeroed before)
+      const int nb = (((ci >> 3) & 15) << 8) | (((cj >> 3) & 15) << 4) | ((ck >> 3) & 15);
+      atomicOr(reinterpret_cast<unsigned long long*>(o.lower_mask) + (int64_t)lower * 64 + (nb >> 6), 1ull << (nb & 63));
+    }
     if (f & 4u) {
       o.lower_first[lower] = leaf;
       o.lower_origin[3 * (int64_t)lower] = ci & ~127;
       o.lower_origin[3 * (int64_t)lower + 1] = cj & ~127;
       o.lower_origin[3 * (int64_t)lower + 2] = ck & ~127;
       o.lower_batch[lower] = t.x;
+      const int nb = (((ci >> 7) & 31) << 10) | (((cj >> 7) & 31) << 5) | ((ck >> 7) & 31);
+      atomicOr(reinterpret_cast<unsigned long long*>(o.upper_mask) + (int64_t)upper * 512 + (nb >> 6), 1ull << (nb & 63));
     }
     if (f & 8u) {
       o.upper_first[upper] = lower;
@@ -371,63 +402,28 @@ __global__ void __launch_bounds__(kThreads) k_leaf_register(const int32_t* __res
   if (lane < 10) rec[l * 10 + lane] = v;
 }
 
-// One warp per lower node: 4096-bit child mask (64 words) and prefix counts.
-__global__ void __launch_bounds__(kThreads) k_lower_register(const int32_t* __restrict__ leaf_origin,
-                                                             const uint32_t* __restrict__ lower_first,
-                                                             int64_t n_lower, int64_t n_leaf,
-                                                             uint64_t* __restrict__ mask,
-                                                             uint32_t* __restrict__ prefix) {
-  __shared__ unsigned long long sm[kThreads / 32][64];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t w = (int64_t)blockIdx.x * (kThreads / 32) + warp;
-  sm[warp][lane] = 0ull;
-  sm[warp][lane + 32] = 0ull;
-  __syncwarp();
-  if (w < n_lower) {
-    const uint32_t first = lower_first[w];
-    const uint32_t end = (w + 1 < n_lower) ? lower_first[w + 1] : (uint32_t)n_leaf;
-    for (uint32_t t = first + lane; t < end; t += 32) {
-      const int i = leaf_origin[3 * (int64_t)t], j = leaf_origin[3 * (int64_t)t + 1], k = leaf_origin[3 * (int64_t)t + 2];
-      const int nb = (((i >> 3) & 15) << 8) | (((j >> 3) & 15) << 4) | ((k >> 3) & 15);
-      atomicOr(&sm[warp][nb >> 6], 1ull << (nb & 63));
-    }
-  }
-  __syncwarp();
+// Per-word exclusive popcount prefix of the lower-node child masks (one warp
+// per node, 64 words); the masks themselves are set in k_count_down.
+__global__ void __launch_bounds__(kThreads) k_lower_prefix(const uint64_t* __restrict__ mask, int64_t n_lower,
+                                                           uint32_t* __restrict__ prefix) {
+  const int lane = threadIdx.x & 31;
+  const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (w >= n_lower) return;
-  const uint64_t a = sm[warp][2 * lane], b = sm[warp][2 * lane + 1];
-  const uint32_t pa = __popcll(a), pb = __popcll(b);
+  const unsigned long long* m = reinterpret_cast<const unsigned long long*>(mask) + w * 64;
+  const uint32_t pa = __popcll(m[2 * lane]), pb = __popcll(m[2 * lane + 1]);
   const uint32_t ex = warp_inclusive_scan<uint32_t>(pa + pb) - (pa + pb);
-  mask[w * 64 + 2 * lane] = a;
-  mask[w * 64 + 2 * lane + 1] = b;
   prefix[w * 64 + 2 * lane] = ex;
   prefix[w * 64 + 2 * lane + 1] = ex + pa;
 }
 
-// One block per upper node: 32768-bit child mask (512 words) and prefix counts.
-__global__ void __launch_bounds__(kThreads) k_upper_register(const int32_t* __restrict__ lower_origin,
-                                                             const uint32_t* __restrict__ upper_first,
-                                                             int64_t n_upper, int64_t n_lower,
-                                                             uint64_t* __restrict__ mask,
-                                                             uint32_t* __restrict__ prefix) {
-  __shared__ unsigned long long sm[512];
+// Same for the upper-node masks (one block per node, 512 words).
+__global__ void __launch_bounds__(kThreads) k_upper_prefix(const uint64_t* __restrict__ mask,
+                                                           uint32_t* __restrict__ prefix) {
   __shared__ uint32_t tmp[33];
   const int64_t u = blockIdx.x;
-  sm[threadIdx.x] = 0ull;
-  sm[threadIdx.x + 256] = 0ull;
-  __syncthreads();
-  const uint32_t first = upper_first[u];
-  const uint32_t end = (u + 1 < n_upper) ? upper_first[u + 1] : (uint32_t)n_lower;
-  for (uint32_t t = first + threadIdx.x; t < end; t += blockDim.x) {
-    const int i = lower_origin[3 * (int64_t)t], j = lower_origin[3 * (int64_t)t + 1], k = lower_origin[3 * (int64_t)t + 2];
-    const int nb = (((i >> 7) & 31) << 10) | (((j >> 7) & 31) << 5) | ((k >> 7) & 31);
-    atomicOr(&sm[nb >> 6], 1ull << (nb & 63));
-  }
-  __syncthreads();
-  const uint64_t a = sm[2 * threadIdx.x], b = sm[2 * threadIdx.x + 1];
-  const uint32_t pa = __popcll(a), pb = __popcll(b);
+  const unsigned long long* m = reinterpret_cast<const unsigned long long*>(mask) + u * 512;
+  const uint32_t pa = __popcll(m[2 * threadIdx.x]), pb = __popcll(m[2 * threadIdx.x + 1]);
   const uint32_t ex = block_exclusive_scan<uint32_t>(pa + pb, tmp, (uint32_t*)nullptr);
-  mask[u * 512 + 2 * threadIdx.x] = a;
-  mask[u * 512 + 2 * threadIdx.x + 1] = b;
   prefix[u * 512 + 2 * threadIdx.x] = ex;
   prefix[u * 512 + 2 * threadIdx.x + 1] = ex + pa;
 }
@@ -518,7 +514,7 @@ fvx_status build_grid_device(const int32_t* coords, int64_t n, const int64_t* of
     FVX_TRY(check_launch("build_plan_init"));
     {
       LaunchScope ls("build_plan_reduce", s);
-      unsigned nb = std::min<unsigned>(grid_for(n, kThreads), 152u * 8u);
+      unsigned nb = std::min<unsigned>(grid_for(n, kThreads), 152u * 2u);
       k_plan_reduce<<<nb, kThreads, 0, s>>>(coords, n, plan);
     }
     FVX_TRY(check_launch("build_plan_reduce"));
@@ -589,7 +585,7 @@ fvx_status build_grid_device(const int32_t* coords, int64_t n, const int64_t* of
       }
       FVX_TRY(check_launch("build_key1"));
       bool in1 = false;
-      FVX_TRY(radix_sort_pairs(ka, va, kb, vb, n, 0, width1, s, &in1));
+      FVX_TRY(radix_sort_pairs(ka, va, kb, vb, n, 0, width1, s, &in1, scr));
       uint64_t* k1 = in1 ? kb : ka;
       uint32_t* v1 = in1 ? vb : va;
       uint64_t* k2 = in1 ? ka : kb;  // the other key buffer receives key2
@@ -601,7 +597,7 @@ fvx_status build_grid_device(const int32_t* coords, int64_t n, const int64_t* of
         k_rle_count<<<(unsigned)nt, kThreads, 0, s>>>(k1, n, partial);
       }
       FVX_TRY(check_launch("build_rle_count"));
-      FVX_TRY(scan_exclusive_u32(partial, partial, nt, nullptr, s));
+      FVX_TRY(scan_exclusive_u32(partial, partial, nt, nullptr, s, scr));
       {
         LaunchScope ls("build_rle_key2", s);
         k_rle_key2<<<(unsigned)nt, kThreads, 0, s>>>(k1, n, v1, coords, partial, L, vbits, runs, k2, run_tile);
@@ -619,7 +615,7 @@ fvx_status build_grid_device(const int32_t* coords, int64_t n, const int64_t* of
     // ---- step 6: sort by key2 (run id above the compacted offsets)
     {
       bool in1 = false;
-      FVX_TRY(radix_sort_pairs(ka, va, kb, vb, n, 0, runbits + vbits, s, &in1));
+      FVX_TRY(radix_sort_pairs(ka, va, kb, vb, n, 0, runbits + vbits, s, &in1, scr));
       if (in1) {
         ka = kb;
         va = vb;
@@ -635,7 +631,7 @@ fvx_status build_grid_device(const int32_t* coords, int64_t n, const int64_t* of
       k_count_tiles<<<(unsigned)ntiles, kThreads, 0, s>>>(ka, n, sh, scanned, ntiles);
     }
     FVX_TRY(check_launch("build_count_tiles"));
-    FVX_TRY(scan_exclusive_u32(scanned, scanned, 4 * ntiles, dcounts + 4, s));
+    FVX_TRY(scan_exclusive_u32(scanned, scanned, 4 * ntiles, dcounts + 4, s, scr));
     {
       LaunchScope ls("build_gather_counts", s);
       k_gather_counts<<<1, 32, 0, s>>>(scanned, ntiles, dcounts + 4, dcounts);
@@ -692,32 +688,32 @@ fvx_status build_grid_device(const int32_t* coords, int64_t n, const int64_t* of
     uint32_t* leaf_first_voxel = scr.get<uint32_t>((size_t)Lf);
     uint32_t* upper_first_voxel = scr.get<uint32_t>((size_t)NU);
     if (!leaf_first_voxel || !upper_first_voxel) return FVX_ERR_ALLOC;
-    BuildOut o{g->ijk,        g->row_to_index,   leaf_first_voxel, g->leaf_origin,  g->leaf_batch,
-               g->lower_first, g->lower_origin,  g->lower_batch,   g->upper_first,  upper_first_voxel,
-               g->upper_origin, g->upper_batch, (int4*)g->upper_tile};
+    BuildOut o{g->ijk,          g->row_to_index, leaf_first_voxel, g->leaf_origin,  g->leaf_batch,
+               g->lower_first,  g->lower_origin, g->lower_batch,   g->upper_first,  upper_first_voxel,
+               g->upper_origin, g->upper_batch,  (int4*)g->upper_tile, g->lower_mask, g->upper_mask};
+    FVX_CUDA(cudaMemsetAsync(g->lower_mask, 0, 512 * (size_t)NL, s));
+    FVX_CUDA(cudaMemsetAsync(g->upper_mask, 0, 4096 * (size_t)NU, s));
     {
       LaunchScope ls("build_count_down", s);
       k_count_down<<<(unsigned)ntiles, kThreads, 0, s>>>(ka, va, n, sh, scanned, ntiles, runs, dec, run_tile, o);
     }
     FVX_TRY(check_launch("build_count_down"));
-    // ---- steps 11-12: masks and prefix counts, leaves up to the root
+    // ---- steps 11-12: leaf masks and prefix counts at every level
     {
       LaunchScope ls("build_leaf_register", s);
       k_leaf_register<<<grid_for(Lf * 32, kThreads), kThreads, 0, s>>>(g->ijk, leaf_first_voxel, Lf, U, g->leaf_rec);
     }
     FVX_TRY(check_launch("build_leaf_register"));
     {
-      LaunchScope ls("build_lower_register", s);
-      k_lower_register<<<grid_for(NL * 32, kThreads), kThreads, 0, s>>>(g->leaf_origin, g->lower_first, NL, Lf,
-                                                                         g->lower_mask, g->lower_prefix);
+      LaunchScope ls("build_lower_prefix", s);
+      k_lower_prefix<<<grid_for(NL * 32, kThreads), kThreads, 0, s>>>(g->lower_mask, NL, g->lower_prefix);
     }
-    FVX_TRY(check_launch("build_lower_register"));
+    FVX_TRY(check_launch("build_lower_prefix"));
     {
-      LaunchScope ls("build_upper_register", s);
-      k_upper_register<<<(unsigned)NU, kThreads, 0, s>>>(g->lower_origin, g->upper_first, NU, NL, g->upper_mask,
-                                                         g->upper_prefix);
+      LaunchScope ls("build_upper_prefix", s);
+      k_upper_prefix<<<(unsigned)NU, kThreads, 0, s>>>(g->upper_mask, g->upper_prefix);
     }
-    FVX_TRY(check_launch("build_upper_register"));
+    FVX_TRY(check_launch("build_upper_prefix"));
     {
       LaunchScope ls("build_batch_offsets", s);
       k_batch_offsets<<<1, 256, 0, s>>>((const int4*)g->upper_tile, upper_first_voxel, NU, U, B,

@@ -17,12 +17,13 @@
 //
 // Two kernels, one per dtype (no dispatch between backends):
 //   * bf16: persistent and warp-specialized.  Producers build each tile's row
-//     table (software-pipelined one tile ahead) and gather A (feature rows)
-//     and B (weight rows) with cp.async into 128B-swizzled K-major stages;
-//     one thread issues tcgen05.mma kind::f16 (bf16 x bf16 -> fp32 in TMEM);
-//     epilogue warps drain a double-buffered TMEM accumulator with tcgen05.ld
-//     while the next tile accumulates.  Output fp32, or bf16 rounded to nearest
-//     even.
+//     table (software-pipelined one tile ahead) and gather A (feature rows,
+//     16-byte pieces) with cp.async into 128B-swizzled K-major stages; the
+//     weights are either resident in shared memory for the whole kernel (when
+//     27*cin*cout*2 bytes fit in 64 KB) or gathered per stage.  One thread
+//     issues tcgen05.mma kind::f16 (bf16 x bf16 -> fp32 in TMEM); epilogue
+//     warps drain a double-buffered TMEM accumulator with tcgen05.ld while the
+//     next tile accumulates.  Output fp32, or bf16 rounded to nearest even.
 //   * fp32: exact FFMA on CUDA cores (no TF32).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -127,13 +128,15 @@ __global__ void __launch_bounds__(kRows) k_conv_f32(const float* __restrict__ x,
 
 // ============================================================== bf16 tcgen05
 // Warp roles of the persistent bf16 kernel: warps 0-3 build each tile's row
-// table and gather A/B into the stage ring, warp 4 issues the MMAs (and owns
+// table and gather into the stage ring, warp 4 issues the MMAs (and owns
 // TMEM), warps 5-8 drain the double-buffered TMEM accumulator to global.
 constexpr int kProducerWarps = 4;
 constexpr int kMmaWarp = kProducerWarps;
 constexpr int kConvThreads = (kProducerWarps + 1 + 4) * 32;
-constexpr int kLag = 2;                                // cp.async groups kept in flight per producer
+constexpr int kMaxStages = 12;
+constexpr int kInfoRing = 4;                           // tiles whose info can be in flight
 constexpr int kATileBytes = kRows * 128;               // 128 rows x 64 bf16 (one 128B swizzle atom wide)
+constexpr int kResidentWBytes = 64 * 1024;             // weights kept in shared memory up to this size
 constexpr unsigned long long kWaitNs = 2000000000ull;  // bounded mbarrier waits: 2 s
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -181,18 +184,36 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+// cp.async.wait_group takes an immediate: at most n groups of this thread left pending.
+__device__ __forceinline__ void cp_async_wait_n(int n) {
+  switch (n) {
+    case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+    case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+    case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+    case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+    case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
+    case 5: asm volatile("cp.async.wait_group 5;" ::: "memory"); break;
+    case 6: asm volatile("cp.async.wait_group 6;" ::: "memory"); break;
+    case 7: asm volatile("cp.async.wait_group 7;" ::: "memory"); break;
+    case 8: asm volatile("cp.async.wait_group 8;" ::: "memory"); break;
+    case 9: asm volatile("cp.async.wait_group 9;" ::: "memory"); break;
+    default: asm volatile("cp.async.wait_group 10;" ::: "memory"); break;
+  }
 }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void producer_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-// UMMA shared-memory descriptor: K-major, 128-byte swizzle, 8-row groups
-// 1024 bytes apart (SBO), leading offset unused for this layout.
+// UMMA shared-memory descriptors (K-major).  128-byte swizzle: 8-row groups
+// 1024 bytes apart (SBO), leading offset unused.  No swizzle: 8 x 16-byte core
+// matrices, LBO = bytes between the two K-adjacent core matrices of one MMA,
+// SBO = bytes between N-adjacent core matrices.
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+__device__ __forceinline__ uint64_t sdesc_plain(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46);
 }
 
 // Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major.
@@ -240,12 +261,19 @@ struct TileTable {
   uint32_t tstart[27];      // the tile's first pair in each list
 };
 
+// What the MMA thread and the epilogue need to know about a tile.
+struct TileInfo {
+  int nst;         // pipeline stages (0: no pairs, the output rows are zero)
+  int npieces;     // real 16-byte pieces per row (offsets present x cin/8)
+  int slot_s[27];  // offsets present (for the resident-weight B descriptors)
+};
+
 struct ConvSmemHead {
   TileTable tab[2];
-  unsigned long long full[8], empty[8];              // stage ring: producers <-> MMA
-  unsigned long long tinfo_full[2], tinfo_empty[2];  // per-tile stage count: producers -> MMA, epilogue
-  unsigned long long acc_full[2], acc_empty[2];      // TMEM accumulators: MMA <-> epilogue
-  int tinfo_nst[2];
+  TileInfo info[kInfoRing];
+  unsigned long long full[kMaxStages], empty[kMaxStages];        // stage ring: producers <-> MMA
+  unsigned long long tinfo_full[kInfoRing], tinfo_empty[kInfoRing];  // tile info: producers -> MMA, epilogue
+  unsigned long long acc_full[2], acc_empty[2];                  // TMEM accumulators: MMA <-> epilogue
   uint32_t tmem_base;
 };
 
@@ -258,7 +286,9 @@ struct ConvArgs {
   void* y;                  // fp32 or bf16 [n_out][cout]
   uint32_t* status;
   int64_t ntiles, n_out;
-  int cin, cout, stages, stage_bytes, tmem_cols, out_bf16;
+  int cin, cout, stages, lag, stage_bytes, tmem_cols, out_bf16;
+  int w_resident;           // weights live in shared memory (no per-stage B tile)
+  int w_bytes;              // resident weight region incl. one zero block (multiple of 1024)
 };
 
 // Producer helpers ----------------------------------------------------------
@@ -293,10 +323,24 @@ __device__ __forceinline__ void store_rows(TileTable& tab, uint32_t tor, const i
   }
 }
 
+// Publishes a tile's info for the MMA thread and the epilogue (thread 0 of
+// the producers).
+__device__ __forceinline__ void publish_info(ConvSmemHead& h, const ConvArgs& a, int j, uint32_t tor, int npieces) {
+  const int r = j & (kInfoRing - 1);
+  if (j >= kInfoRing) mbar_wait(smem_u32(&h.tinfo_empty[r]), (uint32_t)(((j / kInfoRing) - 1) & 1), a.status);
+  h.info[r].nst = (npieces + 7) >> 3;
+  h.info[r].npieces = npieces;
+  int slot = 0;
+  for (int s = 0; s < 27; ++s)
+    if ((tor >> s) & 1u) h.info[r].slot_s[slot++] = s;
+  mbar_arrive(smem_u32(&h.tinfo_full[r]));
+}
+
 __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tc(const __grid_constant__ ConvArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  // stage buffers first (1024-aligned), head after them
-  unsigned char* sbase = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  // [resident weights][stage ring][head], each 1024-aligned
+  unsigned char* wbase = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  unsigned char* sbase = wbase + a.w_bytes;
   ConvSmemHead& h = *reinterpret_cast<ConvSmemHead*>(sbase + (size_t)a.stages * a.stage_bytes);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = a.stages;
@@ -310,9 +354,11 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tc(const __grid_c
       mbar_init(smem_u32(&h.full[i]), kProducerWarps * 32);
       mbar_init(smem_u32(&h.empty[i]), 1);
     }
+    for (int r = 0; r < kInfoRing; ++r) {
+      mbar_init(smem_u32(&h.tinfo_full[r]), 1);
+      mbar_init(smem_u32(&h.tinfo_empty[r]), 4);  // one arrival per epilogue warp
+    }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&h.tinfo_full[b]), 1);
-      mbar_init(smem_u32(&h.tinfo_empty[b]), 4);  // one arrival per epilogue warp
       mbar_init(smem_u32(&h.acc_full[b]), 1);
       mbar_init(smem_u32(&h.acc_empty[b]), 128);
     }
@@ -332,23 +378,40 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tc(const __grid_c
   if (warp < kProducerWarps) {
     // ---------------- producers
     const int m = tid;
+    const int L = a.lag;
     int64_t kg = 0, signaled = 0;  // stage counters, continuing across tiles
+    int64_t kg_end[kInfoRing] = {0, 0, 0, 0};
+    if (a.w_resident) {
+      // resident weights: block (s, piece c) = cout rows x 16 bytes; one zero
+      // block after the 27 * ppo real ones (the B of padded pieces)
+      const uint32_t wdst = smem_u32(wbase);
+      const int nblk = 27 * ppo;
+      for (int e = m; e < (nblk + 1) * a.cout; e += kProducerWarps * 32) {
+        const int blk = e / a.cout, n = e - blk * a.cout;
+        const void* src = a.wt;
+        uint32_t bytes = 0;
+        if (blk < nblk) {
+          const int s = blk / ppo, c = blk - s * ppo;
+          src = a.wt + ((int64_t)s * a.cout + n) * a.cin + c * 8;
+          bytes = 16;
+        }
+        cp_async16(wdst + (uint32_t)e * 16u, src, bytes);
+      }
+      cp_async_commit();  // completes before the first stage is signaled
+    }
     int ps[27];
     // tables of the first tile (exposed once), masks of the second prefetched
     int64_t t = blockIdx.x;
-    uint32_t mk_cur = load_mask(a, t, m), ts_cur = load_tstart(a, t, m);
+    const uint32_t mk0 = load_mask(a, t, m), ts0 = load_tstart(a, t, m);
     uint32_t mk_nxt = load_mask(a, t + G, m), ts_nxt = load_tstart(a, t + G, m);
-    if (m < 27) h.tab[0].tstart[m] = ts_cur;
-    tile_ballots(h.tab[0].tm, mk_cur);
+    if (m < 27) h.tab[0].tstart[m] = ts0;
+    tile_ballots(h.tab[0].tm, mk0);
     producer_bar();
     uint32_t tor = tile_or(h.tab[0].tm);
-    issue_row_loads(h.tab[0], a.in_idx, mk_cur, ps);
+    issue_row_loads(h.tab[0], a.in_idx, mk0, ps);
     store_rows(h.tab[0], tor, ps);
     int total = __popc(tor) * ppo;
-    if (m == 0 && t < a.ntiles) {
-      h.tinfo_nst[0] = (total + 7) >> 3;
-      mbar_arrive(smem_u32(&h.tinfo_full[0]));
-    }
+    if (m == 0 && t < a.ntiles) publish_info(h, a, 0, tor, total);
     producer_bar();
     for (int i = 0; t < a.ntiles; t += G, ++i) {
       const int b = i & 1, nb = b ^ 1;
@@ -364,80 +427,78 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tc(const __grid_c
         tor_n = tile_or(nxt.tm);
         issue_row_loads(nxt, a.in_idx, mk_nxt, ps);
       }
-      const uint32_t mk_n = mk_nxt;
       // (b) prefetch the masks of the tile after next
       mk_nxt = load_mask(a, t + 2 * G, m);
       ts_nxt = load_tstart(a, t + 2 * G, m);
-      // (c) gathers of this tile
-      const int64_t kg_tile0 = kg;       // first stage of this tile
-      const int nst = (total + 7) >> 3;  // stages of 8 pieces (K = 64)
+      // (c) gathers of this tile: 8 pieces (K = 64) per stage
+      const int nst = (total + 7) >> 3;
+      int slot = 0, cb = 0, g = 0;  // running piece -> (offset slot, channel block)
       for (int k = 0; k < nst; ++k, ++kg) {
         const int sb = (int)(kg % S);
         if (kg >= S) mbar_wait(smem_u32(&h.empty[sb]), (uint32_t)((kg / S - 1) & 1), a.status);
         const uint32_t sA = smem_u32(sbase + (size_t)sb * a.stage_bytes);
-        const uint32_t sB = sA + kATileBytes;
+        int64_t boff[8];  // per piece: element offset of its weight row block (non-resident B)
 #pragma unroll
         for (int pc = 0; pc < 8; ++pc) {
-          const int g = 8 * k + pc;
           const void* src = a.x;
           uint32_t bytes = 0;
+          boff[pc] = -1;
           if (g < total) {
-            const int slot = g / ppo, cb = g - slot * ppo;
             const int p = cur.rowp[slot][m];
             if (p >= 0) {
               src = a.x + (int64_t)p * a.cin + cb * 8;
               bytes = 16;
             }
+            boff[pc] = (int64_t)cur.slot_s[slot] * a.cout * a.cin + cb * 8;
+            if (++cb == ppo) {
+              cb = 0;
+              ++slot;
+            }
+            ++g;
           }
           cp_async16(sA + (m >> 3) * 1024 + (m & 7) * 128 + ((pc ^ (m & 7)) << 4), src, bytes);
         }
-        for (int n = m; n < a.cout; n += kProducerWarps * 32) {
+        if (!a.w_resident) {
+          const uint32_t sB = sA + kATileBytes;
+          for (int n = m; n < a.cout; n += kProducerWarps * 32) {
 #pragma unroll
-          for (int pc = 0; pc < 8; ++pc) {
-            const int g = 8 * k + pc;
-            const void* src = a.wt;
-            uint32_t bytes = 0;
-            if (g < total) {
-              const int slot = g / ppo, cb = g - slot * ppo;
-              src = a.wt + ((int64_t)cur.slot_s[slot] * a.cout + n) * a.cin + cb * 8;
-              bytes = 16;
+            for (int pc = 0; pc < 8; ++pc) {
+              const bool real = boff[pc] >= 0;
+              cp_async16(sB + (n >> 3) * 1024 + (n & 7) * 128 + ((pc ^ (n & 7)) << 4),
+                         real ? (const void*)(a.wt + boff[pc] + (int64_t)n * a.cin) : (const void*)a.wt,
+                         real ? 16u : 0u);
             }
-            cp_async16(sB + (n >> 3) * 1024 + (n & 7) * 128 + ((pc ^ (n & 7)) << 4), src, bytes);
           }
         }
         cp_async_commit();
-        if (kg - signaled >= kLag) {
-          cp_async_wait<kLag>();
+        if (kg - signaled >= L) {
+          cp_async_wait_n(L);
           fence_proxy_async();
           mbar_arrive(smem_u32(&h.full[signaled % S]));
           ++signaled;
         }
       }
-      // (d) next tile: row table and its stage count for the MMA and epilogue.
-      // Its count slot is freed by the epilogue of the previous tile, which
-      // needs every stage of that tile signaled: flush any still held back by
-      // the lag (a short tile may not have pushed them out).
-      if (signaled < kg_tile0) {
-        cp_async_wait<0>();
-        fence_proxy_async();
-        while (signaled < kg) {
-          mbar_arrive(smem_u32(&h.full[signaled % S]));
-          ++signaled;
-        }
-      }
+      kg_end[i & (kInfoRing - 1)] = kg;
+      // (d) next tile: row table and its info.  The info slot of tile i+1 is
+      // freed by the epilogue of tile i+1-kInfoRing, which needs every stage
+      // of that tile signaled: flush stages still held back by the lag.
       if (has_next) {
+        const int j = i + 1;
+        if (j >= kInfoRing && signaled < kg_end[(j - kInfoRing) & (kInfoRing - 1)]) {
+          cp_async_wait_n(0);
+          fence_proxy_async();
+          while (signaled < kg) {
+            mbar_arrive(smem_u32(&h.full[signaled % S]));
+            ++signaled;
+          }
+        }
         store_rows(nxt, tor_n, ps);
         total = __popc(tor_n) * ppo;
-        if (m == 0) {
-          if (i + 1 >= 2) mbar_wait(smem_u32(&h.tinfo_empty[nb]), (uint32_t)((((i + 1) >> 1) - 1) & 1), a.status);
-          h.tinfo_nst[nb] = (total + 7) >> 3;
-          mbar_arrive(smem_u32(&h.tinfo_full[nb]));
-        }
+        if (m == 0) publish_info(h, a, j, tor_n, total);
       }
-      (void)mk_n;
       producer_bar();  // tables of the next tile complete; this tile's no longer read
     }
-    cp_async_wait<0>();
+    cp_async_wait_n(0);
     fence_proxy_async();
     while (signaled < kg) {
       mbar_arrive(smem_u32(&h.full[signaled % S]));
@@ -447,24 +508,51 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tc(const __grid_c
     // ---------------- MMA issue (one thread)
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16(kRows, a.cout);
+      const uint32_t wsm = smem_u32(wbase);
+      const uint32_t wblk = (uint32_t)a.cout * 16u;  // bytes per resident weight block
+      const uint32_t zero_blk = wsm + (uint32_t)(27 * ppo) * wblk;
       int64_t kg = 0;
       int i = 0;
       for (int64_t t = blockIdx.x; t < a.ntiles; t += G, ++i) {
-        const int b = i & 1;
-        mbar_wait(smem_u32(&h.tinfo_full[b]), (uint32_t)((i >> 1) & 1), a.status);
-        const int nst = *(volatile int*)&h.tinfo_nst[b];
+        const int r = i & (kInfoRing - 1), b = i & 1;
+        mbar_wait(smem_u32(&h.tinfo_full[r]), (uint32_t)((i / kInfoRing) & 1), a.status);
+        const TileInfo& inf = h.info[r];
+        const int nst = *(volatile const int*)&inf.nst;
+        const int npieces = *(volatile const int*)&inf.npieces;
         if (i >= 2) mbar_wait(smem_u32(&h.acc_empty[b]), (uint32_t)(((i >> 1) - 1) & 1), a.status);
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)b * acc_cols;
+        int slot = 0, cb = 0, g = 0;  // running piece -> (offset slot, channel block)
         for (int k = 0; k < nst; ++k, ++kg) {
           const int sb = (int)(kg % S);
           mbar_wait(smem_u32(&h.full[sb]), (uint32_t)((kg / S) & 1), a.status);
           tc_fence_after();
           const uint32_t sA = smem_u32(sbase + (size_t)sb * a.stage_bytes);
-          const uint32_t sB = sA + kATileBytes;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(d, sdesc_sw128(sA + kk * 32), sdesc_sw128(sB + kk * 32), idesc, (k | kk) ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk) {
+            uint64_t bdesc;
+            if (a.w_resident) {
+              // the MMA's two 8-channel pieces: resident blocks (offset, channel
+              // block), or the zero block past the real pieces; LBO spans them
+              uint32_t addr[2];
+#pragma unroll
+              for (int u = 0; u < 2; ++u) {
+                addr[u] = zero_blk;
+                if (g < npieces) {
+                  addr[u] = wsm + (uint32_t)(inf.slot_s[slot] * ppo + cb) * wblk;
+                  if (++cb == ppo) {
+                    cb = 0;
+                    ++slot;
+                  }
+                }
+                ++g;
+              }
+              bdesc = sdesc_plain(addr[0], addr[1] - addr[0], 128u);
+            } else {
+              bdesc = sdesc_sw128(sA + kATileBytes + kk * 32);
+            }
+            umma_bf16(d, sdesc_sw128(sA + kk * 32), bdesc, idesc, (k | kk) ? 1u : 0u);
+          }
           umma_commit(smem_u32(&h.empty[sb]));
         }
         if (nst > 0) umma_commit(smem_u32(&h.acc_full[b]));
@@ -478,43 +566,43 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tc(const __grid_c
     const int m = quarter * 32 + lane;
     int i = 0;
     for (int64_t t = blockIdx.x; t < a.ntiles; t += G, ++i) {
-      const int b = i & 1;
+      const int b = i & 1, r = i & (kInfoRing - 1);
       mbar_wait(smem_u32(&h.acc_full[b]), (uint32_t)((i >> 1) & 1), a.status);
       tc_fence_after();
-      const int nst = *(volatile int*)&h.tinfo_nst[b];
+      const int nst = *(volatile int*)&h.info[r].nst;
       const int64_t q = t * kRows + m;
       const uint32_t trow = tmem + (uint32_t)b * acc_cols + ((uint32_t)(quarter * 32) << 16);
       for (int c = 0; c < a.cout; c += 16) {
-        uint32_t r[16];
+        uint32_t v[16];
         if (nst > 0) {
-          tmem_ld16(trow + (uint32_t)c, r);
+          tmem_ld16(trow + (uint32_t)c, v);
         } else {
 #pragma unroll
-          for (int v = 0; v < 16; ++v) r[v] = 0u;
+          for (int e = 0; e < 16; ++e) v[e] = 0u;
         }
         if (q < a.n_out && a.out_bf16) {
           uint4 v0, v1;
-          v0.x = pack_bf16x2(__uint_as_float(r[0]), __uint_as_float(r[1]));
-          v0.y = pack_bf16x2(__uint_as_float(r[2]), __uint_as_float(r[3]));
-          v0.z = pack_bf16x2(__uint_as_float(r[4]), __uint_as_float(r[5]));
-          v0.w = pack_bf16x2(__uint_as_float(r[6]), __uint_as_float(r[7]));
-          v1.x = pack_bf16x2(__uint_as_float(r[8]), __uint_as_float(r[9]));
-          v1.y = pack_bf16x2(__uint_as_float(r[10]), __uint_as_float(r[11]));
-          v1.z = pack_bf16x2(__uint_as_float(r[12]), __uint_as_float(r[13]));
-          v1.w = pack_bf16x2(__uint_as_float(r[14]), __uint_as_float(r[15]));
+          v0.x = pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1]));
+          v0.y = pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3]));
+          v0.z = pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5]));
+          v0.w = pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7]));
+          v1.x = pack_bf16x2(__uint_as_float(v[8]), __uint_as_float(v[9]));
+          v1.y = pack_bf16x2(__uint_as_float(v[10]), __uint_as_float(v[11]));
+          v1.z = pack_bf16x2(__uint_as_float(v[12]), __uint_as_float(v[13]));
+          v1.w = pack_bf16x2(__uint_as_float(v[14]), __uint_as_float(v[15]));
           uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.y) + q * a.cout + c);
           dst[0] = v0;
           dst[1] = v1;
         } else if (q < a.n_out) {
           uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<float*>(a.y) + q * a.cout + c);
 #pragma unroll
-          for (int v = 0; v < 4; ++v) dst[v] = make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
         }
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&h.acc_empty[b]));
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&h.tinfo_empty[b]));
+      if (lane == 0) mbar_arrive(smem_u32(&h.tinfo_empty[r]));
     }
   }
   tc_fence_before();
@@ -607,20 +695,26 @@ extern "C" fvx_status fvx_sparse_conv(fvx_grid gin, fvx_grid gout, fvx_kmap m, f
   a.n_out = m->n_out;
   a.cin = (int)cin;
   a.cout = (int)cout;
-  a.stage_bytes = kATileBytes + (int)cout * 128;  // multiple of 1024 since cout % 8 == 0
+  // Weights resident in shared memory when they fit (27 * cin/8 blocks of
+  // cout x 16 bytes plus one zero block); otherwise a B tile per stage.
+  const int64_t wres = (27 * (cin / 8) + 1) * cout * 16;
+  a.w_resident = (wres <= kResidentWBytes) ? 1 : 0;
+  a.w_bytes = a.w_resident ? (int)((wres + 1023) & ~(int64_t)1023) : 0;
+  a.stage_bytes = kATileBytes + (a.w_resident ? 0 : (int)cout * 128);  // multiples of 1024
   // Stage ring (persistent across the CTA's tiles): as deep as shared memory
-  // allows, up to 8; one CTA per SM.
+  // allows, up to kMaxStages; one CTA per SM.
   const int head = (int)sizeof(ConvSmemHead) + 1024;
-  a.stages = (224 * 1024 - head) / a.stage_bytes;
-  if (a.stages > 8) a.stages = 8;
-  if (a.stages < kLag + 1) {
-    set_error("fvx_sparse_conv: cout %lld leaves fewer than %d pipeline stages", (long long)cout, kLag + 1);
+  a.stages = (224 * 1024 - head - a.w_bytes) / a.stage_bytes;
+  if (a.stages > kMaxStages) a.stages = kMaxStages;
+  if (a.stages < 3) {
+    set_error("fvx_sparse_conv: cout %lld leaves fewer than 3 pipeline stages", (long long)cout);
     return FVX_ERR_INVALID_ARG;
   }
+  a.lag = std::min(a.stages - 2, 10);
   int cols = 32;
   while (cols < cout) cols <<= 1;
   a.tmem_cols = cols;  // per accumulator; two accumulators per CTA (<= 512 columns)
-  const size_t smem = 1024 + (size_t)a.stages * a.stage_bytes + sizeof(ConvSmemHead);
+  const size_t smem = 1024 + (size_t)a.w_bytes + (size_t)a.stages * a.stage_bytes + sizeof(ConvSmemHead);
   FVX_CUDA(cudaFuncSetAttribute(k_conv_bf16_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   int dev = 0, sms = 0;
   FVX_CUDA(cudaGetDevice(&dev));

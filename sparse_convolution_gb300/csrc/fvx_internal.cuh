@@ -30,19 +30,32 @@ fvx_status cuda_fail(cudaError_t e, const char* what, const char* file, int line
 void* dalloc(size_t bytes, cudaStream_t s);  // NULL on failure (error recorded)
 void dfree(void* p, cudaStream_t s);
 
-// A set of temporary device buffers freed (stream-ordered) on scope exit.
+// Temporary device buffers of one call: carved (256-byte aligned) from a few
+// large chunks, freed stream-ordered on scope exit.
 struct Scratch {
   cudaStream_t stream;
   std::vector<void*> ptrs;
+  char* cur = nullptr;
+  size_t left = 0;
   explicit Scratch(cudaStream_t s) : stream(s) {}
   ~Scratch() {
     for (void* p : ptrs) dfree(p, stream);
   }
   template <class T>
   T* get(size_t count) {
-    void* p = dalloc(count * sizeof(T) + 16, stream);
-    if (p) ptrs.push_back(p);
-    return (T*)p;
+    const size_t bytes = (count * sizeof(T) + 16 + 255) & ~(size_t)255;
+    if (bytes > left) {
+      const size_t chunk = bytes > ((size_t)32 << 20) ? bytes : ((size_t)32 << 20);
+      void* p = dalloc(chunk, stream);
+      if (!p) return nullptr;
+      ptrs.push_back(p);
+      cur = (char*)p;
+      left = chunk;
+    }
+    T* r = (T*)cur;
+    cur += bytes;
+    left -= bytes;
+    return r;
   }
 };
 
@@ -69,13 +82,14 @@ enum : uint32_t { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_CHECK = 2 };
 // ---------------------------------------------------------------- primitives
 // Exclusive scan of n uint32 values (in may equal out).  If total != NULL the
 // grand total is written to total[0] (device).
-fvx_status scan_exclusive_u32(const uint32_t* in, uint32_t* out, int64_t n, uint32_t* total, cudaStream_t s);
+fvx_status scan_exclusive_u32(const uint32_t* in, uint32_t* out, int64_t n, uint32_t* total, cudaStream_t s,
+                              Scratch& scr);
 
 // Stable LSD radix sort of (key, value) pairs by key bits [bit_lo, bit_hi)
 // with 8-bit digits.  Ping-pongs between (k0,v0) and (k1,v1); returns in
 // *result_in_1 whether the sorted data ends in (k1,v1).
 fvx_status radix_sort_pairs(uint64_t* k0, uint32_t* v0, uint64_t* k1, uint32_t* v1, int64_t n, int bit_lo,
-                            int bit_hi, cudaStream_t s, bool* result_in_1);
+                            int bit_hi, cudaStream_t s, bool* result_in_1, Scratch& scr);
 
 }  // namespace fvx
 

@@ -148,6 +148,154 @@ __global__ void __launch_bounds__(kKmThreads) k_kmap_write(GridDev gin, const in
   }
 }
 
+// ------------------------------------------------------------------ stride 1,
+// bit-parallel.  A leaf mask is 8 words (word x = one x slice, bit y*8+z).
+// For offset d the output voxels of leaf O that have an input neighbour at
+// O + (x,y,z) + d are  out_word[x] & shifted_in_word(x, d): the input word of
+// slice x+dx, shifted by dy rows and dz bits, with the rows / bits that cross
+// the leaf border taken from the y / z / yz neighbour leaves.
+struct Km1Smem {
+  unsigned long long im[27][8];  // input leaf masks of the 27 slots (0 if absent)
+  unsigned long long pre9[27];
+  uint32_t first[27];
+  unsigned long long R[27][8];   // per offset: output voxels with a neighbour there
+  unsigned long long om[8];
+  unsigned long long opre9;
+  uint32_t qf;
+  int nvox;
+  uint16_t vox[512];
+};
+
+__device__ __forceinline__ unsigned long long shift_rows(unsigned long long c, unsigned long long nb, int dj) {
+  return dj == 0 ? c : (dj > 0 ? (c >> 8) | (nb << 56) : (c << 8) | (nb >> 56));
+}
+__device__ __forceinline__ unsigned long long shift_bits(unsigned long long v, unsigned long long vz, int dk) {
+  return dk == 0 ? v
+                 : (dk > 0 ? ((v >> 1) & 0x7F7F7F7F7F7F7F7Full) | ((vz & 0x0101010101010101ull) << 7)
+                           : ((v << 1) & 0xFEFEFEFEFEFEFEFEull) | ((vz & 0x8080808080808080ull) >> 7));
+}
+
+__device__ __forceinline__ unsigned long long km1_word(const Km1Smem& sm, int s, int x) {
+  const int di = s / 9 - 1, dj = (s / 3) % 3 - 1, dk = s % 3 - 1;
+  const int xs = x + di;
+  const int a = (xs + 8) >> 3, xw = xs & 7;
+  const unsigned long long A = sm.im[a * 9 + 4][xw];
+  const unsigned long long Y = dj ? sm.im[a * 9 + (1 + dj) * 3 + 1][xw] : 0ull;
+  const unsigned long long Z = dk ? sm.im[a * 9 + 3 + (1 + dk)][xw] : 0ull;
+  const unsigned long long YZ = (dj && dk) ? sm.im[a * 9 + (1 + dj) * 3 + (1 + dk)][xw] : 0ull;
+  return sm.om[x] & shift_bits(shift_rows(A, Y, dj), shift_rows(Z, YZ, dj), dk);
+}
+
+// Loads the output leaf and its 27 input-leaf slots (tree walks, or the slot
+// table written by the count pass).
+__device__ __forceinline__ void km1_load(Km1Smem& sm, const GridDev& gin, const int32_t* __restrict__ out_origin,
+                                         const int32_t* __restrict__ out_batch,
+                                         const uint64_t* __restrict__ out_rec, int lo,
+                                         const int32_t* __restrict__ nbr_in, int32_t* __restrict__ nbr_out) {
+  const int tid = threadIdx.x;
+  if (tid < 27) {
+    int l;
+    if (nbr_in) {
+      l = nbr_in[(int64_t)lo * 27 + tid];
+    } else {
+      const int a = tid / 9, b = (tid / 3) % 3, c = tid % 3;
+      l = find_leaf(gin, out_batch[lo], out_origin[3 * lo] - 8 + 8 * a, out_origin[3 * lo + 1] - 8 + 8 * b,
+                    out_origin[3 * lo + 2] - 8 + 8 * c);
+      if (nbr_out) nbr_out[(int64_t)lo * 27 + tid] = l;
+    }
+    const unsigned long long* r = reinterpret_cast<const unsigned long long*>(gin.leaf_rec) + (size_t)(l < 0 ? 0 : l) * 10;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) sm.im[tid][w] = l >= 0 ? __ldg(r + w) : 0ull;
+    sm.first[tid] = l >= 0 ? (uint32_t)__ldg(r + 8) : 0u;
+    sm.pre9[tid] = l >= 0 ? __ldg(r + 9) : 0ull;
+  } else if (tid >= 32 && tid < 42) {
+    const unsigned long long v = __ldg(reinterpret_cast<const unsigned long long*>(out_rec) + (size_t)lo * 10 + (tid - 32));
+    if (tid < 40) sm.om[tid - 32] = v;
+    else if (tid == 40) sm.qf = (uint32_t)v;
+    else sm.opre9 = v;
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kKmThreads) k_kmap1_count(GridDev gin, const int32_t* __restrict__ out_origin,
+                                                            const int32_t* __restrict__ out_batch,
+                                                            const uint64_t* __restrict__ out_rec, int64_t n_out_leaf,
+                                                            uint32_t* __restrict__ counts,
+                                                            uint32_t* __restrict__ out_mask,
+                                                            int32_t* __restrict__ nbr_out) {
+  __shared__ Km1Smem sm;
+  const int lo = blockIdx.x, tid = threadIdx.x;
+  km1_load(sm, gin, out_origin, out_batch, out_rec, lo, nullptr, nbr_out);
+  const int s = tid >> 3, x = tid & 7;
+  const unsigned long long R = (s < 27) ? km1_word(sm, s, x) : 0ull;
+  if (s < 27) sm.R[s][x] = R;
+  uint32_t c = (uint32_t)__popcll(R);
+  c += __shfl_xor_sync(0xffffffffu, c, 1);
+  c += __shfl_xor_sync(0xffffffffu, c, 2);
+  c += __shfl_xor_sync(0xffffffffu, c, 4);
+  if (s < 27 && x == 0) counts[(int64_t)s * n_out_leaf + lo] = c;
+  // active output voxels in index order
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int n = tid + h * 256;
+    const int w = n >> 6, bit = n & 63;
+    const unsigned long long m = sm.om[w];
+    if ((m >> bit) & 1ull) {
+      const uint32_t pre = w ? (uint32_t)((sm.opre9 >> (9 * (w - 1))) & 511ull) : 0u;
+      sm.vox[pre + (uint32_t)__popcll(m & ((1ull << bit) - 1ull))] = (uint16_t)n;
+    }
+  }
+  if (tid == 0) sm.nvox = (int)(((sm.opre9 >> 54) & 511ull) + (unsigned long long)__popcll(sm.om[7]));
+  __syncthreads();
+  for (int idx = tid; idx < sm.nvox; idx += kKmThreads) {
+    const int n = sm.vox[idx], w = n >> 6, bit = n & 63;
+    uint32_t mk = 0;
+#pragma unroll
+    for (int t = 0; t < 27; ++t) mk |= (uint32_t)((sm.R[t][w] >> bit) & 1ull) << t;
+    out_mask[sm.qf + idx] = mk;
+  }
+}
+
+__global__ void __launch_bounds__(kKmThreads) k_kmap1_write(GridDev gin, const int32_t* __restrict__ out_origin,
+                                                            const int32_t* __restrict__ out_batch,
+                                                            const uint64_t* __restrict__ out_rec, int64_t n_out_leaf,
+                                                            const uint32_t* __restrict__ starts,
+                                                            const int32_t* __restrict__ nbr_in,
+                                                            int32_t* __restrict__ in_idx,
+                                                            int32_t* __restrict__ out_idx) {
+  __shared__ Km1Smem sm;
+  const int lo = blockIdx.x, tid = threadIdx.x;
+  km1_load(sm, gin, out_origin, out_batch, out_rec, lo, nbr_in, nullptr);
+  const int s = tid >> 3, x = tid & 7;
+  unsigned long long R = (s < 27) ? km1_word(sm, s, x) : 0ull;
+  const uint32_t c = (uint32_t)__popcll(R);
+  uint32_t inc = c;
+#pragma unroll
+  for (int d = 1; d < 8; d <<= 1) {
+    const uint32_t o = __shfl_up_sync(0xffffffffu, inc, d, 8);
+    if (x >= d) inc += o;
+  }
+  if (s >= 27) return;
+  uint32_t e = starts[(int64_t)s * n_out_leaf + lo] + inc - c;
+  const int di = s / 9 - 1, dj = (s / 3) % 3 - 1, dk = s % 3 - 1;
+  const unsigned long long om = sm.om[x];
+  const uint32_t qx = sm.qf + (x ? (uint32_t)((sm.opre9 >> (9 * (x - 1))) & 511ull) : 0u);
+  const int xs = x + di;
+  const int sa = ((xs + 8) >> 3) * 9, xw = (xs & 7) << 6;
+  while (R) {
+    const int b = __ffsll((long long)R) - 1;
+    R &= R - 1ull;
+    const int ys = (b >> 3) + dj, zs = (b & 7) + dk;
+    const int slot = sa + ((ys + 8) >> 3) * 3 + ((zs + 8) >> 3);
+    const int nn = xw | ((ys & 7) << 3) | (zs & 7);
+    const int w = nn >> 6, bit = nn & 63;
+    const uint32_t pre = w ? (uint32_t)((sm.pre9[slot] >> (9 * (w - 1))) & 511ull) : 0u;
+    in_idx[e] = (int32_t)(sm.first[slot] + pre + (uint32_t)__popcll(sm.im[slot][w] & ((1ull << bit) - 1ull)));
+    out_idx[e] = (int32_t)(qx + (uint32_t)__popcll(om & ((1ull << b) - 1ull)));
+    ++e;
+  }
+}
+
 __global__ void k_list_offsets(const uint32_t* __restrict__ starts, int64_t n_out_leaf, const uint32_t* total,
                                uint32_t* __restrict__ out) {
   const int s = threadIdx.x;
@@ -156,14 +304,27 @@ __global__ void k_list_offsets(const uint32_t* __restrict__ starts, int64_t n_ou
 }
 
 // per conv tile of kTileRows outputs: number of outputs with mask bit s
-__global__ void __launch_bounds__(kTileRows) k_tile_counts(const uint32_t* __restrict__ mask, int64_t n_out,
-                                                           int64_t ntiles, uint32_t* __restrict__ cnt) {
-  const int64_t q = (int64_t)blockIdx.x * kTileRows + threadIdx.x;
-  const uint32_t m = (q < n_out) ? mask[q] : 0u;
-  for (int s = 0; s < 27; ++s) {
-    const int c = __syncthreads_count((m >> s) & 1u);
-    if (threadIdx.x == 0) cnt[(int64_t)s * ntiles + blockIdx.x] = (uint32_t)c;
+// (one warp per tile: lane r holds the masks of rows r, r+32, r+64, r+96)
+__global__ void __launch_bounds__(256) k_tile_counts(const uint32_t* __restrict__ mask, int64_t n_out,
+                                                     int64_t ntiles, uint32_t* __restrict__ cnt) {
+  const int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (t >= ntiles) return;
+  uint32_t m[kTileRows / 32];
+#pragma unroll
+  for (int h = 0; h < kTileRows / 32; ++h) {
+    const int64_t q = t * kTileRows + h * 32 + lane;
+    m[h] = (q < n_out) ? mask[q] : 0u;
   }
+  uint32_t mine = 0;  // lane s keeps the count of offset s
+#pragma unroll
+  for (int s = 0; s < 27; ++s) {
+    uint32_t c = 0;
+#pragma unroll
+    for (int h = 0; h < kTileRows / 32; ++h) c += __popc(__ballot_sync(0xffffffffu, (m[h] >> s) & 1u));
+    if (lane == s) mine = c;
+  }
+  if (lane < 27) cnt[(int64_t)lane * ntiles + t] = mine;
 }
 
 size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -217,13 +378,22 @@ extern "C" fvx_status fvx_kernel_map(fvx_grid gin, fvx_grid gout, int32_t ksize,
   m->tile_start = (uint32_t*)((char*)m->block + o_tile);
 
   const GridDev gd = grid_dev(gin);
+  int32_t* nbr = nullptr;  // stride 1: input-leaf slot table written by the count pass
+  if (stride == 1) {
+    nbr = scr.get<int32_t>((size_t)(27 * Lo + 1));
+    if (!nbr) return FVX_ERR_ALLOC;
+  }
   if (Lo > 0) {
     LaunchScope ls("kmap_count", s);
-    k_kmap_count<<<(unsigned)Lo, kKmThreads, 0, s>>>(gd, gout->leaf_origin, gout->leaf_batch, gout->leaf_rec, Lo,
-                                                     stride, counts, m->out_mask);
+    if (stride == 1)
+      k_kmap1_count<<<(unsigned)Lo, kKmThreads, 0, s>>>(gd, gout->leaf_origin, gout->leaf_batch, gout->leaf_rec, Lo,
+                                                        counts, m->out_mask, nbr);
+    else
+      k_kmap_count<<<(unsigned)Lo, kKmThreads, 0, s>>>(gd, gout->leaf_origin, gout->leaf_batch, gout->leaf_rec, Lo,
+                                                       stride, counts, m->out_mask);
   }
   FVX_TRY(check_launch("kmap_count"));
-  FVX_TRY(scan_exclusive_u32(counts, counts, 27 * Lo, dtot + 28, s));
+  FVX_TRY(scan_exclusive_u32(counts, counts, 27 * Lo, dtot + 28, s, scr));
   {
     LaunchScope ls("kmap_list_offsets", s);
     k_list_offsets<<<1, 32, 0, s>>>(counts, Lo, dtot + 28, dtot);
@@ -246,19 +416,24 @@ extern "C" fvx_status fvx_kernel_map(fvx_grid gin, fvx_grid gout, int32_t ksize,
   m->out_idx = (int32_t*)((char*)m->block2 + align_up(4 * (size_t)P));
   if (Lo > 0 && P > 0) {
     LaunchScope ls("kmap_write", s);
-    k_kmap_write<<<(unsigned)Lo, kKmThreads, 0, s>>>(gd, gout->leaf_origin, gout->leaf_batch, gout->leaf_rec, Lo,
-                                                     stride, counts, m->in_idx, m->out_idx);
+    if (stride == 1)
+      k_kmap1_write<<<(unsigned)Lo, kKmThreads, 0, s>>>(gd, gout->leaf_origin, gout->leaf_batch, gout->leaf_rec, Lo,
+                                                        counts, nbr, m->in_idx, m->out_idx);
+    else
+      k_kmap_write<<<(unsigned)Lo, kKmThreads, 0, s>>>(gd, gout->leaf_origin, gout->leaf_batch, gout->leaf_rec, Lo,
+                                                       stride, counts, m->in_idx, m->out_idx);
   }
   FVX_TRY(check_launch("kmap_write"));
   // conv tiling: where each tile's pairs start in every list
   if (m->n_tiles > 0) {
     {
       LaunchScope ls("kmap_tile_counts", s);
-      k_tile_counts<<<(unsigned)m->n_tiles, kTileRows, 0, s>>>(m->out_mask, Nout, m->n_tiles, m->tile_start);
+      k_tile_counts<<<(unsigned)((m->n_tiles * 32 + 255) / 256), 256, 0, s>>>(m->out_mask, Nout, m->n_tiles,
+                                                                             m->tile_start);
     }
     FVX_TRY(check_launch("kmap_tile_counts"));
   }
-  FVX_TRY(scan_exclusive_u32(m->tile_start, m->tile_start, 27 * m->n_tiles, m->tile_start + 27 * m->n_tiles, s));
+  FVX_TRY(scan_exclusive_u32(m->tile_start, m->tile_start, 27 * m->n_tiles, m->tile_start + 27 * m->n_tiles, s, scr));
   *out = m;
   m = nullptr;
   return FVX_OK;

@@ -69,13 +69,13 @@ __global__ void __launch_bounds__(kScanThreads) k_scan_down(const uint32_t* in, 
   }
 }
 
-fvx_status scan_exclusive_u32(const uint32_t* in, uint32_t* out, int64_t n, uint32_t* total, cudaStream_t s) {
+fvx_status scan_exclusive_u32(const uint32_t* in, uint32_t* out, int64_t n, uint32_t* total, cudaStream_t s,
+                              Scratch& scr) {
   if (n <= 0) {
     if (total) FVX_CUDA(cudaMemsetAsync(total, 0, 4, s));
     return FVX_OK;
   }
   const int64_t nt = (n + kScanTile - 1) / kScanTile;
-  Scratch scr(s);
   uint32_t* partial = scr.get<uint32_t>((size_t)nt);
   if (!partial) return FVX_ERR_ALLOC;
   {
@@ -196,16 +196,11 @@ __global__ void __launch_bounds__(kRsThreads) k_radix_scatter(const uint64_t* __
 }
 
 fvx_status radix_sort_pairs(uint64_t* k0, uint32_t* v0, uint64_t* k1, uint32_t* v1, int64_t n, int bit_lo,
-                            int bit_hi, cudaStream_t s, bool* result_in_1) {
+                            int bit_hi, cudaStream_t s, bool* result_in_1, Scratch& scr) {
   *result_in_1 = false;
   if (n <= 1 || bit_hi <= bit_lo) return FVX_OK;
-  static bool attr_set = false;
-  if (!attr_set) {
-    FVX_CUDA(cudaFuncSetAttribute(k_radix_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(RsSmem)));
-    attr_set = true;
-  }
+  FVX_CUDA(cudaFuncSetAttribute(k_radix_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(RsSmem)));
   const int64_t ntiles = (n + kRsTile - 1) / kRsTile;
-  Scratch scr(s);
   uint32_t* counts = scr.get<uint32_t>((size_t)(256 * ntiles));
   if (!counts) return FVX_ERR_ALLOC;
   uint64_t* ks = k0;
@@ -221,7 +216,7 @@ fvx_status radix_sort_pairs(uint64_t* k0, uint32_t* v0, uint64_t* k1, uint32_t* 
       k_radix_hist<<<(unsigned)ntiles, kRsThreads, 0, s>>>(ks, n, lo, dmask, counts, ntiles);
     }
     FVX_TRY(check_launch("radix_hist"));
-    FVX_TRY(scan_exclusive_u32(counts, counts, 256 * ntiles, nullptr, s));
+    FVX_TRY(scan_exclusive_u32(counts, counts, 256 * ntiles, nullptr, s, scr));
     {
       LaunchScope ls("radix_scatter", s);
       k_radix_scatter<<<(unsigned)ntiles, kRsThreads, sizeof(RsSmem), s>>>(ks, vs, kd, vd, n, lo, dmask, counts,
