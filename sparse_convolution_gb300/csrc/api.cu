@@ -38,14 +38,46 @@ static fvx_alloc_fn g_alloc = nullptr;
 static fvx_free_fn g_free = nullptr;
 static void* g_alloc_ctx = nullptr;
 
+// The library's own stream-ordered pool per device.  Its release threshold is
+// unbounded, so memory freed by one call is reused by the next instead of
+// being returned to the driver at every synchronisation (the default pool's
+// behaviour), without changing any pool the rest of the process uses.
+static cudaMemPool_t library_pool() {
+  static cudaMemPool_t pools[64] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!pools[dev]) {
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.handleTypes = cudaMemHandleTypeNone;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t p = nullptr;
+    if (cudaMemPoolCreate(&p, &props) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    uint64_t thr = ~0ull;
+    cudaMemPoolSetAttribute(p, cudaMemPoolAttrReleaseThreshold, &thr);
+    pools[dev] = p;
+  }
+  return pools[dev];
+}
+
 void* dalloc(size_t bytes, cudaStream_t s) {
   if (bytes == 0) bytes = 256;
   void* p = nullptr;
   if (g_alloc) {
     p = g_alloc(bytes, (fvx_stream)s, g_alloc_ctx);
-  } else if (cudaMallocAsync(&p, bytes, s) != cudaSuccess) {
-    cudaGetLastError();
-    p = nullptr;
+  } else {
+    cudaMemPool_t pool = library_pool();
+    cudaError_t e = pool ? cudaMallocFromPoolAsync(&p, bytes, pool, s) : cudaMallocAsync(&p, bytes, s);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      p = nullptr;
+    }
   }
   if (!p) set_error("device allocation of %zu bytes failed", bytes);
   return p;

@@ -166,14 +166,16 @@ __device__ __forceinline__ uint32_t mbar_try(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete; gives up after
-// kWaitNs (or as soon as another CTA has reported a failure), recording
-// DEV_TIMEOUT in the status word.  Returns false on give-up.
+// kWaitNs (or once another CTA has reported a failure), recording DEV_TIMEOUT
+// in the status word.  Returns false on give-up.  The clock and the status
+// word (an L2 round trip) are checked only every 1024 polls so that a
+// completed phase is seen at once.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* status) {
   if (mbar_try(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
-  while (true) {
+  for (uint32_t it = 1;; ++it) {
     if (mbar_try(bar, parity)) return true;
-    if (globaltimer() - t0 > kWaitNs || *(volatile uint32_t*)status != 0u) {
+    if ((it & 1023u) == 0u && (globaltimer() - t0 > kWaitNs || *(volatile uint32_t*)status != 0u)) {
       report_device_error(status, DEV_TIMEOUT);
       return false;
     }
@@ -330,9 +332,8 @@ __device__ __forceinline__ void publish_info(ConvSmemHead& h, const ConvArgs& a,
   if (j >= kInfoRing) mbar_wait(smem_u32(&h.tinfo_empty[r]), (uint32_t)(((j / kInfoRing) - 1) & 1), a.status);
   h.info[r].nst = (npieces + 7) >> 3;
   h.info[r].npieces = npieces;
-  int slot = 0;
   for (int s = 0; s < 27; ++s)
-    if ((tor >> s) & 1u) h.info[r].slot_s[slot++] = s;
+    if ((tor >> s) & 1u) h.info[r].slot_s[__popc(tor & ((1u << s) - 1u))] = s;
   mbar_arrive(smem_u32(&h.tinfo_full[r]));
 }
 

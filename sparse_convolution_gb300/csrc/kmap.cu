@@ -266,33 +266,43 @@ __global__ void __launch_bounds__(kKmThreads) k_kmap1_write(GridDev gin, const i
   __shared__ Km1Smem sm;
   const int lo = blockIdx.x, tid = threadIdx.x;
   km1_load(sm, gin, out_origin, out_batch, out_rec, lo, nbr_in, nullptr);
-  const int s = tid >> 3, x = tid & 7;
-  unsigned long long R = (s < 27) ? km1_word(sm, s, x) : 0ull;
-  const uint32_t c = (uint32_t)__popcll(R);
-  uint32_t inc = c;
-#pragma unroll
-  for (int d = 1; d < 8; d <<= 1) {
-    const uint32_t o = __shfl_up_sync(0xffffffffu, inc, d, 8);
-    if (x >= d) inc += o;
+  {
+    const int s = tid >> 3, x = tid & 7;
+    if (s < 27) sm.R[s][x] = km1_word(sm, s, x);
   }
-  if (s >= 27) return;
-  uint32_t e = starts[(int64_t)s * n_out_leaf + lo] + inc - c;
-  const int di = s / 9 - 1, dj = (s / 3) % 3 - 1, dk = s % 3 - 1;
-  const unsigned long long om = sm.om[x];
-  const uint32_t qx = sm.qf + (x ? (uint32_t)((sm.opre9 >> (9 * (x - 1))) & 511ull) : 0u);
-  const int xs = x + di;
-  const int sa = ((xs + 8) >> 3) * 9, xw = (xs & 7) << 6;
-  while (R) {
-    const int b = __ffsll((long long)R) - 1;
-    R &= R - 1ull;
-    const int ys = (b >> 3) + dj, zs = (b & 7) + dk;
-    const int slot = sa + ((ys + 8) >> 3) * 3 + ((zs + 8) >> 3);
-    const int nn = xw | ((ys & 7) << 3) | (zs & 7);
-    const int w = nn >> 6, bit = nn & 63;
-    const uint32_t pre = w ? (uint32_t)((sm.pre9[slot] >> (9 * (w - 1))) & 511ull) : 0u;
-    in_idx[e] = (int32_t)(sm.first[slot] + pre + (uint32_t)__popcll(sm.im[slot][w] & ((1ull << bit) - 1ull)));
-    out_idx[e] = (int32_t)(qx + (uint32_t)__popcll(om & ((1ull << b) - 1ull)));
-    ++e;
+  __syncthreads();
+  // one warp per offset: per half word, a ballot packs the pairs into a
+  // contiguous run of the list (coalesced stores)
+  const int warp = tid >> 5, lane = tid & 31;
+  const uint32_t lt = lanemask_lt();
+  for (int s = warp; s < 27; s += kKmThreads / 32) {
+    const int di = s / 9 - 1, dj = (s / 3) % 3 - 1, dk = s % 3 - 1;
+    uint32_t e = starts[(int64_t)s * n_out_leaf + lo];
+    for (int x = 0; x < 8; ++x) {
+      const unsigned long long R = sm.R[s][x];
+      if (!R) continue;
+      const unsigned long long om = sm.om[x];
+      const uint32_t qx = sm.qf + (x ? (uint32_t)((sm.opre9 >> (9 * (x - 1))) & 511ull) : 0u);
+      const int xs = x + di;
+      const int sa = ((xs + 8) >> 3) * 9, xw = (xs & 7) << 6;
+#pragma unroll
+      for (int hw = 0; hw < 2; ++hw) {
+        const int b = hw * 32 + lane;
+        const bool has = (R >> b) & 1ull;
+        const uint32_t bal = __ballot_sync(0xffffffffu, has);
+        if (has) {
+          const int ys = (b >> 3) + dj, zs = (b & 7) + dk;
+          const int slot = sa + ((ys + 8) >> 3) * 3 + ((zs + 8) >> 3);
+          const int nn = xw | ((ys & 7) << 3) | (zs & 7);
+          const int w = nn >> 6, bit = nn & 63;
+          const uint32_t pre = w ? (uint32_t)((sm.pre9[slot] >> (9 * (w - 1))) & 511ull) : 0u;
+          const uint32_t pos = e + __popc(bal & lt);
+          in_idx[pos] = (int32_t)(sm.first[slot] + pre + (uint32_t)__popcll(sm.im[slot][w] & ((1ull << bit) - 1ull)));
+          out_idx[pos] = (int32_t)(qx + (uint32_t)__popcll(om & ((1ull << b) - 1ull)));
+        }
+        e += __popc(bal);
+      }
+    }
   }
 }
 
