@@ -129,6 +129,29 @@ class ClockSampler:
                     reasons=sorted(reasons), samples=len(sm))
 
 
+def profiled_traffic(kernel, workload):
+    """DRAM bytes per launch (read + write) of `kernel` from the committed ncu
+    summary under profiles/, if that capture was taken on the current source of
+    the kernel (sha256 of its .cu file recorded in the summary); else None."""
+    import hashlib
+    import re
+
+    src = {"conv_bf16_tc": "conv.cu", "kmap1_write": "kmap.cu"}.get(kernel)
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if src is None or not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    m_rd = re.search(r"dram__bytes_read\.sum[^0-9]*([0-9.]+)\s*MB", text)
+    m_wr = re.search(r"dram__bytes_write\.sum[^0-9]*([0-9.]+)\s*MB", text)
+    if not (m_sha and m_rd and m_wr):
+        return None
+    cur = hashlib.sha256(open(os.path.join(ROOT, "sparse_convolution_gb300", "csrc", src), "rb").read()).hexdigest()
+    if cur != m_sha.group(1):
+        return None
+    return int((float(m_rd.group(1)) + float(m_wr.group(1))) * 1e6)
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -279,7 +302,8 @@ def bench_fvx(args, world, rank, local):
         ach = alg_bytes / (avg_ms / 1e3) / 1e9
         peak = peaks["hbm_gbs"]
         roofline = dict(bound="hbm", kernel=prof_kernel, achieved=round(ach, 1), peak=peak, unit="GB/s",
-                        frac=round(ach / peak, 4), traffic=None, algorithmic_bytes=int(alg_bytes),
+                        frac=round(ach / peak, 4), traffic=profiled_traffic(prof_kernel, w["name"]),
+                        algorithmic_bytes=int(alg_bytes),
                         avg_launch_ms=round(avg_ms, 5), peak_source=f"{peak_kind} (hbm_gbs)")
 
     # end to end through the public API with host buffers

@@ -10,18 +10,18 @@
 // outputs (the tcgen05 M); the K dimension of the tile's GEMM is the
 // concatenation, over the offsets that occur in the tile, of Cin channels each,
 // so empty offsets cost nothing and small Cin (8, 16) still fills K = 64 per
-// pipeline stage.  For output row m and offset s the gathered A row is x[p]
-// where (p, q0+m) is a pair of list s, or zeros; the pair is found from the
-// 27-bit output mask ["DriveRT", "Kernels selected per GPU"] by the rank of m
-// among the tile's rows with bit s, added to the tile's start in list s.
+// pipeline stage.  Because every list is ordered by output, the pairs of list
+// s that belong to a tile form one contiguous segment of at most 128 pairs
+// ("DriveRT", "Shared neighbour maps": the map is built once and read by the
+// convolution); the tile's row table is filled from those segments.
 //
 // Two kernels, one per dtype (no dispatch between backends):
-//   * bf16: persistent and warp-specialized.  Producers build each tile's row
-//     table (software-pipelined one tile ahead) and gather A (feature rows,
-//     16-byte pieces) with cp.async into 128B-swizzled K-major stages; the
-//     weights are either resident in shared memory for the whole kernel (when
+//   * bf16: persistent and warp-specialized.  Eight producer warps build each
+//     tile's row table one tile ahead and gather A (feature rows, 16-byte
+//     pieces) with cp.async into 128B-swizzled K-major stages; the weights are
+//     either resident in shared memory for the whole kernel (when
 //     27*cin*cout*2 bytes fit in 64 KB) or gathered per stage.  One thread
-//     issues tcgen05.mma kind::f16 (bf16 x bf16 -> fp32 in TMEM); epilogue
+//     issues tcgen05.mma kind::f16 (bf16 x bf16 -> fp32 in TMEM); four epilogue
 //     warps drain a double-buffered TMEM accumulator with tcgen05.ld while the
 //     next tile accumulates.  Output fp32, or bf16 rounded to nearest even.
 //   * fp32: exact FFMA on CUDA cores (no TF32).
@@ -39,10 +39,9 @@ namespace {
 
 constexpr int kRows = kTileRows;  // 128
 
-// ============================================================== tile row tables
-// Per tile: for each offset s, the ballot of the tile's rows having bit s, per
-// warp (4 warps x 32 rows).  rank of row m in list s = popcount of the bits
-// before it.
+// ============================================================== fp32 FFMA
+// Per tile of 128 outputs: the rank of row m in list s (popcount of the
+// tile's rows before m with mask bit s) locates its pair in the list.
 struct TileMasks {
   uint32_t wb[27][4];
 };
@@ -62,14 +61,6 @@ __device__ __forceinline__ uint32_t tile_rank(const TileMasks& tm, int s, int wa
   return r;
 }
 
-__device__ __forceinline__ uint32_t tile_or(const TileMasks& tm) {
-  uint32_t o = 0;
-  for (int s = 0; s < 27; ++s)
-    if (tm.wb[s][0] | tm.wb[s][1] | tm.wb[s][2] | tm.wb[s][3]) o |= 1u << s;
-  return o;
-}
-
-// ============================================================== fp32 FFMA
 constexpr int kF32Cols = 16;
 
 __global__ void __launch_bounds__(kRows) k_conv_f32(const float* __restrict__ x, const float* __restrict__ W,
@@ -127,14 +118,17 @@ __global__ void __launch_bounds__(kRows) k_conv_f32(const float* __restrict__ x,
 }
 
 // ============================================================== bf16 tcgen05
-// Warp roles of the persistent bf16 kernel: warps 0-3 build each tile's row
-// table and gather into the stage ring, warp 4 issues the MMAs (and owns
-// TMEM), warps 5-8 drain the double-buffered TMEM accumulator to global.
-constexpr int kProducerWarps = 4;
+// Warp roles of the persistent bf16 kernel: warps 0-7 (two threads per tile
+// row) build each tile's row table and gather into the stage ring, warp 8
+// issues the MMAs (and owns TMEM), warps 9-12 drain the double-buffered TMEM
+// accumulator to global (warp w may read TMEM lanes 32*(w%4) .. +31).
+constexpr int kProducerWarps = 8;
+constexpr int kProducers = kProducerWarps * 32;  // 256: row m = tid & 127, half = tid >> 7
 constexpr int kMmaWarp = kProducerWarps;
 constexpr int kConvThreads = (kProducerWarps + 1 + 4) * 32;
 constexpr int kMaxStages = 12;
 constexpr int kInfoRing = 4;                           // tiles whose info can be in flight
+constexpr int kHalfOffsets = 14;                       // offsets 0..13 -> half 0, 14..26 -> half 1
 constexpr int kATileBytes = kRows * 128;               // 128 rows x 64 bf16 (one 128B swizzle atom wide)
 constexpr int kResidentWBytes = 64 * 1024;             // weights kept in shared memory up to this size
 constexpr unsigned long long kWaitNs = 2000000000ull;  // bounded mbarrier waits: 2 s
@@ -182,8 +176,11 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
   }
 }
 
+// cp.async of 16 bytes (src_bytes 0: zero fill).  No "memory" clobber: the
+// copy only writes the stage buffer, which this thread does not read, and
+// volatile asm statements keep their order (commit / wait below).
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes));
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 // cp.async.wait_group takes an immediate: at most n groups of this thread left pending.
@@ -203,7 +200,7 @@ __device__ __forceinline__ void cp_async_wait_n(int n) {
   }
 }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-__device__ __forceinline__ void producer_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void producer_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 // UMMA shared-memory descriptors (K-major).  128-byte swizzle: 8-row groups
 // 1024 bytes apart (SBO), leading offset unused.  No swizzle: 8 x 16-byte core
@@ -257,10 +254,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 // Row table of one tile (double-buffered: producers fill tile i+1's while
 // gathering tile i's).
 struct TileTable {
-  TileMasks tm;
   int32_t rowp[27][kRows];  // gathered input row for (offset slot, tile row), -1 = zeros
+  uint32_t tstart[27];      // the tile's segment [tstart, tend) in each list
+  uint32_t tend[27];
   int32_t slot_s[27];       // offset of each slot (offsets present in the tile, ascending)
-  uint32_t tstart[27];      // the tile's first pair in each list
+  uint32_t tor;             // bit s: list s has pairs in the tile
 };
 
 // What the MMA thread and the epilogue need to know about a tile.
@@ -273,74 +271,56 @@ struct TileInfo {
 struct ConvSmemHead {
   TileTable tab[2];
   TileInfo info[kInfoRing];
-  unsigned long long full[kMaxStages], empty[kMaxStages];        // stage ring: producers <-> MMA
+  unsigned long long full[kMaxStages], empty[kMaxStages];            // stage ring: producers <-> MMA
   unsigned long long tinfo_full[kInfoRing], tinfo_empty[kInfoRing];  // tile info: producers -> MMA, epilogue
-  unsigned long long acc_full[2], acc_empty[2];                  // TMEM accumulators: MMA <-> epilogue
+  unsigned long long acc_full[2], acc_empty[2];                      // TMEM accumulators: MMA <-> epilogue
   uint32_t tmem_base;
 };
 
 struct ConvArgs {
   const __nv_bfloat16* x;
   const __nv_bfloat16* wt;  // [27][cout][cin], K-major per offset
-  const uint32_t* mask;
   const int32_t* in_idx;
-  const uint32_t* tile_start;
-  void* y;                  // fp32 or bf16 [n_out][cout]
+  const int32_t* out_idx;
+  const uint32_t* tile_start;  // [27 * ntiles + 1], list-major exclusive scan
+  void* y;                     // fp32 or bf16 [n_out][cout]
   uint32_t* status;
   int64_t ntiles, n_out;
   int cin, cout, stages, lag, stage_bytes, tmem_cols, out_bf16;
-  int w_resident;           // weights live in shared memory (no per-stage B tile)
-  int w_bytes;              // resident weight region incl. one zero block (multiple of 1024)
+  int w_resident;  // weights live in shared memory (no per-stage B tile)
+  int w_bytes;     // resident weight region incl. one zero block (multiple of 1024)
 };
 
 // Producer helpers ----------------------------------------------------------
-__device__ __forceinline__ uint32_t load_mask(const ConvArgs& a, int64_t t, int m) {
-  const int64_t q = t * kRows + m;
-  return (t < a.ntiles && q < a.n_out) ? __ldg(a.mask + q) : 0u;
-}
-__device__ __forceinline__ uint32_t load_tstart(const ConvArgs& a, int64_t t, int m) {
-  return (t < a.ntiles && m < 27) ? __ldg(a.tile_start + (int64_t)m * a.ntiles + t) : 0u;
-}
-
-// Issues the 27 independent input-index loads of this thread's row (results
-// land in ps while the caller goes on).  Requires tab.tm / tab.tstart set.
-__device__ __forceinline__ void issue_row_loads(const TileTable& tab, const int32_t* __restrict__ in_idx, uint32_t mk,
-                                                int (&ps)[27]) {
-  const int warp = threadIdx.x >> 5;
-  const uint32_t lt = lanemask_lt();
-#pragma unroll
-  for (int s = 0; s < 27; ++s) ps[s] = ((mk >> s) & 1u) ? __ldg(in_idx + tab.tstart[s] + tile_rank(tab.tm, s, warp, lt)) : -1;
-}
-
-__device__ __forceinline__ void store_rows(TileTable& tab, uint32_t tor, const int (&ps)[27]) {
-  const int m = threadIdx.x;
-  int slot = 0;
-#pragma unroll
-  for (int s = 0; s < 27; ++s) {
-    if ((tor >> s) & 1u) {
-      tab.rowp[slot][m] = ps[s];
-      if (m == 0) tab.slot_s[slot] = s;
-      ++slot;
-    }
+// (start, end) of list s's segment for tile t: consecutive entries of the
+// list-major scan (the entry after the last tile of list s is list s+1's
+// start, and the scan's total closes list 26).
+__device__ __forceinline__ void load_segment(const uint32_t* __restrict__ ts, int64_t ntiles, int64_t t, int s,
+                                             uint32_t& a0, uint32_t& a1) {
+  a0 = 0u;
+  a1 = 0u;
+  if (t < ntiles && s < 27) {
+    a0 = __ldg(ts + (int64_t)s * ntiles + t);
+    a1 = __ldg(ts + (int64_t)s * ntiles + t + 1);
   }
 }
 
-// Publishes a tile's info for the MMA thread and the epilogue (thread 0 of
-// the producers).
-__device__ __forceinline__ void publish_info(ConvSmemHead& h, const ConvArgs& a, int j, uint32_t tor, int npieces) {
+// Publishes a tile's info for the MMA thread and the epilogue (thread 0).
+__device__ __forceinline__ void publish_info(ConvSmemHead& h, uint32_t* status, int j, const TileTable& tab,
+                                             int npieces) {
   const int r = j & (kInfoRing - 1);
-  if (j >= kInfoRing) mbar_wait(smem_u32(&h.tinfo_empty[r]), (uint32_t)(((j / kInfoRing) - 1) & 1), a.status);
+  if (j >= kInfoRing) mbar_wait(smem_u32(&h.tinfo_empty[r]), (uint32_t)(((j / kInfoRing) - 1) & 1), status);
   h.info[r].nst = (npieces + 7) >> 3;
   h.info[r].npieces = npieces;
-  for (int s = 0; s < 27; ++s)
-    if ((tor >> s) & 1u) h.info[r].slot_s[__popc(tor & ((1u << s) - 1u))] = s;
+  const int ns = __popc(tab.tor);
+  for (int k = 0; k < ns; ++k) h.info[r].slot_s[k] = tab.slot_s[k];
   mbar_arrive(smem_u32(&h.tinfo_full[r]));
 }
 
 __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tc(const __grid_constant__ ConvArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // [resident weights][stage ring][head], each 1024-aligned
-  unsigned char* wbase = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  unsigned char* wbase = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   unsigned char* sbase = wbase + a.w_bytes;
   ConvSmemHead& h = *reinterpret_cast<ConvSmemHead*>(sbase + (size_t)a.stages * a.stage_bytes);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -348,11 +328,12 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tc(const __grid_c
   const int ppo = a.cin >> 3;  // 16-byte pieces per (row, offset)
   const uint32_t acc_cols = (uint32_t)a.tmem_cols;
   const int64_t G = gridDim.x;
+  const int64_t ntiles = a.ntiles;
 
   // ---- setup: barriers (thread 0), TMEM for two accumulators (MMA warp)
   if (tid == 0) {
     for (int i = 0; i < S; ++i) {
-      mbar_init(smem_u32(&h.full[i]), kProducerWarps * 32);
+      mbar_init(smem_u32(&h.full[i]), kProducers);
       mbar_init(smem_u32(&h.empty[i]), 1);
     }
     for (int r = 0; r < kInfoRing; ++r) {
@@ -377,97 +358,153 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tc(const __grid_c
   const uint32_t tmem = h.tmem_base;
 
   if (warp < kProducerWarps) {
-    // ---------------- producers
-    const int m = tid;
+    // ---------------- producers: thread (row m, half hf)
+    const int pt = tid, m = pt & (kRows - 1), hf = pt >> 7;
+    const int s_lo = hf * kHalfOffsets, s_hi = hf ? 27 : kHalfOffsets;
     const int L = a.lag;
-    int64_t kg = 0, signaled = 0;  // stage counters, continuing across tiles
+    const __nv_bfloat16* const gx = a.x;
+    const __nv_bfloat16* const gwt = a.wt;
+    const int32_t* const gin = a.in_idx;
+    const int32_t* const gout = a.out_idx;
+    const uint32_t* const gts = a.tile_start;
+    const int cin = a.cin, cout = a.cout, wres = a.w_resident, sbytes = a.stage_bytes;
+    uint32_t* const status = a.status;
+    int64_t kg = 0, signaled = 0;  // stages issued / signaled, continuing across tiles
+    int ring_sb = 0, sig_sb = 0;   // ring slot of the next stage to issue / to signal
+    uint32_t ring_ph = 0;          // parity of ring_sb's current use
     int64_t kg_end[kInfoRing] = {0, 0, 0, 0};
-    if (a.w_resident) {
+    if (wres) {
       // resident weights: block (s, piece c) = cout rows x 16 bytes; one zero
       // block after the 27 * ppo real ones (the B of padded pieces)
       const uint32_t wdst = smem_u32(wbase);
       const int nblk = 27 * ppo;
-      for (int e = m; e < (nblk + 1) * a.cout; e += kProducerWarps * 32) {
-        const int blk = e / a.cout, n = e - blk * a.cout;
-        const void* src = a.wt;
+      for (int e = pt; e < (nblk + 1) * cout; e += kProducers) {
+        const int blk = e / cout, n = e - blk * cout;
+        const void* src = gwt;
         uint32_t bytes = 0;
         if (blk < nblk) {
           const int s = blk / ppo, c = blk - s * ppo;
-          src = a.wt + ((int64_t)s * a.cout + n) * a.cin + c * 8;
+          src = gwt + ((int64_t)s * cout + n) * cin + c * 8;
           bytes = 16;
         }
         cp_async16(wdst + (uint32_t)e * 16u, src, bytes);
       }
       cp_async_commit();  // completes before the first stage is signaled
     }
-    int ps[27];
-    // tables of the first tile (exposed once), masks of the second prefetched
-    int64_t t = blockIdx.x;
-    const uint32_t mk0 = load_mask(a, t, m), ts0 = load_tstart(a, t, m);
-    uint32_t mk_nxt = load_mask(a, t + G, m), ts_nxt = load_tstart(a, t + G, m);
-    if (m < 27) h.tab[0].tstart[m] = ts0;
-    tile_ballots(h.tab[0].tm, mk0);
-    producer_bar();
-    uint32_t tor = tile_or(h.tab[0].tm);
-    issue_row_loads(h.tab[0], a.in_idx, mk0, ps);
-    store_rows(h.tab[0], tor, ps);
-    int total = __popc(tor) * ppo;
-    if (m == 0 && t < a.ntiles) publish_info(h, a, 0, tor, total);
-    producer_bar();
-    for (int i = 0; t < a.ntiles; t += G, ++i) {
-      const int b = i & 1, nb = b ^ 1;
-      const bool has_next = (t + G) < a.ntiles;
-      const TileTable& cur = h.tab[b];
-      TileTable& nxt = h.tab[nb];
-      // (a) next tile: ballots and the 27 index loads (left in flight)
-      uint32_t tor_n = 0;
-      if (has_next) {
-        if (m < 27) nxt.tstart[m] = ts_nxt;
-        tile_ballots(nxt.tm, mk_nxt);
-        producer_bar();
-        tor_n = tile_or(nxt.tm);
-        issue_row_loads(nxt, a.in_idx, mk_nxt, ps);
+
+    // Builds the row table of tile t in tab: segment bounds (prefetched in
+    // sa/se by threads 0..26), offsets present, rows reset to "absent", then
+    // the segment loads of this thread's half of the offsets (left in flight).
+    uint32_t sa = 0, se = 0;
+    int pv[kHalfOffsets], qv[kHalfOffsets];
+    uint32_t vmask = 0;
+    auto table_begin = [&](TileTable& tab, int64_t t) {
+      if (pt < 27) {
+        tab.tstart[pt] = sa;
+        tab.tend[pt] = se;
       }
-      // (b) prefetch the masks of the tile after next
-      mk_nxt = load_mask(a, t + 2 * G, m);
-      ts_nxt = load_tstart(a, t + 2 * G, m);
-      // (c) gathers of this tile: 8 pieces (K = 64) per stage
-      const int nst = (total + 7) >> 3;
-      int slot = 0, cb = 0, g = 0;  // running piece -> (offset slot, channel block)
-      for (int k = 0; k < nst; ++k, ++kg) {
-        const int sb = (int)(kg % S);
-        if (kg >= S) mbar_wait(smem_u32(&h.empty[sb]), (uint32_t)((kg / S - 1) & 1), a.status);
-        const uint32_t sA = smem_u32(sbase + (size_t)sb * a.stage_bytes);
-        int64_t boff[8];  // per piece: element offset of its weight row block (non-resident B)
+      if (warp == 0) {
+        const uint32_t tor = __ballot_sync(0xffffffffu, pt < 27 && se > sa);
+        if (pt < 27 && ((tor >> pt) & 1u)) tab.slot_s[__popc(tor & ((1u << pt) - 1u))] = pt;
+        if (pt == 0) tab.tor = tor;
+      }
+      producer_bar();
+      const uint32_t tor = tab.tor;
+      const int ns = __popc(tor);
+      for (int k = hf; k < ns; k += 2) tab.rowp[k][m] = -1;
+      vmask = 0;
 #pragma unroll
-        for (int pc = 0; pc < 8; ++pc) {
-          const void* src = a.x;
-          uint32_t bytes = 0;
-          boff[pc] = -1;
-          if (g < total) {
-            const int p = cur.rowp[slot][m];
-            if (p >= 0) {
-              src = a.x + (int64_t)p * a.cin + cb * 8;
-              bytes = 16;
-            }
-            boff[pc] = (int64_t)cur.slot_s[slot] * a.cout * a.cin + cb * 8;
+      for (int j = 0; j < kHalfOffsets; ++j) {
+        const int s = s_lo + j;
+        uint32_t e = 0;
+        if (s < s_hi) {
+          const uint32_t b0 = tab.tstart[s], b1 = tab.tend[s];
+          if (b0 + (uint32_t)m < b1) {
+            e = b0 + (uint32_t)m;
+            vmask |= 1u << j;
+          }
+        }
+        pv[j] = __ldg(gin + e);
+        qv[j] = __ldg(gout + e);
+      }
+      (void)t;
+    };
+    // Scatters the loaded pairs into the row table (after every thread's reset).
+    auto table_end = [&](TileTable& tab, int64_t t) {
+      const uint32_t tor = tab.tor;
+      const int64_t q0 = t * kRows;
+#pragma unroll
+      for (int j = 0; j < kHalfOffsets; ++j) {
+        if ((vmask >> j) & 1u) {
+          const int s = s_lo + j;
+          tab.rowp[__popc(tor & ((1u << s) - 1u))][qv[j] - q0] = pv[j];
+        }
+      }
+    };
+
+    int64_t t = blockIdx.x;
+    load_segment(gts, ntiles, t, pt, sa, se);
+    table_begin(h.tab[0], t);
+    producer_bar();
+    table_end(h.tab[0], t);
+    int total = __popc(h.tab[0].tor) * ppo;
+    load_segment(gts, ntiles, t + G, pt, sa, se);
+    producer_bar();
+    if (pt == 0 && t < ntiles) publish_info(h, status, 0, h.tab[0], total);
+    for (int i = 0; t < ntiles; t += G, ++i) {
+      const int b = i & 1, nb = b ^ 1;
+      const bool has_next = (t + G) < ntiles;
+      const TileTable& cur = h.tab[b];
+      // (a) next tile: segment bounds, reset and loads (left in flight)
+      if (has_next) table_begin(h.tab[nb], t + G);
+      // (b) prefetch the segment bounds of the tile after next
+      load_segment(gts, ntiles, t + 2 * G, pt, sa, se);
+      // (c) gathers of this tile: 8 pieces (K = 64) per stage; this thread
+      // takes pieces 4*hf .. 4*hf+3 of its row
+      const int64_t kg_tile0 = kg;
+      const int nst = (total + 7) >> 3;
+      for (int k = 0; k < nst; ++k, ++kg) {
+        const int sb = ring_sb;
+        if (kg >= S) mbar_wait(smem_u32(&h.empty[sb]), ring_ph ^ 1u, status);
+        if (++ring_sb == S) {
+          ring_sb = 0;
+          ring_ph ^= 1u;
+        }
+        const uint32_t sA = smem_u32(sbase + (size_t)sb * sbytes);
+        const int g0 = 8 * k + 4 * hf;
+        int slot = g0 / ppo, cb = g0 - slot * ppo;
+        int pr[4], cbv[4], sv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          pr[u] = -1;
+          sv[u] = -1;
+          cbv[u] = cb;
+          if (g0 + u < total) {
+            pr[u] = cur.rowp[slot][m];
+            sv[u] = cur.slot_s[slot];
             if (++cb == ppo) {
               cb = 0;
               ++slot;
             }
-            ++g;
           }
-          cp_async16(sA + (m >> 3) * 1024 + (m & 7) * 128 + ((pc ^ (m & 7)) << 4), src, bytes);
         }
-        if (!a.w_resident) {
-          const uint32_t sB = sA + kATileBytes;
-          for (int n = m; n < a.cout; n += kProducerWarps * 32) {
 #pragma unroll
-            for (int pc = 0; pc < 8; ++pc) {
-              const bool real = boff[pc] >= 0;
+        for (int u = 0; u < 4; ++u) {
+          const int pc = 4 * hf + u;
+          const bool ok = pr[u] >= 0;
+          cp_async16(sA + (m >> 3) * 1024 + (m & 7) * 128 + ((pc ^ (m & 7)) << 4),
+                     ok ? (const void*)(gx + (int64_t)pr[u] * cin + cbv[u] * 8) : (const void*)gx, ok ? 16u : 0u);
+        }
+        if (!wres) {
+          const uint32_t sB = sA + kATileBytes;
+          for (int n = m; n < cout; n += kRows) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int pc = 4 * hf + u;
+              const bool ok = sv[u] >= 0;
               cp_async16(sB + (n >> 3) * 1024 + (n & 7) * 128 + ((pc ^ (n & 7)) << 4),
-                         real ? (const void*)(a.wt + boff[pc] + (int64_t)n * a.cin) : (const void*)a.wt,
-                         real ? 16u : 0u);
+                         ok ? (const void*)(gwt + ((int64_t)sv[u] * cout + n) * cin + cbv[u] * 8) : (const void*)gwt,
+                         ok ? 16u : 0u);
             }
           }
         }
@@ -475,34 +512,40 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tc(const __grid_c
         if (kg - signaled >= L) {
           cp_async_wait_n(L);
           fence_proxy_async();
-          mbar_arrive(smem_u32(&h.full[signaled % S]));
+          mbar_arrive(smem_u32(&h.full[sig_sb]));
+          if (++sig_sb == S) sig_sb = 0;
           ++signaled;
         }
       }
       kg_end[i & (kInfoRing - 1)] = kg;
-      // (d) next tile: row table and its info.  The info slot of tile i+1 is
-      // freed by the epilogue of tile i+1-kInfoRing, which needs every stage
-      // of that tile signaled: flush stages still held back by the lag.
+      // (d) next tile: scatter its rows; publish its info.  The info slot of
+      // tile i+1 is freed by the epilogue of tile i+1-kInfoRing, which needs
+      // every stage of that tile signaled: flush stages held back by the lag.
       if (has_next) {
         const int j = i + 1;
         if (j >= kInfoRing && signaled < kg_end[(j - kInfoRing) & (kInfoRing - 1)]) {
           cp_async_wait_n(0);
           fence_proxy_async();
           while (signaled < kg) {
-            mbar_arrive(smem_u32(&h.full[signaled % S]));
+            mbar_arrive(smem_u32(&h.full[sig_sb]));
+            if (++sig_sb == S) sig_sb = 0;
             ++signaled;
           }
         }
-        store_rows(nxt, tor_n, ps);
-        total = __popc(tor_n) * ppo;
-        if (m == 0) publish_info(h, a, j, tor_n, total);
+        producer_bar();  // every thread has reset its rows of the next table
+        table_end(h.tab[nb], t + G);
+        total = __popc(h.tab[nb].tor) * ppo;
+        producer_bar();
+        if (pt == 0) publish_info(h, status, j, h.tab[nb], total);
       }
-      producer_bar();  // tables of the next tile complete; this tile's no longer read
+      (void)kg_tile0;
+      producer_bar();  // this tile's table is no longer read
     }
     cp_async_wait_n(0);
     fence_proxy_async();
     while (signaled < kg) {
-      mbar_arrive(smem_u32(&h.full[signaled % S]));
+      mbar_arrive(smem_u32(&h.full[sig_sb]));
+      if (++sig_sb == S) sig_sb = 0;
       ++signaled;
     }
   } else if (warp == kMmaWarp) {
@@ -512,27 +555,34 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tc(const __grid_c
       const uint32_t wsm = smem_u32(wbase);
       const uint32_t wblk = (uint32_t)a.cout * 16u;  // bytes per resident weight block
       const uint32_t zero_blk = wsm + (uint32_t)(27 * ppo) * wblk;
-      int64_t kg = 0;
+      const int wres = a.w_resident, sbytes = a.stage_bytes;
+      uint32_t* const status = a.status;
+      int m_sb = 0;
+      uint32_t m_ph = 0;
       int i = 0;
-      for (int64_t t = blockIdx.x; t < a.ntiles; t += G, ++i) {
+      for (int64_t t = blockIdx.x; t < ntiles; t += G, ++i) {
         const int r = i & (kInfoRing - 1), b = i & 1;
-        mbar_wait(smem_u32(&h.tinfo_full[r]), (uint32_t)((i / kInfoRing) & 1), a.status);
+        mbar_wait(smem_u32(&h.tinfo_full[r]), (uint32_t)((i / kInfoRing) & 1), status);
         const TileInfo& inf = h.info[r];
         const int nst = *(volatile const int*)&inf.nst;
         const int npieces = *(volatile const int*)&inf.npieces;
-        if (i >= 2) mbar_wait(smem_u32(&h.acc_empty[b]), (uint32_t)(((i >> 1) - 1) & 1), a.status);
+        if (i >= 2) mbar_wait(smem_u32(&h.acc_empty[b]), (uint32_t)(((i >> 1) - 1) & 1), status);
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)b * acc_cols;
         int slot = 0, cb = 0, g = 0;  // running piece -> (offset slot, channel block)
-        for (int k = 0; k < nst; ++k, ++kg) {
-          const int sb = (int)(kg % S);
-          mbar_wait(smem_u32(&h.full[sb]), (uint32_t)((kg / S) & 1), a.status);
+        for (int k = 0; k < nst; ++k) {
+          const int sb = m_sb;
+          mbar_wait(smem_u32(&h.full[sb]), m_ph, status);
+          if (++m_sb == S) {
+            m_sb = 0;
+            m_ph ^= 1u;
+          }
           tc_fence_after();
-          const uint32_t sA = smem_u32(sbase + (size_t)sb * a.stage_bytes);
+          const uint32_t sA = smem_u32(sbase + (size_t)sb * sbytes);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             uint64_t bdesc;
-            if (a.w_resident) {
+            if (wres) {
               // the MMA's two 8-channel pieces: resident blocks (offset, channel
               // block), or the zero block past the real pieces; LBO spans them
               uint32_t addr[2];
@@ -565,15 +615,18 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tc(const __grid_c
     // ---------------- epilogue: TMEM -> registers -> global (row per thread)
     const int quarter = warp & 3;  // TMEM lane quarter this warp may access
     const int m = quarter * 32 + lane;
+    const int cout = a.cout, out_bf16 = a.out_bf16;
+    const int64_t n_out = a.n_out;
+    uint32_t* const status = a.status;
     int i = 0;
-    for (int64_t t = blockIdx.x; t < a.ntiles; t += G, ++i) {
+    for (int64_t t = blockIdx.x; t < ntiles; t += G, ++i) {
       const int b = i & 1, r = i & (kInfoRing - 1);
-      mbar_wait(smem_u32(&h.acc_full[b]), (uint32_t)((i >> 1) & 1), a.status);
+      mbar_wait(smem_u32(&h.acc_full[b]), (uint32_t)((i >> 1) & 1), status);
       tc_fence_after();
       const int nst = *(volatile int*)&h.info[r].nst;
       const int64_t q = t * kRows + m;
       const uint32_t trow = tmem + (uint32_t)b * acc_cols + ((uint32_t)(quarter * 32) << 16);
-      for (int c = 0; c < a.cout; c += 16) {
+      for (int c = 0; c < cout; c += 16) {
         uint32_t v[16];
         if (nst > 0) {
           tmem_ld16(trow + (uint32_t)c, v);
@@ -581,7 +634,7 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tc(const __grid_c
 #pragma unroll
           for (int e = 0; e < 16; ++e) v[e] = 0u;
         }
-        if (q < a.n_out && a.out_bf16) {
+        if (q < n_out && out_bf16) {
           uint4 v0, v1;
           v0.x = pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1]));
           v0.y = pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3]));
@@ -591,11 +644,11 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tc(const __grid_c
           v1.y = pack_bf16x2(__uint_as_float(v[10]), __uint_as_float(v[11]));
           v1.z = pack_bf16x2(__uint_as_float(v[12]), __uint_as_float(v[13]));
           v1.w = pack_bf16x2(__uint_as_float(v[14]), __uint_as_float(v[15]));
-          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.y) + q * a.cout + c);
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.y) + q * cout + c);
           dst[0] = v0;
           dst[1] = v1;
-        } else if (q < a.n_out) {
-          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<float*>(a.y) + q * a.cout + c);
+        } else if (q < n_out) {
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<float*>(a.y) + q * cout + c);
 #pragma unroll
           for (int e = 0; e < 4; ++e) dst[e] = make_uint4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
         }
@@ -686,8 +739,8 @@ extern "C" fvx_status fvx_sparse_conv(fvx_grid gin, fvx_grid gout, fvx_kmap m, f
   ConvArgs a;
   a.x = (const __nv_bfloat16*)feats;
   a.wt = wt;
-  a.mask = m->out_mask;
   a.in_idx = m->in_idx;
+  a.out_idx = m->out_idx;
   a.tile_start = m->tile_start;
   a.y = out;
   a.out_bf16 = (dt == FVX_BF16_OUT_BF16) ? 1 : 0;
@@ -711,7 +764,7 @@ extern "C" fvx_status fvx_sparse_conv(fvx_grid gin, fvx_grid gout, fvx_kmap m, f
     set_error("fvx_sparse_conv: cout %lld leaves fewer than 3 pipeline stages", (long long)cout);
     return FVX_ERR_INVALID_ARG;
   }
-  a.lag = std::min(a.stages - 2, 10);
+  a.lag = std::min(a.stages - 2, 4);
   int cols = 32;
   while (cols < cout) cols <<= 1;
   a.tmem_cols = cols;  // per accumulator; two accumulators per CTA (<= 512 columns)
