@@ -180,6 +180,31 @@ fvx_status fvx_kmap_view(fvx_kmap m, const int64_t** offsets_host, const int32_t
 fvx_status fvx_sparse_conv(fvx_grid gin, fvx_grid gout, fvx_kmap m, fvx_dtype dt, const void* feats, int64_t cin,
                            const void* W, int64_t cout, void* out, fvx_stream stream);
 
+/* Sparse convolution that allocates no device memory.
+ *
+ * The pages have no counterpart: this entry point exists for callers that
+ * cannot allocate device memory while they run — for example an inference
+ * runtime whose device memory is planned and reserved once at load time, or a
+ * host process whose allocator forbids new device allocations after start-up.
+ * Same arguments, result and errors as fvx_sparse_conv (inputs and outputs
+ * are still the caller's); its only scratch (the transposed weights and the
+ * bounded-wait status word) lives in a fixed array of 2 MiB + 256 bytes in the
+ * library's device image, which every GPU that loads the library holds until
+ * the process exits.  It calls no cudaMalloc, cudaFree or other allocating
+ * routine.
+ *   - Limit: 27 * cin * cout * 2 bytes <= 2 MiB (cin * cout <= 38836), else
+ *     FVX_ERR_RANGE; FVX_F32 needs no scratch and has no such limit.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call shares the one array and the call clears what must start at
+ *     zero: calls that overlap on the GPU (other streams, other threads) race;
+ *     order them on one stream.
+ *   - A bounded device-side wait that gives up is recorded in that array's
+ *     status word, which fvx_device_status does not read. */
+fvx_status fvx_sparse_conv_noalloc(fvx_grid gin, fvx_grid gout, fvx_kmap m, fvx_dtype dt, const void* feats,
+                                   int64_t cin, const void* W, int64_t cout, void* out, fvx_stream stream);
+
 fvx_status fvx_grid_destroy(fvx_grid g);
 fvx_status fvx_kmap_destroy(fvx_kmap m);
 

@@ -63,6 +63,7 @@ def load():
         "fvx_kernel_map": ([P, P, I32, I32, P, PP], I32),
         "fvx_kmap_view": ([P, PP, PP, PP, PP, P, P], I32),
         "fvx_sparse_conv": ([P, P, P, I32, P, I64, P, I64, P, P], I32),
+        "fvx_sparse_conv_noalloc": ([P, P, P, I32, P, I64, P, I64, P, P], I32),
         "fvx_grid_destroy": ([P], I32),
         "fvx_kmap_destroy": ([P], I32),
         "fvx_status_string": ([I32], ctypes.c_char_p),

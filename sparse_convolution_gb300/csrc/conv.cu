@@ -30,6 +30,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "block_scan.cuh"
 #include "fvx_internal.cuh"
@@ -768,6 +769,141 @@ extern "C" fvx_status fvx_sparse_conv(fvx_grid gin, fvx_grid gout, fvx_kmap m, f
   int cols = 32;
   while (cols < cout) cols <<= 1;
   a.tmem_cols = cols;  // per accumulator; two accumulators per CTA (<= 512 columns)
+  const size_t smem = 1024 + (size_t)a.w_bytes + (size_t)a.stages * a.stage_bytes + sizeof(ConvSmemHead);
+  FVX_CUDA(cudaFuncSetAttribute(k_conv_bf16_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  int dev = 0, sms = 0;
+  FVX_CUDA(cudaGetDevice(&dev));
+  FVX_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  const int64_t grid = std::min<int64_t>(nt, (int64_t)sms);
+  {
+    LaunchScope ls("conv_bf16_tc", s);
+    k_conv_bf16_tc<<<(unsigned)grid, kConvThreads, smem, s>>>(a);
+  }
+  return check_launch("conv_bf16_tc");
+}
+
+// ============================================================== no-allocation variant
+// Scratch of fvx_sparse_conv_noalloc: a fixed array in the library's device
+// image, so the call never allocates.  Every GPU that loads the library holds
+// it until the process exits.  Layout: [status word, 256 bytes][transposed
+// bf16 weights, up to kNoAllocWtBytes].
+namespace {
+constexpr size_t kNoAllocWtBytes = (size_t)2 << 20;
+constexpr size_t kNoAllocBytes = 256 + kNoAllocWtBytes;
+}  // namespace
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+namespace {
+// Device address of g_noalloc_scratch on the current device (the host-side
+// name is only a stand-in; the kernel needs this address).  Looked up once per
+// device, with that device current.
+fvx_status noalloc_scratch(unsigned char** out) {
+  static unsigned char* addr[64] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  FVX_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) {
+    set_error("fvx_sparse_conv_noalloc: device ordinal %d out of range", dev);
+    return FVX_ERR_RANGE;
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    FVX_CUDA(cudaGetSymbolAddress(&p, g_noalloc_scratch));
+    addr[dev] = (unsigned char*)p;
+  }
+  *out = addr[dev];
+  return FVX_OK;
+}
+}  // namespace
+
+extern "C" fvx_status fvx_sparse_conv_noalloc(fvx_grid gin, fvx_grid gout, fvx_kmap m, fvx_dtype dt,
+                                              const void* feats, int64_t cin, const void* W, int64_t cout, void* out,
+                                              fvx_stream stream) {
+  if (!gin || !gout || !m || !W || !out || (gin->n_active > 0 && !feats)) {
+    set_error("fvx_sparse_conv_noalloc: NULL argument");
+    return FVX_ERR_INVALID_ARG;
+  }
+  if (m->gin != gin || m->gout != gout) {
+    set_error("fvx_sparse_conv_noalloc: kernel map was built for other grids");
+    return FVX_ERR_INVALID_ARG;
+  }
+  if (cin < 1 || cout < 1) {
+    set_error("fvx_sparse_conv_noalloc: cin and cout must be >= 1");
+    return FVX_ERR_INVALID_ARG;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  const int64_t nt = m->n_tiles;
+  if (dt == FVX_F32) {  // the fp32 kernel needs no scratch at all
+    if (gout->n_active == 0) return FVX_OK;
+    {
+      LaunchScope ls("conv_f32", s);
+      k_conv_f32<<<(unsigned)nt, kRows, 0, s>>>((const float*)feats, (const float*)W, m->out_mask, m->in_idx,
+                                                m->tile_start, nt, m->n_out, (int)cin, (int)cout, (float*)out);
+    }
+    return check_launch("conv_f32");
+  }
+  if (dt != FVX_BF16 && dt != FVX_BF16_OUT_BF16) {
+    set_error("fvx_sparse_conv_noalloc: unknown dtype %d", (int)dt);
+    return FVX_ERR_INVALID_ARG;
+  }
+  if (cin % 8 != 0 || cout % 16 != 0 || cin > 512 || cout > 256) {
+    set_error("fvx_sparse_conv_noalloc: bf16 needs cin %% 8 == 0 (<= 512) and cout %% 16 == 0 (<= 256); got %lld, %lld",
+              (long long)cin, (long long)cout);
+    return FVX_ERR_INVALID_ARG;
+  }
+  const size_t wt_bytes = (size_t)27 * (size_t)cin * (size_t)cout * 2;
+  if (wt_bytes > kNoAllocWtBytes) {
+    set_error("fvx_sparse_conv_noalloc: 27*cin*cout*2 = %zu bytes of weights exceed the fixed %zu-byte scratch "
+              "(cin*cout must be <= %zu); use fvx_sparse_conv",
+              wt_bytes, kNoAllocWtBytes, kNoAllocWtBytes / 54);
+    return FVX_ERR_RANGE;
+  }
+  if (((uintptr_t)feats | (uintptr_t)out) & 15u) {
+    set_error("fvx_sparse_conv_noalloc: feats and out must be 16-byte aligned");
+    return FVX_ERR_INVALID_ARG;
+  }
+  unsigned char* scratch = nullptr;
+  FVX_TRY(noalloc_scratch(&scratch));
+  if (gout->n_active == 0) return FVX_OK;
+  uint32_t* status = reinterpret_cast<uint32_t*>(scratch);
+  __nv_bfloat16* wt = reinterpret_cast<__nv_bfloat16*>(scratch + 256);
+  FVX_CUDA(cudaMemsetAsync(status, 0, 4, s));  // the array keeps the previous call's contents
+  {
+    LaunchScope ls("conv_transpose_w", s);
+    const int64_t n = 27 * cin * cout;
+    k_transpose_w<<<(unsigned)((n + 255) / 256), 256, 0, s>>>((const __nv_bfloat16*)W, (int)cin, (int)cout, wt);
+  }
+  FVX_TRY(check_launch("conv_transpose_w"));
+
+  ConvArgs a;
+  a.x = (const __nv_bfloat16*)feats;
+  a.wt = wt;
+  a.in_idx = m->in_idx;
+  a.out_idx = m->out_idx;
+  a.tile_start = m->tile_start;
+  a.y = out;
+  a.out_bf16 = (dt == FVX_BF16_OUT_BF16) ? 1 : 0;
+  a.status = status;
+  a.ntiles = nt;
+  a.n_out = m->n_out;
+  a.cin = (int)cin;
+  a.cout = (int)cout;
+  const int64_t wres = (27 * (cin / 8) + 1) * cout * 16;
+  a.w_resident = (wres <= kResidentWBytes) ? 1 : 0;
+  a.w_bytes = a.w_resident ? (int)((wres + 1023) & ~(int64_t)1023) : 0;
+  a.stage_bytes = kATileBytes + (a.w_resident ? 0 : (int)cout * 128);
+  const int head = (int)sizeof(ConvSmemHead) + 1024;
+  a.stages = (224 * 1024 - head - a.w_bytes) / a.stage_bytes;
+  if (a.stages > kMaxStages) a.stages = kMaxStages;
+  if (a.stages < 3) {
+    set_error("fvx_sparse_conv_noalloc: cout %lld leaves fewer than 3 pipeline stages", (long long)cout);
+    return FVX_ERR_INVALID_ARG;
+  }
+  a.lag = std::min(a.stages - 2, 4);
+  int cols = 32;
+  while (cols < cout) cols <<= 1;
+  a.tmem_cols = cols;
   const size_t smem = 1024 + (size_t)a.w_bytes + (size_t)a.stages * a.stage_bytes + sizeof(ConvSmemHead);
   FVX_CUDA(cudaFuncSetAttribute(k_conv_bf16_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   int dev = 0, sms = 0;
