@@ -291,9 +291,9 @@ def bench_fvx(args, world, rank, local):
     # roofline of the profiled kernel
     peaks, peak_kind = measured_peaks()
     if prof_kernel == "conv_bf16_tc":
-        # feats read once, fp32 output written once, weights, one int32 input
-        # index per pair and one 27-bit mask per output
-        alg_bytes = U * cv["cin"] * 2 + U * cv["cout"] * 4 + 27 * cv["cin"] * cv["cout"] * 2 + 4 * npairs + 4 * U
+        # feats read once, fp32 output written once, weights once, and the
+        # kernel map's (in, out) int32 pair read once
+        alg_bytes = U * cv["cin"] * 2 + U * cv["cout"] * 4 + 27 * cv["cin"] * cv["cout"] * 2 + 8 * npairs
     else:
         alg_bytes = None
     avg_ms = prof_ms / max(prof_n, 1)
