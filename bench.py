@@ -170,8 +170,11 @@ def make_workload(name):
 
 def oracle_sample(w, target_rows=250_000):
     """A spatially contiguous crop of the workload (first batch, lowest i)
-    with about target_rows rows: same density and structure, bounded CPU work."""
+    with about target_rows rows (fewer for wide convs, whose fp64 oracle cost
+    grows with cin*cout): same density and structure, bounded CPU work."""
     coords, offs = w["coords"], w["batch_offsets"]
+    width = sum(c["cin"] * c["cout"] for c in w["convs"])
+    target_rows = max(2000, int(target_rows * min(1.0, 2048.0 / width)))
     c = coords[offs[0]:offs[1]]
     if c.shape[0] <= target_rows:
         return c, np.array([0, c.shape[0]], np.int64), "whole first batch element"
@@ -180,23 +183,28 @@ def oracle_sample(w, target_rows=250_000):
     return sel, np.array([0, sel.shape[0]], np.int64), f"crop i < {int(cut)} of batch 0 ({sel.shape[0]} rows)"
 
 
-def run_oracle_step(coords, offs, cv, seed):
+def run_oracle_step(coords, offs, convs, seed):
+    """The oracle's pass over one input: build, then per conv of the workload
+    (coarsen for stride 2) kernel map and conv, each conv reading the last."""
     import oracle
     from sparse_convolution_gb300 import synth
 
     g = oracle.Grid.build(coords, offs)
-    km = oracle.KernelMap(g, g, 1)
-    x = synth.features(seed, g.n_active, cv["cin"])
-    W = synth.weights(seed + 1, cv["cin"], cv["cout"])
-    oracle.conv(km, x.astype(np.float64), W.astype(np.float64))
+    x = synth.features(seed, g.n_active, convs[0]["cin"]).astype(np.float64)
+    gin = g
+    for i, c in enumerate(convs):
+        gout = gin if c["stride"] == 1 else gin.coarsen(c["stride"])
+        km = oracle.KernelMap(gin, gout, c["stride"])
+        W = synth.weights(seed + 1 + i, c["cin"], c["cout"]).astype(np.float64)
+        x, _ = oracle.conv(km, x, W)
+        gin = gout
     return g.n_active
 
 
 def cpu_baseline(w, budget_s=20.0):
     coords, offs, desc = oracle_sample(w)
-    cv = w["convs"][0]
     t0 = time.perf_counter()
-    n = run_oracle_step(coords, offs, cv, 1)
+    n = run_oracle_step(coords, offs, w["convs"], 1)
     dt = time.perf_counter() - t0
     return dict(value=n / dt / 1e6, unit=UNIT, cores=1, kind="oracle",
                 sample=f"{desc}: build+kmap+conv of {n} voxels, single-threaded, {dt:.1f} s",
@@ -209,58 +217,106 @@ def bench_fvx(args, world, rank, local):
 
     from sparse_convolution_gb300 import build_lib
     import sparse_convolution_gb300 as fvx
+    from sparse_convolution_gb300 import synth
 
     torch.cuda.set_device(local)
     build_lib.build()
     fvx.load()
     w = make_workload(args.workload)
-    cv = w["convs"][0]
-    assert cv["stride"] == 1 and w["dtype"] == "bf16"
+    convs = w["convs"]
+    fp32 = w["dtype"] == "f32"
+    dev = torch.device("cuda", local)
     coords_h = torch.from_numpy(w["coords"]).pin_memory()
     offs = w["batch_offsets"]
-    U = int(np.sum(w["n_unique"])) if w["n_unique"] is not None else None
-    from sparse_convolution_gb300 import synth
-
-    dev = torch.device("cuda", local)
     coords = coords_h.to(dev)
-    # feature rows follow the active-voxel index order; values are i.i.d. so any order is a valid input
     g0 = fvx.Grid.build(coords, offs)
     U = g0.n_active
+    n_out = [U]
+    if len(convs) > 1:
+        gc0 = g0.coarsen(2)
+        n_out.append(gc0.n_active)
+        gc0.destroy()
     g0.destroy()
-    x_h = torch.from_numpy(synth.features(w["seed"] + 10, U, cv["cin"])).bfloat16().pin_memory()
-    W_h = torch.from_numpy(synth.weights(w["seed"] + 20, cv["cin"], cv["cout"])).bfloat16().pin_memory()
+    # feature rows follow the active-voxel index order; values are i.i.d., so any order is a valid input
+    fdt = torch.float32 if fp32 else torch.bfloat16
+    x_h = torch.from_numpy(synth.features(w["seed"] + 10, U, convs[0]["cin"], w["feat_kind"])).to(fdt).pin_memory()
+    W_h = [torch.from_numpy(synth.weights(w["seed"] + 20 + i, c["cin"], c["cout"])).to(fdt).pin_memory()
+           for i, c in enumerate(convs)]
     x = x_h.to(dev)
-    W = W_h.to(dev)
-    # bf16 operands, fp32 accumulation and fp32 output (the mode whose error
-    # meets 2e-3 * sum|w*x|; a bf16 output would add a 2^-8 |y| rounding)
-    y = torch.empty((U, cv["cout"]), dtype=torch.float32, device=dev)
+    Ws = [t.to(dev) for t in W_h]
+    # outputs: fp32 (bf16 operands, fp32 accumulation: the mode whose error meets
+    # 2e-3 * sum|w*x|); a conv that feeds the next one writes bf16
+    ys = []
+    for i, c in enumerate(convs):
+        odt = torch.float32 if (fp32 or i == len(convs) - 1) else torch.bfloat16
+        ys.append(torch.empty((n_out[i], c["cout"]), dtype=odt, device=dev))
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
-    def step(ev=None):
-        if ev:
-            ev[0].record(stream)
-        g = fvx.Grid.build(coords, offs)
-        if ev:
-            ev[1].record(stream)
-        km = fvx.KernelMap(g, g, 1)
-        if ev:
-            ev[2].record(stream)
-        fvx.sparse_conv(g, g, km, x, W, out=y)
-        if ev:
-            ev[3].record(stream)
-        return g, km
+    def step(rec, coords_in, x_in, W_in):
+        """One pass of the path.  rec(category) brackets each call with events."""
+        handles = []
+        with rec("build"):
+            g = fvx.Grid.build(coords_in, offs)
+        handles.append(g)
+        src, gin, pairs = x_in, g, []
+        for i, c in enumerate(convs):
+            if c["stride"] == 1:
+                gout = gin
+            else:
+                with rec("build"):
+                    gout = gin.coarsen(c["stride"])
+                handles.append(gout)
+            with rec("kmap"):
+                km = fvx.KernelMap(gin, gout, c["stride"])
+            handles.append(km)
+            pairs.append(km.n_pairs)
+            with rec("conv"):
+                fvx.sparse_conv(gin, gout, km, src, W_in[i], out=ys[i])
+            src, gin = ys[i], gout
+        return handles, pairs
+
+    class NoRec:
+        def __call__(self, cat):
+            return self
+
+        def __enter__(self):
+            return self
+
+        def __exit__(self, *a):
+            return False
+
+    class EventRec:
+        def __init__(self):
+            self.marks = []
+
+        def __call__(self, cat):
+            self.cat = cat
+            return self
+
+        def __enter__(self):
+            self.e0 = torch.cuda.Event(enable_timing=True)
+            self.e0.record(stream)
+            return self
+
+        def __exit__(self, *a):
+            e1 = torch.cuda.Event(enable_timing=True)
+            e1.record(stream)
+            self.marks.append((self.cat, self.e0, e1))
+            return False
+
+    def release(handles):
+        for hnd in reversed(handles):
+            hnd.destroy()
 
     for _ in range(args.warmup):
-        g, km = step()
-        npairs = km.n_pairs
-        km.destroy()
-        g.destroy()
+        hs, pairs = step(NoRec(), coords, x, Ws)
+        release(hs)
     torch.cuda.synchronize()
     fvx.device_status()
 
-    prof_kernel = args.profile_kernel or "conv_bf16_tc"
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    prof_kernel = args.profile_kernel or ("conv_f32" if fp32 else "conv_bf16_tc")
+    recs = EventRec()
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -270,9 +326,8 @@ def bench_fvx(args, world, rank, local):
     l0 = fvx.launch_count()
     for k in range(args.steps):
         flush.fill_(float(k))  # evict L2 between steps (outside the step's events)
-        g, km = step(evs[k])
-        km.destroy()
-        g.destroy()
+        hs, pairs = step(recs, coords, x, Ws)
+        release(hs)
     torch.cuda.synchronize()
     launches = fvx.launch_count() - l0
     prof_ms, prof_n = fvx.profile_read()
@@ -280,67 +335,85 @@ def bench_fvx(args, world, rank, local):
     barrier(world)
     clk = clocks.stop()
     fvx.device_status()
-    t_build = sum(e[0].elapsed_time(e[1]) for e in evs) / 1e3
-    t_kmap = sum(e[1].elapsed_time(e[2]) for e in evs) / 1e3
-    t_conv = sum(e[2].elapsed_time(e[3]) for e in evs) / 1e3
-    t_total = max_over_ranks(t_build + t_kmap + t_conv, world)
+    t = {"build": 0.0, "kmap": 0.0, "conv": 0.0}
+    for cat, e0, e1 in recs.marks:
+        t[cat] += e0.elapsed_time(e1) / 1e3
+    t_total = max_over_ranks(sum(t.values()), world)
     K = args.steps
     value = U * K * world / t_total / 1e6
-    flops = 2.0 * cv["cin"] * cv["cout"] * npairs
+    esz = 4 if fp32 else 2
+    flops = sum(2.0 * c["cin"] * c["cout"] * p for c, p in zip(convs, pairs))
+    # algorithmic bytes of the conv launches of one step: feats read once,
+    # output written once (4 B fp32 / 2 B bf16), weights once, and the kernel
+    # map's (in, out) int32 pair read once
+    alg_bytes = 0
+    n_in = U
+    for i, (c, p) in enumerate(zip(convs, pairs)):
+        alg_bytes += n_in * c["cin"] * esz + n_out[i] * c["cout"] * ys[i].element_size() \
+            + 27 * c["cin"] * c["cout"] * esz + 8 * p
+        n_in = n_out[i]
 
-    # roofline of the profiled kernel
+    # roofline of the profiled kernel (all of its launches in the timed region)
     peaks, peak_kind = measured_peaks()
-    if prof_kernel == "conv_bf16_tc":
-        # feats read once, fp32 output written once, weights once, and the
-        # kernel map's (in, out) int32 pair read once
-        alg_bytes = U * cv["cin"] * 2 + U * cv["cout"] * 4 + 27 * cv["cin"] * cv["cout"] * 2 + 8 * npairs
-    else:
-        alg_bytes = None
-    avg_ms = prof_ms / max(prof_n, 1)
     roofline = None
-    if alg_bytes is not None and prof_n:
-        ach = alg_bytes / (avg_ms / 1e3) / 1e9
-        peak = peaks["hbm_gbs"]
-        roofline = dict(bound="hbm", kernel=prof_kernel, achieved=round(ach, 1), peak=peak, unit="GB/s",
-                        frac=round(ach / peak, 4), traffic=profiled_traffic(prof_kernel, w["name"]),
-                        algorithmic_bytes=int(alg_bytes),
-                        avg_launch_ms=round(avg_ms, 5), peak_source=f"{peak_kind} (hbm_gbs)")
+    if prof_n and prof_kernel in ("conv_bf16_tc", "conv_f32"):
+        sec = prof_ms / 1e3
+        per_launch = prof_n / K  # launches of the kernel per step
+        intensity = flops / alg_bytes
+        if fp32:
+            # FFMA: 152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz (max SM clock)
+            peak = 152 * 128 * 2 * 2.07e9 / 1e12
+            roofline = dict(bound="alu", achieved=round(flops * K / sec / 1e12, 3), peak=round(peak, 1),
+                            unit="TFLOP/s", peak_source="derived: 152 SMs x 128 FP32 lanes x 2 x 2.07 GHz")
+        elif intensity > peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9):
+            peak = peaks["bf16_tflops"]
+            roofline = dict(bound="tensor", achieved=round(flops * K / sec / 1e12, 2), peak=peak, unit="TFLOP/s",
+                            peak_source=f"{peak_kind} (bf16_tflops, burst)")
+        else:
+            peak = peaks["hbm_gbs"]
+            roofline = dict(bound="hbm", achieved=round(alg_bytes * K / sec / 1e9, 1), peak=peak, unit="GB/s",
+                            peak_source=f"{peak_kind} (hbm_gbs)")
+        roofline.update(kernel=prof_kernel, frac=round(roofline["achieved"] / roofline["peak"], 4),
+                        traffic=profiled_traffic(prof_kernel, w["name"]) if len(convs) == 1 else None,
+                        algorithmic_bytes=int(alg_bytes / per_launch), flops=int(flops / per_launch),
+                        avg_launch_ms=round(prof_ms / prof_n, 5), launches_per_step=int(per_launch))
 
-    # end to end through the public API with host buffers
-    e2e_evs = []
-    y_h = torch.empty((U, cv["cout"]), dtype=torch.float32).pin_memory()
+    # end to end through the public API with host buffers: copies in, the
+    # path, the last output back to the host, all inside the timed region
+    e2e_t = []
+    y_h = torch.empty(ys[-1].shape, dtype=ys[-1].dtype).pin_memory()
     for k in range(max(2, min(K, 10))):
         flush.fill_(float(k))
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         cd = coords_h.to(dev, non_blocking=True)
         xd = x_h.to(dev, non_blocking=True)
-        Wd = W_h.to(dev, non_blocking=True)
-        g = fvx.Grid.build(cd, offs)
-        km = fvx.KernelMap(g, g, 1)
-        yd = fvx.sparse_conv(g, g, km, xd, Wd)
-        y_h.copy_(yd, non_blocking=True)
+        Wd = [t_.to(dev, non_blocking=True) for t_ in W_h]
+        hs, _ = step(NoRec(), cd, xd, Wd)
+        y_h.copy_(ys[-1], non_blocking=True)
         e1.record(stream)
         torch.cuda.synchronize()
-        e2e_evs.append(e0.elapsed_time(e1) / 1e3)
-        km.destroy()
-        g.destroy()
-    t_e2e = max_over_ranks(sum(e2e_evs), world)
-    e2e = dict(value=round(U * len(e2e_evs) * world / t_e2e / 1e6, 2), unit=UNIT,
-               h2d_bytes_per_step=int(coords_h.numel() * 4 + x_h.numel() * 2 + W_h.numel() * 2),
-               d2h_bytes_per_step=int(y_h.numel() * 4))
+        e2e_t.append(e0.elapsed_time(e1) / 1e3)
+        release(hs)
+    t_e2e = max_over_ranks(sum(e2e_t), world)
+    e2e = dict(value=round(U * len(e2e_t) * world / t_e2e / 1e6, 2), unit=UNIT,
+               h2d_bytes_per_step=int(coords_h.numel() * 4 + x_h.numel() * x_h.element_size()
+                                      + sum(t_.numel() * t_.element_size() for t_ in W_h)),
+               d2h_bytes_per_step=int(y_h.numel() * y_h.element_size()))
 
     out = dict(metric=METRIC, value=round(value, 2), unit=UNIT, n_gpus=world, steps=K, warmup=args.warmup,
                ms_per_step=round(t_total / K * 1e3, 4), higher_is_better=True, scaling="weak",
-               vs_baseline=None, dtype="bf16", data="synthetic",
-               config=dict(workload=w["name"], rows=int(w["coords"].shape[0]), active_voxels=U, pairs=int(npairs),
-                           cin=cv["cin"], cout=cv["cout"], stride=1, batch=int(len(offs) - 1),
+               vs_baseline=None, dtype="f32" if fp32 else "bf16", data="synthetic",
+               config=dict(workload=w["name"], rows=int(w["coords"].shape[0]), active_voxels=U,
+                           pairs=[int(p) for p in pairs],
+                           convs=[f"{c['cin']}->{c['cout']} stride {c['stride']}" for c in convs],
+                           batch=int(len(offs) - 1),
                            l2="flushed between steps (256 MB write outside the step events)",
                            parallelism=f"replicas x{world}"),
-               components=dict(build_kmap_mvoxels_s=round(U * K / (t_build + t_kmap) / 1e6, 2),
-                               conv_active_pair_tflops=round(flops * K / t_conv / 1e12, 4),
-                               build_ms=round(t_build / K * 1e3, 4), kmap_ms=round(t_kmap / K * 1e3, 4),
-                               conv_ms=round(t_conv / K * 1e3, 4)),
+               components=dict(build_kmap_mvoxels_s=round(U * K / (t["build"] + t["kmap"]) / 1e6, 2),
+                               conv_active_pair_tflops=round(flops * K / t["conv"] / 1e12, 4),
+                               build_ms=round(t["build"] / K * 1e3, 4), kmap_ms=round(t["kmap"] / K * 1e3, 4),
+                               conv_ms=round(t["conv"] / K * 1e3, 4)),
                roofline=roofline, e2e=e2e, gpu_launches=int(launches), clocks=clk)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w)
@@ -358,11 +431,11 @@ def bench_reference(args, world, rank):
     coords, offs, desc = oracle_sample(w, target_rows=120_000)
     cv = w["convs"][0]
     for _ in range(args.warmup):
-        run_oracle_step(coords, offs, cv, 1)
+        run_oracle_step(coords, offs, w["convs"], 1)
     times, n = [], 0
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        n = run_oracle_step(coords, offs, cv, 1)
+        n = run_oracle_step(coords, offs, w["convs"], 1)
         times.append(time.perf_counter() - t0)
     tot = sum(times)
     value = n * args.steps / tot / 1e6
@@ -371,7 +444,8 @@ def bench_reference(args, world, rank):
     return dict(impl="reference", metric=METRIC, value=round(value, 4), unit=UNIT, n_gpus=world, steps=args.steps,
                 warmup=args.warmup, ms_per_step=round(tot / args.steps * 1e3, 2), higher_is_better=True,
                 scaling="weak", vs_baseline=None, dtype="f64", data="synthetic",
-                config=dict(workload=w["name"], sample=desc, cin=cv["cin"], cout=cv["cout"], stride=1),
+                config=dict(workload=w["name"], sample=desc,
+                            convs=[f"{c['cin']}->{c['cout']} stride {c['stride']}" for c in w["convs"]]),
                 cpu_baseline=cb, e2e=dict(value=round(value, 4), unit=UNIT, h2d_bytes_per_step=0,
                                           d2h_bytes_per_step=0))
 

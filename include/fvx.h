@@ -180,6 +180,29 @@ fvx_status fvx_kmap_view(fvx_kmap m, const int64_t** offsets_host, const int32_t
 fvx_status fvx_sparse_conv(fvx_grid gin, fvx_grid gout, fvx_kmap m, fvx_dtype dt, const void* feats, int64_t cin,
                            const void* W, int64_t cout, void* out, fvx_stream stream);
 
+/* Which bf16 kernel fvx_sparse_conv and fvx_sparse_conv_noalloc run
+ * [fVDB paper, "Sparse-convolution operators": several convolution backends,
+ * the leaf-densified one for low channel counts on leaves at least 20%
+ * occupied, picked per case].
+ *   FVX_CONV_AUTO    (default) leaf-densified when the map has stride 1,
+ *                    cin <= 16, cout <= 64 and the output grid's leaves are
+ *                    at least 20% occupied on average; pair-list gather
+ *                    otherwise.
+ *   FVX_CONV_GATHER  always the pair-list kernels (128 consecutive outputs
+ *                    per tile; rows fetched by TMA gather4 when cin is a
+ *                    multiple of 16, else by cp.async).
+ *   FVX_CONV_LEAF    always leaf-densified (each output leaf's 10^3 input
+ *                    window staged densely in shared memory; the pair lists
+ *                    are not read); a call it cannot serve (stride 2,
+ *                    cin > 16, cout > 64) fails with FVX_ERR_INVALID_ARG.
+ * Process-wide; FVX_F32 is unaffected.  Every path meets the same error
+ * bound.  Errors: FVX_ERR_INVALID_ARG for an unknown value. */
+typedef enum { FVX_CONV_AUTO = 0, FVX_CONV_GATHER = 1, FVX_CONV_LEAF = 2 } fvx_conv_algo;
+fvx_status fvx_set_conv_algo(fvx_conv_algo algo);
+/* The kernel family the last successful bf16 convolution on this host thread
+ * launched (FVX_CONV_GATHER or FVX_CONV_LEAF; FVX_CONV_AUTO before any). */
+fvx_conv_algo fvx_last_conv_algo(void);
+
 /* Sparse convolution that allocates no device memory.
  *
  * The pages have no counterpart: this entry point exists for callers that

@@ -24,6 +24,7 @@ LIB_PATH = os.path.join(_HERE, "libfvx.so")
 _lib = None
 
 FVX_F32, FVX_BF16, FVX_BF16_OUT_BF16 = 0, 1, 2
+FVX_CONV_AUTO, FVX_CONV_GATHER, FVX_CONV_LEAF = 0, 1, 2
 
 
 class FvxError(RuntimeError):
@@ -72,6 +73,8 @@ def load():
         "fvx_launch_count": ([], U64),
         "fvx_profile_enable": ([ctypes.c_char_p], I32),
         "fvx_profile_read": ([P, P], I32),
+        "fvx_set_conv_algo": ([I32], I32),
+        "fvx_last_conv_algo": ([], I32),
     }
     for name, (args, res) in sigs.items():
         f = getattr(lib, name)
@@ -263,6 +266,18 @@ def sparse_conv(gin: Grid, gout: Grid, kmap: KernelMap, feats, W, out=None, out_
 
 def device_status(stream=None):
     _check(load().fvx_device_status(_stream(stream)))
+
+
+def set_conv_algo(algo: int) -> None:
+    """FVX_CONV_AUTO (default), FVX_CONV_GATHER or FVX_CONV_LEAF: which bf16
+    convolution kernel family sparse_conv runs (process-wide)."""
+    _check(load().fvx_set_conv_algo(int(algo)))
+
+
+def last_conv_algo() -> int:
+    """FVX_CONV_GATHER or FVX_CONV_LEAF: what the last bf16 convolution on this
+    thread ran (FVX_CONV_AUTO before any)."""
+    return int(load().fvx_last_conv_algo())
 
 
 def launch_count() -> int:

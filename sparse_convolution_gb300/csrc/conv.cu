@@ -25,11 +25,13 @@
 //     warps drain a double-buffered TMEM accumulator with tcgen05.ld while the
 //     next tile accumulates.  Output fp32, or bf16 rounded to nearest even.
 //   * fp32: exact FFMA on CUDA cores (no TF32).
+#include <cuda.h>  // tensor map types only; the encoder comes from the driver at run time
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "block_scan.cuh"
@@ -177,6 +179,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
   }
 }
 
+// Bounded wait that ignores the status word: used only to let copies in
+// flight land before a block exits.
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t it = 0; !mbar_try(bar, parity); ++it)
+    if ((it & 1023u) == 1023u && globaltimer() - t0 > kWaitNs) return;
+}
+
 // cp.async of 16 bytes (src_bytes 0: zero fill).  No "memory" clobber: the
 // copy only writes the stage buffer, which this thread does not read, and
 // volatile asm statements keep their order (commit / wait below).
@@ -214,6 +224,34 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
 __device__ __forceinline__ uint64_t sdesc_plain(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46);
+}
+// K-major with a 32/64/128-byte swizzle (layout type 6/4/2): rows of `row`
+// bytes, 8-row groups 8*row bytes apart (SBO).
+__device__ __forceinline__ uint64_t sdesc_swz(uint32_t saddr, uint32_t layout, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)layout << 61);
+}
+
+// TMA: 4 rows (row indices r0..r3, column col) of a 2-D tensor into shared
+// memory; rows outside the tensor read as zeros.  Completion is counted in
+// bytes on the mbarrier.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int col, int4 rows, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+      "%4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(tmap), "r"(col), "r"(rows.x), "r"(rows.y), "r"(rows.z), "r"(rows.w), "r"(bar)
+      : "memory");
+}
+// TMA: one box of a 2-D tensor at (c0, c1).
+__device__ __forceinline__ void tma_tile2d(uint32_t dst, const void* tmap, int c0, int c1, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(dst),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
 // Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major.
@@ -254,13 +292,17 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 
 // Row table of one tile (double-buffered: producers fill tile i+1's while
 // gathering tile i's).
-struct TileTable {
-  int32_t rowp[27][kRows];  // gathered input row for (offset slot, tile row), -1 = zeros
+struct alignas(16) TileTable {
+  int32_t rowp[27][kRows];  // gathered input row for (offset slot, tile row); -1 (TMA path: n_in) = zeros
   uint32_t tstart[27];      // the tile's segment [tstart, tend) in each list
   uint32_t tend[27];
   int32_t slot_s[27];       // offset of each slot (offsets present in the tile, ascending)
   uint32_t tor;             // bit s: list s has pairs in the tile
 };
+
+// The TMA producers read rowp four entries at a time (16-byte loads) from
+// either table.
+static_assert(sizeof(TileTable) % 16 == 0, "TileTable keeps 16-byte alignment in an array");
 
 // What the MMA thread and the epilogue need to know about a tile.
 struct TileInfo {
@@ -316,6 +358,58 @@ __device__ __forceinline__ void publish_info(ConvSmemHead& h, uint32_t* status, 
   const int ns = __popc(tab.tor);
   for (int k = 0; k < ns; ++k) h.info[r].slot_s[k] = tab.slot_s[k];
   mbar_arrive(smem_u32(&h.tinfo_full[r]));
+}
+
+// Epilogue warps: for each tile, wait for its accumulator, read TMEM (row
+// per thread), write fp32 or bf16 rows, release the accumulator and the
+// tile's info slot.
+__device__ __forceinline__ void conv_epilogue(ConvSmemHead& h, const ConvArgs& a, uint32_t tmem, uint32_t acc_cols,
+                                              int64_t ntiles, int64_t G, int warp, int lane) {
+  const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+  const int m = quarter * 32 + lane;
+  const int cout = a.cout, out_bf16 = a.out_bf16;
+  const int64_t n_out = a.n_out;
+  uint32_t* const status = a.status;
+  int i = 0;
+  for (int64_t t = blockIdx.x; t < ntiles; t += G, ++i) {
+    const int b = i & 1, r = i & (kInfoRing - 1);
+    mbar_wait(smem_u32(&h.acc_full[b]), (uint32_t)((i >> 1) & 1), status);
+    tc_fence_after();
+    const int nst = *(volatile int*)&h.info[r].nst;
+    const int64_t q = t * kRows + m;
+    const uint32_t trow = tmem + (uint32_t)b * acc_cols + ((uint32_t)(quarter * 32) << 16);
+    for (int c = 0; c < cout; c += 16) {
+      uint32_t v[16];
+      if (nst > 0) {
+        tmem_ld16(trow + (uint32_t)c, v);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] = 0u;
+      }
+      if (q < n_out && out_bf16) {
+        uint4 v0, v1;
+        v0.x = pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1]));
+        v0.y = pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3]));
+        v0.z = pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5]));
+        v0.w = pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7]));
+        v1.x = pack_bf16x2(__uint_as_float(v[8]), __uint_as_float(v[9]));
+        v1.y = pack_bf16x2(__uint_as_float(v[10]), __uint_as_float(v[11]));
+        v1.z = pack_bf16x2(__uint_as_float(v[12]), __uint_as_float(v[13]));
+        v1.w = pack_bf16x2(__uint_as_float(v[14]), __uint_as_float(v[15]));
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.y) + q * cout + c);
+        dst[0] = v0;
+        dst[1] = v1;
+      } else if (q < n_out) {
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<float*>(a.y) + q * cout + c);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dst[e] = make_uint4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+      }
+    }
+    tc_fence_before();
+    mbar_arrive(smem_u32(&h.acc_empty[b]));
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&h.tinfo_empty[r]));
+  }
 }
 
 __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tc(const __grid_constant__ ConvArgs a) {
@@ -613,29 +707,456 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tc(const __grid_c
     }
     __syncwarp();
   } else {
-    // ---------------- epilogue: TMEM -> registers -> global (row per thread)
-    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
-    const int m = quarter * 32 + lane;
-    const int cout = a.cout, out_bf16 = a.out_bf16;
-    const int64_t n_out = a.n_out;
+    conv_epilogue(h, a, tmem, acc_cols, ntiles, G, warp, lane);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * acc_cols) : "memory");
+  }
+}
+
+// ============================================================== bf16, TMA-fed
+// For cin a multiple of 16 the gathers go to the Tensor Memory Accelerator:
+// tile::gather4 brings 4 feature rows (their indices from the row table) of
+// one `chunk` of channels (16, 32 or 64 bf16 = one 32/64/128-byte swizzle row)
+// per instruction, and a 2-D box brings the matching weight rows.  A stage is
+// 64 channels of K (64/chunk chunks); absent rows use index n_in, which the
+// TMA reads as zeros.  Completion is counted in bytes on the stage's
+// mbarrier, so producers never wait for their own copies.
+struct alignas(128) ConvTmaArgs {
+  CUtensorMap tmx;  // feats [n_in][cin] bf16: box {chunk, 1}, swizzle 2*chunk bytes
+  CUtensorMap tmw;  // Wt [27*cout][cin] bf16: box {chunk, cout}, same swizzle
+  ConvArgs c;
+  int chunk;   // channels per box row: 16, 32 or 64
+  int layout;  // UMMA layout type of that swizzle: 6 (32 B), 4 (64 B), 2 (128 B)
+  int n_in;    // feature rows; row index n_in reads as zeros
+};
+
+__global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tma(const __grid_constant__ ConvTmaArgs ta) {
+  const ConvArgs& a = ta.c;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* sbase = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  ConvSmemHead& h = *reinterpret_cast<ConvSmemHead*>(sbase + (size_t)a.stages * a.stage_bytes);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int S = a.stages;
+  const int chunk = ta.chunk, rowb = 2 * chunk;  // channels / bytes per box row
+  const int cps = 64 / chunk;                     // chunks per stage
+  const int ncs = a.cin / chunk;                  // chunks per offset
+  const uint32_t acc_cols = (uint32_t)a.tmem_cols;
+  const int64_t G = gridDim.x;
+  const int64_t ntiles = a.ntiles;
+
+  if (tid == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(smem_u32(&h.full[i]), 1);  // one expect_tx arrival + the TMA bytes
+      mbar_init(smem_u32(&h.empty[i]), 1);
+    }
+    for (int r = 0; r < kInfoRing; ++r) {
+      mbar_init(smem_u32(&h.tinfo_full[r]), 1);
+      mbar_init(smem_u32(&h.tinfo_empty[r]), 4);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&h.acc_full[b]), 1);
+      mbar_init(smem_u32(&h.acc_empty[b]), 128);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == kMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&h.tmem_base)),
+                 "r"(2 * acc_cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = h.tmem_base;
+
+  if (warp < kProducerWarps) {
+    // ---------------- producers: row tables (two threads per row), TMA issue
+    const int pt = tid, m = pt & (kRows - 1), hf = pt >> 7;
+    const int s_lo = hf * kHalfOffsets, s_hi = hf ? 27 : kHalfOffsets;
+    const int32_t* const gin = a.in_idx;
+    const int32_t* const gout = a.out_idx;
+    const uint32_t* const gts = a.tile_start;
+    const int cout = a.cout, sbytes = a.stage_bytes, absent = ta.n_in;
+    const uint32_t stage_tx = (uint32_t)(kATileBytes + cout * 128);
+    const int nops_a = cps * 32;  // gather4 ops per stage; then cps weight boxes
     uint32_t* const status = a.status;
-    int i = 0;
-    for (int64_t t = blockIdx.x; t < ntiles; t += G, ++i) {
-      const int b = i & 1, r = i & (kInfoRing - 1);
-      mbar_wait(smem_u32(&h.acc_full[b]), (uint32_t)((i >> 1) & 1), status);
-      tc_fence_after();
-      const int nst = *(volatile int*)&h.info[r].nst;
-      const int64_t q = t * kRows + m;
-      const uint32_t trow = tmem + (uint32_t)b * acc_cols + ((uint32_t)(quarter * 32) << 16);
+    int64_t kg = 0;
+    int ring_sb = 0;
+    uint32_t ring_ph = 0;
+    uint32_t sa = 0, se = 0;
+    int pv[kHalfOffsets], qv[kHalfOffsets];
+    uint32_t vmask = 0;
+    auto table_begin = [&](TileTable& tab) {
+      if (pt < 27) {
+        tab.tstart[pt] = sa;
+        tab.tend[pt] = se;
+      }
+      if (warp == 0) {
+        const uint32_t tor = __ballot_sync(0xffffffffu, pt < 27 && se > sa);
+        if (pt < 27 && ((tor >> pt) & 1u)) tab.slot_s[__popc(tor & ((1u << pt) - 1u))] = pt;
+        if (pt == 0) tab.tor = tor;
+      }
+      producer_bar();
+      const int ns = __popc(tab.tor);
+      for (int k = hf; k < ns; k += 2) tab.rowp[k][m] = absent;
+      vmask = 0;
+#pragma unroll
+      for (int j = 0; j < kHalfOffsets; ++j) {
+        const int s = s_lo + j;
+        uint32_t e = 0;
+        if (s < s_hi) {
+          const uint32_t b0 = tab.tstart[s], b1 = tab.tend[s];
+          if (b0 + (uint32_t)m < b1) {
+            e = b0 + (uint32_t)m;
+            vmask |= 1u << j;
+          }
+        }
+        pv[j] = __ldg(gin + e);
+        qv[j] = __ldg(gout + e);
+      }
+    };
+    auto table_end = [&](TileTable& tab, int64_t t) {
+      const uint32_t tor = tab.tor;
+      const int64_t q0 = t * kRows;
+#pragma unroll
+      for (int j = 0; j < kHalfOffsets; ++j) {
+        if ((vmask >> j) & 1u) {
+          const int s = s_lo + j;
+          tab.rowp[__popc(tor & ((1u << s) - 1u))][qv[j] - q0] = pv[j];
+        }
+      }
+    };
+
+    int64_t t = blockIdx.x;
+    load_segment(gts, ntiles, t, pt, sa, se);
+    table_begin(h.tab[0]);
+    producer_bar();
+    table_end(h.tab[0], t);
+    const int ppc = chunk >> 3;              // 16-byte pieces per chunk (publish_info counts pieces)
+    int total = __popc(h.tab[0].tor) * ncs;  // chunks of the tile
+    load_segment(gts, ntiles, t + G, pt, sa, se);
+    producer_bar();
+    if (pt == 0 && t < ntiles) publish_info(h, status, 0, h.tab[0], total * ppc);
+    // A warp issues its TMA instructions one lane after another, so the ops
+    // of a stage are spread over all producer warps: op = lane * 8 + warp
+    // (gathers first, then the weight boxes).
+    const int op = lane * kProducerWarps + warp;
+    const bool issuer = op < nops_a + cps;
+    for (int i = 0; t < ntiles; t += G, ++i) {
+      const int b = i & 1, nb = b ^ 1;
+      const bool has_next = (t + G) < ntiles;
+      const TileTable& cur = h.tab[b];
+      if (has_next) table_begin(h.tab[nb]);
+      load_segment(gts, ntiles, t + 2 * G, pt, sa, se);
+      const int nst = issuer ? (total + cps - 1) / cps : 0;
+      for (int k = 0; k < nst; ++k, ++kg) {
+        const int sb = ring_sb;
+        if (kg >= S) mbar_wait(smem_u32(&h.empty[sb]), ring_ph ^ 1u, status);
+        if (++ring_sb == S) {
+          ring_sb = 0;
+          ring_ph ^= 1u;
+        }
+        const uint32_t bar = smem_u32(&h.full[sb]);
+        const uint32_t sA = smem_u32(sbase + (size_t)sb * sbytes);
+        const uint32_t sB = sA + kATileBytes;
+        if (op == 0) mbar_arrive_expect_tx(bar, stage_tx);
+        if (op < nops_a) {
+          const int j = op >> 5, r4 = op & 31;
+          const int c = k * cps + j;
+          int4 rows = make_int4(absent, absent, absent, absent);
+          int col = 0;
+          if (c < total) {
+            const int slot = c / ncs;
+            rows = *reinterpret_cast<const int4*>(&cur.rowp[slot][4 * r4]);
+            col = (c - slot * ncs) * chunk;
+          }
+          tma_gather4(sA + (uint32_t)(j * kRows * rowb + r4 * 4 * rowb), &ta.tmx, col, rows, bar);
+        } else {
+          const int j = op - nops_a;
+          const int c = k * cps + j;
+          int c0 = 0, c1 = 27 * cout;  // past the last weight row: zeros
+          if (c < total) {
+            const int slot = c / ncs;
+            c0 = (c - slot * ncs) * chunk;
+            c1 = cur.slot_s[slot] * cout;
+          }
+          tma_tile2d(sB + (uint32_t)(j * cout * rowb), &ta.tmw, c0, c1, bar);
+        }
+      }
+      if (has_next) {
+        producer_bar();  // every thread has reset its rows of the next table
+        table_end(h.tab[nb], t + G);
+        total = __popc(h.tab[nb].tor) * ncs;
+        producer_bar();
+        if (pt == 0) publish_info(h, status, i + 1, h.tab[nb], total * ppc);
+      }
+      producer_bar();  // this tile's table is no longer read
+    }
+    if (pt == 0) {
+      // Normally the MMA thread has seen every stage complete.  After a
+      // give-up, wait (bounded) for the copies still in flight to land before
+      // the block exits: the last use of each ring slot, newest first.
+      int sb = ring_sb;
+      uint32_t ph = ring_ph;
+      for (int64_t u = 0; u < kg && u < S; ++u) {
+        if (sb == 0) {
+          sb = S - 1;
+          ph ^= 1u;
+        } else {
+          --sb;
+        }
+        mbar_drain(smem_u32(&h.full[sb]), ph);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------- MMA issue (one thread)
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(kRows, a.cout);
+      const uint32_t layout = (uint32_t)ta.layout, sbo = 8u * (uint32_t)rowb;
+      const int sbytes = a.stage_bytes, cout = a.cout;
+      uint32_t* const status = a.status;
+      int m_sb = 0;
+      uint32_t m_ph = 0;
+      int i = 0;
+      for (int64_t t = blockIdx.x; t < ntiles; t += G, ++i) {
+        const int r = i & (kInfoRing - 1), b = i & 1;
+        mbar_wait(smem_u32(&h.tinfo_full[r]), (uint32_t)((i / kInfoRing) & 1), status);
+        const int nst = *(volatile const int*)&h.info[r].nst;
+        if (i >= 2) mbar_wait(smem_u32(&h.acc_empty[b]), (uint32_t)(((i >> 1) - 1) & 1), status);
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)b * acc_cols;
+        for (int k = 0; k < nst; ++k) {
+          const int sb = m_sb;
+          mbar_wait(smem_u32(&h.full[sb]), m_ph, status);
+          if (++m_sb == S) {
+            m_sb = 0;
+            m_ph ^= 1u;
+          }
+          tc_fence_after();
+          const uint32_t sA = smem_u32(sbase + (size_t)sb * sbytes);
+          const uint32_t sB = sA + kATileBytes;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const int e = 16 * kk, j = e / chunk;
+            const uint32_t off = (uint32_t)((e - j * chunk) * 2);
+            umma_bf16(d, sdesc_swz(sA + (uint32_t)(j * kRows * rowb) + off, layout, sbo),
+                      sdesc_swz(sB + (uint32_t)(j * cout * rowb) + off, layout, sbo), idesc, (k | kk) ? 1u : 0u);
+          }
+          umma_commit(smem_u32(&h.empty[sb]));
+        }
+        if (nst > 0) umma_commit(smem_u32(&h.acc_full[b]));
+        else mbar_arrive(smem_u32(&h.acc_full[b]));
+      }
+    }
+    __syncwarp();
+  } else {
+    conv_epilogue(h, a, tmem, acc_cols, ntiles, G, warp, lane);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * acc_cols) : "memory");
+  }
+}
+
+// ============================================================== bf16, leaf-densified
+// Submanifold (stride 1) convolution one output leaf at a time, after the
+// "leaf" backend of the fVDB paper (Sparse-convolution operators): the input
+// features around the leaf (its 8^3 voxels plus a one-voxel shell, 10^3
+// positions, zeros where no input voxel is active) are staged densely in
+// shared memory, and every offset of the 3x3x3 stencil becomes a dense GEMM
+// whose A operand is a shifted window of that halo.  No kernel-map lists are
+// read and each input row is fetched once per leaf that needs it.
+//
+// Operand layout (UMMA K-major, no swizzle): a core matrix is 8 rows x 16
+// bytes (8 channels) stored contiguously.  The halo holds, per 8-channel
+// group c8 and x-shift cx (dx = cx - 1), a plane of rows
+//   R(yy, x, zz) = (yy * 8 + x) * 10 + zz,   yy, zz in 0..9, x in 0..7,
+// holding the input at (x + dx, yy - 1, zz - 1) relative to the leaf origin.
+// An M tile is two y-rows of the leaf (y = 2t, 2t + 1; row m = (yl * 8 + x)
+// * 8 + z), so for offset (dx, dy, dz) its 16 eight-row groups start 160
+// bytes apart in plane (c8, cx) at row ((2t + dy + 1) * 8) * 10 + dz + 1.
+// K runs over groups kg = c8 * 27 + s (s = the stencil slot); their start
+// addresses increase with kg, so each MMA (two K groups) takes the distance
+// between its two groups as its leading byte offset.
+constexpr int kLeafThreads = 256;
+constexpr int kLeafPlaneRows = 800;                     // 10 x 8 x 10
+constexpr int kLeafPlaneBytes = kLeafPlaneRows * 16;    // 12800
+constexpr int kLeafMaxCin = 16;
+constexpr int kLeafMaxCout = 64;
+
+struct LeafNbr {           // one neighbouring input leaf (zeros when absent)
+  uint64_t mask[8];
+  uint32_t first;
+  uint32_t pad;
+  uint64_t pre9;
+};
+
+struct LeafConvArgs {
+  GridDev gi;                   // input grid
+  const int32_t* out_origin;    // output grid leaves: origin [L][3], batch [L], record [L][10]
+  const int32_t* out_batch;
+  const uint64_t* out_rec;
+  const __nv_bfloat16* x;       // [n_in][cin]
+  const __nv_bfloat16* wt;      // [27][cout][cin]
+  void* y;                      // [n_out][cout], fp32 or bf16
+  uint32_t* status;
+  int64_t n_leaf_out;
+  int cin, cout, out_bf16, tmem_cols;
+  int halo_bytes, w_bytes;      // shared-memory regions (multiples of 1024)
+};
+
+__device__ __forceinline__ uint32_t leaf_index_in(const LeafNbr& L, int n, bool& active) {
+  const int w = n >> 6, bit = n & 63;
+  const uint64_t m = L.mask[w];
+  active = (m >> bit) & 1ull;
+  const uint32_t pre = w ? (uint32_t)((L.pre9 >> (9 * (w - 1))) & 511ull) : 0u;
+  return L.first + pre + (uint32_t)__popcll(m & ((1ull << bit) - 1ull));
+}
+
+__global__ void __launch_bounds__(kLeafThreads) k_conv_leaf(const __grid_constant__ LeafConvArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* halo = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  unsigned char* wsm = halo + a.halo_bytes;
+  LeafNbr* nbr = reinterpret_cast<LeafNbr*>(wsm + a.w_bytes);
+  unsigned long long* done = reinterpret_cast<unsigned long long*>(nbr + 27);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int cin = a.cin, cout = a.cout, g8 = cin >> 3;
+  const int64_t L = blockIdx.x;
+  if (L >= a.n_leaf_out) return;
+
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(a.tmem_cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (tid == 32) {
+    mbar_init(smem_u32(done), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  const int ob = __ldg(a.out_batch + L);
+  const int ox = __ldg(a.out_origin + 3 * L), oy = __ldg(a.out_origin + 3 * L + 1), oz = __ldg(a.out_origin + 3 * L + 2);
+  // the 27 input leaves around the output leaf (slot = (ex+1)*9 + (ey+1)*3 + (ez+1))
+  if (tid < 27) {
+    const int ex = tid / 9 - 1, ey = (tid / 3) % 3 - 1, ez = tid % 3 - 1;
+    const int l = find_leaf(a.gi, ob, ox + 8 * ex, oy + 8 * ey, oz + 8 * ez);
+    LeafNbr& nb = nbr[tid];
+    if (l >= 0) {
+      const uint64_t* rec = a.gi.leaf_rec + (size_t)l * 10;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) nb.mask[w] = __ldg(reinterpret_cast<const unsigned long long*>(rec) + w);
+      nb.first = (uint32_t)__ldg(reinterpret_cast<const unsigned long long*>(rec) + 8);
+      nb.pre9 = __ldg(reinterpret_cast<const unsigned long long*>(rec) + 9);
+    } else {
+#pragma unroll
+      for (int w = 0; w < 8; ++w) nb.mask[w] = 0ull;
+      nb.first = 0u;
+      nb.pre9 = 0ull;
+    }
+  }
+  // weights: block kg = c8 * 27 + s holds rows co of wt[s][co][8*c8 .. 8*c8+7];
+  // one zero block after the last
+  {
+    const int nkg = 27 * g8;
+    const int nrow = (nkg + 1) * cout;
+    for (int e = tid; e < nrow; e += kLeafThreads) {
+      const int kg = e / cout, co = e - kg * cout;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (kg < nkg) {
+        const int c8 = kg / 27, s = kg - c8 * 27;
+        v = __ldg(reinterpret_cast<const uint4*>(a.wt + ((size_t)s * cout + co) * cin + 8 * c8));
+      }
+      *reinterpret_cast<uint4*>(wsm + (size_t)e * 16) = v;
+    }
+  }
+  __syncthreads();
+  // halo: position (hx, hy, hz) in -1..8 relative to the origin, one 16-byte
+  // piece (8 channels) per item, written to every x-shifted plane holding it
+  {
+    const int nitem = 1000 * g8;
+    for (int e = tid; e < nitem; e += kLeafThreads) {
+      const int pos = e / g8, c8 = e - pos * g8;
+      const int hx = pos / 100 - 1, hy = (pos / 10) % 10 - 1, hz = pos % 10 - 1;
+      const int ex = (hx < 0) ? -1 : (hx > 7 ? 1 : 0), ey = (hy < 0) ? -1 : (hy > 7 ? 1 : 0),
+                ez = (hz < 0) ? -1 : (hz > 7 ? 1 : 0);
+      bool act;
+      const uint32_t idx = leaf_index_in(nbr[(ex + 1) * 9 + (ey + 1) * 3 + (ez + 1)],
+                                         ((hx & 7) << 6) | ((hy & 7) << 3) | (hz & 7), act);
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (act) v = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)idx * cin + 8 * c8));
+      const int rbase = (hy + 1) * 80 + (hz + 1);  // row without the x term
+#pragma unroll
+      for (int cx = 0; cx < 3; ++cx) {
+        const int xx = hx - cx + 1;  // x of the plane row holding this position
+        if (xx >= 0 && xx < 8) {
+          *reinterpret_cast<uint4*>(halo + (size_t)(c8 * 3 + cx) * kLeafPlaneBytes + (size_t)(rbase + xx * 10) * 16) = v;
+        }
+      }
+    }
+  }
+  fence_proxy_async();  // the tensor core reads what the generic proxy wrote
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (tid == 0) {
+    const uint32_t idesc = idesc_bf16(kRows, cout);
+    const uint32_t hbase = smem_u32(halo), wbase = smem_u32(wsm);
+    const int nkg = 27 * g8, npair = (nkg + 1) >> 1;
+    const uint32_t wblk = (uint32_t)cout * 16u;
+    for (int t = 0; t < 4; ++t) {
+      const uint32_t d = tmem + (uint32_t)(t * cout);
+      for (int p = 0; p < npair; ++p) {
+        uint32_t addr[2];
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          int kg = 2 * p + h2;
+          if (kg >= nkg) kg = nkg - 1;  // the zero weight block pairs with a repeat
+          const int c8 = kg / 27, s = kg - c8 * 27;
+          const int cx = s / 9, dy = (s / 3) % 3 - 1, dz = s % 3 - 1;
+          addr[h2] = hbase + (uint32_t)(c8 * 3 + cx) * kLeafPlaneBytes +
+                     (uint32_t)(((2 * t + dy + 1) * 80 + dz + 1) * 16);
+        }
+        const uint64_t ad = sdesc_plain(addr[0], addr[1] - addr[0], 160u);
+        const uint64_t bd = sdesc_plain(wbase + (uint32_t)(2 * p) * wblk, wblk, 128u);
+        umma_bf16(d, ad, bd, idesc, p ? 1u : 0u);
+      }
+    }
+    umma_commit(smem_u32(done));
+  }
+  __syncwarp();
+  mbar_wait(smem_u32(done), 0u, a.status);
+  tc_fence_after();
+
+  // epilogue: warp w reads TMEM lanes 32*(w&3) .. +31 of tiles 2*(w>>2), +1
+  {
+    const int quarter = warp & 3, m = quarter * 32 + lane;
+    const int yl = m >> 6, xq = (m >> 3) & 7, z = m & 7;
+    const uint64_t* rec = a.out_rec + (size_t)L * 10;
+    const uint64_t mw = __ldg(reinterpret_cast<const unsigned long long*>(rec) + xq);
+    const uint32_t first = (uint32_t)__ldg(reinterpret_cast<const unsigned long long*>(rec) + 8);
+    const uint64_t pre9 = __ldg(reinterpret_cast<const unsigned long long*>(rec) + 9);
+    const uint32_t pre = xq ? (uint32_t)((pre9 >> (9 * (xq - 1))) & 511ull) : 0u;
+    for (int tt = 0; tt < 2; ++tt) {
+      const int t = 2 * (warp >> 2) + tt;
+      const int bit = (2 * t + yl) * 8 + z;
+      const bool act = (mw >> bit) & 1ull;
+      const int64_t q = (int64_t)first + pre + __popcll(mw & ((1ull << bit) - 1ull));
+      const uint32_t trow = tmem + (uint32_t)(t * cout) + ((uint32_t)(quarter * 32) << 16);
       for (int c = 0; c < cout; c += 16) {
         uint32_t v[16];
-        if (nst > 0) {
-          tmem_ld16(trow + (uint32_t)c, v);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 16; ++e) v[e] = 0u;
-        }
-        if (q < n_out && out_bf16) {
+        tmem_ld16(trow + (uint32_t)c, v);
+        if (!act) continue;
+        if (a.out_bf16) {
           uint4 v0, v1;
           v0.x = pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1]));
           v0.y = pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3]));
@@ -648,23 +1169,19 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tc(const __grid_c
           uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.y) + q * cout + c);
           dst[0] = v0;
           dst[1] = v1;
-        } else if (q < n_out) {
+        } else {
           uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<float*>(a.y) + q * cout + c);
 #pragma unroll
           for (int e = 0; e < 4; ++e) dst[e] = make_uint4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
         }
       }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&h.acc_empty[b]));
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&h.tinfo_empty[r]));
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == 0) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * acc_cols) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(a.tmem_cols) : "memory");
   }
 }
 
@@ -677,6 +1194,186 @@ __global__ void k_transpose_w(const __nv_bfloat16* __restrict__ W, int cin, int 
   const int64_t s = e / per, r = e - s * per;
   const int co = (int)(r / cin), ci = (int)(r - (int64_t)co * cin);
   wt[e] = W[s * per + (int64_t)ci * cout + co];
+}
+
+// cuTensorMapEncodeTiled, taken from the driver through the runtime (no link
+// against the driver library).  Null when the driver does not provide it.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeTiledFn)p;
+    (void)cudaGetLastError();
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor [rows][cols] (row pitch cols*2 bytes) read in boxes of
+// {box_cols, box_rows}, swizzled to the box row width.
+fvx_status encode_2d(EncodeTiledFn fn, CUtensorMap* tm, const void* base, int64_t cols, int64_t rows, int box_cols,
+                     int box_rows, CUtensorMapSwizzle swz, CUtensorMapL2promotion l2, const char* who) {
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swz, l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("%s: tensor map encoding failed (driver error %d)", who, (int)r);
+    return FVX_ERR_CUDA;
+  }
+  return FVX_OK;
+}
+
+// Fills the kernel arguments and launches the bf16 convolution: the TMA-fed
+// kernel when cin is a multiple of 16 (chunk = the largest of 64, 32, 16
+// dividing cin), else the cp.async kernel.  wt: [27][cout][cin] bf16 weights;
+// status: a zeroed device word.
+std::atomic<int> g_conv_algo{FVX_CONV_AUTO};
+thread_local int t_last_algo = FVX_CONV_AUTO;
+
+// Leaf-densified launch: one block per output leaf, as many blocks per SM as
+// shared memory allows but no more than the tensor memory holds at once.
+fvx_status launch_conv_leaf(const char* who, fvx_grid gin, fvx_kmap m, fvx_dtype dt, const void* feats, int64_t cin,
+                            int64_t cout, void* out, const __nv_bfloat16* wt, uint32_t* status, cudaStream_t s) {
+  const fvx_grid_s* go = m->gout;
+  LeafConvArgs a;
+  a.gi = grid_dev(gin);
+  a.out_origin = go->leaf_origin;
+  a.out_batch = go->leaf_batch;
+  a.out_rec = go->leaf_rec;
+  a.x = (const __nv_bfloat16*)feats;
+  a.wt = wt;
+  a.y = out;
+  a.status = status;
+  a.n_leaf_out = go->n_leaf;
+  a.cin = (int)cin;
+  a.cout = (int)cout;
+  a.out_bf16 = (dt == FVX_BF16_OUT_BF16) ? 1 : 0;
+  const int tcs = (int)((cout + 31) & ~(int64_t)31);  // accumulator columns per M tile
+  int cols = 32;
+  while (cols < 4 * tcs) cols <<= 1;
+  a.tmem_cols = cols;
+  a.halo_bytes = (3 * (int)(cin / 8) * kLeafPlaneBytes + 1023) & ~1023;
+  a.w_bytes = ((27 * (int)(cin / 8) + 1) * (int)cout * 16 + 1023) & ~1023;
+  size_t smem = 1024 + (size_t)a.halo_bytes + a.w_bytes + 27 * sizeof(LeafNbr) + 16;
+  int dev = 0, sm_bytes = 0, reserved = 0;
+  FVX_CUDA(cudaGetDevice(&dev));
+  FVX_CUDA(cudaDeviceGetAttribute(&sm_bytes, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev));
+  FVX_CUDA(cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev));
+  const size_t per_sm = (size_t)(512 / cols);  // blocks whose accumulators fit in TMEM together
+  if ((size_t)sm_bytes / (smem + reserved) > per_sm) smem = (size_t)sm_bytes / (per_sm + 1) - reserved + 16;
+  FVX_CUDA(cudaFuncSetAttribute(k_conv_leaf, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  {
+    LaunchScope ls("conv_leaf", s);
+    k_conv_leaf<<<(unsigned)go->n_leaf, kLeafThreads, smem, s>>>(a);
+  }
+  FVX_TRY(check_launch("conv_leaf"));
+  (void)who;
+  t_last_algo = FVX_CONV_LEAF;
+  return FVX_OK;
+}
+
+fvx_status launch_conv_bf16(const char* who, fvx_grid gin, fvx_kmap m, fvx_dtype dt, const void* feats, int64_t cin,
+                            int64_t cout, void* out, const __nv_bfloat16* wt, uint32_t* status, cudaStream_t s) {
+  const int64_t nt = m->n_tiles;
+  const int algo = g_conv_algo.load(std::memory_order_relaxed);
+  const bool leaf_ok = m->stride == 1 && cin <= kLeafMaxCin && cout <= kLeafMaxCout;
+  if (algo == FVX_CONV_LEAF && !leaf_ok) {
+    set_error("%s: the leaf-densified convolution needs stride 1, cin <= %d and cout <= %d (got stride %d, %lld, %lld)",
+              who, kLeafMaxCin, kLeafMaxCout, (int)m->stride, (long long)cin, (long long)cout);
+    return FVX_ERR_INVALID_ARG;
+  }
+  const fvx_grid_s* go = m->gout;
+  const bool dense_leaves = go->n_leaf > 0 && (double)go->n_active >= 0.2 * 512.0 * (double)go->n_leaf;
+  if (leaf_ok && (algo == FVX_CONV_LEAF || (algo == FVX_CONV_AUTO && dense_leaves)))
+    return launch_conv_leaf(who, gin, m, dt, feats, cin, cout, out, wt, status, s);
+  ConvArgs a;
+  a.x = (const __nv_bfloat16*)feats;
+  a.wt = wt;
+  a.in_idx = m->in_idx;
+  a.out_idx = m->out_idx;
+  a.tile_start = m->tile_start;
+  a.y = out;
+  a.out_bf16 = (dt == FVX_BF16_OUT_BF16) ? 1 : 0;
+  a.status = status;
+  a.ntiles = nt;
+  a.n_out = m->n_out;
+  a.cin = (int)cin;
+  a.cout = (int)cout;
+  int cols = 32;
+  while (cols < cout) cols <<= 1;
+  a.tmem_cols = cols;  // per accumulator; two accumulators per CTA (<= 512 columns)
+  int dev = 0, sms = 0;
+  FVX_CUDA(cudaGetDevice(&dev));
+  FVX_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  const int64_t grid = std::min<int64_t>(nt, (int64_t)sms);
+  const int head = (int)sizeof(ConvSmemHead) + 1024;
+
+  EncodeTiledFn enc = (cin % 16 == 0 && gin->n_active > 0) ? encode_tiled() : nullptr;
+  if (enc) {
+    ConvTmaArgs ta;
+    ta.chunk = (cin % 64 == 0) ? 64 : (cin % 32 == 0) ? 32 : 16;
+    const CUtensorMapSwizzle swz = ta.chunk == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
+                                   : ta.chunk == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                    : CU_TENSOR_MAP_SWIZZLE_32B;
+    ta.layout = ta.chunk == 64 ? 2 : ta.chunk == 32 ? 4 : 6;
+    ta.n_in = (int)gin->n_active;
+    FVX_TRY(encode_2d(enc, &ta.tmx, feats, cin, gin->n_active, ta.chunk, 1, swz, CU_TENSOR_MAP_L2_PROMOTION_NONE, who));
+    FVX_TRY(encode_2d(enc, &ta.tmw, wt, cin, 27 * cout, ta.chunk, (int)cout, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      who));
+    a.w_resident = 0;
+    a.w_bytes = 0;
+    a.lag = 0;
+    a.stage_bytes = kATileBytes + (int)cout * 128;  // multiple of 2048
+    a.stages = std::min((224 * 1024 - head) / a.stage_bytes, kMaxStages);
+    if (a.stages < 3) {
+      set_error("%s: cout %lld leaves fewer than 3 pipeline stages", who, (long long)cout);
+      return FVX_ERR_INVALID_ARG;
+    }
+    ta.c = a;
+    const size_t smem = 1024 + (size_t)a.stages * a.stage_bytes + sizeof(ConvSmemHead);
+    FVX_CUDA(cudaFuncSetAttribute(k_conv_bf16_tma, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    {
+      LaunchScope ls("conv_bf16_tma", s);
+      k_conv_bf16_tma<<<(unsigned)grid, kConvThreads, smem, s>>>(ta);
+    }
+    FVX_TRY(check_launch("conv_bf16_tma"));
+    t_last_algo = FVX_CONV_GATHER;
+    return FVX_OK;
+  }
+
+  // Weights resident in shared memory when they fit (27 * cin/8 blocks of
+  // cout x 16 bytes plus one zero block); otherwise a B tile per stage.
+  const int64_t wres = (27 * (cin / 8) + 1) * cout * 16;
+  a.w_resident = (wres <= kResidentWBytes) ? 1 : 0;
+  a.w_bytes = a.w_resident ? (int)((wres + 1023) & ~(int64_t)1023) : 0;
+  a.stage_bytes = kATileBytes + (a.w_resident ? 0 : (int)cout * 128);  // multiples of 1024
+  // Stage ring (persistent across the CTA's tiles): as deep as shared memory
+  // allows, up to kMaxStages; one CTA per SM.
+  a.stages = (224 * 1024 - head - a.w_bytes) / a.stage_bytes;
+  if (a.stages > kMaxStages) a.stages = kMaxStages;
+  if (a.stages < 3) {
+    set_error("%s: cout %lld leaves fewer than 3 pipeline stages", who, (long long)cout);
+    return FVX_ERR_INVALID_ARG;
+  }
+  a.lag = std::min(a.stages - 2, 4);
+  const size_t smem = 1024 + (size_t)a.w_bytes + (size_t)a.stages * a.stage_bytes + sizeof(ConvSmemHead);
+  FVX_CUDA(cudaFuncSetAttribute(k_conv_bf16_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  {
+    LaunchScope ls("conv_bf16_tc", s);
+    k_conv_bf16_tc<<<(unsigned)grid, kConvThreads, smem, s>>>(a);
+  }
+  FVX_TRY(check_launch("conv_bf16_tc"));
+  t_last_algo = FVX_CONV_GATHER;
+  return FVX_OK;
 }
 
 }  // namespace
@@ -736,50 +1433,7 @@ extern "C" fvx_status fvx_sparse_conv(fvx_grid gin, fvx_grid gout, fvx_kmap m, f
     k_transpose_w<<<(unsigned)((n + 255) / 256), 256, 0, s>>>((const __nv_bfloat16*)W, (int)cin, (int)cout, wt);
   }
   FVX_TRY(check_launch("conv_transpose_w"));
-
-  ConvArgs a;
-  a.x = (const __nv_bfloat16*)feats;
-  a.wt = wt;
-  a.in_idx = m->in_idx;
-  a.out_idx = m->out_idx;
-  a.tile_start = m->tile_start;
-  a.y = out;
-  a.out_bf16 = (dt == FVX_BF16_OUT_BF16) ? 1 : 0;
-  a.status = status;
-  a.ntiles = nt;
-  a.n_out = m->n_out;
-  a.cin = (int)cin;
-  a.cout = (int)cout;
-  // Weights resident in shared memory when they fit (27 * cin/8 blocks of
-  // cout x 16 bytes plus one zero block); otherwise a B tile per stage.
-  const int64_t wres = (27 * (cin / 8) + 1) * cout * 16;
-  a.w_resident = (wres <= kResidentWBytes) ? 1 : 0;
-  a.w_bytes = a.w_resident ? (int)((wres + 1023) & ~(int64_t)1023) : 0;
-  a.stage_bytes = kATileBytes + (a.w_resident ? 0 : (int)cout * 128);  // multiples of 1024
-  // Stage ring (persistent across the CTA's tiles): as deep as shared memory
-  // allows, up to kMaxStages; one CTA per SM.
-  const int head = (int)sizeof(ConvSmemHead) + 1024;
-  a.stages = (224 * 1024 - head - a.w_bytes) / a.stage_bytes;
-  if (a.stages > kMaxStages) a.stages = kMaxStages;
-  if (a.stages < 3) {
-    set_error("fvx_sparse_conv: cout %lld leaves fewer than 3 pipeline stages", (long long)cout);
-    return FVX_ERR_INVALID_ARG;
-  }
-  a.lag = std::min(a.stages - 2, 4);
-  int cols = 32;
-  while (cols < cout) cols <<= 1;
-  a.tmem_cols = cols;  // per accumulator; two accumulators per CTA (<= 512 columns)
-  const size_t smem = 1024 + (size_t)a.w_bytes + (size_t)a.stages * a.stage_bytes + sizeof(ConvSmemHead);
-  FVX_CUDA(cudaFuncSetAttribute(k_conv_bf16_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-  int dev = 0, sms = 0;
-  FVX_CUDA(cudaGetDevice(&dev));
-  FVX_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-  const int64_t grid = std::min<int64_t>(nt, (int64_t)sms);
-  {
-    LaunchScope ls("conv_bf16_tc", s);
-    k_conv_bf16_tc<<<(unsigned)grid, kConvThreads, smem, s>>>(a);
-  }
-  return check_launch("conv_bf16_tc");
+  return launch_conv_bf16("fvx_sparse_conv", gin, m, dt, feats, cin, cout, out, wt, status, s);
 }
 
 // ============================================================== no-allocation variant
@@ -875,44 +1529,16 @@ extern "C" fvx_status fvx_sparse_conv_noalloc(fvx_grid gin, fvx_grid gout, fvx_k
     k_transpose_w<<<(unsigned)((n + 255) / 256), 256, 0, s>>>((const __nv_bfloat16*)W, (int)cin, (int)cout, wt);
   }
   FVX_TRY(check_launch("conv_transpose_w"));
+  return launch_conv_bf16("fvx_sparse_conv_noalloc", gin, m, dt, feats, cin, cout, out, wt, status, s);
+}
 
-  ConvArgs a;
-  a.x = (const __nv_bfloat16*)feats;
-  a.wt = wt;
-  a.in_idx = m->in_idx;
-  a.out_idx = m->out_idx;
-  a.tile_start = m->tile_start;
-  a.y = out;
-  a.out_bf16 = (dt == FVX_BF16_OUT_BF16) ? 1 : 0;
-  a.status = status;
-  a.ntiles = nt;
-  a.n_out = m->n_out;
-  a.cin = (int)cin;
-  a.cout = (int)cout;
-  const int64_t wres = (27 * (cin / 8) + 1) * cout * 16;
-  a.w_resident = (wres <= kResidentWBytes) ? 1 : 0;
-  a.w_bytes = a.w_resident ? (int)((wres + 1023) & ~(int64_t)1023) : 0;
-  a.stage_bytes = kATileBytes + (a.w_resident ? 0 : (int)cout * 128);
-  const int head = (int)sizeof(ConvSmemHead) + 1024;
-  a.stages = (224 * 1024 - head - a.w_bytes) / a.stage_bytes;
-  if (a.stages > kMaxStages) a.stages = kMaxStages;
-  if (a.stages < 3) {
-    set_error("fvx_sparse_conv_noalloc: cout %lld leaves fewer than 3 pipeline stages", (long long)cout);
+extern "C" fvx_status fvx_set_conv_algo(fvx_conv_algo algo) {
+  if (algo != FVX_CONV_AUTO && algo != FVX_CONV_GATHER && algo != FVX_CONV_LEAF) {
+    set_error("fvx_set_conv_algo: unknown value %d", (int)algo);
     return FVX_ERR_INVALID_ARG;
   }
-  a.lag = std::min(a.stages - 2, 4);
-  int cols = 32;
-  while (cols < cout) cols <<= 1;
-  a.tmem_cols = cols;
-  const size_t smem = 1024 + (size_t)a.w_bytes + (size_t)a.stages * a.stage_bytes + sizeof(ConvSmemHead);
-  FVX_CUDA(cudaFuncSetAttribute(k_conv_bf16_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-  int dev = 0, sms = 0;
-  FVX_CUDA(cudaGetDevice(&dev));
-  FVX_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-  const int64_t grid = std::min<int64_t>(nt, (int64_t)sms);
-  {
-    LaunchScope ls("conv_bf16_tc", s);
-    k_conv_bf16_tc<<<(unsigned)grid, kConvThreads, smem, s>>>(a);
-  }
-  return check_launch("conv_bf16_tc");
+  g_conv_algo.store((int)algo, std::memory_order_relaxed);
+  return FVX_OK;
 }
+
+extern "C" fvx_conv_algo fvx_last_conv_algo(void) { return (fvx_conv_algo)t_last_algo; }

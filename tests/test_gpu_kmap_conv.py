@@ -90,8 +90,11 @@ def test_conv_f32_matches_oracle(cuda_device, grids, stride, cin, cout):
     G.assert_conv_close(G.np_(y), yo, ao, G.F32_TOL)
 
 
+# cin a multiple of 16 takes the TMA-fed kernel (16/32/64-channel chunks:
+# 48 -> 3 x 16, 96 -> 3 x 32, 80 -> 5 x 16); other multiples of 8 the
+# cp.async kernel (8, 24, 40).
 @pytest.mark.parametrize("cin,cout", [(8, 16), (16, 32), (32, 64), (64, 64), (128, 128), (128, 256), (24, 48),
-                                      (256, 16)])
+                                      (256, 16), (48, 32), (96, 64), (80, 16), (40, 32), (512, 32), (16, 256)])
 @pytest.mark.parametrize("stride", [1, 2])
 def test_conv_bf16_matches_oracle(cuda_device, grids, stride, cin, cout):
     import sparse_convolution_gb300 as fvx
@@ -99,6 +102,32 @@ def test_conv_bf16_matches_oracle(cuda_device, grids, stride, cin, cout):
     gin, gout, km, okm = _maps(grids, stride)
     x, W = G.bf16_inputs(11, gin.n_active, cin, cout)
     y = fvx.sparse_conv(gin, gout, km, x, W)
+    fvx.device_status()
+    yo, ao = oracle.conv(okm, G.as_f64(x), G.as_f64(W))
+    G.assert_conv_close(G.np_(y.float()), yo, ao, G.BF16_TOL)
+
+
+@pytest.fixture(scope="module")
+def many_tiles():
+    """About 66k voxels in two batches: several hundred 128-row output tiles,
+    so every block of the persistent conv runs several tiles and cycles both
+    of its row-table buffers and its stage ring more than once."""
+    import sparse_convolution_gb300 as fvx
+
+    c, offs = _random(8, 40000, -30, 60, 2)
+    g = G.gpu_grid(c, offs)
+    og = oracle.Grid.build(c, offs)
+    assert g.n_active > 4 * 128 * 152 // 2
+    return g, og, fvx.KernelMap(g, g, 1), oracle.KernelMap(og, og, 1)
+
+
+@pytest.mark.parametrize("cin,cout", [(8, 16), (24, 16), (16, 16), (32, 32), (48, 16), (64, 64)])
+def test_conv_bf16_many_tiles(cuda_device, many_tiles, cin, cout):
+    import sparse_convolution_gb300 as fvx
+
+    g, og, km, okm = many_tiles
+    x, W = G.bf16_inputs(23, g.n_active, cin, cout)
+    y = fvx.sparse_conv(g, g, km, x, W)
     fvx.device_status()
     yo, ao = oracle.conv(okm, G.as_f64(x), G.as_f64(W))
     G.assert_conv_close(G.np_(y.float()), yo, ao, G.BF16_TOL)
@@ -123,17 +152,19 @@ def test_conv_bf16_out_bf16_matches_oracle(cuda_device, grids, stride, cin, cout
     assert torch.equal(y, y32.bfloat16())
 
 
-def test_conv_bf16_identity_is_exact(cuda_device, grids):
-    """W[13] = I, other offsets 0: out == feats bit for bit."""
+@pytest.mark.parametrize("c", [16, 32, 48, 64, 96])
+def test_conv_bf16_identity_is_exact(cuda_device, grids, c):
+    """W[13] = I, other offsets 0: out == feats bit for bit (every channel
+    lands where the operand layout says, for each gather width)."""
     import torch
 
     import sparse_convolution_gb300 as fvx
 
     g = grids["g"]
     km = fvx.KernelMap(g, g, 1)
-    x, _ = G.bf16_inputs(13, g.n_active, 64, 64)
-    W = torch.zeros((27, 64, 64), dtype=torch.bfloat16, device="cuda")
-    W[13] = torch.eye(64, dtype=torch.bfloat16, device="cuda")
+    x, _ = G.bf16_inputs(13, g.n_active, c, c)
+    W = torch.zeros((27, c, c), dtype=torch.bfloat16, device="cuda")
+    W[13] = torch.eye(c, dtype=torch.bfloat16, device="cuda")
     y = fvx.sparse_conv(g, g, km, x, W)
     assert torch.equal(y, x.float())
     assert torch.equal(fvx.sparse_conv(g, g, km, x, W, out_dtype=torch.bfloat16), x)

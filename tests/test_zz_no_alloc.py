@@ -89,3 +89,28 @@ def test_noalloc_fp32_and_limits(cuda_device):
     ob = torch.empty(g.n_active, 256, device="cuda")
     assert _call(lib.fvx_sparse_conv_noalloc, g, km, fvx.FVX_BF16, xb, Wb, ob) == 2  # FVX_ERR_RANGE
     assert b"fixed" in lib.fvx_last_error()
+
+
+def test_noalloc_leaf_kernel(cuda_device):
+    """The leaf-densified kernel through the allocation-free entry point."""
+    import torch
+
+    import sparse_convolution_gb300 as fvx
+
+    lib = fvx.load()
+    g, km = _grid_and_map(5)
+    fvx.set_conv_algo(fvx.FVX_CONV_LEAF)
+    try:
+        for call in range(2):
+            gen = torch.Generator(device="cuda").manual_seed(200 + call)
+            x = torch.randn(g.n_active, 16, device="cuda", generator=gen).bfloat16()
+            W = (torch.randn(27, 16, 32, device="cuda", generator=gen) / 20.0).bfloat16()
+            ref = torch.empty(g.n_active, 32, device="cuda")
+            got = torch.full((g.n_active, 32), float("nan"), device="cuda")
+            assert _call(lib.fvx_sparse_conv, g, km, fvx.FVX_BF16, x, W, ref) == 0, lib.fvx_last_error()
+            assert _call(lib.fvx_sparse_conv_noalloc, g, km, fvx.FVX_BF16, x, W, got) == 0, lib.fvx_last_error()
+            assert fvx.last_conv_algo() == fvx.FVX_CONV_LEAF
+            torch.cuda.synchronize()
+            assert torch.equal(got, ref)
+    finally:
+        fvx.set_conv_algo(fvx.FVX_CONV_AUTO)
