@@ -136,7 +136,8 @@ def profiled_traffic(kernel, workload):
     import hashlib
     import re
 
-    src = {"conv_bf16_tc": "conv.cu", "kmap1_write": "kmap.cu"}.get(kernel)
+    src = {"conv_bf16_tc": "conv.cu", "conv_bf16_tma": "conv.cu", "conv_leaf": "conv.cu",
+           "kmap1_write": "kmap.cu"}.get(kernel)
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     if src is None or not os.path.exists(path):
         return None
@@ -231,10 +232,11 @@ def bench_fvx(args, world, rank, local):
     coords = coords_h.to(dev)
     g0 = fvx.Grid.build(coords, offs)
     U = g0.n_active
-    n_out = [U]
+    n_out, leaves_out = [U], [g0.n_leaf]
     if len(convs) > 1:
         gc0 = g0.coarsen(2)
         n_out.append(gc0.n_active)
+        leaves_out.append(gc0.n_leaf)
         gc0.destroy()
     g0.destroy()
     # feature rows follow the active-voxel index order; values are i.i.d., so any order is a valid input
@@ -252,6 +254,8 @@ def bench_fvx(args, world, rank, local):
         ys.append(torch.empty((n_out[i], c["cout"]), dtype=odt, device=dev))
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
+
+    algos = []  # kernel family each conv ran (recorded on the first step)
 
     def step(rec, coords_in, x_in, W_in):
         """One pass of the path.  rec(category) brackets each call with events."""
@@ -273,6 +277,8 @@ def bench_fvx(args, world, rank, local):
             pairs.append(km.n_pairs)
             with rec("conv"):
                 fvx.sparse_conv(gin, gout, km, src, W_in[i], out=ys[i])
+            if len(algos) < len(convs):
+                algos.append(fvx.last_conv_algo())
             src, gin = ys[i], gout
         return handles, pairs
 
@@ -315,7 +321,16 @@ def bench_fvx(args, world, rank, local):
     torch.cuda.synchronize()
     fvx.device_status()
 
-    prof_kernel = args.profile_kernel or ("conv_f32" if fp32 else "conv_bf16_tc")
+    def kernel_of(i):
+        if fp32:
+            return "conv_f32"
+        if algos[i] == fvx.FVX_CONV_LEAF:
+            return "conv_leaf"
+        return "conv_bf16_tma" if convs[i]["cin"] % 16 == 0 else "conv_bf16_tc"
+
+    conv_kernels = [kernel_of(i) for i in range(len(convs))]
+    # the roofline follows the conv kernel doing the most arithmetic
+    prof_kernel = args.profile_kernel or conv_kernels[0]
     recs = EventRec()
     clocks = ClockSampler(local)
     clocks.start()
@@ -342,21 +357,34 @@ def bench_fvx(args, world, rank, local):
     K = args.steps
     value = U * K * world / t_total / 1e6
     esz = 4 if fp32 else 2
-    flops = sum(2.0 * c["cin"] * c["cout"] * p for c, p in zip(convs, pairs))
-    # algorithmic bytes of the conv launches of one step: feats read once,
-    # output written once (4 B fp32 / 2 B bf16), weights once, and the kernel
-    # map's (in, out) int32 pair read once
-    alg_bytes = 0
+    flops_i = [2.0 * c["cin"] * c["cout"] * p for c, p in zip(convs, pairs)]
+    flops = sum(flops_i)
+    # algorithmic bytes of each conv: feats read once, output written once
+    # (4 B fp32 / 2 B bf16), weights once, plus what locates the inputs: the
+    # kernel map's (in, out) int32 pair for the pair-list kernels, the output
+    # leaf's 80-byte record for the leaf-densified kernel
+    bytes_i = []
     n_in = U
     for i, (c, p) in enumerate(zip(convs, pairs)):
-        alg_bytes += n_in * c["cin"] * esz + n_out[i] * c["cout"] * ys[i].element_size() \
-            + 27 * c["cin"] * c["cout"] * esz + 8 * p
+        where = 80 * leaves_out[i] if conv_kernels[i] == "conv_leaf" else 8 * p
+        bytes_i.append(n_in * c["cin"] * esz + n_out[i] * c["cout"] * ys[i].element_size()
+                       + 27 * c["cin"] * c["cout"] * esz + where)
         n_in = n_out[i]
+    if not args.profile_kernel and len(convs) > 1:
+        prof_kernel = conv_kernels[max(range(len(convs)), key=lambda i: flops_i[i])]
+    mine = [i for i in range(len(convs)) if conv_kernels[i] == prof_kernel]
+    flops_p = sum(flops_i[i] for i in mine)
+    alg_bytes = sum(bytes_i[i] for i in mine)
+    # build + kernel map against HBM: per input row 170 B (key encode, radix
+    # passes, flag scans, sidecars), per output voxel 76 B plus 8 B per pair
+    # (coordinates, leaf words, mask, scans; the pair lists written once)
+    bk_bytes = 170.0 * w["coords"].shape[0] + sum(76.0 * n + 8.0 * p for n, p in zip(n_out, pairs))
 
     # roofline of the profiled kernel (all of its launches in the timed region)
     peaks, peak_kind = measured_peaks()
     roofline = None
-    if prof_n and prof_kernel in ("conv_bf16_tc", "conv_f32"):
+    if prof_n and mine:
+        flops = flops_p
         sec = prof_ms / 1e3
         per_launch = prof_n / K  # launches of the kernel per step
         intensity = flops / alg_bytes
@@ -374,7 +402,7 @@ def bench_fvx(args, world, rank, local):
             roofline = dict(bound="hbm", achieved=round(alg_bytes * K / sec / 1e9, 1), peak=peak, unit="GB/s",
                             peak_source=f"{peak_kind} (hbm_gbs)")
         roofline.update(kernel=prof_kernel, frac=round(roofline["achieved"] / roofline["peak"], 4),
-                        traffic=profiled_traffic(prof_kernel, w["name"]) if len(convs) == 1 else None,
+                        traffic=profiled_traffic(prof_kernel, w["name"]) if len(mine) == 1 else None,
                         algorithmic_bytes=int(alg_bytes / per_launch), flops=int(flops / per_launch),
                         avg_launch_ms=round(prof_ms / prof_n, 5), launches_per_step=int(per_launch))
 
@@ -411,9 +439,13 @@ def bench_fvx(args, world, rank, local):
                            l2="flushed between steps (256 MB write outside the step events)",
                            parallelism=f"replicas x{world}"),
                components=dict(build_kmap_mvoxels_s=round(U * K / (t["build"] + t["kmap"]) / 1e6, 2),
-                               conv_active_pair_tflops=round(flops * K / t["conv"] / 1e12, 4),
+                               conv_active_pair_tflops=round(sum(flops_i) * K / t["conv"] / 1e12, 4),
                                build_ms=round(t["build"] / K * 1e3, 4), kmap_ms=round(t["kmap"] / K * 1e3, 4),
-                               conv_ms=round(t["conv"] / K * 1e3, 4)),
+                               conv_ms=round(t["conv"] / K * 1e3, 4), conv_kernels=conv_kernels,
+                               build_kmap_hbm=dict(algorithmic_bytes=int(bk_bytes),
+                                                   achieved_gbs=round(bk_bytes * K / (t["build"] + t["kmap"]) / 1e9, 1),
+                                                   frac=round(bk_bytes * K / (t["build"] + t["kmap"]) / 1e9
+                                                              / peaks["hbm_gbs"], 4))),
                roofline=roofline, e2e=e2e, gpu_launches=int(launches), clocks=clk)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w)

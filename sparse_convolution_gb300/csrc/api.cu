@@ -140,6 +140,17 @@ LaunchScope::~LaunchScope() {
   }
 }
 
+// After a sync: a nonzero status word (staged to the host with the sync's
+// other values) means a bounded device-side wait gave up during the call.
+fvx_status check_staged_status(const char* who, uint32_t staged, cudaStream_t s) {
+  if (staged == 0u) return FVX_OK;
+  uint32_t* w = device_status_word();
+  if (w) cudaMemsetAsync(w, 0, 4, s);
+  set_error("%s: a bounded device-side wait gave up in this or an earlier unchecked call (device status %u)", who,
+            staged);
+  return staged == DEV_TIMEOUT ? FVX_ERR_DEVICE_TIMEOUT : FVX_ERR_CHECK;
+}
+
 fvx_status check_launch(const char* name) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {

@@ -637,9 +637,16 @@ fvx_status build_grid_device(const int32_t* coords, int64_t n, const int64_t* of
       k_gather_counts<<<1, 32, 0, s>>>(scanned, ntiles, dcounts + 4, dcounts);
     }
     FVX_TRY(check_launch("build_gather_counts"));
-    uint32_t* hc = (uint32_t*)pinned_staging(16);
+    uint32_t* hc = (uint32_t*)pinned_staging(20);
+    uint32_t* dstat = device_status_word();
+    if (!hc || !dstat) {
+      set_error("fvx_build_grid: staging buffer or device status word unavailable");
+      return FVX_ERR_ALLOC;
+    }
     FVX_CUDA(cudaMemcpyAsync(hc, dcounts, 16, cudaMemcpyDeviceToHost, s));
+    FVX_CUDA(cudaMemcpyAsync(hc + 4, dstat, 4, cudaMemcpyDeviceToHost, s));
     FVX_CUDA(cudaStreamSynchronize(s));
+    FVX_TRY(check_staged_status("fvx_build_grid", hc[4], s));
     for (int f = 0; f < 4; ++f) counts[f] = hc[f];
   }
 

@@ -73,6 +73,7 @@ struct LaunchScope {
   ~LaunchScope();
 };
 fvx_status check_launch(const char* name);
+fvx_status check_staged_status(const char* who, uint32_t staged, cudaStream_t s);
 
 // Device status word written by bounded waits / device-side checks.
 uint32_t* device_status_word();  // device pointer (per device, lazily set up)

@@ -409,10 +409,16 @@ extern "C" fvx_status fvx_kernel_map(fvx_grid gin, fvx_grid gout, int32_t ksize,
     k_list_offsets<<<1, 32, 0, s>>>(counts, Lo, dtot + 28, dtot);
   }
   FVX_TRY(check_launch("kmap_list_offsets"));
-  uint32_t* h = (uint32_t*)pinned_staging(28 * 4);
-  if (!h) return FVX_ERR_ALLOC;
+  uint32_t* h = (uint32_t*)pinned_staging(29 * 4);
+  uint32_t* dstat = device_status_word();
+  if (!h || !dstat) {
+    set_error("fvx_kernel_map: staging buffer or device status word unavailable");
+    return FVX_ERR_ALLOC;
+  }
   FVX_CUDA(cudaMemcpyAsync(h, dtot, 28 * 4, cudaMemcpyDeviceToHost, s));
+  FVX_CUDA(cudaMemcpyAsync(h + 28, dstat, 4, cudaMemcpyDeviceToHost, s));
   FVX_CUDA(cudaStreamSynchronize(s));
+  FVX_TRY(check_staged_status("fvx_kernel_map", h[28], s));
   for (int t = 0; t < 28; ++t) m->offsets_host[t] = h[t];
   const int64_t P = m->offsets_host[27];
   if (P >= (int64_t)INT32_MAX) {

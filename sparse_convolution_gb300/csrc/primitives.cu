@@ -1,12 +1,19 @@
 // Device-wide primitives for the IndexGrid build and the kernel map:
-//   * exclusive scan of uint32 (reduce, scan of tile sums, down-sweep);
-//   * stable LSD radix sort of (uint64 key, uint32 value) pairs, 8-bit digits,
-//     one histogram pass and one scatter pass per digit, with the per-(digit,
-//     tile) offsets produced by the scan above.
+//   * exclusive scan of uint32 in a single pass: each 2048-element tile
+//     publishes its sum, then its inclusive prefix, and every later tile adds
+//     up what its predecessors published (decoupled look-back);
+//   * stable LSD radix sort of (uint64 key, uint32 value) pairs, 8-bit digits:
+//     one kernel counts the digits of every pass in a single read of the keys,
+//     then one kernel per pass ranks each 4096-key tile in shared memory and
+//     takes the tile's output offset for each digit from the digit counts its
+//     predecessors published.
+// Tiles take their position from an atomic ticket, so a tile only ever waits
+// for tiles that started before it.  Every wait is bounded (2 s); one that
+// gives up records DEV_TIMEOUT in the device status word.
 // The pages run steps 3-9 of the build on library sort/RLE/scan primitives
 // ["fVDB: A Deep-Learning Framework for Sparse, Large Scale, and High
 // Performance Spatial Intelligence" notes, "GPU-accelerated IndexGrid build"];
-// these are written here for sm_103a with no device-side spin waits.
+// these are written here for sm_103a.
 #include <cuda_runtime.h>
 
 #include "block_scan.cuh"
@@ -14,59 +21,93 @@
 
 namespace fvx {
 
+// ============================================================== look-back helpers
+// Published words: bits 32-33 kind (1 = the tile's own total, 2 = inclusive
+// prefix through the tile), bits 40-47 a pass tag (radix sort), bits 0-31 the
+// value.  Zero = nothing published yet.
+constexpr uint64_t kLbAgg = 1ull << 32;
+constexpr uint64_t kLbInc = 2ull << 32;
+constexpr unsigned long long kLbWaitNs = 2000000000ull;
+constexpr int kLbWindow = 16;  // radix sort: predecessors read per round trip
+
+// A published word carries its own value and nothing else is read on the
+// strength of it, so relaxed device-scope accesses suffice (and several loads
+// can be in flight at once).
+__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned long long lb_clock() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
 // ============================================================== scan
 constexpr int kScanThreads = 256;
 constexpr int kScanItems = 8;
 constexpr int kScanTile = kScanThreads * kScanItems;  // 2048
 
-__global__ void __launch_bounds__(kScanThreads) k_scan_reduce(const uint32_t* __restrict__ in, int64_t n,
-                                                              uint32_t* __restrict__ partial) {
+__global__ void __launch_bounds__(kScanThreads) k_scan_1p(const uint32_t* in, uint32_t* out, int64_t n,
+                                                          uint32_t* __restrict__ total, uint64_t* flags,
+                                                          uint32_t* ticket, int64_t nt, uint32_t* status) {
   __shared__ uint32_t tmp[33];
-  const int64_t base = (int64_t)blockIdx.x * kScanTile;
-  uint32_t s = 0;
-#pragma unroll
-  for (int k = 0; k < kScanItems; ++k) {
-    int64_t i = base + k * kScanThreads + threadIdx.x;
-    if (i < n) s += in[i];
-  }
-  uint32_t tot;
-  block_exclusive_scan<uint32_t>(s, tmp, &tot);
-  if (threadIdx.x == 0) partial[blockIdx.x] = tot;
-}
-
-// Single block: exclusive scan of the tile sums in place; grand total to *total.
-__global__ void __launch_bounds__(1024) k_scan_partials(uint32_t* __restrict__ partial, int64_t np,
-                                                        uint32_t* __restrict__ total) {
-  __shared__ uint32_t tmp[33];
-  uint32_t carry = 0;
-  for (int64_t base = 0; base < np; base += 1024) {
-    int64_t i = base + threadIdx.x;
-    uint32_t v = (i < np) ? partial[i] : 0u;
-    uint32_t tot;
-    uint32_t ex = block_exclusive_scan<uint32_t>(v, tmp, &tot);
-    if (i < np) partial[i] = carry + ex;
-    carry += tot;
-  }
-  if (threadIdx.x == 0 && total) *total = carry;
-}
-
-__global__ void __launch_bounds__(kScanThreads) k_scan_down(const uint32_t* in, uint32_t* out, int64_t n,
-                                                            const uint32_t* __restrict__ partial) {
-  __shared__ uint32_t tmp[33];
-  const int64_t base = (int64_t)blockIdx.x * kScanTile + (int64_t)threadIdx.x * kScanItems;
+  __shared__ uint32_t s_tile, s_prefix;
+  if (threadIdx.x == 0) s_tile = atomicAdd(ticket, 1u);
+  __syncthreads();
+  const int64_t t = s_tile;
+  const int64_t base = t * kScanTile + (int64_t)threadIdx.x * kScanItems;
   uint32_t v[kScanItems];
-  uint32_t s = 0;
+  uint32_t sum = 0;
 #pragma unroll
   for (int k = 0; k < kScanItems; ++k) {
     v[k] = (base + k < n) ? in[base + k] : 0u;
-    s += v[k];
+    sum += v[k];
   }
-  uint32_t ex = block_exclusive_scan<uint32_t>(s, tmp, (uint32_t*)nullptr) + partial[blockIdx.x];
+  uint32_t tot;
+  uint32_t ex = block_exclusive_scan<uint32_t>(sum, tmp, &tot);
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    if (lane == 0) st_relaxed_u64(flags + t, (t == 0 ? kLbInc : kLbAgg) | tot);
+    uint32_t prefix = 0;
+    if (t > 0) {
+      // lane i looks at tile j - i; the window moves back 32 tiles at a time
+      int64_t j = t - 1;
+      const unsigned long long t0 = lb_clock();
+      for (uint32_t it = 1;; ++it) {
+        const int64_t jj = j - lane;
+        const uint64_t f = (jj >= 0) ? ld_relaxed_u64(flags + jj) : kLbInc;  // before tile 0: prefix 0
+        if (!__all_sync(0xffffffffu, ((f >> 32) & 3u) != 0u)) {
+          int give_up = 0;
+          if (lane == 0 && (it & 255u) == 0u && lb_clock() - t0 > kLbWaitNs) give_up = 1;
+          if (__shfl_sync(0xffffffffu, give_up, 0)) {
+            if (lane == 0) report_device_error(status, DEV_TIMEOUT);
+            break;
+          }
+          continue;
+        }
+        const uint32_t incl = __ballot_sync(0xffffffffu, ((f >> 32) & 3u) == 2u);
+        const int first = incl ? __ffs(incl) - 1 : 32;  // nearest tile with an inclusive prefix
+        prefix += warp_reduce_sum<uint32_t>(lane <= first ? (uint32_t)f : 0u);
+        if (incl) break;
+        j -= 32;
+      }
+      if (lane == 0) st_relaxed_u64(flags + t, kLbInc | (uint32_t)(prefix + tot));
+    }
+    if (lane == 0) s_prefix = prefix;
+  }
+  __syncthreads();
+  ex += s_prefix;
 #pragma unroll
   for (int k = 0; k < kScanItems; ++k) {
     if (base + k < n) out[base + k] = ex;
     ex += v[k];
   }
+  if (t == nt - 1 && threadIdx.x == 0 && total) *total = s_prefix + tot;
 }
 
 fvx_status scan_exclusive_u32(const uint32_t* in, uint32_t* out, int64_t n, uint32_t* total, cudaStream_t s,
@@ -75,24 +116,20 @@ fvx_status scan_exclusive_u32(const uint32_t* in, uint32_t* out, int64_t n, uint
     if (total) FVX_CUDA(cudaMemsetAsync(total, 0, 4, s));
     return FVX_OK;
   }
+  uint32_t* status = device_status_word();
+  if (!status) {
+    set_error("scan: device status word unavailable");
+    return FVX_ERR_CUDA;
+  }
   const int64_t nt = (n + kScanTile - 1) / kScanTile;
-  uint32_t* partial = scr.get<uint32_t>((size_t)nt);
-  if (!partial) return FVX_ERR_ALLOC;
+  uint64_t* flags = scr.get<uint64_t>((size_t)nt + 1);  // tile words, then the ticket
+  if (!flags) return FVX_ERR_ALLOC;
+  FVX_CUDA(cudaMemsetAsync(flags, 0, 8 * ((size_t)nt + 1), s));
   {
-    LaunchScope ls("scan_reduce", s);
-    k_scan_reduce<<<(unsigned)nt, kScanThreads, 0, s>>>(in, n, partial);
+    LaunchScope ls("scan_1p", s);
+    k_scan_1p<<<(unsigned)nt, kScanThreads, 0, s>>>(in, out, n, total, flags, (uint32_t*)(flags + nt), nt, status);
   }
-  FVX_TRY(check_launch("scan_reduce"));
-  {
-    LaunchScope ls("scan_partials", s);
-    k_scan_partials<<<1, 1024, 0, s>>>(partial, nt, total);
-  }
-  FVX_TRY(check_launch("scan_partials"));
-  {
-    LaunchScope ls("scan_down", s);
-    k_scan_down<<<(unsigned)nt, kScanThreads, 0, s>>>(in, out, n, partial);
-  }
-  return check_launch("scan_down");
+  return check_launch("scan_1p");
 }
 
 // ============================================================== radix sort
@@ -103,20 +140,33 @@ constexpr int kRsTile = kRsThreads * kRsItems;     // 4096 keys per tile
 constexpr int kRsWarpItems = kRsTile / kRsWarps;   // 512 consecutive keys per warp
 constexpr int kRsRounds = kRsWarpItems / 32;       // 16
 
-__global__ void __launch_bounds__(kRsThreads) k_radix_hist(const uint64_t* __restrict__ keys, int64_t n, int shift,
-                                                           uint32_t dmask, uint32_t* __restrict__ counts,
-                                                           int64_t ntiles) {
-  __shared__ uint32_t h[256];
-  h[threadIdx.x] = 0;
+constexpr int kRsMaxPasses = 8;                    // 64-bit keys
+constexpr int kRsHistTile = 4096;                  // keys per block of the counting kernel
+
+// Digit counts of every pass in one read of the keys: ghist[p][d] += number of
+// keys whose pass-p digit is d (block counts in shared memory, then one global
+// add per nonzero count).
+__global__ void __launch_bounds__(kRsThreads) k_radix_hist_all(const uint64_t* __restrict__ keys, int64_t n,
+                                                               int bit_lo, int bit_hi, int passes,
+                                                               uint32_t* __restrict__ ghist) {
+  __shared__ uint32_t h[kRsMaxPasses * 256];
+  for (int i = threadIdx.x; i < passes * 256; i += kRsThreads) h[i] = 0u;
   __syncthreads();
-  const int64_t base = (int64_t)blockIdx.x * kRsTile;
+  const int64_t b0 = (int64_t)blockIdx.x * kRsHistTile;
 #pragma unroll 4
-  for (int k = 0; k < kRsItems; ++k) {
-    int64_t i = base + k * kRsThreads + threadIdx.x;
-    if (i < n) atomicAdd(&h[(uint32_t)(keys[i] >> shift) & dmask], 1u);
+  for (int k = 0; k < kRsHistTile / kRsThreads; ++k) {
+    const int64_t i = b0 + k * kRsThreads + threadIdx.x;
+    if (i < n) {
+      const uint64_t key = keys[i];
+      for (int p = 0; p < passes; ++p) {
+        const int lo = bit_lo + 8 * p, nb = (bit_hi - lo) < 8 ? (bit_hi - lo) : 8;
+        atomicAdd(&h[p * 256 + ((uint32_t)(key >> lo) & ((1u << nb) - 1u))], 1u);
+      }
+    }
   }
   __syncthreads();
-  counts[(int64_t)threadIdx.x * ntiles + blockIdx.x] = h[threadIdx.x];
+  for (int i = threadIdx.x; i < passes * 256; i += kRsThreads)
+    if (h[i]) atomicAdd(&ghist[i], h[i]);
 }
 
 struct RsSmem {
@@ -128,19 +178,28 @@ struct RsSmem {
   uint32_t tmp[33];
 };
 
-__global__ void __launch_bounds__(kRsThreads) k_radix_scatter(const uint64_t* __restrict__ kin,
-                                                              const uint32_t* __restrict__ vin,
-                                                              uint64_t* __restrict__ kout, uint32_t* __restrict__ vout,
-                                                              int64_t n, int shift, uint32_t dmask,
-                                                              const uint32_t* __restrict__ offs, int64_t ntiles) {
+// One pass: tile t (by ticket) ranks its 4096 keys by digit in shared
+// memory, publishes its count of each digit, adds up the counts its
+// predecessors published (thread d follows digit d), publishes the inclusive
+// count and writes each key to digit_start[d] + predecessors' count + rank.
+__global__ void __launch_bounds__(kRsThreads) k_radix_onesweep(const uint64_t* __restrict__ kin,
+                                                               const uint32_t* __restrict__ vin,
+                                                               uint64_t* __restrict__ kout,
+                                                               uint32_t* __restrict__ vout, int64_t n, int shift,
+                                                               uint32_t dmask, const uint32_t* __restrict__ ghist,
+                                                               uint64_t* state, uint32_t* ticket, uint32_t tag,
+                                                               uint32_t* status) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   RsSmem& sm = *reinterpret_cast<RsSmem*>(smem_raw);
+  __shared__ uint32_t s_tile;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) s_tile = atomicAdd(ticket, 1u);
   for (int d = lane; d < 256; d += 32) sm.whist[warp][d] = 0;
-  sm.goff[tid] = offs[(int64_t)tid * ntiles + blockIdx.x];
-  __syncwarp();
+  // where each digit starts in the output: exclusive scan of the pass's counts
+  const uint32_t gstart = block_exclusive_scan<uint32_t>(ghist[tid], sm.tmp, (uint32_t*)nullptr);
+  const int64_t t = s_tile;  // visible after the scan's barriers
 
-  const int64_t base = (int64_t)blockIdx.x * kRsTile + (int64_t)warp * kRsWarpItems;
+  const int64_t base = t * kRsTile + (int64_t)warp * kRsWarpItems;
   uint64_t key[kRsRounds];
   uint32_t val[kRsRounds];
   uint32_t rank[kRsRounds];
@@ -160,7 +219,7 @@ __global__ void __launch_bounds__(kRsThreads) k_radix_scatter(const uint64_t* __
     rank[r] = old + __popc(peers & lt);
   }
   __syncthreads();
-  {  // per digit: exclusive over warps, then exclusive over digits of the tile totals
+  {  // per digit: exclusive over warps, the tile's count, then the look-back
     const int d = tid;
     uint32_t run = 0;
 #pragma unroll
@@ -169,8 +228,41 @@ __global__ void __launch_bounds__(kRsThreads) k_radix_scatter(const uint64_t* __
       sm.whist[w][d] = run;
       run += c;
     }
-    uint32_t ex = block_exclusive_scan<uint32_t>(run, sm.tmp, (uint32_t*)nullptr);
-    sm.dexcl[d] = ex;
+    const uint64_t tagbits = (uint64_t)tag << 40;
+    uint64_t* mine = state + t * 256 + d;
+    st_relaxed_u64(mine, tagbits | (t == 0 ? kLbInc : kLbAgg) | run);
+    uint32_t prefix = 0;
+    if (t > 0) {
+      // kLbWindow predecessors per round trip, nearest first; the walk stops
+      // at the first inclusive word and resumes at the first unpublished one
+      const unsigned long long t0 = lb_clock();
+      int64_t j = t - 1;
+      bool done = false;
+      for (uint32_t it = 1; !done; ++it) {
+        uint64_t f[kLbWindow];
+#pragma unroll
+        for (int q = 0; q < kLbWindow; ++q)
+          f[q] = (j - q >= 0) ? ld_relaxed_u64(state + (j - q) * 256 + d) : (tagbits | kLbInc);  // before tile 0
+        int q = 0;
+#pragma unroll
+        for (int r = 0; r < kLbWindow; ++r) {
+          if (q != r || done) continue;
+          const bool ready = (uint32_t)(f[r] >> 40) == tag && ((f[r] >> 32) & 3u) != 0u;
+          if (!ready) continue;
+          prefix += (uint32_t)f[r];
+          done = ((f[r] >> 32) & 3u) == 2u;
+          q = r + 1;
+        }
+        j -= q;
+        if (!done && q < kLbWindow && (it & 63u) == 0u && lb_clock() - t0 > kLbWaitNs) {
+          report_device_error(status, DEV_TIMEOUT);
+          break;
+        }
+      }
+      st_relaxed_u64(mine, tagbits | kLbInc | (uint32_t)(prefix + run));
+    }
+    sm.goff[d] = gstart + prefix;
+    sm.dexcl[d] = block_exclusive_scan<uint32_t>(run, sm.tmp, (uint32_t*)nullptr);
   }
   __syncthreads();
 #pragma unroll
@@ -184,7 +276,7 @@ __global__ void __launch_bounds__(kRsThreads) k_radix_scatter(const uint64_t* __
     }
   }
   __syncthreads();
-  const int64_t tbase = (int64_t)blockIdx.x * kRsTile;
+  const int64_t tbase = t * kRsTile;
   const int tile_n = (int)((n - tbase) < kRsTile ? (n - tbase) : kRsTile);
   for (int i = tid; i < tile_n; i += kRsThreads) {
     const uint64_t k = sm.keys[i];
@@ -199,30 +291,44 @@ fvx_status radix_sort_pairs(uint64_t* k0, uint32_t* v0, uint64_t* k1, uint32_t* 
                             int bit_hi, cudaStream_t s, bool* result_in_1, Scratch& scr) {
   *result_in_1 = false;
   if (n <= 1 || bit_hi <= bit_lo) return FVX_OK;
-  FVX_CUDA(cudaFuncSetAttribute(k_radix_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(RsSmem)));
+  uint32_t* status = device_status_word();
+  if (!status) {
+    set_error("radix sort: device status word unavailable");
+    return FVX_ERR_CUDA;
+  }
+  FVX_CUDA(cudaFuncSetAttribute(k_radix_onesweep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(RsSmem)));
+  const int passes = (bit_hi - bit_lo + 7) / 8;
   const int64_t ntiles = (n + kRsTile - 1) / kRsTile;
-  uint32_t* counts = scr.get<uint32_t>((size_t)(256 * ntiles));
-  if (!counts) return FVX_ERR_ALLOC;
+  // one zeroed region: digit counts [passes][256], tickets [8], then the
+  // published words [ntiles][256] shared by all passes (told apart by tag)
+  const size_t words32 = (size_t)passes * 256 + kRsMaxPasses;
+  uint64_t* region = scr.get<uint64_t>(words32 / 2 + (size_t)ntiles * 256);
+  if (!region) return FVX_ERR_ALLOC;
+  uint32_t* ghist = reinterpret_cast<uint32_t*>(region);
+  uint32_t* tickets = ghist + (size_t)passes * 256;
+  uint64_t* state = region + words32 / 2;
+  FVX_CUDA(cudaMemsetAsync(region, 0, 8 * (words32 / 2 + (size_t)ntiles * 256), s));
+  {
+    LaunchScope ls("radix_hist_all", s);
+    const int64_t nb = (n + kRsHistTile - 1) / kRsHistTile;
+    k_radix_hist_all<<<(unsigned)nb, kRsThreads, 0, s>>>(k0, n, bit_lo, bit_hi, passes, ghist);
+  }
+  FVX_TRY(check_launch("radix_hist_all"));
   uint64_t* ks = k0;
   uint32_t* vs = v0;
   uint64_t* kd = k1;
   uint32_t* vd = v1;
   bool in1 = false;
-  for (int lo = bit_lo; lo < bit_hi; lo += 8) {
+  for (int p = 0; p < passes; ++p) {
+    const int lo = bit_lo + 8 * p;
     const int nb = (bit_hi - lo) < 8 ? (bit_hi - lo) : 8;
     const uint32_t dmask = (1u << nb) - 1u;
     {
-      LaunchScope ls("radix_hist", s);
-      k_radix_hist<<<(unsigned)ntiles, kRsThreads, 0, s>>>(ks, n, lo, dmask, counts, ntiles);
+      LaunchScope ls("radix_onesweep", s);
+      k_radix_onesweep<<<(unsigned)ntiles, kRsThreads, sizeof(RsSmem), s>>>(
+          ks, vs, kd, vd, n, lo, dmask, ghist + (size_t)p * 256, state, tickets + p, (uint32_t)(p + 1), status);
     }
-    FVX_TRY(check_launch("radix_hist"));
-    FVX_TRY(scan_exclusive_u32(counts, counts, 256 * ntiles, nullptr, s, scr));
-    {
-      LaunchScope ls("radix_scatter", s);
-      k_radix_scatter<<<(unsigned)ntiles, kRsThreads, sizeof(RsSmem), s>>>(ks, vs, kd, vd, n, lo, dmask, counts,
-                                                                           ntiles);
-    }
-    FVX_TRY(check_launch("radix_scatter"));
+    FVX_TRY(check_launch("radix_onesweep"));
     uint64_t* tk = ks; ks = kd; kd = tk;
     uint32_t* tv = vs; vs = vd; vd = tv;
     in1 = !in1;
