@@ -185,16 +185,18 @@ fvx_status fvx_sparse_conv(fvx_grid gin, fvx_grid gout, fvx_kmap m, fvx_dtype dt
  * the leaf-densified one for low channel counts on leaves at least 20%
  * occupied, picked per case].
  *   FVX_CONV_AUTO    (default) leaf-densified when the map has stride 1,
- *                    cin <= 16, cout <= 64 and the output grid's leaves are
- *                    at least 20% occupied on average; pair-list gather
+ *                    cin is 8 or 16, cout <= 64 and the output grid's leaves
+ *                    are at least 20% occupied on average; pair-list gather
  *                    otherwise.
  *   FVX_CONV_GATHER  always the pair-list kernels (128 consecutive outputs
  *                    per tile; rows fetched by TMA gather4 when cin is a
  *                    multiple of 16, else by cp.async).
  *   FVX_CONV_LEAF    always leaf-densified (each output leaf's 10^3 input
  *                    window staged densely in shared memory; the pair lists
- *                    are not read); a call it cannot serve (stride 2,
- *                    cin > 16, cout > 64) fails with FVX_ERR_INVALID_ARG.
+ *                    are not read; the map's per-leaf table of neighbouring
+ *                    input leaves is); a call it cannot serve (stride 2, cin
+ *                    other than 8 or 16, cout > 64) fails with
+ *                    FVX_ERR_INVALID_ARG.
  * Process-wide; FVX_F32 is unaffected.  Every path meets the same error
  * bound.  Errors: FVX_ERR_INVALID_ARG for an unknown value. */
 typedef enum { FVX_CONV_AUTO = 0, FVX_CONV_GATHER = 1, FVX_CONV_LEAF = 2 } fvx_conv_algo;

@@ -999,7 +999,8 @@ struct LeafNbr {           // one neighbouring input leaf (zeros when absent)
 };
 
 struct LeafConvArgs {
-  GridDev gi;                   // input grid
+  const uint64_t* in_rec;       // input grid leaf records [L][10]
+  const int32_t* nbr;           // [L_out][27] input leaf per leaf offset (the kernel map's table), -1 absent
   const int32_t* out_origin;    // output grid leaves: origin [L][3], batch [L], record [L][10]
   const int32_t* out_batch;
   const uint64_t* out_rec;
@@ -1020,6 +1021,7 @@ __device__ __forceinline__ uint32_t leaf_index_in(const LeafNbr& L, int n, bool&
   return L.first + pre + (uint32_t)__popcll(m & ((1ull << bit) - 1ull));
 }
 
+template <int G8>  // cin / 8
 __global__ void __launch_bounds__(kLeafThreads) k_conv_leaf(const __grid_constant__ LeafConvArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* halo = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -1028,7 +1030,7 @@ __global__ void __launch_bounds__(kLeafThreads) k_conv_leaf(const __grid_constan
   unsigned long long* done = reinterpret_cast<unsigned long long*>(nbr + 27);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int cin = a.cin, cout = a.cout, g8 = cin >> 3;
+  const int cin = a.cin, cout = a.cout, g8 = G8;
   const int64_t L = blockIdx.x;
   if (L >= a.n_leaf_out) return;
 
@@ -1042,15 +1044,12 @@ __global__ void __launch_bounds__(kLeafThreads) k_conv_leaf(const __grid_constan
     mbar_init(smem_u32(done), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  const int ob = __ldg(a.out_batch + L);
-  const int ox = __ldg(a.out_origin + 3 * L), oy = __ldg(a.out_origin + 3 * L + 1), oz = __ldg(a.out_origin + 3 * L + 2);
   // the 27 input leaves around the output leaf (slot = (ex+1)*9 + (ey+1)*3 + (ez+1))
   if (tid < 27) {
-    const int ex = tid / 9 - 1, ey = (tid / 3) % 3 - 1, ez = tid % 3 - 1;
-    const int l = find_leaf(a.gi, ob, ox + 8 * ex, oy + 8 * ey, oz + 8 * ez);
+    const int l = __ldg(a.nbr + L * 27 + tid);
     LeafNbr& nb = nbr[tid];
     if (l >= 0) {
-      const uint64_t* rec = a.gi.leaf_rec + (size_t)l * 10;
+      const uint64_t* rec = a.in_rec + (size_t)l * 10;
 #pragma unroll
       for (int w = 0; w < 8; ++w) nb.mask[w] = __ldg(reinterpret_cast<const unsigned long long*>(rec) + w);
       nb.first = (uint32_t)__ldg(reinterpret_cast<const unsigned long long*>(rec) + 8);
@@ -1079,25 +1078,40 @@ __global__ void __launch_bounds__(kLeafThreads) k_conv_leaf(const __grid_constan
   }
   __syncthreads();
   // halo: position (hx, hy, hz) in -1..8 relative to the origin, one 16-byte
-  // piece (8 channels) per item, written to every x-shifted plane holding it
+  // piece (8 channels) per item, written to every x-shifted plane holding it;
+  // a thread issues all its loads before its first store
   {
-    const int nitem = 1000 * g8;
-    for (int e = tid; e < nitem; e += kLeafThreads) {
-      const int pos = e / g8, c8 = e - pos * g8;
-      const int hx = pos / 100 - 1, hy = (pos / 10) % 10 - 1, hz = pos % 10 - 1;
-      const int ex = (hx < 0) ? -1 : (hx > 7 ? 1 : 0), ey = (hy < 0) ? -1 : (hy > 7 ? 1 : 0),
-                ez = (hz < 0) ? -1 : (hz > 7 ? 1 : 0);
-      bool act;
-      const uint32_t idx = leaf_index_in(nbr[(ex + 1) * 9 + (ey + 1) * 3 + (ez + 1)],
-                                         ((hx & 7) << 6) | ((hy & 7) << 3) | (hz & 7), act);
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (act) v = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)idx * cin + 8 * c8));
-      const int rbase = (hy + 1) * 80 + (hz + 1);  // row without the x term
+    constexpr int kNItem = 1000 * G8;
+    constexpr int kPer = (kNItem + kLeafThreads - 1) / kLeafThreads;
+    uint4 v[kPer];
 #pragma unroll
-      for (int cx = 0; cx < 3; ++cx) {
-        const int xx = hx - cx + 1;  // x of the plane row holding this position
-        if (xx >= 0 && xx < 8) {
-          *reinterpret_cast<uint4*>(halo + (size_t)(c8 * 3 + cx) * kLeafPlaneBytes + (size_t)(rbase + xx * 10) * 16) = v;
+    for (int q = 0; q < kPer; ++q) {
+      const int e = tid + q * kLeafThreads;
+      v[q] = make_uint4(0u, 0u, 0u, 0u);
+      if (e < kNItem) {
+        const int pos = e / G8, c8 = e - pos * G8;
+        const int hx = pos / 100 - 1, hy = (pos / 10) % 10 - 1, hz = pos % 10 - 1;
+        const int ex = (hx < 0) ? -1 : (hx > 7 ? 1 : 0), ey = (hy < 0) ? -1 : (hy > 7 ? 1 : 0),
+                  ez = (hz < 0) ? -1 : (hz > 7 ? 1 : 0);
+        bool act;
+        const uint32_t idx = leaf_index_in(nbr[(ex + 1) * 9 + (ey + 1) * 3 + (ez + 1)],
+                                           ((hx & 7) << 6) | ((hy & 7) << 3) | (hz & 7), act);
+        if (act) v[q] = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)idx * cin + 8 * c8));
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      const int e = tid + q * kLeafThreads;
+      if (e < kNItem) {
+        const int pos = e / G8, c8 = e - pos * G8;
+        const int hx = pos / 100 - 1, hy = (pos / 10) % 10 - 1, hz = pos % 10 - 1;
+        const int rbase = (hy + 1) * 80 + (hz + 1);  // row without the x term
+#pragma unroll
+        for (int cx = 0; cx < 3; ++cx) {
+          const int xx = hx - cx + 1;  // x of the plane row holding this position
+          if (xx >= 0 && xx < 8)
+            *reinterpret_cast<uint4*>(halo + (size_t)(c8 * 3 + cx) * kLeafPlaneBytes + (size_t)(rbase + xx * 10) * 16) =
+                v[q];
         }
       }
     }
@@ -1245,7 +1259,8 @@ fvx_status launch_conv_leaf(const char* who, fvx_grid gin, fvx_kmap m, fvx_dtype
                             int64_t cout, void* out, const __nv_bfloat16* wt, uint32_t* status, cudaStream_t s) {
   const fvx_grid_s* go = m->gout;
   LeafConvArgs a;
-  a.gi = grid_dev(gin);
+  a.in_rec = gin->leaf_rec;
+  a.nbr = m->leaf_nbr;
   a.out_origin = go->leaf_origin;
   a.out_batch = go->leaf_batch;
   a.out_rec = go->leaf_rec;
@@ -1270,10 +1285,11 @@ fvx_status launch_conv_leaf(const char* who, fvx_grid gin, fvx_kmap m, fvx_dtype
   FVX_CUDA(cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev));
   const size_t per_sm = (size_t)(512 / cols);  // blocks whose accumulators fit in TMEM together
   if ((size_t)sm_bytes / (smem + reserved) > per_sm) smem = (size_t)sm_bytes / (per_sm + 1) - reserved + 16;
-  FVX_CUDA(cudaFuncSetAttribute(k_conv_leaf, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  auto kern = (cin == 16) ? k_conv_leaf<2> : k_conv_leaf<1>;
+  FVX_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   {
     LaunchScope ls("conv_leaf", s);
-    k_conv_leaf<<<(unsigned)go->n_leaf, kLeafThreads, smem, s>>>(a);
+    kern<<<(unsigned)go->n_leaf, kLeafThreads, smem, s>>>(a);
   }
   FVX_TRY(check_launch("conv_leaf"));
   (void)who;
@@ -1285,9 +1301,9 @@ fvx_status launch_conv_bf16(const char* who, fvx_grid gin, fvx_kmap m, fvx_dtype
                             int64_t cout, void* out, const __nv_bfloat16* wt, uint32_t* status, cudaStream_t s) {
   const int64_t nt = m->n_tiles;
   const int algo = g_conv_algo.load(std::memory_order_relaxed);
-  const bool leaf_ok = m->stride == 1 && cin <= kLeafMaxCin && cout <= kLeafMaxCout;
+  const bool leaf_ok = m->stride == 1 && m->leaf_nbr != nullptr && (cin == 8 || cin == 16) && cout <= kLeafMaxCout;
   if (algo == FVX_CONV_LEAF && !leaf_ok) {
-    set_error("%s: the leaf-densified convolution needs stride 1, cin <= %d and cout <= %d (got stride %d, %lld, %lld)",
+    set_error("%s: the leaf-densified convolution needs stride 1, cin 8 or %d and cout <= %d (got stride %d, %lld, %lld)",
               who, kLeafMaxCin, kLeafMaxCout, (int)m->stride, (long long)cin, (long long)cout);
     return FVX_ERR_INVALID_ARG;
   }

@@ -134,6 +134,9 @@ struct fvx_kmap_s {
   // is the position in in_idx of the first pair of list s with output >= t*kTileRows.
   uint32_t* tile_start = nullptr;
   int64_t n_tiles = 0;
+  // stride 1: for each output leaf, the input leaf at each of the 27 leaf
+  // offsets ((ex+1)*9 + (ey+1)*3 + ez+1, -1 if absent); null for stride 2
+  int32_t* leaf_nbr = nullptr;
   const fvx_grid_s* gin = nullptr;
   const fvx_grid_s* gout = nullptr;
 };

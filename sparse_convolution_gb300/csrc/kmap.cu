@@ -380,8 +380,11 @@ extern "C" fvx_status fvx_kernel_map(fvx_grid gin, fvx_grid gout, int32_t ksize,
   uint32_t* dtot = scr.get<uint32_t>(32);
   if (!counts || !dtot) return FVX_ERR_ALLOC;
   // mask + conv tiling live in the first block, pairs in the second
+  // (and, for stride 1, the input-leaf slot table the count pass writes,
+  // which the leaf-densified convolution reads too)
   const size_t o_mask = 0, o_tile = align_up(4 * (size_t)Nout);
-  const size_t bytes1 = o_tile + align_up(4 * (size_t)(27 * m->n_tiles + 1));
+  const size_t o_nbr = o_tile + align_up(4 * (size_t)(27 * m->n_tiles + 1));
+  const size_t bytes1 = o_nbr + (stride == 1 ? align_up(4 * (size_t)(27 * Lo + 1)) : 0);
   m->block = dalloc(bytes1, s);
   if (!m->block) return FVX_ERR_ALLOC;
   m->out_mask = (uint32_t*)((char*)m->block + o_mask);
@@ -390,8 +393,8 @@ extern "C" fvx_status fvx_kernel_map(fvx_grid gin, fvx_grid gout, int32_t ksize,
   const GridDev gd = grid_dev(gin);
   int32_t* nbr = nullptr;  // stride 1: input-leaf slot table written by the count pass
   if (stride == 1) {
-    nbr = scr.get<int32_t>((size_t)(27 * Lo + 1));
-    if (!nbr) return FVX_ERR_ALLOC;
+    nbr = (int32_t*)((char*)m->block + o_nbr);
+    m->leaf_nbr = nbr;
   }
   if (Lo > 0) {
     LaunchScope ls("kmap_count", s);
