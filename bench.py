@@ -40,6 +40,8 @@ def parse():
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", default="fvx", choices=["fvx", "reference"])
     p.add_argument("--workload", default="leaf_dense")
+    p.add_argument("--scale", type=float, default=1.0,
+                   help="smaller instance of the same workload generator (< 1), e.g. for profiler captures")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--profile-kernel", default=None, help="kernel whose launches are timed for the roofline")
     return p.parse_args()
@@ -162,11 +164,11 @@ def measured_peaks():
 
 
 # ---------------------------------------------------------------- workload
-def make_workload(name):
+def make_workload(name, scale=1.0):
     from sparse_convolution_gb300 import synth
 
-    w = synth.WORKLOADS[name]()
-    return w
+    f = synth.WORKLOADS[name]
+    return f(scale=scale) if scale != 1.0 else f()
 
 
 def oracle_sample(w, target_rows=250_000):
@@ -223,7 +225,7 @@ def bench_fvx(args, world, rank, local):
     torch.cuda.set_device(local)
     build_lib.build()
     fvx.load()
-    w = make_workload(args.workload)
+    w = make_workload(args.workload, args.scale)
     convs = w["convs"]
     fp32 = w["dtype"] == "f32"
     dev = torch.device("cuda", local)
@@ -459,7 +461,7 @@ def bench_reference(args, world, rank):
     import oracle
 
     oracle.build()
-    w = make_workload(args.workload)
+    w = make_workload(args.workload, args.scale)
     coords, offs, desc = oracle_sample(w, target_rows=120_000)
     cv = w["convs"][0]
     for _ in range(args.warmup):
