@@ -150,14 +150,24 @@ fvx_status fvx_coarsen(fvx_grid g, int32_t stride, fvx_stream stream, fvx_grid* 
  * the same batch.  Pairs are grouped by s, and inside a group ordered by q.
  * ksize must be 3; stride 1 (submanifold: pass gout == gin) or 2 (gout is
  * usually fvx_coarsen(gin, 2)).  gin and gout must have the same batch size.
- * Synchronises the stream once (to size the pair lists; never truncated).
- * [DriveRT, "Compilation and deployment": dynamic sizes, no truncation] */
+ * Does not synchronise: the pair lists are sized for every output having all
+ * 27 neighbours (216 bytes per output voxel of device memory) and the list
+ * offsets stay on the device until fvx_kmap_view is asked for them.  Maps
+ * whose worst case exceeds 8 GiB (environment FVX_KMAP_CAP_BYTES, read once)
+ * or the int32 pair index range synchronise once to size the lists exactly.
+ * Never truncated.
+ * [DriveRT, "Counts kept on the GPU"; "Compilation and deployment": dynamic
+ * sizes, no truncation] */
 fvx_status fvx_kernel_map(fvx_grid gin, fvx_grid gout, int32_t ksize, int32_t stride, fvx_stream stream,
                           fvx_kmap* out);
 
 /* offsets_host: HOST int64 [28] (list s is [offsets[s], offsets[s+1]));
  * in_idx / out_idx: device int32 [n_pairs]; out_mask: device uint32 [n_out],
- * bit s set when output q has a neighbour at slot s.  All owned by the map. */
+ * bit s set when output q has a neighbour at slot s.  All owned by the map.
+ * Any argument may be NULL.  Asking for offsets_host or n_pairs the first
+ * time synchronises the stream the map was built on (which must still exist)
+ * and may return FVX_ERR_DEVICE_TIMEOUT; the pointers and n_out need no
+ * device work. */
 fvx_status fvx_kmap_view(fvx_kmap m, const int64_t** offsets_host, const int32_t** in_idx, const int32_t** out_idx,
                          const uint32_t** out_mask, int64_t* n_pairs, int64_t* n_out);
 

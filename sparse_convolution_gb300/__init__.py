@@ -216,13 +216,32 @@ class KernelMap:
         _check(load().fvx_kernel_map(gin._h, gout._h, int(ksize), int(stride), _stream(stream), ctypes.byref(h)))
         self._h = h
         self.gin, self.gout, self.stride = gin, gout, int(stride)
-        offs, ii, oo, mm = ctypes.c_void_p(), ctypes.c_void_p(), ctypes.c_void_p(), ctypes.c_void_p()
-        npairs, nout = ctypes.c_int64(), ctypes.c_int64()
-        _check(_lib.fvx_kmap_view(h, ctypes.byref(offs), ctypes.byref(ii), ctypes.byref(oo), ctypes.byref(mm),
-                                  ctypes.byref(npairs), ctypes.byref(nout)))
-        self.offsets = np.ctypeslib.as_array((ctypes.c_int64 * 28).from_address(offs.value)).copy()
-        self.n_pairs, self.n_out = int(npairs.value), int(nout.value)
+        ii, oo, mm = ctypes.c_void_p(), ctypes.c_void_p(), ctypes.c_void_p()
+        nout = ctypes.c_int64()
+        _check(_lib.fvx_kmap_view(h, None, ctypes.byref(ii), ctypes.byref(oo), ctypes.byref(mm), None,
+                                  ctypes.byref(nout)))
+        self.n_out = int(nout.value)
         self._ptrs = (ii.value, oo.value, mm.value)
+        self._totals = None
+
+    def _read_totals(self):
+        # the list offsets stay on the device until first asked for (that read
+        # synchronises the map's stream)
+        if self._totals is None:
+            offs, npairs = ctypes.c_void_p(), ctypes.c_int64()
+            _check(_lib.fvx_kmap_view(self._h, ctypes.byref(offs), None, None, None, ctypes.byref(npairs), None))
+            self._totals = (np.ctypeslib.as_array((ctypes.c_int64 * 28).from_address(offs.value)).copy(),
+                            int(npairs.value))
+        return self._totals
+
+    @property
+    def offsets(self):
+        """HOST int64 [28]: list s is pairs [offsets[s], offsets[s+1])."""
+        return self._read_totals()[0]
+
+    @property
+    def n_pairs(self):
+        return self._read_totals()[1]
 
     def destroy(self):
         if getattr(self, "_h", None) and _lib is not None:

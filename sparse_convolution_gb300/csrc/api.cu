@@ -334,6 +334,7 @@ fvx_status fvx_kmap_view(fvx_kmap m, const int64_t** offsets_host, const int32_t
     set_error("fvx_kmap_view: NULL kernel map");
     return FVX_ERR_INVALID_ARG;
   }
+  if (offsets_host || n_pairs) FVX_TRY(kmap_read_totals(m, "fvx_kmap_view"));
   if (offsets_host) *offsets_host = m->offsets_host;
   if (in_idx) *in_idx = m->in_idx;
   if (out_idx) *out_idx = m->out_idx;

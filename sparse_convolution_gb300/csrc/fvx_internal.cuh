@@ -74,6 +74,11 @@ struct LaunchScope {
 };
 fvx_status check_launch(const char* name);
 fvx_status check_staged_status(const char* who, uint32_t staged, cudaStream_t s);
+// Kernel map pair lists are allocated for 27 pairs per output (no count
+// read-back) up to this many bytes (environment FVX_KMAP_CAP_BYTES, default
+// 8 GiB); larger maps read the count first and allocate it exactly.
+size_t kmap_capacity_limit();
+fvx_status kmap_read_totals(fvx_kmap_s* m, const char* who);
 
 // Device status word written by bounded waits / device-side checks.
 uint32_t* device_status_word();  // device pointer (per device, lazily set up)
@@ -124,6 +129,11 @@ struct fvx_kmap_s {
   int32_t stride = 1;
   int64_t n_out = 0, n_pairs = 0;
   int64_t offsets_host[28] = {0};
+  // the 28 list offsets on the device; copied to offsets_host / n_pairs on
+  // the first request (host_ready), so building the map needs no sync
+  uint32_t* dtot = nullptr;
+  bool host_ready = false;
+  int64_t pair_capacity = 0;  // pairs the in_idx / out_idx allocation holds
   void* block = nullptr;   // out_mask + tile_start
   void* block2 = nullptr;  // in_idx + out_idx
   cudaStream_t stream = 0;

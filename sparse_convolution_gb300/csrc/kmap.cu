@@ -17,6 +17,7 @@
 // every (offset, leaf) its position; pass B writes the pairs, ordered by output
 // inside each offset list, without atomics (deterministic).
 #include <cuda_runtime.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "block_scan.cuh"
@@ -344,6 +345,34 @@ size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
 using namespace fvx;
 
+size_t fvx::kmap_capacity_limit() {
+  static size_t limit = [] {
+    const char* e = getenv("FVX_KMAP_CAP_BYTES");
+    return e ? (size_t)strtoull(e, nullptr, 10) : ((size_t)8 << 30);
+  }();
+  return limit;
+}
+
+// Copies the map's 28 list offsets to the host (synchronising its stream) and
+// checks the device status word for a wait that gave up meanwhile.
+fvx_status fvx::kmap_read_totals(fvx_kmap_s* m, const char* who) {
+  if (m->host_ready) return FVX_OK;
+  uint32_t* h = (uint32_t*)pinned_staging(29 * 4);
+  uint32_t* dstat = device_status_word();
+  if (!h || !dstat) {
+    set_error("%s: staging buffer or device status word unavailable", who);
+    return FVX_ERR_ALLOC;
+  }
+  FVX_CUDA(cudaMemcpyAsync(h, m->dtot, 28 * 4, cudaMemcpyDeviceToHost, m->stream));
+  FVX_CUDA(cudaMemcpyAsync(h + 28, dstat, 4, cudaMemcpyDeviceToHost, m->stream));
+  FVX_CUDA(cudaStreamSynchronize(m->stream));
+  FVX_TRY(check_staged_status(who, h[28], m->stream));
+  for (int t = 0; t < 28; ++t) m->offsets_host[t] = h[t];
+  m->n_pairs = m->offsets_host[27];
+  m->host_ready = true;
+  return FVX_OK;
+}
+
 extern "C" fvx_status fvx_kernel_map(fvx_grid gin, fvx_grid gout, int32_t ksize, int32_t stride, fvx_stream stream,
                                      fvx_kmap* out) {
   if (!gin || !gout || !out) {
@@ -377,18 +406,31 @@ extern "C" fvx_status fvx_kernel_map(fvx_grid gin, fvx_grid gout, int32_t ksize,
   m->n_tiles = (Nout + kTileRows - 1) / kTileRows;
 
   uint32_t* counts = scr.get<uint32_t>((size_t)(27 * Lo + 1));
-  uint32_t* dtot = scr.get<uint32_t>(32);
-  if (!counts || !dtot) return FVX_ERR_ALLOC;
-  // mask + conv tiling live in the first block, pairs in the second
-  // (and, for stride 1, the input-leaf slot table the count pass writes,
-  // which the leaf-densified convolution reads too)
-  const size_t o_mask = 0, o_tile = align_up(4 * (size_t)Nout);
+  if (!counts) return FVX_ERR_ALLOC;
+  // mask, list totals and conv tiling live in the first block, pairs in the
+  // second (and, for stride 1, the input-leaf slot table the count pass
+  // writes, which the leaf-densified convolution reads too)
+  const size_t o_mask = 0, o_tot = align_up(4 * (size_t)Nout), o_tile = o_tot + align_up(4 * 32);
   const size_t o_nbr = o_tile + align_up(4 * (size_t)(27 * m->n_tiles + 1));
   const size_t bytes1 = o_nbr + (stride == 1 ? align_up(4 * (size_t)(27 * Lo + 1)) : 0);
   m->block = dalloc(bytes1, s);
   if (!m->block) return FVX_ERR_ALLOC;
   m->out_mask = (uint32_t*)((char*)m->block + o_mask);
+  m->dtot = (uint32_t*)((char*)m->block + o_tot);
   m->tile_start = (uint32_t*)((char*)m->block + o_tile);
+  uint32_t* const dtot = m->dtot;
+  // Pair lists sized for every output having all 27 neighbours, so the map
+  // is built without reading the pair count back; past kMapCapBytes (or the
+  // int32 pair index range) the count is read first and the lists are exact.
+  const int64_t cap = 27 * Nout;
+  const bool by_capacity = cap < (int64_t)INT32_MAX && (size_t)cap * 8 <= kmap_capacity_limit();
+  if (by_capacity) {
+    m->pair_capacity = cap;
+    m->block2 = dalloc(2 * align_up(4 * (size_t)cap), s);
+    if (!m->block2) return FVX_ERR_ALLOC;
+    m->in_idx = (int32_t*)m->block2;
+    m->out_idx = (int32_t*)((char*)m->block2 + align_up(4 * (size_t)cap));
+  }
 
   const GridDev gd = grid_dev(gin);
   int32_t* nbr = nullptr;  // stride 1: input-leaf slot table written by the count pass
@@ -412,28 +454,20 @@ extern "C" fvx_status fvx_kernel_map(fvx_grid gin, fvx_grid gout, int32_t ksize,
     k_list_offsets<<<1, 32, 0, s>>>(counts, Lo, dtot + 28, dtot);
   }
   FVX_TRY(check_launch("kmap_list_offsets"));
-  uint32_t* h = (uint32_t*)pinned_staging(29 * 4);
-  uint32_t* dstat = device_status_word();
-  if (!h || !dstat) {
-    set_error("fvx_kernel_map: staging buffer or device status word unavailable");
-    return FVX_ERR_ALLOC;
+  if (!by_capacity) {
+    FVX_TRY(kmap_read_totals(m, "fvx_kernel_map"));
+    const int64_t P = m->n_pairs;
+    if (P >= (int64_t)INT32_MAX) {
+      set_error("fvx_kernel_map: %lld pairs exceed the int32 pair index range", (long long)P);
+      return FVX_ERR_RANGE;
+    }
+    m->pair_capacity = P;
+    m->block2 = dalloc(2 * align_up(4 * (size_t)P), s);
+    if (!m->block2) return FVX_ERR_ALLOC;
+    m->in_idx = (int32_t*)m->block2;
+    m->out_idx = (int32_t*)((char*)m->block2 + align_up(4 * (size_t)P));
   }
-  FVX_CUDA(cudaMemcpyAsync(h, dtot, 28 * 4, cudaMemcpyDeviceToHost, s));
-  FVX_CUDA(cudaMemcpyAsync(h + 28, dstat, 4, cudaMemcpyDeviceToHost, s));
-  FVX_CUDA(cudaStreamSynchronize(s));
-  FVX_TRY(check_staged_status("fvx_kernel_map", h[28], s));
-  for (int t = 0; t < 28; ++t) m->offsets_host[t] = h[t];
-  const int64_t P = m->offsets_host[27];
-  if (P >= (int64_t)INT32_MAX) {
-    set_error("fvx_kernel_map: %lld pairs exceed the int32 pair index range", (long long)P);
-    return FVX_ERR_RANGE;
-  }
-  m->n_pairs = P;
-  m->block2 = dalloc(2 * align_up(4 * (size_t)P), s);
-  if (!m->block2) return FVX_ERR_ALLOC;
-  m->in_idx = (int32_t*)m->block2;
-  m->out_idx = (int32_t*)((char*)m->block2 + align_up(4 * (size_t)P));
-  if (Lo > 0 && P > 0) {
+  if (Lo > 0 && m->pair_capacity > 0) {
     LaunchScope ls("kmap_write", s);
     if (stride == 1)
       k_kmap1_write<<<(unsigned)Lo, kKmThreads, 0, s>>>(gd, gout->leaf_origin, gout->leaf_batch, gout->leaf_rec, Lo,

@@ -197,3 +197,38 @@ def test_conv_rejects_bad_shapes(cuda_device, grids):
     km2 = fvx.KernelMap(grids["g"], grids["gc"], 2)
     with pytest.raises(fvx.FvxError, match="other grids"):
         fvx.sparse_conv(gin, gout, km2, x2, W2)
+
+
+_EXACT_PATH_CHILD = r"""
+import numpy as np, oracle
+from tests import gpu_common as G
+from tests.test_gpu_kmap_conv import _random
+import sparse_convolution_gb300 as fvx
+c, offs = _random(5, 4000, -20, 40, 2)
+g, og = G.gpu_grid(c, offs), oracle.Grid.build(c, offs)
+for stride in (1, 2):
+    gout, ogout = (g, og) if stride == 1 else (g.coarsen(2), og.coarsen(2))
+    km, okm = fvx.KernelMap(g, gout, stride), oracle.KernelMap(og, ogout, stride)
+    G.assert_kmap_equal(km, okm)
+    x, W = G.bf16_inputs(7, g.n_active, 16, 32)
+    y = fvx.sparse_conv(g, gout, km, x, W)
+    yo, ao = oracle.conv(okm, G.as_f64(x), G.as_f64(W))
+    G.assert_conv_close(G.np_(y.float()), yo, ao, G.BF16_TOL)
+print("exact path ok")
+"""
+
+
+def test_kmap_exact_size_path(cuda_device):
+    """With the capacity limit at 0 the map reads its pair count back and sizes
+    its lists exactly (the path of maps past the limit): same map, same conv.
+    A child process, since the limit is read once per process."""
+    import os
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, FVX_KMAP_CAP_BYTES="0")
+    r = subprocess.run([sys.executable, "-c", _EXACT_PATH_CHILD], env=env, cwd=root, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "exact path ok" in r.stdout
