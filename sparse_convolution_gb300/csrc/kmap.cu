@@ -257,6 +257,13 @@ __global__ void __launch_bounds__(kKmThreads) k_kmap1_count(GridDev gin, const i
   }
 }
 
+// Input index of every position of the output leaf's one-voxel halo
+// (10^3 positions, -1 where no input voxel is active), from the 27 slots.
+struct Km1WriteSmem {
+  Km1Smem k;
+  int32_t hidx[1000];  // (hx+1)*100 + (hy+1)*10 + (hz+1), h in -1..8
+};
+
 __global__ void __launch_bounds__(kKmThreads) k_kmap1_write(GridDev gin, const int32_t* __restrict__ out_origin,
                                                             const int32_t* __restrict__ out_batch,
                                                             const uint64_t* __restrict__ out_rec, int64_t n_out_leaf,
@@ -264,41 +271,44 @@ __global__ void __launch_bounds__(kKmThreads) k_kmap1_write(GridDev gin, const i
                                                             const int32_t* __restrict__ nbr_in,
                                                             int32_t* __restrict__ in_idx,
                                                             int32_t* __restrict__ out_idx) {
-  __shared__ Km1Smem sm;
+  __shared__ Km1WriteSmem sw;
+  Km1Smem& sm = sw.k;
   const int lo = blockIdx.x, tid = threadIdx.x;
   km1_load(sm, gin, out_origin, out_batch, out_rec, lo, nbr_in, nullptr);
-  {
-    const int s = tid >> 3, x = tid & 7;
-    if (s < 27) sm.R[s][x] = km1_word(sm, s, x);
+  for (int h = tid; h < 1000; h += kKmThreads) {
+    const int hx = h / 100 - 1, hy = (h / 10) % 10 - 1, hz = h % 10 - 1;
+    const int slot = ((hx + 8) >> 3) * 9 + ((hy + 8) >> 3) * 3 + ((hz + 8) >> 3);
+    const int w = hx & 7, bit = ((hy & 7) << 3) | (hz & 7);
+    const unsigned long long m = sm.im[slot][w];
+    int32_t v = -1;
+    if ((m >> bit) & 1ull) {
+      const uint32_t pre = w ? (uint32_t)((sm.pre9[slot] >> (9 * (w - 1))) & 511ull) : 0u;
+      v = (int32_t)(sm.first[slot] + pre + (uint32_t)__popcll(m & ((1ull << bit) - 1ull)));
+    }
+    sw.hidx[h] = v;
   }
   __syncthreads();
-  // one warp per offset: per half word, a ballot packs the pairs into a
-  // contiguous run of the list (coalesced stores)
+  // one warp per offset: per half word of an output slice, a ballot packs the
+  // pairs into a contiguous run of the list (coalesced stores)
   const int warp = tid >> 5, lane = tid & 31;
   const uint32_t lt = lanemask_lt();
   for (int s = warp; s < 27; s += kKmThreads / 32) {
     const int di = s / 9 - 1, dj = (s / 3) % 3 - 1, dk = s % 3 - 1;
     uint32_t e = starts[(int64_t)s * n_out_leaf + lo];
     for (int x = 0; x < 8; ++x) {
-      const unsigned long long R = sm.R[s][x];
-      if (!R) continue;
       const unsigned long long om = sm.om[x];
+      if (!om) continue;
       const uint32_t qx = sm.qf + (x ? (uint32_t)((sm.opre9 >> (9 * (x - 1))) & 511ull) : 0u);
-      const int xs = x + di;
-      const int sa = ((xs + 8) >> 3) * 9, xw = (xs & 7) << 6;
+      const int hrow = (x + di + 1) * 100 + (dj + 1) * 10 + (dk + 1);
 #pragma unroll
       for (int hw = 0; hw < 2; ++hw) {
-        const int b = hw * 32 + lane;
-        const bool has = (R >> b) & 1ull;
+        const int b = hw * 32 + lane;  // y * 8 + z
+        const int32_t p = ((om >> b) & 1ull) ? sw.hidx[hrow + (b >> 3) * 10 + (b & 7)] : -1;
+        const bool has = p >= 0;
         const uint32_t bal = __ballot_sync(0xffffffffu, has);
         if (has) {
-          const int ys = (b >> 3) + dj, zs = (b & 7) + dk;
-          const int slot = sa + ((ys + 8) >> 3) * 3 + ((zs + 8) >> 3);
-          const int nn = xw | ((ys & 7) << 3) | (zs & 7);
-          const int w = nn >> 6, bit = nn & 63;
-          const uint32_t pre = w ? (uint32_t)((sm.pre9[slot] >> (9 * (w - 1))) & 511ull) : 0u;
           const uint32_t pos = e + __popc(bal & lt);
-          in_idx[pos] = (int32_t)(sm.first[slot] + pre + (uint32_t)__popcll(sm.im[slot][w] & ((1ull << bit) - 1ull)));
+          in_idx[pos] = p;
           out_idx[pos] = (int32_t)(qx + (uint32_t)__popcll(om & ((1ull << b) - 1ull)));
         }
         e += __popc(bal);
