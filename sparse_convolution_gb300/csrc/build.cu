@@ -234,30 +234,60 @@ struct Shifts {
   int leaf, lower, upper;  // key2 >> shift identifies leaf / lower / upper node
 };
 
-__device__ __forceinline__ uint32_t head_flags(const uint64_t* __restrict__ key, int64_t j, Shifts sh) {
-  if (j == 0) return 0xFu;
-  const uint64_t a = key[j], b = key[j - 1];
+// Flag passes over the sorted key2: each warp takes 256 consecutive keys in
+// 8 rounds of 32 (coalesced loads, all issued up front); the previous key of
+// lane 0 comes from the round before (or memory).  Head flags per item: bit 0
+// new voxel, bit 1 new leaf, bit 2 new lower node, bit 3 new upper node.
+constexpr int kFlagRounds = kFlagTile / kThreads;  // 8 rounds of 32 per warp
+static_assert(kFlagRounds * 32 * (kThreads / 32) == kFlagTile, "flag tile = warps x rounds x 32");
+
+__device__ __forceinline__ uint32_t flags_of(uint64_t a, uint64_t b, bool first, Shifts sh) {
+  if (first) return 0xFu;
   return (a != b ? 1u : 0u) | (((a >> sh.leaf) != (b >> sh.leaf)) ? 2u : 0u) |
          (((a >> sh.lower) != (b >> sh.lower)) ? 4u : 0u) | (((a >> sh.upper) != (b >> sh.upper)) ? 8u : 0u);
 }
 
-__device__ __forceinline__ uint64_t pack_flags(uint32_t f) {
-  return (uint64_t)(f & 1u) | ((uint64_t)((f >> 1) & 1u) << 16) | ((uint64_t)((f >> 2) & 1u) << 32) |
-         ((uint64_t)((f >> 3) & 1u) << 48);
+// Loads a warp's 256 keys (rounds r: item wbase + 32 r + lane) and their head
+// flags; items past n get flags 0.
+__device__ __forceinline__ void warp_flags(const uint64_t* __restrict__ key, int64_t n, int64_t wbase, Shifts sh,
+                                           int lane, uint64_t (&k)[kFlagRounds], uint32_t (&fl)[kFlagRounds]) {
+#pragma unroll
+  for (int r = 0; r < kFlagRounds; ++r) {
+    const int64_t j = wbase + 32 * r + lane;
+    k[r] = (j < n) ? key[j] : 0ull;
+  }
+  uint64_t before = (lane == 0 && wbase > 0 && wbase - 1 < n) ? key[wbase - 1] : 0ull;
+#pragma unroll
+  for (int r = 0; r < kFlagRounds; ++r) {
+    const int64_t j = wbase + 32 * r + lane;
+    uint64_t prev = __shfl_up_sync(0xffffffffu, k[r], 1);
+    const uint64_t last_prev_round = __shfl_sync(0xffffffffu, r ? k[r - 1] : before, 31);
+    if (lane == 0) prev = r ? last_prev_round : before;
+    fl[r] = (j < n) ? flags_of(k[r], prev, j == 0, sh) : 0u;
+  }
 }
 
 __global__ void __launch_bounds__(kThreads) k_count_tiles(const uint64_t* __restrict__ key, int64_t n, Shifts sh,
                                                           uint32_t* __restrict__ partial, int64_t ntiles) {
-  __shared__ uint64_t tmp[33];
-  const int64_t base = (int64_t)blockIdx.x * kFlagTile + (int64_t)threadIdx.x * kFlagItems;
-  uint64_t c = 0;
-  for (int q = 0; q < kFlagItems; ++q) {
-    const int64_t j = base + q;
-    if (j < n) c += pack_flags(head_flags(key, j, sh));
+  __shared__ uint32_t wt[kThreads / 32][4];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t wbase = (int64_t)blockIdx.x * kFlagTile + (int64_t)warp * (32 * kFlagRounds);
+  uint64_t k[kFlagRounds];
+  uint32_t fl[kFlagRounds];
+  warp_flags(key, n, wbase, sh, lane, k, fl);
+  uint32_t tot[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int r = 0; r < kFlagRounds; ++r)
+#pragma unroll
+    for (int f = 0; f < 4; ++f) tot[f] += __popc(__ballot_sync(0xffffffffu, (fl[r] >> f) & 1u));
+  if (lane < 4) wt[warp][lane] = tot[0] * (lane == 0) + tot[1] * (lane == 1) + tot[2] * (lane == 2) + tot[3] * (lane == 3);
+  __syncthreads();
+  if (threadIdx.x < 4) {
+    uint32_t c = 0;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) c += wt[w][threadIdx.x];
+    partial[threadIdx.x * ntiles + blockIdx.x] = c;
   }
-  uint64_t tot;
-  block_exclusive_scan<uint64_t>(c, tmp, &tot);
-  if (threadIdx.x < 4) partial[threadIdx.x * ntiles + blockIdx.x] = (uint32_t)((tot >> (16 * threadIdx.x)) & 0xFFFFu);
 }
 
 __global__ void k_gather_counts(const uint32_t* __restrict__ scanned, int64_t ntiles, const uint32_t* total,
@@ -293,37 +323,58 @@ struct BuildOut {
   uint64_t* upper_mask;
 };
 
-__global__ void __launch_bounds__(kThreads) k_count_down(const uint64_t* __restrict__ key,
+__global__ void __launch_bounds__(kThreads, 3) k_count_down(const uint64_t* __restrict__ key,
                                                          const uint32_t* __restrict__ val, int64_t n, Shifts sh,
                                                          const uint32_t* __restrict__ scanned, int64_t ntiles,
                                                          const __grid_constant__ BitRuns runs, DecodeInfo dec,
                                                          const int4* __restrict__ run_tile, BuildOut o) {
-  __shared__ uint64_t tmp[33];
-  const int64_t base = (int64_t)blockIdx.x * kFlagTile + (int64_t)threadIdx.x * kFlagItems;
-  uint32_t fl[kFlagItems];
-  uint64_t c = 0;
+  __shared__ uint32_t wt[kThreads / 32][4];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t wbase = (int64_t)blockIdx.x * kFlagTile + (int64_t)warp * (32 * kFlagRounds);
+  uint64_t k[kFlagRounds];
+  uint32_t fl[kFlagRounds];
+  uint32_t v[kFlagRounds];
 #pragma unroll
-  for (int q = 0; q < kFlagItems; ++q) {
-    const int64_t j = base + q;
-    fl[q] = (j < n) ? head_flags(key, j, sh) : 0u;
-    c += pack_flags(fl[q]);
+  for (int r = 0; r < kFlagRounds; ++r) {
+    const int64_t j = wbase + 32 * r + lane;
+    v[r] = (j < n) ? val[j] : 0u;
   }
-  const uint64_t ex = block_exclusive_scan<uint64_t>(c, tmp, (uint64_t*)nullptr);
+  warp_flags(key, n, wbase, sh, lane, k, fl);
+  // warp totals of each flag to shared memory
+  uint32_t tot[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int r = 0; r < kFlagRounds; ++r)
+#pragma unroll
+    for (int f = 0; f < 4; ++f) tot[f] += __popc(__ballot_sync(0xffffffffu, (fl[r] >> f) & 1u));
+  if (lane < 4) wt[warp][lane] = tot[0] * (lane == 0) + tot[1] * (lane == 1) + tot[2] * (lane == 2) + tot[3] * (lane == 3);
+  __syncthreads();
+  // running (exclusive) count of each flag before this warp's first item
   uint32_t cnt[4];
 #pragma unroll
-  for (int f = 0; f < 4; ++f)
-    cnt[f] = (uint32_t)((ex >> (16 * f)) & 0xFFFFu) + scanned[f * ntiles + blockIdx.x] - scanned[f * ntiles];
+  for (int f = 0; f < 4; ++f) {
+    uint32_t c = scanned[f * ntiles + blockIdx.x] - scanned[f * ntiles];
+    for (int w = 0; w < warp; ++w) c += wt[w][f];
+    cnt[f] = c;
+  }
+  const uint32_t lt = lanemask_lt();
 #pragma unroll
-  for (int q = 0; q < kFlagItems; ++q) {
-    const int64_t j = base + q;
-    if (j >= n) break;
-    const uint32_t f = fl[q];
+  for (int r = 0; r < kFlagRounds; ++r) {
+    const int64_t j = wbase + 32 * r + lane;
+    const uint32_t f = fl[r];
+    uint32_t bal[4];
 #pragma unroll
-    for (int a = 0; a < 4; ++a) cnt[a] += (f >> a) & 1u;
-    const uint32_t vox = cnt[0] - 1, leaf = cnt[1] - 1, lower = cnt[2] - 1, upper = cnt[3] - 1;
-    o.row_to_index[val[j]] = (int32_t)vox;
+    for (int q = 0; q < 4; ++q) bal[q] = __ballot_sync(0xffffffffu, (f >> q) & 1u);
+    // inclusive count of each flag up to this item, minus one = its node index
+    const uint32_t vox = cnt[0] + __popc(bal[0] & lt) + (f & 1u) - 1u;
+    const uint32_t leaf = cnt[1] + __popc(bal[1] & lt) + ((f >> 1) & 1u) - 1u;
+    const uint32_t lower = cnt[2] + __popc(bal[2] & lt) + ((f >> 2) & 1u) - 1u;
+    const uint32_t upper = cnt[3] + __popc(bal[3] & lt) + ((f >> 3) & 1u) - 1u;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) cnt[q] += __popc(bal[q]);
+    if (j >= n) continue;
+    o.row_to_index[v[r]] = (int32_t)vox;
     if (!(f & 1u)) continue;
-    const uint64_t k2 = key[j];
+    const uint64_t k2 = k[r];
     const uint64_t off = expand_bits(k2 & ((1ull << dec.vbits) - 1ull), runs) | dec.const_bits;
     const int4 t = run_tile[(uint32_t)(k2 >> dec.vbits)];
     const int ci = t.y * 4096 + (int)(((off >> 31) & 31) << 7 | ((off >> 17) & 15) << 3 | ((off >> 6) & 7));
@@ -338,8 +389,7 @@ __global__ void __launch_bounds__(kThreads) k_count_down(const uint64_t* __restr
       o.leaf_origin[3 * (int64_t)leaf + 1] = cj & ~7;
       o.leaf_origin[3 * (int64_t)leaf + 2] = ck & ~7;
       o.leaf_batch[leaf] = t.x;
-    }
-    if (f & 2u) {  // the new leaf is a child of its lower node (masks zeroed before)
+      // the new leaf is a child of its lower node (masks zeroed before)
       const int nb = (((ci >> 3) & 15) << 8) | (((cj >> 3) & 15) << 4) | ((ck >> 3) & 15);
       atomicOr(reinterpret_cast<unsigned long long*>(o.lower_mask) + (int64_t)lower * 64 + (nb >> 6), 1ull << (nb & 63));
     }
