@@ -179,18 +179,61 @@ __global__ void __launch_bounds__(kThreads) k_key2_direct(const int32_t* __restr
 // ---------------------------------------------------------------- step 4 RLE + step 5 key
 constexpr int kFlagItems = 8;
 constexpr int kFlagTile = kThreads * kFlagItems;  // 2048
+// Flag passes over sorted keys: each warp takes 256 consecutive keys in 8
+// rounds of 32 (coalesced loads, all issued up front); the previous key of
+// lane 0 comes from the round before (or memory).
+constexpr int kFlagRounds = kFlagTile / kThreads;  // 8 rounds of 32 per warp
+static_assert(kFlagRounds * 32 * (kThreads / 32) == kFlagTile, "flag tile = warps x rounds x 32");
+
+// A warp's keys k[r] (item wbase + 32 r + lane; 0 past n) and the key before
+// each item (prev; unused for item 0).
+__device__ __forceinline__ void warp_keys(const uint64_t* __restrict__ key, int64_t n, int64_t wbase, int lane,
+                                          uint64_t (&k)[kFlagRounds], uint64_t (&prev)[kFlagRounds]) {
+#pragma unroll
+  for (int r = 0; r < kFlagRounds; ++r) {
+    const int64_t j = wbase + 32 * r + lane;
+    k[r] = (j < n) ? key[j] : 0ull;
+  }
+  const uint64_t before = (lane == 0 && wbase > 0 && wbase - 1 < n) ? key[wbase - 1] : 0ull;
+#pragma unroll
+  for (int r = 0; r < kFlagRounds; ++r) {
+    const uint64_t up = __shfl_up_sync(0xffffffffu, k[r], 1);
+    const uint64_t last = __shfl_sync(0xffffffffu, r ? k[r - 1] : before, 31);
+    prev[r] = (lane == 0) ? (r ? last : before) : up;
+  }
+}
+
+// Block-wide exclusive offset of this warp's count plus the warp counts of
+// the block (one value per warp, through shared memory).
+__device__ __forceinline__ uint32_t warp_offset(uint32_t warp_total, uint32_t* sh, int warp, int lane,
+                                                uint32_t* block_total) {
+  if (lane == 0) sh[warp] = warp_total;
+  __syncthreads();
+  uint32_t off = 0, tot = 0;
+  for (int w = 0; w < kThreads / 32; ++w) {
+    const uint32_t c = sh[w];
+    off += (w < warp) ? c : 0u;
+    tot += c;
+  }
+  if (block_total) *block_total = tot;
+  return off;
+}
 
 __global__ void __launch_bounds__(kThreads) k_rle_count(const uint64_t* __restrict__ key, int64_t n,
                                                         uint32_t* __restrict__ partial) {
-  __shared__ uint32_t tmp[33];
-  const int64_t base = (int64_t)blockIdx.x * kFlagTile + (int64_t)threadIdx.x * kFlagItems;
+  __shared__ uint32_t sh[kThreads / 32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t wbase = (int64_t)blockIdx.x * kFlagTile + (int64_t)warp * (32 * kFlagRounds);
+  uint64_t k[kFlagRounds], prev[kFlagRounds];
+  warp_keys(key, n, wbase, lane, k, prev);
   uint32_t c = 0;
-  for (int q = 0; q < kFlagItems; ++q) {
-    const int64_t j = base + q;
-    if (j < n) c += (j == 0 || key[j] != key[j - 1]) ? 1u : 0u;
+#pragma unroll
+  for (int r = 0; r < kFlagRounds; ++r) {
+    const int64_t j = wbase + 32 * r + lane;
+    c += __popc(__ballot_sync(0xffffffffu, j < n && (j == 0 || k[r] != prev[r])));
   }
   uint32_t tot;
-  block_exclusive_scan<uint32_t>(c, tmp, &tot);
+  warp_offset(c, sh, warp, lane, &tot);
   if (threadIdx.x == 0) partial[blockIdx.x] = tot;
 }
 
@@ -200,31 +243,45 @@ __global__ void __launch_bounds__(kThreads) k_rle_key2(const uint64_t* __restric
                                                        const uint32_t* __restrict__ partial, Key1Layout L,
                                                        int vbits, const __grid_constant__ BitRuns runs,
                                                        uint64_t* __restrict__ key2, int4* __restrict__ run_tile) {
-  __shared__ uint32_t tmp[33];
-  const int64_t base = (int64_t)blockIdx.x * kFlagTile + (int64_t)threadIdx.x * kFlagItems;
-  uint32_t c = 0;
-  for (int q = 0; q < kFlagItems; ++q) {
-    const int64_t j = base + q;
-    if (j < n) c += (j == 0 || key1[j] != key1[j - 1]) ? 1u : 0u;
+  __shared__ uint32_t sh[kThreads / 32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t wbase = (int64_t)blockIdx.x * kFlagTile + (int64_t)warp * (32 * kFlagRounds);
+  uint64_t k[kFlagRounds], prev[kFlagRounds];
+  uint32_t v[kFlagRounds];
+#pragma unroll
+  for (int r = 0; r < kFlagRounds; ++r) {
+    const int64_t j = wbase + 32 * r + lane;
+    v[r] = (j < n) ? val[j] : 0u;
   }
-  uint32_t run = block_exclusive_scan<uint32_t>(c, tmp, (uint32_t*)nullptr) + partial[blockIdx.x];
-  for (int q = 0; q < kFlagItems; ++q) {
-    const int64_t j = base + q;
-    if (j >= n) break;
-    const uint64_t k1 = key1[j];
-    const bool head = (j == 0 || k1 != key1[j - 1]);
-    run += head ? 1u : 0u;
-    const uint32_t r = val[j];
-    const uint64_t o = offset_key(coords[3 * (int64_t)r], coords[3 * (int64_t)r + 1], coords[3 * (int64_t)r + 2]);
-    key2[j] = ((uint64_t)(run - 1) << vbits) | compact_bits(o, runs);
+  warp_keys(key1, n, wbase, lane, k, prev);
+  uint32_t c = 0;
+#pragma unroll
+  for (int r = 0; r < kFlagRounds; ++r) {
+    const int64_t j = wbase + 32 * r + lane;
+    c += __popc(__ballot_sync(0xffffffffu, j < n && (j == 0 || k[r] != prev[r])));
+  }
+  uint32_t run = partial[blockIdx.x] + warp_offset(c, sh, warp, lane, nullptr);  // heads before this warp
+  const uint32_t lt = lanemask_lt();
+#pragma unroll
+  for (int r = 0; r < kFlagRounds; ++r) {
+    const int64_t j = wbase + 32 * r + lane;
+    const bool head = j < n && (j == 0 || k[r] != prev[r]);
+    const uint32_t bal = __ballot_sync(0xffffffffu, head);
+    const uint32_t mine = run + __popc(bal & lt) + (head ? 1u : 0u);  // inclusive: run id + 1
+    run += __popc(bal);
+    if (j >= n) continue;
+    const uint32_t rr = v[r];
+    const uint64_t o = offset_key(coords[3 * (int64_t)rr], coords[3 * (int64_t)rr + 1], coords[3 * (int64_t)rr + 2]);
+    key2[j] = ((uint64_t)(mine - 1) << vbits) | compact_bits(o, runs);
     if (head) {
+      const uint64_t k1 = k[r];
       const int w12 = L.w[1] + L.w[2];
       int4 t;
       t.x = (int)(k1 >> L.tile_bits);
       t.y = (int)((k1 >> w12) & ((1ull << L.w[0]) - 1ull)) + L.tmin[0];
       t.z = (int)((k1 >> L.w[2]) & ((1ull << L.w[1]) - 1ull)) + L.tmin[1];
       t.w = (int)(k1 & ((1ull << L.w[2]) - 1ull)) + L.tmin[2];
-      run_tile[run - 1] = t;
+      run_tile[mine - 1] = t;
     }
   }
 }
@@ -234,12 +291,8 @@ struct Shifts {
   int leaf, lower, upper;  // key2 >> shift identifies leaf / lower / upper node
 };
 
-// Flag passes over the sorted key2: each warp takes 256 consecutive keys in
-// 8 rounds of 32 (coalesced loads, all issued up front); the previous key of
-// lane 0 comes from the round before (or memory).  Head flags per item: bit 0
-// new voxel, bit 1 new leaf, bit 2 new lower node, bit 3 new upper node.
-constexpr int kFlagRounds = kFlagTile / kThreads;  // 8 rounds of 32 per warp
-static_assert(kFlagRounds * 32 * (kThreads / 32) == kFlagTile, "flag tile = warps x rounds x 32");
+// Head flags of the sorted key2 per item: bit 0 new voxel, bit 1 new leaf,
+// bit 2 new lower node, bit 3 new upper node.
 
 __device__ __forceinline__ uint32_t flags_of(uint64_t a, uint64_t b, bool first, Shifts sh) {
   if (first) return 0xFu;
@@ -247,23 +300,15 @@ __device__ __forceinline__ uint32_t flags_of(uint64_t a, uint64_t b, bool first,
          (((a >> sh.lower) != (b >> sh.lower)) ? 4u : 0u) | (((a >> sh.upper) != (b >> sh.upper)) ? 8u : 0u);
 }
 
-// Loads a warp's 256 keys (rounds r: item wbase + 32 r + lane) and their head
-// flags; items past n get flags 0.
+// A warp's 256 keys and their head flags; items past n get flags 0.
 __device__ __forceinline__ void warp_flags(const uint64_t* __restrict__ key, int64_t n, int64_t wbase, Shifts sh,
                                            int lane, uint64_t (&k)[kFlagRounds], uint32_t (&fl)[kFlagRounds]) {
+  uint64_t prev[kFlagRounds];
+  warp_keys(key, n, wbase, lane, k, prev);
 #pragma unroll
   for (int r = 0; r < kFlagRounds; ++r) {
     const int64_t j = wbase + 32 * r + lane;
-    k[r] = (j < n) ? key[j] : 0ull;
-  }
-  uint64_t before = (lane == 0 && wbase > 0 && wbase - 1 < n) ? key[wbase - 1] : 0ull;
-#pragma unroll
-  for (int r = 0; r < kFlagRounds; ++r) {
-    const int64_t j = wbase + 32 * r + lane;
-    uint64_t prev = __shfl_up_sync(0xffffffffu, k[r], 1);
-    const uint64_t last_prev_round = __shfl_sync(0xffffffffu, r ? k[r - 1] : before, 31);
-    if (lane == 0) prev = r ? last_prev_round : before;
-    fl[r] = (j < n) ? flags_of(k[r], prev, j == 0, sh) : 0u;
+    fl[r] = (j < n) ? flags_of(k[r], prev[r], j == 0, sh) : 0u;
   }
 }
 
