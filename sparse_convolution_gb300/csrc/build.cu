@@ -176,6 +176,55 @@ __global__ void __launch_bounds__(kThreads) k_key2_direct(const int32_t* __restr
   val[r] = (uint32_t)r;
 }
 
+// ---------------------------------------------------------------- steps 3-6 by bitmap
+// One batch in one root tile whose compacted offset key has at most
+// kBitmapMaxBits varying bits: a presence bitmap over the whole key space
+// (<= 32 MB, so it stays in L2) replaces the radix sort.  Set one bit per
+// row, scan the words' popcounts, and the set bits in word order are the
+// unique keys in canonical order; a row's index is the rank of its bit.
+constexpr int kBitmapMaxBits = 28;
+
+__global__ void __launch_bounds__(kThreads) k_bitmap_set(const int32_t* __restrict__ coords, int64_t n,
+                                                         const __grid_constant__ BitRuns runs, int4 tile0,
+                                                         unsigned long long* __restrict__ bm,
+                                                         int4* __restrict__ run_tile) {
+  const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (r == 0) run_tile[0] = tile0;
+  if (r >= n) return;
+  const uint64_t key = compact_bits(offset_key(coords[3 * r], coords[3 * r + 1], coords[3 * r + 2]), runs);
+  atomicOr(bm + (key >> 6), 1ull << (key & 63));
+}
+
+// One warp per bitmap word: the word's set bits, in order, to keys[rank].
+__global__ void __launch_bounds__(kThreads) k_bitmap_emit(const uint64_t* __restrict__ bm,
+                                                          const uint32_t* __restrict__ wpre, int64_t nwords,
+                                                          uint64_t* __restrict__ keys) {
+  const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (w >= nwords) return;
+  const uint64_t m = bm[w];
+  if (!m) return;
+  const uint32_t base = wpre[w];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int b = h * 32 + lane;
+    if ((m >> b) & 1ull) keys[base + (uint32_t)__popcll(m & ((1ull << b) - 1ull))] = ((uint64_t)w << 6) | (uint64_t)b;
+  }
+}
+
+// Index of every input row: the rank of its key's bit.
+__global__ void __launch_bounds__(kThreads) k_bitmap_rank(const int32_t* __restrict__ coords, int64_t n,
+                                                          const __grid_constant__ BitRuns runs,
+                                                          const uint64_t* __restrict__ bm,
+                                                          const uint32_t* __restrict__ wpre,
+                                                          int32_t* __restrict__ row_to_index) {
+  const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= n) return;
+  const uint64_t key = compact_bits(offset_key(coords[3 * r], coords[3 * r + 1], coords[3 * r + 2]), runs);
+  const uint64_t m = bm[key >> 6];
+  row_to_index[r] = (int32_t)(wpre[key >> 6] + (uint32_t)__popcll(m & ((1ull << (key & 63)) - 1ull)));
+}
+
 // ---------------------------------------------------------------- step 4 RLE + step 5 key
 constexpr int kFlagItems = 8;
 constexpr int kFlagTile = kThreads * kFlagItems;  // 2048
@@ -312,9 +361,12 @@ __device__ __forceinline__ void warp_flags(const uint64_t* __restrict__ key, int
   }
 }
 
-__global__ void __launch_bounds__(kThreads) k_count_tiles(const uint64_t* __restrict__ key, int64_t n, Shifts sh,
+// n_live (device, may be NULL): the key list is only that long (<= n).
+__global__ void __launch_bounds__(kThreads) k_count_tiles(const uint64_t* __restrict__ key, int64_t n,
+                                                          const uint32_t* __restrict__ n_live, Shifts sh,
                                                           uint32_t* __restrict__ partial, int64_t ntiles) {
   __shared__ uint32_t wt[kThreads / 32][4];
+  if (n_live) n = min(n, (int64_t)*n_live);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t wbase = (int64_t)blockIdx.x * kFlagTile + (int64_t)warp * (32 * kFlagRounds);
   uint64_t k[kFlagRounds];
@@ -368,12 +420,16 @@ struct BuildOut {
   uint64_t* upper_mask;
 };
 
+// val (row id of each key) may be NULL: row_to_index is then written
+// elsewhere (bitmap path, where the keys are already unique).
 __global__ void __launch_bounds__(kThreads, 3) k_count_down(const uint64_t* __restrict__ key,
-                                                         const uint32_t* __restrict__ val, int64_t n, Shifts sh,
+                                                         const uint32_t* __restrict__ val, int64_t n,
+                                                         const uint32_t* __restrict__ n_live, Shifts sh,
                                                          const uint32_t* __restrict__ scanned, int64_t ntiles,
                                                          const __grid_constant__ BitRuns runs, DecodeInfo dec,
                                                          const int4* __restrict__ run_tile, BuildOut o) {
   __shared__ uint32_t wt[kThreads / 32][4];
+  if (n_live) n = min(n, (int64_t)*n_live);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t wbase = (int64_t)blockIdx.x * kFlagTile + (int64_t)warp * (32 * kFlagRounds);
   uint64_t k[kFlagRounds];
@@ -382,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_count_down(const uint64_t* __re
 #pragma unroll
   for (int r = 0; r < kFlagRounds; ++r) {
     const int64_t j = wbase + 32 * r + lane;
-    v[r] = (j < n) ? val[j] : 0u;
+    v[r] = (j < n && val) ? val[j] : 0u;
   }
   warp_flags(key, n, wbase, sh, lane, k, fl);
   // warp totals of each flag to shared memory
@@ -417,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_count_down(const uint64_t* __re
 #pragma unroll
     for (int q = 0; q < 4; ++q) cnt[q] += __popc(bal[q]);
     if (j >= n) continue;
-    o.row_to_index[v[r]] = (int32_t)vox;
+    if (val) o.row_to_index[v[r]] = (int32_t)vox;
     if (!(f & 1u)) continue;
     const uint64_t k2 = k[r];
     const uint64_t off = expand_bits(k2 & ((1ull << dec.vbits) - 1ull), runs) | dec.const_bits;
@@ -592,6 +648,11 @@ fvx_status build_grid_device(const int32_t* coords, int64_t n, const int64_t* of
   int4* run_tile = nullptr;
   uint32_t* scanned = nullptr;
   int64_t ntiles = 0;
+  bool use_bitmap = false;
+  uint64_t* bm = nullptr;       // bitmap path: presence bitmap of the key space
+  uint32_t* bm_pre = nullptr;   // exclusive popcount prefix of its words (+ total)
+  uint32_t* n_live = nullptr;   // device: unique keys (the sorted list's length)
+  int64_t bm_words = 0;
 
   if (n > 0) {
     // ---- step 2 planning: tile range per axis and the varying offset bits
@@ -658,6 +719,7 @@ fvx_status build_grid_device(const int32_t* coords, int64_t n, const int64_t* of
       return FVX_ERR_RANGE;
     }
 
+    use_bitmap = (width1 == 0) && vbits <= kBitmapMaxBits;
     ka = scr.get<uint64_t>((size_t)n);
     va = scr.get<uint32_t>((size_t)n);
     uint64_t* kb = scr.get<uint64_t>((size_t)n);
@@ -665,7 +727,28 @@ fvx_status build_grid_device(const int32_t* coords, int64_t n, const int64_t* of
     run_tile = scr.get<int4>((size_t)max_runs);
     if (!ka || !va || !kb || !vb || !run_tile) return FVX_ERR_ALLOC;
 
-    if (width1 == 0) {
+    if (use_bitmap) {
+      // one batch, one root tile, a key space that fits L2: bitmap instead of sort
+      const int4 tile0 = make_int4(0, P.tmin[0], P.tmin[1], P.tmin[2]);
+      bm_words = ((int64_t)1 << vbits) > 64 ? ((int64_t)1 << vbits) / 64 : 1;
+      bm = scr.get<uint64_t>((size_t)bm_words);
+      bm_pre = scr.get<uint32_t>((size_t)bm_words + 1);
+      if (!bm || !bm_pre) return FVX_ERR_ALLOC;
+      n_live = bm_pre + bm_words;  // the scan's total: number of unique keys
+      FVX_CUDA(cudaMemsetAsync(bm, 0, 8 * (size_t)bm_words, s));
+      {
+        LaunchScope ls("build_bitmap_set", s);
+        k_bitmap_set<<<grid_for(n, kThreads), kThreads, 0, s>>>(coords, n, runs, tile0,
+                                                                (unsigned long long*)bm, run_tile);
+      }
+      FVX_TRY(check_launch("build_bitmap_set"));
+      FVX_TRY(scan_popc64(bm, bm_pre, bm_words, n_live, s, scr));
+      {
+        LaunchScope ls("build_bitmap_emit", s);
+        k_bitmap_emit<<<grid_for(bm_words * 32, kThreads), kThreads, 0, s>>>(bm, bm_pre, bm_words, ka);
+      }
+      FVX_TRY(check_launch("build_bitmap_emit"));
+    } else if (width1 == 0) {
       // one batch, one root tile: steps 2-4 are empty; run 0 is that tile
       const int4 tile0 = make_int4(0, P.tmin[0], P.tmin[1], P.tmin[2]);
       {
@@ -708,7 +791,7 @@ fvx_status build_grid_device(const int32_t* coords, int64_t n, const int64_t* of
       }
     }
     // ---- step 6: sort by key2 (run id above the compacted offsets)
-    {
+    if (!use_bitmap) {
       bool in1 = false;
       FVX_TRY(radix_sort_pairs(ka, va, kb, vb, n, 0, runbits + vbits, s, &in1, scr));
       if (in1) {
@@ -723,7 +806,7 @@ fvx_status build_grid_device(const int32_t* coords, int64_t n, const int64_t* of
     if (!scanned || !dcounts) return FVX_ERR_ALLOC;
     {
       LaunchScope ls("build_count_tiles", s);
-      k_count_tiles<<<(unsigned)ntiles, kThreads, 0, s>>>(ka, n, sh, scanned, ntiles);
+      k_count_tiles<<<(unsigned)ntiles, kThreads, 0, s>>>(ka, n, n_live, sh, scanned, ntiles);
     }
     FVX_TRY(check_launch("build_count_tiles"));
     FVX_TRY(scan_exclusive_u32(scanned, scanned, 4 * ntiles, dcounts + 4, s, scr));
@@ -797,9 +880,15 @@ fvx_status build_grid_device(const int32_t* coords, int64_t n, const int64_t* of
     FVX_CUDA(cudaMemsetAsync(g->upper_mask, 0, 4096 * (size_t)NU, s));
     {
       LaunchScope ls("build_count_down", s);
-      k_count_down<<<(unsigned)ntiles, kThreads, 0, s>>>(ka, va, n, sh, scanned, ntiles, runs, dec, run_tile, o);
+      k_count_down<<<(unsigned)ntiles, kThreads, 0, s>>>(ka, use_bitmap ? nullptr : va, n, n_live, sh, scanned,
+                                                         ntiles, runs, dec, run_tile, o);
     }
     FVX_TRY(check_launch("build_count_down"));
+    if (use_bitmap) {
+      LaunchScope ls("build_bitmap_rank", s);
+      k_bitmap_rank<<<grid_for(n, kThreads), kThreads, 0, s>>>(coords, n, runs, bm, bm_pre, g->row_to_index);
+    }
+    FVX_TRY(check_launch("build_bitmap_rank"));
     // ---- steps 11-12: leaf masks and prefix counts at every level
     {
       LaunchScope ls("build_leaf_register", s);

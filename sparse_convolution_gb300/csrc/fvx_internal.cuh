@@ -91,6 +91,11 @@ enum : uint32_t { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_CHECK = 2 };
 fvx_status scan_exclusive_u32(const uint32_t* in, uint32_t* out, int64_t n, uint32_t* total, cudaStream_t s,
                               Scratch& scr);
 
+// Exclusive scan of the popcounts of n uint64 words (bitmap rank offsets);
+// total as above.
+fvx_status scan_popc64(const uint64_t* words, uint32_t* out, int64_t n, uint32_t* total, cudaStream_t s,
+                       Scratch& scr);
+
 // Stable LSD radix sort of (key, value) pairs by key bits [bit_lo, bit_hi)
 // with 8-bit digits.  Ping-pongs between (k0,v0) and (k1,v1); returns in
 // *result_in_1 whether the sorted data ends in (k1,v1).

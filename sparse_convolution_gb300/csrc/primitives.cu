@@ -52,7 +52,19 @@ constexpr int kScanThreads = 256;
 constexpr int kScanItems = 8;
 constexpr int kScanTile = kScanThreads * kScanItems;  // 2048
 
-__global__ void __launch_bounds__(kScanThreads) k_scan_1p(const uint32_t* in, uint32_t* out, int64_t n,
+// Input of the scan: the uint32 values themselves, or the popcounts of uint64
+// words (bitmap ranks).
+struct ScanU32 {
+  const uint32_t* p;
+  __device__ __forceinline__ uint32_t operator()(int64_t i) const { return p[i]; }
+};
+struct ScanPopc64 {
+  const uint64_t* p;
+  __device__ __forceinline__ uint32_t operator()(int64_t i) const { return (uint32_t)__popcll(p[i]); }
+};
+
+template <class In>
+__global__ void __launch_bounds__(kScanThreads) k_scan_1p(In in, uint32_t* out, int64_t n,
                                                           uint32_t* __restrict__ total, uint64_t* flags,
                                                           uint32_t* ticket, int64_t nt, uint32_t* status) {
   __shared__ uint32_t tmp[33];
@@ -65,7 +77,7 @@ __global__ void __launch_bounds__(kScanThreads) k_scan_1p(const uint32_t* in, ui
   uint32_t sum = 0;
 #pragma unroll
   for (int k = 0; k < kScanItems; ++k) {
-    v[k] = (base + k < n) ? in[base + k] : 0u;
+    v[k] = (base + k < n) ? in(base + k) : 0u;
     sum += v[k];
   }
   uint32_t tot;
@@ -110,8 +122,8 @@ __global__ void __launch_bounds__(kScanThreads) k_scan_1p(const uint32_t* in, ui
   if (t == nt - 1 && threadIdx.x == 0 && total) *total = s_prefix + tot;
 }
 
-fvx_status scan_exclusive_u32(const uint32_t* in, uint32_t* out, int64_t n, uint32_t* total, cudaStream_t s,
-                              Scratch& scr) {
+template <class In>
+fvx_status scan_1p(In in, uint32_t* out, int64_t n, uint32_t* total, cudaStream_t s, Scratch& scr) {
   if (n <= 0) {
     if (total) FVX_CUDA(cudaMemsetAsync(total, 0, 4, s));
     return FVX_OK;
@@ -127,9 +139,20 @@ fvx_status scan_exclusive_u32(const uint32_t* in, uint32_t* out, int64_t n, uint
   FVX_CUDA(cudaMemsetAsync(flags, 0, 8 * ((size_t)nt + 1), s));
   {
     LaunchScope ls("scan_1p", s);
-    k_scan_1p<<<(unsigned)nt, kScanThreads, 0, s>>>(in, out, n, total, flags, (uint32_t*)(flags + nt), nt, status);
+    k_scan_1p<In><<<(unsigned)nt, kScanThreads, 0, s>>>(in, out, n, total, flags, (uint32_t*)(flags + nt), nt,
+                                                        status);
   }
   return check_launch("scan_1p");
+}
+
+fvx_status scan_exclusive_u32(const uint32_t* in, uint32_t* out, int64_t n, uint32_t* total, cudaStream_t s,
+                              Scratch& scr) {
+  return scan_1p(ScanU32{in}, out, n, total, s, scr);
+}
+
+fvx_status scan_popc64(const uint64_t* words, uint32_t* out, int64_t n, uint32_t* total, cudaStream_t s,
+                       Scratch& scr) {
+  return scan_1p(ScanPopc64{words}, out, n, total, s, scr);
 }
 
 // ============================================================== radix sort

@@ -31,6 +31,11 @@ CASES = {
     "ragged_2049": (4, 2049, 100, 40, 1),
     "dense_block": (5, 40000, 0, 32, 1),
     "many_batches": (6, 300, -10, 25, 40),
+    # one batch in one root tile: a key space of <= 2^28 takes the presence
+    # bitmap instead of the sort; the full 4096^3 tile (36 varying bits) sorts
+    "one_tile_bitmap": (7, 30000, 1024, 512, 1),
+    "one_tile_full_width": (8, 30000, 0, 4096, 1),
+    "one_tile_bitmap_27_bits": (9, 20000, 0, 512, 1),
 }
 
 
