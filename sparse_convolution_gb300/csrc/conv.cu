@@ -1027,8 +1027,8 @@ __global__ void __launch_bounds__(kLeafThreads) k_conv_leaf(const __grid_constan
   unsigned char* halo = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   unsigned char* wsm = halo + a.halo_bytes;
   LeafNbr* nbr = reinterpret_cast<LeafNbr*>(wsm + a.w_bytes);
-  unsigned long long* done = reinterpret_cast<unsigned long long*>(nbr + 27);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  unsigned long long* done = reinterpret_cast<unsigned long long*>(nbr + 27);  // one per M tile
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 4);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cin = a.cin, cout = a.cout, g8 = G8;
   const int64_t L = blockIdx.x;
@@ -1041,7 +1041,8 @@ __global__ void __launch_bounds__(kLeafThreads) k_conv_leaf(const __grid_constan
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   if (tid == 32) {
-    mbar_init(smem_u32(done), 1);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) mbar_init(smem_u32(done + t), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   // the 27 input leaves around the output leaf (slot = (ex+1)*9 + (ey+1)*3 + (ez+1))
@@ -1144,14 +1145,13 @@ __global__ void __launch_bounds__(kLeafThreads) k_conv_leaf(const __grid_constan
         const uint64_t bd = sdesc_plain(wbase + (uint32_t)(2 * p) * wblk, wblk, 128u);
         umma_bf16(d, ad, bd, idesc, p ? 1u : 0u);
       }
+      umma_commit(smem_u32(done + t));  // tile t's accumulator is complete
     }
-    umma_commit(smem_u32(done));
   }
   __syncwarp();
-  mbar_wait(smem_u32(done), 0u, a.status);
-  tc_fence_after();
 
-  // epilogue: warp w reads TMEM lanes 32*(w&3) .. +31 of tiles 2*(w>>2), +1
+  // epilogue: warp w reads TMEM lanes 32*(w&3) .. +31 of tiles (w>>2) and
+  // (w>>2) + 2, each as soon as its MMAs complete
   {
     const int quarter = warp & 3, m = quarter * 32 + lane;
     const int yl = m >> 6, xq = (m >> 3) & 7, z = m & 7;
@@ -1161,7 +1161,9 @@ __global__ void __launch_bounds__(kLeafThreads) k_conv_leaf(const __grid_constan
     const uint64_t pre9 = __ldg(reinterpret_cast<const unsigned long long*>(rec) + 9);
     const uint32_t pre = xq ? (uint32_t)((pre9 >> (9 * (xq - 1))) & 511ull) : 0u;
     for (int tt = 0; tt < 2; ++tt) {
-      const int t = 2 * (warp >> 2) + tt;
+      const int t = (warp >> 2) + 2 * tt;
+      mbar_wait(smem_u32(done + t), 0u, a.status);
+      tc_fence_after();
       const int bit = (2 * t + yl) * 8 + z;
       const bool act = (mw >> bit) & 1ull;
       const int64_t q = (int64_t)first + pre + __popcll(mw & ((1ull << bit) - 1ull));
@@ -1278,7 +1280,7 @@ fvx_status launch_conv_leaf(const char* who, fvx_grid gin, fvx_kmap m, fvx_dtype
   a.tmem_cols = cols;
   a.halo_bytes = (3 * (int)(cin / 8) * kLeafPlaneBytes + 1023) & ~1023;
   a.w_bytes = ((27 * (int)(cin / 8) + 1) * (int)cout * 16 + 1023) & ~1023;
-  size_t smem = 1024 + (size_t)a.halo_bytes + a.w_bytes + 27 * sizeof(LeafNbr) + 16;
+  size_t smem = 1024 + (size_t)a.halo_bytes + a.w_bytes + 27 * sizeof(LeafNbr) + 40;
   int dev = 0, sm_bytes = 0, reserved = 0;
   FVX_CUDA(cudaGetDevice(&dev));
   FVX_CUDA(cudaDeviceGetAttribute(&sm_bytes, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev));
