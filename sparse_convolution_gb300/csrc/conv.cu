@@ -985,7 +985,7 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tma(const __grid_
 // K runs over groups kg = c8 * 27 + s (s = the stencil slot); their start
 // addresses increase with kg, so each MMA (two K groups) takes the distance
 // between its two groups as its leading byte offset.
-constexpr int kLeafThreads = 256;
+constexpr int kLeafThreads = 288;  // 4 loader warps, 1 MMA warp, 4 epilogue warps
 constexpr int kLeafPlaneRows = 800;                     // 10 x 8 x 10
 constexpr int kLeafPlaneBytes = kLeafPlaneRows * 16;    // 12800
 constexpr int kLeafMaxCin = 16;
@@ -1010,6 +1010,7 @@ struct LeafConvArgs {
   uint32_t* status;
   int64_t n_leaf_out;
   int cin, cout, out_bf16, tmem_cols;
+  int tile_cols;                // TMEM columns per M-tile accumulator (multiple of 32)
   int halo_bytes, w_bytes;      // shared-memory regions (multiples of 1024)
 };
 
@@ -1021,51 +1022,76 @@ __device__ __forceinline__ uint32_t leaf_index_in(const LeafNbr& L, int n, bool&
   return L.first + pre + (uint32_t)__popcll(m & ((1ull << bit) - 1ull));
 }
 
-template <int G8>  // cin / 8
-__global__ void __launch_bounds__(kLeafThreads) k_conv_leaf(const __grid_constant__ LeafConvArgs a) {
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
-  unsigned char* halo = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  unsigned char* wsm = halo + a.halo_bytes;
-  LeafNbr* nbr = reinterpret_cast<LeafNbr*>(wsm + a.w_bytes);
-  unsigned long long* done = reinterpret_cast<unsigned long long*>(nbr + 27);  // one per M tile
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 4);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int cin = a.cin, cout = a.cout, g8 = G8;
-  const int64_t L = blockIdx.x;
-  if (L >= a.n_leaf_out) return;
+// Persistent version: block g handles output leaves g, g + G, g + 2G, ...
+// Warps 0-3 stage halos into two buffers (while filling leaf i's they fetch
+// the neighbour records of leaf i+1 and the neighbour ids of leaf i+2), warp 4
+// issues the MMAs into two TMEM accumulator sets, warps 5-8 write the outputs
+// tile by tile.  All waits are bounded mbarrier waits.
+constexpr int kLeafLoaderThreads = 128;
+constexpr int kLeafMmaWarp = 4;
 
-  if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+struct LeafBars {
+  unsigned long long halo_full[2], halo_empty[2], acc_full[2][4], acc_empty[2];
+  uint32_t tmem_base;
+};
+
+__device__ __forceinline__ void loader_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ void load_leaf_nbr(const uint64_t* __restrict__ in_rec, int32_t l, uint64_t (&m)[8],
+                                              uint64_t& first, uint64_t& pre9) {
+  if (l >= 0) {
+    const unsigned long long* r = reinterpret_cast<const unsigned long long*>(in_rec) + (size_t)l * 10;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) m[w] = __ldg(r + w);
+    first = __ldg(r + 8);
+    pre9 = __ldg(r + 9);
+  } else {
+#pragma unroll
+    for (int w = 0; w < 8; ++w) m[w] = 0ull;
+    first = 0ull;
+    pre9 = 0ull;
+  }
+}
+__device__ __forceinline__ void store_leaf_nbr(LeafNbr& nb, const uint64_t (&m)[8], uint64_t first, uint64_t pre9) {
+#pragma unroll
+  for (int w = 0; w < 8; ++w) nb.mask[w] = m[w];
+  nb.first = (uint32_t)first;
+  nb.pre9 = pre9;
+}
+
+template <int G8>  // cin / 8
+__global__ void __launch_bounds__(kLeafThreads, G8 == 1 ? 2 : 1) k_conv_leaf(const __grid_constant__ LeafConvArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // [halo 0][halo 1][weights][neighbour records, 2 x 27][barriers]
+  unsigned char* halo0 = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  unsigned char* wsm = halo0 + 2 * (size_t)a.halo_bytes;
+  LeafNbr* info = reinterpret_cast<LeafNbr*>(wsm + a.w_bytes);
+  LeafBars& bars = *reinterpret_cast<LeafBars*>(info + 54);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int cin = a.cin, cout = a.cout;
+  const int64_t G = gridDim.x, nL = a.n_leaf_out;
+  const uint32_t tcs = (uint32_t)a.tile_cols;
+  uint32_t* const status = a.status;
+
+  if (warp == kLeafMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&bars.tmem_base)),
                  "r"(a.tmem_cols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  if (tid == 32) {
-#pragma unroll
-    for (int t = 0; t < 4; ++t) mbar_init(smem_u32(done + t), 1);
+  if (tid == 0) {
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&bars.halo_full[b]), 1);
+      mbar_init(smem_u32(&bars.halo_empty[b]), 1);
+      mbar_init(smem_u32(&bars.acc_empty[b]), 4);  // one arrival per epilogue warp
+      for (int t = 0; t < 4; ++t) mbar_init(smem_u32(&bars.acc_full[b][t]), 1);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  // the 27 input leaves around the output leaf (slot = (ex+1)*9 + (ey+1)*3 + (ez+1))
-  if (tid < 27) {
-    const int l = __ldg(a.nbr + L * 27 + tid);
-    LeafNbr& nb = nbr[tid];
-    if (l >= 0) {
-      const uint64_t* rec = a.in_rec + (size_t)l * 10;
-#pragma unroll
-      for (int w = 0; w < 8; ++w) nb.mask[w] = __ldg(reinterpret_cast<const unsigned long long*>(rec) + w);
-      nb.first = (uint32_t)__ldg(reinterpret_cast<const unsigned long long*>(rec) + 8);
-      nb.pre9 = __ldg(reinterpret_cast<const unsigned long long*>(rec) + 9);
-    } else {
-#pragma unroll
-      for (int w = 0; w < 8; ++w) nb.mask[w] = 0ull;
-      nb.first = 0u;
-      nb.pre9 = 0ull;
-    }
-  }
-  // weights: block kg = c8 * 27 + s holds rows co of wt[s][co][8*c8 .. 8*c8+7];
-  // one zero block after the last
+  // weights, once: block kg = c8 * 27 + s holds rows co of wt[s][co][8*c8 ..
+  // 8*c8+7]; one zero block after the last
   {
-    const int nkg = 27 * g8;
+    const int nkg = 27 * G8;
     const int nrow = (nkg + 1) * cout;
     for (int e = tid; e < nrow; e += kLeafThreads) {
       const int kg = e / cout, co = e - kg * cout;
@@ -1077,125 +1103,171 @@ __global__ void __launch_bounds__(kLeafThreads) k_conv_leaf(const __grid_constan
       *reinterpret_cast<uint4*>(wsm + (size_t)e * 16) = v;
     }
   }
-  __syncthreads();
-  // halo: position (hx, hy, hz) in -1..8 relative to the origin, one 16-byte
-  // piece (8 channels) per item, written to every x-shifted plane holding it;
-  // a thread issues all its loads before its first store
-  {
-    constexpr int kNItem = 1000 * G8;
-    constexpr int kPer = (kNItem + kLeafThreads - 1) / kLeafThreads;
-    uint4 v[kPer];
-#pragma unroll
-    for (int q = 0; q < kPer; ++q) {
-      const int e = tid + q * kLeafThreads;
-      v[q] = make_uint4(0u, 0u, 0u, 0u);
-      if (e < kNItem) {
-        const int pos = e / G8, c8 = e - pos * G8;
-        const int hx = pos / 100 - 1, hy = (pos / 10) % 10 - 1, hz = pos % 10 - 1;
-        const int ex = (hx < 0) ? -1 : (hx > 7 ? 1 : 0), ey = (hy < 0) ? -1 : (hy > 7 ? 1 : 0),
-                  ez = (hz < 0) ? -1 : (hz > 7 ? 1 : 0);
-        bool act;
-        const uint32_t idx = leaf_index_in(nbr[(ex + 1) * 9 + (ey + 1) * 3 + (ez + 1)],
-                                           ((hx & 7) << 6) | ((hy & 7) << 3) | (hz & 7), act);
-        if (act) v[q] = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)idx * cin + 8 * c8));
-      }
-    }
-#pragma unroll
-    for (int q = 0; q < kPer; ++q) {
-      const int e = tid + q * kLeafThreads;
-      if (e < kNItem) {
-        const int pos = e / G8, c8 = e - pos * G8;
-        const int hx = pos / 100 - 1, hy = (pos / 10) % 10 - 1, hz = pos % 10 - 1;
-        const int rbase = (hy + 1) * 80 + (hz + 1);  // row without the x term
-#pragma unroll
-        for (int cx = 0; cx < 3; ++cx) {
-          const int xx = hx - cx + 1;  // x of the plane row holding this position
-          if (xx >= 0 && xx < 8)
-            *reinterpret_cast<uint4*>(halo + (size_t)(c8 * 3 + cx) * kLeafPlaneBytes + (size_t)(rbase + xx * 10) * 16) =
-                v[q];
-        }
-      }
-    }
+  // neighbour records of the first leaf (slot = (ex+1)*9 + (ey+1)*3 + ez+1)
+  if (tid < 27 && (int64_t)blockIdx.x < nL) {
+    uint64_t m[8], f, p9;
+    load_leaf_nbr(a.in_rec, __ldg(a.nbr + (int64_t)blockIdx.x * 27 + tid), m, f, p9);
+    store_leaf_nbr(info[tid], m, f, p9);
   }
-  fence_proxy_async();  // the tensor core reads what the generic proxy wrote
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  const uint32_t tmem = bars.tmem_base;
 
-  if (tid == 0) {
-    const uint32_t idesc = idesc_bf16(kRows, cout);
-    const uint32_t hbase = smem_u32(halo), wbase = smem_u32(wsm);
-    const int nkg = 27 * g8, npair = (nkg + 1) >> 1;
-    const uint32_t wblk = (uint32_t)cout * 16u;
-    for (int t = 0; t < 4; ++t) {
-      const uint32_t d = tmem + (uint32_t)(t * cout);
-      for (int p = 0; p < npair; ++p) {
-        uint32_t addr[2];
+  if (warp < 4) {
+    // ---------------- halo staging (128 threads)
+    constexpr int kNItem = 1000 * G8;
+    constexpr int kPer = (kNItem + kLeafLoaderThreads - 1) / kLeafLoaderThreads;
+    int32_t id_next = -1;
+    if (tid < 27 && (int64_t)blockIdx.x + G < nL) id_next = __ldg(a.nbr + ((int64_t)blockIdx.x + G) * 27 + tid);
+    int i = 0;
+    for (int64_t L = blockIdx.x; L < nL; L += G, ++i) {
+      const int b = i & 1;
+      const bool have_next = L + G < nL;
+      // records of the next leaf (its ids came one iteration earlier)
+      uint64_t rm[8], rf = 0ull, rp = 0ull;
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          int kg = 2 * p + h2;
-          if (kg >= nkg) kg = nkg - 1;  // the zero weight block pairs with a repeat
-          const int c8 = kg / 27, s = kg - c8 * 27;
-          const int cx = s / 9, dy = (s / 3) % 3 - 1, dz = s % 3 - 1;
-          addr[h2] = hbase + (uint32_t)(c8 * 3 + cx) * kLeafPlaneBytes +
-                     (uint32_t)(((2 * t + dy + 1) * 80 + dz + 1) * 16);
+      for (int w = 0; w < 8; ++w) rm[w] = 0ull;
+      if (tid < 27 && have_next) load_leaf_nbr(a.in_rec, id_next, rm, rf, rp);
+      // halo loads of this leaf
+      const LeafNbr* nb = info + 27 * b;
+      uint4 v[kPer];
+#pragma unroll
+      for (int q = 0; q < kPer; ++q) {
+        const int e = tid + q * kLeafLoaderThreads;
+        v[q] = make_uint4(0u, 0u, 0u, 0u);
+        if (e < kNItem) {
+          const int pos = e / G8, c8 = e - pos * G8;
+          const int hx = pos / 100 - 1, hy = (pos / 10) % 10 - 1, hz = pos % 10 - 1;
+          const int ex = (hx < 0) ? -1 : (hx > 7 ? 1 : 0), ey = (hy < 0) ? -1 : (hy > 7 ? 1 : 0),
+                    ez = (hz < 0) ? -1 : (hz > 7 ? 1 : 0);
+          bool act;
+          const uint32_t idx = leaf_index_in(nb[(ex + 1) * 9 + (ey + 1) * 3 + (ez + 1)],
+                                             ((hx & 7) << 6) | ((hy & 7) << 3) | (hz & 7), act);
+          if (act) v[q] = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)idx * cin + 8 * c8));
         }
-        const uint64_t ad = sdesc_plain(addr[0], addr[1] - addr[0], 160u);
-        const uint64_t bd = sdesc_plain(wbase + (uint32_t)(2 * p) * wblk, wblk, 128u);
-        umma_bf16(d, ad, bd, idesc, p ? 1u : 0u);
       }
-      umma_commit(smem_u32(done + t));  // tile t's accumulator is complete
+      // ids of the leaf after next
+      int32_t id_next2 = -1;
+      if (tid < 27 && L + 2 * G < nL) id_next2 = __ldg(a.nbr + (L + 2 * G) * 27 + tid);
+      // the buffer is free once the MMAs of leaf i-2 have completed
+      if (i >= 2) mbar_wait(smem_u32(&bars.halo_empty[b]), (uint32_t)(((i >> 1) - 1) & 1), status);
+      unsigned char* halo = halo0 + (size_t)b * a.halo_bytes;
+#pragma unroll
+      for (int q = 0; q < kPer; ++q) {
+        const int e = tid + q * kLeafLoaderThreads;
+        if (e < kNItem) {
+          const int pos = e / G8, c8 = e - pos * G8;
+          const int hx = pos / 100 - 1, hy = (pos / 10) % 10 - 1, hz = pos % 10 - 1;
+          const int rbase = (hy + 1) * 80 + (hz + 1);  // row without the x term
+#pragma unroll
+          for (int cx = 0; cx < 3; ++cx) {
+            const int xx = hx - cx + 1;  // x of the plane row holding this position
+            if (xx >= 0 && xx < 8)
+              *reinterpret_cast<uint4*>(halo + (size_t)(c8 * 3 + cx) * kLeafPlaneBytes + (size_t)(rbase + xx * 10) * 16) =
+                  v[q];
+          }
+        }
+      }
+      if (tid < 27 && have_next) store_leaf_nbr(info[27 * (b ^ 1) + tid], rm, rf, rp);
+      id_next = id_next2;
+      fence_proxy_async();  // the tensor core reads what the generic proxy wrote
+      loader_bar();
+      if (tid == 0) mbar_arrive(smem_u32(&bars.halo_full[b]));
     }
-  }
-  __syncwarp();
-
-  // epilogue: warp w reads TMEM lanes 32*(w&3) .. +31 of tiles (w>>2) and
-  // (w>>2) + 2, each as soon as its MMAs complete
-  {
+  } else if (warp == kLeafMmaWarp) {
+    // ---------------- MMA issue (one thread)
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(kRows, cout);
+      const uint32_t wbase = smem_u32(wsm);
+      const int nkg = 27 * G8, npair = (nkg + 1) >> 1;
+      const uint32_t wblk = (uint32_t)cout * 16u;
+      int i = 0;
+      for (int64_t L = blockIdx.x; L < nL; L += G, ++i) {
+        const int b = i & 1;
+        mbar_wait(smem_u32(&bars.halo_full[b]), (uint32_t)((i >> 1) & 1), status);
+        if (i >= 2) mbar_wait(smem_u32(&bars.acc_empty[b]), (uint32_t)(((i >> 1) - 1) & 1), status);
+        tc_fence_after();
+        const uint32_t hbase = smem_u32(halo0) + (uint32_t)b * (uint32_t)a.halo_bytes;
+        for (int t = 0; t < 4; ++t) {
+          const uint32_t d = tmem + (uint32_t)(b * 4 + t) * tcs;
+          for (int p = 0; p < npair; ++p) {
+            uint32_t addr[2];
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              int kg = 2 * p + h2;
+              if (kg >= nkg) kg = nkg - 1;  // the zero weight block pairs with a repeat
+              const int c8 = kg / 27, s = kg - c8 * 27;
+              const int cx = s / 9, dy = (s / 3) % 3 - 1, dz = s % 3 - 1;
+              addr[h2] = hbase + (uint32_t)(c8 * 3 + cx) * kLeafPlaneBytes +
+                         (uint32_t)(((2 * t + dy + 1) * 80 + dz + 1) * 16);
+            }
+            const uint64_t ad = sdesc_plain(addr[0], addr[1] - addr[0], 160u);
+            const uint64_t bd = sdesc_plain(wbase + (uint32_t)(2 * p) * wblk, wblk, 128u);
+            umma_bf16(d, ad, bd, idesc, p ? 1u : 0u);
+          }
+          umma_commit(smem_u32(&bars.acc_full[b][t]));  // tile t's accumulator is complete
+        }
+        umma_commit(smem_u32(&bars.halo_empty[b]));  // halo b may be refilled
+      }
+      // let the last halo releases land before the block exits
+      const int n_done = i;
+      for (int k = n_done - 1; k >= 0 && k >= n_done - 2; --k)
+        mbar_drain(smem_u32(&bars.halo_empty[k & 1]), (uint32_t)((k >> 1) & 1));
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue (warps 5-8): TMEM lane quarter warp & 3, one
+    // output position per thread in each of the 4 tiles
     const int quarter = warp & 3, m = quarter * 32 + lane;
     const int yl = m >> 6, xq = (m >> 3) & 7, z = m & 7;
-    const uint64_t* rec = a.out_rec + (size_t)L * 10;
-    const uint64_t mw = __ldg(reinterpret_cast<const unsigned long long*>(rec) + xq);
-    const uint32_t first = (uint32_t)__ldg(reinterpret_cast<const unsigned long long*>(rec) + 8);
-    const uint64_t pre9 = __ldg(reinterpret_cast<const unsigned long long*>(rec) + 9);
-    const uint32_t pre = xq ? (uint32_t)((pre9 >> (9 * (xq - 1))) & 511ull) : 0u;
-    for (int tt = 0; tt < 2; ++tt) {
-      const int t = (warp >> 2) + 2 * tt;
-      mbar_wait(smem_u32(done + t), 0u, a.status);
-      tc_fence_after();
-      const int bit = (2 * t + yl) * 8 + z;
-      const bool act = (mw >> bit) & 1ull;
-      const int64_t q = (int64_t)first + pre + __popcll(mw & ((1ull << bit) - 1ull));
-      const uint32_t trow = tmem + (uint32_t)(t * cout) + ((uint32_t)(quarter * 32) << 16);
-      for (int c = 0; c < cout; c += 16) {
-        uint32_t v[16];
-        tmem_ld16(trow + (uint32_t)c, v);
-        if (!act) continue;
-        if (a.out_bf16) {
-          uint4 v0, v1;
-          v0.x = pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1]));
-          v0.y = pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3]));
-          v0.z = pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5]));
-          v0.w = pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7]));
-          v1.x = pack_bf16x2(__uint_as_float(v[8]), __uint_as_float(v[9]));
-          v1.y = pack_bf16x2(__uint_as_float(v[10]), __uint_as_float(v[11]));
-          v1.z = pack_bf16x2(__uint_as_float(v[12]), __uint_as_float(v[13]));
-          v1.w = pack_bf16x2(__uint_as_float(v[14]), __uint_as_float(v[15]));
-          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.y) + q * cout + c);
-          dst[0] = v0;
-          dst[1] = v1;
-        } else {
-          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<float*>(a.y) + q * cout + c);
+    int i = 0;
+    for (int64_t L = blockIdx.x; L < nL; L += G, ++i) {
+      const int b = i & 1;
+      const unsigned long long* rec = reinterpret_cast<const unsigned long long*>(a.out_rec) + (size_t)L * 10;
+      const uint64_t mw = __ldg(rec + xq);
+      const uint32_t first = (uint32_t)__ldg(rec + 8);
+      const uint64_t pre9 = __ldg(rec + 9);
+      const uint32_t pre = xq ? (uint32_t)((pre9 >> (9 * (xq - 1))) & 511ull) : 0u;
+      for (int t = 0; t < 4; ++t) {
+        mbar_wait(smem_u32(&bars.acc_full[b][t]), (uint32_t)((i >> 1) & 1), status);
+        tc_fence_after();
+        const int bit = (2 * t + yl) * 8 + z;
+        const bool act = (mw >> bit) & 1ull;
+        const int64_t q = (int64_t)first + pre + __popcll(mw & ((1ull << bit) - 1ull));
+        const uint32_t trow = tmem + (uint32_t)(b * 4 + t) * tcs + ((uint32_t)(quarter * 32) << 16);
+        for (int c = 0; c < cout; c += 16) {
+          uint32_t v[16];
+          tmem_ld16(trow + (uint32_t)c, v);
+          if (!act) continue;
+          if (a.out_bf16) {
+            uint4 v0, v1;
+            v0.x = pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1]));
+            v0.y = pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3]));
+            v0.z = pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5]));
+            v0.w = pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7]));
+            v1.x = pack_bf16x2(__uint_as_float(v[8]), __uint_as_float(v[9]));
+            v1.y = pack_bf16x2(__uint_as_float(v[10]), __uint_as_float(v[11]));
+            v1.z = pack_bf16x2(__uint_as_float(v[12]), __uint_as_float(v[13]));
+            v1.w = pack_bf16x2(__uint_as_float(v[14]), __uint_as_float(v[15]));
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.y) + q * cout + c);
+            dst[0] = v0;
+            dst[1] = v1;
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<float*>(a.y) + q * cout + c);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+            for (int e = 0; e < 4; ++e) dst[e] = make_uint4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+          }
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars.acc_empty[b]));
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == kLeafMmaWarp) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(a.tmem_cols) : "memory");
   }
@@ -1274,24 +1346,28 @@ fvx_status launch_conv_leaf(const char* who, fvx_grid gin, fvx_kmap m, fvx_dtype
   a.cin = (int)cin;
   a.cout = (int)cout;
   a.out_bf16 = (dt == FVX_BF16_OUT_BF16) ? 1 : 0;
-  const int tcs = (int)((cout + 31) & ~(int64_t)31);  // accumulator columns per M tile
+  a.tile_cols = (int)((cout + 31) & ~(int64_t)31);  // accumulator columns per M tile
   int cols = 32;
-  while (cols < 4 * tcs) cols <<= 1;
+  while (cols < 8 * a.tile_cols) cols <<= 1;  // two sets of 4 tiles
   a.tmem_cols = cols;
   a.halo_bytes = (3 * (int)(cin / 8) * kLeafPlaneBytes + 1023) & ~1023;
   a.w_bytes = ((27 * (int)(cin / 8) + 1) * (int)cout * 16 + 1023) & ~1023;
-  size_t smem = 1024 + (size_t)a.halo_bytes + a.w_bytes + 27 * sizeof(LeafNbr) + 40;
-  int dev = 0, sm_bytes = 0, reserved = 0;
+  const size_t smem = 1024 + 2 * (size_t)a.halo_bytes + a.w_bytes + 54 * sizeof(LeafNbr) + sizeof(LeafBars);
+  int dev = 0, sms = 0, sm_bytes = 0, reserved = 0;
   FVX_CUDA(cudaGetDevice(&dev));
+  FVX_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
   FVX_CUDA(cudaDeviceGetAttribute(&sm_bytes, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev));
   FVX_CUDA(cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev));
-  const size_t per_sm = (size_t)(512 / cols);  // blocks whose accumulators fit in TMEM together
-  if ((size_t)sm_bytes / (smem + reserved) > per_sm) smem = (size_t)sm_bytes / (per_sm + 1) - reserved + 16;
+  // blocks per SM: what shared memory holds, and no more than the tensor
+  // memory holds at once (a block waits in tcgen05.alloc otherwise)
+  int per_sm = (int)((size_t)sm_bytes / (smem + (size_t)reserved));
+  per_sm = std::max(1, std::min(per_sm, 512 / cols));
   auto kern = (cin == 16) ? k_conv_leaf<2> : k_conv_leaf<1>;
   FVX_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  const int64_t grid = std::min<int64_t>(go->n_leaf, (int64_t)sms * per_sm);
   {
     LaunchScope ls("conv_leaf", s);
-    kern<<<(unsigned)go->n_leaf, kLeafThreads, smem, s>>>(a);
+    kern<<<(unsigned)grid, kLeafThreads, smem, s>>>(a);
   }
   FVX_TRY(check_launch("conv_leaf"));
   (void)who;
