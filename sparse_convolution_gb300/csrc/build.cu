@@ -195,20 +195,18 @@ __global__ void __launch_bounds__(kThreads) k_bitmap_set(const int32_t* __restri
   atomicOr(bm + (key >> 6), 1ull << (key & 63));
 }
 
-// One warp per bitmap word: the word's set bits, in order, to keys[rank].
+// One thread per bitmap word: the word's set bits, in order, to keys[rank].
 __global__ void __launch_bounds__(kThreads) k_bitmap_emit(const uint64_t* __restrict__ bm,
                                                           const uint32_t* __restrict__ wpre, int64_t nwords,
                                                           uint64_t* __restrict__ keys) {
-  const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
+  const int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (w >= nwords) return;
-  const uint64_t m = bm[w];
-  if (!m) return;
-  const uint32_t base = wpre[w];
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int b = h * 32 + lane;
-    if ((m >> b) & 1ull) keys[base + (uint32_t)__popcll(m & ((1ull << b) - 1ull))] = ((uint64_t)w << 6) | (uint64_t)b;
+  uint64_t m = bm[w];
+  uint32_t pos = wpre[w];
+  while (m) {
+    const int b = __ffsll((long long)m) - 1;
+    keys[pos++] = ((uint64_t)w << 6) | (uint64_t)b;
+    m &= m - 1ull;
   }
 }
 
@@ -745,7 +743,7 @@ fvx_status build_grid_device(const int32_t* coords, int64_t n, const int64_t* of
       FVX_TRY(scan_popc64(bm, bm_pre, bm_words, n_live, s, scr));
       {
         LaunchScope ls("build_bitmap_emit", s);
-        k_bitmap_emit<<<grid_for(bm_words * 32, kThreads), kThreads, 0, s>>>(bm, bm_pre, bm_words, ka);
+        k_bitmap_emit<<<grid_for(bm_words, kThreads), kThreads, 0, s>>>(bm, bm_pre, bm_words, ka);
       }
       FVX_TRY(check_launch("build_bitmap_emit"));
     } else if (width1 == 0) {

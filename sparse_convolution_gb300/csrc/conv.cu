@@ -1185,11 +1185,20 @@ __global__ void __launch_bounds__(kLeafThreads, G8 == 1 ? 2 : 1) k_conv_leaf(con
       int i = 0;
       for (int64_t L = blockIdx.x; L < nL; L += G, ++i) {
         const int b = i & 1;
+        // tiles (2 y-rows of every x-slice) without an active output get no MMAs
+        const unsigned long long* orec = reinterpret_cast<const unsigned long long*>(a.out_rec) + (size_t)L * 10;
+        uint64_t occ = 0;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) occ |= __ldg(orec + w);
         mbar_wait(smem_u32(&bars.halo_full[b]), (uint32_t)((i >> 1) & 1), status);
         if (i >= 2) mbar_wait(smem_u32(&bars.acc_empty[b]), (uint32_t)(((i >> 1) - 1) & 1), status);
         tc_fence_after();
         const uint32_t hbase = smem_u32(halo0) + (uint32_t)b * (uint32_t)a.halo_bytes;
         for (int t = 0; t < 4; ++t) {
+          if (((occ >> (16 * t)) & 0xFFFFull) == 0ull) {
+            mbar_arrive(smem_u32(&bars.acc_full[b][t]));  // nothing to write in this tile
+            continue;
+          }
           const uint32_t d = tmem + (uint32_t)(b * 4 + t) * tcs;
           for (int p = 0; p < npair; ++p) {
             uint32_t addr[2];
