@@ -94,8 +94,7 @@ __global__ void __launch_bounds__(kThreads) k_plan_reduce(const int32_t* __restr
                                                           PlanDev* __restrict__ plan) {
   int tmin[3] = {INT_MAX, INT_MAX, INT_MAX}, tmax[3] = {INT_MIN, INT_MIN, INT_MIN};
   unsigned long long o_or = 0ull, o_and = ~0ull;
-  for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < n; r += (int64_t)gridDim.x * blockDim.x) {
-    const int i = coords[3 * r], j = coords[3 * r + 1], k = coords[3 * r + 2];
+  auto take = [&](int i, int j, int k) {
     const int t[3] = {i >> 12, j >> 12, k >> 12};
 #pragma unroll
     for (int a = 0; a < 3; ++a) {
@@ -105,6 +104,23 @@ __global__ void __launch_bounds__(kThreads) k_plan_reduce(const int32_t* __restr
     const uint64_t o = offset_key(i, j, k);
     o_or |= o;
     o_and &= o;
+  };
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t first = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if ((reinterpret_cast<uintptr_t>(coords) & 15u) == 0u) {
+    // four rows (three 16-byte loads) per thread and step
+    const int64_t n4 = n >> 2;
+    const int4* c4 = reinterpret_cast<const int4*>(coords);
+    for (int64_t g = first; g < n4; g += stride) {
+      const int4 a = __ldg(c4 + 3 * g), b = __ldg(c4 + 3 * g + 1), c = __ldg(c4 + 3 * g + 2);
+      take(a.x, a.y, a.z);
+      take(a.w, b.x, b.y);
+      take(b.z, b.w, c.x);
+      take(c.y, c.z, c.w);
+    }
+    for (int64_t r = 4 * n4 + first; r < n; r += stride) take(coords[3 * r], coords[3 * r + 1], coords[3 * r + 2]);
+  } else {
+    for (int64_t r = first; r < n; r += stride) take(coords[3 * r], coords[3 * r + 1], coords[3 * r + 2]);
   }
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) {
@@ -195,19 +211,27 @@ __global__ void __launch_bounds__(kThreads) k_bitmap_set(const int32_t* __restri
   atomicOr(bm + (key >> 6), 1ull << (key & 63));
 }
 
-// One thread per bitmap word: the word's set bits, in order, to keys[rank].
+// One thread per bitmap word; a block gathers the set bits of its 256 words in
+// order in shared memory (32-bit keys: the key space has at most 28 bits) and
+// writes them out as one contiguous, coalesced run of the key list.
 __global__ void __launch_bounds__(kThreads) k_bitmap_emit(const uint64_t* __restrict__ bm,
                                                           const uint32_t* __restrict__ wpre, int64_t nwords,
                                                           uint64_t* __restrict__ keys) {
-  const int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (w >= nwords) return;
-  uint64_t m = bm[w];
-  uint32_t pos = wpre[w];
+  extern __shared__ uint32_t skey[];  // kThreads * 64 entries at most
+  __shared__ uint32_t tmp[33];
+  const int64_t w0 = (int64_t)blockIdx.x * kThreads;
+  const int64_t w = w0 + threadIdx.x;
+  uint64_t m = (w < nwords) ? bm[w] : 0ull;
+  uint32_t total;
+  uint32_t pos = block_exclusive_scan<uint32_t>((uint32_t)__popcll(m), tmp, &total);
   while (m) {
     const int b = __ffsll((long long)m) - 1;
-    keys[pos++] = ((uint64_t)w << 6) | (uint64_t)b;
+    skey[pos++] = ((uint32_t)w << 6) | (uint32_t)b;
     m &= m - 1ull;
   }
+  __syncthreads();
+  const uint32_t base = wpre[w0];
+  for (uint32_t e = threadIdx.x; e < total; e += kThreads) keys[base + e] = skey[e];
 }
 
 // Index of every input row: the rank of its key's bit.
@@ -668,7 +692,7 @@ fvx_status build_grid_device(const int32_t* coords, int64_t n, const int64_t* of
     FVX_TRY(check_launch("build_plan_init"));
     {
       LaunchScope ls("build_plan_reduce", s);
-      unsigned nb = std::min<unsigned>(grid_for(n, kThreads), 152u * 2u);
+      unsigned nb = std::min<unsigned>(grid_for((n + 3) / 4, kThreads), 152u * 8u);
       k_plan_reduce<<<nb, kThreads, 0, s>>>(coords, n, plan);
     }
     FVX_TRY(check_launch("build_plan_reduce"));
@@ -743,7 +767,9 @@ fvx_status build_grid_device(const int32_t* coords, int64_t n, const int64_t* of
       FVX_TRY(scan_popc64(bm, bm_pre, bm_words, n_live, s, scr));
       {
         LaunchScope ls("build_bitmap_emit", s);
-        k_bitmap_emit<<<grid_for(bm_words, kThreads), kThreads, 0, s>>>(bm, bm_pre, bm_words, ka);
+        FVX_CUDA(cudaFuncSetAttribute(k_bitmap_emit, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      kThreads * 64 * 4));
+        k_bitmap_emit<<<grid_for(bm_words, kThreads), kThreads, kThreads * 64 * 4, s>>>(bm, bm_pre, bm_words, ka);
       }
       FVX_TRY(check_launch("build_bitmap_emit"));
     } else if (width1 == 0) {
