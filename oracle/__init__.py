@@ -55,6 +55,9 @@ def _load():
         "oracle_lookup": ([P, P, P, I64, P], None),
         "oracle_coarsen": ([P, I32], P),
         "oracle_kernel_map": ([P, P, I32], P),
+        "oracle_kernel_map_transposed": ([P, P, I32], P),
+        "oracle_refine": ([P, I32], P),
+        "oracle_conv_wgrad": ([P, P, I64, P, I64, P], None),
         "oracle_kmap_free": ([P], None),
         "oracle_kmap_pairs": ([P], I64),
         "oracle_kmap_export": ([P, P, P, P, P], None),
@@ -158,14 +161,25 @@ class Grid:
             raise ValueError("oracle_coarsen: bad stride")
         return Grid(h, self.B)
 
+    def refine(self, factor: int = 2) -> "Grid":
+        """All factor^3 children of every voxel (the refined grid)."""
+        h = _load().oracle_refine(self._h, int(factor))
+        if not h:
+            raise ValueError("oracle_refine: bad factor")
+        return Grid(h, self.B)
+
 
 class KernelMap:
     """Per-offset (in, out) pair lists of a 3x3x3 kernel, ordered by output."""
 
-    def __init__(self, gin: Grid, gout: Grid, stride: int):
-        self._h = _load().oracle_kernel_map(gin._h, gout._h, int(stride))
+    def __init__(self, gin: Grid, gout: Grid, stride: int, transposed: bool = False):
+        """transposed: the map of the transposed convolution (output voxel p of
+        gout, input voxel q of gin with stride * ijk(q) + d_s = ijk(p))."""
+        f = _load().oracle_kernel_map_transposed if transposed else _load().oracle_kernel_map
+        self._h = f(gin._h, gout._h, int(stride))
         if not self._h:
             raise ValueError("oracle_kernel_map: bad stride")
+        self.transposed = bool(transposed)
         self.stride = int(stride)
         self.n_out = gout.n_active
         P = int(_lib.oracle_kmap_pairs(self._h))
@@ -192,6 +206,17 @@ def conv(kmap: KernelMap, x: np.ndarray, W: np.ndarray):
     a = np.zeros((kmap.n_out, cout), np.float64)
     _load().oracle_conv(kmap._h, _ptr(x), cin, _ptr(W), cout, _ptr(y), _ptr(a))
     return y, a
+
+
+def conv_wgrad(kmap: KernelMap, x: np.ndarray, dy: np.ndarray):
+    """dW [27, cin, cout] (fp64): per list s, the sum over its pairs (p, q) of
+    the outer product x[p] (x) dy[q]."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    dy = np.ascontiguousarray(dy, dtype=np.float64)
+    cin, cout = x.shape[1], dy.shape[1]
+    dW = np.zeros((27, cin, cout), np.float64)
+    _load().oracle_conv_wgrad(kmap._h, _ptr(x), cin, _ptr(dy), cout, _ptr(dW))
+    return dW
 
 
 def conv_rows(gin: Grid, gout: Grid, stride: int, rows: np.ndarray, x: np.ndarray, W: np.ndarray):

@@ -332,6 +332,21 @@ oracle_grid* oracle_coarsen(const oracle_grid* g, int32_t stride) {
   return build_from_voxel_rows(rows, g->B);
 }
 
+// Refined grid: every voxel's factor^3 children, factor * ijk + (0..factor-1)^3,
+// per batch.  [fVDB-ONNX, §1.2 Grid-to-Grid ops: RefinedGrid]
+oracle_grid* oracle_refine(const oracle_grid* g, int32_t factor) {
+  if (factor < 1) return nullptr;
+  std::vector<Voxel> rows;
+  rows.reserve(g->voxels.size() * (size_t)factor * factor * factor);
+  for (const Voxel& v : g->voxels)
+    for (int a = 0; a < factor; ++a)
+      for (int b = 0; b < factor; ++b)
+        for (int c = 0; c < factor; ++c)
+          rows.push_back(Voxel{v.b, (int32_t)((int64_t)factor * v.i + a), (int32_t)((int64_t)factor * v.j + b),
+                               (int32_t)((int64_t)factor * v.k + c)});
+  return build_from_voxel_rows(rows, g->B);
+}
+
 // 3x3x3 kernel map: for every output voxel q (ascending) and offset slot s,
 // look up the input voxel at stride*ijk_out(q) + d_s in the same batch.
 // [DriveRT, Shared neighbour maps]; mask bit s set when the pair exists
@@ -383,6 +398,61 @@ void oracle_kmap_export(const oracle_kmap* m, int64_t* offsets, int32_t* in_idx,
 //   a[q,co] = the same sum of |x[p,ci] * W[s,ci,co]|
 // x: [n_in, cin], W: [27, cin, cout], y/a: [n_out, cout], row-major doubles.
 // [fVDB-notes, Sparse-convolution operators: gather-GEMM-scatter]
+// Kernel map of the transposed convolution: for every output voxel p of gout
+// (ascending) and slot s, the input voxel q of gin with stride * ijk(q) + d_s =
+// ijk(p) in the same batch, i.e. q = (ijk(p) - d_s) / stride when that division
+// is exact.  [fVDB-ONNX, §1.2 Grid-to-Grid ops: ConvTransposeGrid]  Its pairs are
+// those of oracle_kernel_map(gout, gin, stride) with input and output swapped.
+oracle_kmap* oracle_kernel_map_transposed(const oracle_grid* gin, const oracle_grid* gout, int32_t stride) {
+  if (stride != 1 && stride != 2) return nullptr;
+  oracle_kmap* m = new oracle_kmap();
+  m->stride = stride;
+  m->n_out = (int64_t)gout->voxels.size();
+  m->out_mask.assign((size_t)m->n_out, 0);
+  std::vector<std::vector<int32_t>> lin(27), lout(27);
+  for (int64_t p = 0; p < m->n_out; ++p) {
+    const Voxel& o = gout->voxels[p];
+    for (int di = -1; di <= 1; ++di)
+      for (int dj = -1; dj <= 1; ++dj)
+        for (int dk = -1; dk <= 1; ++dk) {
+          const int s = (di + 1) * 9 + (dj + 1) * 3 + (dk + 1);
+          const int64_t ci = (int64_t)o.i - di, cj = (int64_t)o.j - dj, ck = (int64_t)o.k - dk;
+          if (ci % stride != 0 || cj % stride != 0 || ck % stride != 0) continue;
+          Voxel c{o.b, (int32_t)(ci / stride), (int32_t)(cj / stride), (int32_t)(ck / stride)};
+          auto it = gin->index.find(c);
+          if (it != gin->index.end()) {
+            lin[s].push_back((int32_t)it->second);
+            lout[s].push_back((int32_t)p);
+            m->out_mask[p] |= 1u << s;
+          }
+        }
+  }
+  m->offsets.assign(28, 0);
+  for (int s = 0; s < 27; ++s) m->offsets[s + 1] = m->offsets[s] + (int64_t)lin[s].size();
+  for (int s = 0; s < 27; ++s) {
+    m->in_idx.insert(m->in_idx.end(), lin[s].begin(), lin[s].end());
+    m->out_idx.insert(m->out_idx.end(), lout[s].begin(), lout[s].end());
+  }
+  return m;
+}
+
+// Weight gradient: dW[s][ci][co] = sum over the pairs (p, q) of list s of
+// x[p][ci] * dy[q][co], in double.  [fVDB-notes, Sparse-convolution operators:
+// training computes gradients through the general (pair-list) backend]
+void oracle_conv_wgrad(const oracle_kmap* m, const double* x, int64_t cin, const double* dy, int64_t cout,
+                       double* dW) {
+  std::memset(dW, 0, sizeof(double) * (size_t)(27 * cin * cout));
+  for (int s = 0; s < 27; ++s) {
+    double* Ws = dW + (size_t)s * cin * cout;
+    for (int64_t e = m->offsets[s]; e < m->offsets[s + 1]; ++e) {
+      const double* xp = x + (size_t)m->in_idx[e] * cin;
+      const double* gq = dy + (size_t)m->out_idx[e] * cout;
+      for (int64_t ci = 0; ci < cin; ++ci)
+        for (int64_t co = 0; co < cout; ++co) Ws[ci * cout + co] += xp[ci] * gq[co];
+    }
+  }
+}
+
 void oracle_conv(const oracle_kmap* m, const double* x, int64_t cin, const double* W, int64_t cout, double* y,
                  double* a) {
   std::memset(y, 0, sizeof(double) * (size_t)(m->n_out * cout));

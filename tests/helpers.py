@@ -178,3 +178,49 @@ def key64(batch, ijk):
     off = (off * 8 + v[:, 1]) * 8 + v[:, 2]
     t = ((b * 16 + tile[:, 0] + 8) * 16 + tile[:, 1] + 8) * 16 + tile[:, 2] + 8
     return (t << 36) | off
+
+
+def dense_conv_transpose_active(ijk_in, x, W, ijk_out, stride):
+    """Dense conv_transpose3d (torch, float64, padding 1; output_padding 1 for
+    stride 2) over a zero-filled box holding the input grid, read back at the
+    active outputs: out[stride*i + d] += x[i] W[d] for d in {-1,0,1}^3."""
+    import torch
+
+    ijk_in = np.asarray(ijk_in, dtype=np.int64)
+    ijk_out = np.asarray(ijk_out, dtype=np.int64)
+    lo = np.minimum(ijk_in.min(0), np.floor_divide(ijk_out.min(0), stride)) - 2
+    hi = np.maximum(ijk_in.max(0), np.floor_divide(ijk_out.max(0), stride)) + 3
+    size = hi - lo
+    cin, cout = W.shape[1], W.shape[2]
+    dense = torch.zeros((1, cin) + tuple(int(v) for v in size), dtype=torch.float64)
+    rel = ijk_in - lo
+    dense[0, :, rel[:, 0], rel[:, 1], rel[:, 2]] = torch.from_numpy(np.asarray(x, np.float64)).T
+    # transposed-conv weight [cin, cout, kd, kh, kw]; slot s = kd*9 + kh*3 + kw
+    wt = torch.from_numpy(np.asarray(W, np.float64)).reshape(3, 3, 3, cin, cout).permute(3, 4, 0, 1, 2).contiguous()
+    y = torch.nn.functional.conv_transpose3d(dense, wt, stride=stride, padding=1, output_padding=stride - 1)
+    # dense output index o is coordinate stride*lo + o
+    orel = ijk_out - stride * lo
+    return y[0, :, orel[:, 0], orel[:, 1], orel[:, 2]].T.numpy()
+
+
+def dense_conv_wgrad(ijk_in, x, ijk_out, dy, stride, cin, cout):
+    """Gradient with respect to W of sum(conv(x, W)[active outputs] * dy), by
+    torch autograd on the dense conv3d (float64) of dense_conv_active."""
+    import torch
+
+    ijk_in = np.asarray(ijk_in, dtype=np.int64)
+    ijk_out = np.asarray(ijk_out, dtype=np.int64)
+    lo = np.minimum(ijk_in.min(0), stride * ijk_out.min(0)) - 2
+    lo = lo - np.mod(lo, 2)
+    hi = np.maximum(ijk_in.max(0), stride * ijk_out.max(0)) + 3
+    size = hi - lo
+    dense = torch.zeros((1, cin) + tuple(int(v) for v in size), dtype=torch.float64)
+    rel = ijk_in - lo
+    dense[0, :, rel[:, 0], rel[:, 1], rel[:, 2]] = torch.from_numpy(np.asarray(x, np.float64)).T
+    w = torch.zeros((cout, cin, 3, 3, 3), dtype=torch.float64, requires_grad=True)
+    y = torch.nn.functional.conv3d(dense, w, stride=stride, padding=1)
+    orel = ijk_out - lo // stride
+    ya = y[0, :, orel[:, 0], orel[:, 1], orel[:, 2]].T
+    (ya * torch.from_numpy(np.asarray(dy, np.float64))).sum().backward()
+    # w.grad [cout, cin, kd, kh, kw] -> dW [27, cin, cout]
+    return w.grad.permute(2, 3, 4, 1, 0).reshape(27, cin, cout).numpy()

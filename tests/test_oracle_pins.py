@@ -262,3 +262,98 @@ def test_dense_check_detects_flipped_kernel():
     y_tr, _ = oracle.conv(km, x, W.transpose(0, 2, 1).copy())
     assert np.max(np.abs(y_flip - ref)) > 1e-3
     assert np.max(np.abs(y_tr - ref)) > 1e-3
+
+
+# ------------------------------------------------------------ transposed conv, backward, refine
+@pytest.mark.parametrize("stride", [1, 2])
+def test_transposed_map_is_swapped_forward_map(stride):
+    """Pairs of the transposed map (output p of the fine grid, input q of the
+    coarse one) = pairs of the forward map with input and output swapped, per
+    offset list, ordered by p."""
+    coords, offs = _random_grid(61 + stride, n=2500, span=30, lo=-15, B=2)
+    fine = oracle.Grid.build(coords, offs)
+    coarse = fine if stride == 1 else fine.coarsen(2)
+    fwd = oracle.KernelMap(fine, coarse, stride)
+    tr = oracle.KernelMap(coarse, fine, stride, transposed=True)
+    assert tr.n_pairs == fwd.n_pairs
+    assert np.array_equal(np.diff(tr.offsets), np.diff(fwd.offsets))
+    for s in range(27):
+        a, b = fwd.offsets[s], fwd.offsets[s + 1]
+        c, d = tr.offsets[s], tr.offsets[s + 1]
+        exp = np.stack([fwd.out_idx[a:b], fwd.in_idx[a:b]], 1)  # (in, out) of the transposed map
+        exp = exp[np.argsort(exp[:, 1], kind="stable")]
+        got = np.stack([tr.in_idx[c:d], tr.out_idx[c:d]], 1)
+        assert np.array_equal(exp, got), s
+        assert np.all(np.diff(tr.out_idx[c:d]) > 0)
+    # mask bit s of output p: p has a pair in list s
+    for s in range(27):
+        c, d = tr.offsets[s], tr.offsets[s + 1]
+        m = np.zeros(fine.n_active, bool)
+        m[tr.out_idx[c:d]] = True
+        assert np.array_equal(m, (tr.mask >> s) & 1 == 1)
+
+
+@pytest.mark.parametrize("stride,cin,cout", [(2, 4, 6), (1, 5, 3)])
+def test_transposed_conv_matches_dense_conv_transpose3d(stride, cin, cout):
+    coords, offs = _random_grid(71 + stride, n=900, span=16, lo=-9, B=1, dup=0.0)
+    fine = oracle.Grid.build(coords, offs)
+    coarse = fine if stride == 1 else fine.coarsen(2)
+    tr = oracle.KernelMap(coarse, fine, stride, transposed=True)
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal((coarse.n_active, cin))
+    W = rng.standard_normal((27, cin, cout))
+    y, a = oracle.conv(tr, x, W)
+    ref = H.dense_conv_transpose_active(coarse.voxels()["ijk"], x, W, fine.voxels()["ijk"], stride)
+    assert np.max(np.abs(y - ref)) <= 1e-12 * max(1.0, np.max(a))
+
+
+@pytest.mark.parametrize("stride", [1, 2])
+def test_adjoint_identity(stride):
+    """<conv(u; K, W), v> = <u, conv(v; K^T, W^T)>: the transposed map with the
+    per-offset transposed weights is the adjoint (the input gradient)."""
+    coords, offs = _random_grid(81 + stride, n=1200, span=18, lo=-9, B=2)
+    fine = oracle.Grid.build(coords, offs)
+    coarse = fine if stride == 1 else fine.coarsen(2)
+    fwd = oracle.KernelMap(fine, coarse, stride)
+    tr = oracle.KernelMap(coarse, fine, stride, transposed=True)
+    rng = np.random.default_rng(7)
+    u = rng.standard_normal((fine.n_active, 5))
+    v = rng.standard_normal((coarse.n_active, 3))
+    W = rng.standard_normal((27, 5, 3))
+    y, _ = oracle.conv(fwd, u, W)
+    z, _ = oracle.conv(tr, v, W.transpose(0, 2, 1).copy())
+    lhs, rhs = float(np.sum(y * v)), float(np.sum(u * z))
+    assert abs(lhs - rhs) <= 1e-10 * max(1.0, abs(lhs))
+    # a transposed map built with the forward (unmirrored) offsets breaks it
+    if stride == 1:
+        z_bad, _ = oracle.conv(fwd, v, W.transpose(0, 2, 1).copy())
+        assert abs(float(np.sum(u * z_bad)) - lhs) > 1e-6
+
+
+@pytest.mark.parametrize("stride,cin,cout", [(1, 4, 5), (2, 3, 4)])
+def test_wgrad_matches_autograd(stride, cin, cout):
+    coords, offs = _random_grid(91 + stride, n=800, span=14, lo=-7, B=1, dup=0.0)
+    fine = oracle.Grid.build(coords, offs)
+    coarse = fine if stride == 1 else fine.coarsen(2)
+    km = oracle.KernelMap(fine, coarse, stride)
+    rng = np.random.default_rng(8)
+    x = rng.standard_normal((fine.n_active, cin))
+    dy = rng.standard_normal((coarse.n_active, cout))
+    dW = oracle.conv_wgrad(km, x, dy)
+    ref = H.dense_conv_wgrad(fine.voxels()["ijk"], x, coarse.voxels()["ijk"], dy, stride, cin, cout)
+    assert np.max(np.abs(dW - ref)) <= 1e-10 * max(1.0, np.max(np.abs(ref)))
+
+
+def test_refine_is_all_children():
+    coords, offs = _random_grid(99, n=700, span=20, lo=-10, B=2)
+    g = oracle.Grid.build(coords, offs)
+    r = g.refine(2)
+    v, vr = g.voxels(), r.voxels()
+    kids = np.stack(np.meshgrid(*[np.arange(2)] * 3, indexing="ij"), -1).reshape(-1, 3)
+    exp = (2 * v["ijk"][:, None, :].astype(np.int64) + kids[None]).reshape(-1, 3)
+    eb = np.repeat(v["batch"], 8)
+    exp = np.unique(np.concatenate([eb[:, None], exp], 1), axis=0)
+    got = np.unique(np.concatenate([vr["batch"][:, None], vr["ijk"]], 1).astype(np.int64), axis=0)
+    assert np.array_equal(exp, got)
+    assert r.n_active == 8 * g.n_active  # children of distinct voxels are distinct
+    assert np.array_equal(r.coarsen(2).voxels()["ijk"], v["ijk"])
