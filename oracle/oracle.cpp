@@ -347,6 +347,10 @@ oracle_grid* oracle_refine(const oracle_grid* g, int32_t factor) {
   return build_from_voxel_rows(rows, g->B);
 }
 
+// A coordinate a grid can hold.  Neighbour positions are computed exactly in
+// 64 bits; one outside int32 is no voxel of any grid (no wrap-around).
+static bool in_int32(int64_t v) { return v >= INT32_MIN && v <= INT32_MAX; }
+
 // 3x3x3 kernel map: for every output voxel q (ascending) and offset slot s,
 // look up the input voxel at stride*ijk_out(q) + d_s in the same batch.
 // [DriveRT, Shared neighbour maps]; mask bit s set when the pair exists
@@ -364,8 +368,10 @@ oracle_kmap* oracle_kernel_map(const oracle_grid* gin, const oracle_grid* gout, 
       for (int dj = -1; dj <= 1; ++dj)
         for (int dk = -1; dk <= 1; ++dk) {
           int s = (di + 1) * 9 + (dj + 1) * 3 + (dk + 1);
-          Voxel c{o.b, (int32_t)((int64_t)stride * o.i + di), (int32_t)((int64_t)stride * o.j + dj),
-                  (int32_t)((int64_t)stride * o.k + dk)};
+          const int64_t ci = (int64_t)stride * o.i + di, cj = (int64_t)stride * o.j + dj,
+                        ck = (int64_t)stride * o.k + dk;
+          if (!in_int32(ci) || !in_int32(cj) || !in_int32(ck)) continue;  // no such voxel: no pair
+          Voxel c{o.b, (int32_t)ci, (int32_t)cj, (int32_t)ck};
           auto it = gin->index.find(c);
           if (it != gin->index.end()) {
             lin[s].push_back((int32_t)it->second);
@@ -418,6 +424,7 @@ oracle_kmap* oracle_kernel_map_transposed(const oracle_grid* gin, const oracle_g
           const int s = (di + 1) * 9 + (dj + 1) * 3 + (dk + 1);
           const int64_t ci = (int64_t)o.i - di, cj = (int64_t)o.j - dj, ck = (int64_t)o.k - dk;
           if (ci % stride != 0 || cj % stride != 0 || ck % stride != 0) continue;
+          if (!in_int32(ci / stride) || !in_int32(cj / stride) || !in_int32(ck / stride)) continue;
           Voxel c{o.b, (int32_t)(ci / stride), (int32_t)(cj / stride), (int32_t)(ck / stride)};
           auto it = gin->index.find(c);
           if (it != gin->index.end()) {
@@ -487,8 +494,10 @@ void oracle_conv_rows(const oracle_grid* gin, const oracle_grid* gout, int32_t s
       for (int dj = -1; dj <= 1; ++dj)
         for (int dk = -1; dk <= 1; ++dk) {
           int s = (di + 1) * 9 + (dj + 1) * 3 + (dk + 1);
-          Voxel c{o.b, (int32_t)((int64_t)stride * o.i + di), (int32_t)((int64_t)stride * o.j + dj),
-                  (int32_t)((int64_t)stride * o.k + dk)};
+          const int64_t pi = (int64_t)stride * o.i + di, pj = (int64_t)stride * o.j + dj,
+                        pk = (int64_t)stride * o.k + dk;
+          if (!in_int32(pi) || !in_int32(pj) || !in_int32(pk)) continue;  // no such voxel: no pair
+          Voxel c{o.b, (int32_t)pi, (int32_t)pj, (int32_t)pk};
           auto it = gin->index.find(c);
           if (it == gin->index.end()) continue;
           const double* xp = x + (size_t)it->second * cin;

@@ -264,6 +264,46 @@ def test_dense_check_detects_flipped_kernel():
     assert np.max(np.abs(y_tr - ref)) > 1e-3
 
 
+def _pairs_python_ints(vin, vout, stride, transposed):
+    """Brute-force (slot, in, out) triples in Python integers (no fixed-width
+    arithmetic, so no wrap-around at the int32 edges)."""
+    index = {(int(b), *map(int, ijk)): n for n, (b, ijk) in enumerate(zip(vin["batch"], vin["ijk"]))}
+    out = set()
+    for q, (b, ijk) in enumerate(zip(vout["batch"], vout["ijk"])):
+        for s in range(27):
+            d = (s // 9 - 1, (s // 3) % 3 - 1, s % 3 - 1)
+            if transposed:
+                c = [int(x) - e for x, e in zip(ijk, d)]
+                if any(v % stride for v in c):
+                    continue
+                c = [v // stride for v in c]
+            else:
+                c = [stride * int(x) + e for x, e in zip(ijk, d)]
+            p = index.get((int(b), *c))
+            if p is not None:
+                out.add((s, p, q))
+    return out
+
+
+@pytest.mark.parametrize("stride", [1, 2])
+@pytest.mark.parametrize("transposed", [False, True])
+def test_kmap_int32_edges_do_not_wrap(stride, transposed):
+    """Voxels at both ends of the int32 range in one batch: a neighbour
+    position past an end is no voxel (IndexGrid coordinates are int32 ijk), so
+    2^31 - 1 and -2^31 never pair."""
+    M = 2 ** 31 - 1
+    c = np.array([[M, 0, 0], [-M - 1, 0, 0], [M - 1, 0, 0], [M, M, M], [-M - 1, -M - 1, -M - 1],
+                  [-M - 1, M, 0], [M, -M - 1, 5]], np.int32)
+    fine = oracle.Grid.build(c, [0, len(c)])
+    coarse = fine if stride == 1 else fine.coarsen(2)
+    gi, go = (coarse, fine) if transposed else (fine, coarse)
+    km = oracle.KernelMap(gi, go, stride, transposed=transposed)
+    exp = _pairs_python_ints(gi.voxels(), go.voxels(), stride, transposed)
+    assert H.kmap_triples(km.offsets, km.in_idx, km.out_idx) == sorted(exp)
+    if stride == 1:  # only the centre pairs and the one pair along i at the top
+        assert len(exp) == len(c) + 2
+
+
 # ------------------------------------------------------------ transposed conv, backward, refine
 @pytest.mark.parametrize("stride", [1, 2])
 def test_transposed_map_is_swapped_forward_map(stride):
