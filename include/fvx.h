@@ -142,6 +142,15 @@ fvx_status fvx_lookup(fvx_grid g, const int32_t* coords, const int32_t* batch_id
  * ConvGrid]  Synchronises like fvx_build_grid. */
 fvx_status fvx_coarsen(fvx_grid g, int32_t stride, fvx_stream stream, fvx_grid* out);
 
+/* Refined grid: every voxel ijk of g replaced by its factor^3 children
+ * factor*ijk + {0..factor-1}^3, same batch; the output grid of a transposed
+ * strided conv whose kernel covers one stride cell.  factor 1..1024 and
+ * n_active * factor^3 <= 2^31 - 2 (FVX_ERR_RANGE otherwise); a child
+ * coordinate outside int32 is found on the device and reported as
+ * FVX_ERR_CHECK.  Voxels in the output are ordered like any built grid.
+ * [fVDB-ONNX §1.2 RefinedGrid]  Synchronises like fvx_build_grid. */
+fvx_status fvx_refine(fvx_grid g, int32_t factor, fvx_stream stream, fvx_grid* out);
+
 /* ---------------------------------------------------------------------------
  * Kernel map  [DriveRT, "Shared neighbour maps"; "Kernels selected per GPU"]
  *
@@ -170,6 +179,23 @@ fvx_status fvx_kernel_map(fvx_grid gin, fvx_grid gout, int32_t ksize, int32_t st
  * device work. */
 fvx_status fvx_kmap_view(fvx_kmap m, const int64_t** offsets_host, const int32_t** in_idx, const int32_t** out_idx,
                          const uint32_t** out_mask, int64_t* n_pairs, int64_t* n_out);
+
+/* Kernel map of the transposed (inverse) convolution
+ * [fVDB-ONNX §1.2 ConvTransposeGrid: the transposed conv scatters each input
+ * voxel to stride*ijk + d].  For every output voxel q of gout and slot s (d as
+ * above), the input voxel p of gin with stride*ijk(p) + d == ijk(q), when
+ * ijk(q) - d is divisible by stride.  It pairs exactly what
+ * fvx_kernel_map(gout, gin, 3, stride) pairs, with the roles of input and
+ * output swapped and the same slot numbers, so
+ *   - fvx_sparse_conv over it computes the transposed convolution of gin's
+ *     features onto gout (gout usually fvx_refine(gin, 2) for stride 2, or
+ *     gin itself for stride 1), and
+ *   - fvx_sparse_conv_dgrad over fvx_kernel_map_transposed(gout, gin, ...)
+ *     computes the input gradient of a forward conv from gin to gout.
+ * Same layout, sizing, synchronisation and errors as fvx_kernel_map; the bf16
+ * leaf-densified kernels never run on it. */
+fvx_status fvx_kernel_map_transposed(fvx_grid gin, fvx_grid gout, int32_t ksize, int32_t stride, fvx_stream stream,
+                                     fvx_kmap* out);
 
 /* ---------------------------------------------------------------------------
  * Sparse convolution (gather - GEMM - scatter)  [fVDB-notes, "Sparse-
@@ -239,6 +265,36 @@ fvx_conv_algo fvx_last_conv_algo(void);
  *     status word, which fvx_device_status does not read. */
 fvx_status fvx_sparse_conv_noalloc(fvx_grid gin, fvx_grid gout, fvx_kmap m, fvx_dtype dt, const void* feats,
                                    int64_t cin, const void* W, int64_t cout, void* out, fvx_stream stream);
+
+/* ---------------------------------------------------------------------------
+ * Backward pass of fvx_sparse_conv  [fVDB paper, "Limitations and future
+ * work": training computes its gradients through the pair-list (IGEMM)
+ * backend]
+ *
+ * Input gradient, for y = conv(x, W) over the map of (gin, gout):
+ *   dx[p, ci] = sum_s sum_{(p,q) in list s} sum_co dout[q, co] * W[s, ci, co]
+ * mt: fvx_kernel_map_transposed(gout, gin, 3, stride) (FVX_ERR_INVALID_ARG
+ *     for any other map).
+ * dout device [gout.n_active, cout]; W device [27, cin, cout] as in
+ *     fvx_sparse_conv; dx device [gin.n_active, cin], caller-allocated, fully
+ *     overwritten (zero where no pair reaches it).
+ * Types as fvx_sparse_conv with the roles of cin and cout swapped: bf16
+ *     needs cout a multiple of 8 (<= 512), cin a multiple of 16 (<= 256),
+ *     dout, W and dx 16-byte aligned; FVX_F32 any sizes >= 1 (it transposes W
+ *     into library scratch first).  Runs the pair-list kernels. */
+fvx_status fvx_sparse_conv_dgrad(fvx_grid gin, fvx_grid gout, fvx_kmap mt, fvx_dtype dt, const void* dout,
+                                 int64_t cout, const void* W, int64_t cin, void* dx, fvx_stream stream);
+
+/* Weight gradient over the forward map m of (gin, gout):
+ *   dW[s, ci, co] = sum_{(p,q) in list s} feats[p, ci] * dout[q, co]
+ * feats device [gin.n_active, cin], dout device [gout.n_active, cout], both
+ * fp32 (FVX_F32) or bf16 (FVX_BF16); dW device fp32 [27, cin, cout],
+ * caller-allocated, fully overwritten.  Products and sums in fp32 (bf16
+ * inputs are widened exactly); the summation order is not fixed (atomic
+ * adds), so results may differ between runs in the last bits.
+ * 1 <= cin, cout <= 65536.  Errors: FVX_ERR_INVALID_ARG. */
+fvx_status fvx_sparse_conv_wgrad(fvx_grid gin, fvx_grid gout, fvx_kmap m, fvx_dtype dt, const void* feats,
+                                 int64_t cin, const void* dout, int64_t cout, float* dW, fvx_stream stream);
 
 fvx_status fvx_grid_destroy(fvx_grid g);
 fvx_status fvx_kmap_destroy(fvx_kmap m);

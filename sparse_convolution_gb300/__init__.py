@@ -62,9 +62,13 @@ def load():
         "fvx_lookup": ([P, P, P, I64, P, P], I32),
         "fvx_coarsen": ([P, I32, P, PP], I32),
         "fvx_kernel_map": ([P, P, I32, I32, P, PP], I32),
+        "fvx_kernel_map_transposed": ([P, P, I32, I32, P, PP], I32),
+        "fvx_refine": ([P, I32, P, PP], I32),
         "fvx_kmap_view": ([P, PP, PP, PP, PP, P, P], I32),
         "fvx_sparse_conv": ([P, P, P, I32, P, I64, P, I64, P, P], I32),
         "fvx_sparse_conv_noalloc": ([P, P, P, I32, P, I64, P, I64, P, P], I32),
+        "fvx_sparse_conv_dgrad": ([P, P, P, I32, P, I64, P, I64, P, P], I32),
+        "fvx_sparse_conv_wgrad": ([P, P, P, I32, P, I64, P, I64, P, P], I32),
         "fvx_grid_destroy": ([P], I32),
         "fvx_kmap_destroy": ([P], I32),
         "fvx_status_string": ([I32], ctypes.c_char_p),
@@ -207,15 +211,24 @@ class Grid:
         _check(load().fvx_coarsen(self._h, int(stride), _stream(stream), ctypes.byref(h)))
         return Grid(h)
 
+    def refine(self, factor=2, stream=None) -> "Grid":
+        """Every voxel's factor^3 children (the refined grid)."""
+        h = ctypes.c_void_p()
+        _check(load().fvx_refine(self._h, int(factor), _stream(stream), ctypes.byref(h)))
+        return Grid(h)
+
 
 class KernelMap:
     """Per-offset (in, out) pair lists of a 3x3x3 kernel (library-owned)."""
 
-    def __init__(self, gin: Grid, gout: Grid, stride=1, ksize=3, stream=None):
+    def __init__(self, gin: Grid, gout: Grid, stride=1, ksize=3, stream=None, transposed=False):
+        """transposed: the map of the transposed convolution (output voxel q
+        paired with the input p where stride * ijk(p) + d == ijk(q))."""
         h = ctypes.c_void_p()
-        _check(load().fvx_kernel_map(gin._h, gout._h, int(ksize), int(stride), _stream(stream), ctypes.byref(h)))
+        f = load().fvx_kernel_map_transposed if transposed else load().fvx_kernel_map
+        _check(f(gin._h, gout._h, int(ksize), int(stride), _stream(stream), ctypes.byref(h)))
         self._h = h
-        self.gin, self.gout, self.stride = gin, gout, int(stride)
+        self.gin, self.gout, self.stride, self.transposed = gin, gout, int(stride), bool(transposed)
         ii, oo, mm = ctypes.c_void_p(), ctypes.c_void_p(), ctypes.c_void_p()
         nout = ctypes.c_int64()
         _check(_lib.fvx_kmap_view(h, None, ctypes.byref(ii), ctypes.byref(oo), ctypes.byref(mm), None,
@@ -280,6 +293,52 @@ def sparse_conv(gin: Grid, gout: Grid, kmap: KernelMap, feats, W, out=None, out_
     assert out.dtype == odt and out.is_contiguous() and tuple(out.shape) == (gout.n_active, cout)
     _check(load().fvx_sparse_conv(gin._h, gout._h, kmap._h, dt, _ptr(feats), cin, _ptr(W), cout, _ptr(out),
                                   _stream(stream)))
+    return out
+
+
+def sparse_conv_dgrad(gin: Grid, gout: Grid, kmap_t: KernelMap, dout, W, out=None, out_dtype=None, stream=None):
+    """Input gradient of sparse_conv(gin, gout, ...): dx [gin.n_active, cin].
+
+    kmap_t: KernelMap(gout, gin, stride, transposed=True).  dout [gout.n_active,
+    cout] and W [27, cin, cout] both float32 or both bfloat16 (float32 dx by
+    default, bfloat16 with out_dtype=torch.bfloat16)."""
+    import torch
+
+    assert dout.dtype == W.dtype and dout.is_cuda and W.is_cuda
+    if dout.dtype == torch.float32:
+        dt, odt = FVX_F32, torch.float32
+    else:
+        assert dout.dtype == torch.bfloat16
+        odt = out_dtype or (out.dtype if out is not None else torch.float32)
+        dt = {torch.float32: FVX_BF16, torch.bfloat16: FVX_BF16_OUT_BF16}[odt]
+    dout = dout.contiguous()
+    W = W.contiguous()
+    cin, cout = W.shape[1], W.shape[2]
+    assert W.shape[0] == 27 and dout.shape[1] == cout
+    if out is None:
+        out = torch.empty((gin.n_active, cin), dtype=odt, device=dout.device)
+    assert out.dtype == odt and out.is_contiguous() and tuple(out.shape) == (gin.n_active, cin)
+    _check(load().fvx_sparse_conv_dgrad(gin._h, gout._h, kmap_t._h, dt, _ptr(dout), cout, _ptr(W), cin, _ptr(out),
+                                        _stream(stream)))
+    return out
+
+
+def sparse_conv_wgrad(gin: Grid, gout: Grid, kmap: KernelMap, feats, dout, out=None, stream=None):
+    """Weight gradient of sparse_conv(gin, gout, kmap, feats, W): float32
+    [27, cin, cout].  feats and dout both float32 or both bfloat16."""
+    import torch
+
+    assert feats.dtype == dout.dtype and feats.is_cuda and dout.is_cuda
+    dt = FVX_F32 if feats.dtype == torch.float32 else FVX_BF16
+    assert dt == FVX_F32 or feats.dtype == torch.bfloat16
+    feats = feats.contiguous()
+    dout = dout.contiguous()
+    cin, cout = feats.shape[1], dout.shape[1]
+    if out is None:
+        out = torch.empty((27, cin, cout), dtype=torch.float32, device=feats.device)
+    assert out.dtype == torch.float32 and out.is_contiguous() and tuple(out.shape) == (27, cin, cout)
+    _check(load().fvx_sparse_conv_wgrad(gin._h, gout._h, kmap._h, dt, _ptr(feats), cin, _ptr(dout), cout, _ptr(out),
+                                        _stream(stream)))
     return out
 
 

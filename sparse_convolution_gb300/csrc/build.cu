@@ -635,6 +635,30 @@ __global__ void k_coarsen_coords(const int32_t* __restrict__ ijk, int64_t n, int
   }
 }
 
+// Children of every voxel for the refined grid: row t*f^3 + c holds
+// factor * ijk[t] + (c / f^2, (c / f) % f, c % f).  A coordinate that does not
+// fit int32 is recorded in the status word (the build reports it).
+__global__ void k_refine_coords(const int32_t* __restrict__ ijk, int64_t n, int factor, int32_t* __restrict__ out,
+                                uint32_t* status) {
+  const int64_t f3 = (int64_t)factor * factor * factor;
+  const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= n * f3) return;
+  const int64_t t = r / f3;
+  const int c = (int)(r - t * f3);
+  const int ch[3] = {c / (factor * factor), (c / factor) % factor, c % factor};
+#pragma unroll
+  for (int a = 0; a < 3; ++a) {
+    const int64_t v = (int64_t)factor * ijk[3 * t + a] + ch[a];
+    if (v < INT32_MIN || v > INT32_MAX) report_device_error(status, DEV_CHECK);
+    out[3 * r + a] = (int32_t)v;
+  }
+}
+
+__global__ void k_scale_offsets(const int64_t* __restrict__ in, int n, int64_t f, int64_t* __restrict__ out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) out[i] = in[i] * f;
+}
+
 int bits_for(uint64_t maxval) {  // bits needed to represent 0..maxval
   int b = 0;
   while (b < 64 && (maxval >> b) != 0) ++b;
@@ -1022,6 +1046,45 @@ fvx_status fvx_coarsen(fvx_grid g, int32_t stride, fvx_stream stream, fvx_grid* 
   }
   fvx_grid_s* r = nullptr;
   FVX_TRY(build_grid_device(c, U, g->voxel_batch_offsets, g->B, s, &r));
+  *out = r;
+  return FVX_OK;
+}
+
+fvx_status fvx_refine(fvx_grid g, int32_t factor, fvx_stream stream, fvx_grid* out) {
+  if (!g || !out || factor < 1) {
+    set_error("fvx_refine: bad argument (factor must be >= 1)");
+    return FVX_ERR_INVALID_ARG;
+  }
+  *out = nullptr;
+  const int64_t U = g->n_active, f3 = (int64_t)factor * factor * factor;
+  if (factor > 1024 || U * f3 > (int64_t)INT32_MAX - 1) {
+    set_error("fvx_refine: %lld voxels x %lld children exceed the row limit", (long long)U, (long long)f3);
+    return FVX_ERR_RANGE;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  uint32_t* status = device_status_word();
+  if (!status) {
+    set_error("fvx_refine: device status word unavailable");
+    return FVX_ERR_CUDA;
+  }
+  Scratch scr(s);
+  int32_t* c = scr.get<int32_t>((size_t)(3 * U * f3 + 3));
+  int64_t* offs = scr.get<int64_t>((size_t)g->B + 1);
+  if (!c || !offs) return FVX_ERR_ALLOC;
+  if (U > 0) {
+    {
+      LaunchScope ls("refine_coords", s);
+      k_refine_coords<<<grid_for(U * f3, kThreads), kThreads, 0, s>>>(g->ijk, U, factor, c, status);
+    }
+    FVX_TRY(check_launch("refine_coords"));
+  }
+  {
+    LaunchScope ls("refine_offsets", s);
+    k_scale_offsets<<<grid_for(g->B + 1, kThreads), kThreads, 0, s>>>(g->voxel_batch_offsets, g->B + 1, f3, offs);
+  }
+  FVX_TRY(check_launch("refine_offsets"));
+  fvx_grid_s* r = nullptr;
+  FVX_TRY(build_grid_device(c, U * f3, offs, g->B, s, &r));
   *out = r;
   return FVX_OK;
 }

@@ -1282,9 +1282,76 @@ __global__ void __launch_bounds__(kLeafThreads, G8 == 1 ? 2 : 1) k_conv_leaf(con
   }
 }
 
+// ============================================================== weight gradient
+// dW[s][ci][co] = sum over the pairs (p, q) of list s of x[p][ci] * dy[q][co]
+// (fp32 accumulation).  Blocks stride over chunks of the pair array (a chunk
+// may span several lists; the list bounds come from the map's device
+// offsets); a block owns a 32 x 32 tile of (ci, co), stages 32 pairs' input
+// and gradient channels in shared memory at a time, and adds each
+// (chunk, list) partial to dW with one atomic per entry.
+constexpr int kWgChunk = 32768;  // pairs per block step
+constexpr int kWgTile = 32;      // channels per tile side
+
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T>
+__global__ void __launch_bounds__(256) k_conv_wgrad(const T* __restrict__ x, const T* __restrict__ dy,
+                                                    const int32_t* __restrict__ in_idx,
+                                                    const int32_t* __restrict__ out_idx,
+                                                    const uint32_t* __restrict__ dtot, int cin, int cout,
+                                                    float* __restrict__ dW) {
+  __shared__ float sx[kWgTile][kWgTile + 1], sg[kWgTile][kWgTile + 1];
+  __shared__ uint32_t off[28];
+  const int tid = threadIdx.x;
+  if (tid < 28) off[tid] = __ldg(dtot + tid);
+  __syncthreads();
+  const uint32_t P = off[27];
+  const int tiles_co = (cout + kWgTile - 1) / kWgTile;
+  const int ci0 = (int)(blockIdx.y / tiles_co) * kWgTile, co0 = (int)(blockIdx.y % tiles_co) * kWgTile;
+  const int ci_l = tid >> 3, co_l = (tid & 7) * 4;  // this thread's entries: (ci_l, co_l .. co_l + 3)
+  const int lp = tid >> 3, lc = (tid & 7) * 4;       // staging: pair lp, channels lc .. lc + 3
+  const int64_t nchunks = ((int64_t)P + kWgChunk - 1) / kWgChunk;
+  for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
+    const uint32_t lo = (uint32_t)(c * kWgChunk), hi = min(P, lo + (uint32_t)kWgChunk);
+    for (int sl = 0; sl < 27; ++sl) {
+      const uint32_t a0 = max(lo, off[sl]), a1 = min(hi, off[sl + 1]);
+      if (a0 >= a1) continue;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      for (uint32_t e0 = a0; e0 < a1; e0 += kWgTile) {
+        const uint32_t e = e0 + (uint32_t)lp;
+        const bool ok = e < a1;
+        const int64_t p = ok ? __ldg(in_idx + e) : 0, q = ok ? __ldg(out_idx + e) : 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int ci = ci0 + lc + k, co = co0 + lc + k;
+          sx[lp][lc + k] = (ok && ci < cin) ? to_f32(x[p * cin + ci]) : 0.f;
+          sg[lp][lc + k] = (ok && co < cout) ? to_f32(dy[q * cout + co]) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int j = 0; j < kWgTile; ++j) {
+          const float av = sx[j][ci_l];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) acc[k] = fmaf(av, sg[j][co_l + k], acc[k]);
+        }
+        __syncthreads();
+      }
+      const int ci = ci0 + ci_l;
+      if (ci < cin) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int co = co0 + co_l + k;
+          if (co < cout) atomicAdd(dW + ((size_t)sl * cin + ci) * cout + co, acc[k]);
+        }
+      }
+    }
+  }
+}
+
 // W [27][cin][cout] -> Wt [27][cout][cin] (bf16), the K-major B operand.
-__global__ void k_transpose_w(const __nv_bfloat16* __restrict__ W, int cin, int cout,
-                              __nv_bfloat16* __restrict__ wt) {
+template <typename T>
+__global__ void k_transpose_w(const T* __restrict__ W, int cin, int cout, T* __restrict__ wt) {
   const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t per = (int64_t)cin * cout;
   if (e >= 27 * per) return;
@@ -1533,7 +1600,7 @@ extern "C" fvx_status fvx_sparse_conv(fvx_grid gin, fvx_grid gout, fvx_kmap m, f
   {
     LaunchScope ls("conv_transpose_w", s);
     const int64_t n = 27 * cin * cout;
-    k_transpose_w<<<(unsigned)((n + 255) / 256), 256, 0, s>>>((const __nv_bfloat16*)W, (int)cin, (int)cout, wt);
+    k_transpose_w<__nv_bfloat16><<<(unsigned)((n + 255) / 256), 256, 0, s>>>((const __nv_bfloat16*)W, (int)cin, (int)cout, wt);
   }
   FVX_TRY(check_launch("conv_transpose_w"));
   return launch_conv_bf16("fvx_sparse_conv", gin, m, dt, feats, cin, cout, out, wt, status, s);
@@ -1629,10 +1696,117 @@ extern "C" fvx_status fvx_sparse_conv_noalloc(fvx_grid gin, fvx_grid gout, fvx_k
   {
     LaunchScope ls("conv_transpose_w", s);
     const int64_t n = 27 * cin * cout;
-    k_transpose_w<<<(unsigned)((n + 255) / 256), 256, 0, s>>>((const __nv_bfloat16*)W, (int)cin, (int)cout, wt);
+    k_transpose_w<__nv_bfloat16><<<(unsigned)((n + 255) / 256), 256, 0, s>>>((const __nv_bfloat16*)W, (int)cin, (int)cout, wt);
   }
   FVX_TRY(check_launch("conv_transpose_w"));
   return launch_conv_bf16("fvx_sparse_conv_noalloc", gin, m, dt, feats, cin, cout, out, wt, status, s);
+}
+
+extern "C" fvx_status fvx_sparse_conv_wgrad(fvx_grid gin, fvx_grid gout, fvx_kmap m, fvx_dtype dt,
+                                            const void* feats, int64_t cin, const void* dout, int64_t cout, float* dW,
+                                            fvx_stream stream) {
+  if (!gin || !gout || !m || !dW || (gin->n_active > 0 && !feats) || (gout->n_active > 0 && !dout)) {
+    set_error("fvx_sparse_conv_wgrad: NULL argument");
+    return FVX_ERR_INVALID_ARG;
+  }
+  if (m->gin != gin || m->gout != gout) {
+    set_error("fvx_sparse_conv_wgrad: kernel map was built for other grids");
+    return FVX_ERR_INVALID_ARG;
+  }
+  if (cin < 1 || cout < 1 || cin > 65536 || cout > 65536) {
+    set_error("fvx_sparse_conv_wgrad: need 1 <= cin, cout <= 65536 (got %lld, %lld)", (long long)cin,
+              (long long)cout);
+    return FVX_ERR_INVALID_ARG;
+  }
+  if (dt != FVX_F32 && dt != FVX_BF16) {
+    set_error("fvx_sparse_conv_wgrad: dtype must be FVX_F32 or FVX_BF16 (got %d)", (int)dt);
+    return FVX_ERR_INVALID_ARG;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  FVX_CUDA(cudaMemsetAsync(dW, 0, sizeof(float) * 27 * (size_t)cin * (size_t)cout, s));
+  if (m->pair_capacity == 0) return FVX_OK;
+  int dev = 0, sms = 0;
+  FVX_CUDA(cudaGetDevice(&dev));
+  FVX_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  const int64_t tiles = ((cin + kWgTile - 1) / kWgTile) * ((cout + kWgTile - 1) / kWgTile);
+  const int64_t chunks = (m->pair_capacity + kWgChunk - 1) / kWgChunk;
+  const unsigned gx = (unsigned)std::max<int64_t>(1, std::min<int64_t>(chunks, (int64_t)sms * 8 / std::max<int64_t>(1, std::min<int64_t>(tiles, 8))));
+  if (tiles > 65535) {
+    set_error("fvx_sparse_conv_wgrad: %lld channel tiles exceed the grid limit", (long long)tiles);
+    return FVX_ERR_INVALID_ARG;
+  }
+  const dim3 grid(gx, (unsigned)tiles);
+  {
+    LaunchScope ls("conv_wgrad", s);
+    if (dt == FVX_F32)
+      k_conv_wgrad<float><<<grid, 256, 0, s>>>((const float*)feats, (const float*)dout, m->in_idx, m->out_idx,
+                                               m->dtot, (int)cin, (int)cout, dW);
+    else
+      k_conv_wgrad<__nv_bfloat16><<<grid, 256, 0, s>>>((const __nv_bfloat16*)feats, (const __nv_bfloat16*)dout,
+                                                       m->in_idx, m->out_idx, m->dtot, (int)cin, (int)cout, dW);
+  }
+  return check_launch("conv_wgrad");
+}
+
+// Input gradient of y = conv(x, W): dx[p] = sum over the pairs (p, q) of list
+// s of dy[q] W[s]^T, i.e. the convolution of dy over the transposed map with
+// the per-offset transposed weights.  The bf16 kernels take their B operand
+// as [27][n][k] with k contiguous; for this product that is W itself.
+extern "C" fvx_status fvx_sparse_conv_dgrad(fvx_grid gin, fvx_grid gout, fvx_kmap mt, fvx_dtype dt,
+                                            const void* dout, int64_t cout, const void* W, int64_t cin, void* dx,
+                                            fvx_stream stream) {
+  if (!gin || !gout || !mt || !W || !dx || (gout->n_active > 0 && !dout)) {
+    set_error("fvx_sparse_conv_dgrad: NULL argument");
+    return FVX_ERR_INVALID_ARG;
+  }
+  if (!mt->transposed || mt->gin != gout || mt->gout != gin) {
+    set_error("fvx_sparse_conv_dgrad: needs the transposed kernel map built for (gout, gin)");
+    return FVX_ERR_INVALID_ARG;
+  }
+  if (cin < 1 || cout < 1) {
+    set_error("fvx_sparse_conv_dgrad: cin and cout must be >= 1");
+    return FVX_ERR_INVALID_ARG;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  if (gin->n_active == 0) return FVX_OK;
+  if (dt == FVX_F32) {
+    Scratch scr(s);
+    float* wt = scr.get<float>((size_t)(27 * cin * cout));
+    if (!wt) return FVX_ERR_ALLOC;
+    {
+      LaunchScope ls("conv_transpose_w", s);
+      const int64_t n = 27 * cin * cout;
+      k_transpose_w<float><<<(unsigned)((n + 255) / 256), 256, 0, s>>>((const float*)W, (int)cin, (int)cout, wt);
+    }
+    FVX_TRY(check_launch("conv_transpose_w"));
+    {
+      LaunchScope ls("conv_f32", s);
+      k_conv_f32<<<(unsigned)mt->n_tiles, kRows, 0, s>>>((const float*)dout, wt, mt->out_mask, mt->in_idx,
+                                                          mt->tile_start, mt->n_tiles, mt->n_out, (int)cout,
+                                                          (int)cin, (float*)dx);
+    }
+    return check_launch("conv_f32");
+  }
+  if (dt != FVX_BF16 && dt != FVX_BF16_OUT_BF16) {
+    set_error("fvx_sparse_conv_dgrad: unknown dtype %d", (int)dt);
+    return FVX_ERR_INVALID_ARG;
+  }
+  if (cout % 8 != 0 || cin % 16 != 0 || cout > 512 || cin > 256) {
+    set_error("fvx_sparse_conv_dgrad: bf16 needs cout %% 8 == 0 (<= 512) and cin %% 16 == 0 (<= 256); got %lld, %lld",
+              (long long)cout, (long long)cin);
+    return FVX_ERR_INVALID_ARG;
+  }
+  if (((uintptr_t)dout | (uintptr_t)dx | (uintptr_t)W) & 15u) {
+    set_error("fvx_sparse_conv_dgrad: dout, W and dx must be 16-byte aligned");
+    return FVX_ERR_INVALID_ARG;
+  }
+  uint32_t* status = device_status_word();
+  if (!status) {
+    set_error("fvx_sparse_conv_dgrad: device status word unavailable");
+    return FVX_ERR_CUDA;
+  }
+  return launch_conv_bf16("fvx_sparse_conv_dgrad", gout, mt, dt, dout, cout, cin, dx, (const __nv_bfloat16*)W, status,
+                          s);
 }
 
 extern "C" fvx_status fvx_set_conv_algo(fvx_conv_algo algo) {

@@ -132,6 +132,7 @@ struct fvx_grid_s {
 
 struct fvx_kmap_s {
   int32_t stride = 1;
+  bool transposed = false;  // map of the transposed convolution (see fvx_kernel_map_transposed)
   int64_t n_out = 0, n_pairs = 0;
   int64_t offsets_host[28] = {0};
   // the 28 list offsets on the device; copied to offsets_host / n_pairs on
@@ -221,6 +222,14 @@ __device__ __forceinline__ int find_leaf(const GridDev& g, int b, int i, int j, 
   if (w < 0) return -1;
   const int nl = ((((i >> 3) & 15) << 8) | (((j >> 3) & 15) << 4) | ((k >> 3) & 15));
   return child_index(g.lower_mask + (size_t)w * 64, g.lower_prefix + (size_t)w * 64, __ldg(g.lower_first + w), nl);
+}
+
+// find_leaf for a leaf origin computed in 64 bits: -1 when it lies outside the
+// int32 coordinate range (no grid holds such a leaf).
+__device__ __forceinline__ int find_leaf_wide(const GridDev& g, int b, long long i, long long j, long long k) {
+  const long long lo = -2147483648ll, hi = 2147483647ll;
+  if (i < lo || i > hi || j < lo || j > hi || k < lo || k > hi) return -1;
+  return find_leaf(g, b, (int)i, (int)j, (int)k);
 }
 
 // Index of voxel n (0..511) inside leaf record rec, or -1: two branches (bit

@@ -38,19 +38,33 @@ struct KmSmem {
   uint32_t omask[512];
   int nvox;
   uint32_t qfirst;
+  int toff[3];  // transposed map: origin / stride minus the input leaf base (0 or 4)
 };
 
+// Loads the output leaf's voxels and the 27 input leaves around a base point:
+// the input point of the output leaf's origin (stride * origin), or, for the
+// transposed map, the origin of the input leaf holding origin / stride.  Leaf
+// origins are computed in 64 bits so that none wraps at the int32 edges.
 __device__ __forceinline__ void km_prologue(KmSmem& sm, const GridDev& gin, const int32_t* __restrict__ out_origin,
                                             const int32_t* __restrict__ out_batch,
-                                            const uint64_t* __restrict__ out_rec, int stride, int lo) {
+                                            const uint64_t* __restrict__ out_rec, int stride, int transposed,
+                                            int lo) {
   const int tid = threadIdx.x;
+  if (tid < 3) {
+    const int o = out_origin[3 * lo + tid];
+    const int q = stride == 2 ? (o >> 1) : o;
+    sm.toff[tid] = transposed ? q - (q & ~7) : 0;
+  }
   if (tid < 27) {
     const int a = tid / 9, b = (tid / 3) % 3, c = tid % 3;
     const int bt = out_batch[lo];
-    const int oi = stride * out_origin[3 * lo] - 8 + 8 * a;
-    const int oj = stride * out_origin[3 * lo + 1] - 8 + 8 * b;
-    const int ok = stride * out_origin[3 * lo + 2] - 8 + 8 * c;
-    const int l = find_leaf(gin, bt, oi, oj, ok);
+    long long bs[3];
+#pragma unroll
+    for (int e = 0; e < 3; ++e) {
+      const int o = out_origin[3 * lo + e];
+      bs[e] = transposed ? (long long)((stride == 2 ? (o >> 1) : o) & ~7) : (long long)stride * o;
+    }
+    const int l = find_leaf_wide(gin, bt, bs[0] - 8 + 8 * a, bs[1] - 8 + 8 * b, bs[2] - 8 + 8 * c);
     sm.nleaf[tid] = l;
     if (l >= 0) {
       const unsigned long long* r = reinterpret_cast<const unsigned long long*>(gin.leaf_rec) + (size_t)l * 10;
@@ -97,21 +111,43 @@ __device__ __forceinline__ int km_neighbour(const KmSmem& sm, int n, int stride,
   return (int)(sm.first[slot] + pre + (uint32_t)__popcll(m & ((1ull << bit) - 1ull)));
 }
 
+// Transposed map: input index of the voxel q with stride * ijk(q) + d = ijk of
+// output voxel n, or -1 (also when the division is not exact).  Works on the
+// local coordinate (n's position in its leaf minus d, in [-1, 8]); the leaf
+// origin is a multiple of 8, so exactness and the quotient follow from it.
+__device__ __forceinline__ int km_neighbour_t(const KmSmem& sm, int n, int stride, int di, int dj, int dk) {
+  const int li = (n >> 6) - di, lj = ((n >> 3) & 7) - dj, lk = (n & 7) - dk;
+  const int sh = stride == 2 ? 1 : 0;
+  if (sh && ((li | lj | lk) & 1)) return -1;
+  // stride 1: r in [7, 16]; stride 2: li >> 1 in [0, 4], toff in {0, 4}, r in [8, 16]
+  const int ri = sm.toff[0] + (li >> sh) + 8, rj = sm.toff[1] + (lj >> sh) + 8, rk = sm.toff[2] + (lk >> sh) + 8;
+  const int slot = (ri >> 3) * 9 + (rj >> 3) * 3 + (rk >> 3);
+  if (sm.nleaf[slot] < 0) return -1;
+  const int nn = ((ri & 7) << 6) | ((rj & 7) << 3) | (rk & 7);
+  const int w = nn >> 6, bit = nn & 63;
+  const unsigned long long m = sm.mask[slot][w];
+  if (!((m >> bit) & 1ull)) return -1;
+  const uint32_t pre = w ? (uint32_t)((sm.pre9[slot] >> (9 * (w - 1))) & 511ull) : 0u;
+  return (int)(sm.first[slot] + pre + (uint32_t)__popcll(m & ((1ull << bit) - 1ull)));
+}
+
 __global__ void __launch_bounds__(kKmThreads) k_kmap_count(GridDev gin, const int32_t* __restrict__ out_origin,
                                                            const int32_t* __restrict__ out_batch,
                                                            const uint64_t* __restrict__ out_rec, int64_t n_out_leaf,
-                                                           int stride, uint32_t* __restrict__ counts,
+                                                           int stride, int transposed, uint32_t* __restrict__ counts,
                                                            uint32_t* __restrict__ out_mask) {
   __shared__ KmSmem sm;
   const int lo = blockIdx.x;
-  km_prologue(sm, gin, out_origin, out_batch, out_rec, stride, lo);
+  km_prologue(sm, gin, out_origin, out_batch, out_rec, stride, transposed, lo);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int s = warp; s < 27; s += kKmWarps) {
     const int di = s / 9 - 1, dj = (s / 3) % 3 - 1, dk = s % 3 - 1;
     uint32_t cnt = 0;
     for (int c0 = 0; c0 < sm.nvox; c0 += 32) {
       const int idx = c0 + lane;
-      const int p = (idx < sm.nvox) ? km_neighbour(sm, sm.vox[idx], stride, di, dj, dk) : -1;
+      const int p = (idx < sm.nvox) ? (transposed ? km_neighbour_t(sm, sm.vox[idx], stride, di, dj, dk)
+                                                  : km_neighbour(sm, sm.vox[idx], stride, di, dj, dk))
+                                    : -1;
       cnt += __popc(__ballot_sync(0xffffffffu, p >= 0));
       if (p >= 0) atomicOr(&sm.omask[idx], 1u << s);
     }
@@ -124,12 +160,13 @@ __global__ void __launch_bounds__(kKmThreads) k_kmap_count(GridDev gin, const in
 __global__ void __launch_bounds__(kKmThreads) k_kmap_write(GridDev gin, const int32_t* __restrict__ out_origin,
                                                            const int32_t* __restrict__ out_batch,
                                                            const uint64_t* __restrict__ out_rec, int64_t n_out_leaf,
-                                                           int stride, const uint32_t* __restrict__ starts,
+                                                           int stride, int transposed,
+                                                           const uint32_t* __restrict__ starts,
                                                            int32_t* __restrict__ in_idx,
                                                            int32_t* __restrict__ out_idx) {
   __shared__ KmSmem sm;
   const int lo = blockIdx.x;
-  km_prologue(sm, gin, out_origin, out_batch, out_rec, stride, lo);
+  km_prologue(sm, gin, out_origin, out_batch, out_rec, stride, transposed, lo);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t lt = lanemask_lt();
   for (int s = warp; s < 27; s += kKmWarps) {
@@ -137,7 +174,9 @@ __global__ void __launch_bounds__(kKmThreads) k_kmap_write(GridDev gin, const in
     uint32_t pos = starts[(int64_t)s * n_out_leaf + lo];
     for (int c0 = 0; c0 < sm.nvox; c0 += 32) {
       const int idx = c0 + lane;
-      const int p = (idx < sm.nvox) ? km_neighbour(sm, sm.vox[idx], stride, di, dj, dk) : -1;
+      const int p = (idx < sm.nvox) ? (transposed ? km_neighbour_t(sm, sm.vox[idx], stride, di, dj, dk)
+                                                  : km_neighbour(sm, sm.vox[idx], stride, di, dj, dk))
+                                    : -1;
       const uint32_t bal = __ballot_sync(0xffffffffu, p >= 0);
       if (p >= 0) {
         const uint32_t e = pos + __popc(bal & lt);
@@ -200,8 +239,8 @@ __device__ __forceinline__ void km1_load(Km1Smem& sm, const GridDev& gin, const 
       l = nbr_in[(int64_t)lo * 27 + tid];
     } else {
       const int a = tid / 9, b = (tid / 3) % 3, c = tid % 3;
-      l = find_leaf(gin, out_batch[lo], out_origin[3 * lo] - 8 + 8 * a, out_origin[3 * lo + 1] - 8 + 8 * b,
-                    out_origin[3 * lo + 2] - 8 + 8 * c);
+      l = find_leaf_wide(gin, out_batch[lo], (long long)out_origin[3 * lo] - 8 + 8 * a,
+                         (long long)out_origin[3 * lo + 1] - 8 + 8 * b, (long long)out_origin[3 * lo + 2] - 8 + 8 * c);
       if (nbr_out) nbr_out[(int64_t)lo * 27 + tid] = l;
     }
     const unsigned long long* r = reinterpret_cast<const unsigned long long*>(gin.leaf_rec) + (size_t)(l < 0 ? 0 : l) * 10;
@@ -383,19 +422,20 @@ fvx_status fvx::kmap_read_totals(fvx_kmap_s* m, const char* who) {
   return FVX_OK;
 }
 
-extern "C" fvx_status fvx_kernel_map(fvx_grid gin, fvx_grid gout, int32_t ksize, int32_t stride, fvx_stream stream,
-                                     fvx_kmap* out) {
+namespace {
+fvx_status kernel_map_impl(const char* who, fvx_grid gin, fvx_grid gout, int32_t ksize, int32_t stride,
+                           bool transposed, fvx_stream stream, fvx_kmap* out) {
   if (!gin || !gout || !out) {
-    set_error("fvx_kernel_map: NULL argument");
+    set_error("%s: NULL argument", who);
     return FVX_ERR_INVALID_ARG;
   }
   *out = nullptr;
   if (ksize != 3 || (stride != 1 && stride != 2)) {
-    set_error("fvx_kernel_map: need ksize == 3 and stride 1 or 2 (got %d, %d)", ksize, stride);
+    set_error("%s: need ksize == 3 and stride 1 or 2 (got %d, %d)", who, ksize, stride);
     return FVX_ERR_INVALID_ARG;
   }
   if (gin->B != gout->B) {
-    set_error("fvx_kernel_map: batch sizes differ (%d vs %d)", gin->B, gout->B);
+    set_error("%s: batch sizes differ (%d vs %d)", who, gin->B, gout->B);
     return FVX_ERR_INVALID_ARG;
   }
   cudaStream_t s = (cudaStream_t)stream;
@@ -408,6 +448,7 @@ extern "C" fvx_status fvx_kernel_map(fvx_grid gin, fvx_grid gout, int32_t ksize,
     }
   } guard{&m};
   m->stride = stride;
+  m->transposed = transposed;
   m->n_out = gout->n_active;
   m->stream = s;
   m->gin = gin;
@@ -422,7 +463,8 @@ extern "C" fvx_status fvx_kernel_map(fvx_grid gin, fvx_grid gout, int32_t ksize,
   // writes, which the leaf-densified convolution reads too)
   const size_t o_mask = 0, o_tot = align_up(4 * (size_t)Nout), o_tile = o_tot + align_up(4 * 32);
   const size_t o_nbr = o_tile + align_up(4 * (size_t)(27 * m->n_tiles + 1));
-  const size_t bytes1 = o_nbr + (stride == 1 ? align_up(4 * (size_t)(27 * Lo + 1)) : 0);
+  const bool bitpar = stride == 1 && !transposed;  // bit-parallel stride-1 kernels
+  const size_t bytes1 = o_nbr + (bitpar ? align_up(4 * (size_t)(27 * Lo + 1)) : 0);
   m->block = dalloc(bytes1, s);
   if (!m->block) return FVX_ERR_ALLOC;
   m->out_mask = (uint32_t*)((char*)m->block + o_mask);
@@ -444,18 +486,18 @@ extern "C" fvx_status fvx_kernel_map(fvx_grid gin, fvx_grid gout, int32_t ksize,
 
   const GridDev gd = grid_dev(gin);
   int32_t* nbr = nullptr;  // stride 1: input-leaf slot table written by the count pass
-  if (stride == 1) {
+  if (bitpar) {
     nbr = (int32_t*)((char*)m->block + o_nbr);
     m->leaf_nbr = nbr;
   }
   if (Lo > 0) {
     LaunchScope ls("kmap_count", s);
-    if (stride == 1)
+    if (bitpar)
       k_kmap1_count<<<(unsigned)Lo, kKmThreads, 0, s>>>(gd, gout->leaf_origin, gout->leaf_batch, gout->leaf_rec, Lo,
                                                         counts, m->out_mask, nbr);
     else
       k_kmap_count<<<(unsigned)Lo, kKmThreads, 0, s>>>(gd, gout->leaf_origin, gout->leaf_batch, gout->leaf_rec, Lo,
-                                                       stride, counts, m->out_mask);
+                                                       stride, transposed ? 1 : 0, counts, m->out_mask);
   }
   FVX_TRY(check_launch("kmap_count"));
   FVX_TRY(scan_exclusive_u32(counts, counts, 27 * Lo, dtot + 28, s, scr));
@@ -465,10 +507,10 @@ extern "C" fvx_status fvx_kernel_map(fvx_grid gin, fvx_grid gout, int32_t ksize,
   }
   FVX_TRY(check_launch("kmap_list_offsets"));
   if (!by_capacity) {
-    FVX_TRY(kmap_read_totals(m, "fvx_kernel_map"));
+    FVX_TRY(kmap_read_totals(m, who));
     const int64_t P = m->n_pairs;
     if (P >= (int64_t)INT32_MAX) {
-      set_error("fvx_kernel_map: %lld pairs exceed the int32 pair index range", (long long)P);
+      set_error("%s: %lld pairs exceed the int32 pair index range", who, (long long)P);
       return FVX_ERR_RANGE;
     }
     m->pair_capacity = P;
@@ -479,12 +521,12 @@ extern "C" fvx_status fvx_kernel_map(fvx_grid gin, fvx_grid gout, int32_t ksize,
   }
   if (Lo > 0 && m->pair_capacity > 0) {
     LaunchScope ls("kmap_write", s);
-    if (stride == 1)
+    if (bitpar)
       k_kmap1_write<<<(unsigned)Lo, kKmThreads, 0, s>>>(gd, gout->leaf_origin, gout->leaf_batch, gout->leaf_rec, Lo,
                                                         counts, nbr, m->in_idx, m->out_idx);
     else
       k_kmap_write<<<(unsigned)Lo, kKmThreads, 0, s>>>(gd, gout->leaf_origin, gout->leaf_batch, gout->leaf_rec, Lo,
-                                                       stride, counts, m->in_idx, m->out_idx);
+                                                       stride, transposed ? 1 : 0, counts, m->in_idx, m->out_idx);
   }
   FVX_TRY(check_launch("kmap_write"));
   // conv tiling: where each tile's pairs start in every list
@@ -500,4 +542,15 @@ extern "C" fvx_status fvx_kernel_map(fvx_grid gin, fvx_grid gout, int32_t ksize,
   *out = m;
   m = nullptr;
   return FVX_OK;
+}
+}  // namespace
+
+extern "C" fvx_status fvx_kernel_map(fvx_grid gin, fvx_grid gout, int32_t ksize, int32_t stride, fvx_stream stream,
+                                     fvx_kmap* out) {
+  return kernel_map_impl("fvx_kernel_map", gin, gout, ksize, stride, false, stream, out);
+}
+
+extern "C" fvx_status fvx_kernel_map_transposed(fvx_grid gin, fvx_grid gout, int32_t ksize, int32_t stride,
+                                                fvx_stream stream, fvx_kmap* out) {
+  return kernel_map_impl("fvx_kernel_map_transposed", gin, gout, ksize, stride, true, stream, out);
 }

@@ -232,3 +232,22 @@ def test_kmap_exact_size_path(cuda_device):
                        timeout=600)
     assert r.returncode == 0, r.stdout + r.stderr
     assert "exact path ok" in r.stdout
+
+
+@pytest.mark.parametrize("stride", [1, 2])
+@pytest.mark.parametrize("transposed", [False, True])
+def test_kmap_int32_edges(cuda_device, stride, transposed):
+    """Voxels at both ends of the int32 range in one batch: a neighbour past an
+    end is no voxel, so the two ends never pair (no wrap-around)."""
+    import sparse_convolution_gb300 as fvx
+
+    M = 2 ** 31 - 1
+    c = np.array([[M, 0, 0], [-M - 1, 0, 0], [M - 1, 0, 0], [M, M, M], [-M - 1, -M - 1, -M - 1],
+                  [-M - 1, M, 0], [M, -M - 1, 5], [M - 8, 3, 3], [-M + 7, 3, 3]], np.int32)
+    g, og = G.gpu_grid(c, [0, len(c)]), oracle.Grid.build(c, [0, len(c)])
+    gc, ogc = (g, og) if stride == 1 else (g.coarsen(2), og.coarsen(2))
+    if transposed:
+        km, okm = fvx.KernelMap(gc, g, stride, transposed=True), oracle.KernelMap(ogc, og, stride, transposed=True)
+    else:
+        km, okm = fvx.KernelMap(g, gc, stride), oracle.KernelMap(og, ogc, stride)
+    G.assert_kmap_equal(km, okm)
