@@ -428,7 +428,7 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tc(const __grid_c
   // ---- setup: barriers (thread 0), TMEM for two accumulators (MMA warp)
   if (tid == 0) {
     for (int i = 0; i < S; ++i) {
-      mbar_init(smem_u32(&h.full[i]), kProducers);
+      mbar_init(smem_u32(&h.full[i]), kProducerWarps);  // one arrival per producer warp
       mbar_init(smem_u32(&h.empty[i]), 1);
     }
     for (int r = 0; r < kInfoRing; ++r) {
@@ -554,10 +554,13 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tc(const __grid_c
       if (has_next) table_begin(h.tab[nb], t + G);
       // (b) prefetch the segment bounds of the tile after next
       load_segment(gts, ntiles, t + 2 * G, pt, sa, se);
-      // (c) gathers of this tile: 8 pieces (K = 64) per stage; this thread
-      // takes pieces 4*hf .. 4*hf+3 of its row
+      // (c) gathers of this tile: 8 pieces (K = 64) per stage.  Eight
+      // consecutive threads copy the eight 16-byte pieces of one row, so a
+      // warp instruction touches 4 rows (4 cache lines for cin >= 64) rather
+      // than 32; this thread takes piece pc of rows pt/8 + 32u.
       const int64_t kg_tile0 = kg;
       const int nst = (total + 7) >> 3;
+      const int pc = pt & 7, r0 = pt >> 3;
       for (int k = 0; k < nst; ++k, ++kg) {
         const int sb = ring_sb;
         if (kg >= S) mbar_wait(smem_u32(&h.empty[sb]), ring_ph ^ 1u, status);
@@ -566,48 +569,34 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tc(const __grid_c
           ring_ph ^= 1u;
         }
         const uint32_t sA = smem_u32(sbase + (size_t)sb * sbytes);
-        const int g0 = 8 * k + 4 * hf;
-        int slot = g0 / ppo, cb = g0 - slot * ppo;
-        int pr[4], cbv[4], sv[4];
+        const int g = 8 * k + pc;
+        const bool gok = g < total;
+        const int slot = gok ? g / ppo : 0;
+        const int64_t coff = gok ? (int64_t)(g - slot * ppo) * 8 : 0;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          pr[u] = -1;
-          sv[u] = -1;
-          cbv[u] = cb;
-          if (g0 + u < total) {
-            pr[u] = cur.rowp[slot][m];
-            sv[u] = cur.slot_s[slot];
-            if (++cb == ppo) {
-              cb = 0;
-              ++slot;
-            }
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int pc = 4 * hf + u;
-          const bool ok = pr[u] >= 0;
-          cp_async16(sA + (m >> 3) * 1024 + (m & 7) * 128 + ((pc ^ (m & 7)) << 4),
-                     ok ? (const void*)(gx + (int64_t)pr[u] * cin + cbv[u] * 8) : (const void*)gx, ok ? 16u : 0u);
+          const int r = r0 + 32 * u;
+          const int p = gok ? cur.rowp[slot][r] : -1;
+          const bool ok = p >= 0;
+          cp_async16(sA + (r >> 3) * 1024 + (r & 7) * 128 + ((pc ^ (r & 7)) << 4),
+                     ok ? (const void*)(gx + (int64_t)p * cin + coff) : (const void*)gx, ok ? 16u : 0u);
         }
         if (!wres) {
           const uint32_t sB = sA + kATileBytes;
-          for (int n = m; n < cout; n += kRows) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int pc = 4 * hf + u;
-              const bool ok = sv[u] >= 0;
-              cp_async16(sB + (n >> 3) * 1024 + (n & 7) * 128 + ((pc ^ (n & 7)) << 4),
-                         ok ? (const void*)(gwt + ((int64_t)sv[u] * cout + n) * cin + cbv[u] * 8) : (const void*)gwt,
-                         ok ? 16u : 0u);
-            }
+          const int sw = gok ? cur.slot_s[slot] : -1;
+          for (int n = r0; n < cout; n += 32) {
+            const bool ok = sw >= 0;
+            cp_async16(sB + (n >> 3) * 1024 + (n & 7) * 128 + ((pc ^ (n & 7)) << 4),
+                       ok ? (const void*)(gwt + ((int64_t)sw * cout + n) * cin + coff) : (const void*)gwt,
+                       ok ? 16u : 0u);
           }
         }
         cp_async_commit();
         if (kg - signaled >= L) {
           cp_async_wait_n(L);
           fence_proxy_async();
-          mbar_arrive(smem_u32(&h.full[sig_sb]));
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&h.full[sig_sb]));
           if (++sig_sb == S) sig_sb = 0;
           ++signaled;
         }
@@ -621,8 +610,9 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tc(const __grid_c
         if (j >= kInfoRing && signaled < kg_end[(j - kInfoRing) & (kInfoRing - 1)]) {
           cp_async_wait_n(0);
           fence_proxy_async();
+          __syncwarp();
           while (signaled < kg) {
-            mbar_arrive(smem_u32(&h.full[sig_sb]));
+            if (lane == 0) mbar_arrive(smem_u32(&h.full[sig_sb]));
             if (++sig_sb == S) sig_sb = 0;
             ++signaled;
           }
@@ -638,8 +628,9 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tc(const __grid_c
     }
     cp_async_wait_n(0);
     fence_proxy_async();
+    __syncwarp();
     while (signaled < kg) {
-      mbar_arrive(smem_u32(&h.full[sig_sb]));
+      if (lane == 0) mbar_arrive(smem_u32(&h.full[sig_sb]));
       if (++sig_sb == S) sig_sb = 0;
       ++signaled;
     }
@@ -916,12 +907,27 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tma(const __grid_
   } else if (warp == kMmaWarp) {
     // ---------------- MMA issue (one thread)
     if (lane == 0) {
+      // The issue loop is kept to a few instructions per MMA (one thread
+      // issues them all): descriptors of stage 0 and the per-K-step offsets
+      // (in the descriptors' 16-byte address units) are computed once, and a
+      // stage's descriptors are stage 0's plus its slot offset.
       const uint32_t idesc = idesc_bf16(kRows, a.cout);
       const uint32_t layout = (uint32_t)ta.layout, sbo = 8u * (uint32_t)rowb;
-      const int sbytes = a.stage_bytes, cout = a.cout;
+      const int cout = a.cout;
       uint32_t* const status = a.status;
+      const uint64_t adesc0 = sdesc_swz(smem_u32(sbase), layout, sbo);
+      const uint64_t bdesc0 = sdesc_swz(smem_u32(sbase) + kATileBytes, layout, sbo);
+      uint32_t aoff[4], boff[4];
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const int e = 16 * kk, j = e / chunk;
+        const uint32_t off = (uint32_t)((e - j * chunk) * 2);
+        aoff[kk] = ((uint32_t)(j * kRows * rowb) + off) >> 4;
+        boff[kk] = ((uint32_t)(j * cout * rowb) + off) >> 4;
+      }
+      const uint32_t sunits = (uint32_t)a.stage_bytes >> 4;
       int m_sb = 0;
-      uint32_t m_ph = 0;
+      uint32_t m_ph = 0, m_off = 0;  // ring slot, its parity, its offset in 16-byte units
       int i = 0;
       for (int64_t t = blockIdx.x; t < ntiles; t += G, ++i) {
         const int r = i & (kInfoRing - 1), b = i & 1;
@@ -931,23 +937,20 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tma(const __grid_
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)b * acc_cols;
         for (int k = 0; k < nst; ++k) {
-          const int sb = m_sb;
-          mbar_wait(smem_u32(&h.full[sb]), m_ph, status);
+          mbar_wait(smem_u32(&h.full[m_sb]), m_ph, status);
+          tc_fence_after();
+          const uint64_t ad = adesc0 + m_off, bd = bdesc0 + m_off;
+          umma_bf16(d, ad + aoff[0], bd + boff[0], idesc, k > 0 ? 1u : 0u);
+          umma_bf16(d, ad + aoff[1], bd + boff[1], idesc, 1u);
+          umma_bf16(d, ad + aoff[2], bd + boff[2], idesc, 1u);
+          umma_bf16(d, ad + aoff[3], bd + boff[3], idesc, 1u);
+          umma_commit(smem_u32(&h.empty[m_sb]));
+          m_off += sunits;
           if (++m_sb == S) {
             m_sb = 0;
             m_ph ^= 1u;
+            m_off = 0;
           }
-          tc_fence_after();
-          const uint32_t sA = smem_u32(sbase + (size_t)sb * sbytes);
-          const uint32_t sB = sA + kATileBytes;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const int e = 16 * kk, j = e / chunk;
-            const uint32_t off = (uint32_t)((e - j * chunk) * 2);
-            umma_bf16(d, sdesc_swz(sA + (uint32_t)(j * kRows * rowb) + off, layout, sbo),
-                      sdesc_swz(sB + (uint32_t)(j * cout * rowb) + off, layout, sbo), idesc, (k | kk) ? 1u : 0u);
-          }
-          umma_commit(smem_u32(&h.empty[sb]));
         }
         if (nst > 0) umma_commit(smem_u32(&h.acc_full[b]));
         else mbar_arrive(smem_u32(&h.acc_full[b]));
@@ -1180,8 +1183,30 @@ __global__ void __launch_bounds__(kLeafThreads, G8 == 1 ? 2 : 1) k_conv_leaf(con
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16(kRows, cout);
       const uint32_t wbase = smem_u32(wsm);
-      const int nkg = 27 * G8, npair = (nkg + 1) >> 1;
       const uint32_t wblk = (uint32_t)cout * 16u;
+      // Descriptors of every MMA for halo buffer 0 and tile 0, computed once
+      // and kept in registers (the loops over p are unrolled); buffer b and
+      // tile t add b * halo_bytes + t * 2560 bytes (two y-rows of 80 16-byte
+      // rows) to the start address, so the issue loop is an add per MMA.
+      constexpr int kNkg = 27 * G8, kNpair = (kNkg + 1) >> 1;
+      uint64_t adesc[kNpair];
+#pragma unroll
+      for (int p = 0; p < kNpair; ++p) {
+        uint32_t addr[2];
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          int kg = 2 * p + h2;
+          if (kg >= kNkg) kg = kNkg - 1;  // the zero weight block pairs with a repeat
+          const int c8 = kg / 27, s = kg - c8 * 27;
+          const int cx = s / 9, dy = (s / 3) % 3 - 1, dz = s % 3 - 1;
+          addr[h2] = smem_u32(halo0) + (uint32_t)(c8 * 3 + cx) * kLeafPlaneBytes +
+                     (uint32_t)(((dy + 1) * 80 + dz + 1) * 16);
+        }
+        adesc[p] = sdesc_plain(addr[0], addr[1] - addr[0], 160u);
+      }
+      const uint64_t bdesc0 = sdesc_plain(wbase, wblk, 128u);
+      const uint32_t bstep = (2u * wblk) >> 4;
+      const uint32_t hunits = (uint32_t)a.halo_bytes >> 4;
       int i = 0;
       for (int64_t L = blockIdx.x; L < nL; L += G, ++i) {
         const int b = i & 1;
@@ -1193,28 +1218,16 @@ __global__ void __launch_bounds__(kLeafThreads, G8 == 1 ? 2 : 1) k_conv_leaf(con
         mbar_wait(smem_u32(&bars.halo_full[b]), (uint32_t)((i >> 1) & 1), status);
         if (i >= 2) mbar_wait(smem_u32(&bars.acc_empty[b]), (uint32_t)(((i >> 1) - 1) & 1), status);
         tc_fence_after();
-        const uint32_t hbase = smem_u32(halo0) + (uint32_t)b * (uint32_t)a.halo_bytes;
         for (int t = 0; t < 4; ++t) {
           if (((occ >> (16 * t)) & 0xFFFFull) == 0ull) {
             mbar_arrive(smem_u32(&bars.acc_full[b][t]));  // nothing to write in this tile
             continue;
           }
           const uint32_t d = tmem + (uint32_t)(b * 4 + t) * tcs;
-          for (int p = 0; p < npair; ++p) {
-            uint32_t addr[2];
+          const uint64_t toff = (uint64_t)((uint32_t)b * hunits + (uint32_t)t * 160u);
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-              int kg = 2 * p + h2;
-              if (kg >= nkg) kg = nkg - 1;  // the zero weight block pairs with a repeat
-              const int c8 = kg / 27, s = kg - c8 * 27;
-              const int cx = s / 9, dy = (s / 3) % 3 - 1, dz = s % 3 - 1;
-              addr[h2] = hbase + (uint32_t)(c8 * 3 + cx) * kLeafPlaneBytes +
-                         (uint32_t)(((2 * t + dy + 1) * 80 + dz + 1) * 16);
-            }
-            const uint64_t ad = sdesc_plain(addr[0], addr[1] - addr[0], 160u);
-            const uint64_t bd = sdesc_plain(wbase + (uint32_t)(2 * p) * wblk, wblk, 128u);
-            umma_bf16(d, ad, bd, idesc, p ? 1u : 0u);
-          }
+          for (int p = 0; p < kNpair; ++p)
+            umma_bf16(d, adesc[p] + toff, bdesc0 + (uint64_t)(p * bstep), idesc, p ? 1u : 0u);
           umma_commit(smem_u32(&bars.acc_full[b][t]));  // tile t's accumulator is complete
         }
         umma_commit(smem_u32(&bars.halo_empty[b]));  // halo b may be refilled
