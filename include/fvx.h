@@ -209,8 +209,9 @@ fvx_status fvx_kernel_map_transposed(fvx_grid gin, fvx_grid gout, int32_t ksize,
  * out    device [gout.n_active, cout], row-major, caller-allocated, fully
  *        overwritten; bf16 for FVX_BF16_OUT_BF16, else fp32.
  * FVX_BF16 / FVX_BF16_OUT_BF16: tcgen05 tensor cores, fp32 accumulation in
- *           TMEM.  cin a multiple of 8 (<= 512), cout a multiple of 16
- *           (<= 256); feats and out 16-byte aligned.
+ *           TMEM.  cin and cout multiples of 8 (cin <= 512, cout <= 256; the
+ *           MMA's N is cout rounded up to 16, the extra columns are not
+ *           written); feats and out 16-byte aligned.
  * FVX_F32:  fp32 FFMA throughout (no TF32).  cin, cout >= 1.
  * m must have been built for (gin, gout).  Errors: FVX_ERR_INVALID_ARG. */
 fvx_status fvx_sparse_conv(fvx_grid gin, fvx_grid gout, fvx_kmap m, fvx_dtype dt, const void* feats, int64_t cin,
@@ -253,8 +254,9 @@ fvx_conv_algo fvx_last_conv_algo(void);
  * library's device image, which every GPU that loads the library holds until
  * the process exits.  It calls no cudaMalloc, cudaFree or other allocating
  * routine.
- *   - Limit: 27 * cin * cout * 2 bytes <= 2 MiB (cin * cout <= 38836), else
- *     FVX_ERR_RANGE; FVX_F32 needs no scratch and has no such limit.
+ *   - Limit: 27 * cin * cout16 * 2 bytes <= 2 MiB (cout16 = cout rounded up
+ *     to 16; cin * cout16 <= 38836), else FVX_ERR_RANGE; FVX_F32 needs no
+ *     scratch and has no such limit.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture.
@@ -279,9 +281,11 @@ fvx_status fvx_sparse_conv_noalloc(fvx_grid gin, fvx_grid gout, fvx_kmap m, fvx_
  *     fvx_sparse_conv; dx device [gin.n_active, cin], caller-allocated, fully
  *     overwritten (zero where no pair reaches it).
  * Types as fvx_sparse_conv with the roles of cin and cout swapped: bf16
- *     needs cout a multiple of 8 (<= 512), cin a multiple of 16 (<= 256),
- *     dout, W and dx 16-byte aligned; FVX_F32 any sizes >= 1 (it transposes W
- *     into library scratch first).  Runs the pair-list kernels. */
+ *     needs cout and cin multiples of 8 (cout <= 512, cin <= 256), dout, W
+ *     and dx 16-byte aligned (cin not a multiple of 16: W is first copied
+ *     into library scratch with zero rows up to the next multiple); FVX_F32
+ *     any sizes >= 1 (it transposes W into library scratch first).  Runs the
+ *     pair-list kernels. */
 fvx_status fvx_sparse_conv_dgrad(fvx_grid gin, fvx_grid gout, fvx_kmap mt, fvx_dtype dt, const void* dout,
                                  int64_t cout, const void* W, int64_t cin, void* dx, fvx_stream stream);
 

@@ -330,6 +330,7 @@ struct ConvArgs {
   uint32_t* status;
   int64_t ntiles, n_out;
   int cin, cout, stages, lag, stage_bytes, tmem_cols, out_bf16;
+  int cout_store;  // output columns written (cout is the MMA N: cout_store rounded up to 16)
   int w_resident;  // weights live in shared memory (no per-stage B tile)
   int w_bytes;     // resident weight region incl. one zero block (multiple of 1024)
 };
@@ -367,7 +368,7 @@ __device__ __forceinline__ void conv_epilogue(ConvSmemHead& h, const ConvArgs& a
                                               int64_t ntiles, int64_t G, int warp, int lane) {
   const int quarter = warp & 3;  // TMEM lane quarter this warp may access
   const int m = quarter * 32 + lane;
-  const int cout = a.cout, out_bf16 = a.out_bf16;
+  const int cout = a.cout, cs = a.cout_store, out_bf16 = a.out_bf16;
   const int64_t n_out = a.n_out;
   uint32_t* const status = a.status;
   int i = 0;
@@ -386,7 +387,10 @@ __device__ __forceinline__ void conv_epilogue(ConvSmemHead& h, const ConvArgs& a
 #pragma unroll
         for (int e = 0; e < 16; ++e) v[e] = 0u;
       }
-      if (q < n_out && out_bf16) {
+      // columns c .. c+15 of the MMA; the last block of a cout_store that is
+      // an odd multiple of 8 writes its first 8 only
+      const int ncol = min(16, cs - c);
+      if (q < n_out && ncol > 0 && out_bf16) {
         uint4 v0, v1;
         v0.x = pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1]));
         v0.y = pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3]));
@@ -396,13 +400,17 @@ __device__ __forceinline__ void conv_epilogue(ConvSmemHead& h, const ConvArgs& a
         v1.y = pack_bf16x2(__uint_as_float(v[10]), __uint_as_float(v[11]));
         v1.z = pack_bf16x2(__uint_as_float(v[12]), __uint_as_float(v[13]));
         v1.w = pack_bf16x2(__uint_as_float(v[14]), __uint_as_float(v[15]));
-        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.y) + q * cout + c);
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.y) + q * cs + c);
         dst[0] = v0;
-        dst[1] = v1;
-      } else if (q < n_out) {
-        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<float*>(a.y) + q * cout + c);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) dst[e] = make_uint4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+        if (ncol == 16) dst[1] = v1;
+      } else if (q < n_out && ncol > 0) {
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<float*>(a.y) + q * cs + c);
+        dst[0] = make_uint4(v[0], v[1], v[2], v[3]);
+        dst[1] = make_uint4(v[4], v[5], v[6], v[7]);
+        if (ncol == 16) {
+          dst[2] = make_uint4(v[8], v[9], v[10], v[11]);
+          dst[3] = make_uint4(v[12], v[13], v[14], v[15]);
+        }
       }
     }
     tc_fence_before();
@@ -1362,15 +1370,26 @@ __global__ void __launch_bounds__(256) k_conv_wgrad(const T* __restrict__ x, con
   }
 }
 
-// W [27][cin][cout] -> Wt [27][cout][cin] (bf16), the K-major B operand.
+// W [27][cin][cout] -> Wt [27][coutp][cin], the K-major B operand; rows
+// co >= cout (padding of the MMA's N up to coutp) are zero.
 template <typename T>
-__global__ void k_transpose_w(const T* __restrict__ W, int cin, int cout, T* __restrict__ wt) {
+__global__ void k_transpose_w(const T* __restrict__ W, int cin, int cout, int coutp, T* __restrict__ wt) {
   const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t per = (int64_t)cin * cout;
+  const int64_t per = (int64_t)cin * coutp;
   if (e >= 27 * per) return;
   const int64_t s = e / per, r = e - s * per;
   const int co = (int)(r / cin), ci = (int)(r - (int64_t)co * cin);
-  wt[e] = W[s * per + (int64_t)ci * cout + co];
+  wt[e] = co < cout ? W[s * (int64_t)cin * cout + (int64_t)ci * cout + co] : T(0.0f);
+}
+
+// W [27][n][k] -> [27][np][k] with rows n .. np-1 zero (bf16).
+__global__ void k_pad_rows(const __nv_bfloat16* __restrict__ W, int n, int np, int k, __nv_bfloat16* __restrict__ out) {
+  const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t per = (int64_t)np * k;
+  if (e >= 27 * per) return;
+  const int64_t s = e / per, r = e - s * per;
+  const int row = (int)(r / k), col = (int)(r - (int64_t)row * k);
+  out[e] = row < n ? W[(s * n + row) * (int64_t)k + col] : __float2bfloat16(0.0f);
 }
 
 // cuTensorMapEncodeTiled, taken from the driver through the runtime (no link
@@ -1464,14 +1483,20 @@ fvx_status launch_conv_leaf(const char* who, fvx_grid gin, fvx_kmap m, fvx_dtype
   return FVX_OK;
 }
 
+// cout_real: output columns (a multiple of 8); the MMA's N is that rounded up
+// to 16, and wt holds [27][N][cin] with zero rows past cout_real.
 fvx_status launch_conv_bf16(const char* who, fvx_grid gin, fvx_kmap m, fvx_dtype dt, const void* feats, int64_t cin,
-                            int64_t cout, void* out, const __nv_bfloat16* wt, uint32_t* status, cudaStream_t s) {
+                            int64_t cout_real, void* out, const __nv_bfloat16* wt, uint32_t* status, cudaStream_t s) {
   const int64_t nt = m->n_tiles;
+  const int64_t cout = (cout_real + 15) & ~(int64_t)15;
   const int algo = g_conv_algo.load(std::memory_order_relaxed);
-  const bool leaf_ok = m->stride == 1 && m->leaf_nbr != nullptr && (cin == 8 || cin == 16) && cout <= kLeafMaxCout;
+  const bool leaf_ok = m->stride == 1 && m->leaf_nbr != nullptr && (cin == 8 || cin == 16) && cout <= kLeafMaxCout &&
+                       cout == cout_real;
   if (algo == FVX_CONV_LEAF && !leaf_ok) {
-    set_error("%s: the leaf-densified convolution needs stride 1, cin 8 or %d and cout <= %d (got stride %d, %lld, %lld)",
-              who, kLeafMaxCin, kLeafMaxCout, (int)m->stride, (long long)cin, (long long)cout);
+    set_error("%s: the leaf-densified convolution needs a forward stride-1 map, cin 8 or %d and cout a multiple of 16 "
+              "<= %d (got stride %d%s, %lld, %lld)",
+              who, kLeafMaxCin, kLeafMaxCout, (int)m->stride, m->transposed ? " transposed" : "", (long long)cin,
+              (long long)cout_real);
     return FVX_ERR_INVALID_ARG;
   }
   const fvx_grid_s* go = m->gout;
@@ -1491,6 +1516,7 @@ fvx_status launch_conv_bf16(const char* who, fvx_grid gin, fvx_kmap m, fvx_dtype
   a.n_out = m->n_out;
   a.cin = (int)cin;
   a.cout = (int)cout;
+  a.cout_store = (int)cout_real;
   int cols = 32;
   while (cols < cout) cols <<= 1;
   a.tmem_cols = cols;  // per accumulator; two accumulators per CTA (<= 512 columns)
@@ -1593,8 +1619,8 @@ extern "C" fvx_status fvx_sparse_conv(fvx_grid gin, fvx_grid gout, fvx_kmap m, f
     set_error("fvx_sparse_conv: unknown dtype %d", (int)dt);
     return FVX_ERR_INVALID_ARG;
   }
-  if (cin % 8 != 0 || cout % 16 != 0 || cin > 512 || cout > 256) {
-    set_error("fvx_sparse_conv: bf16 needs cin %% 8 == 0 (<= 512) and cout %% 16 == 0 (<= 256); got %lld, %lld",
+  if (cin % 8 != 0 || cout % 8 != 0 || cin > 512 || cout > 256) {
+    set_error("fvx_sparse_conv: bf16 needs cin %% 8 == 0 (<= 512) and cout %% 8 == 0 (<= 256); got %lld, %lld",
               (long long)cin, (long long)cout);
     return FVX_ERR_INVALID_ARG;
   }
@@ -1608,12 +1634,14 @@ extern "C" fvx_status fvx_sparse_conv(fvx_grid gin, fvx_grid gout, fvx_kmap m, f
     return FVX_ERR_CUDA;
   }
   Scratch scr(s);
-  __nv_bfloat16* wt = scr.get<__nv_bfloat16>((size_t)(27 * cin * cout));
+  const int64_t coutp = (cout + 15) & ~(int64_t)15;
+  __nv_bfloat16* wt = scr.get<__nv_bfloat16>((size_t)(27 * cin * coutp));
   if (!wt) return FVX_ERR_ALLOC;
   {
     LaunchScope ls("conv_transpose_w", s);
-    const int64_t n = 27 * cin * cout;
-    k_transpose_w<__nv_bfloat16><<<(unsigned)((n + 255) / 256), 256, 0, s>>>((const __nv_bfloat16*)W, (int)cin, (int)cout, wt);
+    const int64_t n = 27 * cin * coutp;
+    k_transpose_w<__nv_bfloat16><<<(unsigned)((n + 255) / 256), 256, 0, s>>>((const __nv_bfloat16*)W, (int)cin,
+                                                                             (int)cout, (int)coutp, wt);
   }
   FVX_TRY(check_launch("conv_transpose_w"));
   return launch_conv_bf16("fvx_sparse_conv", gin, m, dt, feats, cin, cout, out, wt, status, s);
@@ -1684,15 +1712,16 @@ extern "C" fvx_status fvx_sparse_conv_noalloc(fvx_grid gin, fvx_grid gout, fvx_k
     set_error("fvx_sparse_conv_noalloc: unknown dtype %d", (int)dt);
     return FVX_ERR_INVALID_ARG;
   }
-  if (cin % 8 != 0 || cout % 16 != 0 || cin > 512 || cout > 256) {
-    set_error("fvx_sparse_conv_noalloc: bf16 needs cin %% 8 == 0 (<= 512) and cout %% 16 == 0 (<= 256); got %lld, %lld",
+  if (cin % 8 != 0 || cout % 8 != 0 || cin > 512 || cout > 256) {
+    set_error("fvx_sparse_conv_noalloc: bf16 needs cin %% 8 == 0 (<= 512) and cout %% 8 == 0 (<= 256); got %lld, %lld",
               (long long)cin, (long long)cout);
     return FVX_ERR_INVALID_ARG;
   }
-  const size_t wt_bytes = (size_t)27 * (size_t)cin * (size_t)cout * 2;
+  const int64_t coutp = (cout + 15) & ~(int64_t)15;
+  const size_t wt_bytes = (size_t)27 * (size_t)cin * (size_t)coutp * 2;
   if (wt_bytes > kNoAllocWtBytes) {
-    set_error("fvx_sparse_conv_noalloc: 27*cin*cout*2 = %zu bytes of weights exceed the fixed %zu-byte scratch "
-              "(cin*cout must be <= %zu); use fvx_sparse_conv",
+    set_error("fvx_sparse_conv_noalloc: 27*cin*cout*2 = %zu bytes of weights (cout rounded up to 16) exceed the fixed "
+              "%zu-byte scratch (cin*cout must be <= %zu); use fvx_sparse_conv",
               wt_bytes, kNoAllocWtBytes, kNoAllocWtBytes / 54);
     return FVX_ERR_RANGE;
   }
@@ -1708,8 +1737,9 @@ extern "C" fvx_status fvx_sparse_conv_noalloc(fvx_grid gin, fvx_grid gout, fvx_k
   FVX_CUDA(cudaMemsetAsync(status, 0, 4, s));  // the array keeps the previous call's contents
   {
     LaunchScope ls("conv_transpose_w", s);
-    const int64_t n = 27 * cin * cout;
-    k_transpose_w<__nv_bfloat16><<<(unsigned)((n + 255) / 256), 256, 0, s>>>((const __nv_bfloat16*)W, (int)cin, (int)cout, wt);
+    const int64_t n = 27 * cin * coutp;
+    k_transpose_w<__nv_bfloat16><<<(unsigned)((n + 255) / 256), 256, 0, s>>>((const __nv_bfloat16*)W, (int)cin,
+                                                                             (int)cout, (int)coutp, wt);
   }
   FVX_TRY(check_launch("conv_transpose_w"));
   return launch_conv_bf16("fvx_sparse_conv_noalloc", gin, m, dt, feats, cin, cout, out, wt, status, s);
@@ -1789,7 +1819,8 @@ extern "C" fvx_status fvx_sparse_conv_dgrad(fvx_grid gin, fvx_grid gout, fvx_kma
     {
       LaunchScope ls("conv_transpose_w", s);
       const int64_t n = 27 * cin * cout;
-      k_transpose_w<float><<<(unsigned)((n + 255) / 256), 256, 0, s>>>((const float*)W, (int)cin, (int)cout, wt);
+      k_transpose_w<float><<<(unsigned)((n + 255) / 256), 256, 0, s>>>((const float*)W, (int)cin, (int)cout,
+                                                                       (int)cout, wt);
     }
     FVX_TRY(check_launch("conv_transpose_w"));
     {
@@ -1804,8 +1835,8 @@ extern "C" fvx_status fvx_sparse_conv_dgrad(fvx_grid gin, fvx_grid gout, fvx_kma
     set_error("fvx_sparse_conv_dgrad: unknown dtype %d", (int)dt);
     return FVX_ERR_INVALID_ARG;
   }
-  if (cout % 8 != 0 || cin % 16 != 0 || cout > 512 || cin > 256) {
-    set_error("fvx_sparse_conv_dgrad: bf16 needs cout %% 8 == 0 (<= 512) and cin %% 16 == 0 (<= 256); got %lld, %lld",
+  if (cout % 8 != 0 || cin % 8 != 0 || cout > 512 || cin > 256) {
+    set_error("fvx_sparse_conv_dgrad: bf16 needs cout %% 8 == 0 (<= 512) and cin %% 8 == 0 (<= 256); got %lld, %lld",
               (long long)cout, (long long)cin);
     return FVX_ERR_INVALID_ARG;
   }
@@ -1818,8 +1849,21 @@ extern "C" fvx_status fvx_sparse_conv_dgrad(fvx_grid gin, fvx_grid gout, fvx_kma
     set_error("fvx_sparse_conv_dgrad: device status word unavailable");
     return FVX_ERR_CUDA;
   }
-  return launch_conv_bf16("fvx_sparse_conv_dgrad", gout, mt, dt, dout, cout, cin, dx, (const __nv_bfloat16*)W, status,
-                          s);
+  if (cin % 16 == 0)
+    return launch_conv_bf16("fvx_sparse_conv_dgrad", gout, mt, dt, dout, cout, cin, dx, (const __nv_bfloat16*)W,
+                            status, s);
+  // the MMA's N (cin here) rounds up to 16: a copy of W with zero rows
+  Scratch scr(s);
+  const int64_t cinp = (cin + 15) & ~(int64_t)15;
+  __nv_bfloat16* wp = scr.get<__nv_bfloat16>((size_t)(27 * cinp * cout));
+  if (!wp) return FVX_ERR_ALLOC;
+  {
+    LaunchScope ls("conv_pad_w", s);
+    const int64_t n = 27 * cinp * cout;
+    k_pad_rows<<<(unsigned)((n + 255) / 256), 256, 0, s>>>((const __nv_bfloat16*)W, (int)cin, (int)cinp, (int)cout, wp);
+  }
+  FVX_TRY(check_launch("conv_pad_w"));
+  return launch_conv_bf16("fvx_sparse_conv_dgrad", gout, mt, dt, dout, cout, cin, dx, wp, status, s);
 }
 
 extern "C" fvx_status fvx_set_conv_algo(fvx_conv_algo algo) {

@@ -182,7 +182,7 @@ def _fwd(grids, stride):
     return grids["g"], grids["gc"], grids["og"], grids["ogc"]
 
 
-@pytest.mark.parametrize("cin,cout", [(16, 16), (32, 64), (64, 32), (16, 8), (128, 128)])
+@pytest.mark.parametrize("cin,cout", [(16, 16), (32, 64), (64, 32), (16, 8), (128, 128), (8, 16), (24, 8), (40, 64)])
 @pytest.mark.parametrize("stride", [1, 2])
 def test_dgrad_bf16(cuda_device, grids, stride, cin, cout):
     """dx = conv of dy over the transposed map with per-offset W^T."""

@@ -203,6 +203,9 @@ def test_leaf_refusals(cuda_device, dense_case):
     x, W = G.bf16_inputs(3, g.n_active, 8, 128)
     with pytest.raises(fvx.FvxError, match="leaf-densified"):
         fvx.sparse_conv(g, g, km, x, W)
+    x, W = G.bf16_inputs(3, g.n_active, 8, 8)  # N = 8 is padded to 16 by the pair-list kernels only
+    with pytest.raises(fvx.FvxError, match="leaf-densified"):
+        fvx.sparse_conv(g, g, km, x, W)
     gc = g.coarsen(2)
     km2 = fvx.KernelMap(g, gc, 2)
     x, W = G.bf16_inputs(3, g.n_active, 8, 16)

@@ -94,7 +94,8 @@ def test_conv_f32_matches_oracle(cuda_device, grids, stride, cin, cout):
 # 48 -> 3 x 16, 96 -> 3 x 32, 80 -> 5 x 16); other multiples of 8 the
 # cp.async kernel (8, 24, 40).
 @pytest.mark.parametrize("cin,cout", [(8, 16), (16, 32), (32, 64), (64, 64), (128, 128), (128, 256), (24, 48),
-                                      (256, 16), (48, 32), (96, 64), (80, 16), (40, 32), (512, 32), (16, 256)])
+                                      (256, 16), (48, 32), (96, 64), (80, 16), (40, 32), (512, 32), (16, 256),
+                                      (16, 8), (64, 24), (8, 8), (24, 40), (128, 136)])
 @pytest.mark.parametrize("stride", [1, 2])
 def test_conv_bf16_matches_oracle(cuda_device, grids, stride, cin, cout):
     import sparse_convolution_gb300 as fvx
@@ -133,7 +134,7 @@ def test_conv_bf16_many_tiles(cuda_device, many_tiles, cin, cout):
     G.assert_conv_close(G.np_(y.float()), yo, ao, G.BF16_TOL)
 
 
-@pytest.mark.parametrize("cin,cout", [(8, 16), (64, 64), (128, 256)])
+@pytest.mark.parametrize("cin,cout", [(8, 16), (64, 64), (128, 256), (16, 8), (32, 24)])
 @pytest.mark.parametrize("stride", [1, 2])
 def test_conv_bf16_out_bf16_matches_oracle(cuda_device, grids, stride, cin, cout):
     """bf16-rounded output: the stated bound plus one bf16 rounding of y."""

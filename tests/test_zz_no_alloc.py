@@ -36,7 +36,8 @@ def _call(fn, g, km, dt, x, W, out):
               W.shape[2], ctypes.c_void_p(out.data_ptr()), stream)
 
 
-@pytest.mark.parametrize("cin,cout,out_bf16", [(8, 16, False), (64, 64, False), (128, 128, True)])
+@pytest.mark.parametrize("cin,cout,out_bf16", [(8, 16, False), (64, 64, False), (128, 128, True), (16, 8, False),
+                                              (24, 40, True)])
 def test_noalloc_matches_allocating_conv(cuda_device, cin, cout, out_bf16):
     import torch
 
