@@ -1370,6 +1370,398 @@ __global__ void __launch_bounds__(256) k_conv_wgrad(const T* __restrict__ x, con
   }
 }
 
+// Weight gradient for narrow layers (cin * cout <= 1024, cin + cout <= 64),
+// fp32 FFMA.  A warp owns runs of up to kWsRun pairs of one list and keeps
+// the whole cin x cout partial in registers (lane l holds entries l, l + 32,
+// ..., J of them); 32 pairs at a time are staged in shared memory as fp32
+// rows [x | dy].  When both rows are whole 16-byte pieces the warp copies
+// the 32 pairs' pieces with one 16-byte load per lane and piece (the lanes of
+// a row read it together); otherwise each lane copies its own pair element
+// by element.  Every lane then walks the 32 staged pairs, and the run's
+// partial is added to dW with one atomic per entry.
+constexpr int kWsRun = 2048;
+constexpr int kWsWarps = 4;
+constexpr int kWsRow = 65;  // staged row pitch in floats (cin + cout <= 64, odd against bank conflicts)
+
+__device__ __forceinline__ void unpack16(const uint4 v, float* d, float) {
+  d[0] = __uint_as_float(v.x);
+  d[1] = __uint_as_float(v.y);
+  d[2] = __uint_as_float(v.z);
+  d[3] = __uint_as_float(v.w);
+}
+__device__ __forceinline__ void unpack16(const uint4 v, float* d, __nv_bfloat16) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    d[2 * k] = __uint_as_float(w[k] << 16);
+    d[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+  }
+}
+
+template <typename T, int J>
+__global__ void __launch_bounds__(kWsWarps * 32) k_conv_wgrad_small(const T* __restrict__ x, const T* __restrict__ dy,
+                                                                    const int32_t* __restrict__ in_idx,
+                                                                    const int32_t* __restrict__ out_idx,
+                                                                    const uint32_t* __restrict__ dtot, int cin,
+                                                                    int cout, int vec_ok, float* __restrict__ dW) {
+  __shared__ float buf[kWsWarps][32][kWsRow];
+  __shared__ uint32_t off[28], rcum[28];
+  constexpr int kPer = 16 / (int)sizeof(T);  // elements per 16-byte piece
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid < 28) off[tid] = __ldg(dtot + tid);
+  __syncthreads();
+  if (tid == 0) {
+    uint32_t c = 0;
+    for (int s = 0; s < 27; ++s) {
+      rcum[s] = c;
+      c += (off[s + 1] - off[s] + (uint32_t)kWsRun - 1) / (uint32_t)kWsRun;
+    }
+    rcum[27] = c;
+  }
+  __syncthreads();
+  const int E = cin * cout;
+  const bool vec = vec_ok && cin % kPer == 0 && cout % kPer == 0;  // vec_ok: both arrays 16-byte aligned
+  const int px = cin / kPer, pr = (cin + cout) / kPer;  // pieces of x, of the whole staged row
+  int eci[J], eco[J];  // this lane's entries (past E: read valid columns, never added)
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    const int e = lane + 32 * j;
+    eci[j] = e < E ? e / cout : 0;
+    eco[j] = e < E ? cin + e % cout : cin;
+  }
+  float (*b)[kWsRow] = buf[warp];
+  const uint32_t nruns = rcum[27];
+  for (uint32_t r = blockIdx.x * kWsWarps + warp; r < nruns; r += gridDim.x * kWsWarps) {
+    int s = 0;
+    while (s < 26 && rcum[s + 1] <= r) ++s;
+    const uint32_t a0 = off[s] + (r - rcum[s]) * (uint32_t)kWsRun, a1 = min(a0 + (uint32_t)kWsRun, off[s + 1]);
+    float acc[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) acc[j] = 0.f;
+    for (uint32_t e0 = a0; e0 < a1; e0 += 32) {
+      const uint32_t e = e0 + (uint32_t)lane;
+      const int np = (int)min(32u, a1 - e0);
+      const int p = e < a1 ? __ldg(in_idx + e) : 0, q = e < a1 ? __ldg(out_idx + e) : 0;
+      if (vec) {
+        for (int k = lane; k < 32 * pr; k += 32) {
+          const int pp = k / pr, piece = k - pp * pr;
+          // every lane runs pr iterations (32 * pr pieces), so the warp is converged here
+          const int pi = __shfl_sync(0xffffffffu, p, pp), qi = __shfl_sync(0xffffffffu, q, pp);
+          if (pp < np) {
+            const T* src = piece < px ? x + (int64_t)pi * cin + piece * kPer : dy + (int64_t)qi * cout + (piece - px) * kPer;
+            float v[8];
+            unpack16(__ldg(reinterpret_cast<const uint4*>(src)), v, T());
+#pragma unroll
+            for (int c = 0; c < kPer; ++c) b[pp][piece * kPer + c] = v[c];
+          }
+        }
+      } else if (e < a1) {
+        for (int c = 0; c < cin; ++c) b[lane][c] = to_f32(x[(int64_t)p * cin + c]);
+        for (int c = 0; c < cout; ++c) b[lane][cin + c] = to_f32(dy[(int64_t)q * cout + c]);
+      }
+      __syncwarp();
+      for (int pp = 0; pp < np; ++pp) {
+#pragma unroll
+        for (int j = 0; j < J; ++j) acc[j] = fmaf(b[pp][eci[j]], b[pp][eco[j]], acc[j]);
+      }
+      __syncwarp();
+    }
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const int e = lane + 32 * j;
+      if (e < E) atomicAdd(dW + (size_t)s * E + e, acc[j]);
+    }
+  }
+}
+
+template <typename T>
+void launch_wgrad_small(unsigned grid, cudaStream_t s, const void* x, const void* dy, const int32_t* in_idx,
+                        const int32_t* out_idx, const uint32_t* dtot, int cin, int cout, float* dW) {
+  const int J = (cin * cout + 31) / 32;
+  auto kern = J <= 1 ? k_conv_wgrad_small<T, 1>
+              : J <= 2 ? k_conv_wgrad_small<T, 2>
+              : J <= 4 ? k_conv_wgrad_small<T, 4>
+              : J <= 8 ? k_conv_wgrad_small<T, 8>
+              : J <= 16 ? k_conv_wgrad_small<T, 16>
+                        : k_conv_wgrad_small<T, 32>;
+  const int vec_ok = (((uintptr_t)x | (uintptr_t)dy) & 15u) == 0 ? 1 : 0;
+  kern<<<grid, kWsWarps * 32, 0, s>>>((const T*)x, (const T*)dy, in_idx, out_idx, dtot, cin, cout, vec_ok, dW);
+}
+
+// ============================================================== weight gradient, tensor cores
+// dW[s] = X_s^T dY_s over the pairs of list s: a contraction over pairs (K),
+// with M = input channels and N = output channels.  The rows that TMA
+// tile::gather4 brings (one pair per 128-byte shared-memory row, 64 channels
+// of x or dy) already form the MN-major operand layout: 64 channels along a
+// swizzled 128-byte row, pairs (K) down the rows, 8-row groups 1024 bytes
+// apart.  A work unit is up to kWgUnit pairs of one list for one tile of
+// 128 input x up to 256 output channels; its fp32 accumulator lives in tensor
+// memory and is added to dW with one atomic per entry at the end.  Four
+// producer warps share the gathers of a stage (a warp's TMA instructions
+// issue one lane after another), one thread issues the MMAs, four warps the
+// atomics (with two accumulators, the atomics of a unit overlap the MMAs of
+// the next).  cin and cout multiples of 64.
+constexpr int kWgUnit = 4096;        // pairs per work unit
+constexpr int kWgProducerWarps = 4;  // warps 0-3 issue the gathers, warp 4 the MMAs, warps 5-8 the atomics
+constexpr int kWgMmaWarp = kWgProducerWarps;
+constexpr int kWgThreads = (kWgProducerWarps + 5) * 32;
+constexpr int kWgAtom = 8192;        // 64 pairs x 128 bytes
+constexpr int kWgMaxStages = 8;
+
+struct alignas(128) WgradArgs {
+  CUtensorMap tmx;  // x [n_in][cin] bf16, box {64, 1}, 128-byte swizzle
+  CUtensorMap tmy;  // dy [n_out][cout] bf16, box {64, 1}, 128-byte swizzle
+  const int32_t* in_idx;
+  const int32_t* out_idx;
+  const uint32_t* dtot;  // list offsets [28]
+  float* dW;
+  uint32_t* status;
+  int cin, cout, n_in, n_out;
+  int mt, nt;            // channel tiles: 128 of cin, 256 of cout
+  int stages, stage_bytes, b_off;  // stage = [A: 2 atoms][B: up to 4 atoms]
+};
+
+struct WgradHead {
+  unsigned long long full[kWgMaxStages], empty[kWgMaxStages], acc_full[2], acc_empty[2];
+  uint32_t off[28];   // list offsets
+  uint32_t ucum[28];  // units before list s
+  uint32_t tmem_base;
+};
+
+struct WgUnit {
+  int s, mt, nt;
+  uint32_t start, end;
+};
+
+__device__ __forceinline__ WgUnit wg_unit(const WgradHead& h, const WgradArgs& a, uint32_t v) {
+  const uint32_t tiles = (uint32_t)(a.mt * a.nt);
+  const uint32_t tile = v % tiles, cu = v / tiles;
+  int s = 0;
+  while (s < 26 && h.ucum[s + 1] <= cu) ++s;
+  WgUnit u;
+  u.s = s;
+  u.mt = (int)(tile / (uint32_t)a.nt);
+  u.nt = (int)(tile % (uint32_t)a.nt);
+  u.start = h.off[s] + (cu - h.ucum[s]) * (uint32_t)kWgUnit;
+  u.end = min(u.start + (uint32_t)kWgUnit, h.off[s + 1]);
+  return u;
+}
+
+// MN-major operand with the 128-byte swizzle: 64-element atoms along M (or
+// N) lbo bytes apart, 8-row groups along K sbo bytes apart.
+__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor, kind::f16, D fp32, A and B bf16, both MN-major.
+__device__ __forceinline__ uint32_t idesc_bf16_mn(int M, int N) {
+  return idesc_bf16(M, N) | (1u << 15) | (1u << 16);
+}
+
+__global__ void __launch_bounds__(kWgThreads, 1) k_conv_wgrad_tc(const __grid_constant__ WgradArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* sbase = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  // the stage ring, 16 KB of slack (the MMAs never read past a stage, the
+  // slack only keeps every descriptor's reach inside the allocation), head
+  WgradHead& h = *reinterpret_cast<WgradHead*>(sbase + (size_t)a.stages * a.stage_bytes + 16384);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int S = a.stages;
+  const int64_t G = gridDim.x;
+  uint32_t* const status = a.status;
+
+  // zero the stage ring: a tile of 64 input channels reads its second A atom
+  // as zeros, and no copy ever writes there
+  for (int e = tid; e < a.stages * a.stage_bytes / 16; e += kWgThreads)
+    reinterpret_cast<uint4*>(sbase)[e] = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async();
+  if (tid == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(smem_u32(&h.full[i]), 1);
+      mbar_init(smem_u32(&h.empty[i]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&h.acc_full[b]), 1);
+      mbar_init(smem_u32(&h.acc_empty[b]), 4);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (tid < 28) h.off[tid] = __ldg(a.dtot + tid);
+  if (warp == kWgMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&h.tmem_base)),
+                 "r"(512)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  __syncthreads();
+  if (tid == 0) {
+    uint32_t c = 0;
+    for (int s = 0; s < 27; ++s) {
+      h.ucum[s] = c;
+      c += (h.off[s + 1] - h.off[s] + (uint32_t)kWgUnit - 1) / (uint32_t)kWgUnit;
+    }
+    h.ucum[27] = c;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = h.tmem_base;
+  const uint32_t nunits = h.ucum[27] * (uint32_t)(a.mt * a.nt);
+
+  if (warp < kWgProducerWarps) {
+    // ---------------- producers: row indices (every producer warp loads all
+    // 64 of a stage) and TMA gathers (op = 4 * lane + warp)
+    int64_t kg = 0;
+    int ring_sb = 0;
+    uint32_t ring_ph = 0;
+    for (uint32_t v = blockIdx.x; v < nunits; v += (uint32_t)G) {
+      const WgUnit u = wg_unit(h, a, v);
+      const int a_atoms = min(2, (a.cin - u.mt * 128) / 64);
+      const int b_atoms = min(4, (a.cout - u.nt * 256) / 64);
+      const uint32_t bytes = (uint32_t)(a_atoms + b_atoms) * (uint32_t)kWgAtom;
+      const int nops = 16 * (a_atoms + b_atoms);
+      const int nst = (int)((u.end - u.start + 63) / 64);
+      // indices of a stage: lane l holds pairs 2l and 2l+1 (absent rows read
+      // as zeros through the out-of-range row index)
+      auto load_idx = [&](int k, int (&pi)[2], int (&qi)[2]) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const uint32_t e = u.start + (uint32_t)(64 * k + 2 * lane + j);
+          const bool ok = k < nst && e < u.end;
+          pi[j] = ok ? __ldg(a.in_idx + e) : a.n_in;
+          qi[j] = ok ? __ldg(a.out_idx + e) : a.n_out;
+        }
+      };
+      int p0[2], q0[2], p1[2], q1[2];
+      load_idx(0, p0, q0);
+      load_idx(1, p1, q1);
+      for (int k = 0; k < nst; ++k, ++kg) {
+        int p2[2], q2[2];
+        load_idx(k + 2, p2, q2);  // two stages ahead
+        const int sb = ring_sb;
+        if (kg >= S) mbar_wait(smem_u32(&h.empty[sb]), ring_ph ^ 1u, status);
+        if (++ring_sb == S) {
+          ring_sb = 0;
+          ring_ph ^= 1u;
+        }
+        const uint32_t bar = smem_u32(&h.full[sb]);
+        const uint32_t sA = smem_u32(sbase + (size_t)sb * a.stage_bytes), sB = sA + (uint32_t)a.b_off;
+        if (warp == 0 && lane == 0) mbar_arrive_expect_tx(bar, bytes);
+        {
+          const int op = 4 * lane + warp;  // < 128: covers the at most 96 ops of a stage
+          const int r4 = op & 15, atom = op >> 4;  // atoms 0..a_atoms-1: x, then dy
+          const bool isA = atom < a_atoms;
+          // rows 4 r4 .. 4 r4 + 3 are held by lanes 2 r4 (two) and 2 r4 + 1 (two)
+          const int l0 = 2 * r4, l1 = 2 * r4 + 1;
+          const int x0 = __shfl_sync(0xffffffffu, p0[0], l0), x1 = __shfl_sync(0xffffffffu, p0[1], l0);
+          const int x2 = __shfl_sync(0xffffffffu, p0[0], l1), x3 = __shfl_sync(0xffffffffu, p0[1], l1);
+          const int y0 = __shfl_sync(0xffffffffu, q0[0], l0), y1 = __shfl_sync(0xffffffffu, q0[1], l0);
+          const int y2 = __shfl_sync(0xffffffffu, q0[0], l1), y3 = __shfl_sync(0xffffffffu, q0[1], l1);
+          if (op < nops) {
+            if (isA)
+              tma_gather4(sA + (uint32_t)(atom * kWgAtom + r4 * 512), &a.tmx, u.mt * 128 + 64 * atom,
+                          make_int4(x0, x1, x2, x3), bar);
+            else
+              tma_gather4(sB + (uint32_t)((atom - a_atoms) * kWgAtom + r4 * 512), &a.tmy,
+                          u.nt * 256 + 64 * (atom - a_atoms), make_int4(y0, y1, y2, y3), bar);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          p0[j] = p1[j];
+          q0[j] = q1[j];
+          p1[j] = p2[j];
+          q1[j] = q2[j];
+        }
+      }
+    }
+    if (warp == 0 && lane == 0) {
+      // after a give-up, let the copies in flight land before the block exits
+      int sb = ring_sb;
+      uint32_t ph = ring_ph;
+      for (int64_t c = 0; c < kg && c < S; ++c) {
+        if (sb == 0) {
+          sb = S - 1;
+          ph ^= 1u;
+        } else {
+          --sb;
+        }
+        mbar_drain(smem_u32(&h.full[sb]), ph);
+      }
+    }
+  } else if (warp == kWgMmaWarp) {
+    // ---------------- MMA issue (one thread)
+    if (lane == 0) {
+      const uint64_t a0 = sdesc_mn_sw128(smem_u32(sbase), (uint32_t)kWgAtom, 1024u);
+      const uint64_t b0 = sdesc_mn_sw128(smem_u32(sbase) + (uint32_t)a.b_off, (uint32_t)kWgAtom, 1024u);
+      const uint32_t sunits = (uint32_t)a.stage_bytes >> 4;
+      int m_sb = 0;
+      uint32_t m_ph = 0, m_off = 0;
+      int i = 0;
+      for (uint32_t v = blockIdx.x; v < nunits; v += (uint32_t)G, ++i) {
+        const WgUnit u = wg_unit(h, a, v);
+        const int nst = (int)((u.end - u.start + 63) / 64);
+        const uint32_t idesc = idesc_bf16_mn(128, 64 * min(4, (a.cout - u.nt * 256) / 64));
+        const int b = i & 1;
+        if (i >= 2) mbar_wait(smem_u32(&h.acc_empty[b]), (uint32_t)(((i >> 1) - 1) & 1), status);
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)b * 256u;
+        for (int k = 0; k < nst; ++k) {
+          mbar_wait(smem_u32(&h.full[m_sb]), m_ph, status);
+          tc_fence_after();
+          const uint64_t ad = a0 + m_off, bd = b0 + m_off;
+          // K steps of 16 pairs: two 8-row groups, 2048 bytes
+          umma_bf16(d, ad, bd, idesc, k > 0 ? 1u : 0u);
+          umma_bf16(d, ad + 128, bd + 128, idesc, 1u);
+          umma_bf16(d, ad + 256, bd + 256, idesc, 1u);
+          umma_bf16(d, ad + 384, bd + 384, idesc, 1u);
+          umma_commit(smem_u32(&h.empty[m_sb]));
+          m_off += sunits;
+          if (++m_sb == S) {
+            m_sb = 0;
+            m_ph ^= 1u;
+            m_off = 0;
+          }
+        }
+        umma_commit(smem_u32(&h.acc_full[b]));
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue: TMEM lane quarter warp & 3 = input channels
+    // 32 q .. 32 q + 31 of the tile; atomics into dW
+    const int quarter = warp & 3, row = quarter * 32 + lane;
+    int i = 0;
+    for (uint32_t v = blockIdx.x; v < nunits; v += (uint32_t)G, ++i) {
+      const WgUnit u = wg_unit(h, a, v);
+      const int b = i & 1;
+      const int ncols = 64 * min(4, (a.cout - u.nt * 256) / 64);
+      mbar_wait(smem_u32(&h.acc_full[b]), (uint32_t)((i >> 1) & 1), status);
+      tc_fence_after();
+      const int ci = u.mt * 128 + row;
+      float* dst = a.dW + ((size_t)u.s * a.cin + (size_t)ci) * a.cout + (size_t)u.nt * 256;
+      const uint32_t trow = tmem + (uint32_t)b * 256u + ((uint32_t)(quarter * 32) << 16);
+      for (int c = 0; c < ncols; c += 16) {
+        uint32_t r[16];
+        tmem_ld16(trow + (uint32_t)c, r);
+        if (ci < a.cin) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) atomicAdd(dst + c + j, __uint_as_float(r[j]));
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&h.acc_empty[b]));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWgMmaWarp) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512) : "memory");
+  }
+}
+
 // W [27][cin][cout] -> Wt [27][coutp][cin], the K-major B operand; rows
 // co >= cout (padding of the MMA's N up to coutp) are zero.
 template <typename T>
@@ -1771,6 +2163,53 @@ extern "C" fvx_status fvx_sparse_conv_wgrad(fvx_grid gin, fvx_grid gout, fvx_kma
   int dev = 0, sms = 0;
   FVX_CUDA(cudaGetDevice(&dev));
   FVX_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  EncodeTiledFn enc = (dt == FVX_BF16 && cin % 64 == 0 && cout % 64 == 0 && gin->n_active > 0 && gout->n_active > 0 &&
+                       (((uintptr_t)feats | (uintptr_t)dout) & 15u) == 0)
+                          ? encode_tiled()
+                          : nullptr;
+  if (enc) {
+    uint32_t* status = device_status_word();
+    if (!status) {
+      set_error("fvx_sparse_conv_wgrad: device status word unavailable");
+      return FVX_ERR_CUDA;
+    }
+    WgradArgs wa;
+    FVX_TRY(encode_2d(enc, &wa.tmx, feats, cin, gin->n_active, 64, 1, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "fvx_sparse_conv_wgrad"));
+    FVX_TRY(encode_2d(enc, &wa.tmy, dout, cout, gout->n_active, 64, 1, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "fvx_sparse_conv_wgrad"));
+    wa.in_idx = m->in_idx;
+    wa.out_idx = m->out_idx;
+    wa.dtot = m->dtot;
+    wa.dW = dW;
+    wa.status = status;
+    wa.cin = (int)cin;
+    wa.cout = (int)cout;
+    wa.n_in = (int)gin->n_active;
+    wa.n_out = (int)gout->n_active;
+    wa.mt = (int)((cin + 127) / 128);
+    wa.nt = (int)((cout + 255) / 256);
+    wa.b_off = 2 * kWgAtom;
+    wa.stage_bytes = wa.b_off + kWgAtom * (int)std::min<int64_t>(4, cout / 64);
+    const int head = (int)sizeof(WgradHead);
+    wa.stages = std::min(kWgMaxStages, (224 * 1024 - 1024 - 16384 - head) / wa.stage_bytes);
+    const size_t smem = 1024 + (size_t)wa.stages * wa.stage_bytes + 16384 + head;
+    FVX_CUDA(cudaFuncSetAttribute(k_conv_wgrad_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    {
+      LaunchScope ls("conv_wgrad_tc", s);
+      k_conv_wgrad_tc<<<(unsigned)sms, kWgThreads, smem, s>>>(wa);
+    }
+    return check_launch("conv_wgrad_tc");
+  }
+  if (cin * cout <= 1024 && cin + cout <= 64) {
+    const unsigned grid = (unsigned)sms * 4;  // 4 blocks of 4 warps per SM (128 registers a thread)
+    LaunchScope ls("conv_wgrad_small", s);
+    if (dt == FVX_F32)
+      launch_wgrad_small<float>(grid, s, feats, dout, m->in_idx, m->out_idx, m->dtot, (int)cin, (int)cout, dW);
+    else
+      launch_wgrad_small<__nv_bfloat16>(grid, s, feats, dout, m->in_idx, m->out_idx, m->dtot, (int)cin, (int)cout, dW);
+    return check_launch("conv_wgrad_small");
+  }
   const int64_t tiles = ((cin + kWgTile - 1) / kWgTile) * ((cout + kWgTile - 1) / kWgTile);
   const int64_t chunks = (m->pair_capacity + kWgChunk - 1) / kWgChunk;
   const unsigned gx = (unsigned)std::max<int64_t>(1, std::min<int64_t>(chunks, (int64_t)sms * 8 / std::max<int64_t>(1, std::min<int64_t>(tiles, 8))));

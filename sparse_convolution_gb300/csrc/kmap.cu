@@ -262,7 +262,7 @@ __global__ void __launch_bounds__(kKmThreads) k_kmap1_count(GridDev gin, const i
                                                             const uint64_t* __restrict__ out_rec, int64_t n_out_leaf,
                                                             uint32_t* __restrict__ counts,
                                                             uint32_t* __restrict__ out_mask,
-                                                            int32_t* __restrict__ nbr_out) {
+                                                            int32_t* __restrict__ nbr_out, int mirror) {
   __shared__ Km1Smem sm;
   const int lo = blockIdx.x, tid = threadIdx.x;
   km1_load(sm, gin, out_origin, out_batch, out_rec, lo, nullptr, nbr_out);
@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(kKmThreads) k_kmap1_count(GridDev gin, const i
   c += __shfl_xor_sync(0xffffffffu, c, 1);
   c += __shfl_xor_sync(0xffffffffu, c, 2);
   c += __shfl_xor_sync(0xffffffffu, c, 4);
-  if (s < 27 && x == 0) counts[(int64_t)s * n_out_leaf + lo] = c;
+  if (s < 27 && x == 0) counts[(int64_t)(mirror ? 26 - s : s) * n_out_leaf + lo] = c;
   // active output voxels in index order
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(kKmThreads) k_kmap1_count(GridDev gin, const i
     const int n = sm.vox[idx], w = n >> 6, bit = n & 63;
     uint32_t mk = 0;
 #pragma unroll
-    for (int t = 0; t < 27; ++t) mk |= (uint32_t)((sm.R[t][w] >> bit) & 1ull) << t;
+    for (int t = 0; t < 27; ++t) mk |= (uint32_t)((sm.R[t][w] >> bit) & 1ull) << (mirror ? 26 - t : t);
     out_mask[sm.qf + idx] = mk;
   }
 }
@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(kKmThreads) k_kmap1_write(GridDev gin, const i
                                                             const uint32_t* __restrict__ starts,
                                                             const int32_t* __restrict__ nbr_in,
                                                             int32_t* __restrict__ in_idx,
-                                                            int32_t* __restrict__ out_idx) {
+                                                            int32_t* __restrict__ out_idx, int mirror) {
   __shared__ Km1WriteSmem sw;
   Km1Smem& sm = sw.k;
   const int lo = blockIdx.x, tid = threadIdx.x;
@@ -333,7 +333,7 @@ __global__ void __launch_bounds__(kKmThreads) k_kmap1_write(GridDev gin, const i
   const uint32_t lt = lanemask_lt();
   for (int s = warp; s < 27; s += kKmThreads / 32) {
     const int di = s / 9 - 1, dj = (s / 3) % 3 - 1, dk = s % 3 - 1;
-    uint32_t e = starts[(int64_t)s * n_out_leaf + lo];
+    uint32_t e = starts[(int64_t)(mirror ? 26 - s : s) * n_out_leaf + lo];
     for (int x = 0; x < 8; ++x) {
       const unsigned long long om = sm.om[x];
       if (!om) continue;
@@ -463,7 +463,10 @@ fvx_status kernel_map_impl(const char* who, fvx_grid gin, fvx_grid gout, int32_t
   // writes, which the leaf-densified convolution reads too)
   const size_t o_mask = 0, o_tot = align_up(4 * (size_t)Nout), o_tile = o_tot + align_up(4 * 32);
   const size_t o_nbr = o_tile + align_up(4 * (size_t)(27 * m->n_tiles + 1));
-  const bool bitpar = stride == 1 && !transposed;  // bit-parallel stride-1 kernels
+  // Stride 1 runs the bit-parallel kernels.  Its transposed map pairs output
+  // p with the input at p - d, which the forward map lists under the mirrored
+  // offset -d (slot 26 - s): the same kernels write each list to slot 26 - s.
+  const bool bitpar = stride == 1;
   const size_t bytes1 = o_nbr + (bitpar ? align_up(4 * (size_t)(27 * Lo + 1)) : 0);
   m->block = dalloc(bytes1, s);
   if (!m->block) return FVX_ERR_ALLOC;
@@ -488,13 +491,13 @@ fvx_status kernel_map_impl(const char* who, fvx_grid gin, fvx_grid gout, int32_t
   int32_t* nbr = nullptr;  // stride 1: input-leaf slot table written by the count pass
   if (bitpar) {
     nbr = (int32_t*)((char*)m->block + o_nbr);
-    m->leaf_nbr = nbr;
+    if (!transposed) m->leaf_nbr = nbr;  // the leaf-densified conv takes forward maps only
   }
   if (Lo > 0) {
     LaunchScope ls("kmap_count", s);
     if (bitpar)
       k_kmap1_count<<<(unsigned)Lo, kKmThreads, 0, s>>>(gd, gout->leaf_origin, gout->leaf_batch, gout->leaf_rec, Lo,
-                                                        counts, m->out_mask, nbr);
+                                                        counts, m->out_mask, nbr, transposed ? 1 : 0);
     else
       k_kmap_count<<<(unsigned)Lo, kKmThreads, 0, s>>>(gd, gout->leaf_origin, gout->leaf_batch, gout->leaf_rec, Lo,
                                                        stride, transposed ? 1 : 0, counts, m->out_mask);
@@ -523,7 +526,7 @@ fvx_status kernel_map_impl(const char* who, fvx_grid gin, fvx_grid gout, int32_t
     LaunchScope ls("kmap_write", s);
     if (bitpar)
       k_kmap1_write<<<(unsigned)Lo, kKmThreads, 0, s>>>(gd, gout->leaf_origin, gout->leaf_batch, gout->leaf_rec, Lo,
-                                                        counts, nbr, m->in_idx, m->out_idx);
+                                                        counts, nbr, m->in_idx, m->out_idx, transposed ? 1 : 0);
     else
       k_kmap_write<<<(unsigned)Lo, kKmThreads, 0, s>>>(gd, gout->leaf_origin, gout->leaf_batch, gout->leaf_rec, Lo,
                                                        stride, transposed ? 1 : 0, counts, m->in_idx, m->out_idx);
