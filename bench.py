@@ -10,7 +10,9 @@ Prints ONE JSON line (rank 0).  `value` is whole-step throughput in active
 voxels per second (Mvoxels/s) with inputs resident in HBM; `components` splits
 it into the two quantities the metric names (build+kmap Mvoxels/s and conv
 active-pair TFLOP/s).  `--impl reference` times the CPU oracle on a bounded
-sample of the same workload instead.
+sample of the same workload instead.  `--pass backward` times the training
+backward of the workload's convs instead (transposed kernel map, input and
+weight gradients; its own metric, in TFLOP/s).
 """
 from __future__ import annotations
 
@@ -44,6 +46,9 @@ def parse():
                    help="smaller instance of the same workload generator (< 1), e.g. for profiler captures")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--profile-kernel", default=None, help="kernel whose launches are timed for the roofline")
+    p.add_argument("--pass", dest="which", default="forward", choices=["forward", "backward"],
+                   help="forward: build -> kernel map -> conv (the default step); backward: the training "
+                        "backward of the workload's convs (transposed kernel map, input and weight gradients)")
     return p.parse_args()
 
 
@@ -514,6 +519,211 @@ def bench_fvx(args, world, rank, local):
     return out
 
 
+# ---------------------------------------------------------------- backward pass
+BWD_METRIC = "sparse conv3d backward (input + weight gradient) active-pair TFLOP/s"
+
+
+def oracle_backward(coords, offs, convs, seed):
+    """The oracle's backward of the workload's first conv on a sample: the
+    transposed map, dx = conv of dy over it with W^T, and dW.  Returns the
+    active-pair flops (4 * pairs * cin * cout)."""
+    import oracle
+    from sparse_convolution_gb300 import synth
+
+    c = convs[0]
+    g = oracle.Grid.build(coords, offs)
+    go = g if c["stride"] == 1 else g.coarsen(c["stride"])
+    km = oracle.KernelMap(g, go, c["stride"])
+    kt = oracle.KernelMap(go, g, c["stride"], transposed=True)
+    x = synth.features(seed, g.n_active, c["cin"]).astype(np.float64)
+    dy = synth.features(seed + 1, go.n_active, c["cout"]).astype(np.float64)
+    W = synth.weights(seed + 2, c["cin"], c["cout"]).astype(np.float64)
+    oracle.conv(kt, dy, np.ascontiguousarray(W.transpose(0, 2, 1)))
+    oracle.conv_wgrad(km, x, dy)
+    return 4.0 * km.n_pairs * c["cin"] * c["cout"]
+
+
+def bench_backward(args, world, rank, local):
+    """Backward of the workload's convs with the forward pass's grids and
+    kernel maps given (built once, outside the timed region).  A step, per
+    conv: the transposed kernel map (gout -> gin), dx = fvx_sparse_conv_dgrad,
+    dW = fvx_sparse_conv_wgrad.  value = active-pair flops of the two
+    gradients (2 * 2 * pairs * cin * cout) per second."""
+    import torch
+
+    from sparse_convolution_gb300 import build_lib
+    import sparse_convolution_gb300 as fvx
+    from sparse_convolution_gb300 import synth
+
+    torch.cuda.set_device(local)
+    build_lib.build()
+    fvx.load()
+    w = make_workload(args.workload, args.scale)
+    convs = w["convs"]
+    fp32 = w["dtype"] == "f32"
+    dev = torch.device("cuda", local)
+    fdt = torch.float32 if fp32 else torch.bfloat16
+    g = fvx.Grid.build(torch.from_numpy(w["coords"]).to(dev), w["batch_offsets"])
+    grids, kms, pairs = [g], [], []
+    for c in convs:
+        gin = grids[-1]
+        gout = gin if c["stride"] == 1 else gin.coarsen(c["stride"])
+        grids.append(gout)
+        km = fvx.KernelMap(gin, gout, c["stride"])
+        kms.append(km)
+        pairs.append(km.n_pairs)
+    gi = [grids[i] for i in range(len(convs))]
+    go = [grids[i + 1] for i in range(len(convs))]
+    x_h = [torch.from_numpy(synth.features(w["seed"] + 30 + i, gi[i].n_active, c["cin"], w["feat_kind"])).to(fdt)
+           .pin_memory() for i, c in enumerate(convs)]
+    dy_h = [torch.from_numpy(synth.features(w["seed"] + 40 + i, go[i].n_active, c["cout"], w["feat_kind"])).to(fdt)
+            .pin_memory() for i, c in enumerate(convs)]
+    W_h = [torch.from_numpy(synth.weights(w["seed"] + 20 + i, c["cin"], c["cout"])).to(fdt).pin_memory()
+           for i, c in enumerate(convs)]
+    xs = [t.to(dev) for t in x_h]
+    dys = [t.to(dev) for t in dy_h]
+    Ws = [t.to(dev) for t in W_h]
+    dxs = [torch.empty((gi[i].n_active, c["cin"]), dtype=torch.float32, device=dev) for i, c in enumerate(convs)]
+    dWs = [torch.empty((27, c["cin"], c["cout"]), dtype=torch.float32, device=dev) for c in convs]
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def wgrad_kernel(c):  # the library's choice for this layer
+        if c["cin"] * c["cout"] <= 1024 and c["cin"] + c["cout"] <= 64:
+            return "conv_wgrad_small"
+        if not fp32 and c["cin"] % 8 == 0 and c["cout"] % 8 == 0:
+            return "conv_wgrad_tc"
+        return "conv_wgrad"
+
+    marks = []
+
+    def rec(cat, fn):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        r = fn()
+        e1.record(stream)
+        marks.append((cat, e0, e1))
+        return r
+
+    def step(x_in, dy_in, W_in, dx_out, dW_out, timed):
+        for i, c in enumerate(convs):
+            if timed:
+                kt = rec("kmap_t", lambda: fvx.KernelMap(go[i], gi[i], c["stride"], transposed=True))
+                rec("dgrad", lambda: fvx.sparse_conv_dgrad(gi[i], go[i], kt, dy_in[i], W_in[i], out=dx_out[i]))
+                rec("wgrad", lambda: fvx.sparse_conv_wgrad(gi[i], go[i], kms[i], x_in[i], dy_in[i], out=dW_out[i]))
+            else:
+                kt = fvx.KernelMap(go[i], gi[i], c["stride"], transposed=True)
+                fvx.sparse_conv_dgrad(gi[i], go[i], kt, dy_in[i], W_in[i], out=dx_out[i])
+                fvx.sparse_conv_wgrad(gi[i], go[i], kms[i], x_in[i], dy_in[i], out=dW_out[i])
+            kt.destroy()
+
+    for _ in range(args.warmup):
+        step(xs, dys, Ws, dxs, dWs, False)
+    torch.cuda.synchronize()
+    fvx.device_status()
+    flops_i = [4.0 * p * c["cin"] * c["cout"] for c, p in zip(convs, pairs)]
+    big = max(range(len(convs)), key=lambda i: flops_i[i])
+    prof_kernel = args.profile_kernel or wgrad_kernel(convs[big])
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    fvx.profile_enable(prof_kernel)
+    l0 = fvx.launch_count()
+    K = args.steps
+    for k in range(K):
+        flush.fill_(float(k))
+        step(xs, dys, Ws, dxs, dWs, True)
+    torch.cuda.synchronize()
+    launches = fvx.launch_count() - l0
+    prof_ms, prof_n = fvx.profile_read()
+    fvx.profile_enable(None)
+    barrier(world)
+    clk = clocks.stop()
+    fvx.device_status()
+    t = {"kmap_t": 0.0, "dgrad": 0.0, "wgrad": 0.0}
+    for cat, e0, e1 in marks:
+        t[cat] += e0.elapsed_time(e1) / 1e3
+    t_total = max_over_ranks(sum(t.values()), world)
+    value = sum(flops_i) * K * world / t_total / 1e12
+
+    peaks, peak_kind = measured_peaks()
+    roofline = None
+    if prof_n:
+        mine = [i for i, c in enumerate(convs) if wgrad_kernel(c) == prof_kernel]
+        wflops = sum(flops_i[i] / 2 for i in mine)  # the weight gradient's half
+        ach = wflops * K / (prof_ms / 1e3) / 1e12
+        if prof_kernel == "conv_wgrad_tc":
+            roofline = dict(bound="tensor", achieved=round(ach, 2), peak=peaks["bf16_tflops"], unit="TFLOP/s",
+                            peak_source=f"{peak_kind} (bf16_tflops, burst)")
+        else:
+            peak = 152 * 128 * 2 * 2.07e9 / 1e12
+            roofline = dict(bound="alu", achieved=round(ach, 3), peak=round(peak, 1), unit="TFLOP/s",
+                            peak_source="derived: 152 SMs x 128 FP32 lanes x 2 x 2.07 GHz")
+        roofline.update(kernel=prof_kernel, frac=round(roofline["achieved"] / roofline["peak"], 4), traffic=None,
+                        flops=int(wflops / max(1, prof_n // K)), avg_launch_ms=round(prof_ms / prof_n, 5),
+                        launches_per_step=int(prof_n // K))
+
+    # end to end: every step uploads x, dy and W from pinned host memory and
+    # downloads dx and dW, inside the timed region (one stream)
+    n_e2e = max(2, min(K, 10))
+    xd = [torch.empty_like(t_) for t_ in xs]
+    dyd = [torch.empty_like(t_) for t_ in dys]
+    Wd = [torch.empty_like(t_) for t_ in Ws]
+    dx_h = [torch.empty(t_.shape, dtype=t_.dtype).pin_memory() for t_ in dxs]
+    dW_h = [torch.empty(t_.shape, dtype=t_.dtype).pin_memory() for t_ in dWs]
+
+    def e2e_step():
+        for d_, h_ in zip(xd + dyd + Wd, x_h + dy_h + W_h):
+            d_.copy_(h_, non_blocking=True)
+        step(xd, dyd, Wd, dxs, dWs, False)
+        for h_, d_ in zip(dx_h + dW_h, dxs + dWs):
+            h_.copy_(d_, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_e2e = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+    e2e = dict(value=round(sum(flops_i) * n_e2e * world / t_e2e / 1e12, 3), unit="TFLOP/s",
+               h2d_bytes_per_step=int(sum(t_.numel() * t_.element_size() for t_ in x_h + dy_h + W_h)),
+               d2h_bytes_per_step=int(sum(t_.numel() * t_.element_size() for t_ in dx_h + dW_h)), steps=n_e2e)
+    out = dict(metric=BWD_METRIC, value=round(value, 3), unit="TFLOP/s", n_gpus=world, steps=K, warmup=args.warmup,
+               ms_per_step=round(t_total / K * 1e3, 4), higher_is_better=True, scaling="weak", vs_baseline=None,
+               dtype="f32" if fp32 else "bf16", data="synthetic",
+               config=dict(workload=w["name"], active_voxels=int(g.n_active), pairs=[int(p) for p in pairs],
+                           convs=[f"{c['cin']}->{c['cout']} stride {c['stride']}" for c in convs],
+                           step="per conv: transposed kernel map, input gradient, weight gradient",
+                           l2="flushed between steps (256 MB write outside the step events)",
+                           parallelism=f"replicas x{world}"),
+               components=dict(kmap_t_ms=round(t["kmap_t"] / K * 1e3, 4), dgrad_ms=round(t["dgrad"] / K * 1e3, 4),
+                               wgrad_ms=round(t["wgrad"] / K * 1e3, 4),
+                               dgrad_tflops=round(sum(flops_i) / 2 * K / t["dgrad"] / 1e12, 3),
+                               wgrad_tflops=round(sum(flops_i) / 2 * K / t["wgrad"] / 1e12, 3),
+                               wgrad_kernels=[wgrad_kernel(c) for c in convs]),
+               roofline=roofline, e2e=e2e, gpu_launches=int(launches), clocks=clk)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        coords, offs, desc = oracle_sample(w, target_rows=60_000)
+        t0 = time.perf_counter()
+        fl = oracle_backward(coords, offs, convs, 1)
+        dt = time.perf_counter() - t0
+        out["cpu_baseline"] = dict(value=fl / dt / 1e12, unit="TFLOP/s", cores=1, kind="oracle",
+                                   sample=f"{desc}: backward of the first conv (transposed map, dx, dW), "
+                                          f"single-threaded, {dt:.1f} s", host_cores=os.cpu_count())
+    for km in kms:
+        km.destroy()
+    for gr in grids[1:]:
+        if gr is not g:
+            gr.destroy()
+    g.destroy()
+    return out
+
+
 # ---------------------------------------------------------------- reference arm (the oracle)
 def bench_reference(args, world, rank):
     if rank != 0:
@@ -549,6 +759,8 @@ def main():
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         out = bench_reference(args, world, rank)
+    elif args.which == "backward":
+        out = bench_backward(args, world, rank, local)
     else:
         out = bench_fvx(args, world, rank, local)
     if rank == 0 and out is not None:

@@ -1500,7 +1500,9 @@ void launch_wgrad_small(unsigned grid, cudaStream_t s, const void* x, const void
 // producer warps share the gathers of a stage (a warp's TMA instructions
 // issue one lane after another), one thread issues the MMAs, four warps the
 // atomics (with two accumulators, the atomics of a unit overlap the MMAs of
-// the next).  cin and cout multiples of 64.
+// the next).  cin and cout multiples of 8: a tile's last 64-channel atom may
+// reach past the rows' end, where the gather reads zeros, and those MMA rows
+// and columns are not written back.
 constexpr int kWgUnit = 4096;        // pairs per work unit
 constexpr int kWgProducerWarps = 4;  // warps 0-3 issue the gathers, warp 4 the MMAs, warps 5-8 the atomics
 constexpr int kWgMmaWarp = kWgProducerWarps;
@@ -1616,8 +1618,8 @@ __global__ void __launch_bounds__(kWgThreads, 1) k_conv_wgrad_tc(const __grid_co
     uint32_t ring_ph = 0;
     for (uint32_t v = blockIdx.x; v < nunits; v += (uint32_t)G) {
       const WgUnit u = wg_unit(h, a, v);
-      const int a_atoms = min(2, (a.cin - u.mt * 128) / 64);
-      const int b_atoms = min(4, (a.cout - u.nt * 256) / 64);
+      const int a_atoms = min(2, (a.cin - u.mt * 128 + 63) / 64);  // a partial atom reads zeros past cin
+      const int b_atoms = min(4, (a.cout - u.nt * 256 + 63) / 64);
       const uint32_t bytes = (uint32_t)(a_atoms + b_atoms) * (uint32_t)kWgAtom;
       const int nops = 16 * (a_atoms + b_atoms);
       const int nst = (int)((u.end - u.start + 63) / 64);
@@ -1701,7 +1703,7 @@ __global__ void __launch_bounds__(kWgThreads, 1) k_conv_wgrad_tc(const __grid_co
       for (uint32_t v = blockIdx.x; v < nunits; v += (uint32_t)G, ++i) {
         const WgUnit u = wg_unit(h, a, v);
         const int nst = (int)((u.end - u.start + 63) / 64);
-        const uint32_t idesc = idesc_bf16_mn(128, 64 * min(4, (a.cout - u.nt * 256) / 64));
+        const uint32_t idesc = idesc_bf16_mn(128, 64 * min(4, (a.cout - u.nt * 256 + 63) / 64));
         const int b = i & 1;
         if (i >= 2) mbar_wait(smem_u32(&h.acc_empty[b]), (uint32_t)(((i >> 1) - 1) & 1), status);
         tc_fence_after();
@@ -1735,7 +1737,8 @@ __global__ void __launch_bounds__(kWgThreads, 1) k_conv_wgrad_tc(const __grid_co
     for (uint32_t v = blockIdx.x; v < nunits; v += (uint32_t)G, ++i) {
       const WgUnit u = wg_unit(h, a, v);
       const int b = i & 1;
-      const int ncols = 64 * min(4, (a.cout - u.nt * 256) / 64);
+      const int ncols = 64 * min(4, (a.cout - u.nt * 256 + 63) / 64);  // MMA columns
+      const int nreal = min(256, a.cout - u.nt * 256);                   // of them output channels
       mbar_wait(smem_u32(&h.acc_full[b]), (uint32_t)((i >> 1) & 1), status);
       tc_fence_after();
       const int ci = u.mt * 128 + row;
@@ -1744,9 +1747,10 @@ __global__ void __launch_bounds__(kWgThreads, 1) k_conv_wgrad_tc(const __grid_co
       for (int c = 0; c < ncols; c += 16) {
         uint32_t r[16];
         tmem_ld16(trow + (uint32_t)c, r);
-        if (ci < a.cin) {
+        if (ci < a.cin && c < nreal) {  // nreal is a multiple of 8
 #pragma unroll
-          for (int j = 0; j < 16; ++j) atomicAdd(dst + c + j, __uint_as_float(r[j]));
+          for (int j = 0; j < 16; ++j)
+            if (j < 8 || c + 8 < nreal) atomicAdd(dst + c + j, __uint_as_float(r[j]));
         }
       }
       tc_fence_before();
@@ -2163,8 +2167,11 @@ extern "C" fvx_status fvx_sparse_conv_wgrad(fvx_grid gin, fvx_grid gout, fvx_kma
   int dev = 0, sms = 0;
   FVX_CUDA(cudaGetDevice(&dev));
   FVX_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-  EncodeTiledFn enc = (dt == FVX_BF16 && cin % 64 == 0 && cout % 64 == 0 && gin->n_active > 0 && gout->n_active > 0 &&
-                       (((uintptr_t)feats | (uintptr_t)dout) & 15u) == 0)
+  // tensor cores for bf16 unless the layer is narrow enough for the register
+  // kernel below
+  const bool narrow = cin * cout <= 1024 && cin + cout <= 64;
+  EncodeTiledFn enc = (dt == FVX_BF16 && !narrow && cin % 8 == 0 && cout % 8 == 0 && gin->n_active > 0 &&
+                       gout->n_active > 0 && (((uintptr_t)feats | (uintptr_t)dout) & 15u) == 0)
                           ? encode_tiled()
                           : nullptr;
   if (enc) {
@@ -2190,7 +2197,7 @@ extern "C" fvx_status fvx_sparse_conv_wgrad(fvx_grid gin, fvx_grid gout, fvx_kma
     wa.mt = (int)((cin + 127) / 128);
     wa.nt = (int)((cout + 255) / 256);
     wa.b_off = 2 * kWgAtom;
-    wa.stage_bytes = wa.b_off + kWgAtom * (int)std::min<int64_t>(4, cout / 64);
+    wa.stage_bytes = wa.b_off + kWgAtom * (int)std::min<int64_t>(4, (cout + 63) / 64);
     const int head = (int)sizeof(WgradHead);
     wa.stages = std::min(kWgMaxStages, (224 * 1024 - 1024 - 16384 - head) / wa.stage_bytes);
     const size_t smem = 1024 + (size_t)wa.stages * wa.stage_bytes + 16384 + head;
@@ -2201,7 +2208,7 @@ extern "C" fvx_status fvx_sparse_conv_wgrad(fvx_grid gin, fvx_grid gout, fvx_kma
     }
     return check_launch("conv_wgrad_tc");
   }
-  if (cin * cout <= 1024 && cin + cout <= 64) {
+  if (narrow) {
     const unsigned grid = (unsigned)sms * 4;  // 4 blocks of 4 warps per SM (128 registers a thread)
     LaunchScope ls("conv_wgrad_small", s);
     if (dt == FVX_F32)
