@@ -978,7 +978,7 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tma(const __grid_
 
 // ============================================================== bf16, leaf-densified
 // Submanifold (stride 1) convolution one output leaf at a time, after the
-// "leaf" backend of the fVDB paper (Sparse-convolution operators): the input
+// "leaf" backend of the fVDB reading notes (Sparse-convolution operators): the input
 // features around the leaf (its 8^3 voxels plus a one-voxel shell, 10^3
 // positions, zeros where no input voxel is active) are staged densely in
 // shared memory, and every offset of the 3x3x3 stencil becomes a dense GEMM

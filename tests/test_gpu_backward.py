@@ -9,7 +9,7 @@ fp32 inputs run exact fp32 FFMA, 1e-5 * sum|x*dy| per element; bf16 inputs
 (the oracle is fed the same bf16-rounded values) run the tensor cores with
 fp32 accumulation when both channel counts are multiples of 64 (otherwise
 fp32 FFMA), and meet the bf16 bound 2e-3 * sum|x*dy|.  Training computes its gradients through the pair-list
-backend ("fVDB" paper, Limitations and future work)."""
+backend ("fVDB" reading notes, Limitations and future work)."""
 import numpy as np
 import pytest
 

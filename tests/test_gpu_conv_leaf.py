@@ -1,4 +1,4 @@
-"""The leaf-densified bf16 convolution (fVDB paper, "Sparse-convolution
+"""The leaf-densified bf16 convolution (fVDB reading notes, "Sparse-convolution
 operators": the leaf backend densifies each 8^3 leaf plus a one-voxel halo in
 shared memory and runs the stencil as dense tensor-core GEMMs).
 
