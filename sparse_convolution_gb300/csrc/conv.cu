@@ -1021,6 +1021,7 @@ struct LeafConvArgs {
   uint32_t* status;
   int64_t n_leaf_out;
   int cin, cout, out_bf16, tmem_cols;
+  int cout_store;               // output columns written (cout is the MMA N)
   int tile_cols;                // TMEM columns per M-tile accumulator (multiple of 32)
   int halo_bytes, w_bytes;      // shared-memory regions (multiples of 1024)
 };
@@ -1251,6 +1252,7 @@ __global__ void __launch_bounds__(kLeafThreads, G8 == 1 ? 2 : 1) k_conv_leaf(con
     // output position per thread in each of the 4 tiles
     const int quarter = warp & 3, m = quarter * 32 + lane;
     const int yl = m >> 6, xq = (m >> 3) & 7, z = m & 7;
+    const int cs = a.cout_store;
     int i = 0;
     for (int64_t L = blockIdx.x; L < nL; L += G, ++i) {
       const int b = i & 1;
@@ -1269,7 +1271,8 @@ __global__ void __launch_bounds__(kLeafThreads, G8 == 1 ? 2 : 1) k_conv_leaf(con
         for (int c = 0; c < cout; c += 16) {
           uint32_t v[16];
           tmem_ld16(trow + (uint32_t)c, v);
-          if (!act) continue;
+          const int ncol = min(16, cs - c);  // 16, 8 (cout_store an odd multiple of 8) or none
+          if (!act || ncol <= 0) continue;
           if (a.out_bf16) {
             uint4 v0, v1;
             v0.x = pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1]));
@@ -1280,13 +1283,17 @@ __global__ void __launch_bounds__(kLeafThreads, G8 == 1 ? 2 : 1) k_conv_leaf(con
             v1.y = pack_bf16x2(__uint_as_float(v[10]), __uint_as_float(v[11]));
             v1.z = pack_bf16x2(__uint_as_float(v[12]), __uint_as_float(v[13]));
             v1.w = pack_bf16x2(__uint_as_float(v[14]), __uint_as_float(v[15]));
-            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.y) + q * cout + c);
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.y) + q * cs + c);
             dst[0] = v0;
-            dst[1] = v1;
+            if (ncol == 16) dst[1] = v1;
           } else {
-            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<float*>(a.y) + q * cout + c);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) dst[e] = make_uint4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<float*>(a.y) + q * cs + c);
+            dst[0] = make_uint4(v[0], v[1], v[2], v[3]);
+            dst[1] = make_uint4(v[4], v[5], v[6], v[7]);
+            if (ncol == 16) {
+              dst[2] = make_uint4(v[8], v[9], v[10], v[11]);
+              dst[3] = make_uint4(v[12], v[13], v[14], v[15]);
+            }
           }
         }
       }
@@ -1372,16 +1379,18 @@ __global__ void __launch_bounds__(256) k_conv_wgrad(const T* __restrict__ x, con
 
 // Weight gradient for narrow layers (cin * cout <= 1024, cin + cout <= 64),
 // fp32 FFMA.  A warp owns runs of up to kWsRun pairs of one list and keeps
-// the whole cin x cout partial in registers (lane l holds entries l, l + 32,
-// ..., J of them); 32 pairs at a time are staged in shared memory as fp32
-// rows [x | dy].  When both rows are whole 16-byte pieces the warp copies
-// the 32 pairs' pieces with one 16-byte load per lane and piece (the lanes of
-// a row read it together); otherwise each lane copies its own pair element
-// by element.  Every lane then walks the 32 staged pairs, and the run's
-// partial is added to dW with one atomic per entry.
+// the whole cin x cout partial in registers, J = ceil(cin*cout / 32) entries
+// per lane; 32 pairs at a time are staged in shared memory as fp32 rows
+// [x | dy] (dy from a 16-byte-aligned column).  When both rows are whole
+// 16-byte pieces the warp copies the 32 pairs' pieces with one 16-byte load
+// per lane and piece; otherwise each lane copies its own pair element by
+// element.  When cout is a multiple of J (and J of 4) a lane's J entries are
+// one input channel and J consecutive output channels, read per pair as one
+// scalar and J/4 16-byte loads; otherwise entry l + 32 j per lane, two scalar
+// loads per entry.  The run's partial is added to dW with one atomic per entry.
 constexpr int kWsRun = 2048;
 constexpr int kWsWarps = 4;
-constexpr int kWsRow = 65;  // staged row pitch in floats (cin + cout <= 64, odd against bank conflicts)
+constexpr int kWsRow = 68;  // staged row pitch in floats: x at 0, dy at round4(cin), <= 67
 
 __device__ __forceinline__ void unpack16(const uint4 v, float* d, float) {
   d[0] = __uint_as_float(v.x);
@@ -1398,13 +1407,13 @@ __device__ __forceinline__ void unpack16(const uint4 v, float* d, __nv_bfloat16)
   }
 }
 
-template <typename T, int J>
+template <typename T, int J, bool kRowMap>
 __global__ void __launch_bounds__(kWsWarps * 32) k_conv_wgrad_small(const T* __restrict__ x, const T* __restrict__ dy,
                                                                     const int32_t* __restrict__ in_idx,
                                                                     const int32_t* __restrict__ out_idx,
                                                                     const uint32_t* __restrict__ dtot, int cin,
                                                                     int cout, int vec_ok, float* __restrict__ dW) {
-  __shared__ float buf[kWsWarps][32][kWsRow];
+  __shared__ __align__(16) float buf[kWsWarps][32][kWsRow];
   __shared__ uint32_t off[28], rcum[28];
   constexpr int kPer = 16 / (int)sizeof(T);  // elements per 16-byte piece
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1420,14 +1429,20 @@ __global__ void __launch_bounds__(kWsWarps * 32) k_conv_wgrad_small(const T* __r
   }
   __syncthreads();
   const int E = cin * cout;
+  const int xo = (cin + 3) & ~3;  // staged column of dy[0]
   const bool vec = vec_ok && cin % kPer == 0 && cout % kPer == 0;  // vec_ok: both arrays 16-byte aligned
   const int px = cin / kPer, pr = (cin + cout) / kPer;  // pieces of x, of the whole staged row
-  int eci[J], eco[J];  // this lane's entries (past E: read valid columns, never added)
+  int eci[kRowMap ? 1 : J], eco[kRowMap ? 1 : J];
+  if (kRowMap) {  // entries lane*J .. lane*J + J-1: channel ci, outputs co0 ..
+    eci[0] = (lane * J) / cout;
+    eco[0] = xo + (lane * J) % cout;
+  } else {  // entries lane + 32 j (past E: read valid columns, never added)
 #pragma unroll
-  for (int j = 0; j < J; ++j) {
-    const int e = lane + 32 * j;
-    eci[j] = e < E ? e / cout : 0;
-    eco[j] = e < E ? cin + e % cout : cin;
+    for (int j = 0; j < (kRowMap ? 1 : J); ++j) {
+      const int e = lane + 32 * j;
+      eci[j] = e < E ? e / cout : 0;
+      eco[j] = e < E ? xo + e % cout : xo;
+    }
   }
   float (*b)[kWsRow] = buf[warp];
   const uint32_t nruns = rcum[27];
@@ -1438,38 +1453,66 @@ __global__ void __launch_bounds__(kWsWarps * 32) k_conv_wgrad_small(const T* __r
     float acc[J];
 #pragma unroll
     for (int j = 0; j < J; ++j) acc[j] = 0.f;
+    // pair indices one batch ahead (their load latency overlaps this batch)
+    int pn = a0 + (uint32_t)lane < a1 ? __ldg(in_idx + a0 + lane) : 0;
+    int qn = a0 + (uint32_t)lane < a1 ? __ldg(out_idx + a0 + lane) : 0;
     for (uint32_t e0 = a0; e0 < a1; e0 += 32) {
       const uint32_t e = e0 + (uint32_t)lane;
       const int np = (int)min(32u, a1 - e0);
-      const int p = e < a1 ? __ldg(in_idx + e) : 0, q = e < a1 ? __ldg(out_idx + e) : 0;
+      const int p = pn, q = qn;
+      const uint32_t en = e + 32u;
+      pn = en < a1 ? __ldg(in_idx + en) : 0;
+      qn = en < a1 ? __ldg(out_idx + en) : 0;
       if (vec) {
         for (int k = lane; k < 32 * pr; k += 32) {
           const int pp = k / pr, piece = k - pp * pr;
           // every lane runs pr iterations (32 * pr pieces), so the warp is converged here
           const int pi = __shfl_sync(0xffffffffu, p, pp), qi = __shfl_sync(0xffffffffu, q, pp);
           if (pp < np) {
-            const T* src = piece < px ? x + (int64_t)pi * cin + piece * kPer : dy + (int64_t)qi * cout + (piece - px) * kPer;
+            const bool isx = piece < px;
+            const T* src = isx ? x + (int64_t)pi * cin + piece * kPer : dy + (int64_t)qi * cout + (piece - px) * kPer;
             float v[8];
             unpack16(__ldg(reinterpret_cast<const uint4*>(src)), v, T());
+            const int col = isx ? piece * kPer : xo + (piece - px) * kPer;
 #pragma unroll
-            for (int c = 0; c < kPer; ++c) b[pp][piece * kPer + c] = v[c];
+            for (int c = 0; c < kPer; ++c) b[pp][col + c] = v[c];
           }
         }
       } else if (e < a1) {
         for (int c = 0; c < cin; ++c) b[lane][c] = to_f32(x[(int64_t)p * cin + c]);
-        for (int c = 0; c < cout; ++c) b[lane][cin + c] = to_f32(dy[(int64_t)q * cout + c]);
+        for (int c = 0; c < cout; ++c) b[lane][xo + c] = to_f32(dy[(int64_t)q * cout + c]);
       }
       __syncwarp();
-      for (int pp = 0; pp < np; ++pp) {
+      if (kRowMap) {
+        for (int pp = 0; pp < np; ++pp) {
+          const float xv = b[pp][eci[0]];
 #pragma unroll
-        for (int j = 0; j < J; ++j) acc[j] = fmaf(b[pp][eci[j]], b[pp][eco[j]], acc[j]);
+          for (int j = 0; j < J; j += 4) {
+            const float4 g = *reinterpret_cast<const float4*>(&b[pp][eco[0] + j]);
+            acc[j] = fmaf(xv, g.x, acc[j]);
+            acc[j + 1] = fmaf(xv, g.y, acc[j + 1]);
+            acc[j + 2] = fmaf(xv, g.z, acc[j + 2]);
+            acc[j + 3] = fmaf(xv, g.w, acc[j + 3]);
+          }
+        }
+      } else {
+        for (int pp = 0; pp < np; ++pp) {
+#pragma unroll
+          for (int j = 0; j < J; ++j) acc[j] = fmaf(b[pp][eci[j]], b[pp][eco[j]], acc[j]);
+        }
       }
       __syncwarp();
     }
+    if (kRowMap) {
+      float* dst = dW + (size_t)s * E + lane * J;
 #pragma unroll
-    for (int j = 0; j < J; ++j) {
-      const int e = lane + 32 * j;
-      if (e < E) atomicAdd(dW + (size_t)s * E + e, acc[j]);
+      for (int j = 0; j < J; ++j) atomicAdd(dst + j, acc[j]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < J; ++j) {
+        const int e = lane + 32 * j;
+        if (e < E) atomicAdd(dW + (size_t)s * E + e, acc[j]);
+      }
     }
   }
 }
@@ -1477,13 +1520,22 @@ __global__ void __launch_bounds__(kWsWarps * 32) k_conv_wgrad_small(const T* __r
 template <typename T>
 void launch_wgrad_small(unsigned grid, cudaStream_t s, const void* x, const void* dy, const int32_t* in_idx,
                         const int32_t* out_idx, const uint32_t* dtot, int cin, int cout, float* dW) {
-  const int J = (cin * cout + 31) / 32;
-  auto kern = J <= 1 ? k_conv_wgrad_small<T, 1>
-              : J <= 2 ? k_conv_wgrad_small<T, 2>
-              : J <= 4 ? k_conv_wgrad_small<T, 4>
-              : J <= 8 ? k_conv_wgrad_small<T, 8>
-              : J <= 16 ? k_conv_wgrad_small<T, 16>
-                        : k_conv_wgrad_small<T, 32>;
+  const int E = cin * cout, J = (E + 31) / 32;
+  // entries by row: every lane owns J (a multiple of 4) consecutive outputs of one channel
+  const bool rowmap = E % 32 == 0 && J % 4 == 0 && cout % J == 0;
+  decltype(&k_conv_wgrad_small<T, 1, false>) kern;
+  if (rowmap)
+    kern = J == 4 ? k_conv_wgrad_small<T, 4, true>
+           : J == 8 ? k_conv_wgrad_small<T, 8, true>
+           : J == 16 ? k_conv_wgrad_small<T, 16, true>
+                     : k_conv_wgrad_small<T, 32, true>;
+  else
+    kern = J <= 1 ? k_conv_wgrad_small<T, 1, false>
+           : J <= 2 ? k_conv_wgrad_small<T, 2, false>
+           : J <= 4 ? k_conv_wgrad_small<T, 4, false>
+           : J <= 8 ? k_conv_wgrad_small<T, 8, false>
+           : J <= 16 ? k_conv_wgrad_small<T, 16, false>
+                     : k_conv_wgrad_small<T, 32, false>;
   const int vec_ok = (((uintptr_t)x | (uintptr_t)dy) & 15u) == 0 ? 1 : 0;
   kern<<<grid, kWsWarps * 32, 0, s>>>((const T*)x, (const T*)dy, in_idx, out_idx, dtot, cin, cout, vec_ok, dW);
 }
@@ -1494,16 +1546,19 @@ void launch_wgrad_small(unsigned grid, cudaStream_t s, const void* x, const void
 // tile::gather4 brings (one pair per 128-byte shared-memory row, 64 channels
 // of x or dy) already form the MN-major operand layout: 64 channels along a
 // swizzled 128-byte row, pairs (K) down the rows, 8-row groups 1024 bytes
-// apart.  A work unit is up to kWgUnit pairs of one list for one tile of
-// 128 input x up to 256 output channels; its fp32 accumulator lives in tensor
-// memory and is added to dW with one atomic per entry at the end.  Four
+// apart.  A work unit is the pairs of one list whose outputs fall in a run of
+// kWgTiles conv tiles (128 outputs each), for one tile of 128 input x up to
+// 256 output channels; its fp32 accumulator lives in tensor memory and is
+// added to dW with one atomic per entry at the end.  Units go output run
+// first, list second, so the blocks running at any moment gather rows of one
+// region of the grid and the rows stay in L2 across the 27 lists.  Four
 // producer warps share the gathers of a stage (a warp's TMA instructions
 // issue one lane after another), one thread issues the MMAs, four warps the
 // atomics (with two accumulators, the atomics of a unit overlap the MMAs of
 // the next).  cin and cout multiples of 8: a tile's last 64-channel atom may
 // reach past the rows' end, where the gather reads zeros, and those MMA rows
 // and columns are not written back.
-constexpr int kWgUnit = 4096;        // pairs per work unit
+constexpr int kWgTiles = 32;         // conv tiles (of 128 outputs) per work unit
 constexpr int kWgProducerWarps = 4;  // warps 0-3 issue the gathers, warp 4 the MMAs, warps 5-8 the atomics
 constexpr int kWgMmaWarp = kWgProducerWarps;
 constexpr int kWgThreads = (kWgProducerWarps + 5) * 32;
@@ -1515,7 +1570,8 @@ struct alignas(128) WgradArgs {
   CUtensorMap tmy;  // dy [n_out][cout] bf16, box {64, 1}, 128-byte swizzle
   const int32_t* in_idx;
   const int32_t* out_idx;
-  const uint32_t* dtot;  // list offsets [28]
+  const uint32_t* tile_start;  // [27 * ntiles + 1]: start of each (list, tile) segment
+  int64_t ntiles;
   float* dW;
   uint32_t* status;
   int cin, cout, n_in, n_out;
@@ -1525,8 +1581,6 @@ struct alignas(128) WgradArgs {
 
 struct WgradHead {
   unsigned long long full[kWgMaxStages], empty[kWgMaxStages], acc_full[2], acc_empty[2];
-  uint32_t off[28];   // list offsets
-  uint32_t ucum[28];  // units before list s
   uint32_t tmem_base;
 };
 
@@ -1535,17 +1589,20 @@ struct WgUnit {
   uint32_t start, end;
 };
 
-__device__ __forceinline__ WgUnit wg_unit(const WgradHead& h, const WgradArgs& a, uint32_t v) {
+// Unit v: channel tile fastest, then list, then output run.  Every role
+// decodes the same sequence and skips the same empty units.
+__device__ __forceinline__ WgUnit wg_unit(const WgradArgs& a, uint32_t v) {
   const uint32_t tiles = (uint32_t)(a.mt * a.nt);
-  const uint32_t tile = v % tiles, cu = v / tiles;
-  int s = 0;
-  while (s < 26 && h.ucum[s + 1] <= cu) ++s;
+  const uint32_t tile = v % tiles, sr = v / tiles;
+  const int s = (int)(sr % 27u);
+  const int64_t r = sr / 27u;
+  const int64_t t0 = r * kWgTiles, t1 = min(a.ntiles, t0 + kWgTiles);
   WgUnit u;
   u.s = s;
   u.mt = (int)(tile / (uint32_t)a.nt);
   u.nt = (int)(tile % (uint32_t)a.nt);
-  u.start = h.off[s] + (cu - h.ucum[s]) * (uint32_t)kWgUnit;
-  u.end = min(u.start + (uint32_t)kWgUnit, h.off[s + 1]);
+  u.start = __ldg(a.tile_start + (int64_t)s * a.ntiles + t0);
+  u.end = __ldg(a.tile_start + (int64_t)s * a.ntiles + t1);
   return u;
 }
 
@@ -1588,27 +1645,17 @@ __global__ void __launch_bounds__(kWgThreads, 1) k_conv_wgrad_tc(const __grid_co
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (tid < 28) h.off[tid] = __ldg(a.dtot + tid);
   if (warp == kWgMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&h.tmem_base)),
                  "r"(512)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  __syncthreads();
-  if (tid == 0) {
-    uint32_t c = 0;
-    for (int s = 0; s < 27; ++s) {
-      h.ucum[s] = c;
-      c += (h.off[s + 1] - h.off[s] + (uint32_t)kWgUnit - 1) / (uint32_t)kWgUnit;
-    }
-    h.ucum[27] = c;
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = h.tmem_base;
-  const uint32_t nunits = h.ucum[27] * (uint32_t)(a.mt * a.nt);
+  const uint32_t nunits = (uint32_t)((a.ntiles + kWgTiles - 1) / kWgTiles) * 27u * (uint32_t)(a.mt * a.nt);
 
   if (warp < kWgProducerWarps) {
     // ---------------- producers: row indices (every producer warp loads all
@@ -1617,7 +1664,8 @@ __global__ void __launch_bounds__(kWgThreads, 1) k_conv_wgrad_tc(const __grid_co
     int ring_sb = 0;
     uint32_t ring_ph = 0;
     for (uint32_t v = blockIdx.x; v < nunits; v += (uint32_t)G) {
-      const WgUnit u = wg_unit(h, a, v);
+      const WgUnit u = wg_unit(a, v);
+      if (u.end == u.start) continue;
       const int a_atoms = min(2, (a.cin - u.mt * 128 + 63) / 64);  // a partial atom reads zeros past cin
       const int b_atoms = min(4, (a.cout - u.nt * 256 + 63) / 64);
       const uint32_t bytes = (uint32_t)(a_atoms + b_atoms) * (uint32_t)kWgAtom;
@@ -1700,8 +1748,9 @@ __global__ void __launch_bounds__(kWgThreads, 1) k_conv_wgrad_tc(const __grid_co
       int m_sb = 0;
       uint32_t m_ph = 0, m_off = 0;
       int i = 0;
-      for (uint32_t v = blockIdx.x; v < nunits; v += (uint32_t)G, ++i) {
-        const WgUnit u = wg_unit(h, a, v);
+      for (uint32_t v = blockIdx.x; v < nunits; v += (uint32_t)G) {
+        const WgUnit u = wg_unit(a, v);
+        if (u.end == u.start) continue;
         const int nst = (int)((u.end - u.start + 63) / 64);
         const uint32_t idesc = idesc_bf16_mn(128, 64 * min(4, (a.cout - u.nt * 256 + 63) / 64));
         const int b = i & 1;
@@ -1726,6 +1775,7 @@ __global__ void __launch_bounds__(kWgThreads, 1) k_conv_wgrad_tc(const __grid_co
           }
         }
         umma_commit(smem_u32(&h.acc_full[b]));
+        ++i;
       }
     }
     __syncwarp();
@@ -1734,8 +1784,9 @@ __global__ void __launch_bounds__(kWgThreads, 1) k_conv_wgrad_tc(const __grid_co
     // 32 q .. 32 q + 31 of the tile; atomics into dW
     const int quarter = warp & 3, row = quarter * 32 + lane;
     int i = 0;
-    for (uint32_t v = blockIdx.x; v < nunits; v += (uint32_t)G, ++i) {
-      const WgUnit u = wg_unit(h, a, v);
+    for (uint32_t v = blockIdx.x; v < nunits; v += (uint32_t)G) {
+      const WgUnit u = wg_unit(a, v);
+      if (u.end == u.start) continue;
       const int b = i & 1;
       const int ncols = 64 * min(4, (a.cout - u.nt * 256 + 63) / 64);  // MMA columns
       const int nreal = min(256, a.cout - u.nt * 256);                   // of them output channels
@@ -1756,6 +1807,7 @@ __global__ void __launch_bounds__(kWgThreads, 1) k_conv_wgrad_tc(const __grid_co
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&h.acc_empty[b]));
+      ++i;
     }
   }
   tc_fence_before();
@@ -1778,14 +1830,17 @@ __global__ void k_transpose_w(const T* __restrict__ W, int cin, int cout, int co
   wt[e] = co < cout ? W[s * (int64_t)cin * cout + (int64_t)ci * cout + co] : T(0.0f);
 }
 
-// W [27][n][k] -> [27][np][k] with rows n .. np-1 zero (bf16).
-__global__ void k_pad_rows(const __nv_bfloat16* __restrict__ W, int n, int np, int k, __nv_bfloat16* __restrict__ out) {
+// W [27][n][k] -> [27][np][k] with rows n .. np-1 zero (bf16); mirror: slot
+// s of the output takes slot 26 - s of W.
+__global__ void k_pad_rows(const __nv_bfloat16* __restrict__ W, int n, int np, int k, int mirror,
+                           __nv_bfloat16* __restrict__ out) {
   const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t per = (int64_t)np * k;
   if (e >= 27 * per) return;
   const int64_t s = e / per, r = e - s * per;
+  const int64_t sw = mirror ? 26 - s : s;
   const int row = (int)(r / k), col = (int)(r - (int64_t)row * k);
-  out[e] = row < n ? W[(s * n + row) * (int64_t)k + col] : __float2bfloat16(0.0f);
+  out[e] = row < n ? W[(sw * n + row) * (int64_t)k + col] : __float2bfloat16(0.0f);
 }
 
 // cuTensorMapEncodeTiled, taken from the driver through the runtime (no link
@@ -1833,12 +1888,16 @@ thread_local int t_last_algo = FVX_CONV_AUTO;
 
 // Leaf-densified launch: one block per output leaf, as many blocks per SM as
 // shared memory allows but no more than the tensor memory holds at once.
-fvx_status launch_conv_leaf(const char* who, fvx_grid gin, fvx_kmap m, fvx_dtype dt, const void* feats, int64_t cin,
-                            int64_t cout, void* out, const __nv_bfloat16* wt, uint32_t* status, cudaStream_t s) {
+// nbr: the map's table of the 27 input leaves around each output leaf;
+// wt: [27][cout][cin] (cout a multiple of 16, the MMA's N), of which the first
+// cout_store output columns are written.
+fvx_status launch_conv_leaf(const char* who, fvx_grid gin, fvx_kmap m, const int32_t* nbr, fvx_dtype dt,
+                            const void* feats, int64_t cin, int64_t cout, int64_t cout_store, void* out,
+                            const __nv_bfloat16* wt, uint32_t* status, cudaStream_t s) {
   const fvx_grid_s* go = m->gout;
   LeafConvArgs a;
   a.in_rec = gin->leaf_rec;
-  a.nbr = m->leaf_nbr;
+  a.nbr = nbr;
   a.out_origin = go->leaf_origin;
   a.out_batch = go->leaf_batch;
   a.out_rec = go->leaf_rec;
@@ -1849,6 +1908,7 @@ fvx_status launch_conv_leaf(const char* who, fvx_grid gin, fvx_kmap m, fvx_dtype
   a.n_leaf_out = go->n_leaf;
   a.cin = (int)cin;
   a.cout = (int)cout;
+  a.cout_store = (int)cout_store;
   a.out_bf16 = (dt == FVX_BF16_OUT_BF16) ? 1 : 0;
   a.tile_cols = (int)((cout + 31) & ~(int64_t)31);  // accumulator columns per M tile
   int cols = 32;
@@ -1898,7 +1958,7 @@ fvx_status launch_conv_bf16(const char* who, fvx_grid gin, fvx_kmap m, fvx_dtype
   const fvx_grid_s* go = m->gout;
   const bool dense_leaves = go->n_leaf > 0 && (double)go->n_active >= 0.2 * 512.0 * (double)go->n_leaf;
   if (leaf_ok && (algo == FVX_CONV_LEAF || (algo == FVX_CONV_AUTO && dense_leaves)))
-    return launch_conv_leaf(who, gin, m, dt, feats, cin, cout, out, wt, status, s);
+    return launch_conv_leaf(who, gin, m, m->leaf_nbr, dt, feats, cin, cout, cout, out, wt, status, s);
   ConvArgs a;
   a.x = (const __nv_bfloat16*)feats;
   a.wt = wt;
@@ -2187,7 +2247,8 @@ extern "C" fvx_status fvx_sparse_conv_wgrad(fvx_grid gin, fvx_grid gout, fvx_kma
                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, "fvx_sparse_conv_wgrad"));
     wa.in_idx = m->in_idx;
     wa.out_idx = m->out_idx;
-    wa.dtot = m->dtot;
+    wa.tile_start = m->tile_start;
+    wa.ntiles = m->n_tiles;
     wa.dW = dW;
     wa.status = status;
     wa.cin = (int)cin;
@@ -2202,14 +2263,19 @@ extern "C" fvx_status fvx_sparse_conv_wgrad(fvx_grid gin, fvx_grid gout, fvx_kma
     wa.stages = std::min(kWgMaxStages, (224 * 1024 - 1024 - 16384 - head) / wa.stage_bytes);
     const size_t smem = 1024 + (size_t)wa.stages * wa.stage_bytes + 16384 + head;
     FVX_CUDA(cudaFuncSetAttribute(k_conv_wgrad_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    const int64_t units = (m->n_tiles + kWgTiles - 1) / kWgTiles * 27 * wa.mt * wa.nt;
+    if (units >= (int64_t)UINT32_MAX) {
+      set_error("fvx_sparse_conv_wgrad: %lld work units exceed the 32-bit unit index", (long long)units);
+      return FVX_ERR_RANGE;
+    }
     {
       LaunchScope ls("conv_wgrad_tc", s);
-      k_conv_wgrad_tc<<<(unsigned)sms, kWgThreads, smem, s>>>(wa);
+      k_conv_wgrad_tc<<<(unsigned)std::min<int64_t>(units, sms), kWgThreads, smem, s>>>(wa);
     }
     return check_launch("conv_wgrad_tc");
   }
   if (narrow) {
-    const unsigned grid = (unsigned)sms * 4;  // 4 blocks of 4 warps per SM (128 registers a thread)
+    const unsigned grid = (unsigned)sms * 8;  // up to 6 resident blocks of 4 warps per SM (shared memory)
     LaunchScope ls("conv_wgrad_small", s);
     if (dt == FVX_F32)
       launch_wgrad_small<float>(grid, s, feats, dout, m->in_idx, m->out_idx, m->dtot, (int)cin, (int)cout, dW);
@@ -2295,6 +2361,37 @@ extern "C" fvx_status fvx_sparse_conv_dgrad(fvx_grid gin, fvx_grid gout, fvx_kma
     set_error("fvx_sparse_conv_dgrad: device status word unavailable");
     return FVX_ERR_CUDA;
   }
+  // Stride 1: dx[p] = sum_s dy[p - d_s] W[s]^T = sum_s dy[p + d_s] W[26 - s]^T,
+  // the leaf-densified convolution of dy with the slot-mirrored weights (W as
+  // stored is [N = cin][K = cout] per slot), over the transposed map's table
+  // of neighbouring leaves.  Same choice rule as the forward conv.
+  {
+    const int algo = g_conv_algo.load(std::memory_order_relaxed);
+    const int64_t cinp = (cin + 15) & ~(int64_t)15;
+    const fvx_grid_s* go = mt->gout;  // the grid dx lives on
+    const bool leaf_ok = mt->stride == 1 && mt->leaf_nbr_t != nullptr && (cout == 8 || cout == 16) &&
+                         cinp <= kLeafMaxCout;
+    const bool dense = go->n_leaf > 0 && (double)go->n_active >= 0.2 * 512.0 * (double)go->n_leaf;
+    if (algo == FVX_CONV_LEAF && !leaf_ok) {
+      set_error("fvx_sparse_conv_dgrad: the leaf-densified convolution needs stride 1, cout 8 or 16 and cin <= %d",
+                kLeafMaxCout);
+      return FVX_ERR_INVALID_ARG;
+    }
+    if (leaf_ok && (algo == FVX_CONV_LEAF || (algo == FVX_CONV_AUTO && dense))) {
+      Scratch scr(s);
+      __nv_bfloat16* wm = scr.get<__nv_bfloat16>((size_t)(27 * cinp * cout));
+      if (!wm) return FVX_ERR_ALLOC;
+      {
+        LaunchScope ls("conv_pad_w", s);
+        const int64_t n = 27 * cinp * cout;
+        k_pad_rows<<<(unsigned)((n + 255) / 256), 256, 0, s>>>((const __nv_bfloat16*)W, (int)cin, (int)cinp,
+                                                               (int)cout, 1, wm);
+      }
+      FVX_TRY(check_launch("conv_pad_w"));
+      return launch_conv_leaf("fvx_sparse_conv_dgrad", gout, mt, mt->leaf_nbr_t, dt, dout, cout, cinp, cin, dx, wm,
+                              status, s);
+    }
+  }
   if (cin % 16 == 0)
     return launch_conv_bf16("fvx_sparse_conv_dgrad", gout, mt, dt, dout, cout, cin, dx, (const __nv_bfloat16*)W,
                             status, s);
@@ -2306,7 +2403,8 @@ extern "C" fvx_status fvx_sparse_conv_dgrad(fvx_grid gin, fvx_grid gout, fvx_kma
   {
     LaunchScope ls("conv_pad_w", s);
     const int64_t n = 27 * cinp * cout;
-    k_pad_rows<<<(unsigned)((n + 255) / 256), 256, 0, s>>>((const __nv_bfloat16*)W, (int)cin, (int)cinp, (int)cout, wp);
+    k_pad_rows<<<(unsigned)((n + 255) / 256), 256, 0, s>>>((const __nv_bfloat16*)W, (int)cin, (int)cinp, (int)cout, 0,
+                                                           wp);
   }
   FVX_TRY(check_launch("conv_pad_w"));
   return launch_conv_bf16("fvx_sparse_conv_dgrad", gout, mt, dt, dout, cout, cin, dx, wp, status, s);

@@ -151,8 +151,11 @@ struct fvx_kmap_s {
   uint32_t* tile_start = nullptr;
   int64_t n_tiles = 0;
   // stride 1: for each output leaf, the input leaf at each of the 27 leaf
-  // offsets ((ex+1)*9 + (ey+1)*3 + ez+1, -1 if absent); null for stride 2
+  // offsets ((ex+1)*9 + (ey+1)*3 + ez+1, -1 if absent); null for stride 2.
+  // A forward map keeps it in leaf_nbr, a transposed one in leaf_nbr_t (the
+  // forward conv must not take a transposed map for a forward one).
   int32_t* leaf_nbr = nullptr;
+  int32_t* leaf_nbr_t = nullptr;
   const fvx_grid_s* gin = nullptr;
   const fvx_grid_s* gout = nullptr;
 };

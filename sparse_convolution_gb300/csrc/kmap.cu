@@ -491,7 +491,7 @@ fvx_status kernel_map_impl(const char* who, fvx_grid gin, fvx_grid gout, int32_t
   int32_t* nbr = nullptr;  // stride 1: input-leaf slot table written by the count pass
   if (bitpar) {
     nbr = (int32_t*)((char*)m->block + o_nbr);
-    if (!transposed) m->leaf_nbr = nbr;  // the leaf-densified conv takes forward maps only
+    (transposed ? m->leaf_nbr_t : m->leaf_nbr) = nbr;  // the forward conv's leaf path takes forward maps only
   }
   if (Lo > 0) {
     LaunchScope ls("kmap_count", s);

@@ -316,3 +316,63 @@ def test_wgrad_empty_input(cuda_device, grids):
     out = torch.full((27, 16, 16), 7.0, device="cuda")
     fvx.sparse_conv_wgrad(e, grids["gc"], km, x, dy, out=out)
     assert int((out != 0).sum()) == 0
+
+
+@pytest.fixture(scope="module")
+def dense_grid():
+    """A solid ball (radius 13, two batches, one shifted to negative
+    coordinates): leaves well above 20% occupied."""
+    r = np.arange(-14, 15)
+    c = np.stack(np.meshgrid(r, r, r, indexing="ij"), -1).reshape(-1, 3)
+    ball = c[(c ** 2).sum(1) <= 13 ** 2].astype(np.int32)
+    coords = np.concatenate([ball + 40, ball - 21])
+    offs = np.array([0, len(ball), 2 * len(ball)], np.int64)
+    rng = np.random.default_rng(3)
+    perm = np.concatenate([rng.permutation(len(ball)), len(ball) + rng.permutation(len(ball))])
+    coords = coords[perm]
+    g = G.gpu_grid(coords, offs)
+    og = oracle.Grid.build(coords, offs)
+    assert g.n_active >= 0.2 * 512 * g.n_leaf
+    return g, og
+
+
+@pytest.mark.parametrize("cin,cout", [(8, 16), (16, 16), (32, 8), (64, 16), (24, 8)])
+@pytest.mark.parametrize("algo", ["auto", "leaf", "gather"])
+def test_dgrad_leaf_densified(cuda_device, dense_grid, cin, cout, algo):
+    """Stride-1 input gradient on dense leaves: the leaf-densified kernel with
+    slot-mirrored weights (automatic choice or forced) and the pair-list
+    kernels give the oracle's result within the bf16 bound."""
+    import torch
+
+    import sparse_convolution_gb300 as fvx
+    from sparse_convolution_gb300 import synth
+
+    g, og = dense_grid
+    kt = fvx.KernelMap(g, g, 1, transposed=True)
+    okt = oracle.KernelMap(og, og, 1, transposed=True)
+    dy = torch.from_numpy(synth.features(71, g.n_active, cout)).cuda().bfloat16()
+    W = torch.from_numpy(synth.weights(72, cin, cout)).cuda().bfloat16()
+    fvx.set_conv_algo({"auto": fvx.FVX_CONV_AUTO, "leaf": fvx.FVX_CONV_LEAF, "gather": fvx.FVX_CONV_GATHER}[algo])
+    try:
+        dx = fvx.sparse_conv_dgrad(g, g, kt, dy, W)
+        fvx.device_status()
+        ran = fvx.last_conv_algo()
+    finally:
+        fvx.set_conv_algo(fvx.FVX_CONV_AUTO)
+    assert ran == (fvx.FVX_CONV_GATHER if algo == "gather" else fvx.FVX_CONV_LEAF)
+    ref, a = oracle.conv(okt, G.as_f64(dy), np.ascontiguousarray(G.as_f64(W).transpose(0, 2, 1)))
+    G.assert_conv_close(G.np_(dx.float()), ref, a, G.BF16_TOL)
+
+
+def test_forward_conv_refuses_leaf_on_transposed_map(cuda_device, dense_grid):
+    """A transposed map's leaf table serves the input gradient only: the
+    forward conv over a transposed map takes the pair-list kernels."""
+    import sparse_convolution_gb300 as fvx
+
+    g, og = dense_grid
+    kt = fvx.KernelMap(g, g, 1, transposed=True)
+    x, W = G.bf16_inputs(5, g.n_active, 16, 16)
+    y = fvx.sparse_conv(g, g, kt, x, W)
+    assert fvx.last_conv_algo() == fvx.FVX_CONV_GATHER
+    yo, ao = oracle.conv(oracle.KernelMap(og, og, 1, transposed=True), G.as_f64(x), G.as_f64(W))
+    G.assert_conv_close(G.np_(y.float()), yo, ao, G.BF16_TOL)
