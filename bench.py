@@ -144,7 +144,7 @@ def profiled_traffic(kernel, workload):
     import re
 
     src = {"conv_bf16_tc": "conv.cu", "conv_bf16_tma": "conv.cu", "conv_leaf": "conv.cu",
-           "kmap1_write": "kmap.cu"}.get(kernel)
+           "conv_wgrad_tc": "conv.cu", "kmap1_write": "kmap.cu"}.get(kernel)
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     if src is None or not os.path.exists(path):
         return None
@@ -661,7 +661,8 @@ def bench_backward(args, world, rank, local):
             peak = 152 * 128 * 2 * 2.07e9 / 1e12
             roofline = dict(bound="alu", achieved=round(ach, 3), peak=round(peak, 1), unit="TFLOP/s",
                             peak_source="derived: 152 SMs x 128 FP32 lanes x 2 x 2.07 GHz")
-        roofline.update(kernel=prof_kernel, frac=round(roofline["achieved"] / roofline["peak"], 4), traffic=None,
+        roofline.update(kernel=prof_kernel, frac=round(roofline["achieved"] / roofline["peak"], 4),
+                        traffic=profiled_traffic(prof_kernel, w["name"]) if len(mine) == 1 else None,
                         flops=int(wflops / max(1, prof_n // K)), avg_launch_ms=round(prof_ms / prof_n, 5),
                         launches_per_step=int(prof_n // K))
 
