@@ -327,31 +327,33 @@ __global__ void __launch_bounds__(kKmThreads) k_kmap1_write(GridDev gin, const i
     sw.hidx[h] = v;
   }
   __syncthreads();
-  // one warp per offset: per half word of an output slice, a ballot packs the
-  // pairs into a contiguous run of the list (coalesced stores)
+  // the neighbour words of every (offset, slice), as the count pass had them
+  if (tid < 27 * 8) sm.R[tid >> 3][tid & 7] = km1_word(sm, tid >> 3, tid & 7);
+  __syncthreads();
+  // one warp per offset: the pairs of slice x are the set bits of R[s][x], in
+  // output order; a lane's bits b = lane and lane + 32 go to their rank in R
+  // (coalesced runs, no ballots)
   const int warp = tid >> 5, lane = tid & 31;
-  const uint32_t lt = lanemask_lt();
   for (int s = warp; s < 27; s += kKmThreads / 32) {
     const int di = s / 9 - 1, dj = (s / 3) % 3 - 1, dk = s % 3 - 1;
     uint32_t e = starts[(int64_t)(mirror ? 26 - s : s) * n_out_leaf + lo];
     for (int x = 0; x < 8; ++x) {
+      const unsigned long long R = sm.R[s][x];
+      if (!R) continue;
       const unsigned long long om = sm.om[x];
-      if (!om) continue;
       const uint32_t qx = sm.qf + (x ? (uint32_t)((sm.opre9 >> (9 * (x - 1))) & 511ull) : 0u);
       const int hrow = (x + di + 1) * 100 + (dj + 1) * 10 + (dk + 1);
 #pragma unroll
       for (int hw = 0; hw < 2; ++hw) {
         const int b = hw * 32 + lane;  // y * 8 + z
-        const int32_t p = ((om >> b) & 1ull) ? sw.hidx[hrow + (b >> 3) * 10 + (b & 7)] : -1;
-        const bool has = p >= 0;
-        const uint32_t bal = __ballot_sync(0xffffffffu, has);
-        if (has) {
-          const uint32_t pos = e + __popc(bal & lt);
-          in_idx[pos] = p;
-          out_idx[pos] = (int32_t)(qx + (uint32_t)__popcll(om & ((1ull << b) - 1ull)));
+        if ((R >> b) & 1ull) {
+          const unsigned long long below = (1ull << b) - 1ull;
+          const uint32_t pos = e + (uint32_t)__popcll(R & below);
+          in_idx[pos] = sw.hidx[hrow + (b >> 3) * 10 + (b & 7)];
+          out_idx[pos] = (int32_t)(qx + (uint32_t)__popcll(om & below));
         }
-        e += __popc(bal);
       }
+      e += (uint32_t)__popcll(R);
     }
   }
 }
