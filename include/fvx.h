@@ -284,8 +284,13 @@ fvx_status fvx_sparse_conv_noalloc(fvx_grid gin, fvx_grid gout, fvx_kmap m, fvx_
  *     needs cout and cin multiples of 8 (cout <= 512, cin <= 256), dout, W
  *     and dx 16-byte aligned (cin not a multiple of 16: W is first copied
  *     into library scratch with zero rows up to the next multiple); FVX_F32
- *     any sizes >= 1 (it transposes W into library scratch first).  Runs the
- *     pair-list kernels. */
+ *     any sizes >= 1 (it transposes W into library scratch first).
+ * Kernels: bf16 stride 1 with cout 8 or 16, cin <= 64 and the grid of dx at
+ *     least 20% occupied per leaf (or FVX_CONV_LEAF set) runs the
+ *     leaf-densified kernel with the slot-mirrored weights (dx[p] = sum_s
+ *     dout[p + d_s] W[26 - s]^T); FVX_CONV_LEAF with any other shape fails
+ *     with FVX_ERR_INVALID_ARG; everything else runs the pair-list kernels
+ *     over mt.  Same error bound as fvx_sparse_conv. */
 fvx_status fvx_sparse_conv_dgrad(fvx_grid gin, fvx_grid gout, fvx_kmap mt, fvx_dtype dt, const void* dout,
                                  int64_t cout, const void* W, int64_t cin, void* dx, fvx_stream stream);
 
@@ -293,10 +298,15 @@ fvx_status fvx_sparse_conv_dgrad(fvx_grid gin, fvx_grid gout, fvx_kmap mt, fvx_d
  *   dW[s, ci, co] = sum_{(p,q) in list s} feats[p, ci] * dout[q, co]
  * feats device [gin.n_active, cin], dout device [gout.n_active, cout], both
  * fp32 (FVX_F32) or bf16 (FVX_BF16); dW device fp32 [27, cin, cout],
- * caller-allocated, fully overwritten.  Products and sums in fp32 (bf16
- * inputs are widened exactly); the summation order is not fixed (atomic
- * adds), so results may differ between runs in the last bits.
- * 1 <= cin, cout <= 65536.  Errors: FVX_ERR_INVALID_ARG. */
+ * caller-allocated, fully overwritten.  Kernels: cin * cout <= 1024 and
+ * cin + cout <= 64, fp32 FFMA with the partial in registers; other bf16
+ * layers with cin and cout multiples of 8, tcgen05 tensor cores (bf16
+ * products, fp32 accumulation in tensor memory; within 2e-3 * sum|x*dy|);
+ * the rest, tiled fp32 FFMA (fp32 inputs: within 1e-5 * sum|x*dy|).  Partial
+ * sums are added with fp32 atomics, so the summation order is not fixed and
+ * results may differ between runs in the last bits.
+ * 1 <= cin, cout <= 65536.  Errors: FVX_ERR_INVALID_ARG; FVX_ERR_RANGE past
+ * 2^32 tensor-core work units. */
 fvx_status fvx_sparse_conv_wgrad(fvx_grid gin, fvx_grid gout, fvx_kmap m, fvx_dtype dt, const void* feats,
                                  int64_t cin, const void* dout, int64_t cout, float* dW, fvx_stream stream);
 
