@@ -731,6 +731,7 @@ struct alignas(128) ConvTmaArgs {
   int chunk;   // channels per box row: 16, 32 or 64
   int layout;  // UMMA layout type of that swizzle: 6 (32 B), 4 (64 B), 2 (128 B)
   int n_in;    // feature rows; row index n_in reads as zeros
+  int ksteps;  // MMAs (16 channels of K each) per stage: 4 (K = 64) or 8 (K = 128)
 };
 
 __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tma(const __grid_constant__ ConvTmaArgs ta) {
@@ -741,7 +742,9 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tma(const __grid_
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = a.stages;
   const int chunk = ta.chunk, rowb = 2 * chunk;  // channels / bytes per box row
-  const int cps = 64 / chunk;                     // chunks per stage
+  const int ksteps = ta.ksteps;                   // 16-channel MMA steps per stage
+  const int cps = 16 * ksteps / chunk;            // chunks per stage
+  const uint32_t a_bytes = (uint32_t)(ksteps / 4) * kATileBytes;  // A region of a stage
   const int ncs = a.cin / chunk;                  // chunks per offset
   const uint32_t acc_cols = (uint32_t)a.tmem_cols;
   const int64_t G = gridDim.x;
@@ -781,7 +784,7 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tma(const __grid_
     const int32_t* const gout = a.out_idx;
     const uint32_t* const gts = a.tile_start;
     const int cout = a.cout, sbytes = a.stage_bytes, absent = ta.n_in;
-    const uint32_t stage_tx = (uint32_t)(kATileBytes + cout * 128);
+    const uint32_t stage_tx = a_bytes + (uint32_t)(cout * 32 * ksteps);
     const int nops_a = cps * 32;  // gather4 ops per stage; then cps weight boxes
     uint32_t* const status = a.status;
     int64_t kg = 0;
@@ -840,7 +843,10 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tma(const __grid_
     int total = __popc(h.tab[0].tor) * ncs;  // chunks of the tile
     load_segment(gts, ntiles, t + G, pt, sa, se);
     producer_bar();
-    if (pt == 0 && t < ntiles) publish_info(h, status, 0, h.tab[0], total * ppc);
+    // publish_info counts 8 pieces (64 channels) per stage; a 128-channel
+    // stage is two of those
+    const int pscale = 4 / (ksteps / 4) * ppc / 4;  // ppc, or ppc / 2 for 128-channel stages
+    if (pt == 0 && t < ntiles) publish_info(h, status, 0, h.tab[0], total * pscale);
     // A warp issues its TMA instructions one lane after another, so the ops
     // of a stage are spread over all producer warps: op = lane * 8 + warp
     // (gathers first, then the weight boxes).
@@ -862,7 +868,7 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tma(const __grid_
         }
         const uint32_t bar = smem_u32(&h.full[sb]);
         const uint32_t sA = smem_u32(sbase + (size_t)sb * sbytes);
-        const uint32_t sB = sA + kATileBytes;
+        const uint32_t sB = sA + a_bytes;
         if (op == 0) mbar_arrive_expect_tx(bar, stage_tx);
         if (op < nops_a) {
           const int j = op >> 5, r4 = op & 31;
@@ -892,7 +898,7 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tma(const __grid_
         table_end(h.tab[nb], t + G);
         total = __popc(h.tab[nb].tor) * ncs;
         producer_bar();
-        if (pt == 0) publish_info(h, status, i + 1, h.tab[nb], total * ppc);
+        if (pt == 0) publish_info(h, status, i + 1, h.tab[nb], total * pscale);
       }
       producer_bar();  // this tile's table is no longer read
     }
@@ -924,10 +930,10 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tma(const __grid_
       const int cout = a.cout;
       uint32_t* const status = a.status;
       const uint64_t adesc0 = sdesc_swz(smem_u32(sbase), layout, sbo);
-      const uint64_t bdesc0 = sdesc_swz(smem_u32(sbase) + kATileBytes, layout, sbo);
-      uint32_t aoff[4], boff[4];
+      const uint64_t bdesc0 = sdesc_swz(smem_u32(sbase) + a_bytes, layout, sbo);
+      uint32_t aoff[8], boff[8];
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
+      for (int kk = 0; kk < 8; ++kk) {
         const int e = 16 * kk, j = e / chunk;
         const uint32_t off = (uint32_t)((e - j * chunk) * 2);
         aoff[kk] = ((uint32_t)(j * kRows * rowb) + off) >> 4;
@@ -952,6 +958,12 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tma(const __grid_
           umma_bf16(d, ad + aoff[1], bd + boff[1], idesc, 1u);
           umma_bf16(d, ad + aoff[2], bd + boff[2], idesc, 1u);
           umma_bf16(d, ad + aoff[3], bd + boff[3], idesc, 1u);
+          if (ksteps == 8) {
+            umma_bf16(d, ad + aoff[4], bd + boff[4], idesc, 1u);
+            umma_bf16(d, ad + aoff[5], bd + boff[5], idesc, 1u);
+            umma_bf16(d, ad + aoff[6], bd + boff[6], idesc, 1u);
+            umma_bf16(d, ad + aoff[7], bd + boff[7], idesc, 1u);
+          }
           umma_commit(smem_u32(&h.empty[m_sb]));
           m_off += sunits;
           if (++m_sb == S) {
@@ -1997,7 +2009,15 @@ fvx_status launch_conv_bf16(const char* who, fvx_grid gin, fvx_kmap m, fvx_dtype
     a.w_resident = 0;
     a.w_bytes = 0;
     a.lag = 0;
-    a.stage_bytes = kATileBytes + (int)cout * 128;  // multiple of 2048
+    // K per stage: 128 channels (half as many stages: each stage carries a
+    // fixed cost in the producers and the MMA thread, measured 1.4x faster
+    // than 64-channel stages at cin 64-128), or 64 when a ring of 3 such
+    // stages does not fit or the stage's TMA operations (32 gathers and one
+    // weight box per chunk) would outnumber the 256 producer threads
+    // (16-channel chunks)
+    const int ops128 = (128 / ta.chunk) * 33;
+    ta.ksteps = ((224 * 1024 - head) / (2 * (kATileBytes + (int)cout * 128)) >= 3 && ops128 <= kProducers) ? 8 : 4;
+    a.stage_bytes = (ta.ksteps / 4) * (kATileBytes + (int)cout * 128);  // multiple of 2048
     a.stages = std::min((224 * 1024 - head) / a.stage_bytes, kMaxStages);
     if (a.stages < 3) {
       set_error("%s: cout %lld leaves fewer than 3 pipeline stages", who, (long long)cout);
