@@ -1574,8 +1574,7 @@ constexpr int kWgTiles = 32;         // conv tiles (of 128 outputs) per work uni
 constexpr int kWgProducerWarps = 4;  // warps 0-3 issue the gathers, warp 4 the MMAs, warps 5-8 the atomics
 constexpr int kWgMmaWarp = kWgProducerWarps;
 constexpr int kWgThreads = (kWgProducerWarps + 5) * 32;
-constexpr int kWgAtom = 8192;        // 64 pairs x 128 bytes
-constexpr int kWgMaxStages = 8;
+constexpr int kWgMaxStages = 8;      // an atom = (pairs per stage) x 128 bytes: 64 or 128 pairs
 
 struct alignas(128) WgradArgs {
   CUtensorMap tmx;  // x [n_in][cin] bf16, box {64, 1}, 128-byte swizzle
@@ -1630,7 +1629,11 @@ __device__ __forceinline__ uint32_t idesc_bf16_mn(int M, int N) {
   return idesc_bf16(M, N) | (1u << 15) | (1u << 16);
 }
 
+template <int kPairs>  // pairs per stage: 64, or 128 when a stage has at most 4 channel atoms
 __global__ void __launch_bounds__(kWgThreads, 1) k_conv_wgrad_tc(const __grid_constant__ WgradArgs a) {
+  constexpr int kAtom = kPairs * 128;  // one 64-channel atom of a stage
+  constexpr int kQ = kPairs / 4;       // gather4 operations per atom
+  constexpr int kPer = kPairs / 32;    // pair indices per lane
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sbase = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   // the stage ring, 16 KB of slack (the MMAs never read past a stage, the
@@ -1680,25 +1683,25 @@ __global__ void __launch_bounds__(kWgThreads, 1) k_conv_wgrad_tc(const __grid_co
       if (u.end == u.start) continue;
       const int a_atoms = min(2, (a.cin - u.mt * 128 + 63) / 64);  // a partial atom reads zeros past cin
       const int b_atoms = min(4, (a.cout - u.nt * 256 + 63) / 64);
-      const uint32_t bytes = (uint32_t)(a_atoms + b_atoms) * (uint32_t)kWgAtom;
-      const int nops = 16 * (a_atoms + b_atoms);
-      const int nst = (int)((u.end - u.start + 63) / 64);
-      // indices of a stage: lane l holds pairs 2l and 2l+1 (absent rows read
-      // as zeros through the out-of-range row index)
-      auto load_idx = [&](int k, int (&pi)[2], int (&qi)[2]) {
+      const uint32_t bytes = (uint32_t)(a_atoms + b_atoms) * (uint32_t)kAtom;
+      const int nops = kQ * (a_atoms + b_atoms);
+      const int nst = (int)((u.end - u.start + kPairs - 1) / kPairs);
+      // indices of a stage: lane l holds pairs kPer*l .. kPer*l + kPer-1
+      // (absent rows read as zeros through the out-of-range row index)
+      auto load_idx = [&](int k, int (&pi)[kPer], int (&qi)[kPer]) {
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const uint32_t e = u.start + (uint32_t)(64 * k + 2 * lane + j);
+        for (int j = 0; j < kPer; ++j) {
+          const uint32_t e = u.start + (uint32_t)(kPairs * k + kPer * lane + j);
           const bool ok = k < nst && e < u.end;
           pi[j] = ok ? __ldg(a.in_idx + e) : a.n_in;
           qi[j] = ok ? __ldg(a.out_idx + e) : a.n_out;
         }
       };
-      int p0[2], q0[2], p1[2], q1[2];
+      int p0[kPer], q0[kPer], p1[kPer], q1[kPer];
       load_idx(0, p0, q0);
       load_idx(1, p1, q1);
       for (int k = 0; k < nst; ++k, ++kg) {
-        int p2[2], q2[2];
+        int p2[kPer], q2[kPer];
         load_idx(k + 2, p2, q2);  // two stages ahead
         const int sb = ring_sb;
         if (kg >= S) mbar_wait(smem_u32(&h.empty[sb]), ring_ph ^ 1u, status);
@@ -1710,26 +1713,43 @@ __global__ void __launch_bounds__(kWgThreads, 1) k_conv_wgrad_tc(const __grid_co
         const uint32_t sA = smem_u32(sbase + (size_t)sb * a.stage_bytes), sB = sA + (uint32_t)a.b_off;
         if (warp == 0 && lane == 0) mbar_arrive_expect_tx(bar, bytes);
         {
-          const int op = 4 * lane + warp;  // < 128: covers the at most 96 ops of a stage
-          const int r4 = op & 15, atom = op >> 4;  // atoms 0..a_atoms-1: x, then dy
+          const int op = 4 * lane + warp;  // < 128: covers the at most 128 ops of a stage
+          const int r4 = op % kQ, atom = op / kQ;  // atoms 0..a_atoms-1: x, then dy
           const bool isA = atom < a_atoms;
-          // rows 4 r4 .. 4 r4 + 3 are held by lanes 2 r4 (two) and 2 r4 + 1 (two)
-          const int l0 = 2 * r4, l1 = 2 * r4 + 1;
-          const int x0 = __shfl_sync(0xffffffffu, p0[0], l0), x1 = __shfl_sync(0xffffffffu, p0[1], l0);
-          const int x2 = __shfl_sync(0xffffffffu, p0[0], l1), x3 = __shfl_sync(0xffffffffu, p0[1], l1);
-          const int y0 = __shfl_sync(0xffffffffu, q0[0], l0), y1 = __shfl_sync(0xffffffffu, q0[1], l0);
-          const int y2 = __shfl_sync(0xffffffffu, q0[0], l1), y3 = __shfl_sync(0xffffffffu, q0[1], l1);
+          // rows 4 r4 .. 4 r4 + 3: with 64 pairs held by lanes 2 r4 and
+          // 2 r4 + 1 (two each), with 128 pairs by lane r4 (four)
+          int x0, x1, x2, x3, y0, y1, y2, y3;
+          if (kPer == 2) {
+            const int l0 = 2 * r4, l1 = 2 * r4 + 1;
+            x0 = __shfl_sync(0xffffffffu, p0[0], l0);
+            x1 = __shfl_sync(0xffffffffu, p0[kPer - 1], l0);
+            x2 = __shfl_sync(0xffffffffu, p0[0], l1);
+            x3 = __shfl_sync(0xffffffffu, p0[kPer - 1], l1);
+            y0 = __shfl_sync(0xffffffffu, q0[0], l0);
+            y1 = __shfl_sync(0xffffffffu, q0[kPer - 1], l0);
+            y2 = __shfl_sync(0xffffffffu, q0[0], l1);
+            y3 = __shfl_sync(0xffffffffu, q0[kPer - 1], l1);
+          } else {
+            x0 = __shfl_sync(0xffffffffu, p0[0], r4);
+            x1 = __shfl_sync(0xffffffffu, p0[1 % kPer], r4);
+            x2 = __shfl_sync(0xffffffffu, p0[2 % kPer], r4);
+            x3 = __shfl_sync(0xffffffffu, p0[3 % kPer], r4);
+            y0 = __shfl_sync(0xffffffffu, q0[0], r4);
+            y1 = __shfl_sync(0xffffffffu, q0[1 % kPer], r4);
+            y2 = __shfl_sync(0xffffffffu, q0[2 % kPer], r4);
+            y3 = __shfl_sync(0xffffffffu, q0[3 % kPer], r4);
+          }
           if (op < nops) {
             if (isA)
-              tma_gather4(sA + (uint32_t)(atom * kWgAtom + r4 * 512), &a.tmx, u.mt * 128 + 64 * atom,
+              tma_gather4(sA + (uint32_t)(atom * kAtom + r4 * 512), &a.tmx, u.mt * 128 + 64 * atom,
                           make_int4(x0, x1, x2, x3), bar);
             else
-              tma_gather4(sB + (uint32_t)((atom - a_atoms) * kWgAtom + r4 * 512), &a.tmy,
+              tma_gather4(sB + (uint32_t)((atom - a_atoms) * kAtom + r4 * 512), &a.tmy,
                           u.nt * 256 + 64 * (atom - a_atoms), make_int4(y0, y1, y2, y3), bar);
           }
         }
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
+        for (int j = 0; j < kPer; ++j) {
           p0[j] = p1[j];
           q0[j] = q1[j];
           p1[j] = p2[j];
@@ -1754,8 +1774,8 @@ __global__ void __launch_bounds__(kWgThreads, 1) k_conv_wgrad_tc(const __grid_co
   } else if (warp == kWgMmaWarp) {
     // ---------------- MMA issue (one thread)
     if (lane == 0) {
-      const uint64_t a0 = sdesc_mn_sw128(smem_u32(sbase), (uint32_t)kWgAtom, 1024u);
-      const uint64_t b0 = sdesc_mn_sw128(smem_u32(sbase) + (uint32_t)a.b_off, (uint32_t)kWgAtom, 1024u);
+      const uint64_t a0 = sdesc_mn_sw128(smem_u32(sbase), (uint32_t)kAtom, 1024u);
+      const uint64_t b0 = sdesc_mn_sw128(smem_u32(sbase) + (uint32_t)a.b_off, (uint32_t)kAtom, 1024u);
       const uint32_t sunits = (uint32_t)a.stage_bytes >> 4;
       int m_sb = 0;
       uint32_t m_ph = 0, m_off = 0;
@@ -1763,7 +1783,7 @@ __global__ void __launch_bounds__(kWgThreads, 1) k_conv_wgrad_tc(const __grid_co
       for (uint32_t v = blockIdx.x; v < nunits; v += (uint32_t)G) {
         const WgUnit u = wg_unit(a, v);
         if (u.end == u.start) continue;
-        const int nst = (int)((u.end - u.start + 63) / 64);
+        const int nst = (int)((u.end - u.start + kPairs - 1) / kPairs);
         const uint32_t idesc = idesc_bf16_mn(128, 64 * min(4, (a.cout - u.nt * 256 + 63) / 64));
         const int b = i & 1;
         if (i >= 2) mbar_wait(smem_u32(&h.acc_empty[b]), (uint32_t)(((i >> 1) - 1) & 1), status);
@@ -1775,9 +1795,8 @@ __global__ void __launch_bounds__(kWgThreads, 1) k_conv_wgrad_tc(const __grid_co
           const uint64_t ad = a0 + m_off, bd = b0 + m_off;
           // K steps of 16 pairs: two 8-row groups, 2048 bytes
           umma_bf16(d, ad, bd, idesc, k > 0 ? 1u : 0u);
-          umma_bf16(d, ad + 128, bd + 128, idesc, 1u);
-          umma_bf16(d, ad + 256, bd + 256, idesc, 1u);
-          umma_bf16(d, ad + 384, bd + 384, idesc, 1u);
+#pragma unroll
+          for (int kk = 1; kk < kPairs / 16; ++kk) umma_bf16(d, ad + 128 * kk, bd + 128 * kk, idesc, 1u);
           umma_commit(smem_u32(&h.empty[m_sb]));
           m_off += sunits;
           if (++m_sb == S) {
@@ -2277,12 +2296,19 @@ extern "C" fvx_status fvx_sparse_conv_wgrad(fvx_grid gin, fvx_grid gout, fvx_kma
     wa.n_out = (int)gout->n_active;
     wa.mt = (int)((cin + 127) / 128);
     wa.nt = (int)((cout + 255) / 256);
-    wa.b_off = 2 * kWgAtom;
-    wa.stage_bytes = wa.b_off + kWgAtom * (int)std::min<int64_t>(4, (cout + 63) / 64);
+    // 128 pairs a stage (half as many stages) when its gathers fit the 128
+    // producer threads (at most 4 channel atoms) and 3 stages fit
+    const int atoms = (int)std::min<int64_t>(2, (cin + 63) / 64) + (int)std::min<int64_t>(4, (cout + 63) / 64);
     const int head = (int)sizeof(WgradHead);
+    const int pairs = (atoms <= 4 && (224 * 1024 - 1024 - 16384 - head) / (128 * 128 * (2 + atoms - 1)) >= 3)
+                          ? 128 : 64;
+    const int atom_bytes = pairs * 128;
+    wa.b_off = 2 * atom_bytes;
+    wa.stage_bytes = wa.b_off + atom_bytes * (int)std::min<int64_t>(4, (cout + 63) / 64);
     wa.stages = std::min(kWgMaxStages, (224 * 1024 - 1024 - 16384 - head) / wa.stage_bytes);
     const size_t smem = 1024 + (size_t)wa.stages * wa.stage_bytes + 16384 + head;
-    FVX_CUDA(cudaFuncSetAttribute(k_conv_wgrad_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    auto wkern = pairs == 128 ? k_conv_wgrad_tc<128> : k_conv_wgrad_tc<64>;
+    FVX_CUDA(cudaFuncSetAttribute(wkern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     const int64_t units = (m->n_tiles + kWgTiles - 1) / kWgTiles * 27 * wa.mt * wa.nt;
     if (units >= (int64_t)UINT32_MAX) {
       set_error("fvx_sparse_conv_wgrad: %lld work units exceed the 32-bit unit index", (long long)units);
@@ -2290,7 +2316,7 @@ extern "C" fvx_status fvx_sparse_conv_wgrad(fvx_grid gin, fvx_grid gout, fvx_kma
     }
     {
       LaunchScope ls("conv_wgrad_tc", s);
-      k_conv_wgrad_tc<<<(unsigned)std::min<int64_t>(units, sms), kWgThreads, smem, s>>>(wa);
+      wkern<<<(unsigned)std::min<int64_t>(units, sms), kWgThreads, smem, s>>>(wa);
     }
     return check_launch("conv_wgrad_tc");
   }
