@@ -93,3 +93,34 @@ def test_package_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(fvx, "LIB_PATH", str(tmp_path / "libfvx.so"))
     with pytest.raises(fvx.FvxError, match="missing"):
         fvx.load()
+
+
+def test_backward_entry_points_validate_on_host(lib):
+    """The transposed map, refined grid and gradient entry points reject NULL
+    handles and bad arguments before any device work."""
+    out = ctypes.c_void_p()
+    assert lib.fvx_kernel_map_transposed(None, None, 3, 2, None, ctypes.byref(out)) == 1
+    assert lib.fvx_refine(None, 2, None, ctypes.byref(out)) == 1
+    assert lib.fvx_sparse_conv_dgrad(None, None, None, 1, None, 16, None, 8, None, None) == 1
+    assert lib.fvx_sparse_conv_wgrad(None, None, None, 1, None, 8, None, 16, None, None) == 1
+    assert b"NULL" in lib.fvx_last_error() or b"bad argument" in lib.fvx_last_error()
+
+
+def test_reference_arm_line_on_cpu():
+    """bench.py --impl reference: the oracle's line on the host (tiny
+    workload), with the keys the driver reads."""
+    import sys
+
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+
+    class A:
+        warmup = 0
+        steps = 1
+        workload = "tiny_shell"
+        scale = 1.0
+
+    out = bench.bench_reference(A, 1, 0)
+    assert out["impl"] == "reference" and out["value"] > 0 and out["unit"] == bench.UNIT
+    assert out["cpu_baseline"]["kind"] == "oracle" and out["cpu_baseline"]["cores"] == 1
+    assert out["e2e"]["h2d_bytes_per_step"] == 0 and out["e2e"]["value"] == out["value"]
