@@ -7,7 +7,8 @@
  *   [fVDB-notes]  "fVDB: A Deep-Learning Framework for Sparse, Large Scale, and
  *                 High Performance Spatial Intelligence" (reading notes):
  *                 "Core method", "IndexGrid", "GPU-accelerated IndexGrid
- *                 build", "Sparse-convolution operators".
+ *                 build", "Sparse-convolution operators", "Limitations and
+ *                 future work".
  *   [fVDB-ONNX]   "Proposal: ONNX Runtime support for fVDB operations",
  *                 §1.1 Tensor Representations, §1.2 Custom Operator Schemas.
  *   [DriveRT]     "DriveRT": "Shared neighbour maps", "Counts kept on the GPU",
@@ -218,7 +219,7 @@ fvx_status fvx_sparse_conv(fvx_grid gin, fvx_grid gout, fvx_kmap m, fvx_dtype dt
                            const void* W, int64_t cout, void* out, fvx_stream stream);
 
 /* Which bf16 kernel fvx_sparse_conv and fvx_sparse_conv_noalloc run
- * [fVDB notes, "Sparse-convolution operators": several convolution backends,
+ * [fVDB-notes, "Sparse-convolution operators": several convolution backends,
  * the leaf-densified one for low channel counts on leaves at least 20%
  * occupied, picked per case].
  *   FVX_CONV_AUTO    (default) leaf-densified when the map has stride 1,
@@ -269,7 +270,7 @@ fvx_status fvx_sparse_conv_noalloc(fvx_grid gin, fvx_grid gout, fvx_kmap m, fvx_
                                    int64_t cin, const void* W, int64_t cout, void* out, fvx_stream stream);
 
 /* ---------------------------------------------------------------------------
- * Backward pass of fvx_sparse_conv  [fVDB notes, "Limitations and future
+ * Backward pass of fvx_sparse_conv  [fVDB-notes, "Limitations and future
  * work": training computes its gradients through the pair-list (IGEMM)
  * backend]
  *
