@@ -31,8 +31,25 @@ def test_header_declares_the_boundary():
     names = _declared()
     for n in ("fvx_build_grid", "fvx_kernel_map", "fvx_sparse_conv", "fvx_lookup", "fvx_coarsen",
               "fvx_grid_view", "fvx_kmap_view", "fvx_grid_destroy", "fvx_kmap_destroy", "fvx_set_allocator",
-              "fvx_status_string", "fvx_last_error"):
+              "fvx_status_string", "fvx_last_error", "fvx_refine", "fvx_kernel_map_transposed",
+              "fvx_sparse_conv_dgrad", "fvx_sparse_conv_wgrad"):
         assert n in names
+
+
+def test_header_is_plain_c(tmp_path):
+    """The boundary compiles as ISO C (no C++ or CUDA types), with and without
+    extern "C" handling."""
+    import shutil
+    import subprocess
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use.c"
+    src.write_text('#include "fvx.h"\nint main(void) { fvx_grid g = 0; (void)g; return (int)FVX_OK; }\n')
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+                        "-fsyntax-only", str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
 
 
 def test_library_exports_every_declared_symbol(lib):
