@@ -141,3 +141,35 @@ def test_reference_arm_line_on_cpu():
     assert out["impl"] == "reference" and out["value"] > 0 and out["unit"] == bench.UNIT
     assert out["cpu_baseline"]["kind"] == "oracle" and out["cpu_baseline"]["cores"] == 1
     assert out["e2e"]["h2d_bytes_per_step"] == 0 and out["e2e"]["value"] == out["value"]
+
+
+def test_c_program_links_and_calls_the_library(lib, tmp_path):
+    """A plain C program links libfvx.so and gets status codes and messages
+    from it (host paths only)."""
+    import shutil
+    import subprocess
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    pkg = os.path.join(ROOT, "sparse_convolution_gb300")
+    src = tmp_path / "use.c"
+    src.write_text(r"""
+#include <stdio.h>
+#include <string.h>
+#include "fvx.h"
+int main(void) {
+  fvx_grid g = 0;
+  if (fvx_refine(NULL, 2, NULL, &g) != FVX_ERR_INVALID_ARG) return 1;
+  if (strstr(fvx_last_error(), "fvx_refine") == NULL) return 2;
+  if (strcmp(fvx_status_string(FVX_ERR_RANGE), "FVX_ERR_RANGE") != 0) return 3;
+  puts("ok");
+  return 0;
+}
+""")
+    exe = tmp_path / "use"
+    r = subprocess.run([cc, "-std=c99", "-I", os.path.join(ROOT, "include"), str(src), "-L", pkg, "-lfvx",
+                        "-Wl,-rpath," + pkg, "-o", str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", (r.returncode, r.stdout, r.stderr)
