@@ -231,6 +231,53 @@ def test_conv_matches_dense_conv3d(stride, cin, cout):
     assert np.allclose(yr, y[rows], rtol=0, atol=1e-12) and np.allclose(ar, a[rows], rtol=0, atol=1e-12)
 
 
+@pytest.mark.parametrize("stride,transposed", [(1, False), (2, False), (2, True)])
+def test_conv_tolerance_scale_is_abs_conv(stride, transposed):
+    """The per-element scale a[q, co] = sum over pairs and channels of |x w|,
+    which every conv tolerance multiplies, is the convolution of |x| with |W|
+    ("fVDB" reading notes, Sparse-convolution operators: the sum that defines
+    each output).  Pinned to torch's dense conv3d (conv_transpose3d for the
+    transposed map) of the absolute inputs, so an a that is off by any factor
+    (counted twice, accumulated into the wrong row, taken from one offset only)
+    fails here, not just an a that is too small."""
+    coords, offs = _random_grid(33 + stride + 10 * transposed, n=900, span=16, lo=-9, B=1, dup=0.0)
+    fine = oracle.Grid.build(coords, offs)
+    coarse = fine if stride == 1 else fine.coarsen(2)
+    gin, gout = (coarse, fine) if transposed else (fine, coarse)
+    km = oracle.KernelMap(gin, gout, stride, transposed=transposed)
+    rng = np.random.default_rng(6)
+    cin, cout = 5, 3
+    x = rng.standard_normal((gin.n_active, cin))
+    W = rng.standard_normal((27, cin, cout))
+    _, a = oracle.conv(km, x, W)
+    dense = H.dense_conv_transpose_active if transposed else H.dense_conv_active
+    ref = dense(gin.voxels()["ijk"], np.abs(x), np.abs(W), gout.voxels()["ijk"], stride)
+    assert np.max(np.abs(a - ref)) <= 1e-12 * np.max(ref)
+    assert np.max(np.abs(2.0 * a - ref)) > 0.1 * np.max(ref)  # the check sees a factor of 2
+    if not transposed:
+        rows = rng.choice(gout.n_active, size=40, replace=False)
+        _, ar = oracle.conv_rows(gin, gout, stride, rows, x, W)
+        assert np.max(np.abs(ar - ref[rows])) <= 1e-12 * np.max(ref)
+
+
+@pytest.mark.parametrize("stride", [1, 2])
+def test_wgrad_tolerance_scale_is_abs_wgrad(stride):
+    """The weight gradient's tolerance scale, conv_wgrad(|x|, |dy|) = sum over
+    pairs of |x[p]|^T |dy[q]|, equals torch autograd's weight gradient of the
+    dense conv3d with the absolute inputs."""
+    coords, offs = _random_grid(95 + stride, n=700, span=14, lo=-7, B=1, dup=0.0)
+    fine = oracle.Grid.build(coords, offs)
+    coarse = fine if stride == 1 else fine.coarsen(2)
+    km = oracle.KernelMap(fine, coarse, stride)
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal((fine.n_active, 4))
+    dy = rng.standard_normal((coarse.n_active, 6))
+    a = oracle.conv_wgrad(km, np.abs(x), np.abs(dy))
+    ref = H.dense_conv_wgrad(fine.voxels()["ijk"], np.abs(x), coarse.voxels()["ijk"], np.abs(dy), stride, 4, 6)
+    assert np.max(np.abs(a - ref)) <= 1e-12 * np.max(ref)
+    assert np.max(np.abs(2.0 * a - ref)) > 0.1 * np.max(ref)
+
+
 def test_conv_identity_and_ones():
     coords, offs = _random_grid(41, n=800, span=12, lo=0, B=1, dup=0.0)
     g = oracle.Grid.build(coords, offs)
