@@ -2,17 +2,21 @@
 unsorted int32 coordinates -> 3x3x3 kernel map -> bf16 sparse convolution.
 
 One step = one pass of the whole path over the workload: fvx_build_grid,
-fvx_kernel_map (submanifold, stride 1), fvx_sparse_conv.  The default workload
-is the leaf-dense grid (union of 40 solid ellipsoids with radii 8-40 in a 256^3
-box, bf16 8 -> 16).
+fvx_kernel_map, fvx_sparse_conv (and, for a stride-2 layer, fvx_coarsen and
+its map and conv).  The default workload is the largest: a batch of 8
+narrow-band grids in 1024^3 boxes (12.0M voxels from 17.1M unsorted rows with
+30% duplicates, bf16 32 -> 64).  The four other workloads (tiny shell, leaf
+dense, narrow band, LiDAR) are timed the same way after it and reported under
+components.per_workload (skip with --no-all-workloads).
 
 Prints ONE JSON line (rank 0).  `value` is whole-step throughput in active
 voxels per second (Mvoxels/s) with inputs resident in HBM; `components` splits
 it into the two quantities the metric names (build+kmap Mvoxels/s and conv
 active-pair TFLOP/s).  `--impl reference` times the CPU oracle on a bounded
-sample of the same workload instead.  `--pass backward` times the training
-backward of the workload's convs instead (transposed kernel map, input and
-weight gradients; its own metric, in TFLOP/s).
+crop of the same workload instead (the crop the line's cpu_baseline times).
+`--pass backward` times the training backward of the workload's convs
+instead (transposed kernel map, input and weight gradients; its own metric,
+in TFLOP/s).
 """
 from __future__ import annotations
 
@@ -41,7 +45,9 @@ def parse():
     p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", default="fvx", choices=["fvx", "reference"])
-    p.add_argument("--workload", default="leaf_dense")
+    p.add_argument("--workload", default="batched_narrow_band")
+    p.add_argument("--no-all-workloads", dest="all_workloads", action="store_false",
+                   help="time only --workload (no per-workload entries for the other four)")
     p.add_argument("--scale", type=float, default=1.0,
                    help="smaller instance of the same workload generator (< 1), e.g. for profiler captures")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -176,16 +182,17 @@ def make_workload(name, scale=1.0):
     return f(scale=scale) if scale != 1.0 else f()
 
 
-def oracle_sample(w, target_rows=250_000):
-    """A spatially contiguous crop of the workload (first batch, lowest i)
-    with about target_rows rows (fewer for wide convs, whose fp64 oracle cost
-    grows with cin*cout): same density and structure, bounded CPU work."""
+def oracle_sample(w, target_rows=30_000):
+    """A spatially contiguous crop of the workload (first batch element, lowest
+    i) with about target_rows rows (fewer for wide convs, whose fp64 oracle
+    cost grows with cin*cout): same density and structure, bounded CPU work.
+    The CPU baseline and the reference arm time the same crop."""
     coords, offs = w["coords"], w["batch_offsets"]
     width = sum(c["cin"] * c["cout"] for c in w["convs"])
     target_rows = max(2000, int(target_rows * min(1.0, 2048.0 / width)))
     c = coords[offs[0]:offs[1]]
     if c.shape[0] <= target_rows:
-        return c, np.array([0, c.shape[0]], np.int64), "whole first batch element"
+        return c, np.array([0, c.shape[0]], np.int64), f"whole first batch element ({c.shape[0]} rows)"
     cut = np.partition(c[:, 0], target_rows)[target_rows]
     sel = c[c[:, 0] < cut]
     return sel, np.array([0, sel.shape[0]], np.int64), f"crop i < {int(cut)} of batch 0 ({sel.shape[0]} rows)"
@@ -193,242 +200,323 @@ def oracle_sample(w, target_rows=250_000):
 
 def run_oracle_step(coords, offs, convs, seed):
     """The oracle's pass over one input: build, then per conv of the workload
-    (coarsen for stride 2) kernel map and conv, each conv reading the last."""
+    (coarsen for stride 2) kernel map and conv, each conv reading the last.
+    Returns (active voxels, seconds in build + kernel maps, seconds in convs,
+    active-pair flops)."""
     import oracle
     from sparse_convolution_gb300 import synth
 
+    t0 = time.perf_counter()
     g = oracle.Grid.build(coords, offs)
+    t_bk = time.perf_counter() - t0
+    t_cv = 0.0
+    flops = 0.0
     x = synth.features(seed, g.n_active, convs[0]["cin"]).astype(np.float64)
     gin = g
     for i, c in enumerate(convs):
+        t0 = time.perf_counter()
         gout = gin if c["stride"] == 1 else gin.coarsen(c["stride"])
         km = oracle.KernelMap(gin, gout, c["stride"])
+        t_bk += time.perf_counter() - t0
         W = synth.weights(seed + 1 + i, c["cin"], c["cout"]).astype(np.float64)
+        t0 = time.perf_counter()
         x, _ = oracle.conv(km, x, W)
+        t_cv += time.perf_counter() - t0
+        flops += 2.0 * c["cin"] * c["cout"] * km.n_pairs
         gin = gout
-    return g.n_active
+    return g.n_active, t_bk, t_cv, flops
 
 
-def cpu_baseline(w, budget_s=20.0):
+def oracle_passes(w, min_s, max_passes):
+    """Repeats the oracle's pass over the shared crop until min_s seconds (at
+    most max_passes passes); returns the per-pass figures and the crop."""
     coords, offs, desc = oracle_sample(w)
+    n, tb, tc, fl, k = 0, 0.0, 0.0, 0.0, 0
     t0 = time.perf_counter()
-    n = run_oracle_step(coords, offs, w["convs"], 1)
-    dt = time.perf_counter() - t0
-    return dict(value=n / dt / 1e6, unit=UNIT, cores=1, kind="oracle",
-                sample=f"{desc}: build+kmap+conv of {n} voxels, single-threaded, {dt:.1f} s",
+    while k < max_passes and (k == 0 or time.perf_counter() - t0 < min_s):
+        n, b, c, fl = run_oracle_step(coords, offs, w["convs"], 1)
+        tb, tc, k = tb + b, tc + c, k + 1
+    return dict(n=n, t_bk=tb / k, t_cv=tc / k, flops=fl, passes=k, desc=desc)
+
+
+def cpu_baseline(w):
+    """The oracle as it stands, single-threaded, on the crop the reference
+    arm times (10-30 s of CPU work)."""
+    r = oracle_passes(w, min_s=10.0, max_passes=8)
+    t = r["t_bk"] + r["t_cv"]
+    return dict(value=round(r["n"] / t / 1e6, 6), unit=UNIT, cores=1, kind="oracle",
+                sample=f"{r['desc']}: oracle build + kernel map + conv of {r['n']} voxels per pass, "
+                       f"{r['passes']} passes, single-threaded",
+                build_kmap_mvoxels_s=round(r["n"] / r["t_bk"] / 1e6, 6),
+                conv_active_pair_gflops=round(r["flops"] / r["t_cv"] / 1e9, 4),
                 host_cores=os.cpu_count())
 
 
 # ---------------------------------------------------------------- GPU arm
-def bench_fvx(args, world, rank, local):
-    import torch
+def conv_kernel_name(fvx, algo, fp32, cin):
+    if fp32:
+        return "conv_f32"
+    if algo == fvx.FVX_CONV_LEAF:
+        return "conv_leaf"
+    return "conv_bf16_tma" if cin % 16 == 0 else "conv_bf16_tc"
 
-    from sparse_convolution_gb300 import build_lib
-    import sparse_convolution_gb300 as fvx
-    from sparse_convolution_gb300 import synth
 
-    torch.cuda.set_device(local)
-    build_lib.build()
-    fvx.load()
-    w = make_workload(args.workload, args.scale)
-    convs = w["convs"]
-    fp32 = w["dtype"] == "f32"
-    dev = torch.device("cuda", local)
-    coords_h = torch.from_numpy(w["coords"]).pin_memory()
-    offs = w["batch_offsets"]
-    coords = coords_h.to(dev)
-    g0 = fvx.Grid.build(coords, offs)
-    U = g0.n_active
-    n_out, leaves_out = [U], [g0.n_leaf]
-    if len(convs) > 1:
-        gc0 = g0.coarsen(2)
-        n_out.append(gc0.n_active)
-        leaves_out.append(gc0.n_leaf)
-        gc0.destroy()
-    g0.destroy()
-    # feature rows follow the active-voxel index order; values are i.i.d., so any order is a valid input
-    fdt = torch.float32 if fp32 else torch.bfloat16
-    x_h = torch.from_numpy(synth.features(w["seed"] + 10, U, convs[0]["cin"], w["feat_kind"])).to(fdt).pin_memory()
-    W_h = [torch.from_numpy(synth.weights(w["seed"] + 20 + i, c["cin"], c["cout"])).to(fdt).pin_memory()
-           for i, c in enumerate(convs)]
-    x = x_h.to(dev)
-    Ws = [t.to(dev) for t in W_h]
-    # outputs: fp32 (bf16 operands, fp32 accumulation: the mode whose error meets
-    # 2e-3 * sum|w*x|); a conv that feeds the next one writes bf16
-    ys = []
-    for i, c in enumerate(convs):
-        odt = torch.float32 if (fp32 or i == len(convs) - 1) else torch.bfloat16
-        ys.append(torch.empty((n_out[i], c["cout"]), dtype=odt, device=dev))
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+def ffma_peak(sm_count, peaks):
+    """FP32 FFMA peak: SMs x 128 FP32 lanes x 2 flops x the maximum SM clock."""
+    mhz = float(peaks.get("sm_max_mhz", 2070.0))
+    return sm_count * 128 * 2 * mhz * 1e6 / 1e12, f"derived: {sm_count} SMs x 128 FP32 lanes x 2 x {mhz:.0f} MHz"
+
+
+def conv_roofline(flops, alg_bytes, sec, fp32, peaks, peak_kind, sm_count):
+    """Roofline of one conv kernel: FFMA for fp32, else tensor or HBM by the
+    kernel's arithmetic intensity against the measured ridge."""
+    if fp32:
+        peak, src = ffma_peak(sm_count, peaks)
+        r = dict(bound="alu", achieved=round(flops / sec / 1e12, 3), peak=round(peak, 1), unit="TFLOP/s",
+                 peak_source=src)
+    elif flops / alg_bytes > peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9):
+        r = dict(bound="tensor", achieved=round(flops / sec / 1e12, 2), peak=peaks["bf16_tflops"], unit="TFLOP/s",
+                 peak_source=f"{peak_kind} (bf16_tflops, burst)")
+    else:
+        r = dict(bound="hbm", achieved=round(alg_bytes / sec / 1e9, 1), peak=peaks["hbm_gbs"], unit="GB/s",
+                 peak_source=f"{peak_kind} (hbm_gbs)")
+    r["frac"] = round(r["achieved"] / r["peak"], 4)
+    return r
+
+
+class Workload:
+    """One workload resident on the device: pinned host inputs, their device
+    copies, output buffers, and the sizes of its grids."""
+
+    def __init__(self, fvx, torch, synth, w, dev):
+        self.w, self.dev = w, dev
+        self.convs = w["convs"]
+        self.fp32 = w["dtype"] == "f32"
+        self.offs = w["batch_offsets"]
+        self.coords_h = torch.from_numpy(w["coords"]).pin_memory()
+        self.coords = self.coords_h.to(dev)
+        g0 = fvx.Grid.build(self.coords, self.offs)
+        self.U = g0.n_active
+        self.n_out, self.leaves_out = [self.U], [g0.n_leaf]
+        gin = g0
+        for c in self.convs[1:]:  # a later conv reads the previous one's output grid
+            gc = gin.coarsen(c["stride"]) if c["stride"] != 1 else gin
+            self.n_out.append(gc.n_active)
+            self.leaves_out.append(gc.n_leaf)
+            if gc is not gin and gin is not g0:
+                gin.destroy()
+            gin = gc
+        if gin is not g0:
+            gin.destroy()
+        g0.destroy()
+        # feature rows follow the active-voxel index order; values are i.i.d.,
+        # so any order is a valid input
+        fdt = torch.float32 if self.fp32 else torch.bfloat16
+        self.x_h = torch.from_numpy(synth.features(w["seed"] + 10, self.U, self.convs[0]["cin"],
+                                                   w["feat_kind"])).to(fdt).pin_memory()
+        self.W_h = [torch.from_numpy(synth.weights(w["seed"] + 20 + i, c["cin"], c["cout"])).to(fdt).pin_memory()
+                    for i, c in enumerate(self.convs)]
+        self.x = self.x_h.to(dev)
+        self.Ws = [t.to(dev) for t in self.W_h]
+        # outputs: fp32 (bf16 operands, fp32 accumulation: the mode whose error
+        # meets 2e-3 * sum|w*x|); a conv that feeds the next one writes bf16
+        self.ys = []
+        for i, c in enumerate(self.convs):
+            odt = torch.float32 if (self.fp32 or i == len(self.convs) - 1) else torch.bfloat16
+            self.ys.append(torch.empty((self.n_out[i], c["cout"]), dtype=odt, device=dev))
+
+
+def forward_step(fvx, wl, rec, coords_in, x_in, W_in, ys, stream=None, algos=None, pair_counts=None):
+    """One pass of the path: build, then per conv (coarsen for stride 2)
+    kernel map and conv.  rec(category) brackets each call with events.
+    Returns the handles to release."""
+    handles = []
+    with rec("build"):
+        g = fvx.Grid.build(coords_in, wl.offs, stream=stream)
+    handles.append(g)
+    src, gin = x_in, g
+    for i, c in enumerate(wl.convs):
+        if c["stride"] == 1:
+            gout = gin
+        else:
+            with rec("build"):
+                gout = gin.coarsen(c["stride"], stream=stream)
+            handles.append(gout)
+        with rec("kmap"):
+            km = fvx.KernelMap(gin, gout, c["stride"], stream=stream)
+        handles.append(km)
+        if pair_counts is not None and len(pair_counts) < len(wl.convs):  # read once (the read synchronises)
+            pair_counts.append(km.n_pairs)
+        with rec(f"conv{i}"):
+            fvx.sparse_conv(gin, gout, km, src, W_in[i], out=ys[i], stream=stream)
+        if algos is not None and len(algos) < len(wl.convs):
+            algos.append(fvx.last_conv_algo())
+        src, gin = ys[i], gout
+    return handles
+
+
+def release(handles):
+    for hnd in reversed(handles):
+        hnd.destroy()
+
+
+class EventRec:
+    """Records (category, start event, end event) around each bracketed call
+    on the given stream."""
+
+    def __init__(self, torch, stream):
+        self.torch, self.stream, self.marks = torch, stream, []
+
+    def __call__(self, cat):
+        self.cat = cat
+        return self
+
+    def __enter__(self):
+        self.e0 = self.torch.cuda.Event(enable_timing=True)
+        self.e0.record(self.stream)
+        return self
+
+    def __exit__(self, *a):
+        e1 = self.torch.cuda.Event(enable_timing=True)
+        e1.record(self.stream)
+        self.marks.append((self.cat, self.e0, e1))
+        return False
+
+
+class NoRec:
+    def __call__(self, cat):
+        return self
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+def time_forward(fvx, torch, wl, K, warmup, flush, peaks, peak_kind, sm_count, world=1, clocks=None):
+    """Warm-up, then K timed steps (L2 flushed before each, outside the
+    events).  Per call category CUDA-event time; per conv kernel the launch
+    durations the library's event timing records.  Returns the workload's
+    figures and the raw timing for the caller's line."""
     stream = torch.cuda.current_stream()
-
-    algos = []  # kernel family each conv ran (recorded on the first step)
-    pair_counts = []  # pairs of each conv's kernel map (first step)
-
-    def step(rec, coords_in, x_in, W_in):
-        """One pass of the path.  rec(category) brackets each call with events."""
-        handles = []
-        with rec("build"):
-            g = fvx.Grid.build(coords_in, offs)
-        handles.append(g)
-        src, gin = x_in, g
-        for i, c in enumerate(convs):
-            if c["stride"] == 1:
-                gout = gin
-            else:
-                with rec("build"):
-                    gout = gin.coarsen(c["stride"])
-                handles.append(gout)
-            with rec("kmap"):
-                km = fvx.KernelMap(gin, gout, c["stride"])
-            handles.append(km)
-            if len(pair_counts) < len(convs):  # read once (the read synchronises)
-                pair_counts.append(km.n_pairs)
-            with rec("conv"):
-                fvx.sparse_conv(gin, gout, km, src, W_in[i], out=ys[i])
-            if len(algos) < len(convs):
-                algos.append(fvx.last_conv_algo())
-            src, gin = ys[i], gout
-        return handles, pair_counts
-
-    class NoRec:
-        def __call__(self, cat):
-            return self
-
-        def __enter__(self):
-            return self
-
-        def __exit__(self, *a):
-            return False
-
-    class EventRec:
-        def __init__(self):
-            self.marks = []
-
-        def __call__(self, cat):
-            self.cat = cat
-            return self
-
-        def __enter__(self):
-            self.e0 = torch.cuda.Event(enable_timing=True)
-            self.e0.record(stream)
-            return self
-
-        def __exit__(self, *a):
-            e1 = torch.cuda.Event(enable_timing=True)
-            e1.record(stream)
-            self.marks.append((self.cat, self.e0, e1))
-            return False
-
-    def release(handles):
-        for hnd in reversed(handles):
-            hnd.destroy()
-
-    for _ in range(args.warmup):
-        hs, pairs = step(NoRec(), coords, x, Ws)
-        release(hs)
+    algos, pairs = [], []
+    for _ in range(max(1, warmup)):
+        release(forward_step(fvx, wl, NoRec(), wl.coords, wl.x, wl.Ws, wl.ys, algos=algos, pair_counts=pairs))
     torch.cuda.synchronize()
     fvx.device_status()
-
-    def kernel_of(i):
-        if fp32:
-            return "conv_f32"
-        if algos[i] == fvx.FVX_CONV_LEAF:
-            return "conv_leaf"
-        return "conv_bf16_tma" if convs[i]["cin"] % 16 == 0 else "conv_bf16_tc"
-
-    conv_kernels = [kernel_of(i) for i in range(len(convs))]
-    # the roofline follows the conv kernel doing the most arithmetic
-    prof_kernel = args.profile_kernel or conv_kernels[0]
-    recs = EventRec()
-    clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.3)
+    kernels = [conv_kernel_name(fvx, algos[i], wl.fp32, c["cin"]) for i, c in enumerate(wl.convs)]
+    flops_i = [2.0 * c["cin"] * c["cout"] * p for c, p in zip(wl.convs, pairs)]
+    # the kernel timed in the main loop: the one doing the most arithmetic
+    main_k = kernels[max(range(len(wl.convs)), key=lambda i: flops_i[i])]
+    recs = EventRec(torch, stream)
+    if clocks is not None:
+        clocks.start()
+        time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize()
-    fvx.profile_enable(prof_kernel)
+    fvx.profile_enable(main_k)
     l0 = fvx.launch_count()
-    for k in range(args.steps):
+    for k in range(K):
         flush.fill_(float(k))  # evict L2 between steps (outside the step's events)
-        hs, pairs = step(recs, coords, x, Ws)
-        release(hs)
+        release(forward_step(fvx, wl, recs, wl.coords, wl.x, wl.Ws, wl.ys))
     torch.cuda.synchronize()
     launches = fvx.launch_count() - l0
-    prof_ms, prof_n = fvx.profile_read()
+    each = {main_k: fvx.profile_read_each(cap=64 * K)}
     fvx.profile_enable(None)
     barrier(world)
-    clk = clocks.stop()
+    clk = clocks.stop() if clocks is not None else None
     fvx.device_status()
-    t = {"build": 0.0, "kmap": 0.0, "conv": 0.0}
+    # a conv kernel other than the main one: timed in a second loop of its own
+    for kn in sorted(set(kernels) - {main_k}):
+        fvx.profile_enable(kn)
+        for k in range(K):
+            flush.fill_(float(k))
+            release(forward_step(fvx, wl, NoRec(), wl.coords, wl.x, wl.Ws, wl.ys))
+        torch.cuda.synchronize()
+        each[kn] = fvx.profile_read_each(cap=64 * K)
+        fvx.profile_enable(None)
+    t = {}
     for cat, e0, e1 in recs.marks:
-        t[cat] += e0.elapsed_time(e1) / 1e3
-    t_total = max_over_ranks(sum(t.values()), world)
-    K = args.steps
-    value = U * K * world / t_total / 1e6
-    esz = 4 if fp32 else 2
-    flops_i = [2.0 * c["cin"] * c["cout"] * p for c, p in zip(convs, pairs)]
-    flops = sum(flops_i)
-    # algorithmic bytes of each conv: feats read once, output written once
-    # (4 B fp32 / 2 B bf16), weights once, plus what locates the inputs: the
-    # kernel map's (in, out) int32 pair for the pair-list kernels, the output
-    # leaf's 80-byte record for the leaf-densified kernel
-    bytes_i = []
-    n_in = U
-    for i, (c, p) in enumerate(zip(convs, pairs)):
-        where = 80 * leaves_out[i] if conv_kernels[i] == "conv_leaf" else 8 * p
-        bytes_i.append(n_in * c["cin"] * esz + n_out[i] * c["cout"] * ys[i].element_size()
-                       + 27 * c["cin"] * c["cout"] * esz + where)
-        n_in = n_out[i]
-    if not args.profile_kernel and len(convs) > 1:
-        prof_kernel = conv_kernels[max(range(len(convs)), key=lambda i: flops_i[i])]
-    mine = [i for i in range(len(convs)) if conv_kernels[i] == prof_kernel]
-    flops_p = sum(flops_i[i] for i in mine)
-    alg_bytes = sum(bytes_i[i] for i in mine)
-    # build + kernel map against HBM: per input row 170 B (key encode, radix
-    # passes, flag scans, sidecars), per output voxel 76 B plus 8 B per pair
-    # (coordinates, leaf words, mask, scans; the pair lists written once)
-    bk_bytes = 170.0 * w["coords"].shape[0] + sum(76.0 * n + 8.0 * p for n, p in zip(n_out, pairs))
+        t[cat] = t.get(cat, 0.0) + e0.elapsed_time(e1) / 1e3
+    t_conv = sum(v for c_, v in t.items() if c_.startswith("conv"))
+    t_total = t["build"] + t["kmap"] + t_conv
+    # per conv: its kernel's launches (launch order within a step = conv order)
+    per_conv = []
+    esz = 4 if wl.fp32 else 2
+    n_in = wl.U
+    for i, (c, p) in enumerate(zip(wl.convs, pairs)):
+        kn = kernels[i]
+        same = [j for j in range(len(wl.convs)) if kernels[j] == kn]
+        durs = each[kn]
+        per_step = len(durs) // K if K else 0
+        mine = []
+        if per_step == len(same):
+            pos = same.index(i)
+            mine = durs[pos::per_step]
+        sec = sum(mine) / 1e3 if mine else t[f"conv{i}"]
+        nk = len(mine) if mine else K
+        # algorithmic bytes: feats read once, output written once (4 B fp32 /
+        # 2 B bf16), weights once, plus what locates the inputs: the kernel
+        # map's (in, out) int32 pair for the pair-list kernels, the output
+        # leaf's 80-byte record for the leaf-densified kernel
+        where = 80 * wl.leaves_out[i] if kn == "conv_leaf" else 8 * p
+        alg = (n_in * c["cin"] * esz + wl.n_out[i] * c["cout"] * wl.ys[i].element_size()
+               + 27 * c["cin"] * c["cout"] * esz + where)
+        rl = conv_roofline(flops_i[i] * nk, alg * nk, sec, wl.fp32, peaks, peak_kind, sm_count)
+        per_conv.append(dict(conv=f"{c['cin']}->{c['cout']} stride {c['stride']}", kernel=kn, pairs=int(p),
+                             mean_pairs_per_output=round(p / wl.n_out[i], 3),
+                             kernel_ms=round(sec / nk * 1e3, 5), call_ms=round(t[f"conv{i}"] / K * 1e3, 5),
+                             active_pair_tflops=round(flops_i[i] * nk / sec / 1e12, 3),
+                             algorithmic_bytes=int(alg), flops=int(flops_i[i]), roofline=rl,
+                             kernel_timing="CUDA events around each launch" if mine else "call events"))
+        n_in = wl.n_out[i]
+    # build + kernel map against HBM, as effective bandwidth: per input row
+    # 170 B (key encode, about five radix passes, flag scans, sidecars; the
+    # one-tile bitmap path sorts nothing but is credited the same bytes), per
+    # output voxel 76 B plus 8 B per pair (coordinates, leaf words, mask,
+    # scans; the pair lists written once)
+    rows = wl.w["coords"].shape[0]
+    b_bytes = 170.0 * rows
+    k_bytes = sum(76.0 * n + 8.0 * p for n, p in zip(wl.n_out, pairs))
+    hbm = peaks["hbm_gbs"]
+    s1 = [c for c in range(len(wl.convs)) if wl.convs[c]["stride"] == 1]
+    entry = dict(
+        workload=wl.w["name"], rows=int(rows), active_voxels=int(wl.U), batch=int(len(wl.offs) - 1),
+        mean_active_neighbours=(round(pairs[s1[0]] / wl.n_out[s1[0]] - 1.0, 3) if s1 else None),
+        step_ms=round(t_total / K * 1e3, 4), build_ms=round(t["build"] / K * 1e3, 4),
+        kmap_ms=round(t["kmap"] / K * 1e3, 4), conv_ms=round(t_conv / K * 1e3, 4),
+        step_mvoxels_s=round(wl.U * K / t_total / 1e6, 2),
+        build_kmap_mvoxels_s=round(wl.U * K / (t["build"] + t["kmap"]) / 1e6, 2),
+        build_kmap_hbm=dict(
+            kind="effective bandwidth: fixed per-unit bytes over measured time",
+            build_bytes=int(b_bytes), kmap_bytes=int(k_bytes),
+            build_gbs=round(b_bytes * K / t["build"] / 1e9, 1), kmap_gbs=round(k_bytes * K / t["kmap"] / 1e9, 1),
+            build_frac=round(b_bytes * K / t["build"] / 1e9 / hbm, 4),
+            kmap_frac=round(k_bytes * K / t["kmap"] / 1e9 / hbm, 4),
+            frac=round((b_bytes + k_bytes) * K / (t["build"] + t["kmap"]) / 1e9 / hbm, 4)),
+        conv_active_pair_tflops=round(sum(flops_i) * K / t_conv / 1e12, 4),
+        convs=per_conv)
+    raw = dict(t_total=t_total, pairs=pairs, kernels=kernels, launches=launches, clocks=clk, main_kernel=main_k)
+    return entry, raw
 
-    # roofline of the profiled kernel (all of its launches in the timed region)
-    peaks, peak_kind = measured_peaks()
-    roofline = None
-    if prof_n and mine:
-        flops = flops_p
-        sec = prof_ms / 1e3
-        per_launch = prof_n / K  # launches of the kernel per step
-        intensity = flops / alg_bytes
-        if fp32:
-            # FFMA: 152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz (max SM clock)
-            peak = 152 * 128 * 2 * 2.07e9 / 1e12
-            roofline = dict(bound="alu", achieved=round(flops * K / sec / 1e12, 3), peak=round(peak, 1),
-                            unit="TFLOP/s", peak_source="derived: 152 SMs x 128 FP32 lanes x 2 x 2.07 GHz")
-        elif intensity > peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9):
-            peak = peaks["bf16_tflops"]
-            roofline = dict(bound="tensor", achieved=round(flops * K / sec / 1e12, 2), peak=peak, unit="TFLOP/s",
-                            peak_source=f"{peak_kind} (bf16_tflops, burst)")
-        else:
-            peak = peaks["hbm_gbs"]
-            roofline = dict(bound="hbm", achieved=round(alg_bytes * K / sec / 1e9, 1), peak=peak, unit="GB/s",
-                            peak_source=f"{peak_kind} (hbm_gbs)")
-        roofline.update(kernel=prof_kernel, frac=round(roofline["achieved"] / roofline["peak"], 4),
-                        traffic=profiled_traffic(prof_kernel, w["name"]) if len(mine) == 1 else None,
-                        algorithmic_bytes=int(alg_bytes / per_launch), flops=int(flops / per_launch),
-                        avg_launch_ms=round(prof_ms / prof_n, 5), launches_per_step=int(per_launch))
 
-    # end to end through the public API with host buffers: every step copies
-    # its inputs in from pinned host memory and its result back out, all inside
-    # the timed region.  Steps are pipelined two deep, as a serving loop would
-    # run them: each slot has its own stream (build -> kernel map -> conv ->
-    # result download) and an upload stream (features and weights) that
-    # overlaps the slot's build; step k's download overlaps step k+1's work.
+def e2e_forward(fvx, torch, wl, K, world):
+    """End to end through the public API with host buffers: every step copies
+    its inputs in from pinned host memory and its result back out, all inside
+    the timed region.  Steps are pipelined two deep, as a serving loop would
+    run them: each slot has its own stream (build -> kernel map -> conv ->
+    result download) and an upload stream (features and weights) that
+    overlaps the slot's build; step k's download overlaps step k+1's work."""
+    dev = wl.dev
     n_e2e = max(2, min(K, 10))
     main_s = [torch.cuda.Stream(device=dev) for _ in range(2)]
     up_s = [torch.cuda.Stream(device=dev) for _ in range(2)]
-    cd_slot = [torch.empty_like(coords) for _ in range(2)]
-    xd_slot = [torch.empty_like(x) for _ in range(2)]
-    Wd_slot = [[torch.empty_like(t_) for t_ in Ws] for _ in range(2)]
-    ys_slot = [[torch.empty_like(y_) for y_ in ys] for _ in range(2)]
-    y_h = [torch.empty(ys[-1].shape, dtype=ys[-1].dtype).pin_memory() for _ in range(2)]
+    cd_slot = [torch.empty_like(wl.coords) for _ in range(2)]
+    xd_slot = [torch.empty_like(wl.x) for _ in range(2)]
+    Wd_slot = [[torch.empty_like(t_) for t_ in wl.Ws] for _ in range(2)]
+    ys_slot = [[torch.empty_like(y_) for y_ in wl.ys] for _ in range(2)]
+    y_h = [torch.empty(wl.ys[-1].shape, dtype=wl.ys[-1].dtype).pin_memory() for _ in range(2)]
     conv_done = [None, None]
     up_done = [None, None]
 
@@ -438,9 +526,9 @@ def bench_fvx(args, world, rank, local):
         with torch.cuda.stream(us):
             if conv_done[sl] is not None:
                 us.wait_event(conv_done[sl])  # the slot's previous step has read its inputs
-            cd_slot[sl].copy_(coords_h, non_blocking=True)
-            xd_slot[sl].copy_(x_h, non_blocking=True)
-            for d_, h_ in zip(Wd_slot[sl], W_h):
+            cd_slot[sl].copy_(wl.coords_h, non_blocking=True)
+            xd_slot[sl].copy_(wl.x_h, non_blocking=True)
+            for d_, h_ in zip(Wd_slot[sl], wl.W_h):
                 d_.copy_(h_, non_blocking=True)
             ev = torch.cuda.Event()
             ev.record(us)
@@ -451,18 +539,7 @@ def bench_fvx(args, world, rank, local):
         ms = main_s[sl]
         with torch.cuda.stream(ms):
             ms.wait_event(up_done[sl])
-            handles = []
-            g = fvx.Grid.build(cd_slot[sl], offs, stream=ms)
-            handles.append(g)
-            src, gin = xd_slot[sl], g
-            for i, c in enumerate(convs):
-                gout = gin if c["stride"] == 1 else gin.coarsen(c["stride"], stream=ms)
-                if gout is not gin:
-                    handles.append(gout)
-                km = fvx.KernelMap(gin, gout, c["stride"], stream=ms)
-                handles.append(km)
-                fvx.sparse_conv(gin, gout, km, src, Wd_slot[sl][i], out=ys_slot[sl][i], stream=ms)
-                src, gin = ys_slot[sl][i], gout
+            handles = forward_step(fvx, wl, NoRec(), cd_slot[sl], xd_slot[sl], Wd_slot[sl], ys_slot[sl], stream=ms)
             done = torch.cuda.Event()
             done.record(ms)
             conv_done[sl] = done
@@ -490,30 +567,76 @@ def bench_fvx(args, world, rank, local):
     e_end.record(main_s[0])
     torch.cuda.synchronize()
     t_e2e = max_over_ranks(e_start.elapsed_time(e_end) / 1e3, world)
-    e2e = dict(value=round(U * n_e2e * world / t_e2e / 1e6, 2), unit=UNIT,
-               h2d_bytes_per_step=int(coords_h.numel() * 4 + x_h.numel() * x_h.element_size()
-                                      + sum(t_.numel() * t_.element_size() for t_ in W_h)),
-               d2h_bytes_per_step=int(y_h[0].numel() * y_h[0].element_size()),
-               steps=n_e2e, pipeline="2 steps in flight on 2 streams; step k+1's uploads overlap step k")
+    return dict(value=round(wl.U * n_e2e * world / t_e2e / 1e6, 2), unit=UNIT,
+                h2d_bytes_per_step=int(wl.coords_h.numel() * 4 + wl.x_h.numel() * wl.x_h.element_size()
+                                       + sum(t_.numel() * t_.element_size() for t_ in wl.W_h)),
+                d2h_bytes_per_step=int(y_h[0].numel() * y_h[0].element_size()),
+                steps=n_e2e, pipeline="2 steps in flight on 2 streams; step k+1's uploads overlap step k")
+
+
+def bench_fvx(args, world, rank, local):
+    import torch
+
+    from sparse_convolution_gb300 import build_lib
+    import sparse_convolution_gb300 as fvx
+    from sparse_convolution_gb300 import synth
+
+    torch.cuda.set_device(local)
+    build_lib.build()
+    fvx.load()
+    dev = torch.device("cuda", local)
+    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
+    peaks, peak_kind = measured_peaks()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    K = args.steps
+
+    w = make_workload(args.workload, args.scale)
+    wl = Workload(fvx, torch, synth, w, dev)
+    clocks = ClockSampler(local)
+    entry, raw = time_forward(fvx, torch, wl, K, args.warmup, flush, peaks, peak_kind, sm_count, world, clocks)
+    t_total = max_over_ranks(raw["t_total"], world)
+    value = wl.U * K * world / t_total / 1e6
+    # the line's roofline: the conv kernel doing the most arithmetic
+    big = max(range(len(entry["convs"])), key=lambda i: entry["convs"][i]["flops"])
+    cv = entry["convs"][big]
+    roofline = dict(cv["roofline"])
+    same = [c for c in entry["convs"] if c["kernel"] == cv["kernel"]]
+    roofline.update(kernel=cv["kernel"], conv=cv["conv"],
+                    traffic=profiled_traffic(cv["kernel"], w["name"]) if len(same) == 1 else None,
+                    algorithmic_bytes=cv["algorithmic_bytes"], flops=cv["flops"], avg_launch_ms=cv["kernel_ms"],
+                    launches_per_step=1)
+    e2e = e2e_forward(fvx, torch, wl, K, world)
+    del wl
+
+    # the other workloads (parity-test sizes of the same generators at full
+    # size), each timed the same way; the headline's entry comes first
+    per_workload = [entry]
+    if args.all_workloads and args.scale == 1.0 and rank == 0:
+        for name in synth.WORKLOADS:
+            if name == args.workload:
+                continue
+            wo = Workload(fvx, torch, synth, make_workload(name), dev)
+            e, _ = time_forward(fvx, torch, wo, K, args.warmup, flush, peaks, peak_kind, sm_count, 1, None)
+            per_workload.append(e)
+            del wo
+            torch.cuda.empty_cache()
 
     out = dict(metric=METRIC, value=round(value, 2), unit=UNIT, n_gpus=world, steps=K, warmup=args.warmup,
                ms_per_step=round(t_total / K * 1e3, 4), higher_is_better=True, scaling="weak",
-               vs_baseline=None, dtype="f32" if fp32 else "bf16", data="synthetic",
-               config=dict(workload=w["name"], rows=int(w["coords"].shape[0]), active_voxels=U,
-                           pairs=[int(p) for p in pairs],
-                           convs=[f"{c['cin']}->{c['cout']} stride {c['stride']}" for c in convs],
-                           batch=int(len(offs) - 1),
+               vs_baseline=None, dtype="f32" if w["dtype"] == "f32" else "bf16", data="synthetic",
+               config=dict(workload=w["name"], rows=int(w["coords"].shape[0]), active_voxels=entry["active_voxels"],
+                           pairs=[c["pairs"] for c in entry["convs"]],
+                           convs=[c["conv"] for c in entry["convs"]],
+                           mean_active_neighbours=entry["mean_active_neighbours"],
+                           batch=entry["batch"],
                            l2="flushed between steps (256 MB write outside the step events)",
-                           parallelism=f"replicas x{world}"),
-               components=dict(build_kmap_mvoxels_s=round(U * K / (t["build"] + t["kmap"]) / 1e6, 2),
-                               conv_active_pair_tflops=round(sum(flops_i) * K / t["conv"] / 1e12, 4),
-                               build_ms=round(t["build"] / K * 1e3, 4), kmap_ms=round(t["kmap"] / K * 1e3, 4),
-                               conv_ms=round(t["conv"] / K * 1e3, 4), conv_kernels=conv_kernels,
-                               build_kmap_hbm=dict(algorithmic_bytes=int(bk_bytes),
-                                                   achieved_gbs=round(bk_bytes * K / (t["build"] + t["kmap"]) / 1e9, 1),
-                                                   frac=round(bk_bytes * K / (t["build"] + t["kmap"]) / 1e9
-                                                              / peaks["hbm_gbs"], 4))),
-               roofline=roofline, e2e=e2e, gpu_launches=int(launches), clocks=clk)
+                           parallelism=f"replicas x{world}", sm_count=sm_count),
+               components=dict(build_kmap_mvoxels_s=entry["build_kmap_mvoxels_s"],
+                               conv_active_pair_tflops=entry["conv_active_pair_tflops"],
+                               build_ms=entry["build_ms"], kmap_ms=entry["kmap_ms"], conv_ms=entry["conv_ms"],
+                               conv_kernels=raw["kernels"], build_kmap_hbm=entry["build_kmap_hbm"],
+                               per_workload=per_workload),
+               roofline=roofline, e2e=e2e, gpu_launches=int(raw["launches"]), clocks=raw["clocks"])
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w)
     return out
@@ -658,9 +781,9 @@ def bench_backward(args, world, rank, local):
             roofline = dict(bound="tensor", achieved=round(ach, 2), peak=peaks["bf16_tflops"], unit="TFLOP/s",
                             peak_source=f"{peak_kind} (bf16_tflops, burst)")
         else:
-            peak = 152 * 128 * 2 * 2.07e9 / 1e12
+            peak, src = ffma_peak(torch.cuda.get_device_properties(dev).multi_processor_count, peaks)
             roofline = dict(bound="alu", achieved=round(ach, 3), peak=round(peak, 1), unit="TFLOP/s",
-                            peak_source="derived: 152 SMs x 128 FP32 lanes x 2 x 2.07 GHz")
+                            peak_source=src)
         roofline.update(kernel=prof_kernel, frac=round(roofline["achieved"] / roofline["peak"], 4),
                         traffic=profiled_traffic(prof_kernel, w["name"]) if len(mine) == 1 else None,
                         flops=int(wflops / max(1, prof_n // K)), avg_launch_ms=round(prof_ms / prof_n, 5),
@@ -727,31 +850,35 @@ def bench_backward(args, world, rank, local):
 
 # ---------------------------------------------------------------- reference arm (the oracle)
 def bench_reference(args, world, rank):
+    """The oracle, as it stands, single-threaded on the host: W + K passes
+    over the crop that the fvx line's cpu_baseline times (oracle_sample), each
+    pass build + kernel map + conv of the workload's layers."""
     if rank != 0:
         return None
     import oracle
 
     oracle.build()
     w = make_workload(args.workload, args.scale)
-    coords, offs, desc = oracle_sample(w, target_rows=120_000)
-    cv = w["convs"][0]
+    coords, offs, desc = oracle_sample(w)
     for _ in range(args.warmup):
         run_oracle_step(coords, offs, w["convs"], 1)
-    times, n = [], 0
+    n, tb, tc, fl = 0, 0.0, 0.0, 0.0
     for _ in range(args.steps):
-        t0 = time.perf_counter()
-        n = run_oracle_step(coords, offs, w["convs"], 1)
-        times.append(time.perf_counter() - t0)
-    tot = sum(times)
+        n, b, c, fl = run_oracle_step(coords, offs, w["convs"], 1)
+        tb, tc = tb + b, tc + c
+    tot = tb + tc
     value = n * args.steps / tot / 1e6
-    cb = dict(value=round(value, 4), unit=UNIT, cores=1, kind="oracle",
-              sample=f"{desc}: build+kmap+conv of {n} voxels per step, single-threaded", host_cores=os.cpu_count())
-    return dict(impl="reference", metric=METRIC, value=round(value, 4), unit=UNIT, n_gpus=world, steps=args.steps,
+    cb = dict(value=round(value, 6), unit=UNIT, cores=1, kind="oracle",
+              sample=f"{desc}: oracle build + kernel map + conv of {n} voxels per pass, {args.steps} passes, "
+                     f"single-threaded",
+              build_kmap_mvoxels_s=round(n * args.steps / tb / 1e6, 6),
+              conv_active_pair_gflops=round(fl * args.steps / tc / 1e9, 4), host_cores=os.cpu_count())
+    return dict(impl="reference", metric=METRIC, value=round(value, 6), unit=UNIT, n_gpus=world, steps=args.steps,
                 warmup=args.warmup, ms_per_step=round(tot / args.steps * 1e3, 2), higher_is_better=True,
                 scaling="weak", vs_baseline=None, dtype="f64", data="synthetic",
                 config=dict(workload=w["name"], sample=desc,
                             convs=[f"{c['cin']}->{c['cout']} stride {c['stride']}" for c in w["convs"]]),
-                cpu_baseline=cb, e2e=dict(value=round(value, 4), unit=UNIT, h2d_bytes_per_step=0,
+                cpu_baseline=cb, e2e=dict(value=round(value, 6), unit=UNIT, h2d_bytes_per_step=0,
                                           d2h_bytes_per_step=0))
 
 

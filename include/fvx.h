@@ -337,6 +337,11 @@ uint64_t fvx_launch_count(void);
  * Pass NULL to disable. */
 fvx_status fvx_profile_enable(const char* kernel_name);
 fvx_status fvx_profile_read(double* total_ms, int64_t* launches);
+/* The same timed launches one by one, in launch order: writes the duration
+ * in milliseconds of the first min(cap, launches) of them to ms_each (host
+ * array of cap doubles) and the number of timed launches to *launches.
+ * Errors: FVX_ERR_INVALID_ARG for a NULL output or cap < 0. */
+fvx_status fvx_profile_read_each(double* ms_each, int64_t cap, int64_t* launches);
 
 #ifdef __cplusplus
 }

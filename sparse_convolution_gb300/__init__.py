@@ -77,6 +77,7 @@ def load():
         "fvx_launch_count": ([], U64),
         "fvx_profile_enable": ([ctypes.c_char_p], I32),
         "fvx_profile_read": ([P, P], I32),
+        "fvx_profile_read_each": ([P, ctypes.c_int64, P], I32),
         "fvx_set_conv_algo": ([I32], I32),
         "fvx_last_conv_algo": ([], I32),
     }
@@ -370,3 +371,11 @@ def profile_read():
     ms, n = ctypes.c_double(), ctypes.c_int64()
     _check(load().fvx_profile_read(ctypes.byref(ms), ctypes.byref(n)))
     return float(ms.value), int(n.value)
+
+
+def profile_read_each(cap=4096):
+    """Durations (ms) of the timed launches, in launch order."""
+    buf = (ctypes.c_double * cap)()
+    n = ctypes.c_int64()
+    _check(load().fvx_profile_read_each(buf, cap, ctypes.byref(n)))
+    return [float(buf[i]) for i in range(min(cap, n.value))]

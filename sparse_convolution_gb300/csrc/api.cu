@@ -249,6 +249,26 @@ fvx_status fvx_profile_read(double* total_ms, int64_t* launches) {
   return FVX_OK;
 }
 
+fvx_status fvx_profile_read_each(double* ms_each, int64_t cap, int64_t* launches) {
+  if (!launches || cap < 0 || (cap > 0 && !ms_each)) {
+    set_error("fvx_profile_read_each: NULL output or negative cap");
+    return FVX_ERR_INVALID_ARG;
+  }
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  int64_t i = 0;
+  for (auto& p : g_prof_events) {
+    if (i < cap) {
+      FVX_CUDA(cudaEventSynchronize(p.b));
+      float ms = 0;
+      FVX_CUDA(cudaEventElapsedTime(&ms, p.a, p.b));
+      ms_each[i] = ms;
+    }
+    ++i;
+  }
+  *launches = (int64_t)g_prof_events.size();
+  return FVX_OK;
+}
+
 fvx_status fvx_device_status(fvx_stream stream) {
   uint32_t* w = device_status_word();
   if (!w) {

@@ -146,19 +146,26 @@ def narrow_band_voxels(rng, box=2048, rmin=20.0, rmax=150.0, band=1.5, min_voxel
 def _band_union(parts, spheres, band, box):
     v = np.concatenate(parts, axis=0) if parts else np.zeros((0, 3), np.int64)
     key = (v[:, 0] * box + v[:, 1]) * box + v[:, 2]
-    key = np.unique(key)
+    key.sort()
+    if key.shape[0]:
+        key = key[np.concatenate([[True], key[1:] != key[:-1]])]
     v = np.stack([key // (box * box), (key // box) % box, key % box], axis=1)
-    # union SDF = min_s(|p - c_s| - r_s); drop voxels deep inside another sphere
+    # union SDF = min_s(|p - c_s| - r_s); drop voxels deep inside another
+    # sphere.  Rows are sorted by x, so the voxels within a sphere's x extent
+    # form one slice.
     p = v + 0.5
     keep = np.ones(v.shape[0], dtype=bool)
     for ctr, r in spheres:
-        near = np.all(np.abs(p - ctr) <= r, axis=1)
+        a = np.searchsorted(p[:, 0], ctr[0] - r, side="left")
+        b = np.searchsorted(p[:, 0], ctr[0] + r, side="right")
+        if a >= b:
+            continue
+        ps = p[a:b]
+        near = np.all(np.abs(ps - ctr) <= r, axis=1)
         if not near.any():
             continue
-        d = np.sqrt(((p[near] - ctr) ** 2).sum(axis=1)) - r
-        bad = np.zeros(v.shape[0], dtype=bool)
-        bad[np.nonzero(near)[0][d < -band]] = True
-        keep &= ~bad
+        d = np.sqrt(((ps[near] - ctr) ** 2).sum(axis=1)) - r
+        keep[a + np.nonzero(near)[0][d < -band]] = False
     return v[keep].astype(np.int32)
 
 
@@ -166,7 +173,9 @@ def lidar_points(rng, beams=64, azimuths=2048, el_lo=-25.0, el_hi=3.0, height=1.
                  box_lo=1.0, box_hi=5.0, extent=72.0, keep_out=3.0, returns=5, jitter=0.02):
     """A spinning LiDAR at the origin, ``height`` above a ground plane, with
     ``n_boxes`` axis-aligned boxes resting on the ground.  Each ray keeps its
-    nearest hit; each hit gives ``returns`` points jittered by N(0, jitter)."""
+    nearest hit; each hit gives ``returns`` points whose measured range is
+    jittered by N(0, jitter), i.e. each point moves along its own ray (range
+    noise, the error a time-of-flight sensor makes)."""
     el = np.deg2rad(np.linspace(el_lo, el_hi, beams))
     az = np.arange(azimuths) * (2.0 * np.pi / azimuths)
     E, A = np.meshgrid(el, az, indexing="ij")
@@ -193,15 +202,17 @@ def lidar_points(rng, beams=64, azimuths=2048, el_lo=-25.0, el_hi=3.0, height=1.
         hit = (tmax >= np.maximum(tmin, 0.0)) & (tmin > 0)
         t = np.where(hit & (tmin < t), tmin, t)
     ok = np.isfinite(t)
-    p = d[ok] * t[ok, None]
-    p = np.repeat(p, returns, axis=0) + rng.normal(0.0, jitter, size=(p.shape[0] * returns, 3))
-    return p
+    dr = np.repeat(d[ok], returns, axis=0)
+    tr = np.repeat(t[ok], returns) + rng.normal(0.0, jitter, size=dr.shape[0])
+    return dr * tr[:, None]
 
 
-def voxelize(points, voxel=0.1, lo=(-72.0, -72.0, -2.0), hi=(72.0, 72.0, 2.0)):
-    """Signed voxel coordinates floor(p / voxel) of the points inside [lo, hi)."""
+def voxelize(points, voxel=0.1, lo=(-72.0, -72.0, -2.0), hi=(72.0, 72.0, 2.0), shift=(0.0, 0.0, 0.0)):
+    """Signed voxel coordinates floor((p + shift) / voxel) of the points whose
+    shifted position lies inside [lo, hi) (lo, hi multiples of ``voxel``)."""
     lo = np.asarray(lo)
     hi = np.asarray(hi)
+    points = points + np.asarray(shift, dtype=np.float64)
     inside = np.all((points >= lo) & (points < hi), axis=1)
     ijk = np.floor(points[inside] / voxel).astype(np.int64)
     lo_i = np.round(lo / voxel).astype(np.int64)
@@ -271,13 +282,19 @@ def narrow_band(seed=3, scale=1.0, min_voxels=8_000_000):
 
 
 def lidar(seed=4, scale=1.0):
-    """64 beams x 2048 azimuths, ground + 60 boxes, 5 jittered returns per hit,
-    0.1 m voxels over [-72,72)^2 x [-2,2) m (signed coords, duplicates kept);
-    bf16 128 -> 128 submanifold, then 128 -> 256 stride 2."""
+    """64 beams x 2048 azimuths, ground + 60 boxes, 5 returns per hit with
+    N(0, 0.02 m) range noise, 0.1 m voxels over a 1440 x 1440 x 40 grid
+    (signed coords, duplicates kept); bf16 128 -> 128 submanifold, then
+    128 -> 256 stride 2.
+
+    The grid's vertical placement is not given: its 40 voxel layers span
+    [-1.85, 2.15) m around the sensor, so the ground plane (1.8 m below it)
+    runs through the middle of a layer instead of along a layer boundary,
+    where the noise would split every ground voxel into two layers."""
     rng = np.random.default_rng(seed)
     az = max(64, int(round(2048 * scale)))
     p = lidar_points(rng, azimuths=az)
-    c = voxelize(p)
+    c = voxelize(p, shift=(0.0, 0.0, 0.05))
     out = _finish([c], rng)
     out["n_unique"] = None  # rows carry duplicates; the unique count is the build's job
     out.update(name=f"lidar_{az}az", dtype="bf16",
