@@ -265,9 +265,18 @@ fvx_conv_algo fvx_last_conv_algo(void);
  *     zero: calls that overlap on the GPU (other streams, other threads) race;
  *     order them on one stream.
  *   - A bounded device-side wait that gives up is recorded in that array's
- *     status word, which fvx_device_status does not read. */
+ *     status word, which each call clears when it starts and
+ *     fvx_noalloc_status reads (fvx_device_status does not). */
 fvx_status fvx_sparse_conv_noalloc(fvx_grid gin, fvx_grid gout, fvx_kmap m, fvx_dtype dt, const void* feats,
                                    int64_t cin, const void* W, int64_t cout, void* out, fvx_stream stream);
+
+/* Status of the last fvx_sparse_conv_noalloc call on the current device,
+ * without allocating: synchronises `stream`, reads the status word of the
+ * fixed scratch array into a host variable, clears it, and returns FVX_OK,
+ * FVX_ERR_DEVICE_TIMEOUT (a bounded wait gave up; the output is incomplete)
+ * or FVX_ERR_CHECK.  Call it after each no-alloc call whose result matters:
+ * the next call clears the word. */
+fvx_status fvx_noalloc_status(fvx_stream stream);
 
 /* ---------------------------------------------------------------------------
  * Backward pass of fvx_sparse_conv  [fVDB-notes, "Limitations and future

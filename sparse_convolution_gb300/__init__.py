@@ -67,6 +67,8 @@ def load():
         "fvx_kmap_view": ([P, PP, PP, PP, PP, P, P], I32),
         "fvx_sparse_conv": ([P, P, P, I32, P, I64, P, I64, P, P], I32),
         "fvx_sparse_conv_noalloc": ([P, P, P, I32, P, I64, P, I64, P, P], I32),
+        "fvx_noalloc_status": ([P], I32),
+        "fvx_testing_bounded_wait": ([I32, U64, P], I32),
         "fvx_sparse_conv_dgrad": ([P, P, P, I32, P, I64, P, I64, P, P], I32),
         "fvx_sparse_conv_wgrad": ([P, P, P, I32, P, I64, P, I64, P, P], I32),
         "fvx_grid_destroy": ([P], I32),
@@ -345,6 +347,12 @@ def sparse_conv_wgrad(gin: Grid, gout: Grid, kmap: KernelMap, feats, dout, out=N
 
 def device_status(stream=None):
     _check(load().fvx_device_status(_stream(stream)))
+
+
+def noalloc_status(stream=None):
+    """Status of the last fvx_sparse_conv_noalloc call (raises FvxError on a
+    recorded timeout or check failure)."""
+    _check(load().fvx_noalloc_status(_stream(stream)))
 
 
 def set_conv_algo(algo: int) -> None:

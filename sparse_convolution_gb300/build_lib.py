@@ -30,7 +30,7 @@ def _nvcc():
 
 
 def _deps():
-    return glob.glob(os.path.join(CSRC, "*")) + [os.path.join(ROOT, "include", "fvx.h"), __file__]
+    return glob.glob(os.path.join(CSRC, "*")) + glob.glob(os.path.join(ROOT, "include", "*.h")) + [__file__]
 
 
 def needs_build() -> bool:

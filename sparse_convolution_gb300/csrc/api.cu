@@ -13,6 +13,7 @@
 #include <vector>
 
 #include "fvx_internal.cuh"
+#include "../../include/fvx_testing.h"
 
 namespace fvx {
 
@@ -66,6 +67,8 @@ static cudaMemPool_t library_pool() {
   return pools[dev];
 }
 
+thread_local const char* t_entry = nullptr;
+
 void* dalloc(size_t bytes, cudaStream_t s) {
   if (bytes == 0) bytes = 256;
   void* p = nullptr;
@@ -79,7 +82,7 @@ void* dalloc(size_t bytes, cudaStream_t s) {
       p = nullptr;
     }
   }
-  if (!p) set_error("device allocation of %zu bytes failed", bytes);
+  if (!p) set_error("%s: device allocation of %zu bytes failed", t_entry ? t_entry : "fvx", bytes);
   return p;
 }
 
@@ -267,6 +270,24 @@ fvx_status fvx_profile_read_each(double* ms_each, int64_t cap, int64_t* launches
   }
   *launches = (int64_t)g_prof_events.size();
   return FVX_OK;
+}
+
+fvx_status fvx_testing_bounded_wait(int32_t kind, uint64_t limit_ns, fvx_stream stream) {
+  if ((kind != 0 && kind != 1) || limit_ns < 1000ull || limit_ns > 2000000000ull) {
+    set_error("fvx_testing_bounded_wait: kind must be 0 or 1 and 1 us <= limit_ns <= 2 s (got %d, %llu)", kind,
+              (unsigned long long)limit_ns);
+    return FVX_ERR_INVALID_ARG;
+  }
+  uint32_t* w = device_status_word();
+  if (!w) {
+    set_error("fvx_testing_bounded_wait: could not set up the device status word");
+    return FVX_ERR_CUDA;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  if (kind == 0) return testing_mbar_wait(limit_ns, w, s);
+  // a word of the status block that is zeroed when the block is set up and
+  // never written: a published flag that nothing sets
+  return testing_flag_wait(reinterpret_cast<const uint64_t*>(w + 16), limit_ns, w, s);
 }
 
 fvx_status fvx_device_status(fvx_stream stream) {

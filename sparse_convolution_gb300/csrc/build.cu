@@ -973,6 +973,7 @@ extern "C" {
 
 fvx_status fvx_build_grid(const int32_t* coords, int64_t n_rows, const int64_t* batch_offsets, int32_t B,
                           fvx_stream stream, fvx_grid* out) {
+  EntryScope entry_("fvx_build_grid");
   if (!out || !batch_offsets || (n_rows > 0 && !coords)) {
     set_error("fvx_build_grid: NULL argument");
     return FVX_ERR_INVALID_ARG;
@@ -1010,6 +1011,7 @@ fvx_status fvx_build_grid(const int32_t* coords, int64_t n_rows, const int64_t* 
 
 fvx_status fvx_lookup(fvx_grid g, const int32_t* coords, const int32_t* batch_idx, int64_t n, int32_t* out_idx,
                       fvx_stream stream) {
+  EntryScope entry_("fvx_lookup");
   if (!g || n < 0 || (n > 0 && (!coords || !out_idx))) {
     set_error("fvx_lookup: bad argument");
     return FVX_ERR_INVALID_ARG;
@@ -1024,6 +1026,7 @@ fvx_status fvx_lookup(fvx_grid g, const int32_t* coords, const int32_t* batch_id
 }
 
 fvx_status fvx_coarsen(fvx_grid g, int32_t stride, fvx_stream stream, fvx_grid* out) {
+  EntryScope entry_("fvx_coarsen");
   if (!g || !out || stride < 1) {
     set_error("fvx_coarsen: bad argument (stride must be >= 1)");
     return FVX_ERR_INVALID_ARG;
@@ -1051,6 +1054,7 @@ fvx_status fvx_coarsen(fvx_grid g, int32_t stride, fvx_stream stream, fvx_grid* 
 }
 
 fvx_status fvx_refine(fvx_grid g, int32_t factor, fvx_stream stream, fvx_grid* out) {
+  EntryScope entry_("fvx_refine");
   if (!g || !out || factor < 1) {
     set_error("fvx_refine: bad argument (factor must be >= 1)");
     return FVX_ERR_INVALID_ARG;

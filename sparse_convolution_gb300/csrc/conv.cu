@@ -167,12 +167,13 @@ __device__ __forceinline__ uint32_t mbar_try(uint32_t bar, uint32_t parity) {
 // in the status word.  Returns false on give-up.  The clock and the status
 // word (an L2 round trip) are checked only every 1024 polls so that a
 // completed phase is seen at once.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* status) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* status,
+                                          unsigned long long limit_ns = kWaitNs) {
   if (mbar_try(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try(bar, parity)) return true;
-    if ((it & 1023u) == 0u && (globaltimer() - t0 > kWaitNs || *(volatile uint32_t*)status != 0u)) {
+    if ((it & 1023u) == 0u && (globaltimer() - t0 > limit_ns || *(volatile uint32_t*)status != 0u)) {
       report_device_error(status, DEV_TIMEOUT);
       return false;
     }
@@ -703,6 +704,9 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tc(const __grid_c
         if (nst > 0) umma_commit(smem_u32(&h.acc_full[b]));
         else mbar_arrive(smem_u32(&h.acc_full[b]));
       }
+      // every MMA has completed before tensor memory is freed (after a
+      // give-up the epilogue may not have waited for them)
+      if (i > 0) mbar_drain(smem_u32(&h.acc_full[(i - 1) & 1]), (uint32_t)(((i - 1) >> 1) & 1));
     }
     __syncwarp();
   } else {
@@ -975,6 +979,9 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tma(const __grid_
         if (nst > 0) umma_commit(smem_u32(&h.acc_full[b]));
         else mbar_arrive(smem_u32(&h.acc_full[b]));
       }
+      // every MMA has completed before tensor memory is freed (after a
+      // give-up the epilogue may not have waited for them)
+      if (i > 0) mbar_drain(smem_u32(&h.acc_full[(i - 1) & 1]), (uint32_t)(((i - 1) >> 1) & 1));
     }
     __syncwarp();
   } else {
@@ -1808,6 +1815,8 @@ __global__ void __launch_bounds__(kWgThreads, 1) k_conv_wgrad_tc(const __grid_co
         umma_commit(smem_u32(&h.acc_full[b]));
         ++i;
       }
+      // every MMA has completed before tensor memory is freed
+      if (i > 0) mbar_drain(smem_u32(&h.acc_full[(i - 1) & 1]), (uint32_t)(((i - 1) >> 1) & 1));
     }
     __syncwarp();
   } else {
@@ -2080,13 +2089,37 @@ fvx_status launch_conv_bf16(const char* who, fvx_grid gin, fvx_kmap m, fvx_dtype
   return FVX_OK;
 }
 
+// ============================================================== test hook
+// The conv kernels' bounded mbarrier wait on a barrier that nothing arrives
+// at: it gives up after limit_ns and records the timeout in the status word.
+__global__ void k_testing_mbar_wait(unsigned long long limit_ns, uint32_t* status) {
+  __shared__ __align__(8) unsigned long long bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0u, status, limit_ns);
+  __syncthreads();
+}
+
 }  // namespace
+
+fvx_status testing_mbar_wait(unsigned long long limit_ns, uint32_t* status, cudaStream_t s) {
+  {
+    LaunchScope ls("testing_mbar_wait", s);
+    k_testing_mbar_wait<<<1, 32, 0, s>>>(limit_ns, status);
+  }
+  return check_launch("testing_mbar_wait");
+}
+
 }  // namespace fvx
 
 using namespace fvx;
 
 extern "C" fvx_status fvx_sparse_conv(fvx_grid gin, fvx_grid gout, fvx_kmap m, fvx_dtype dt, const void* feats,
                                       int64_t cin, const void* W, int64_t cout, void* out, fvx_stream stream) {
+  EntryScope entry_("fvx_sparse_conv");
   if (!gin || !gout || !m || !W || !out || (gin->n_active > 0 && !feats)) {
     set_error("fvx_sparse_conv: NULL argument");
     return FVX_ERR_INVALID_ARG;
@@ -2194,8 +2227,8 @@ extern "C" fvx_status fvx_sparse_conv_noalloc(fvx_grid gin, fvx_grid gout, fvx_k
   }
   cudaStream_t s = (cudaStream_t)stream;
   const int64_t nt = m->n_tiles;
+  if (gout->n_active == 0) return FVX_OK;
   if (dt == FVX_F32) {  // the fp32 kernel needs no scratch at all
-    if (gout->n_active == 0) return FVX_OK;
     {
       LaunchScope ls("conv_f32", s);
       k_conv_f32<<<(unsigned)nt, kRows, 0, s>>>((const float*)feats, (const float*)W, m->out_mask, m->in_idx,
@@ -2226,7 +2259,6 @@ extern "C" fvx_status fvx_sparse_conv_noalloc(fvx_grid gin, fvx_grid gout, fvx_k
   }
   unsigned char* scratch = nullptr;
   FVX_TRY(noalloc_scratch(&scratch));
-  if (gout->n_active == 0) return FVX_OK;
   uint32_t* status = reinterpret_cast<uint32_t*>(scratch);
   __nv_bfloat16* wt = reinterpret_cast<__nv_bfloat16*>(scratch + 256);
   FVX_CUDA(cudaMemsetAsync(status, 0, 4, s));  // the array keeps the previous call's contents
@@ -2240,9 +2272,30 @@ extern "C" fvx_status fvx_sparse_conv_noalloc(fvx_grid gin, fvx_grid gout, fvx_k
   return launch_conv_bf16("fvx_sparse_conv_noalloc", gin, m, dt, feats, cin, cout, out, wt, status, s);
 }
 
+extern "C" fvx_status fvx_noalloc_status(fvx_stream stream) {
+  unsigned char* scratch = nullptr;
+  FVX_TRY(noalloc_scratch(&scratch));
+  cudaStream_t s = (cudaStream_t)stream;
+  uint32_t h = 0;  // pageable host word: the copy allocates nothing
+  FVX_CUDA(cudaMemcpyAsync(&h, scratch, 4, cudaMemcpyDeviceToHost, s));
+  FVX_CUDA(cudaStreamSynchronize(s));
+  FVX_CUDA(cudaMemsetAsync(scratch, 0, 4, s));
+  FVX_CUDA(cudaStreamSynchronize(s));
+  if (h == DEV_TIMEOUT) {
+    set_error("fvx_noalloc_status: a bounded device-side wait gave up in the last fvx_sparse_conv_noalloc call");
+    return FVX_ERR_DEVICE_TIMEOUT;
+  }
+  if (h != DEV_OK) {
+    set_error("fvx_noalloc_status: a device-side check failed in the last fvx_sparse_conv_noalloc call (code %u)", h);
+    return FVX_ERR_CHECK;
+  }
+  return FVX_OK;
+}
+
 extern "C" fvx_status fvx_sparse_conv_wgrad(fvx_grid gin, fvx_grid gout, fvx_kmap m, fvx_dtype dt,
                                             const void* feats, int64_t cin, const void* dout, int64_t cout, float* dW,
                                             fvx_stream stream) {
+  EntryScope entry_("fvx_sparse_conv_wgrad");
   if (!gin || !gout || !m || !dW || (gin->n_active > 0 && !feats) || (gout->n_active > 0 && !dout)) {
     set_error("fvx_sparse_conv_wgrad: NULL argument");
     return FVX_ERR_INVALID_ARG;
@@ -2356,6 +2409,7 @@ extern "C" fvx_status fvx_sparse_conv_wgrad(fvx_grid gin, fvx_grid gout, fvx_kma
 extern "C" fvx_status fvx_sparse_conv_dgrad(fvx_grid gin, fvx_grid gout, fvx_kmap mt, fvx_dtype dt,
                                             const void* dout, int64_t cout, const void* W, int64_t cin, void* dx,
                                             fvx_stream stream) {
+  EntryScope entry_("fvx_sparse_conv_dgrad");
   if (!gin || !gout || !mt || !W || !dx || (gout->n_active > 0 && !dout)) {
     set_error("fvx_sparse_conv_dgrad: NULL argument");
     return FVX_ERR_INVALID_ARG;

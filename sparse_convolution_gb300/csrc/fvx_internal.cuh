@@ -27,6 +27,15 @@ fvx_status cuda_fail(cudaError_t e, const char* what, const char* file, int line
   } while (0)
 
 // ---------------------------------------------------------------- memory
+// Name of the public call this host thread is in, for messages of helpers
+// that do not know it (a failed device allocation names its entry point).
+extern thread_local const char* t_entry;
+struct EntryScope {
+  const char* prev;
+  explicit EntryScope(const char* name) : prev(t_entry) { t_entry = name; }
+  ~EntryScope() { t_entry = prev; }
+};
+
 void* dalloc(size_t bytes, cudaStream_t s);  // NULL on failure (error recorded)
 void dfree(void* p, cudaStream_t s);
 
@@ -84,6 +93,11 @@ fvx_status kmap_read_totals(fvx_kmap_s* m, const char* who);
 uint32_t* device_status_word();  // device pointer (per device, lazily set up)
 
 enum : uint32_t { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_CHECK = 2 };
+
+// Test hooks (fvx_testing_bounded_wait): one bounded wait of each form on
+// something nothing completes, giving up after limit_ns.
+fvx_status testing_mbar_wait(unsigned long long limit_ns, uint32_t* status, cudaStream_t s);
+fvx_status testing_flag_wait(const uint64_t* flag, unsigned long long limit_ns, uint32_t* status, cudaStream_t s);
 
 // ---------------------------------------------------------------- primitives
 // Exclusive scan of n uint32 values (in may equal out).  If total != NULL the

@@ -552,10 +552,12 @@ fvx_status kernel_map_impl(const char* who, fvx_grid gin, fvx_grid gout, int32_t
 
 extern "C" fvx_status fvx_kernel_map(fvx_grid gin, fvx_grid gout, int32_t ksize, int32_t stride, fvx_stream stream,
                                      fvx_kmap* out) {
+  EntryScope entry_("fvx_kernel_map");
   return kernel_map_impl("fvx_kernel_map", gin, gout, ksize, stride, false, stream, out);
 }
 
 extern "C" fvx_status fvx_kernel_map_transposed(fvx_grid gin, fvx_grid gout, int32_t ksize, int32_t stride,
                                                 fvx_stream stream, fvx_kmap* out) {
+  EntryScope entry_("fvx_kernel_map_transposed");
   return kernel_map_impl("fvx_kernel_map_transposed", gin, gout, ksize, stride, true, stream, out);
 }

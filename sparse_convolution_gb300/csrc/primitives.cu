@@ -46,6 +46,10 @@ __device__ __forceinline__ unsigned long long lb_clock() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
+// True once a look-back wait that started at t0 has run past limit_ns.
+__device__ __forceinline__ bool lb_expired(unsigned long long t0, unsigned long long limit_ns) {
+  return lb_clock() - t0 > limit_ns;
+}
 
 // ============================================================== scan
 constexpr int kScanThreads = 256;
@@ -95,7 +99,7 @@ __global__ void __launch_bounds__(kScanThreads) k_scan_1p(In in, uint32_t* out, 
         const uint64_t f = (jj >= 0) ? ld_relaxed_u64(flags + jj) : kLbInc;  // before tile 0: prefix 0
         if (!__all_sync(0xffffffffu, ((f >> 32) & 3u) != 0u)) {
           int give_up = 0;
-          if (lane == 0 && (it & 255u) == 0u && lb_clock() - t0 > kLbWaitNs) give_up = 1;
+          if (lane == 0 && (it & 255u) == 0u && lb_expired(t0, kLbWaitNs)) give_up = 1;
           if (__shfl_sync(0xffffffffu, give_up, 0)) {
             if (lane == 0) report_device_error(status, DEV_TIMEOUT);
             break;
@@ -277,7 +281,7 @@ __global__ void __launch_bounds__(kRsThreads) k_radix_onesweep(const uint64_t* _
           q = r + 1;
         }
         j -= q;
-        if (!done && q < kLbWindow && (it & 63u) == 0u && lb_clock() - t0 > kLbWaitNs) {
+        if (!done && q < kLbWindow && (it & 63u) == 0u && lb_expired(t0, kLbWaitNs)) {
           report_device_error(status, DEV_TIMEOUT);
           break;
         }
@@ -358,6 +362,33 @@ fvx_status radix_sort_pairs(uint64_t* k0, uint32_t* v0, uint64_t* k1, uint32_t* 
   }
   *result_in_1 = in1;
   return FVX_OK;
+}
+
+// ============================================================== test hook
+// One warp polls a published word that nothing sets, the way the scan's
+// look-back polls its predecessors, and gives up after limit_ns the same way:
+// the bounded wait and its status report, without a real wait running out.
+__global__ void k_testing_flag_wait(const uint64_t* flag, unsigned long long limit_ns, uint32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const unsigned long long t0 = lb_clock();
+  for (uint32_t it = 1;; ++it) {
+    const uint64_t f = ld_relaxed_u64(flag);
+    if (__all_sync(0xffffffffu, ((f >> 32) & 3u) != 0u)) return;
+    int give_up = 0;
+    if (lane == 0 && (it & 255u) == 0u && lb_expired(t0, limit_ns)) give_up = 1;
+    if (__shfl_sync(0xffffffffu, give_up, 0)) {
+      if (lane == 0) report_device_error(status, DEV_TIMEOUT);
+      return;
+    }
+  }
+}
+
+fvx_status testing_flag_wait(const uint64_t* flag, unsigned long long limit_ns, uint32_t* status, cudaStream_t s) {
+  {
+    LaunchScope ls("testing_flag_wait", s);
+    k_testing_flag_wait<<<1, 32, 0, s>>>(flag, limit_ns, status);
+  }
+  return check_launch("testing_flag_wait");
 }
 
 }  // namespace fvx

@@ -174,26 +174,30 @@ def neighbours_independent(uniq_in, ijk_out, b_out, stride, rows):
     return res
 
 
-def check_kmap_sampled(km, uniq_in, ijk_out, b_out, stride, rows):
+def check_kmap_full(km, uniq_in, ijk_out, b_out, stride):
+    """Every output's 27 neighbours, list by list: list s must hold exactly
+    the outputs whose position stride*ijk + d_s is an input voxel, in
+    ascending order, each with that voxel's index (searchsorted in the sorted
+    canonical keys of the input grid); the masks must agree."""
     ii, oo, mm = (np_(t) for t in km.pairs())
     offs = km.offsets
     assert offs[0] == 0 and np.all(np.diff(offs) >= 0) and offs[27] == km.n_pairs
-    mm = mm.astype(np.uint64)
-    assert int(H.popcount64(mm).sum()) == km.n_pairs
+    n_out = ijk_out.shape[0]
+    mask = np.zeros(n_out, np.uint32)
+    base = stride * ijk_out.astype(np.int64)
+    last = uniq_in.shape[0] - 1
     for s in range(27):
-        seg = oo[offs[s]:offs[s + 1]]
-        assert np.all(np.diff(seg) > 0), f"list {s} not ordered by output"
-    exp = neighbours_independent(uniq_in, ijk_out, b_out, stride, rows)
-    for s in range(27):
+        d = np.array([s // 9 - 1, (s // 3) % 3 - 1, s % 3 - 1], np.int64)
+        k = H.key64(b_out, base + d)
+        pos = np.searchsorted(uniq_in, k)
+        np.minimum(pos, last, out=pos)
+        hit = uniq_in[pos] == k
         seg_o = oo[offs[s]:offs[s + 1]]
         seg_i = ii[offs[s]:offs[s + 1]]
-        pos = np.searchsorted(seg_o, rows)
-        posc = np.minimum(pos, max(seg_o.shape[0] - 1, 0))
-        found = (seg_o.shape[0] > 0) & (seg_o[posc] == rows) if seg_o.shape[0] else np.zeros(rows.shape, bool)
-        got = np.where(found, seg_i[posc] if seg_o.shape[0] else -1, -1)
-        assert np.array_equal(got, exp[:, s]), f"offset {s}"
-        assert np.array_equal(((mm[rows] >> np.uint64(s)) & np.uint64(1)).astype(bool), exp[:, s] >= 0)
-    return exp
+        assert np.array_equal(seg_o, np.flatnonzero(hit)), f"list {s}: outputs"
+        assert np.array_equal(seg_i, pos[hit]), f"list {s}: inputs"
+        mask[hit] |= np.uint32(1 << s)
+    assert np.array_equal(mm.astype(np.uint32), mask)
 
 
 def conv_rows_independent(nbr, x64, W64):

@@ -21,8 +21,8 @@ def lib():
     return fvx.load()
 
 
-def _declared():
-    txt = open(os.path.join(ROOT, "include", "fvx.h")).read()
+def _declared(header="fvx.h"):
+    txt = open(os.path.join(ROOT, "include", header)).read()
     txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
     return sorted(set(re.findall(r"\b(fvx_[a-z_0-9]+)\s*\(", txt)))
 
@@ -32,8 +32,12 @@ def test_header_declares_the_boundary():
     for n in ("fvx_build_grid", "fvx_kernel_map", "fvx_sparse_conv", "fvx_lookup", "fvx_coarsen",
               "fvx_grid_view", "fvx_kmap_view", "fvx_grid_destroy", "fvx_kmap_destroy", "fvx_set_allocator",
               "fvx_status_string", "fvx_last_error", "fvx_refine", "fvx_kernel_map_transposed",
-              "fvx_sparse_conv_dgrad", "fvx_sparse_conv_wgrad"):
-        assert n in names
+              "fvx_sparse_conv_dgrad", "fvx_sparse_conv_wgrad", "fvx_sparse_conv_noalloc", "fvx_noalloc_status",
+              "fvx_set_conv_algo", "fvx_last_conv_algo", "fvx_device_status", "fvx_grid_counts",
+              "fvx_grid_batch_offsets", "fvx_launch_count", "fvx_profile_enable", "fvx_profile_read",
+              "fvx_profile_read_each"):
+        assert n in names, n
+    assert _declared("fvx_testing.h") == ["fvx_testing_bounded_wait"]
 
 
 def test_header_is_plain_c(tmp_path):
@@ -46,15 +50,25 @@ def test_header_is_plain_c(tmp_path):
     if cc is None:
         pytest.skip("no C compiler")
     src = tmp_path / "use.c"
-    src.write_text('#include "fvx.h"\nint main(void) { fvx_grid g = 0; (void)g; return (int)FVX_OK; }\n')
+    src.write_text('#include "fvx.h"\n#include "fvx_testing.h"\n'
+                   'int main(void) { fvx_grid g = 0; (void)g; return (int)FVX_OK; }\n')
     r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
                         "-fsyntax-only", str(src)], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
 
 
 def test_library_exports_every_declared_symbol(lib):
-    missing = [n for n in _declared() if not hasattr(lib, n)]
+    missing = [n for n in _declared() + _declared("fvx_testing.h") if not hasattr(lib, n)]
     assert not missing, missing
+
+
+def test_testing_hook_validates_on_host(lib):
+    """The bounded-wait test hook refuses a kind or limit outside its range
+    before any device work."""
+    assert lib.fvx_testing_bounded_wait(2, 10_000, None) == 1
+    assert lib.fvx_testing_bounded_wait(0, 10, None) == 1
+    assert lib.fvx_testing_bounded_wait(1, 3_000_000_000, None) == 1
+    assert b"fvx_testing_bounded_wait" in lib.fvx_last_error()
 
 
 def test_status_strings(lib):

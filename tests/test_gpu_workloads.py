@@ -3,8 +3,9 @@
 Reduced sizes: bit-exact topology and kernel maps against the CPU oracle, conv
 against the oracle within tolerance.  Full sizes (the sizes the benchmark
 times): topology bit-exact against an independent numpy derivation from the
-sorted unique keys, kernel maps exact on sampled outputs, conv within tolerance
-on sampled output rows recomputed in numpy fp64.
+sorted unique keys, kernel maps bit-exact on every output and slot (numpy
+searchsorted in the sorted keys), conv within tolerance on sampled output rows
+recomputed in numpy fp64.
 """
 import numpy as np
 import pytest
@@ -88,7 +89,7 @@ def test_batched_reduced_oracle(cuda_device):
 
 # ---------------------------------------------------------------- full sizes
 
-def _full_size(w, n_kmap_rows=100_000, n_conv_rows=3000):
+def _full_size(w, n_conv_rows=3000):
     import torch
 
     import sparse_convolution_gb300 as fvx
@@ -110,8 +111,7 @@ def _full_size(w, n_kmap_rows=100_000, n_conv_rows=3000):
             assert np.array_equal(H.key64(vb_out, t["ijk"]), exp)
             ijk_out = t["ijk"]
         km = fvx.KernelMap(g, gout, stride)
-        rows = rng.choice(gout.n_active, size=min(n_kmap_rows, gout.n_active), replace=False)
-        G.check_kmap_sampled(km, uniq, ijk_out, vb_out, stride, np.sort(rows))
+        G.check_kmap_full(km, uniq, ijk_out, vb_out, stride)
         if x is None:
             if w["dtype"] == "f32":
                 x = torch.from_numpy(synth.features(w["seed"] + 10, g.n_active, cv["cin"], w["feat_kind"])).cuda()

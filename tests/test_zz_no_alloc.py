@@ -55,6 +55,7 @@ def test_noalloc_matches_allocating_conv(cuda_device, cin, cout, out_bf16):
         got = torch.full((g.n_active, cout), float("nan"), device="cuda", dtype=odt)
         assert _call(lib.fvx_sparse_conv, g, km, dt, x, W, ref) == 0, lib.fvx_last_error()
         assert _call(lib.fvx_sparse_conv_noalloc, g, km, dt, x, W, got) == 0, lib.fvx_last_error()
+        assert lib.fvx_noalloc_status(ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)) == 0
         torch.cuda.synchronize()
         # same kernel and arithmetic: within the conv tolerance (2e-3 * sum|w*x|),
         # and in fact identical
@@ -115,3 +116,59 @@ def test_noalloc_leaf_kernel(cuda_device):
             assert torch.equal(got, ref)
     finally:
         fvx.set_conv_algo(fvx.FVX_CONV_AUTO)
+
+
+ALLOC_FN = ctypes.CFUNCTYPE(ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p)
+FREE_FN = ctypes.CFUNCTYPE(None, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p)
+
+
+def test_noalloc_calls_no_allocator(cuda_device):
+    """With an allocator installed that refuses every request and counts
+    them, the no-alloc entry point (called here before any allocating
+    convolution in this test) runs, is never asked for memory, and matches
+    fvx_sparse_conv called afterwards with the default allocator."""
+    import torch
+
+    import sparse_convolution_gb300 as fvx
+
+    lib = fvx.load()
+    g, km = _grid_and_map(31)
+    gen = torch.Generator(device="cuda").manual_seed(31)
+    x = torch.randn(g.n_active, 32, device="cuda", generator=gen).bfloat16()
+    W = (torch.randn(27, 32, 64, device="cuda", generator=gen) / 30.0).bfloat16()
+    got = [torch.full((g.n_active, 64), float("nan"), device="cuda") for _ in range(2)]
+    calls = []
+    refuse = ALLOC_FN(lambda n, s, c: calls.append(n) or None)
+    no_free = FREE_FN(lambda p, s, c: calls.append(-1))
+    torch.cuda.synchronize()
+    assert lib.fvx_set_allocator(ctypes.cast(refuse, ctypes.c_void_p), ctypes.cast(no_free, ctypes.c_void_p),
+                                 None) == 0
+    try:
+        for out in got:  # two calls in a row
+            assert _call(lib.fvx_sparse_conv_noalloc, g, km, fvx.FVX_BF16, x, W, out) == 0, lib.fvx_last_error()
+            assert lib.fvx_noalloc_status(ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)) == 0
+        torch.cuda.synchronize()
+    finally:
+        lib.fvx_set_allocator(None, None, None)
+    assert calls == [], calls
+    ref = torch.empty(g.n_active, 64, device="cuda")
+    assert _call(lib.fvx_sparse_conv, g, km, fvx.FVX_BF16, x, W, ref) == 0, lib.fvx_last_error()
+    torch.cuda.synchronize()
+    assert torch.equal(got[0], ref) and torch.equal(got[1], ref)
+
+
+def test_noalloc_empty_output_and_errors_match(cuda_device):
+    """An empty output grid returns FVX_OK from both entry points, whatever
+    the channel counts, as fvx_sparse_conv does."""
+    import torch
+
+    import sparse_convolution_gb300 as fvx
+
+    lib = fvx.load()
+    g = fvx.Grid.build(torch.zeros((0, 3), dtype=torch.int32, device="cuda"), [0, 0])
+    km = fvx.KernelMap(g, g, 1)
+    x = torch.zeros(1, 8, device="cuda", dtype=torch.bfloat16)
+    W = torch.zeros(27, 8, 12, device="cuda", dtype=torch.bfloat16)  # 12: not a multiple of 8
+    out = torch.zeros(1, 12, device="cuda")
+    assert _call(lib.fvx_sparse_conv, g, km, fvx.FVX_BF16, x, W, out) == 0
+    assert _call(lib.fvx_sparse_conv_noalloc, g, km, fvx.FVX_BF16, x, W, out) == 0
