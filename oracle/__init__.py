@@ -29,7 +29,7 @@ def build(force: bool = False) -> str:
     """Compile ``liboracle.so`` with the host C++ compiler (portable flags)."""
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".tmp{os.getpid()}"
-        subprocess.check_call(["g++", "-std=c++17", "-O2", "-fPIC", "-shared", "-o", tmp, _SRC])
+        subprocess.check_call(["g++", "-std=c++17", "-O2", "-ffp-contract=off", "-fPIC", "-shared", "-o", tmp, _SRC])
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -63,6 +63,10 @@ def _load():
         "oracle_kmap_export": ([P, P, P, P, P], None),
         "oracle_conv": ([P, P, I64, P, I64, P, P], None),
         "oracle_conv_rows": ([P, P, I32, P, I64, P, I64, P, I64, P, P], None),
+        "oracle_voxels_along_rays": ([P, P, P, P, I64, ctypes.c_float, ctypes.c_float], P),
+        "oracle_rays_hits": ([P], I64),
+        "oracle_rays_export": ([P, P, P, P], None),
+        "oracle_rays_free": ([P], None),
     }
     for name, (args, res) in sigs.items():
         f = getattr(lib, name)
@@ -230,3 +234,27 @@ def conv_rows(gin: Grid, gout: Grid, stride: int, rows: np.ndarray, x: np.ndarra
     _load().oracle_conv_rows(gin._h, gout._h, int(stride), _ptr(rows), rows.shape[0], _ptr(x), cin, _ptr(W), cout,
                              _ptr(y), _ptr(a))
     return y, a
+
+
+def voxels_along_rays(grid: Grid, origins: np.ndarray, dirs: np.ndarray, batch=None, tmin=0.0, tmax=float("inf")):
+    """Active voxels each ray passes through, in order ("fVDB" reading notes,
+    HDDA; the exact definition is in oracle.cpp).  Returns (offsets int64
+    [n+1], voxel index int32 [hits], t float32 [hits, 2] = entry, exit)."""
+    lib = _load()
+    o = np.ascontiguousarray(origins, np.float32).reshape(-1, 3)
+    d = np.ascontiguousarray(dirs, np.float32).reshape(-1, 3)
+    n = o.shape[0]
+    b = None if batch is None else np.ascontiguousarray(batch, np.int32).reshape(-1)
+    h = lib.oracle_voxels_along_rays(grid._h, _ptr(o), _ptr(d), None if b is None else _ptr(b), n,
+                                     ctypes.c_float(tmin), ctypes.c_float(tmax))
+    if not h:
+        raise ValueError("ray batch index out of range")
+    try:
+        nh = int(lib.oracle_rays_hits(h))
+        offs = np.zeros(n + 1, np.int64)
+        vox = np.zeros(nh, np.int32)
+        t = np.zeros((nh, 2), np.float32)
+        lib.oracle_rays_export(h, _ptr(offs), _ptr(vox), _ptr(t))
+    finally:
+        lib.oracle_rays_free(h)
+    return offs, vox, t

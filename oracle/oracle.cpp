@@ -39,6 +39,9 @@
 //     cross-correlation, no kernel flip.
 //   * Conv: y[q,co] = sum_s sum_{(p,q) in list s} sum_ci x[p,ci] * W[s,ci,co],
 //     accumulated in double.  A[q,co] = same sum of |x * w| (tolerance scale).
+//   * Voxels along rays [fVDB-notes, HDDA]: see the definition above
+//     oracle_voxels_along_rays (fp32 plane-crossing times, positive-length
+//     visits of active cells, in order).
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -47,6 +50,8 @@
 #include <vector>
 #include <algorithm>
 #include <array>
+#include <cmath>
+#include <limits>
 
 namespace {
 
@@ -131,6 +136,12 @@ struct oracle_grid {
   std::vector<uint64_t> upper_mask;    // [n_upper][512]
   std::vector<uint32_t> upper_prefix;  // [n_upper][512]
   std::vector<uint32_t> upper_first;   // first child lower-node index
+};
+
+struct oracle_rays {
+  std::vector<int64_t> offsets;  // [n_rays + 1]
+  std::vector<int32_t> voxel;    // active index of each hit
+  std::vector<float> t;          // [hits][2]: t_enter, t_exit
 };
 
 struct oracle_kmap {
@@ -511,5 +522,154 @@ void oracle_conv_rows(const oracle_grid* gin, const oracle_grid* gout, int32_t s
         }
   }
 }
+
+}  // extern "C"
+
+// ---------------------------------------------------------------- voxels along rays
+// [fVDB-notes, HDDA] marches rays through the grid with one DDA per tree level
+// so that empty nodes are crossed in one step; what it yields is the voxels
+// each ray passes through.  This oracle gets the same voxels the slow way: one
+// per-voxel DDA that steps through every cell and asks the map whether the
+// cell is active.
+//
+// Definition (written out here and in the CUDA source; the two share no code):
+//   * voxel (i,j,k) is the cell [i,i+1) x [j,j+1) x [k,k+1) in index space;
+//     the ray is o + t d with fp32 o, d; inv_a = 1 / d_a (fp32, rounded once).
+//   * The ray crosses the plane x_a = n at T_a(n) = ((float)n - o_a) * inv_a,
+//     two fp32 operations each rounded to nearest (no fused multiply-add).
+//   * [tmin, tmax] is clipped to the bounding box [lo, hi + 1) of the batch
+//     element's active voxels by the same plane times (slab method); a
+//     direction component of 0 keeps the ray only if lo_a <= o_a < hi_a + 1;
+//     d = 0 or an empty clip gives no hits.
+//   * At time t the ray is in cell c_a = max{n : T_a(n) <= t} (d_a > 0),
+//     min{n : T_a(n) <= t} - 1 (d_a < 0), floor(o_a) (d_a = 0).
+//   * A hit is an active cell the ray occupies for a time interval of
+//     positive length inside the clipped segment [t0, t1): its index and
+//     [t_enter, t_exit) = the times of the crossings that enter and leave it,
+//     clipped to [t0, t1).  Hits come in order of t_enter.
+// Any box holding all active voxels gives the same hits (cells outside hold
+// none, and a hit's entry crossing is never before the box's), so the CUDA
+// path may clip to a larger box.
+namespace {
+
+float plane_time(int64_t n, float o, float inv) {
+  const float diff = (float)n - o;
+  return diff * inv;
+}
+
+// Cell coordinate along one axis at time t (definition above).
+int64_t cell_at(float o, float d, float inv, float t) {
+  if (d > 0.0f) {
+    int64_t n = (int64_t)std::floor((double)o + (double)t * (double)d);
+    while (plane_time(n + 1, o, inv) <= t) ++n;
+    while (plane_time(n, o, inv) > t) --n;
+    return n;
+  }
+  if (d < 0.0f) {
+    int64_t m = (int64_t)std::floor((double)o + (double)t * (double)d) + 1;
+    while (plane_time(m - 1, o, inv) <= t) --m;
+    while (plane_time(m, o, inv) > t) ++m;
+    return m - 1;
+  }
+  return (int64_t)std::floor((double)o);
+}
+
+void march_one(const oracle_grid* g, const int64_t* lo, const int64_t* hi, int32_t b, const float* o,
+               const float* d, float tmin, float tmax, oracle_rays* out) {
+  if (d[0] == 0.0f && d[1] == 0.0f && d[2] == 0.0f) return;
+  float inv[3];
+  float t0 = tmin, t1 = tmax;
+  for (int a = 0; a < 3; ++a) {
+    if (d[a] == 0.0f) {
+      inv[a] = 0.0f;
+      if (o[a] < (float)lo[a] || o[a] >= (float)(hi[a] + 1)) return;
+      continue;
+    }
+    inv[a] = 1.0f / d[a];
+    float ta = plane_time(lo[a], o[a], inv[a]), tb = plane_time(hi[a] + 1, o[a], inv[a]);
+    if (ta > tb) std::swap(ta, tb);
+    t0 = std::max(t0, ta);
+    t1 = std::min(t1, tb);
+  }
+  if (!(t0 < t1)) return;
+  int64_t c[3];
+  float next[3];
+  const float inf = std::numeric_limits<float>::infinity();
+  for (int a = 0; a < 3; ++a) {
+    c[a] = cell_at(o[a], d[a], inv[a], t0);
+    next[a] = d[a] > 0.0f ? plane_time(c[a] + 1, o[a], inv[a]) : d[a] < 0.0f ? plane_time(c[a], o[a], inv[a]) : inf;
+  }
+  float enter = t0;
+  for (;;) {
+    const float T = std::min(next[0], std::min(next[1], next[2]));
+    const float exit = std::min(T, t1);
+    if (exit > enter) {
+      auto it = g->index.find(Voxel{b, (int32_t)c[0], (int32_t)c[1], (int32_t)c[2]});
+      if (it != g->index.end()) {
+        out->voxel.push_back((int32_t)it->second);
+        out->t.push_back(enter);
+        out->t.push_back(exit);
+      }
+    }
+    if (T >= t1) break;
+    for (int a = 0; a < 3; ++a) {
+      if (next[a] != T) continue;
+      if (d[a] > 0.0f) {
+        c[a] += 1;
+        next[a] = plane_time(c[a] + 1, o[a], inv[a]);
+      } else {
+        c[a] -= 1;
+        next[a] = plane_time(c[a], o[a], inv[a]);
+      }
+    }
+    enter = T;
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+// Rays [n][3] origins and directions (index space, fp32), batch element of
+// each ray (NULL: all 0), one segment [tmin, tmax] for all.  Returns the hits
+// in CSR form (see the definition above); nullptr for a batch out of range.
+oracle_rays* oracle_voxels_along_rays(const oracle_grid* g, const float* origins, const float* dirs,
+                                      const int32_t* batch, int64_t n, float tmin, float tmax) {
+  std::vector<int64_t> lo((size_t)g->B * 3, 0), hi((size_t)g->B * 3, 0);
+  std::vector<char> any((size_t)g->B, 0);
+  for (const Voxel& v : g->voxels) {
+    const int64_t c[3] = {v.i, v.j, v.k};
+    for (int a = 0; a < 3; ++a) {
+      int64_t& l = lo[(size_t)v.b * 3 + a];
+      int64_t& h = hi[(size_t)v.b * 3 + a];
+      if (!any[(size_t)v.b] || c[a] < l) l = c[a];
+      if (!any[(size_t)v.b] || c[a] > h) h = c[a];
+    }
+    any[(size_t)v.b] = 1;
+  }
+  oracle_rays* r = new oracle_rays();
+  r->offsets.push_back(0);
+  for (int64_t q = 0; q < n; ++q) {
+    const int32_t b = batch ? batch[q] : 0;
+    if (b < 0 || b >= g->B) {
+      delete r;
+      return nullptr;
+    }
+    if (any[(size_t)b])
+      march_one(g, &lo[(size_t)b * 3], &hi[(size_t)b * 3], b, origins + 3 * q, dirs + 3 * q, tmin, tmax, r);
+    r->offsets.push_back((int64_t)r->voxel.size());
+  }
+  return r;
+}
+
+int64_t oracle_rays_hits(const oracle_rays* r) { return (int64_t)r->voxel.size(); }
+
+void oracle_rays_export(const oracle_rays* r, int64_t* offsets, int32_t* voxel, float* t) {
+  std::memcpy(offsets, r->offsets.data(), r->offsets.size() * 8);
+  std::memcpy(voxel, r->voxel.data(), r->voxel.size() * 4);
+  std::memcpy(t, r->t.data(), r->t.size() * 4);
+}
+
+void oracle_rays_free(oracle_rays* r) { delete r; }
 
 }  // extern "C"

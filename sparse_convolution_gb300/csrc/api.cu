@@ -154,6 +154,23 @@ fvx_status check_staged_status(const char* who, uint32_t staged, cudaStream_t s)
   return staged == DEV_TIMEOUT ? FVX_ERR_DEVICE_TIMEOUT : FVX_ERR_CHECK;
 }
 
+fvx_status device_sm_count(int* sms) {
+  static int counts[64] = {0};
+  int dev = 0;
+  FVX_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) {
+    set_error("device ordinal %d out of range", dev);
+    return FVX_ERR_RANGE;
+  }
+  if (counts[dev] == 0) {
+    int n = 0;
+    FVX_CUDA(cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev));
+    counts[dev] = n;
+  }
+  *sms = counts[dev];
+  return FVX_OK;
+}
+
 fvx_status check_launch(const char* name) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {

@@ -716,7 +716,9 @@ fvx_status build_grid_device(const int32_t* coords, int64_t n, const int64_t* of
     FVX_TRY(check_launch("build_plan_init"));
     {
       LaunchScope ls("build_plan_reduce", s);
-      unsigned nb = std::min<unsigned>(grid_for((n + 3) / 4, kThreads), 152u * 8u);
+      int sms = 0;
+      FVX_TRY(device_sm_count(&sms));
+      unsigned nb = std::min<unsigned>(grid_for((n + 3) / 4, kThreads), (unsigned)sms * 8u);
       k_plan_reduce<<<nb, kThreads, 0, s>>>(coords, n, plan);
     }
     FVX_TRY(check_launch("build_plan_reduce"));

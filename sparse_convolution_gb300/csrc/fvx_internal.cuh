@@ -82,6 +82,8 @@ struct LaunchScope {
   ~LaunchScope();
 };
 fvx_status check_launch(const char* name);
+// Streaming multiprocessors of the current device (queried once per device).
+fvx_status device_sm_count(int* sms);
 fvx_status check_staged_status(const char* who, uint32_t staged, cudaStream_t s);
 // Kernel map pair lists are allocated for 27 pairs per output (no count
 // read-back) up to this many bytes (environment FVX_KMAP_CAP_BYTES, default
