@@ -574,6 +574,67 @@ def e2e_forward(fvx, torch, wl, K, world):
                 steps=n_e2e, pipeline="2 steps in flight on 2 streams; step k+1's uploads overlap step k")
 
 
+def time_rays(fvx, torch, synth, box, K, warmup, flush, peaks):
+    """Voxels along rays (HDDA) on the narrow-band scene of side ``box`` with
+    a 1024 x 1024 pinhole camera: K whole calls (count pass, scan, one
+    synchronisation for the total, output allocation, write pass), each timed
+    with CUDA events after an L2 flush; per kernel, its launch durations."""
+    w = synth.ray_scene(box)
+    o_h, d_h = synth.camera_rays(box, 1024)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    g = fvx.Grid.build(torch.from_numpy(w["coords"]).to(dev), w["batch_offsets"])
+    o = torch.from_numpy(o_h).to(dev)
+    d = torch.from_numpy(d_h).to(dev)
+    for _ in range(max(1, warmup)):
+        fvx.Hits(g, o, d).destroy()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ts, hits = [], 0
+    for k in range(K):
+        flush.fill_(float(k))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        h = fvx.Hits(g, o, d)
+        e1.record(stream)
+        hits = h.n_hits
+        h.destroy()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    kern = {}
+    for kn in ("rays_count", "rays_write"):
+        fvx.profile_enable(kn)
+        for k in range(K):
+            flush.fill_(float(k))
+            fvx.Hits(g, o, d).destroy()
+        torch.cuda.synchronize()
+        ms, nl = fvx.profile_read()
+        fvx.profile_enable(None)
+        kern[kn + "_ms"] = round(ms / max(1, nl), 5)
+    fvx.device_status()
+    n = o_h.shape[0]
+    ms = statistics.median(ts)
+    # bytes the call must move: rays read by both passes (24 B each), counts
+    # written and read, offsets written (8 B per ray), hits written (4 B
+    # index + 8 B times)
+    alg = 2 * 24 * n + 8 * n + 8 * (n + 1) + 12 * hits
+    out = dict(scene=w["name"], voxels=int(g.n_active), rays=int(n), hits=int(hits),
+               rays_with_hits=int(np.count_nonzero(np.diff(ray_offsets(fvx, g, o, d)) > 0)),
+               ms_per_call=round(ms, 4), mrays_per_s=round(n / ms / 1e3, 2), mhits_per_s=round(hits / ms / 1e3, 2),
+               kernels=kern,
+               hbm=dict(algorithmic_bytes=int(alg), achieved_gbs=round(alg / ms / 1e6, 1),
+                        frac=round(alg / ms / 1e6 / peaks["hbm_gbs"], 4),
+                        note="the walk is bound by dependent node loads per ray, not by bytes"))
+    g.destroy()
+    return out
+
+
+def ray_offsets(fvx, g, o, d):
+    h = fvx.Hits(g, o, d)
+    off = h.arrays()[0].cpu().numpy()
+    h.destroy()
+    return off
+
+
 def bench_fvx(args, world, rank, local):
     import torch
 
@@ -621,6 +682,12 @@ def bench_fvx(args, world, rank, local):
             del wo
             torch.cuda.empty_cache()
 
+    rays = []
+    if args.all_workloads and args.scale == 1.0 and rank == 0:
+        for box in (128, 1024):
+            rays.append(time_rays(fvx, torch, synth, box, K, args.warmup, flush, peaks))
+            torch.cuda.empty_cache()
+
     out = dict(metric=METRIC, value=round(value, 2), unit=UNIT, n_gpus=world, steps=K, warmup=args.warmup,
                ms_per_step=round(t_total / K * 1e3, 4), higher_is_better=True, scaling="weak",
                vs_baseline=None, dtype="f32" if w["dtype"] == "f32" else "bf16", data="synthetic",
@@ -635,7 +702,7 @@ def bench_fvx(args, world, rank, local):
                                conv_active_pair_tflops=entry["conv_active_pair_tflops"],
                                build_ms=entry["build_ms"], kmap_ms=entry["kmap_ms"], conv_ms=entry["conv_ms"],
                                conv_kernels=raw["kernels"], build_kmap_hbm=entry["build_kmap_hbm"],
-                               per_workload=per_workload),
+                               per_workload=per_workload, rays=rays),
                roofline=roofline, e2e=e2e, gpu_launches=int(raw["launches"]), clocks=raw["clocks"])
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w)

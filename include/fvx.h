@@ -43,6 +43,7 @@ extern "C" {
 
 typedef struct fvx_grid_s* fvx_grid;
 typedef struct fvx_kmap_s* fvx_kmap;
+typedef struct fvx_hits_s* fvx_hits; /* voxels along rays (library-owned) */
 typedef void* fvx_stream; /* cudaStream_t */
 
 typedef enum {
@@ -319,6 +320,39 @@ fvx_status fvx_sparse_conv_dgrad(fvx_grid gin, fvx_grid gout, fvx_kmap mt, fvx_d
  * 2^32 tensor-core work units. */
 fvx_status fvx_sparse_conv_wgrad(fvx_grid gin, fvx_grid gout, fvx_kmap m, fvx_dtype dt, const void* feats,
                                  int64_t cin, const void* dout, int64_t cout, float* dW, fvx_stream stream);
+
+/* ---------------------------------------------------------------------------
+ * Voxels along rays ("fVDB" reading notes, HDDA: one DDA per tree level at
+ * 4096^3, 128^3, 8^3 and 1^3 cells; empty nodes are crossed in one step).
+ *
+ * For each ray, the active voxels it passes through, in order, with the
+ * interval of the ray parameter t spent in each.  Definition (exact, fp32):
+ *   - voxel (i,j,k) is the cell [i,i+1) x [j,j+1) x [k,k+1) in index space;
+ *     the ray is o + t d; inv_a = 1/d_a rounded once; the ray crosses the
+ *     plane x_a = n at T_a(n) = ((float)n - o_a) * inv_a (two fp32 roundings);
+ *   - [tmin, tmax] is clipped to the batch element's voxels by those plane
+ *     times; at time t the ray is in cell c_a = max{n : T_a(n) <= t}
+ *     (d_a > 0), min{n : T_a(n) <= t} - 1 (d_a < 0), floor(o_a) (d_a = 0);
+ *   - a hit is an active cell occupied for a time interval of positive
+ *     length: its voxel index and [t_enter, t_exit) (crossing times clipped
+ *     to the segment).  Rays that graze an edge or corner do not hit the
+ *     cells they only touch.  d = 0 gives no hits.
+ * origins, dirs: device float [n_rays, 3] (finite); ray_batch: device int32
+ * [n_rays] batch element of each ray, or NULL (all in element 0).  Voxel
+ * coordinates must lie in [-2^24, 2^24) (cell faces exact in fp32).
+ * Two passes (count, write) and one host synchronisation (the total sizes
+ * the output; nothing is truncated).  The handle owns the result: offsets
+ * device int64 [n_rays + 1] (CSR: ray r's hits are [offsets[r],
+ * offsets[r+1])), voxel device int32 [n_hits], t device float [n_hits, 2].
+ * Errors: FVX_ERR_INVALID_ARG (NULL, negative count, NaN tmin/tmax);
+ * FVX_ERR_RANGE (n_rays or n_hits >= 2^31); FVX_ERR_CHECK (a ray_batch value
+ * outside [0, B), or voxels outside the coordinate range); FVX_ERR_ALLOC. */
+fvx_status fvx_voxels_along_rays(fvx_grid g, const float* origins, const float* dirs, const int32_t* ray_batch,
+                                 int64_t n_rays, float tmin, float tmax, fvx_stream stream, fvx_hits* out);
+/* Device pointers owned by h (NULL arguments are skipped). */
+fvx_status fvx_hits_view(fvx_hits h, const int64_t** offsets, const int32_t** voxel, const float** t,
+                         int64_t* n_hits, int64_t* n_rays);
+fvx_status fvx_hits_destroy(fvx_hits h);
 
 fvx_status fvx_grid_destroy(fvx_grid g);
 fvx_status fvx_kmap_destroy(fvx_kmap m);

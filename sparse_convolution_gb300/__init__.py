@@ -71,6 +71,9 @@ def load():
         "fvx_testing_bounded_wait": ([I32, U64, P], I32),
         "fvx_sparse_conv_dgrad": ([P, P, P, I32, P, I64, P, I64, P, P], I32),
         "fvx_sparse_conv_wgrad": ([P, P, P, I32, P, I64, P, I64, P, P], I32),
+        "fvx_voxels_along_rays": ([P, P, P, P, I64, ctypes.c_float, ctypes.c_float, P, PP], I32),
+        "fvx_hits_view": ([P, PP, PP, PP, P, P], I32),
+        "fvx_hits_destroy": ([P], I32),
         "fvx_grid_destroy": ([P], I32),
         "fvx_kmap_destroy": ([P], I32),
         "fvx_status_string": ([I32], ctypes.c_char_p),
@@ -117,14 +120,15 @@ class _DevArray:
         self._owner = owner
 
 
-_TYPESTR = {"i4": "<i4", "i8": "<i8", "u4": "<u4", "u8": "<u8"}
+_TYPESTR = {"i4": "<i4", "i8": "<i8", "u4": "<u4", "u8": "<u8", "f4": "<f4"}
 
 
 def _view(ptr, shape, code, owner):
     import torch
 
     if any(int(s) == 0 for s in shape) or not ptr:
-        dt = {"i4": torch.int32, "i8": torch.int64, "u4": torch.uint32, "u8": torch.uint64}[code]
+        dt = {"i4": torch.int32, "i8": torch.int64, "u4": torch.uint32, "u8": torch.uint64,
+              "f4": torch.float32}[code]
         return torch.zeros(tuple(int(s) for s in shape), dtype=dt, device="cuda")
     t = torch.as_tensor(_DevArray(ptr, shape, _TYPESTR[code], owner), device="cuda")
     return t.clone()
@@ -270,6 +274,46 @@ class KernelMap:
         ii, oo, mm = self._ptrs
         return (_view(ii, (self.n_pairs,), "i4", self), _view(oo, (self.n_pairs,), "i4", self),
                 _view(mm, (self.n_out,), "u4", self))
+
+
+class Hits:
+    """Active voxels along rays (library-owned CSR result of
+    fvx_voxels_along_rays)."""
+
+    def __init__(self, grid: Grid, origins, dirs, batch=None, tmin=0.0, tmax=float("inf"), stream=None):
+        import torch
+
+        assert origins.dtype == torch.float32 and dirs.dtype == torch.float32 and origins.is_cuda and dirs.is_cuda
+        origins = origins.contiguous()
+        dirs = dirs.contiguous()
+        n = origins.shape[0]
+        assert tuple(origins.shape) == (n, 3) and tuple(dirs.shape) == (n, 3)
+        if batch is not None:
+            batch = batch.to(torch.int32).contiguous()
+        h = ctypes.c_void_p()
+        _check(load().fvx_voxels_along_rays(grid._h, _ptr(origins), _ptr(dirs), _ptr(batch), n,
+                                            ctypes.c_float(tmin), ctypes.c_float(tmax), _stream(stream),
+                                            ctypes.byref(h)))
+        self._h = h
+        off, vox, t = ctypes.c_void_p(), ctypes.c_void_p(), ctypes.c_void_p()
+        nh, nr = ctypes.c_int64(), ctypes.c_int64()
+        _check(_lib.fvx_hits_view(h, ctypes.byref(off), ctypes.byref(vox), ctypes.byref(t), ctypes.byref(nh),
+                                  ctypes.byref(nr)))
+        self.n_hits, self.n_rays = int(nh.value), int(nr.value)
+        self._ptrs = (off.value, vox.value, t.value)
+
+    def arrays(self):
+        """(offsets int64 [n_rays + 1], voxel int32 [n_hits], t float32 [n_hits, 2]), device copies."""
+        off, vox, t = self._ptrs
+        return (_view(off, (self.n_rays + 1,), "i8", self), _view(vox, (self.n_hits,), "i4", self),
+                _view(t, (self.n_hits, 2), "f4", self))
+
+    def destroy(self):
+        if getattr(self, "_h", None) and _lib is not None:
+            _lib.fvx_hits_destroy(self._h)
+            self._h = None
+
+    __del__ = destroy
 
 
 def sparse_conv(gin: Grid, gout: Grid, kmap: KernelMap, feats, W, out=None, out_dtype=None, stream=None):

@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libfvx.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
 
-SOURCES = ["api.cu", "primitives.cu", "build.cu", "kmap.cu", "conv.cu"]
+SOURCES = ["api.cu", "primitives.cu", "build.cu", "kmap.cu", "conv.cu", "rays.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

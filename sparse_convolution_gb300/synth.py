@@ -119,9 +119,11 @@ def _sphere_band(ctr, r, band, box):
     return v[np.abs(d) <= band]
 
 
-def narrow_band_voxels(rng, box=2048, rmin=20.0, rmax=150.0, band=1.5, min_voxels=None, n_spheres=None):
+def narrow_band_voxels(rng, box=2048, rmin=20.0, rmax=150.0, band=1.5, min_voxels=None, n_spheres=None,
+                       centre_lo=0.0, centre_hi=1.0):
     """Band of half-width ``band`` around the zero level set of a union of
-    random spheres (centres uniform in the box, radii uniform in [rmin, rmax]).
+    random spheres (centres uniform in [centre_lo, centre_hi) * box per axis,
+    radii uniform in [rmin, rmax]).
 
     Either a fixed ``n_spheres`` or: add spheres (in seed order) until the band
     holds at least ``min_voxels`` voxels.
@@ -130,7 +132,7 @@ def narrow_band_voxels(rng, box=2048, rmin=20.0, rmax=150.0, band=1.5, min_voxel
     while True:
         if n_spheres is not None and len(spheres) >= n_spheres:
             break
-        ctr = rng.uniform(0, box, size=3)
+        ctr = rng.uniform(centre_lo * box, centre_hi * box, size=3)
         r = float(rng.uniform(rmin, rmax))
         spheres.append((ctr, r))
         v = _sphere_band(ctr, r, band, box)
@@ -319,6 +321,43 @@ def batched_narrow_band(seed=5, B=8, scale=1.0, min_voxels_per_grid=1_250_000, d
     out.update(name=f"batched_narrow_band_{B}x{box}", dtype="bf16", convs=[dict(cin=32, cout=64, stride=1)],
                feat_kind="normal", seed=seed)
     return out
+
+
+def ray_scene(box=1024, seed=7):
+    """Narrow band (3 voxels wide) around a union of 6 spheres with centres in
+    the middle of a ``box``^3 grid and radii 0.15-0.3 * box: a closed surface
+    filling most of a camera's view, as the pages' 3-voxel narrow band of a
+    scanned model (not available here) does."""
+    rng = np.random.default_rng(seed)
+    v = narrow_band_voxels(rng, box=box, rmin=0.15 * box, rmax=0.3 * box, band=1.5, n_spheres=6,
+                           centre_lo=0.3, centre_hi=0.7)
+    out = _finish([v], rng)
+    out.update(name=f"ray_scene_{box}", seed=seed)
+    return out
+
+
+def camera_rays(box, n_side, seed=11, distance=1.5, half_width=0.5):
+    """A pinhole camera outside a ``box``^3 grid looking at its centre:
+    ``n_side``^2 rays (index space, float32) from a random direction at
+    ``distance`` * box from the centre; the view spans +-half_width * box at
+    the centre."""
+    rng = np.random.default_rng(seed)
+    c = np.full(3, box / 2.0)
+    v = rng.normal(size=3)
+    v /= np.linalg.norm(v)
+    eye = c + v * distance * box
+    fwd = -v
+    up = np.array([0.0, 0.0, 1.0]) if abs(fwd[2]) < 0.9 else np.array([1.0, 0.0, 0.0])
+    right = np.cross(fwd, up)
+    right /= np.linalg.norm(right)
+    up = np.cross(right, fwd)
+    half = np.arctan(half_width / distance)  # half field of view
+    u = np.tan(half) * ((np.arange(n_side) + 0.5) / n_side * 2.0 - 1.0)
+    U, V = np.meshgrid(u, u, indexing="ij")
+    d = fwd[None, :] + U.reshape(-1, 1) * right[None, :] + V.reshape(-1, 1) * up[None, :]
+    d /= np.linalg.norm(d, axis=1, keepdims=True)
+    o = np.repeat(eye[None, :], d.shape[0], axis=0)
+    return np.ascontiguousarray(o, np.float32), np.ascontiguousarray(d, np.float32)
 
 
 WORKLOADS = {
