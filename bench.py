@@ -350,7 +350,7 @@ def forward_step(fvx, wl, rec, coords_in, x_in, W_in, ys, stream=None, algos=Non
         with rec(f"conv{i}"):
             fvx.sparse_conv(gin, gout, km, src, W_in[i], out=ys[i], stream=stream)
         if algos is not None and len(algos) < len(wl.convs):
-            algos.append(fvx.last_conv_algo())
+            algos.append(fvx.last_conv_kernel())
         src, gin = ys[i], gout
     return handles
 
@@ -405,7 +405,7 @@ def time_forward(fvx, torch, wl, K, warmup, flush, peaks, peak_kind, sm_count, w
         release(forward_step(fvx, wl, NoRec(), wl.coords, wl.x, wl.Ws, wl.ys, algos=algos, pair_counts=pairs))
     torch.cuda.synchronize()
     fvx.device_status()
-    kernels = [conv_kernel_name(fvx, algos[i], wl.fp32, c["cin"]) for i, c in enumerate(wl.convs)]
+    kernels = list(algos)  # kernel names the library reports for each conv
     flops_i = [2.0 * c["cin"] * c["cout"] * p for c, p in zip(wl.convs, pairs)]
     # the kernel timed in the main loop: the one doing the most arithmetic
     main_k = kernels[max(range(len(wl.convs)), key=lambda i: flops_i[i])]

@@ -228,8 +228,16 @@ fvx_status fvx_sparse_conv(fvx_grid gin, fvx_grid gout, fvx_kmap m, fvx_dtype dt
  *                    are at least 20% occupied on average; pair-list gather
  *                    otherwise.
  *   FVX_CONV_GATHER  always the pair-list kernels (128 consecutive outputs
- *                    per tile; rows fetched by TMA gather4 when cin is a
- *                    multiple of 16, else by cp.async).
+ *                    per tile), direct (below).
+ *   FVX_CONV_DIRECT  the pair-list kernel that fetches every pair's input row
+ *                    from global memory (TMA gather4 when cin is a multiple
+ *                    of 16, else cp.async).
+ *   FVX_CONV_UNION   the pair-list kernel that fetches each distinct input
+ *                    row of a tile once into shared memory and builds the
+ *                    tensor-core operands from there; cin 32 or 64, cout <=
+ *                    128, else FVX_ERR_INVALID_ARG.  Same results as the
+ *                    direct kernel (bit for bit); slower on the workloads
+ *                    measured, so only run when asked for.
  *   FVX_CONV_LEAF    always leaf-densified (each output leaf's 10^3 input
  *                    window staged densely in shared memory; the pair lists
  *                    are not read; the map's per-leaf table of neighbouring
@@ -238,11 +246,22 @@ fvx_status fvx_sparse_conv(fvx_grid gin, fvx_grid gout, fvx_kmap m, fvx_dtype dt
  *                    FVX_ERR_INVALID_ARG.
  * Process-wide; FVX_F32 is unaffected.  Every path meets the same error
  * bound.  Errors: FVX_ERR_INVALID_ARG for an unknown value. */
-typedef enum { FVX_CONV_AUTO = 0, FVX_CONV_GATHER = 1, FVX_CONV_LEAF = 2 } fvx_conv_algo;
+typedef enum {
+  FVX_CONV_AUTO = 0,
+  FVX_CONV_GATHER = 1,
+  FVX_CONV_LEAF = 2,
+  FVX_CONV_DIRECT = 3,
+  FVX_CONV_UNION = 4
+} fvx_conv_algo;
 fvx_status fvx_set_conv_algo(fvx_conv_algo algo);
 /* The kernel family the last successful bf16 convolution on this host thread
- * launched (FVX_CONV_GATHER or FVX_CONV_LEAF; FVX_CONV_AUTO before any). */
+ * launched (FVX_CONV_GATHER for every pair-list kernel, or FVX_CONV_LEAF;
+ * FVX_CONV_AUTO before any). */
 fvx_conv_algo fvx_last_conv_algo(void);
+/* Name of the kernel the last convolution on this host thread launched
+ * ("conv_union", "conv_bf16_tma", "conv_bf16_tc", "conv_leaf", "conv_f32";
+ * "" before any).  Static storage; not freed. */
+const char* fvx_last_conv_kernel(void);
 
 /* Sparse convolution that allocates no device memory.
  *

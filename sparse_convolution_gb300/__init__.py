@@ -24,7 +24,7 @@ LIB_PATH = os.path.join(_HERE, "libfvx.so")
 _lib = None
 
 FVX_F32, FVX_BF16, FVX_BF16_OUT_BF16 = 0, 1, 2
-FVX_CONV_AUTO, FVX_CONV_GATHER, FVX_CONV_LEAF = 0, 1, 2
+FVX_CONV_AUTO, FVX_CONV_GATHER, FVX_CONV_LEAF, FVX_CONV_DIRECT, FVX_CONV_UNION = 0, 1, 2, 3, 4
 
 
 class FvxError(RuntimeError):
@@ -85,6 +85,7 @@ def load():
         "fvx_profile_read_each": ([P, ctypes.c_int64, P], I32),
         "fvx_set_conv_algo": ([I32], I32),
         "fvx_last_conv_algo": ([], I32),
+        "fvx_last_conv_kernel": ([], ctypes.c_char_p),
     }
     for name, (args, res) in sigs.items():
         f = getattr(lib, name)
@@ -409,6 +410,11 @@ def last_conv_algo() -> int:
     """FVX_CONV_GATHER or FVX_CONV_LEAF: what the last bf16 convolution on this
     thread ran (FVX_CONV_AUTO before any)."""
     return int(load().fvx_last_conv_algo())
+
+
+def last_conv_kernel() -> str:
+    """Name of the kernel the last convolution on this thread launched."""
+    return load().fvx_last_conv_kernel().decode()
 
 
 def launch_count() -> int:

@@ -365,7 +365,8 @@ __device__ __forceinline__ void publish_info(ConvSmemHead& h, uint32_t* status, 
 // Epilogue warps: for each tile, wait for its accumulator, read TMEM (row
 // per thread), write fp32 or bf16 rows, release the accumulator and the
 // tile's info slot.
-__device__ __forceinline__ void conv_epilogue(ConvSmemHead& h, const ConvArgs& a, uint32_t tmem, uint32_t acc_cols,
+template <class Head>
+__device__ __forceinline__ void conv_epilogue(Head& h, const ConvArgs& a, uint32_t tmem, uint32_t acc_cols,
                                               int64_t ntiles, int64_t G, int warp, int lane) {
   const int quarter = warp & 3;  // TMEM lane quarter this warp may access
   const int m = quarter * 32 + lane;
@@ -990,6 +991,492 @@ __global__ void __launch_bounds__(kConvThreads, 1) k_conv_bf16_tma(const __grid_
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * acc_cols) : "memory");
+  }
+}
+
+// ============================================================== bf16, pair lists through a tile union
+// The kernel above gathers one input row per (pair, stage) from L2, and the
+// rate at which an SM can have rows brought in (about nine cycles per row,
+// whatever the method) bounds it far below the tensor pipe.  A tile's pairs
+// name few distinct input rows (on narrow bands about 300 for some 2,650
+// pairs), so here each distinct row is fetched once per tile, by TMA gather4,
+// into a "union" buffer in shared memory, and every stage's A tile is built
+// from the union by shared-memory copies (16 bytes per lane, swizzle applied
+// on both sides, no bank conflicts), which cost a fraction of a fetch.
+//
+// Warp roles (544 threads):
+//   warps 0-3   tables: per tile, read the list segments, hash the input rows
+//               of a group of offsets into the union (ids in hash order), write
+//               the group's table (union row of every (offset, tile row) or
+//               -1) and gather the union rows; two union buffers, so the next
+//               group loads while the current one is copied.  A tile whose
+//               union would exceed the buffer is split into groups of
+//               offsets, each a multiple of the offsets one stage holds, so a
+//               tile's stage count is known before it is grouped.
+//   warps 4-11  copies: per stage, the A tile (128 rows x 64 channels, the
+//               layout the TMA kernel's stages have) from the union; zeros
+//               where a row has no pair; one thread loads the stage's weights
+//               by TMA.
+//   warp 12     MMA issue and TMEM owner (as in the TMA kernel).
+//   warps 13-16 epilogue (as in the TMA kernel).
+// The MMA thread, the stage layout and the epilogue are those of
+// k_conv_bf16_tma; only the way A reaches shared memory differs.
+constexpr int kUnTableWarps = 4;
+constexpr int kUnTable = kUnTableWarps * 32;
+constexpr int kUnCopyWarps = 8;
+constexpr int kUnCopy = kUnCopyWarps * 32;
+constexpr int kUnMmaWarp = kUnTableWarps + kUnCopyWarps;  // 12
+constexpr int kUnThreads = (kUnMmaWarp + 1 + 4) * 32;     // 544
+constexpr int kUnHash = 2048;                             // hash slots (> 4x the largest union)
+constexpr int kUnMaxRows = 512;                           // union rows a buffer may hold at most
+constexpr int kUnMaxStages = 8;
+
+// One union buffer's group: offsets (chunks) [lo, hi) of a tile whose present
+// offsets are slot_s[0 .. total).
+struct UnGroup {
+  int16_t rowu[27][kRows];  // union row of (chunk lo + j, tile row m); -1: no pair
+  int32_t slot_s[27];
+  int32_t lo, hi, total;    // lo < 0: no further groups
+  int32_t q0lo, q0hi;       // first output row of the tile (64-bit, split)
+};
+
+struct UnHead {
+  UnGroup grp[2];
+  int32_t hkey[kUnHash];  // input row, -1: empty
+  int16_t hval[kUnHash];  // its union row
+  int32_t uidx[kUnMaxRows];
+  int32_t tp[27][kUnTable];  // input row of table thread tt's pair in present offset j (-1: none)
+  uint8_t tm[27][kUnTable];  // its tile row
+  int16_t tk[27][kUnTable];  // its hash slot
+  uint32_t tstart[27], tend[27];
+  int32_t tslot[27];
+  int32_t tn, ovf, scan[kUnTableWarps];
+  TileInfo info[kInfoRing];
+  unsigned long long full[kUnMaxStages], empty[kUnMaxStages];  // A/B stage ring: copies <-> MMA
+  unsigned long long gfull[2], gempty[2];                      // union buffers: tables <-> copies
+  unsigned long long tinfo_full[kInfoRing], tinfo_empty[kInfoRing];
+  unsigned long long acc_full[2], acc_empty[2];
+  uint32_t tmem_base;
+};
+
+struct alignas(128) UnionArgs {
+  CUtensorMap tmx;  // feats [n_in][cin] bf16: box {cin, 1}, swizzle 2*cin bytes
+  CUtensorMap tmw;  // Wt [27*cout][cin] bf16: box {cin, cout}, same swizzle
+  ConvArgs c;
+  int rowb;         // bytes per feature row: 64 (cin 32) or 128 (cin 64)
+  int layout;       // UMMA layout type of that swizzle: 4 (64 B) or 2 (128 B)
+  int n_in;         // feature rows; row index n_in reads as zeros
+  int cps;          // offsets (chunks) per stage: 64 / cin
+  int umax;         // union rows per buffer
+  int ubytes;       // bytes per union buffer (multiple of 1024)
+};
+
+// Byte offset of 16-byte piece `piece` of row `r` in rows of `rowb` bytes laid
+// out with the matching TMA/UMMA swizzle (128 B: piece ^ (r & 7); 64 B:
+// piece ^ ((r >> 1) & 3)); the buffer is 1024-byte aligned.
+__device__ __forceinline__ uint32_t swz_off(int r, int piece, int rowb) {
+  return rowb == 128 ? (uint32_t)(r * 128 + ((piece ^ (r & 7)) << 4))
+                     : (uint32_t)(r * 64 + ((piece ^ ((r >> 1) & 3)) << 4));
+}
+
+__device__ __forceinline__ int un_hash(int p) { return (int)(((uint32_t)p * 2654435761u) >> 21); }
+__device__ __forceinline__ void table_bar() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+
+// Table warps (tt = thread 0..127 of warps 0-3).
+template <int ROWB>
+__device__ void union_tables(UnHead& h, const UnionArgs& ua, unsigned char* ubase, int64_t ntiles, int64_t G,
+                             int tt) {
+  constexpr int cps = 128 / ROWB;  // offsets per stage
+  const ConvArgs& a = ua.c;
+  const int32_t* const gin = a.in_idx;
+  const int32_t* const gout = a.out_idx;
+  const int umax = ua.umax;
+  const int lane = tt & 31, w = tt >> 5;
+  uint32_t* const status = a.status;
+  int64_t ng = 0;  // groups published so far (buffer ng & 1)
+  int i = 0;
+  for (int64_t t = blockIdx.x; t < ntiles; t += G, ++i) {
+    // the tile's segment in every list; the offsets present, in order
+    uint32_t sa = 0, se = 0;
+    load_segment(a.tile_start, ntiles, t, tt, sa, se);
+    if (tt < 32) {
+      const uint32_t tor = __ballot_sync(0xffffffffu, tt < 27 && se > sa);
+      if (tt < 27 && ((tor >> tt) & 1u)) {
+        const int j = __popc(tor & ((1u << tt) - 1u));
+        h.tslot[j] = tt;
+        h.tstart[j] = sa;  // indexed by present offset from here on
+        h.tend[j] = se;
+      }
+      if (tt == 0) h.tn = __popc(tor);
+    }
+    table_bar();
+    const int tn = h.tn;
+    if (tt == 0) {  // stage count of the tile for the MMA thread and the epilogue
+      const int r = i & (kInfoRing - 1);
+      if (i >= kInfoRing) mbar_wait(smem_u32(&h.tinfo_empty[r]), (uint32_t)(((i / kInfoRing) - 1) & 1), status);
+      h.info[r].nst = (tn + cps - 1) / cps;
+      mbar_arrive(smem_u32(&h.tinfo_full[r]));
+    }
+    const int64_t q0 = t * kRows;
+    // this thread's pair of every present offset (row tt of its segment):
+    // input row in registers, tile row in shared memory; all loads issued
+    // before any is used
+    // input rows straight into shared memory (4-byte cp.async, all in flight
+    // at once), tile rows through registers in two batches
+#pragma unroll
+    for (int j = 0; j < 27; ++j) {
+      const uint32_t e = h.tstart[j] + (uint32_t)tt;
+      if (j < tn && e < h.tend[j])
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(&h.tp[j][tt])), "l"(gin + e) : "memory");
+      else
+        h.tp[j][tt] = -1;
+    }
+    cp_async_commit();
+#pragma unroll
+    for (int b0 = 0; b0 < 27; b0 += 14) {
+      int qv[14];
+#pragma unroll
+      for (int j = 0; j < 14; ++j) {
+        if (b0 + j >= 27) break;
+        const uint32_t e = h.tstart[b0 + j] + (uint32_t)tt;
+        qv[j] = (b0 + j < tn && e < h.tend[b0 + j]) ? __ldg(gout + e) : -1;
+      }
+#pragma unroll
+      for (int j = 0; j < 14; ++j) {
+        if (b0 + j >= 27) break;
+        if (qv[j] >= 0) h.tm[b0 + j][tt] = (uint8_t)(qv[j] - (int)q0);
+      }
+    }
+    cp_async_wait_n(0);  // this thread's own copies; only it reads its column
+    int lo = 0;
+    while (lo < tn) {
+      int hi = tn;
+      for (;;) {  // hash the input rows of chunks [lo, hi); halve on overflow
+        for (int k = tt; k < kUnHash; k += kUnTable) h.hkey[k] = -1;
+        if (tt == 0) h.ovf = 0;
+        table_bar();
+        // first probe of every entry at once (independent atomics), then the
+        // few that met another row probe on
+        uint32_t clash = 0;  // bit j: entry j's home slot holds another row
+#pragma unroll
+        for (int b0 = 0; b0 < 27; b0 += 9) {
+          int old[9];
+#pragma unroll
+          for (int j = 0; j < 9; ++j) {
+            const int jj = b0 + j;
+            old[j] = (jj >= lo && jj < hi && h.tp[jj][tt] >= 0) ? atomicCAS(&h.hkey[un_hash(h.tp[jj][tt])], -1, h.tp[jj][tt]) : -1;
+          }
+#pragma unroll
+          for (int j = 0; j < 9; ++j)
+            if (old[j] >= 0 && old[j] != h.tp[b0 + j][tt]) clash |= 1u << (b0 + j);
+        }
+#pragma unroll
+        for (int j = 0; j < 27; ++j) {
+          if (j < lo || j >= hi || h.tp[j][tt] < 0) continue;
+          const int p = h.tp[j][tt];
+          int k = un_hash(p), it = 0;
+          if ((clash >> j) & 1u) {
+            int o;
+            do {
+              k = (k + 1) & (kUnHash - 1);
+              o = atomicCAS(&h.hkey[k], -1, p);
+              ++it;
+            } while (o >= 0 && o != p && it < 64);
+            if (it == 64) h.ovf = 1 << 20;  // table crowded: an overflow whatever the count
+          }
+          h.tk[j][tt] = (int16_t)k;
+        }
+        // distinct rows = occupied slots
+        int occ = 0;
+#pragma unroll
+        for (int k = 0; k < kUnHash / kUnTable; ++k) occ += h.hkey[tt * (kUnHash / kUnTable) + k] >= 0;
+        occ = __reduce_add_sync(0xffffffffu, occ);
+        table_bar();  // all inserts done, every thread counted its slots
+        if ((tt & 31) == 0) atomicAdd(&h.ovf, occ);  // ovf collects the count (or is already > umax)
+        table_bar();
+        const int ovf = h.ovf > umax;
+        table_bar();  // every thread has read the flag before it is reset
+        if (!ovf) break;
+        const int n = hi - lo;
+        int keep = ((n / 2) / cps) * cps;  // a group of cps chunks (<= 256 rows) always fits
+        if (keep < cps) keep = cps;
+        hi = lo + keep;
+      }
+      // union rows in hash-table order: 16 slots per thread, block-wide scan
+      constexpr int kPer = kUnHash / kUnTable;
+      int key[kPer];
+      int occ = 0;
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        key[k] = h.hkey[tt * kPer + k];
+        occ += key[k] >= 0;
+      }
+      int incl = occ;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += v;
+      }
+      if (lane == 31) h.scan[w] = incl;
+      table_bar();
+      int u = incl - occ;
+      for (int v = 0; v < w; ++v) u += h.scan[v];
+      const int nu = h.scan[0] + h.scan[1] + h.scan[2] + h.scan[3];
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        if (key[k] >= 0) {
+          h.hval[tt * kPer + k] = (int16_t)u;
+          h.uidx[u] = key[k];
+          ++u;
+        }
+      }
+      // the buffer this group goes to was used two groups ago: wait until the
+      // copy warps have released it
+      const int gs = (int)(ng & 1);
+      if (ng >= 2) mbar_wait(smem_u32(&h.gempty[gs]), (uint32_t)(((ng >> 1) - 1) & 1), status);
+      UnGroup& gr = h.grp[gs];
+      {  // -1 everywhere for chunks [lo, hi) (16-byte stores)
+        uint4* z = reinterpret_cast<uint4*>(&gr.rowu[0][0]);
+        const int n16 = (hi - lo) * kRows * 2 / 16;
+        for (int k = tt; k < n16; k += kUnTable) z[k] = make_uint4(~0u, ~0u, ~0u, ~0u);
+      }
+      if (tt < 27) gr.slot_s[tt] = h.tslot[tt];
+      if (tt == 0) {
+        gr.lo = lo;
+        gr.hi = hi;
+        gr.total = tn;
+      }
+      table_bar();
+#pragma unroll
+      for (int j = 0; j < 27; ++j)
+        if (j >= lo && j < hi && h.tp[j][tt] >= 0) gr.rowu[j - lo][h.tm[j][tt]] = h.hval[h.tk[j][tt]];
+      table_bar();  // group table and union list complete
+      // union rows by TMA gather4 (rows past nu: index n_in reads zeros)
+      const int nops = (nu + 3) >> 2;
+      const uint32_t gbar = smem_u32(&h.gfull[gs]);
+      if (tt == 0) mbar_arrive_expect_tx(gbar, (uint32_t)(nops * 4 * ROWB));
+      const uint32_t ub = smem_u32(ubase + (size_t)gs * ua.ubytes);
+      for (int op = tt; op < nops; op += kUnTable) {
+        const int r0 = 4 * op;
+        int4 rows;
+        rows.x = h.uidx[r0];
+        rows.y = r0 + 1 < nu ? h.uidx[r0 + 1] : ua.n_in;
+        rows.z = r0 + 2 < nu ? h.uidx[r0 + 2] : ua.n_in;
+        rows.w = r0 + 3 < nu ? h.uidx[r0 + 3] : ua.n_in;
+        tma_gather4(ub + (uint32_t)(r0 * ROWB), &ua.tmx, 0, rows, gbar);
+      }
+      ++ng;
+      lo = hi;
+      table_bar();  // the hash table and the union list are rebuilt for the next group
+    }
+  }
+  // no further groups
+  const int gs = (int)(ng & 1);
+  if (ng >= 2) mbar_wait(smem_u32(&h.gempty[gs]), (uint32_t)(((ng >> 1) - 1) & 1), status);
+  if (tt == 0) {
+    h.grp[gs].lo = -1;
+    mbar_arrive(smem_u32(&h.gfull[gs]));
+  }
+}
+
+// Copy warps (ct = thread 0..255 of warps 4-11): the stages of every group in
+// order, A from the group's union, B (the offsets' weights) by TMA.  Returns
+// the number of stages produced (for the drain at exit).
+template <int ROWB>
+__device__ int64_t union_copies(UnHead& h, const UnionArgs& ua, unsigned char* sbase, unsigned char* ubase, int ct) {
+  const ConvArgs& a = ua.c;
+  constexpr int cps = 128 / ROWB, rowb = ROWB, ppr = ROWB / 16;
+  const int cout = a.cout, S = a.stages;
+  const int lane = ct & 31;
+  const uint32_t sbytes = (uint32_t)a.stage_bytes;
+  const uint32_t a_bytes = (uint32_t)(cps * kRows * rowb);
+  const uint32_t b_tx = (uint32_t)(cps * cout * rowb);
+  constexpr int per_stage = cps * kRows * ppr;  // 16-byte pieces of A per stage (1024)
+  uint32_t* const status = a.status;
+  int64_t kg = 0;
+  int ring_sb = 0;
+  uint32_t ring_ph = 0;
+  for (int64_t n = 0;; ++n) {
+    const int gs = (int)(n & 1);
+    mbar_wait(smem_u32(&h.gfull[gs]), (uint32_t)((n >> 1) & 1), status);
+    const UnGroup& gr = h.grp[gs];
+    const int lo = *(volatile const int*)&gr.lo;
+    if (lo < 0) break;
+    const int hi = gr.hi, total = gr.total;
+    const unsigned char* ub = ubase + (size_t)gs * ua.ubytes;
+    for (int k = lo / cps; k * cps < hi; ++k, ++kg) {
+      const int sb = ring_sb;
+      if (kg >= S) mbar_wait(smem_u32(&h.empty[sb]), ring_ph ^ 1u, status);
+      if (++ring_sb == S) {
+        ring_sb = 0;
+        ring_ph ^= 1u;
+      }
+      unsigned char* sA = sbase + (size_t)sb * sbytes;
+      const uint32_t bar = smem_u32(&h.full[sb]);
+      if (ct == 0) {
+        mbar_arrive_expect_tx(bar, b_tx);
+        for (int j = 0; j < cps; ++j) {
+          const int c = k * cps + j;
+          const int c1 = c < total ? gr.slot_s[c] * cout : 27 * cout;  // past the last weight row: zeros
+          tma_tile2d(smem_u32(sA) + a_bytes + (uint32_t)(j * cout * rowb), &ua.tmw, 0, c1, bar);
+        }
+      }
+      int uu[per_stage / kUnCopy];
+#pragma unroll
+      for (int r = 0; r < per_stage / kUnCopy; ++r) {  // union rows first (independent loads)
+        const int q = ct + r * kUnCopy;
+        const int j = q / (kRows * ppr), m = (q / ppr) % kRows;
+        const int c = k * cps + j;
+        uu[r] = c < hi ? (int)gr.rowu[c - lo][m] : -1;
+      }
+      uint4 v[per_stage / kUnCopy];
+#pragma unroll
+      for (int r = 0; r < per_stage / kUnCopy; ++r) {
+        const int piece = (ct + r * kUnCopy) % ppr;
+        v[r] = uu[r] >= 0 ? *reinterpret_cast<const uint4*>(ub + swz_off(uu[r], piece, rowb))
+                          : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int r = 0; r < per_stage / kUnCopy; ++r) {
+        const int q = ct + r * kUnCopy;
+        const int j = q / (kRows * ppr), m = (q / ppr) % kRows, piece = q % ppr;
+        *reinterpret_cast<uint4*>(sA + (size_t)j * kRows * rowb + swz_off(m, piece, rowb)) = v[r];
+      }
+      fence_proxy_async();  // generic stores -> the MMA's (async proxy) reads
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&h.gempty[gs]));
+  }
+  return kg;
+}
+
+template <int ROWB>
+__global__ void __launch_bounds__(kUnThreads, 1) k_conv_union(const __grid_constant__ UnionArgs ua) {
+  const ConvArgs& a = ua.c;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // [stage ring][union buffers x 2][head], each 1024-aligned
+  unsigned char* sbase = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  unsigned char* ubase = sbase + (size_t)a.stages * a.stage_bytes;
+  UnHead& h = *reinterpret_cast<UnHead*>(ubase + 2 * (size_t)ua.ubytes);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int S = a.stages;
+  constexpr int rowb = ROWB, cps = 128 / ROWB;
+  const uint32_t acc_cols = (uint32_t)a.tmem_cols;
+  const int64_t G = gridDim.x;
+  const int64_t ntiles = a.ntiles;
+
+  if (tid == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(smem_u32(&h.full[i]), kUnCopyWarps + 1);  // one arrival per copy warp + the weights' expect_tx
+      mbar_init(smem_u32(&h.empty[i]), 1);
+    }
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(smem_u32(&h.gfull[g]), 1);
+      mbar_init(smem_u32(&h.gempty[g]), kUnCopyWarps);
+    }
+    for (int r = 0; r < kInfoRing; ++r) {
+      mbar_init(smem_u32(&h.tinfo_full[r]), 1);
+      mbar_init(smem_u32(&h.tinfo_empty[r]), 4);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&h.acc_full[b]), 1);
+      mbar_init(smem_u32(&h.acc_empty[b]), 128);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == kUnMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&h.tmem_base)),
+                 "r"(2 * acc_cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = h.tmem_base;
+
+  if (warp < kUnTableWarps) {
+    union_tables<ROWB>(h, ua, ubase, ntiles, G, tid);
+  } else if (warp < kUnMmaWarp) {
+    const int ct = tid - kUnTable;
+    const int64_t kg = union_copies<ROWB>(h, ua, sbase, ubase, ct);
+    if (ct == 0) {
+      // Normally the MMA thread has seen every stage's weights land.  After a
+      // give-up, wait (bounded) for those copies before the block exits.
+      int sb = (int)(kg % S);
+      uint32_t ph = (uint32_t)((kg / S) & 1);
+      for (int64_t u = 0; u < kg && u < S; ++u) {
+        if (sb == 0) {
+          sb = S - 1;
+          ph ^= 1u;
+        } else {
+          --sb;
+        }
+        mbar_drain(smem_u32(&h.full[sb]), ph);
+      }
+    }
+  } else if (warp == kUnMmaWarp) {
+    // ---------------- MMA issue (one thread), as in k_conv_bf16_tma
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(kRows, a.cout);
+      const uint32_t layout = (uint32_t)ua.layout, sbo = 8u * (uint32_t)rowb;
+      const int cout = a.cout;
+      uint32_t* const status = a.status;
+      const uint32_t a_bytes = (uint32_t)(cps * kRows * rowb);
+      const uint64_t adesc0 = sdesc_swz(smem_u32(sbase), layout, sbo);
+      const uint64_t bdesc0 = sdesc_swz(smem_u32(sbase) + a_bytes, layout, sbo);
+      uint32_t aoff[4], boff[4];
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {  // 16 channels per MMA, 64 per stage
+        const int e = 16 * kk, j = e / (rowb / 2);
+        const uint32_t off = (uint32_t)((e - j * (rowb / 2)) * 2);
+        aoff[kk] = ((uint32_t)(j * kRows * rowb) + off) >> 4;
+        boff[kk] = ((uint32_t)(j * cout * rowb) + off) >> 4;
+      }
+      const uint32_t sunits = (uint32_t)a.stage_bytes >> 4;
+      int m_sb = 0;
+      uint32_t m_ph = 0, m_off = 0;
+      int i = 0;
+      for (int64_t t = blockIdx.x; t < ntiles; t += G, ++i) {
+        const int r = i & (kInfoRing - 1), b = i & 1;
+        mbar_wait(smem_u32(&h.tinfo_full[r]), (uint32_t)((i / kInfoRing) & 1), status);
+        const int nst = *(volatile const int*)&h.info[r].nst;
+        if (i >= 2) mbar_wait(smem_u32(&h.acc_empty[b]), (uint32_t)(((i >> 1) - 1) & 1), status);
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)b * acc_cols;
+        for (int k = 0; k < nst; ++k) {
+          mbar_wait(smem_u32(&h.full[m_sb]), m_ph, status);
+          tc_fence_after();
+          const uint64_t ad = adesc0 + m_off, bd = bdesc0 + m_off;
+          umma_bf16(d, ad + aoff[0], bd + boff[0], idesc, k > 0 ? 1u : 0u);
+          umma_bf16(d, ad + aoff[1], bd + boff[1], idesc, 1u);
+          umma_bf16(d, ad + aoff[2], bd + boff[2], idesc, 1u);
+          umma_bf16(d, ad + aoff[3], bd + boff[3], idesc, 1u);
+          umma_commit(smem_u32(&h.empty[m_sb]));
+          m_off += sunits;
+          if (++m_sb == S) {
+            m_sb = 0;
+            m_ph ^= 1u;
+            m_off = 0;
+          }
+        }
+        if (nst > 0) umma_commit(smem_u32(&h.acc_full[b]));
+        else mbar_arrive(smem_u32(&h.acc_full[b]));
+      }
+      // every MMA has completed before tensor memory is freed
+      if (i > 0) mbar_drain(smem_u32(&h.acc_full[(i - 1) & 1]), (uint32_t)(((i - 1) >> 1) & 1));
+    }
+    __syncwarp();
+  } else {
+    conv_epilogue(h, a, tmem, acc_cols, ntiles, G, warp, lane);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kUnMmaWarp) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * acc_cols) : "memory");
   }
@@ -1925,6 +2412,7 @@ fvx_status encode_2d(EncodeTiledFn fn, CUtensorMap* tm, const void* base, int64_
 // status: a zeroed device word.
 std::atomic<int> g_conv_algo{FVX_CONV_AUTO};
 thread_local int t_last_algo = FVX_CONV_AUTO;
+thread_local const char* t_last_kernel = "";
 
 // Leaf-densified launch: one block per output leaf, as many blocks per SM as
 // shared memory allows but no more than the tensor memory holds at once.
@@ -1976,6 +2464,61 @@ fvx_status launch_conv_leaf(const char* who, fvx_grid gin, fvx_kmap m, const int
   FVX_TRY(check_launch("conv_leaf"));
   (void)who;
   t_last_algo = FVX_CONV_LEAF;
+  t_last_kernel = "conv_leaf";
+  return FVX_OK;
+}
+
+// Union-staged pair-list launch (cin 32 or 64, cout <= 128): stage ring and
+// two union buffers sized to shared memory; FVX_ERR_CAPACITY when they cannot
+// hold at least one stage's worth of rows (the caller falls back).
+fvx_status launch_conv_union(const char* who, EncodeTiledFn enc, fvx_grid gin, ConvArgs a, const void* feats,
+                             const __nv_bfloat16* wt, int sms, cudaStream_t s) {
+  UnionArgs ua;
+  const int cin = a.cin, cout = a.cout;
+  ua.rowb = 2 * cin;
+  ua.layout = cin == 64 ? 2 : 4;
+  ua.n_in = (int)gin->n_active;
+  ua.cps = 64 / cin;
+  const CUtensorMapSwizzle swz = cin == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  FVX_TRY(encode_2d(enc, &ua.tmx, feats, cin, gin->n_active, cin, 1, swz, CU_TENSOR_MAP_L2_PROMOTION_NONE, who));
+  FVX_TRY(encode_2d(enc, &ua.tmw, wt, cin, 27 * (int64_t)cout, cin, cout, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    who));
+  a.stage_bytes = kRows * 128 + ua.cps * cout * ua.rowb;  // A: 128 rows x 64 channels; B: the offsets' weights
+  a.w_resident = 0;
+  a.w_bytes = 0;
+  a.lag = 0;
+  int optin = 0, dev = 0;
+  FVX_CUDA(cudaGetDevice(&dev));
+  FVX_CUDA(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
+  const int budget = optin - 1024 - (int)sizeof(UnHead);
+  // unions of up to kUnMaxRows rows; as many stages as then fit (at most
+  // kUnMaxStages), else three stages and whatever union that leaves
+  int ubytes = kUnMaxRows * ua.rowb;
+  int S = (budget - 2 * ubytes) / a.stage_bytes;
+  if (S < 3) {
+    S = 3;
+    ubytes = ((budget - 3 * a.stage_bytes) / 2) & ~1023;
+  }
+  S = std::min(S, kUnMaxStages);
+  ua.ubytes = ubytes;
+  ua.umax = std::min(kUnMaxRows, ubytes / ua.rowb);
+  if (ua.umax < ua.cps * kRows) {
+    set_error("%s: cout %d leaves no room for a union of %d rows", who, cout, ua.cps * kRows);
+    return FVX_ERR_CAPACITY;
+  }
+  a.stages = S;
+  ua.c = a;
+  const size_t smem = 1024 + (size_t)S * a.stage_bytes + 2 * (size_t)ubytes + sizeof(UnHead);
+  auto kern = cin == 64 ? k_conv_union<128> : k_conv_union<64>;
+  FVX_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  const int64_t grid = std::min<int64_t>(a.ntiles, (int64_t)sms);
+  {
+    LaunchScope ls("conv_union", s);
+    kern<<<(unsigned)grid, kUnThreads, smem, s>>>(ua);
+  }
+  FVX_TRY(check_launch("conv_union"));
+  t_last_algo = FVX_CONV_GATHER;
+  t_last_kernel = "conv_union";
   return FVX_OK;
 }
 
@@ -2022,6 +2565,22 @@ fvx_status launch_conv_bf16(const char* who, fvx_grid gin, fvx_kmap m, fvx_dtype
   const int64_t grid = std::min<int64_t>(nt, (int64_t)sms);
   const int head = (int)sizeof(ConvSmemHead) + 1024;
 
+  const bool union_ok = (cin == 32 || cin == 64) && cout <= 128 && gin->n_active > 0;
+  if (algo == FVX_CONV_UNION && !union_ok) {
+    set_error("%s: the union-staged convolution needs cin 32 or 64 and cout <= 128 (got %lld, %lld)", who,
+              (long long)cin, (long long)cout_real);
+    return FVX_ERR_INVALID_ARG;
+  }
+  // the union-staged kernel runs when asked for: measured slower than the
+  // direct one on every workload here (its per-tile tables cost more than the
+  // gathers they save), so the automatic choice stays direct
+  if (union_ok && algo == FVX_CONV_UNION) {
+    EncodeTiledFn uenc = encode_tiled();
+    if (uenc) {
+      const fvx_status st = launch_conv_union(who, uenc, gin, a, feats, wt, sms, s);
+      if (st != FVX_ERR_CAPACITY || algo == FVX_CONV_UNION) return st;
+    }
+  }
   EncodeTiledFn enc = (cin % 16 == 0 && gin->n_active > 0) ? encode_tiled() : nullptr;
   if (enc) {
     ConvTmaArgs ta;
@@ -2060,6 +2619,7 @@ fvx_status launch_conv_bf16(const char* who, fvx_grid gin, fvx_kmap m, fvx_dtype
     }
     FVX_TRY(check_launch("conv_bf16_tma"));
     t_last_algo = FVX_CONV_GATHER;
+    t_last_kernel = "conv_bf16_tma";
     return FVX_OK;
   }
 
@@ -2086,6 +2646,7 @@ fvx_status launch_conv_bf16(const char* who, fvx_grid gin, fvx_kmap m, fvx_dtype
   }
   FVX_TRY(check_launch("conv_bf16_tc"));
   t_last_algo = FVX_CONV_GATHER;
+  t_last_kernel = "conv_bf16_tc";
   return FVX_OK;
 }
 
@@ -2137,6 +2698,7 @@ extern "C" fvx_status fvx_sparse_conv(fvx_grid gin, fvx_grid gout, fvx_kmap m, f
   if (gout->n_active == 0) return FVX_OK;
   if (dt == FVX_F32) {
     {
+      t_last_kernel = "conv_f32";
       LaunchScope ls("conv_f32", s);
       k_conv_f32<<<(unsigned)nt, kRows, 0, s>>>((const float*)feats, (const float*)W, m->out_mask, m->in_idx,
                                                 m->tile_start, nt, m->n_out, (int)cin, (int)cout, (float*)out);
@@ -2230,6 +2792,7 @@ extern "C" fvx_status fvx_sparse_conv_noalloc(fvx_grid gin, fvx_grid gout, fvx_k
   if (gout->n_active == 0) return FVX_OK;
   if (dt == FVX_F32) {  // the fp32 kernel needs no scratch at all
     {
+      t_last_kernel = "conv_f32";
       LaunchScope ls("conv_f32", s);
       k_conv_f32<<<(unsigned)nt, kRows, 0, s>>>((const float*)feats, (const float*)W, m->out_mask, m->in_idx,
                                                 m->tile_start, nt, m->n_out, (int)cin, (int)cout, (float*)out);
@@ -2436,6 +2999,7 @@ extern "C" fvx_status fvx_sparse_conv_dgrad(fvx_grid gin, fvx_grid gout, fvx_kma
     }
     FVX_TRY(check_launch("conv_transpose_w"));
     {
+      t_last_kernel = "conv_f32";
       LaunchScope ls("conv_f32", s);
       k_conv_f32<<<(unsigned)mt->n_tiles, kRows, 0, s>>>((const float*)dout, wt, mt->out_mask, mt->in_idx,
                                                           mt->tile_start, mt->n_tiles, mt->n_out, (int)cout,
@@ -2511,7 +3075,8 @@ extern "C" fvx_status fvx_sparse_conv_dgrad(fvx_grid gin, fvx_grid gout, fvx_kma
 }
 
 extern "C" fvx_status fvx_set_conv_algo(fvx_conv_algo algo) {
-  if (algo != FVX_CONV_AUTO && algo != FVX_CONV_GATHER && algo != FVX_CONV_LEAF) {
+  if (algo != FVX_CONV_AUTO && algo != FVX_CONV_GATHER && algo != FVX_CONV_LEAF && algo != FVX_CONV_DIRECT &&
+      algo != FVX_CONV_UNION) {
     set_error("fvx_set_conv_algo: unknown value %d", (int)algo);
     return FVX_ERR_INVALID_ARG;
   }
@@ -2520,3 +3085,5 @@ extern "C" fvx_status fvx_set_conv_algo(fvx_conv_algo algo) {
 }
 
 extern "C" fvx_conv_algo fvx_last_conv_algo(void) { return (fvx_conv_algo)t_last_algo; }
+
+extern "C" const char* fvx_last_conv_kernel(void) { return t_last_kernel; }
