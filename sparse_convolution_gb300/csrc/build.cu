@@ -192,6 +192,23 @@ __global__ void __launch_bounds__(kThreads) k_key2_direct(const int32_t* __restr
   val[r] = (uint32_t)r;
 }
 
+// step 5 key when every batch element lies in one root tile (the same one):
+// the run of a row is its batch element, so key2 = batch above the compacted
+// offsets, without the stage-1 sort and run numbering (run ids may skip
+// empty batch elements; they only order keys and index run_tile)
+__global__ void __launch_bounds__(kThreads) k_key2_batch(const int32_t* __restrict__ coords, int64_t n,
+                                                         const int64_t* __restrict__ offs, int B,
+                                                         const __grid_constant__ BitRuns runs, int vbits, int4 tile0,
+                                                         uint64_t* __restrict__ key, uint32_t* __restrict__ val,
+                                                         int4* __restrict__ run_tile) {
+  const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (r < B) run_tile[r] = make_int4((int)r, tile0.y, tile0.z, tile0.w);
+  if (r >= n) return;
+  const int b = batch_of_row(offs, B, r);
+  key[r] = ((uint64_t)b << vbits) | compact_bits(offset_key(coords[3 * r], coords[3 * r + 1], coords[3 * r + 2]), runs);
+  val[r] = (uint32_t)r;
+}
+
 // ---------------------------------------------------------------- steps 3-6 by bitmap
 // One batch in one root tile whose compacted offset key has at most
 // kBitmapMaxBits varying bits: a presence bitmap over the whole key space
@@ -760,7 +777,11 @@ fvx_status build_grid_device(const int32_t* coords, int64_t n, const int64_t* of
     sh.leaf = __builtin_popcountll(vm & 0x1FFull);
     sh.lower = __builtin_popcountll(vm & 0x1FFFFFull);
     sh.upper = vbits;
-    const uint64_t max_runs = (width1 >= 63) ? (uint64_t)n : std::min<uint64_t>((uint64_t)n, 1ull << width1);
+    // runs: (batch, tile) pairs present, or with a single tile the batch
+    // elements themselves (run id = batch index)
+    const uint64_t max_runs = (width1 > 0 && L.tile_bits == 0) ? (uint64_t)B
+                              : (width1 >= 63)                 ? (uint64_t)n
+                                                               : std::min<uint64_t>((uint64_t)n, 1ull << width1);
     const int runbits = bits_for(max_runs - 1);
     if (runbits + vbits > 64) {
       set_error("fvx_build_grid: %d rows spread over too many root tiles for a 64-bit key", (int)n);
@@ -806,6 +827,15 @@ fvx_status build_grid_device(const int32_t* coords, int64_t n, const int64_t* of
         k_key2_direct<<<grid_for(n, kThreads), kThreads, 0, s>>>(coords, n, runs, tile0, ka, va, run_tile);
       }
       FVX_TRY(check_launch("build_key2_direct"));
+    } else if (L.tile_bits == 0) {
+      // several batch elements, all in the one root tile: run = batch
+      const int4 tile0 = make_int4(0, P.tmin[0], P.tmin[1], P.tmin[2]);
+      {
+        LaunchScope ls("build_key2_batch", s);
+        k_key2_batch<<<grid_for(std::max<int64_t>(n, B), kThreads), kThreads, 0, s>>>(coords, n, offs_dev, B, runs,
+                                                                                        vbits, tile0, ka, va, run_tile);
+      }
+      FVX_TRY(check_launch("build_key2_batch"));
     } else {
       {
         LaunchScope ls("build_key1", s);
