@@ -28,7 +28,7 @@ namespace fvx {
 constexpr uint64_t kLbAgg = 1ull << 32;
 constexpr uint64_t kLbInc = 2ull << 32;
 constexpr unsigned long long kLbWaitNs = 2000000000ull;
-constexpr int kLbWindow = 16;  // radix sort: predecessors read per round trip
+constexpr int kLbWindow = 8;   // radix sort: predecessors read per round trip
 
 // A published word carries its own value and nothing else is read on the
 // strength of it, so relaxed device-scope accesses suffice (and several loads
@@ -209,7 +209,7 @@ struct RsSmem {
 // memory, publishes its count of each digit, adds up the counts its
 // predecessors published (thread d follows digit d), publishes the inclusive
 // count and writes each key to digit_start[d] + predecessors' count + rank.
-__global__ void __launch_bounds__(kRsThreads) k_radix_onesweep(const uint64_t* __restrict__ kin,
+__global__ void __launch_bounds__(kRsThreads, 3) k_radix_onesweep(const uint64_t* __restrict__ kin,
                                                                const uint32_t* __restrict__ vin,
                                                                uint64_t* __restrict__ kout,
                                                                uint32_t* __restrict__ vout, int64_t n, int shift,
@@ -228,15 +228,13 @@ __global__ void __launch_bounds__(kRsThreads) k_radix_onesweep(const uint64_t* _
 
   const int64_t base = t * kRsTile + (int64_t)warp * kRsWarpItems;
   uint64_t key[kRsRounds];
-  uint32_t val[kRsRounds];
-  uint32_t rank[kRsRounds];
+  uint32_t rank[kRsRounds];  // values are read again when scattered (registers for a third block per SM)
   const uint32_t lt = lanemask_lt();
 #pragma unroll
   for (int r = 0; r < kRsRounds; ++r) {
     const int64_t i = base + r * 32 + lane;
     const bool valid = i < n;
     key[r] = valid ? kin[i] : 0ull;
-    val[r] = valid ? vin[i] : 0u;
     const uint32_t d = valid ? ((uint32_t)(key[r] >> shift) & dmask) : (256u + lane);
     const uint32_t peers = __match_any_sync(0xffffffffu, d);
     const uint32_t old = valid ? sm.whist[warp][d] : 0u;
@@ -299,7 +297,7 @@ __global__ void __launch_bounds__(kRsThreads) k_radix_onesweep(const uint64_t* _
       const uint32_t d = (uint32_t)(key[r] >> shift) & dmask;
       const uint32_t lpos = sm.dexcl[d] + sm.whist[warp][d] + rank[r];
       sm.keys[lpos] = key[r];
-      sm.vals[lpos] = val[r];
+      sm.vals[lpos] = vin[i];
     }
   }
   __syncthreads();
@@ -324,6 +322,9 @@ fvx_status radix_sort_pairs(uint64_t* k0, uint32_t* v0, uint64_t* k1, uint32_t* 
     return FVX_ERR_CUDA;
   }
   FVX_CUDA(cudaFuncSetAttribute(k_radix_onesweep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(RsSmem)));
+  // three blocks per SM: shared memory for three tiles, registers for three (launch bounds)
+  FVX_CUDA(cudaFuncSetAttribute(k_radix_onesweep, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                (int)cudaSharedmemCarveoutMaxShared));
   const int passes = (bit_hi - bit_lo + 7) / 8;
   const int64_t ntiles = (n + kRsTile - 1) / kRsTile;
   // one zeroed region: digit counts [passes][256], tickets [8], then the
