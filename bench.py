@@ -149,7 +149,7 @@ def profiled_traffic(kernel, workload):
     import hashlib
     import re
 
-    src = {"conv_bf16_tc": "conv.cu", "conv_bf16_tma": "conv.cu", "conv_leaf": "conv.cu",
+    src = {"conv_bf16_tc": "conv.cu", "conv_bf16_tma": "conv.cu", "conv_leaf": "conv.cu", "conv_halo": "conv.cu",
            "conv_wgrad_tc": "conv.cu", "kmap1_write": "kmap.cu"}.get(kernel)
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     if src is None or not os.path.exists(path):
@@ -459,8 +459,10 @@ def time_forward(fvx, torch, wl, K, warmup, flush, peaks, peak_kind, sm_count, w
         # algorithmic bytes: feats read once, output written once (4 B fp32 /
         # 2 B bf16), weights once, plus what locates the inputs: the kernel
         # map's (in, out) int32 pair for the pair-list kernels, the output
-        # leaf's 80-byte record for the leaf-densified kernel
-        where = 80 * wl.leaves_out[i] if kn == "conv_leaf" else 8 * p
+        # leaf's 80-byte record for the leaf-densified kernel, that record and
+        # the leaf's 27 int32 neighbour-leaf ids for the halo-staged kernel
+        where = (80 * wl.leaves_out[i] if kn == "conv_leaf" else 188 * wl.leaves_out[i] if kn == "conv_halo"
+                 else 8 * p)
         alg = (n_in * c["cin"] * esz + wl.n_out[i] * c["cout"] * wl.ys[i].element_size()
                + 27 * c["cin"] * c["cout"] * esz + where)
         rl = conv_roofline(flops_i[i] * nk, alg * nk, sec, wl.fp32, peaks, peak_kind, sm_count)

@@ -225,8 +225,10 @@ fvx_status fvx_sparse_conv(fvx_grid gin, fvx_grid gout, fvx_kmap m, fvx_dtype dt
  * occupied, picked per case].
  *   FVX_CONV_AUTO    (default) leaf-densified when the map has stride 1,
  *                    cin is 8 or 16, cout <= 64 and the output grid's leaves
- *                    are at least 20% occupied on average; pair-list gather
- *                    otherwise.
+ *                    are at least 20% occupied on average; halo-staged when
+ *                    the map has stride 1, cin is 32, cout <= 64 and the
+ *                    output leaves hold at least 48 active voxels on
+ *                    average; pair-list gather otherwise.
  *   FVX_CONV_GATHER  always the pair-list kernels (128 consecutive outputs
  *                    per tile), direct (below).
  *   FVX_CONV_DIRECT  the pair-list kernel that fetches every pair's input row
@@ -238,6 +240,14 @@ fvx_status fvx_sparse_conv(fvx_grid gin, fvx_grid gout, fvx_kmap m, fvx_dtype dt
  *                    128, else FVX_ERR_INVALID_ARG.  Same results as the
  *                    direct kernel (bit for bit); slower on the workloads
  *                    measured, so only run when asked for.
+ *   FVX_CONV_HALO    always halo-staged (each output leaf's 10^3 input
+ *                    window fetched once into shared memory, at the positions
+ *                    that hold an input voxel; the operands of the leaf's
+ *                    active outputs, 128 per tile, built from there in tensor
+ *                    memory; the pair lists are not read, the map's leaf table
+ *                    is); a call it cannot serve (stride 2, a transposed map,
+ *                    cin other than 32, cout > 64) fails with
+ *                    FVX_ERR_INVALID_ARG.
  *   FVX_CONV_LEAF    always leaf-densified (each output leaf's 10^3 input
  *                    window staged densely in shared memory; the pair lists
  *                    are not read; the map's per-leaf table of neighbouring
@@ -251,15 +261,17 @@ typedef enum {
   FVX_CONV_GATHER = 1,
   FVX_CONV_LEAF = 2,
   FVX_CONV_DIRECT = 3,
-  FVX_CONV_UNION = 4
+  FVX_CONV_UNION = 4,
+  FVX_CONV_HALO = 5
 } fvx_conv_algo;
 fvx_status fvx_set_conv_algo(fvx_conv_algo algo);
 /* The kernel family the last successful bf16 convolution on this host thread
- * launched (FVX_CONV_GATHER for every pair-list kernel, or FVX_CONV_LEAF;
- * FVX_CONV_AUTO before any). */
+ * launched (FVX_CONV_GATHER for every pair-list kernel, FVX_CONV_LEAF or
+ * FVX_CONV_HALO; FVX_CONV_AUTO before any). */
 fvx_conv_algo fvx_last_conv_algo(void);
 /* Name of the kernel the last convolution on this host thread launched
- * ("conv_union", "conv_bf16_tma", "conv_bf16_tc", "conv_leaf", "conv_f32";
+ * ("conv_halo", "conv_union", "conv_bf16_tma", "conv_bf16_tc", "conv_leaf",
+ * "conv_f32";
  * "" before any).  Static storage; not freed. */
 const char* fvx_last_conv_kernel(void);
 

@@ -24,7 +24,7 @@ LIB_PATH = os.path.join(_HERE, "libfvx.so")
 _lib = None
 
 FVX_F32, FVX_BF16, FVX_BF16_OUT_BF16 = 0, 1, 2
-FVX_CONV_AUTO, FVX_CONV_GATHER, FVX_CONV_LEAF, FVX_CONV_DIRECT, FVX_CONV_UNION = 0, 1, 2, 3, 4
+FVX_CONV_AUTO, FVX_CONV_GATHER, FVX_CONV_LEAF, FVX_CONV_DIRECT, FVX_CONV_UNION, FVX_CONV_HALO = 0, 1, 2, 3, 4, 5
 
 
 class FvxError(RuntimeError):
@@ -401,14 +401,15 @@ def noalloc_status(stream=None):
 
 
 def set_conv_algo(algo: int) -> None:
-    """FVX_CONV_AUTO (default), FVX_CONV_GATHER or FVX_CONV_LEAF: which bf16
-    convolution kernel family sparse_conv runs (process-wide)."""
+    """FVX_CONV_AUTO (default), FVX_CONV_GATHER, FVX_CONV_DIRECT,
+    FVX_CONV_UNION, FVX_CONV_HALO or FVX_CONV_LEAF: which bf16 convolution
+    kernel sparse_conv runs (process-wide)."""
     _check(load().fvx_set_conv_algo(int(algo)))
 
 
 def last_conv_algo() -> int:
-    """FVX_CONV_GATHER or FVX_CONV_LEAF: what the last bf16 convolution on this
-    thread ran (FVX_CONV_AUTO before any)."""
+    """FVX_CONV_GATHER, FVX_CONV_LEAF or FVX_CONV_HALO: what the last bf16
+    convolution on this thread ran (FVX_CONV_AUTO before any)."""
     return int(load().fvx_last_conv_algo())
 
 

@@ -1816,6 +1816,507 @@ __global__ void __launch_bounds__(kLeafThreads, G8 == 1 ? 2 : 1) k_conv_leaf(con
   }
 }
 
+// ============================================================== bf16, halo-staged
+// Submanifold (stride 1) convolution of 32-channel inputs over the ACTIVE
+// outputs of each output leaf.  The input window of a leaf (its 8^3 voxels and
+// a one-voxel shell: 10^3 positions) is fetched once into a shared-memory pool,
+// only at the positions that hold an input voxel (TMA gather4, four pool rows
+// per operation); the weights stay resident in shared memory.  An M tile is
+// 128 active outputs of one leaf, or the tail of one leaf and the head of the
+// block's next leaf; K runs over the 27 offsets, two per stage: offset s =
+// (dx+1)*9 + (dy+1)*3 + dz+1 takes, for the output at window position w, the
+// pool row of window position w + 100 dx + 10 dy + dz (zeros where no input
+// voxel is there).  The A operand of each stage is written row by row into
+// tensor memory (tcgen05.st, one row per thread) and the MMA reads it from
+// there (A in TMEM, B in shared memory), so the stage costs shared memory only
+// the pool reads.  Every input row is fetched once per output leaf whose
+// window holds it instead of once per pair, and no MMA row is spent on an
+// inactive position.
+//   warps 0-3   window loader: the 27 neighbour leaves' records (prefetched a
+//               leaf ahead), the window map (position -> pool row), the
+//               window positions of the leaf's outputs, the gathers; up to
+//               kHaloWins windows resident, pool rows allocated in order.
+//   warps 4-11  operand rows: warps 4-7 the first offset of each stage, warps
+//               8-11 the second, thread = tile row (its warp's TMEM lane
+//               quarter); they also pack the tiles and publish them.
+//   warp 12     MMA issue and TMEM owner (two accumulators, the A ring).
+//   warps 13-16 epilogue: row m of a tile to its output row.
+constexpr int kHaloPos = 1000;                       // window positions
+constexpr int kHaloRowB = 64;                        // pool row: 32 bf16 channels
+constexpr int kHaloPoolUnits = 384;                  // pool of 384 x 4 rows (96 KB)
+constexpr int kHaloWins = 4;                         // window descriptors
+constexpr int kHaloJoinMax = kHaloPoolUnits * 4 - kHaloPos;  // a window this small leaves room for any next one
+constexpr int kHaloTileStages = 14;                  // 27 offsets, two per stage
+constexpr int kHaloMaxRing = 16;                     // A stages in tensor memory at most
+constexpr int kHaloMaxCout = 64;
+constexpr int kHaloRowWarp0 = 4;                    // first operand-row warp                     // resident weights: 27 x 64 x 64 B
+constexpr double kHaloAutoPerLeaf = 48.0;            // mean active outputs per leaf for the automatic choice
+
+struct HaloWin {
+  int16_t slot[kHaloPos];  // pool row of each window position; -1: no input voxel there
+  int16_t opos[512];       // window position of the leaf's k-th active output
+  int64_t first;           // output row of the leaf's first active voxel
+  int32_t n;               // active outputs of the leaf
+  int32_t nact;            // window positions holding an input voxel
+  int32_t ustart;          // first pool unit (allocation counter, not reduced)
+  int32_t pad;
+};
+
+struct HaloTile {
+  int64_t q0a, q0b;  // output rows of tile rows 0 and ca
+  int32_t ca;        // rows taken from the first leaf
+  int32_t nrows;     // rows of the tile; -1: no further tiles
+};
+
+struct HaloHead {
+  HaloWin win[kHaloWins];
+  LeafNbr nb[2][27];       // neighbour records of the loader's current and next leaf
+  int32_t rows[kHaloPos];  // input row of each new pool row (loader only)
+  int32_t scan[4];
+  HaloTile tile[kInfoRing];
+  unsigned long long afull[kHaloMaxRing], aempty[kHaloMaxRing];  // A stages: rows <-> MMA
+  unsigned long long wfull[kHaloWins], wempty[kHaloWins];        // windows: loader <-> rows
+  unsigned long long tinfo_full[kInfoRing], tinfo_empty[kInfoRing];
+  unsigned long long acc_full[2], acc_empty[2];
+  uint32_t tmem_base;
+};
+
+struct alignas(128) HaloArgs {
+  CUtensorMap tmx;          // feats [n_in][32] bf16: box {32, 1}, 64-byte swizzle
+  const __nv_bfloat16* wt;  // [27][cout][32] bf16
+  const uint64_t* in_rec;   // input grid leaf records [L][10]
+  const int32_t* nbr;       // [L_out][27] input leaf per leaf offset, -1 absent
+  const uint64_t* out_rec;  // output grid leaf records [L_out][10]
+  void* y;                  // [n_out][cout_store], fp32 or bf16
+  uint32_t* status;
+  int64_t n_leaf_out;
+  int n_in;                 // feature rows; row index n_in reads as zeros
+  int cout, cout_store, out_bf16, stages, acc_cols, w_bytes;
+};
+
+// A operand from tensor memory (row m in lane m, bf16 pairs along the columns).
+__device__ __forceinline__ void umma_bf16_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Window loader (warps 0-3, thread lt = 0..127).
+__device__ void halo_loader(HaloHead& h, const HaloArgs& a, unsigned char* pool, int lt) {
+  const int64_t G = gridDim.x, nL = a.n_leaf_out;
+  uint32_t* const status = a.status;
+  const int lane = lt & 31, w = lt >> 5;
+  int32_t id_next = -1;
+  if (lt < 27 && (int64_t)blockIdx.x + G < nL) id_next = __ldg(a.nbr + ((int64_t)blockIdx.x + G) * 27 + lt);
+  int i = 0;
+  int ucur = 0;  // pool units allocated so far
+  int rel = 0;   // windows known to be released
+  for (int64_t L = blockIdx.x; L < nL; L += G, ++i) {
+    const int b = i & 1, d = i % kHaloWins;
+    const bool have_next = L + G < nL;
+    // records of the next leaf (its ids came one iteration earlier), ids of the one after
+    uint64_t rm[8], rf = 0ull, rp = 0ull;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) rm[k] = 0ull;
+    if (lt < 27 && have_next) load_leaf_nbr(a.in_rec, id_next, rm, rf, rp);
+    int32_t id_next2 = -1;
+    if (lt < 27 && L + 2 * G < nL) id_next2 = __ldg(a.nbr + (L + 2 * G) * 27 + lt);
+    // this leaf's output record: bits 4 lt .. 4 lt + 3 (word lt / 16)
+    const unsigned long long* orec = reinterpret_cast<const unsigned long long*>(a.out_rec) + (size_t)L * 10;
+    const uint64_t ow = __ldg(orec + (lt >> 4));
+    const uint64_t ofirst = __ldg(orec + 8);
+    const uint64_t opre9 = __ldg(orec + 9);
+    // window positions 8 lt .. 8 lt + 7: input voxel present, its row
+    const LeafNbr* nb = h.nb[b];
+    uint32_t idx[8];
+    uint32_t act = 0u;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int p = 8 * lt + e;
+      idx[e] = 0u;
+      if (p < kHaloPos) {
+        const int hx = p / 100 - 1, hy = (p / 10) % 10 - 1, hz = p % 10 - 1;
+        const int ex = (hx < 0) ? -1 : (hx > 7 ? 1 : 0), ey = (hy < 0) ? -1 : (hy > 7 ? 1 : 0),
+                  ez = (hz < 0) ? -1 : (hz > 7 ? 1 : 0);
+        bool ac;
+        idx[e] = leaf_index_in(nb[(ex + 1) * 9 + (ey + 1) * 3 + (ez + 1)], ((hx & 7) << 6) | ((hy & 7) << 3) | (hz & 7),
+                               ac);
+        act |= (ac ? 1u : 0u) << e;
+      }
+    }
+    const int cnt = __popc(act);
+    int incl = cnt;
+#pragma unroll
+    for (int s = 1; s < 32; s <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, s);
+      if (lane >= s) incl += v;
+    }
+    if (lane == 31) h.scan[w] = incl;
+    loader_bar();  // scan totals visible; every thread done with the previous leaf's rows
+    int base = incl - cnt;
+    for (int v = 0; v < w; ++v) base += h.scan[v];
+    const int nact = h.scan[0] + h.scan[1] + h.scan[2] + h.scan[3];
+    const int nun = (nact + 3) >> 2;
+    // room: descriptor d is free once window i - kHaloWins is released; the
+    // pool units [ucur, ucur + nun) once every window starting before
+    // ucur + nun - kHaloPoolUnits is (windows are released in order)
+    while (rel < i && (rel <= i - kHaloWins || h.win[rel % kHaloWins].ustart < ucur + nun - kHaloPoolUnits)) {
+      mbar_wait(smem_u32(&h.wempty[rel % kHaloWins]), (uint32_t)((rel / kHaloWins) & 1), status);
+      ++rel;
+    }
+    HaloWin& win = h.win[d];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int p = 8 * lt + e;
+      if (p < kHaloPos) {
+        if ((act >> e) & 1u) {
+          win.slot[p] = (int16_t)((((ucur + (base >> 2)) % kHaloPoolUnits) << 2) | (base & 3));
+          h.rows[base] = (int32_t)idx[e];
+          ++base;
+        } else {
+          win.slot[p] = -1;
+        }
+      }
+    }
+    {  // window positions of the active outputs, in output order
+      const int wd = lt >> 4;
+      const uint32_t pre = wd ? (uint32_t)((opre9 >> (9 * (wd - 1))) & 511ull) : 0u;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int p = 4 * lt + e, bit = p & 63;
+        if ((ow >> bit) & 1ull) {
+          const int rank = (int)(pre + (uint32_t)__popcll(ow & ((1ull << bit) - 1ull)));
+          win.opos[rank] = (int16_t)((((p >> 6) + 1) * 10 + ((p >> 3) & 7) + 1) * 10 + (p & 7) + 1);
+        }
+      }
+      if (lt == 112) win.n = (int)(pre + (uint32_t)__popcll(ow));  // word 7: prefix + its own count
+      if (lt == 0) {
+        win.first = (int64_t)ofirst;
+        win.nact = nact;
+        win.ustart = ucur;
+      }
+    }
+    if (lt < 27 && have_next) store_leaf_nbr(h.nb[b ^ 1][lt], rm, rf, rp);
+    id_next = id_next2;
+    loader_bar();  // window map, output positions and row list complete
+    const uint32_t wb = smem_u32(&h.wfull[d]);
+    if (lt == 0) mbar_arrive_expect_tx(wb, (uint32_t)(nun * 4 * kHaloRowB));
+    for (int op = lt; op < nun; op += kLeafLoaderThreads) {
+      const int r0 = 4 * op;
+      int4 rows;
+      rows.x = h.rows[r0];
+      rows.y = r0 + 1 < nact ? h.rows[r0 + 1] : a.n_in;
+      rows.z = r0 + 2 < nact ? h.rows[r0 + 2] : a.n_in;
+      rows.w = r0 + 3 < nact ? h.rows[r0 + 3] : a.n_in;
+      tma_gather4(smem_u32(pool) + (uint32_t)(((ucur + op) % kHaloPoolUnits) * 4 * kHaloRowB), &a.tmx, 0, rows, wb);
+    }
+    ucur += nun;
+  }
+  // normally the row warps have seen every window land; after a give-up, let
+  // the last gathers finish before the block exits
+  if (lt == 0)
+    for (int k = i - 1; k >= 0 && k >= i - kHaloWins; --k)
+      mbar_drain(smem_u32(&h.wfull[k % kHaloWins]), (uint32_t)((k / kHaloWins) & 1));
+}
+
+// Operand-row warps (ct = thread 0..255 of warps 4-11).  Warp group g = ct /
+// 128 writes offset 2k + g of stage k; thread = tile row m in its warp's TMEM
+// lane quarter.  Tiles are packed here: 128 rows from the current leaf, or
+// its remaining rows and then the head of the block's next leaf (when the
+// current window is small enough that the next one always fits in the pool
+// beside it).  Returns the number of stages produced.
+__device__ int64_t halo_rows(HaloHead& h, const HaloArgs& a, const unsigned char* pool, uint32_t tmem, int ct) {
+  const int64_t G = gridDim.x, nL = a.n_leaf_out;
+  const int64_t nW = ((int64_t)blockIdx.x < nL) ? (nL - 1 - (int64_t)blockIdx.x) / G + 1 : 0;  // this block's leaves
+  const int S = a.stages;
+  const int lane = ct & 31, cw = ct >> 5, grp = cw >> 2, quarter = (kHaloRowWarp0 + cw) & 3;
+  const int m = quarter * 32 + lane;
+  const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(2 * a.acc_cols) + (uint32_t)(16 * grp);
+  uint32_t* const status = a.status;
+  int64_t kg = 0;
+  int ring_sb = 0;
+  uint32_t ring_ph = 0;
+  int nt = 0;          // tiles published
+  int64_t loaded = 0;  // windows seen landed
+  int64_t j = 0;       // current window
+  int r = 0;           // its next output
+  auto land = [&](int64_t x) {  // wait until window x has landed
+    while (loaded <= x) {
+      mbar_wait(smem_u32(&h.wfull[loaded % kHaloWins]), (uint32_t)((loaded / kHaloWins) & 1), status);
+      ++loaded;
+    }
+  };
+  auto release = [&](int64_t x) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&h.wempty[x % kHaloWins]));
+  };
+  while (j < nW) {
+    land(j);
+    const HaloWin& wa = h.win[j % kHaloWins];
+    const int na = *(volatile const int*)&wa.n;
+    const int ca = min(kRows, na - r);
+    const bool join = ca < kRows && j + 1 < nW && *(volatile const int*)&wa.nact <= kHaloJoinMax;
+    int cb = 0;
+    const HaloWin* wbp = nullptr;
+    if (join) {
+      land(j + 1);
+      wbp = &h.win[(j + 1) % kHaloWins];
+      cb = min(kRows - ca, *(volatile const int*)&wbp->n);
+    }
+    const int nrows = ca + cb;
+    if (ct == 0) {  // the tile for the MMA thread and the epilogue
+      const int ri = nt & (kInfoRing - 1);
+      if (nt >= kInfoRing) mbar_wait(smem_u32(&h.tinfo_empty[ri]), (uint32_t)(((nt / kInfoRing) - 1) & 1), status);
+      HaloTile& t = h.tile[ri];
+      t.q0a = *(volatile const int64_t*)&wa.first + r;
+      t.q0b = join ? *(volatile const int64_t*)&wbp->first : 0;
+      t.ca = ca;
+      t.nrows = nrows;
+      mbar_arrive(smem_u32(&h.tinfo_full[ri]));
+    }
+    ++nt;
+    // this thread's row: window and window position
+    const int16_t* sl = nullptr;
+    int pos = 0;
+    if (m < ca) {
+      sl = wa.slot;
+      pos = wa.opos[r + m];
+    } else if (m < nrows) {
+      sl = wbp->slot;
+      pos = wbp->opos[m - ca];
+    }
+    // pool rows of every stage's offset, looked up at once
+    int u[kHaloTileStages];
+#pragma unroll
+    for (int k = 0; k < kHaloTileStages; ++k) {
+      const int s = 2 * k + grp;
+      const int dsh = 100 * (s / 9) + 10 * ((s / 3) % 3) + s % 3 - 111;
+      u[k] = (sl != nullptr && s < 27) ? (int)sl[pos + dsh] : -1;
+    }
+#pragma unroll
+    for (int k = 0; k < kHaloTileStages; ++k, ++kg) {
+      const int sb = ring_sb;
+      if (kg >= S) mbar_wait(smem_u32(&h.aempty[sb]), ring_ph ^ 1u, status);
+      tc_fence_after();  // the MMAs that read this stage have completed
+      if (++ring_sb == S) {
+        ring_sb = 0;
+        ring_ph ^= 1u;
+      }
+      if (2 * k + grp < 27) {  // warp-uniform: the last stage has one offset
+        uint32_t v[16];
+        if (u[k] >= 0) {
+#pragma unroll
+          for (int p = 0; p < 4; ++p) {
+            const uint4 q = *reinterpret_cast<const uint4*>(pool + swz_off(u[k], p, kHaloRowB));
+            v[4 * p] = q.x;
+            v[4 * p + 1] = q.y;
+            v[4 * p + 2] = q.z;
+            v[4 * p + 3] = q.w;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[e] = 0u;
+        }
+        tmem_st16(tl + (uint32_t)(sb * 32), v);
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&h.afull[sb]));
+    }
+    // windows done with
+    r += ca;
+    if (r == na) {
+      release(j);
+      ++j;
+      r = 0;
+      if (join) {
+        r = cb;
+        if (cb == *(volatile const int*)&wbp->n) {
+          release(j);
+          ++j;
+          r = 0;
+        }
+      }
+    }
+  }
+  if (ct == 0) {  // no further tiles
+    const int ri = nt & (kInfoRing - 1);
+    if (nt >= kInfoRing) mbar_wait(smem_u32(&h.tinfo_empty[ri]), (uint32_t)(((nt / kInfoRing) - 1) & 1), status);
+    h.tile[ri].nrows = -1;
+    mbar_arrive(smem_u32(&h.tinfo_full[ri]));
+  }
+  return kg;
+}
+
+__global__ void __launch_bounds__(kUnThreads, 1) k_conv_halo(const __grid_constant__ HaloArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // [resident weights][pool][head], each 1024-aligned
+  unsigned char* wsm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  unsigned char* pool = wsm + a.w_bytes;
+  HaloHead& h = *reinterpret_cast<HaloHead*>(pool + (size_t)kHaloPoolUnits * 4 * kHaloRowB);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int S = a.stages, cout = a.cout;
+  const uint32_t acc_cols = (uint32_t)a.acc_cols;
+  const int64_t nL = a.n_leaf_out;
+  uint32_t* const status = a.status;
+
+  if (tid == 0) {
+    for (int k = 0; k < S; ++k) {
+      mbar_init(smem_u32(&h.afull[k]), kUnCopyWarps);  // one arrival per operand-row warp
+      mbar_init(smem_u32(&h.aempty[k]), 1);
+    }
+    for (int k = 0; k < kHaloWins; ++k) {
+      mbar_init(smem_u32(&h.wfull[k]), 1);
+      mbar_init(smem_u32(&h.wempty[k]), kUnCopyWarps);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&h.acc_full[b]), 1);
+      mbar_init(smem_u32(&h.acc_empty[b]), 128);
+    }
+    for (int r = 0; r < kInfoRing; ++r) {
+      mbar_init(smem_u32(&h.tinfo_full[r]), 1);
+      mbar_init(smem_u32(&h.tinfo_empty[r]), 4);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == kUnMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&h.tmem_base)),
+                 "r"(512)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  // weights, once: row s*cout + co holds wt[s][co][0..31] (64 B, 64-byte swizzle)
+  for (int e = tid; e < 27 * cout * 4; e += kUnThreads) {
+    const int rr = e >> 2, p = e & 3;
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.wt + (size_t)rr * 32 + 8 * p));
+    *reinterpret_cast<uint4*>(wsm + swz_off(rr, p, kHaloRowB)) = v;
+  }
+  fence_proxy_async();  // the tensor core reads what the generic proxy wrote
+  // neighbour records of the first leaf
+  if (tid < 27 && (int64_t)blockIdx.x < nL) {
+    uint64_t mk[8], f, p9;
+    load_leaf_nbr(a.in_rec, __ldg(a.nbr + (int64_t)blockIdx.x * 27 + tid), mk, f, p9);
+    store_leaf_nbr(h.nb[0][tid], mk, f, p9);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = h.tmem_base;
+
+  if (warp < kLeafLoaderThreads / 32) {
+    halo_loader(h, a, pool, tid);
+  } else if (warp < kUnMmaWarp) {
+    halo_rows(h, a, pool, tmem, tid - kLeafLoaderThreads);
+  } else if (warp == kUnMmaWarp) {
+    // ---------------- MMA issue (one thread): A from tensor memory, B resident
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(kRows, cout);
+      const uint32_t sbo = 8u * kHaloRowB;
+      const uint32_t wbase = smem_u32(wsm);
+      const uint32_t acol = 2u * acc_cols;
+      int m_sb = 0;
+      uint32_t m_ph = 0;
+      int i = 0;
+      for (;; ++i) {
+        const int r = i & (kInfoRing - 1), b = i & 1;
+        if (!mbar_wait(smem_u32(&h.tinfo_full[r]), (uint32_t)((i / kInfoRing) & 1), status)) break;
+        if (*(volatile const int*)&h.tile[r].nrows < 0) break;
+        if (i >= 2 && !mbar_wait(smem_u32(&h.acc_empty[b]), (uint32_t)(((i >> 1) - 1) & 1), status)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)b * acc_cols;
+        for (int k = 0; k < kHaloTileStages; ++k) {
+          mbar_wait(smem_u32(&h.afull[m_sb]), m_ph, status);
+          tc_fence_after();
+          const uint32_t ta = tmem + acol + (uint32_t)(m_sb * 32);
+          const int nk = 2 * k + 1 < 27 ? 4 : 2;  // 16 channels per MMA: offset 2k + kk / 2, channels 16 (kk & 1) ..
+          for (int kk = 0; kk < nk; ++kk) {
+            const uint32_t baddr = wbase + (uint32_t)((2 * k + (kk >> 1)) * cout * kHaloRowB) + (uint32_t)((kk & 1) * 32);
+            umma_bf16_ts(d, ta + (uint32_t)(kk * 8), sdesc_swz(baddr, 4u, sbo), idesc, (k > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(smem_u32(&h.aempty[m_sb]));
+          if (++m_sb == S) {
+            m_sb = 0;
+            m_ph ^= 1u;
+          }
+        }
+        umma_commit(smem_u32(&h.acc_full[b]));
+      }
+      // every MMA has completed before tensor memory is freed
+      if (i > 0) mbar_drain(smem_u32(&h.acc_full[(i - 1) & 1]), (uint32_t)(((i - 1) >> 1) & 1));
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue (warps 13-16): TMEM lane quarter warp & 3
+    const int quarter = warp & 3, m = quarter * 32 + lane;
+    const int cs = a.cout_store, out_bf16 = a.out_bf16;
+    for (int i = 0;; ++i) {
+      const int r = i & (kInfoRing - 1), b = i & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&h.tinfo_full[r]), (uint32_t)((i / kInfoRing) & 1), status)))
+        break;
+      const HaloTile& t = h.tile[r];
+      const int nrows = *(volatile const int*)&t.nrows;
+      if (nrows < 0) break;
+      const int ca = *(volatile const int*)&t.ca;
+      const int64_t q = m < ca ? *(volatile const int64_t*)&t.q0a + m : *(volatile const int64_t*)&t.q0b + (m - ca);
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&h.acc_full[b]), (uint32_t)((i >> 1) & 1), status))) break;
+      tc_fence_after();
+      const uint32_t trow = tmem + (uint32_t)b * acc_cols + ((uint32_t)(quarter * 32) << 16);
+      for (int c = 0; c < cout; c += 16) {
+        uint32_t v[16];
+        tmem_ld16(trow + (uint32_t)c, v);
+        const int ncol = min(16, cs - c);  // 16, 8 (cout_store an odd multiple of 8) or none
+        if (m >= nrows || ncol <= 0) continue;
+        if (out_bf16) {
+          uint4 v0, v1;
+          v0.x = pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1]));
+          v0.y = pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3]));
+          v0.z = pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5]));
+          v0.w = pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7]));
+          v1.x = pack_bf16x2(__uint_as_float(v[8]), __uint_as_float(v[9]));
+          v1.y = pack_bf16x2(__uint_as_float(v[10]), __uint_as_float(v[11]));
+          v1.z = pack_bf16x2(__uint_as_float(v[12]), __uint_as_float(v[13]));
+          v1.w = pack_bf16x2(__uint_as_float(v[14]), __uint_as_float(v[15]));
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.y) + q * cs + c);
+          dst[0] = v0;
+          if (ncol == 16) dst[1] = v1;
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<float*>(a.y) + q * cs + c);
+          dst[0] = make_uint4(v[0], v[1], v[2], v[3]);
+          dst[1] = make_uint4(v[4], v[5], v[6], v[7]);
+          if (ncol == 16) {
+            dst[2] = make_uint4(v[8], v[9], v[10], v[11]);
+            dst[3] = make_uint4(v[12], v[13], v[14], v[15]);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&h.acc_empty[b]));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&h.tinfo_empty[r]));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kUnMmaWarp) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512) : "memory");
+  }
+}
+
 // ============================================================== weight gradient
 // dW[s][ci][co] = sum over the pairs (p, q) of list s of x[p][ci] * dy[q][co]
 // (fp32 accumulation).  Blocks stride over chunks of the pair array (a chunk
@@ -2468,6 +2969,55 @@ fvx_status launch_conv_leaf(const char* who, fvx_grid gin, fvx_kmap m, const int
   return FVX_OK;
 }
 
+// Halo-staged launch (stride-1 forward map with its leaf table, cin 32, MMA N
+// = cout <= 64): persistent, one block per SM; the weights resident in shared
+// memory beside the window pool, the A ring in the tensor memory the two
+// accumulators leave free.
+fvx_status launch_conv_halo(const char* who, EncodeTiledFn enc, fvx_grid gin, fvx_kmap m, fvx_dtype dt,
+                            const void* feats, int64_t cout, int64_t cout_store, void* out, const __nv_bfloat16* wt,
+                            uint32_t* status, cudaStream_t s) {
+  const fvx_grid_s* go = m->gout;
+  HaloArgs a;
+  FVX_TRY(encode_2d(enc, &a.tmx, feats, 32, gin->n_active, 32, 1, CU_TENSOR_MAP_SWIZZLE_64B,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE, who));
+  a.wt = wt;
+  a.in_rec = gin->leaf_rec;
+  a.nbr = m->leaf_nbr;
+  a.out_rec = go->leaf_rec;
+  a.y = out;
+  a.status = status;
+  a.n_leaf_out = go->n_leaf;
+  a.n_in = (int)gin->n_active;
+  a.cout = (int)cout;
+  a.cout_store = (int)cout_store;
+  a.out_bf16 = (dt == FVX_BF16_OUT_BF16) ? 1 : 0;
+  int cols = 32;
+  while (cols < cout) cols <<= 1;
+  a.acc_cols = cols;                                                 // per accumulator; two accumulators
+  a.stages = std::min((512 - 2 * cols) / 32, kHaloMaxRing);          // A stages: 32 columns each
+  a.w_bytes = (int)((27 * cout * kHaloRowB + 1023) & ~(int64_t)1023);  // a multiple of 1024 already
+  const size_t smem = 1024 + (size_t)a.w_bytes + (size_t)kHaloPoolUnits * 4 * kHaloRowB + sizeof(HaloHead);
+  int optin = 0, dev = 0;
+  FVX_CUDA(cudaGetDevice(&dev));
+  FVX_CUDA(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
+  if (smem > (size_t)optin) {
+    set_error("%s: the halo-staged convolution needs %zu bytes of shared memory (%d per block)", who, smem, optin);
+    return FVX_ERR_CAPACITY;
+  }
+  FVX_CUDA(cudaFuncSetAttribute(k_conv_halo, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  int sms = 0;
+  FVX_TRY(device_sm_count(&sms));
+  const int64_t grid = std::min<int64_t>(go->n_leaf, (int64_t)sms);
+  {
+    LaunchScope ls("conv_halo", s);
+    k_conv_halo<<<(unsigned)grid, kUnThreads, smem, s>>>(a);
+  }
+  FVX_TRY(check_launch("conv_halo"));
+  t_last_algo = FVX_CONV_HALO;
+  t_last_kernel = "conv_halo";
+  return FVX_OK;
+}
+
 // Union-staged pair-list launch (cin 32 or 64, cout <= 128): stage ring and
 // two union buffers sized to shared memory; FVX_ERR_CAPACITY when they cannot
 // hold at least one stage's worth of rows (the caller falls back).
@@ -2542,6 +3092,26 @@ fvx_status launch_conv_bf16(const char* who, fvx_grid gin, fvx_kmap m, fvx_dtype
   const bool dense_leaves = go->n_leaf > 0 && (double)go->n_active >= 0.2 * 512.0 * (double)go->n_leaf;
   if (leaf_ok && (algo == FVX_CONV_LEAF || (algo == FVX_CONV_AUTO && dense_leaves)))
     return launch_conv_leaf(who, gin, m, m->leaf_nbr, dt, feats, cin, cout, cout, out, wt, status, s);
+  // halo-staged: stride 1, cin 32; automatic when the output leaves hold at
+  // least kHaloAutoPerLeaf active voxels on average (sparser leaves leave
+  // most of each 128-row tile empty)
+  const bool halo_ok =
+      m->stride == 1 && m->leaf_nbr != nullptr && cin == 32 && cout <= kHaloMaxCout && gin->n_active > 0;
+  if (algo == FVX_CONV_HALO && !halo_ok) {
+    set_error("%s: the halo-staged convolution needs a forward stride-1 map, cin 32 and cout <= %d (got stride "
+              "%d%s, %lld, %lld)",
+              who, kHaloMaxCout, (int)m->stride, m->transposed ? " transposed" : "", (long long)cin,
+              (long long)cout_real);
+    return FVX_ERR_INVALID_ARG;
+  }
+  const bool halo_auto = go->n_leaf > 0 && (double)go->n_active >= kHaloAutoPerLeaf * (double)go->n_leaf;
+  if (halo_ok && (algo == FVX_CONV_HALO || (algo == FVX_CONV_AUTO && halo_auto))) {
+    EncodeTiledFn henc = encode_tiled();
+    if (henc) {
+      const fvx_status st = launch_conv_halo(who, henc, gin, m, dt, feats, cout, cout_real, out, wt, status, s);
+      if (st != FVX_ERR_CAPACITY || algo == FVX_CONV_HALO) return st;
+    }
+  }
   ConvArgs a;
   a.x = (const __nv_bfloat16*)feats;
   a.wt = wt;
@@ -3076,7 +3646,7 @@ extern "C" fvx_status fvx_sparse_conv_dgrad(fvx_grid gin, fvx_grid gout, fvx_kma
 
 extern "C" fvx_status fvx_set_conv_algo(fvx_conv_algo algo) {
   if (algo != FVX_CONV_AUTO && algo != FVX_CONV_GATHER && algo != FVX_CONV_LEAF && algo != FVX_CONV_DIRECT &&
-      algo != FVX_CONV_UNION) {
+      algo != FVX_CONV_UNION && algo != FVX_CONV_HALO) {
     set_error("fvx_set_conv_algo: unknown value %d", (int)algo);
     return FVX_ERR_INVALID_ARG;
   }

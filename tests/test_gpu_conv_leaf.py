@@ -187,7 +187,10 @@ def test_auto_choice(cuda_device, dense_case, sparse_case):
         fvx.sparse_conv(g, g, km, x, W)
         assert fvx.last_conv_algo() == want
     g, _, km, _ = dense_case
-    x, W = G.bf16_inputs(3, g.n_active, 32, 32)  # too many channels for the leaf kernel
+    x, W = G.bf16_inputs(3, g.n_active, 32, 32)  # too many channels for the leaf kernel: the halo-staged one
+    fvx.sparse_conv(g, g, km, x, W)
+    assert fvx.last_conv_algo() == fvx.FVX_CONV_HALO
+    x, W = G.bf16_inputs(3, g.n_active, 64, 32)  # neither leaf kernel: pair lists
     fvx.sparse_conv(g, g, km, x, W)
     assert fvx.last_conv_algo() == fvx.FVX_CONV_GATHER
 
