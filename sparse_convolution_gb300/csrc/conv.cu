@@ -188,6 +188,16 @@ __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
     if ((it & 1023u) == 1023u && globaltimer() - t0 > kWaitNs) return;
 }
 
+// mbar_wait with its polling loop out of line: the first poll inline, the
+// rest (rare in a pipeline that keeps up) in one shared copy of the code.
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, uint32_t* status) {
+  return mbar_wait(bar, parity, status);
+}
+__device__ __forceinline__ bool mbar_wait_lean(uint32_t bar, uint32_t parity, uint32_t* status) {
+  if (mbar_try(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, status);
+}
+
 // cp.async of 16 bytes (src_bytes 0: zero fill).  No "memory" clobber: the
 // copy only writes the stage buffer, which this thread does not read, and
 // volatile asm statements keep their order (commit / wait below).
@@ -1839,14 +1849,20 @@ __global__ void __launch_bounds__(kLeafThreads, G8 == 1 ? 2 : 1) k_conv_leaf(con
 //   warps 4-11  operand rows: warps 4-7 the first offset of each stage, warps
 //               8-11 the second, thread = tile row (its warp's TMEM lane
 //               quarter); they also pack the tiles and publish them.
-//   warp 12     MMA issue and TMEM owner (two accumulators, the A ring).
-//   warps 13-16 epilogue: row m of a tile to its output row.
+//   warp 12     MMA issue and TMEM owner: per tile two accumulator chains
+//               (input channels 0-15 and 16-31 of every offset, issued
+//               alternately so that consecutive MMAs are independent: a chain
+//               of dependent N <= 64 MMAs runs at the MMA latency, not its
+//               throughput), two tiles in flight, and the A ring.
+//   warps 13-16 epilogue: the two chains added, row m of a tile to its
+//               output row.
 constexpr int kHaloPos = 1000;                       // window positions
 constexpr int kHaloRowB = 64;                        // pool row: 32 bf16 channels
-constexpr int kHaloPoolUnits = 384;                  // pool of 384 x 4 rows (96 KB)
+constexpr int kHaloPoolRows = 1536;                  // pool rows (96 KB)
 constexpr int kHaloWins = 4;                         // window descriptors
-constexpr int kHaloJoinMax = kHaloPoolUnits * 4 - kHaloPos;  // a window this small leaves room for any next one
+constexpr int kHaloJoinMax = kHaloPoolRows - kHaloPos;  // a window this small leaves room for any next one
 constexpr int kHaloTileStages = 14;                  // 27 offsets, two per stage
+static_assert(kHaloTileStages % 2 == 0, "the operand rows produce stages in pairs");
 constexpr int kHaloMaxRing = 16;                     // A stages in tensor memory at most
 constexpr int kHaloMaxCout = 64;
 constexpr int kHaloRowWarp0 = 4;                    // first operand-row warp                     // resident weights: 27 x 64 x 64 B
@@ -1858,7 +1874,7 @@ struct HaloWin {
   int64_t first;           // output row of the leaf's first active voxel
   int32_t n;               // active outputs of the leaf
   int32_t nact;            // window positions holding an input voxel
-  int32_t ustart;          // first pool unit (allocation counter, not reduced)
+  int32_t ustart;          // first pool row (allocation counter, not reduced)
   int32_t pad;
 };
 
@@ -1871,7 +1887,6 @@ struct HaloTile {
 struct HaloHead {
   HaloWin win[kHaloWins];
   LeafNbr nb[2][27];       // neighbour records of the loader's current and next leaf
-  int32_t rows[kHaloPos];  // input row of each new pool row (loader only)
   int32_t scan[4];
   HaloTile tile[kInfoRing];
   unsigned long long afull[kHaloMaxRing], aempty[kHaloMaxRing];  // A stages: rows <-> MMA
@@ -1881,8 +1896,8 @@ struct HaloHead {
   uint32_t tmem_base;
 };
 
-struct alignas(128) HaloArgs {
-  CUtensorMap tmx;          // feats [n_in][32] bf16: box {32, 1}, 64-byte swizzle
+struct HaloArgs {
+  const __nv_bfloat16* x;   // feats [n_in][32] bf16
   const __nv_bfloat16* wt;  // [27][cout][32] bf16
   const uint64_t* in_rec;   // input grid leaf records [L][10]
   const int32_t* nbr;       // [L_out][27] input leaf per leaf offset, -1 absent
@@ -1890,7 +1905,6 @@ struct alignas(128) HaloArgs {
   void* y;                  // [n_out][cout_store], fp32 or bf16
   uint32_t* status;
   int64_t n_leaf_out;
-  int n_in;                 // feature rows; row index n_in reads as zeros
   int cout, cout_store, out_bf16, stages, acc_cols, w_bytes;
 };
 
@@ -1913,16 +1927,48 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// Window loader (warps 0-3, thread lt = 0..127).
+// Window loader (warps 0-3, thread lt = 0..127).  Thread c < 100 owns window
+// column c = (hx+1)*10 + hy+1: the ten positions hz = -1..8 above (hx, hy),
+// which lie in three leaves (ez = -1: local z 7; ez = 0: local z 0..7, one
+// byte of a mask word; ez = +1: local z 0).  It finds its column's input
+// voxels and their rows from those three records, takes pool rows for them
+// (a block-wide scan over the columns, so the window is stored in window
+// order), and copies the rows itself (cp.async, 16 bytes at a time, to their
+// swizzled places); every loader thread then makes the window's barrier track
+// its copies.
+__device__ __forceinline__ uint32_t leaf_pre(const LeafNbr& L, int w) {
+  return w ? (uint32_t)((L.pre9 >> (9 * (w - 1))) & 511ull) : 0u;
+}
+__device__ __forceinline__ void cp_async16_row(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ void halo_loader(HaloHead& h, const HaloArgs& a, unsigned char* pool, int lt) {
   const int64_t G = gridDim.x, nL = a.n_leaf_out;
   uint32_t* const status = a.status;
   const int lane = lt & 31, w = lt >> 5;
+  // this thread's window column
+  const int hx = lt / 10 - 1, hy = lt % 10 - 1;
+  const int ex = (hx < 0) ? -1 : (hx > 7 ? 1 : 0), ey = (hy < 0) ? -1 : (hy > 7 ? 1 : 0);
+  const int nb0 = (ex + 1) * 9 + (ey + 1) * 3;  // its leaf below; + 1 its own level, + 2 above
+  const int xl = hx & 7, yb = (hy & 7) * 8;     // mask word and the column's first bit in it
   int32_t id_next = -1;
   if (lt < 27 && (int64_t)blockIdx.x + G < nL) id_next = __ldg(a.nbr + ((int64_t)blockIdx.x + G) * 27 + lt);
   int i = 0;
-  int ucur = 0;  // pool units allocated so far
+  int ucur = 0;  // pool rows allocated so far
   int rel = 0;   // windows known to be released
   for (int64_t L = blockIdx.x; L < nL; L += G, ++i) {
     const int b = i & 1, d = i % kHaloWins;
@@ -1939,23 +1985,17 @@ __device__ void halo_loader(HaloHead& h, const HaloArgs& a, unsigned char* pool,
     const uint64_t ow = __ldg(orec + (lt >> 4));
     const uint64_t ofirst = __ldg(orec + 8);
     const uint64_t opre9 = __ldg(orec + 9);
-    // window positions 8 lt .. 8 lt + 7: input voxel present, its row
-    const LeafNbr* nb = h.nb[b];
-    uint32_t idx[8];
-    uint32_t act = 0u;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int p = 8 * lt + e;
-      idx[e] = 0u;
-      if (p < kHaloPos) {
-        const int hx = p / 100 - 1, hy = (p / 10) % 10 - 1, hz = p % 10 - 1;
-        const int ex = (hx < 0) ? -1 : (hx > 7 ? 1 : 0), ey = (hy < 0) ? -1 : (hy > 7 ? 1 : 0),
-                  ez = (hz < 0) ? -1 : (hz > 7 ? 1 : 0);
-        bool ac;
-        idx[e] = leaf_index_in(nb[(ex + 1) * 9 + (ey + 1) * 3 + (ez + 1)], ((hx & 7) << 6) | ((hy & 7) << 3) | (hz & 7),
-                               ac);
-        act |= (ac ? 1u : 0u) << e;
-      }
+    // the column: active bits (bit hz + 1) and the input row of its first
+    // voxel in each of the three leaves
+    uint32_t act = 0u, r_lo = 0u, r_mid = 0u, r_hi = 0u;
+    if (lt < 100) {
+      const LeafNbr* nb = h.nb[b] + nb0;
+      const uint64_t wl = nb[0].mask[xl], wm = nb[1].mask[xl], wh = nb[2].mask[xl];
+      const uint32_t byte = (uint32_t)(wm >> yb) & 0xFFu;
+      act = (uint32_t)((wl >> (yb + 7)) & 1ull) | (byte << 1) | ((uint32_t)((wh >> yb) & 1ull) << 9);
+      r_lo = nb[0].first + leaf_pre(nb[0], xl) + (uint32_t)__popcll(wl & ((2ull << (yb + 6)) - 1ull));
+      r_mid = nb[1].first + leaf_pre(nb[1], xl) + (uint32_t)__popcll(yb ? (wm & ((1ull << yb) - 1ull)) : 0ull);
+      r_hi = nb[2].first + leaf_pre(nb[2], xl) + (uint32_t)__popcll(yb ? (wh & ((1ull << yb) - 1ull)) : 0ull);
     }
     const int cnt = __popc(act);
     int incl = cnt;
@@ -1965,31 +2005,40 @@ __device__ void halo_loader(HaloHead& h, const HaloArgs& a, unsigned char* pool,
       if (lane >= s) incl += v;
     }
     if (lane == 31) h.scan[w] = incl;
-    loader_bar();  // scan totals visible; every thread done with the previous leaf's rows
+    loader_bar();  // scan totals visible
     int base = incl - cnt;
     for (int v = 0; v < w; ++v) base += h.scan[v];
     const int nact = h.scan[0] + h.scan[1] + h.scan[2] + h.scan[3];
-    const int nun = (nact + 3) >> 2;
     // room: descriptor d is free once window i - kHaloWins is released; the
-    // pool units [ucur, ucur + nun) once every window starting before
-    // ucur + nun - kHaloPoolUnits is (windows are released in order)
-    while (rel < i && (rel <= i - kHaloWins || h.win[rel % kHaloWins].ustart < ucur + nun - kHaloPoolUnits)) {
-      mbar_wait(smem_u32(&h.wempty[rel % kHaloWins]), (uint32_t)((rel / kHaloWins) & 1), status);
+    // pool rows [ucur, ucur + nact) once every window starting before
+    // ucur + nact - kHaloPoolRows is (windows are released in order)
+    while (rel < i && (rel <= i - kHaloWins || h.win[rel % kHaloWins].ustart < ucur + nact - kHaloPoolRows)) {
+      mbar_wait_lean(smem_u32(&h.wempty[rel % kHaloWins]), (uint32_t)((rel / kHaloWins) & 1), status);
       ++rel;
     }
     HaloWin& win = h.win[d];
+    if (lt < 100) {
+      // pool rows and copies of the column's voxels, in window order
+      const uint32_t pbase = smem_u32(pool);
+      uint32_t sl[5];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int p = 8 * lt + e;
-      if (p < kHaloPos) {
+      for (int e = 0; e < 10; ++e) {
+        int16_t v = -1;
         if ((act >> e) & 1u) {
-          win.slot[p] = (int16_t)((((ucur + (base >> 2)) % kHaloPoolUnits) << 2) | (base & 3));
-          h.rows[base] = (int32_t)idx[e];
+          const int prow = (ucur + base) % kHaloPoolRows;
+          v = (int16_t)prow;
+          const uint32_t row = e == 0 ? r_lo : e == 9 ? r_hi : r_mid + (uint32_t)__popc((act >> 1) & ((1u << (e - 1)) - 1u));
+          const __nv_bfloat16* src = a.x + (size_t)row * 32;
+#pragma unroll
+          for (int p = 0; p < 4; ++p) cp_async16_row(pbase + swz_off(prow, p, kHaloRowB), src + 8 * p);
           ++base;
-        } else {
-          win.slot[p] = -1;
         }
+        if (e & 1) sl[e >> 1] |= (uint32_t)(uint16_t)v << 16;
+        else sl[e >> 1] = (uint32_t)(uint16_t)v;
       }
+      uint32_t* dst = reinterpret_cast<uint32_t*>(&win.slot[10 * lt]);  // 20 bytes per column, 4-byte aligned
+#pragma unroll
+      for (int k = 0; k < 5; ++k) dst[k] = sl[k];
     }
     {  // window positions of the active outputs, in output order
       const int wd = lt >> 4;
@@ -2011,25 +2060,17 @@ __device__ void halo_loader(HaloHead& h, const HaloArgs& a, unsigned char* pool,
     }
     if (lt < 27 && have_next) store_leaf_nbr(h.nb[b ^ 1][lt], rm, rf, rp);
     id_next = id_next2;
-    loader_bar();  // window map, output positions and row list complete
-    const uint32_t wb = smem_u32(&h.wfull[d]);
-    if (lt == 0) mbar_arrive_expect_tx(wb, (uint32_t)(nun * 4 * kHaloRowB));
-    for (int op = lt; op < nun; op += kLeafLoaderThreads) {
-      const int r0 = 4 * op;
-      int4 rows;
-      rows.x = h.rows[r0];
-      rows.y = r0 + 1 < nact ? h.rows[r0 + 1] : a.n_in;
-      rows.z = r0 + 2 < nact ? h.rows[r0 + 2] : a.n_in;
-      rows.w = r0 + 3 < nact ? h.rows[r0 + 3] : a.n_in;
-      tma_gather4(smem_u32(pool) + (uint32_t)(((ucur + op) % kHaloPoolUnits) * 4 * kHaloRowB), &a.tmx, 0, rows, wb);
-    }
-    ucur += nun;
+    // the window's barrier completes once every loader thread's copies have
+    // landed (one arrival per thread, counted at initialisation) and thread 0
+    // has published the descriptor
+    cp_async_mbar_arrive_noinc(smem_u32(&h.wfull[d]));
+    loader_bar();  // every thread done with this leaf's records and scan totals
+    if (lt == 0) mbar_arrive(smem_u32(&h.wfull[d]));
+    ucur += nact;
   }
   // normally the row warps have seen every window land; after a give-up, let
-  // the last gathers finish before the block exits
-  if (lt == 0)
-    for (int k = i - 1; k >= 0 && k >= i - kHaloWins; --k)
-      mbar_drain(smem_u32(&h.wfull[k % kHaloWins]), (uint32_t)((k / kHaloWins) & 1));
+  // this thread's last copies finish before the block exits
+  cp_async_wait_all();
 }
 
 // Operand-row warps (ct = thread 0..255 of warps 4-11).  Warp group g = ct /
@@ -2044,7 +2085,7 @@ __device__ int64_t halo_rows(HaloHead& h, const HaloArgs& a, const unsigned char
   const int S = a.stages;
   const int lane = ct & 31, cw = ct >> 5, grp = cw >> 2, quarter = (kHaloRowWarp0 + cw) & 3;
   const int m = quarter * 32 + lane;
-  const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(2 * a.acc_cols) + (uint32_t)(16 * grp);
+  const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(4 * a.acc_cols) + (uint32_t)(16 * grp);
   uint32_t* const status = a.status;
   int64_t kg = 0;
   int ring_sb = 0;
@@ -2055,7 +2096,7 @@ __device__ int64_t halo_rows(HaloHead& h, const HaloArgs& a, const unsigned char
   int r = 0;           // its next output
   auto land = [&](int64_t x) {  // wait until window x has landed
     while (loaded <= x) {
-      mbar_wait(smem_u32(&h.wfull[loaded % kHaloWins]), (uint32_t)((loaded / kHaloWins) & 1), status);
+      mbar_wait_lean(smem_u32(&h.wfull[loaded % kHaloWins]), (uint32_t)((loaded / kHaloWins) & 1), status);
       ++loaded;
     }
   };
@@ -2079,7 +2120,7 @@ __device__ int64_t halo_rows(HaloHead& h, const HaloArgs& a, const unsigned char
     const int nrows = ca + cb;
     if (ct == 0) {  // the tile for the MMA thread and the epilogue
       const int ri = nt & (kInfoRing - 1);
-      if (nt >= kInfoRing) mbar_wait(smem_u32(&h.tinfo_empty[ri]), (uint32_t)(((nt / kInfoRing) - 1) & 1), status);
+      if (nt >= kInfoRing) mbar_wait_lean(smem_u32(&h.tinfo_empty[ri]), (uint32_t)(((nt / kInfoRing) - 1) & 1), status);
       HaloTile& t = h.tile[ri];
       t.q0a = *(volatile const int64_t*)&wa.first + r;
       t.q0b = join ? *(volatile const int64_t*)&wbp->first : 0;
@@ -2098,44 +2139,62 @@ __device__ int64_t halo_rows(HaloHead& h, const HaloArgs& a, const unsigned char
       sl = wbp->slot;
       pos = wbp->opos[m - ca];
     }
-    // pool rows of every stage's offset, looked up at once
-    int u[kHaloTileStages];
-#pragma unroll
-    for (int k = 0; k < kHaloTileStages; ++k) {
-      const int s = 2 * k + grp;
+    // two stages per tensor-memory wait: both stages' pool rows loaded first
+    // (before the ring wait), both stored, one wait, two arrivals; the pool
+    // rows of the next pair looked up meanwhile.  The loop stays rolled: the
+    // four warp roles run different code at once, and an unrolled body misses
+    // in the instruction cache.
+    auto lookup = [&](int k, int t) {
+      const int s = 2 * (k + t) + grp;
       const int dsh = 100 * (s / 9) + 10 * ((s / 3) % 3) + s % 3 - 111;
-      u[k] = (sl != nullptr && s < 27) ? (int)sl[pos + dsh] : -1;
-    }
-#pragma unroll
-    for (int k = 0; k < kHaloTileStages; ++k, ++kg) {
-      const int sb = ring_sb;
-      if (kg >= S) mbar_wait(smem_u32(&h.aempty[sb]), ring_ph ^ 1u, status);
-      tc_fence_after();  // the MMAs that read this stage have completed
-      if (++ring_sb == S) {
-        ring_sb = 0;
-        ring_ph ^= 1u;
+      return (sl != nullptr && s < 27) ? (int)sl[pos + dsh] : -1;
+    };
+    int un0 = lookup(0, 0), un1 = lookup(0, 1);
+#pragma unroll 1
+    for (int k = 0; k < kHaloTileStages; k += 2, kg += 2) {
+      const int uc[2] = {un0, un1};
+      if (k + 2 < kHaloTileStages) {
+        un0 = lookup(k + 2, 0);
+        un1 = lookup(k + 2, 1);
       }
-      if (2 * k + grp < 27) {  // warp-uniform: the last stage has one offset
-        uint32_t v[16];
-        if (u[k] >= 0) {
+      uint32_t v[2][16];
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const int u = uc[t];
+        if (u >= 0) {
 #pragma unroll
           for (int p = 0; p < 4; ++p) {
-            const uint4 q = *reinterpret_cast<const uint4*>(pool + swz_off(u[k], p, kHaloRowB));
-            v[4 * p] = q.x;
-            v[4 * p + 1] = q.y;
-            v[4 * p + 2] = q.z;
-            v[4 * p + 3] = q.w;
+            const uint4 q = *reinterpret_cast<const uint4*>(pool + swz_off(u, p, kHaloRowB));
+            v[t][4 * p] = q.x;
+            v[t][4 * p + 1] = q.y;
+            v[t][4 * p + 2] = q.z;
+            v[t][4 * p + 3] = q.w;
           }
         } else {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) v[e] = 0u;
+          for (int e = 0; e < 16; ++e) v[t][e] = 0u;
         }
-        tmem_st16(tl + (uint32_t)(sb * 32), v);
-        tmem_st_wait();
       }
+      int sb[2];
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        sb[t] = ring_sb;
+        if (kg + t >= S) mbar_wait_lean(smem_u32(&h.aempty[ring_sb]), ring_ph ^ 1u, status);
+        if (++ring_sb == S) {
+          ring_sb = 0;
+          ring_ph ^= 1u;
+        }
+      }
+      tc_fence_after();  // the MMAs that read these stages have completed
+      tmem_st16(tl + (uint32_t)(sb[0] * 32), v[0]);
+      if (2 * (k + 1) + grp < 27) tmem_st16(tl + (uint32_t)(sb[1] * 32), v[1]);  // warp-uniform: offset 26 is the last
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&h.afull[sb]));
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&h.afull[sb[0]]));
+        mbar_arrive(smem_u32(&h.afull[sb[1]]));
+      }
     }
     // windows done with
     r += ca;
@@ -2155,7 +2214,7 @@ __device__ int64_t halo_rows(HaloHead& h, const HaloArgs& a, const unsigned char
   }
   if (ct == 0) {  // no further tiles
     const int ri = nt & (kInfoRing - 1);
-    if (nt >= kInfoRing) mbar_wait(smem_u32(&h.tinfo_empty[ri]), (uint32_t)(((nt / kInfoRing) - 1) & 1), status);
+    if (nt >= kInfoRing) mbar_wait_lean(smem_u32(&h.tinfo_empty[ri]), (uint32_t)(((nt / kInfoRing) - 1) & 1), status);
     h.tile[ri].nrows = -1;
     mbar_arrive(smem_u32(&h.tinfo_full[ri]));
   }
@@ -2167,7 +2226,7 @@ __global__ void __launch_bounds__(kUnThreads, 1) k_conv_halo(const __grid_consta
   // [resident weights][pool][head], each 1024-aligned
   unsigned char* wsm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   unsigned char* pool = wsm + a.w_bytes;
-  HaloHead& h = *reinterpret_cast<HaloHead*>(pool + (size_t)kHaloPoolUnits * 4 * kHaloRowB);
+  HaloHead& h = *reinterpret_cast<HaloHead*>(pool + (size_t)kHaloPoolRows * kHaloRowB);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = a.stages, cout = a.cout;
   const uint32_t acc_cols = (uint32_t)a.acc_cols;
@@ -2180,7 +2239,7 @@ __global__ void __launch_bounds__(kUnThreads, 1) k_conv_halo(const __grid_consta
       mbar_init(smem_u32(&h.aempty[k]), 1);
     }
     for (int k = 0; k < kHaloWins; ++k) {
-      mbar_init(smem_u32(&h.wfull[k]), 1);
+      mbar_init(smem_u32(&h.wfull[k]), kLeafLoaderThreads + 1);
       mbar_init(smem_u32(&h.wempty[k]), kUnCopyWarps);
     }
     for (int b = 0; b < 2; ++b) {
@@ -2225,29 +2284,38 @@ __global__ void __launch_bounds__(kUnThreads, 1) k_conv_halo(const __grid_consta
     // ---------------- MMA issue (one thread): A from tensor memory, B resident
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16(kRows, cout);
-      const uint32_t sbo = 8u * kHaloRowB;
-      const uint32_t wbase = smem_u32(wsm);
-      const uint32_t acol = 2u * acc_cols;
+      // B of stage k, MMA kk (offset 2k + kk / 2, channels 16 (kk & 1) ..):
+      // the descriptor of offset 0 advanced in 16-byte units
+      const uint64_t bdesc0 = sdesc_swz(smem_u32(wsm), 4u, 8u * kHaloRowB);
+      const uint32_t bo2 = (uint32_t)(cout * kHaloRowB) >> 4, bstep = 2u * bo2;
+      const uint32_t abase = tmem + 4u * acc_cols;
+      const uint32_t afull0 = smem_u32(&h.afull[0]), aempty0 = smem_u32(&h.aempty[0]);
       int m_sb = 0;
       uint32_t m_ph = 0;
       int i = 0;
       for (;; ++i) {
         const int r = i & (kInfoRing - 1), b = i & 1;
-        if (!mbar_wait(smem_u32(&h.tinfo_full[r]), (uint32_t)((i / kInfoRing) & 1), status)) break;
+        if (!mbar_wait_lean(smem_u32(&h.tinfo_full[r]), (uint32_t)((i / kInfoRing) & 1), status)) break;
         if (*(volatile const int*)&h.tile[r].nrows < 0) break;
-        if (i >= 2 && !mbar_wait(smem_u32(&h.acc_empty[b]), (uint32_t)(((i >> 1) - 1) & 1), status)) break;
+        if (i >= 2 && !mbar_wait_lean(smem_u32(&h.acc_empty[b]), (uint32_t)(((i >> 1) - 1) & 1), status)) break;
         tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)b * acc_cols;
+        // two accumulator chains, channels 0-15 and 16-31 of every offset,
+        // issued alternately: consecutive MMAs do not wait for each other
+        const uint32_t d0 = tmem + (uint32_t)(2 * b) * acc_cols, d1 = d0 + acc_cols;
+        uint64_t bd = bdesc0;
+#pragma unroll 1
         for (int k = 0; k < kHaloTileStages; ++k) {
-          mbar_wait(smem_u32(&h.afull[m_sb]), m_ph, status);
+          mbar_wait_lean(afull0 + (uint32_t)(m_sb * 8), m_ph, status);
           tc_fence_after();
-          const uint32_t ta = tmem + acol + (uint32_t)(m_sb * 32);
-          const int nk = 2 * k + 1 < 27 ? 4 : 2;  // 16 channels per MMA: offset 2k + kk / 2, channels 16 (kk & 1) ..
-          for (int kk = 0; kk < nk; ++kk) {
-            const uint32_t baddr = wbase + (uint32_t)((2 * k + (kk >> 1)) * cout * kHaloRowB) + (uint32_t)((kk & 1) * 32);
-            umma_bf16_ts(d, ta + (uint32_t)(kk * 8), sdesc_swz(baddr, 4u, sbo), idesc, (k > 0 || kk > 0) ? 1u : 0u);
+          const uint32_t ta = abase + (uint32_t)(m_sb * 32);
+          umma_bf16_ts(d0, ta, bd, idesc, k > 0 ? 1u : 0u);
+          umma_bf16_ts(d1, ta + 8u, bd + 2u, idesc, k > 0 ? 1u : 0u);
+          if (2 * k + 1 < 27) {  // the last stage holds offset 26 alone
+            umma_bf16_ts(d0, ta + 16u, bd + bo2, idesc, 1u);
+            umma_bf16_ts(d1, ta + 24u, bd + bo2 + 2u, idesc, 1u);
           }
-          umma_commit(smem_u32(&h.aempty[m_sb]));
+          umma_commit(aempty0 + (uint32_t)(m_sb * 8));
+          bd += bstep;
           if (++m_sb == S) {
             m_sb = 0;
             m_ph ^= 1u;
@@ -2265,19 +2333,23 @@ __global__ void __launch_bounds__(kUnThreads, 1) k_conv_halo(const __grid_consta
     const int cs = a.cout_store, out_bf16 = a.out_bf16;
     for (int i = 0;; ++i) {
       const int r = i & (kInfoRing - 1), b = i & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&h.tinfo_full[r]), (uint32_t)((i / kInfoRing) & 1), status)))
+      if (!__all_sync(0xffffffffu, mbar_wait_lean(smem_u32(&h.tinfo_full[r]), (uint32_t)((i / kInfoRing) & 1), status)))
         break;
       const HaloTile& t = h.tile[r];
       const int nrows = *(volatile const int*)&t.nrows;
       if (nrows < 0) break;
       const int ca = *(volatile const int*)&t.ca;
       const int64_t q = m < ca ? *(volatile const int64_t*)&t.q0a + m : *(volatile const int64_t*)&t.q0b + (m - ca);
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&h.acc_full[b]), (uint32_t)((i >> 1) & 1), status))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait_lean(smem_u32(&h.acc_full[b]), (uint32_t)((i >> 1) & 1), status))) break;
       tc_fence_after();
-      const uint32_t trow = tmem + (uint32_t)b * acc_cols + ((uint32_t)(quarter * 32) << 16);
+      const uint32_t trow = tmem + (uint32_t)(2 * b) * acc_cols + ((uint32_t)(quarter * 32) << 16);
       for (int c = 0; c < cout; c += 16) {
-        uint32_t v[16];
-        tmem_ld16(trow + (uint32_t)c, v);
+        uint32_t v[16], w2[16];
+        tmem_ld16_nowait(trow + (uint32_t)c, v);
+        tmem_ld16_nowait(trow + acc_cols + (uint32_t)c, w2);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) + __uint_as_float(w2[e]));  // the two chains
         const int ncol = min(16, cs - c);  // 16, 8 (cout_store an odd multiple of 8) or none
         if (m >= nrows || ncol <= 0) continue;
         if (out_bf16) {
@@ -2971,15 +3043,13 @@ fvx_status launch_conv_leaf(const char* who, fvx_grid gin, fvx_kmap m, const int
 
 // Halo-staged launch (stride-1 forward map with its leaf table, cin 32, MMA N
 // = cout <= 64): persistent, one block per SM; the weights resident in shared
-// memory beside the window pool, the A ring in the tensor memory the two
-// accumulators leave free.
-fvx_status launch_conv_halo(const char* who, EncodeTiledFn enc, fvx_grid gin, fvx_kmap m, fvx_dtype dt,
-                            const void* feats, int64_t cout, int64_t cout_store, void* out, const __nv_bfloat16* wt,
-                            uint32_t* status, cudaStream_t s) {
+// memory beside the window pool, the A ring in the tensor memory the four
+// accumulators (two tiles x two chains) leave free.
+fvx_status launch_conv_halo(const char* who, fvx_grid gin, fvx_kmap m, fvx_dtype dt, const void* feats, int64_t cout,
+                            int64_t cout_store, void* out, const __nv_bfloat16* wt, uint32_t* status, cudaStream_t s) {
   const fvx_grid_s* go = m->gout;
   HaloArgs a;
-  FVX_TRY(encode_2d(enc, &a.tmx, feats, 32, gin->n_active, 32, 1, CU_TENSOR_MAP_SWIZZLE_64B,
-                    CU_TENSOR_MAP_L2_PROMOTION_NONE, who));
+  a.x = (const __nv_bfloat16*)feats;
   a.wt = wt;
   a.in_rec = gin->leaf_rec;
   a.nbr = m->leaf_nbr;
@@ -2987,16 +3057,15 @@ fvx_status launch_conv_halo(const char* who, EncodeTiledFn enc, fvx_grid gin, fv
   a.y = out;
   a.status = status;
   a.n_leaf_out = go->n_leaf;
-  a.n_in = (int)gin->n_active;
   a.cout = (int)cout;
   a.cout_store = (int)cout_store;
   a.out_bf16 = (dt == FVX_BF16_OUT_BF16) ? 1 : 0;
   int cols = 32;
   while (cols < cout) cols <<= 1;
-  a.acc_cols = cols;                                                 // per accumulator; two accumulators
-  a.stages = std::min((512 - 2 * cols) / 32, kHaloMaxRing);          // A stages: 32 columns each
+  a.acc_cols = cols;                                          // per accumulator: two tiles x two chains
+  a.stages = std::min((512 - 4 * cols) / 32, kHaloMaxRing);   // A stages: 32 columns each
   a.w_bytes = (int)((27 * cout * kHaloRowB + 1023) & ~(int64_t)1023);  // a multiple of 1024 already
-  const size_t smem = 1024 + (size_t)a.w_bytes + (size_t)kHaloPoolUnits * 4 * kHaloRowB + sizeof(HaloHead);
+  const size_t smem = 1024 + (size_t)a.w_bytes + (size_t)kHaloPoolRows * kHaloRowB + sizeof(HaloHead);
   int optin = 0, dev = 0;
   FVX_CUDA(cudaGetDevice(&dev));
   FVX_CUDA(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
@@ -3106,11 +3175,8 @@ fvx_status launch_conv_bf16(const char* who, fvx_grid gin, fvx_kmap m, fvx_dtype
   }
   const bool halo_auto = go->n_leaf > 0 && (double)go->n_active >= kHaloAutoPerLeaf * (double)go->n_leaf;
   if (halo_ok && (algo == FVX_CONV_HALO || (algo == FVX_CONV_AUTO && halo_auto))) {
-    EncodeTiledFn henc = encode_tiled();
-    if (henc) {
-      const fvx_status st = launch_conv_halo(who, henc, gin, m, dt, feats, cout, cout_real, out, wt, status, s);
-      if (st != FVX_ERR_CAPACITY || algo == FVX_CONV_HALO) return st;
-    }
+    const fvx_status st = launch_conv_halo(who, gin, m, dt, feats, cout, cout_real, out, wt, status, s);
+    if (st != FVX_ERR_CAPACITY || algo == FVX_CONV_HALO) return st;
   }
   ConvArgs a;
   a.x = (const __nv_bfloat16*)feats;

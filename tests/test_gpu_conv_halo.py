@@ -80,9 +80,11 @@ def test_halo_matches_oracle_and_direct(cuda_device, case, cout):
     G.assert_conv_close(G.np_(y), yo, ao, G.BF16_TOL)
     yd, kd = _conv_with(fvx.FVX_CONV_DIRECT, g, g, km, x, W)
     assert kd == "conv_bf16_tma"
-    # the same nonzero products in the same order of accumulation (absent
-    # neighbours add exact zeros): equal to the direct kernel
-    assert torch.equal(yd, y)
+    G.assert_conv_close(G.np_(yd), yo, ao, G.BF16_TOL)
+    # the same products; the halo kernel sums input channels 0-15 and 16-31 in
+    # two fp32 chains and adds them, the direct kernel in one: equal up to
+    # fp32 rounding (relative to sum|w*x|)
+    assert np.all(np.abs(G.np_(y) - G.np_(yd)) <= 1e-5 * ao + 1e-30)
     yb, _ = _conv_with(fvx.FVX_CONV_HALO, g, g, km, x, W, out_dtype=torch.bfloat16)
     assert torch.equal(yb, y.bfloat16())
 
