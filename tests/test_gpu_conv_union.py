@@ -125,6 +125,9 @@ def test_union_refusals(cuda_device):
         with pytest.raises(fvx.FvxError) as e:
             _conv_with(fvx.FVX_CONV_UNION, g, g, km, x, W)
         assert e.value.status == "FVX_ERR_INVALID_ARG"
+    x, W = G.bf16_inputs(1, g.n_active, 64, 64)
+    _, kern = _conv_with(fvx.FVX_CONV_AUTO, g, g, km, x, W)
+    assert kern == "conv_bf16_tma"  # the automatic choice never takes the union-staged kernel
     x, W = G.bf16_inputs(1, g.n_active, 32, 64)
     _, kern = _conv_with(fvx.FVX_CONV_AUTO, g, g, km, x, W)
-    assert kern == "conv_bf16_tma"  # the automatic choice stays direct
+    assert kern == "conv_halo"  # 32 channels on leaves this full: the halo-staged kernel
