@@ -2,7 +2,9 @@
 //   * exclusive scan of uint32 in a single pass: each 2048-element tile
 //     publishes its sum, then its inclusive prefix, and every later tile adds
 //     up what its predecessors published (decoupled look-back);
-//   * stable LSD radix sort of (uint64 key, uint32 value) pairs, 8-bit digits:
+//   * stable LSD radix sort of (uint64 key, uint32 value) pairs, digits of up
+//     to 9 bits (the key's bits spread evenly over as few passes as that
+//     allows: 33 bits take four passes, not five of 8 bits):
 //     one kernel counts the digits of every pass in a single read of the keys,
 //     then one kernel per pass ranks each 4096-key tile in shared memory and
 //     takes the tile's output offset for each digit from the digit counts its
@@ -168,16 +170,23 @@ constexpr int kRsWarpItems = kRsTile / kRsWarps;   // 512 consecutive keys per w
 constexpr int kRsRounds = kRsWarpItems / 32;       // 16
 
 constexpr int kRsMaxPasses = 8;                    // 64-bit keys
+constexpr int kRsMaxBins = 512;                    // digits of up to 9 bits
 constexpr int kRsHistTile = 4096;                  // keys per block of the counting kernel
+
+// The passes of one sort: pass p sorts bits [lo[p], lo[p] + nb[p]).
+struct RsPasses {
+  int n;
+  int lo[kRsMaxPasses], nb[kRsMaxPasses];
+};
 
 // Digit counts of every pass in one read of the keys: ghist[p][d] += number of
 // keys whose pass-p digit is d (block counts in shared memory, then one global
-// add per nonzero count).
+// add per nonzero count); pass p's counts start at p * kRsMaxBins.
 __global__ void __launch_bounds__(kRsThreads) k_radix_hist_all(const uint64_t* __restrict__ keys, int64_t n,
-                                                               int bit_lo, int bit_hi, int passes,
-                                                               uint32_t* __restrict__ ghist) {
-  __shared__ uint32_t h[kRsMaxPasses * 256];
-  for (int i = threadIdx.x; i < passes * 256; i += kRsThreads) h[i] = 0u;
+                                                               RsPasses ps, uint32_t* __restrict__ ghist) {
+  __shared__ uint32_t h[kRsMaxPasses * kRsMaxBins];
+  const int passes = ps.n;
+  for (int i = threadIdx.x; i < passes * kRsMaxBins; i += kRsThreads) h[i] = 0u;
   __syncthreads();
   const int64_t b0 = (int64_t)blockIdx.x * kRsHistTile;
 #pragma unroll 4
@@ -185,30 +194,31 @@ __global__ void __launch_bounds__(kRsThreads) k_radix_hist_all(const uint64_t* _
     const int64_t i = b0 + k * kRsThreads + threadIdx.x;
     if (i < n) {
       const uint64_t key = keys[i];
-      for (int p = 0; p < passes; ++p) {
-        const int lo = bit_lo + 8 * p, nb = (bit_hi - lo) < 8 ? (bit_hi - lo) : 8;
-        atomicAdd(&h[p * 256 + ((uint32_t)(key >> lo) & ((1u << nb) - 1u))], 1u);
-      }
+      for (int p = 0; p < passes; ++p)
+        atomicAdd(&h[p * kRsMaxBins + ((uint32_t)(key >> ps.lo[p]) & ((1u << ps.nb[p]) - 1u))], 1u);
     }
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < passes * 256; i += kRsThreads)
+  for (int i = threadIdx.x; i < passes * kRsMaxBins; i += kRsThreads)
     if (h[i]) atomicAdd(&ghist[i], h[i]);
 }
 
+template <int BINS>
 struct RsSmem {
   uint64_t keys[kRsTile];
   uint32_t vals[kRsTile];
-  uint32_t whist[kRsWarps][256];
-  uint32_t dexcl[256];
-  uint32_t goff[256];
+  uint32_t whist[kRsWarps][BINS];
+  uint32_t dexcl[BINS];
+  uint32_t goff[BINS];
   uint32_t tmp[33];
 };
 
 // One pass: tile t (by ticket) ranks its 4096 keys by digit in shared
 // memory, publishes its count of each digit, adds up the counts its
-// predecessors published (thread d follows digit d), publishes the inclusive
-// count and writes each key to digit_start[d] + predecessors' count + rank.
+// predecessors published (thread j follows digits j * DPT .. j * DPT + DPT-1)
+// publishes the inclusive count and writes each key to digit_start[d] +
+// predecessors' count + rank.  BINS = 256 (digits of up to 8 bits) or 512.
+template <int BINS>
 __global__ void __launch_bounds__(kRsThreads, 3) k_radix_onesweep(const uint64_t* __restrict__ kin,
                                                                const uint32_t* __restrict__ vin,
                                                                uint64_t* __restrict__ kout,
@@ -216,14 +226,21 @@ __global__ void __launch_bounds__(kRsThreads, 3) k_radix_onesweep(const uint64_t
                                                                uint32_t dmask, const uint32_t* __restrict__ ghist,
                                                                uint64_t* state, uint32_t* ticket, uint32_t tag,
                                                                uint32_t* status) {
+  constexpr int DPT = BINS / kRsThreads;  // digits per thread in the per-digit steps
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  RsSmem& sm = *reinterpret_cast<RsSmem*>(smem_raw);
+  RsSmem<BINS>& sm = *reinterpret_cast<RsSmem<BINS>*>(smem_raw);
   __shared__ uint32_t s_tile;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) s_tile = atomicAdd(ticket, 1u);
-  for (int d = lane; d < 256; d += 32) sm.whist[warp][d] = 0;
+  for (int d = lane; d < BINS; d += 32) sm.whist[warp][d] = 0;
   // where each digit starts in the output: exclusive scan of the pass's counts
-  const uint32_t gstart = block_exclusive_scan<uint32_t>(ghist[tid], sm.tmp, (uint32_t*)nullptr);
+  uint32_t gcnt[DPT], gsum = 0;
+#pragma unroll
+  for (int j = 0; j < DPT; ++j) {
+    gcnt[j] = ghist[tid * DPT + j];
+    gsum += gcnt[j];
+  }
+  const uint32_t gstart0 = block_exclusive_scan<uint32_t>(gsum, sm.tmp, (uint32_t*)nullptr);
   const int64_t t = s_tile;  // visible after the scan's barriers
 
   const int64_t base = t * kRsTile + (int64_t)warp * kRsWarpItems;
@@ -235,7 +252,7 @@ __global__ void __launch_bounds__(kRsThreads, 3) k_radix_onesweep(const uint64_t
     const int64_t i = base + r * 32 + lane;
     const bool valid = i < n;
     key[r] = valid ? kin[i] : 0ull;
-    const uint32_t d = valid ? ((uint32_t)(key[r] >> shift) & dmask) : (256u + lane);
+    const uint32_t d = valid ? ((uint32_t)(key[r] >> shift) & dmask) : ((uint32_t)BINS + lane);
     const uint32_t peers = __match_any_sync(0xffffffffu, d);
     const uint32_t old = valid ? sm.whist[warp][d] : 0u;
     __syncwarp();
@@ -245,49 +262,70 @@ __global__ void __launch_bounds__(kRsThreads, 3) k_radix_onesweep(const uint64_t
   }
   __syncthreads();
   {  // per digit: exclusive over warps, the tile's count, then the look-back
-    const int d = tid;
-    uint32_t run = 0;
+    uint32_t run[DPT], prefix[DPT], rsum = 0;
 #pragma unroll
-    for (int w = 0; w < kRsWarps; ++w) {
-      uint32_t c = sm.whist[w][d];
-      sm.whist[w][d] = run;
-      run += c;
+    for (int j = 0; j < DPT; ++j) {
+      const int d = tid * DPT + j;
+      uint32_t acc = 0;
+#pragma unroll
+      for (int w = 0; w < kRsWarps; ++w) {
+        uint32_t c = sm.whist[w][d];
+        sm.whist[w][d] = acc;
+        acc += c;
+      }
+      run[j] = acc;
+      rsum += acc;
+      prefix[j] = 0;
     }
     const uint64_t tagbits = (uint64_t)tag << 40;
-    uint64_t* mine = state + t * 256 + d;
-    st_relaxed_u64(mine, tagbits | (t == 0 ? kLbInc : kLbAgg) | run);
-    uint32_t prefix = 0;
+#pragma unroll
+    for (int j = 0; j < DPT; ++j)
+      st_relaxed_u64(state + t * BINS + tid * DPT + j, tagbits | (t == 0 ? kLbInc : kLbAgg) | run[j]);
     if (t > 0) {
       // kLbWindow predecessors per round trip, nearest first; the walk stops
       // at the first inclusive word and resumes at the first unpublished one
       const unsigned long long t0 = lb_clock();
-      int64_t j = t - 1;
-      bool done = false;
-      for (uint32_t it = 1; !done; ++it) {
-        uint64_t f[kLbWindow];
 #pragma unroll
-        for (int q = 0; q < kLbWindow; ++q)
-          f[q] = (j - q >= 0) ? ld_relaxed_u64(state + (j - q) * 256 + d) : (tagbits | kLbInc);  // before tile 0
-        int q = 0;
+      for (int jd = 0; jd < DPT; ++jd) {
+        const int d = tid * DPT + jd;
+        int64_t j = t - 1;
+        bool done = false;
+        for (uint32_t it = 1; !done; ++it) {
+          uint64_t f[kLbWindow];
 #pragma unroll
-        for (int r = 0; r < kLbWindow; ++r) {
-          if (q != r || done) continue;
-          const bool ready = (uint32_t)(f[r] >> 40) == tag && ((f[r] >> 32) & 3u) != 0u;
-          if (!ready) continue;
-          prefix += (uint32_t)f[r];
-          done = ((f[r] >> 32) & 3u) == 2u;
-          q = r + 1;
+          for (int q = 0; q < kLbWindow; ++q)
+            f[q] = (j - q >= 0) ? ld_relaxed_u64(state + (j - q) * BINS + d) : (tagbits | kLbInc);  // before tile 0
+          int q = 0;
+#pragma unroll
+          for (int r = 0; r < kLbWindow; ++r) {
+            if (q != r || done) continue;
+            const bool ready = (uint32_t)(f[r] >> 40) == tag && ((f[r] >> 32) & 3u) != 0u;
+            if (!ready) continue;
+            prefix[jd] += (uint32_t)f[r];
+            done = ((f[r] >> 32) & 3u) == 2u;
+            q = r + 1;
+          }
+          j -= q;
+          if (!done && q < kLbWindow && (it & 63u) == 0u && lb_expired(t0, kLbWaitNs)) {
+            report_device_error(status, DEV_TIMEOUT);
+            break;
+          }
         }
-        j -= q;
-        if (!done && q < kLbWindow && (it & 63u) == 0u && lb_expired(t0, kLbWaitNs)) {
-          report_device_error(status, DEV_TIMEOUT);
-          break;
-        }
+        st_relaxed_u64(state + t * BINS + d, tagbits | kLbInc | (uint32_t)(prefix[jd] + run[jd]));
       }
-      st_relaxed_u64(mine, tagbits | kLbInc | (uint32_t)(prefix + run));
     }
-    sm.goff[d] = gstart + prefix;
-    sm.dexcl[d] = block_exclusive_scan<uint32_t>(run, sm.tmp, (uint32_t*)nullptr);
+    uint32_t gs = gstart0;
+#pragma unroll
+    for (int j = 0; j < DPT; ++j) {
+      sm.goff[tid * DPT + j] = gs + prefix[j];
+      gs += gcnt[j];
+    }
+    uint32_t de = block_exclusive_scan<uint32_t>(rsum, sm.tmp, (uint32_t*)nullptr);
+#pragma unroll
+    for (int j = 0; j < DPT; ++j) {
+      sm.dexcl[tid * DPT + j] = de;
+      de += run[j];
+    }
   }
   __syncthreads();
 #pragma unroll
@@ -321,25 +359,40 @@ fvx_status radix_sort_pairs(uint64_t* k0, uint32_t* v0, uint64_t* k1, uint32_t* 
     set_error("radix sort: device status word unavailable");
     return FVX_ERR_CUDA;
   }
-  FVX_CUDA(cudaFuncSetAttribute(k_radix_onesweep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(RsSmem)));
-  // three blocks per SM: shared memory for three tiles, registers for three (launch bounds)
-  FVX_CUDA(cudaFuncSetAttribute(k_radix_onesweep, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                (int)cudaSharedmemCarveoutMaxShared));
-  const int passes = (bit_hi - bit_lo + 7) / 8;
+  for (auto kern : {k_radix_onesweep<256>, k_radix_onesweep<512>}) {
+    const int bytes = kern == k_radix_onesweep<256> ? (int)sizeof(RsSmem<256>) : (int)sizeof(RsSmem<512>);
+    FVX_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
+    // three blocks per SM: shared memory for three tiles, registers for three (launch bounds)
+    FVX_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  (int)cudaSharedmemCarveoutMaxShared));
+  }
+  // as few passes as digits of up to 9 bits allow, 8-bit digits when that
+  // takes no more passes; the bits spread evenly (first passes one wider)
+  const int bits = bit_hi - bit_lo;
+  int passes = (bits + 7) / 8;
+  if ((bits + 8) / 9 < passes) passes = (bits + 8) / 9;
+  RsPasses ps;
+  ps.n = passes;
+  for (int p = 0, lo = bit_lo; p < passes; ++p) {
+    ps.nb[p] = bits / passes + (p < bits % passes ? 1 : 0);
+    ps.lo[p] = lo;
+    lo += ps.nb[p];
+  }
   const int64_t ntiles = (n + kRsTile - 1) / kRsTile;
-  // one zeroed region: digit counts [passes][256], tickets [8], then the
-  // published words [ntiles][256] shared by all passes (told apart by tag)
-  const size_t words32 = (size_t)passes * 256 + kRsMaxPasses;
-  uint64_t* region = scr.get<uint64_t>(words32 / 2 + (size_t)ntiles * 256);
+  // one zeroed region: digit counts [passes][kRsMaxBins], tickets [8], then
+  // the published words [ntiles][kRsMaxBins] shared by all passes (told apart
+  // by tag)
+  const size_t words32 = (size_t)passes * kRsMaxBins + kRsMaxPasses;
+  uint64_t* region = scr.get<uint64_t>(words32 / 2 + (size_t)ntiles * kRsMaxBins);
   if (!region) return FVX_ERR_ALLOC;
   uint32_t* ghist = reinterpret_cast<uint32_t*>(region);
-  uint32_t* tickets = ghist + (size_t)passes * 256;
+  uint32_t* tickets = ghist + (size_t)passes * kRsMaxBins;
   uint64_t* state = region + words32 / 2;
-  FVX_CUDA(cudaMemsetAsync(region, 0, 8 * (words32 / 2 + (size_t)ntiles * 256), s));
+  FVX_CUDA(cudaMemsetAsync(region, 0, 8 * (words32 / 2 + (size_t)ntiles * kRsMaxBins), s));
   {
     LaunchScope ls("radix_hist_all", s);
     const int64_t nb = (n + kRsHistTile - 1) / kRsHistTile;
-    k_radix_hist_all<<<(unsigned)nb, kRsThreads, 0, s>>>(k0, n, bit_lo, bit_hi, passes, ghist);
+    k_radix_hist_all<<<(unsigned)nb, kRsThreads, 0, s>>>(k0, n, ps, ghist);
   }
   FVX_TRY(check_launch("radix_hist_all"));
   uint64_t* ks = k0;
@@ -348,13 +401,17 @@ fvx_status radix_sort_pairs(uint64_t* k0, uint32_t* v0, uint64_t* k1, uint32_t* 
   uint32_t* vd = v1;
   bool in1 = false;
   for (int p = 0; p < passes; ++p) {
-    const int lo = bit_lo + 8 * p;
-    const int nb = (bit_hi - lo) < 8 ? (bit_hi - lo) : 8;
-    const uint32_t dmask = (1u << nb) - 1u;
+    const uint32_t dmask = (1u << ps.nb[p]) - 1u;
     {
       LaunchScope ls("radix_onesweep", s);
-      k_radix_onesweep<<<(unsigned)ntiles, kRsThreads, sizeof(RsSmem), s>>>(
-          ks, vs, kd, vd, n, lo, dmask, ghist + (size_t)p * 256, state, tickets + p, (uint32_t)(p + 1), status);
+      if (ps.nb[p] > 8)
+        k_radix_onesweep<512><<<(unsigned)ntiles, kRsThreads, sizeof(RsSmem<512>), s>>>(
+            ks, vs, kd, vd, n, ps.lo[p], dmask, ghist + (size_t)p * kRsMaxBins, state, tickets + p,
+            (uint32_t)(p + 1), status);
+      else
+        k_radix_onesweep<256><<<(unsigned)ntiles, kRsThreads, sizeof(RsSmem<256>), s>>>(
+            ks, vs, kd, vd, n, ps.lo[p], dmask, ghist + (size_t)p * kRsMaxBins, state, tickets + p,
+            (uint32_t)(p + 1), status);
     }
     FVX_TRY(check_launch("radix_onesweep"));
     uint64_t* tk = ks; ks = kd; kd = tk;
