@@ -297,12 +297,19 @@ __global__ void __launch_bounds__(kKmThreads) k_kmap1_count(GridDev gin, const i
 }
 
 // Input index of every position of the output leaf's one-voxel halo
-// (10^3 positions, -1 where no input voxel is active), from the 27 slots.
+// (10^3 positions, -1 where no input voxel is active), from the 27 slots, and
+// where each (offset, slice) run of the leaf's pairs starts in its list.
 struct Km1WriteSmem {
   Km1Smem k;
-  int32_t hidx[1000];  // (hx+1)*100 + (hy+1)*10 + (hz+1), h in -1..8
+  int32_t hidx[1000];   // (hx+1)*100 + (hy+1)*10 + (hz+1), h in -1..8
+  uint32_t pos0[27][8]; // list position of the first pair of (offset s, slice x)
 };
 
+// One thread per active output voxel (index order), looping over the 27
+// offsets in step: a voxel with a neighbour at offset s writes its pair at
+// its rank among the leaf's voxels with that neighbour, so the lanes of a
+// warp write consecutive entries of one list at a time.  Work scales with the
+// leaf's active voxels, not with its 512 positions.
 __global__ void __launch_bounds__(kKmThreads) k_kmap1_write(GridDev gin, const int32_t* __restrict__ out_origin,
                                                             const int32_t* __restrict__ out_batch,
                                                             const uint64_t* __restrict__ out_rec, int64_t n_out_leaf,
@@ -326,34 +333,50 @@ __global__ void __launch_bounds__(kKmThreads) k_kmap1_write(GridDev gin, const i
     }
     sw.hidx[h] = v;
   }
-  __syncthreads();
-  // the neighbour words of every (offset, slice), as the count pass had them
-  if (tid < 27 * 8) sm.R[tid >> 3][tid & 7] = km1_word(sm, tid >> 3, tid & 7);
-  __syncthreads();
-  // one warp per offset: the pairs of slice x are the set bits of R[s][x], in
-  // output order; a lane's bits b = lane and lane + 32 go to their rank in R
-  // (coalesced runs, no ballots)
-  const int warp = tid >> 5, lane = tid & 31;
-  for (int s = warp; s < 27; s += kKmThreads / 32) {
-    const int di = s / 9 - 1, dj = (s / 3) % 3 - 1, dk = s % 3 - 1;
-    uint32_t e = starts[(int64_t)(mirror ? 26 - s : s) * n_out_leaf + lo];
-    for (int x = 0; x < 8; ++x) {
-      const unsigned long long R = sm.R[s][x];
-      if (!R) continue;
-      const unsigned long long om = sm.om[x];
-      const uint32_t qx = sm.qf + (x ? (uint32_t)((sm.opre9 >> (9 * (x - 1))) & 511ull) : 0u);
-      const int hrow = (x + di + 1) * 100 + (dj + 1) * 10 + (dk + 1);
+  {
+    // the neighbour words of every (offset, slice), as the count pass had
+    // them; thread s * 8 + x, so the eight slices of an offset are eight
+    // consecutive lanes and their running pair counts one segmented scan
+    const int s = tid >> 3, x = tid & 7;
+    const unsigned long long R = (s < 27) ? km1_word(sm, s, x) : 0ull;
+    const uint32_t c = (uint32_t)__popcll(R);
+    uint32_t incl = c;
 #pragma unroll
-      for (int hw = 0; hw < 2; ++hw) {
-        const int b = hw * 32 + lane;  // y * 8 + z
-        if ((R >> b) & 1ull) {
-          const unsigned long long below = (1ull << b) - 1ull;
-          const uint32_t pos = e + (uint32_t)__popcll(R & below);
-          in_idx[pos] = sw.hidx[hrow + (b >> 3) * 10 + (b & 7)];
-          out_idx[pos] = (int32_t)(qx + (uint32_t)__popcll(om & below));
-        }
+    for (int d = 1; d < 8; d <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xffffffffu, incl, d, 8);
+      if (x >= d) incl += v;
+    }
+    if (s < 27) {
+      sm.R[s][x] = R;
+      sw.pos0[s][x] = starts[(int64_t)(mirror ? 26 - s : s) * n_out_leaf + lo] + incl - c;
+    }
+  }
+  // active output voxels in index order
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int n = tid + h * 256;
+    const int w = n >> 6, bit = n & 63;
+    const unsigned long long m = sm.om[w];
+    if ((m >> bit) & 1ull) {
+      const uint32_t pre = w ? (uint32_t)((sm.opre9 >> (9 * (w - 1))) & 511ull) : 0u;
+      sm.vox[pre + (uint32_t)__popcll(m & ((1ull << bit) - 1ull))] = (uint16_t)n;
+    }
+  }
+  const int nvox = (int)(((sm.opre9 >> 54) & 511ull) + (unsigned long long)__popcll(sm.om[7]));
+  __syncthreads();
+  for (int idx = tid; idx < nvox; idx += kKmThreads) {
+    const int n = sm.vox[idx], x = n >> 6, b = n & 63;
+    const unsigned long long below = (1ull << b) - 1ull;
+    const int h0 = (x + 1) * 100 + ((b >> 3) + 1) * 10 + (b & 7) + 1;  // the voxel's own halo position
+    const int32_t q = (int32_t)(sm.qf + (uint32_t)idx);
+#pragma unroll
+    for (int s = 0; s < 27; ++s) {
+      const unsigned long long R = sm.R[s][x];
+      if ((R >> b) & 1ull) {
+        const uint32_t pos = sw.pos0[s][x] + (uint32_t)__popcll(R & below);
+        in_idx[pos] = sw.hidx[h0 + (s / 9 - 1) * 100 + ((s / 3) % 3 - 1) * 10 + (s % 3 - 1)];
+        out_idx[pos] = q;
       }
-      e += (uint32_t)__popcll(R);
     }
   }
 }
