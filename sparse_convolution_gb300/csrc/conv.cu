@@ -1830,8 +1830,8 @@ __global__ void __launch_bounds__(kLeafThreads, G8 == 1 ? 2 : 1) k_conv_leaf(con
 // Submanifold (stride 1) convolution of 32-channel inputs over the ACTIVE
 // outputs of each output leaf.  The input window of a leaf (its 8^3 voxels and
 // a one-voxel shell: 10^3 positions) is fetched once into a shared-memory pool,
-// only at the positions that hold an input voxel (TMA gather4, four pool rows
-// per operation); the weights stay resident in shared memory.  An M tile is
+// only at the positions that hold an input voxel (cp.async, one window column
+// per loader thread); the weights stay resident in shared memory.  An M tile is
 // 128 active outputs of one leaf, or the tail of one leaf and the head of the
 // block's next leaf; K runs over the 27 offsets, two per stage: offset s =
 // (dx+1)*9 + (dy+1)*3 + dz+1 takes, for the output at window position w, the
@@ -1849,11 +1849,11 @@ __global__ void __launch_bounds__(kLeafThreads, G8 == 1 ? 2 : 1) k_conv_leaf(con
 //   warps 4-11  operand rows: warps 4-7 the first offset of each stage, warps
 //               8-11 the second, thread = tile row (its warp's TMEM lane
 //               quarter); they also pack the tiles and publish them.
-//   warp 12     MMA issue and TMEM owner: per tile two accumulator chains
-//               (input channels 0-15 and 16-31 of every offset, issued
-//               alternately so that consecutive MMAs are independent: a chain
-//               of dependent N <= 64 MMAs runs at the MMA latency, not its
-//               throughput), two tiles in flight, and the A ring.
+//   warp 12     MMA issue and TMEM owner: per tile two accumulators (input
+//               channels 0-15 and 16-31 of every offset), two tiles in
+//               flight, and a 7-slot A ring; a tile's 14 stages are unrolled
+//               so the issuing thread keeps up with 128 x 64 x 16 MMAs
+//               (about 49 cycles each on this GPU).
 //   warps 13-16 epilogue: the two chains added, row m of a tile to its
 //               output row.
 constexpr int kHaloPos = 1000;                       // window positions
@@ -1863,7 +1863,8 @@ constexpr int kHaloWins = 4;                         // window descriptors
 constexpr int kHaloJoinMax = kHaloPoolRows - kHaloPos;  // a window this small leaves room for any next one
 constexpr int kHaloTileStages = 14;                  // 27 offsets, two per stage
 static_assert(kHaloTileStages % 2 == 0, "the operand rows produce stages in pairs");
-constexpr int kHaloMaxRing = 16;                     // A stages in tensor memory at most
+constexpr int kHaloRing = 7;                         // A stages in tensor memory: a tile is two laps
+static_assert(kHaloTileStages == 2 * kHaloRing, "each stage of a tile has a fixed ring slot and parity");
 constexpr int kHaloMaxCout = 64;
 constexpr int kHaloRowWarp0 = 4;                    // first operand-row warp                     // resident weights: 27 x 64 x 64 B
 constexpr double kHaloAutoPerLeaf = 48.0;            // mean active outputs per leaf for the automatic choice
@@ -1889,7 +1890,7 @@ struct HaloHead {
   LeafNbr nb[2][27];       // neighbour records of the loader's current and next leaf
   int32_t scan[4];
   HaloTile tile[kInfoRing];
-  unsigned long long afull[kHaloMaxRing], aempty[kHaloMaxRing];  // A stages: rows <-> MMA
+  unsigned long long afull[kHaloRing], aempty[kHaloRing];  // A stages: rows <-> MMA
   unsigned long long wfull[kHaloWins], wempty[kHaloWins];        // windows: loader <-> rows
   unsigned long long tinfo_full[kInfoRing], tinfo_empty[kInfoRing];
   unsigned long long acc_full[2], acc_empty[2];
@@ -2284,14 +2285,12 @@ __global__ void __launch_bounds__(kUnThreads, 1) k_conv_halo(const __grid_consta
     // ---------------- MMA issue (one thread): A from tensor memory, B resident
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16(kRows, cout);
-      // B of stage k, MMA kk (offset 2k + kk / 2, channels 16 (kk & 1) ..):
-      // the descriptor of offset 0 advanced in 16-byte units
+      // B of stage k: offsets 2k and 2k + 1, each two MMAs (channels 0-15,
+      // 16-31): the descriptor of offset 0 advanced in 16-byte units
       const uint64_t bdesc0 = sdesc_swz(smem_u32(wsm), 4u, 8u * kHaloRowB);
-      const uint32_t bo2 = (uint32_t)(cout * kHaloRowB) >> 4, bstep = 2u * bo2;
+      const uint32_t bo2 = (uint32_t)(cout * kHaloRowB) >> 4;
       const uint32_t abase = tmem + 4u * acc_cols;
       const uint32_t afull0 = smem_u32(&h.afull[0]), aempty0 = smem_u32(&h.aempty[0]);
-      int m_sb = 0;
-      uint32_t m_ph = 0;
       int i = 0;
       for (;; ++i) {
         const int r = i & (kInfoRing - 1), b = i & 1;
@@ -2299,26 +2298,30 @@ __global__ void __launch_bounds__(kUnThreads, 1) k_conv_halo(const __grid_consta
         if (*(volatile const int*)&h.tile[r].nrows < 0) break;
         if (i >= 2 && !mbar_wait_lean(smem_u32(&h.acc_empty[b]), (uint32_t)(((i >> 1) - 1) & 1), status)) break;
         tc_fence_after();
-        // two accumulator chains, channels 0-15 and 16-31 of every offset,
-        // issued alternately: consecutive MMAs do not wait for each other
+        // two accumulators (channels 0-15 and 16-31 of every offset), added
+        // in the epilogue.  A tile is two laps of the 7-slot ring, each lap
+        // unrolled, so the ring slots are constants and the single issuing
+        // thread spends a few instructions per MMA (an issue loop with
+        // run-time ring bookkeeping costs more cycles per MMA than a
+        // 128 x 64 x 16 MMA takes to execute).
         const uint32_t d0 = tmem + (uint32_t)(2 * b) * acc_cols, d1 = d0 + acc_cols;
         uint64_t bd = bdesc0;
 #pragma unroll 1
-        for (int k = 0; k < kHaloTileStages; ++k) {
-          mbar_wait_lean(afull0 + (uint32_t)(m_sb * 8), m_ph, status);
-          tc_fence_after();
-          const uint32_t ta = abase + (uint32_t)(m_sb * 32);
-          umma_bf16_ts(d0, ta, bd, idesc, k > 0 ? 1u : 0u);
-          umma_bf16_ts(d1, ta + 8u, bd + 2u, idesc, k > 0 ? 1u : 0u);
-          if (2 * k + 1 < 27) {  // the last stage holds offset 26 alone
-            umma_bf16_ts(d0, ta + 16u, bd + bo2, idesc, 1u);
-            umma_bf16_ts(d1, ta + 24u, bd + bo2 + 2u, idesc, 1u);
-          }
-          umma_commit(aempty0 + (uint32_t)(m_sb * 8));
-          bd += bstep;
-          if (++m_sb == S) {
-            m_sb = 0;
-            m_ph ^= 1u;
+        for (int lap = 0; lap < 2; ++lap) {
+#pragma unroll
+          for (int j = 0; j < kHaloRing; ++j) {
+            mbar_wait_lean(afull0 + (uint32_t)(j * 8), (uint32_t)lap, status);
+            tc_fence_after();
+            const uint32_t ta = abase + (uint32_t)(j * 32);
+            const uint32_t acc = (j > 0 || lap > 0) ? 1u : 0u;
+            umma_bf16_ts(d0, ta, bd, idesc, acc);
+            umma_bf16_ts(d1, ta + 8u, bd + 2u, idesc, acc);
+            if (j < kHaloRing - 1 || lap == 0) {  // the last stage holds offset 26 alone
+              umma_bf16_ts(d0, ta + 16u, bd + bo2, idesc, 1u);
+              umma_bf16_ts(d1, ta + 24u, bd + bo2 + 2u, idesc, 1u);
+            }
+            umma_commit(aempty0 + (uint32_t)(j * 8));
+            bd += 2u * bo2;
           }
         }
         umma_commit(smem_u32(&h.acc_full[b]));
@@ -3063,7 +3066,7 @@ fvx_status launch_conv_halo(const char* who, fvx_grid gin, fvx_kmap m, fvx_dtype
   int cols = 32;
   while (cols < cout) cols <<= 1;
   a.acc_cols = cols;                                          // per accumulator: two tiles x two chains
-  a.stages = std::min((512 - 4 * cols) / 32, kHaloMaxRing);   // A stages: 32 columns each
+  a.stages = kHaloRing;  // A stages of 32 columns: 224 beside the four accumulators
   a.w_bytes = (int)((27 * cout * kHaloRowB + 1023) & ~(int64_t)1023);  // a multiple of 1024 already
   const size_t smem = 1024 + (size_t)a.w_bytes + (size_t)kHaloPoolRows * kHaloRowB + sizeof(HaloHead);
   int optin = 0, dev = 0;
