@@ -227,7 +227,7 @@ __device__ __forceinline__ unsigned long long km1_word(const Km1Smem& sm, int s,
 }
 
 // Loads the output leaf and its 27 input-leaf slots (tree walks, or the slot
-// table written by the count pass).
+// table written by k_kmap1_nbr).
 __device__ __forceinline__ void km1_load(Km1Smem& sm, const GridDev& gin, const int32_t* __restrict__ out_origin,
                                          const int32_t* __restrict__ out_batch,
                                          const uint64_t* __restrict__ out_rec, int lo,
@@ -257,15 +257,30 @@ __device__ __forceinline__ void km1_load(Km1Smem& sm, const GridDev& gin, const 
   __syncthreads();
 }
 
+// The 27 input leaves around every output leaf (slot (a,b,c): the leaf at
+// origin - 8 + 8 * (a,b,c)), one tree walk per thread: the walks' dependent
+// loads overlap across many threads instead of 27 per block.
+__global__ void __launch_bounds__(256) k_kmap1_nbr(GridDev gin, const int32_t* __restrict__ out_origin,
+                                                   const int32_t* __restrict__ out_batch, int64_t n_out_leaf,
+                                                   int32_t* __restrict__ nbr) {
+  const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= 27 * n_out_leaf) return;
+  const int64_t lo = e / 27;
+  const int t = (int)(e - lo * 27);
+  const int a = t / 9, b = (t / 3) % 3, c = t % 3;
+  nbr[e] = find_leaf_wide(gin, out_batch[lo], (long long)out_origin[3 * lo] - 8 + 8 * a,
+                          (long long)out_origin[3 * lo + 1] - 8 + 8 * b, (long long)out_origin[3 * lo + 2] - 8 + 8 * c);
+}
+
 __global__ void __launch_bounds__(kKmThreads) k_kmap1_count(GridDev gin, const int32_t* __restrict__ out_origin,
                                                             const int32_t* __restrict__ out_batch,
                                                             const uint64_t* __restrict__ out_rec, int64_t n_out_leaf,
                                                             uint32_t* __restrict__ counts,
                                                             uint32_t* __restrict__ out_mask,
-                                                            int32_t* __restrict__ nbr_out, int mirror) {
+                                                            const int32_t* __restrict__ nbr_in, int mirror) {
   __shared__ Km1Smem sm;
   const int lo = blockIdx.x, tid = threadIdx.x;
-  km1_load(sm, gin, out_origin, out_batch, out_rec, lo, nullptr, nbr_out);
+  km1_load(sm, gin, out_origin, out_batch, out_rec, lo, nbr_in, nullptr);
   const int s = tid >> 3, x = tid & 7;
   const unsigned long long R = (s < 27) ? km1_word(sm, s, x) : 0ull;
   if (s < 27) sm.R[s][x] = R;
@@ -484,7 +499,7 @@ fvx_status kernel_map_impl(const char* who, fvx_grid gin, fvx_grid gout, int32_t
   uint32_t* counts = scr.get<uint32_t>((size_t)(27 * Lo + 1));
   if (!counts) return FVX_ERR_ALLOC;
   // mask, list totals and conv tiling live in the first block, pairs in the
-  // second (and, for stride 1, the input-leaf slot table the count pass
+  // second (and, for stride 1, the input-leaf slot table k_kmap1_nbr
   // writes, which the leaf-densified convolution reads too)
   const size_t o_mask = 0, o_tot = align_up(4 * (size_t)Nout), o_tile = o_tot + align_up(4 * 32);
   const size_t o_nbr = o_tile + align_up(4 * (size_t)(27 * m->n_tiles + 1));
@@ -513,11 +528,16 @@ fvx_status kernel_map_impl(const char* who, fvx_grid gin, fvx_grid gout, int32_t
   }
 
   const GridDev gd = grid_dev(gin);
-  int32_t* nbr = nullptr;  // stride 1: input-leaf slot table written by the count pass
+  int32_t* nbr = nullptr;  // stride 1: input-leaf slot table (k_kmap1_nbr)
   if (bitpar) {
     nbr = (int32_t*)((char*)m->block + o_nbr);
     (transposed ? m->leaf_nbr_t : m->leaf_nbr) = nbr;  // the forward conv's leaf path takes forward maps only
   }
+  if (Lo > 0 && bitpar) {
+    LaunchScope ls("kmap_nbr", s);
+    k_kmap1_nbr<<<(unsigned)((27 * Lo + 255) / 256), 256, 0, s>>>(gd, gout->leaf_origin, gout->leaf_batch, Lo, nbr);
+  }
+  FVX_TRY(check_launch("kmap_nbr"));
   if (Lo > 0) {
     LaunchScope ls("kmap_count", s);
     if (bitpar)
