@@ -1848,14 +1848,13 @@ __global__ void __launch_bounds__(kLeafThreads, G8 == 1 ? 2 : 1) k_conv_leaf(con
 //               kHaloWins windows resident, pool rows allocated in order.
 //   warps 4-11  operand rows: warps 4-7 the first offset of each stage, warps
 //               8-11 the second, thread = tile row (its warp's TMEM lane
-//               quarter); they also pack the tiles and publish them.
-//   warp 12     MMA issue and TMEM owner: per tile two accumulators (input
-//               channels 0-15 and 16-31 of every offset), two tiles in
-//               flight, and a 7-slot A ring; a tile's 14 stages are unrolled
-//               so the issuing thread keeps up with 128 x 64 x 16 MMAs
-//               (about 49 cycles each on this GPU).
-//   warps 13-16 epilogue: the two chains added, row m of a tile to its
-//               output row.
+//               quarter); two stages (four offsets) per ring slot; they also
+//               pack the tiles and publish them.
+//   warp 12     MMA issue and TMEM owner: one accumulator per tile, two
+//               tiles in flight, the rest of tensor memory a ring of A slots
+//               (six at cout 64); one commit per slot (a commit costs the
+//               tensor pipe about as much as an MMA of this size).
+//   warps 13-16 epilogue: row m of a tile to its output row.
 constexpr int kHaloPos = 1000;                       // window positions
 constexpr int kHaloRowB = 64;                        // pool row: 32 bf16 channels
 constexpr int kHaloPoolRows = 1536;                  // pool rows (96 KB)
@@ -1863,8 +1862,7 @@ constexpr int kHaloWins = 4;                         // window descriptors
 constexpr int kHaloJoinMax = kHaloPoolRows - kHaloPos;  // a window this small leaves room for any next one
 constexpr int kHaloTileStages = 14;                  // 27 offsets, two per stage
 static_assert(kHaloTileStages % 2 == 0, "the operand rows produce stages in pairs");
-constexpr int kHaloRing = 7;                         // A stages in tensor memory: a tile is two laps
-static_assert(kHaloTileStages == 2 * kHaloRing, "each stage of a tile has a fixed ring slot and parity");
+constexpr int kHaloMaxPairs = 7;                     // A ring slots in tensor memory (two stages, 64 columns each)
 constexpr int kHaloMaxCout = 64;
 constexpr int kHaloRowWarp0 = 4;                    // first operand-row warp                     // resident weights: 27 x 64 x 64 B
 constexpr double kHaloAutoPerLeaf = 48.0;            // mean active outputs per leaf for the automatic choice
@@ -1890,7 +1888,7 @@ struct HaloHead {
   LeafNbr nb[2][27];       // neighbour records of the loader's current and next leaf
   int32_t scan[4];
   HaloTile tile[kInfoRing];
-  unsigned long long afull[kHaloRing], aempty[kHaloRing];  // A stages: rows <-> MMA
+  unsigned long long afull[kHaloMaxPairs], aempty[kHaloMaxPairs];  // A slots (stage pairs): rows <-> MMA
   unsigned long long wfull[kHaloWins], wempty[kHaloWins];        // windows: loader <-> rows
   unsigned long long tinfo_full[kInfoRing], tinfo_empty[kInfoRing];
   unsigned long long acc_full[2], acc_empty[2];
@@ -2086,10 +2084,10 @@ __device__ int64_t halo_rows(HaloHead& h, const HaloArgs& a, const unsigned char
   const int S = a.stages;
   const int lane = ct & 31, cw = ct >> 5, grp = cw >> 2, quarter = (kHaloRowWarp0 + cw) & 3;
   const int m = quarter * 32 + lane;
-  const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(4 * a.acc_cols) + (uint32_t)(16 * grp);
+  const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(2 * a.acc_cols) + (uint32_t)(16 * grp);
   uint32_t* const status = a.status;
-  int64_t kg = 0;
-  int ring_sb = 0;
+  int64_t pg = 0;  // stage pairs produced
+  int ring_ps = 0;
   uint32_t ring_ph = 0;
   int nt = 0;          // tiles published
   int64_t loaded = 0;  // windows seen landed
@@ -2152,7 +2150,7 @@ __device__ int64_t halo_rows(HaloHead& h, const HaloArgs& a, const unsigned char
     };
     int un0 = lookup(0, 0), un1 = lookup(0, 1);
 #pragma unroll 1
-    for (int k = 0; k < kHaloTileStages; k += 2, kg += 2) {
+    for (int k = 0; k < kHaloTileStages; k += 2, ++pg) {
       const int uc[2] = {un0, un1};
       if (k + 2 < kHaloTileStages) {
         un0 = lookup(k + 2, 0);
@@ -2176,26 +2174,19 @@ __device__ int64_t halo_rows(HaloHead& h, const HaloArgs& a, const unsigned char
           for (int e = 0; e < 16; ++e) v[t][e] = 0u;
         }
       }
-      int sb[2];
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        sb[t] = ring_sb;
-        if (kg + t >= S) mbar_wait_lean(smem_u32(&h.aempty[ring_sb]), ring_ph ^ 1u, status);
-        if (++ring_sb == S) {
-          ring_sb = 0;
-          ring_ph ^= 1u;
-        }
+      const int ps = ring_ps;
+      if (pg >= S) mbar_wait_lean(smem_u32(&h.aempty[ps]), ring_ph ^ 1u, status);
+      if (++ring_ps == S) {
+        ring_ps = 0;
+        ring_ph ^= 1u;
       }
-      tc_fence_after();  // the MMAs that read these stages have completed
-      tmem_st16(tl + (uint32_t)(sb[0] * 32), v[0]);
-      if (2 * (k + 1) + grp < 27) tmem_st16(tl + (uint32_t)(sb[1] * 32), v[1]);  // warp-uniform: offset 26 is the last
+      tc_fence_after();  // the MMAs that read this slot have completed
+      tmem_st16(tl + (uint32_t)(ps * 64), v[0]);
+      if (2 * (k + 1) + grp < 27) tmem_st16(tl + (uint32_t)(ps * 64 + 32), v[1]);  // warp-uniform: offset 26 is the last
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(smem_u32(&h.afull[sb[0]]));
-        mbar_arrive(smem_u32(&h.afull[sb[1]]));
-      }
+      if (lane == 0) mbar_arrive(smem_u32(&h.afull[ps]));
     }
     // windows done with
     r += ca;
@@ -2219,7 +2210,7 @@ __device__ int64_t halo_rows(HaloHead& h, const HaloArgs& a, const unsigned char
     h.tile[ri].nrows = -1;
     mbar_arrive(smem_u32(&h.tinfo_full[ri]));
   }
-  return kg;
+  return pg;
 }
 
 __global__ void __launch_bounds__(kUnThreads, 1) k_conv_halo(const __grid_constant__ HaloArgs a) {
@@ -2285,12 +2276,14 @@ __global__ void __launch_bounds__(kUnThreads, 1) k_conv_halo(const __grid_consta
     // ---------------- MMA issue (one thread): A from tensor memory, B resident
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16(kRows, cout);
-      // B of stage k: offsets 2k and 2k + 1, each two MMAs (channels 0-15,
-      // 16-31): the descriptor of offset 0 advanced in 16-byte units
+      // B of offset s: the descriptor of offset 0 advanced by s * cout rows
+      // (16-byte units); channels 16-31 two units further
       const uint64_t bdesc0 = sdesc_swz(smem_u32(wsm), 4u, 8u * kHaloRowB);
       const uint32_t bo2 = (uint32_t)(cout * kHaloRowB) >> 4;
-      const uint32_t abase = tmem + 4u * acc_cols;
+      const uint32_t abase = tmem + 2u * acc_cols;
       const uint32_t afull0 = smem_u32(&h.afull[0]), aempty0 = smem_u32(&h.aempty[0]);
+      int m_ps = 0;
+      uint32_t m_ph = 0;
       int i = 0;
       for (;; ++i) {
         const int r = i & (kInfoRing - 1), b = i & 1;
@@ -2298,30 +2291,28 @@ __global__ void __launch_bounds__(kUnThreads, 1) k_conv_halo(const __grid_consta
         if (*(volatile const int*)&h.tile[r].nrows < 0) break;
         if (i >= 2 && !mbar_wait_lean(smem_u32(&h.acc_empty[b]), (uint32_t)(((i >> 1) - 1) & 1), status)) break;
         tc_fence_after();
-        // two accumulators (channels 0-15 and 16-31 of every offset), added
-        // in the epilogue.  A tile is two laps of the 7-slot ring, each lap
-        // unrolled, so the ring slots are constants and the single issuing
-        // thread spends a few instructions per MMA (an issue loop with
-        // run-time ring bookkeeping costs more cycles per MMA than a
-        // 128 x 64 x 16 MMA takes to execute).
-        const uint32_t d0 = tmem + (uint32_t)(2 * b) * acc_cols, d1 = d0 + acc_cols;
+        // one accumulator per tile; a ring slot holds offsets 4k .. 4k+3 of
+        // the tile (the last slot 24 .. 26), two MMAs each (input channels
+        // 0-15, 16-31), one commit per slot
+        const uint32_t d = tmem + (uint32_t)b * acc_cols;
         uint64_t bd = bdesc0;
 #pragma unroll 1
-        for (int lap = 0; lap < 2; ++lap) {
+        for (int k = 0; k < kHaloTileStages / 2; ++k) {
+          mbar_wait_lean(afull0 + (uint32_t)(m_ps * 8), m_ph, status);
+          tc_fence_after();
+          const uint32_t ta = abase + (uint32_t)(m_ps * 64);
 #pragma unroll
-          for (int j = 0; j < kHaloRing; ++j) {
-            mbar_wait_lean(afull0 + (uint32_t)(j * 8), (uint32_t)lap, status);
-            tc_fence_after();
-            const uint32_t ta = abase + (uint32_t)(j * 32);
-            const uint32_t acc = (j > 0 || lap > 0) ? 1u : 0u;
-            umma_bf16_ts(d0, ta, bd, idesc, acc);
-            umma_bf16_ts(d1, ta + 8u, bd + 2u, idesc, acc);
-            if (j < kHaloRing - 1 || lap == 0) {  // the last stage holds offset 26 alone
-              umma_bf16_ts(d0, ta + 16u, bd + bo2, idesc, 1u);
-              umma_bf16_ts(d1, ta + 24u, bd + bo2 + 2u, idesc, 1u);
+          for (int o = 0; o < 4; ++o) {
+            if (o < 3 || k < kHaloTileStages / 2 - 1) {
+              umma_bf16_ts(d, ta + (uint32_t)(16 * o), bd, idesc, (k > 0 || o > 0) ? 1u : 0u);
+              umma_bf16_ts(d, ta + (uint32_t)(16 * o + 8), bd + 2u, idesc, 1u);
             }
-            umma_commit(aempty0 + (uint32_t)(j * 8));
-            bd += 2u * bo2;
+            bd += bo2;
+          }
+          umma_commit(aempty0 + (uint32_t)(m_ps * 8));
+          if (++m_ps == S) {
+            m_ps = 0;
+            m_ph ^= 1u;
           }
         }
         umma_commit(smem_u32(&h.acc_full[b]));
@@ -2345,14 +2336,10 @@ __global__ void __launch_bounds__(kUnThreads, 1) k_conv_halo(const __grid_consta
       const int64_t q = m < ca ? *(volatile const int64_t*)&t.q0a + m : *(volatile const int64_t*)&t.q0b + (m - ca);
       if (!__all_sync(0xffffffffu, mbar_wait_lean(smem_u32(&h.acc_full[b]), (uint32_t)((i >> 1) & 1), status))) break;
       tc_fence_after();
-      const uint32_t trow = tmem + (uint32_t)(2 * b) * acc_cols + ((uint32_t)(quarter * 32) << 16);
+      const uint32_t trow = tmem + (uint32_t)b * acc_cols + ((uint32_t)(quarter * 32) << 16);
       for (int c = 0; c < cout; c += 16) {
-        uint32_t v[16], w2[16];
-        tmem_ld16_nowait(trow + (uint32_t)c, v);
-        tmem_ld16_nowait(trow + acc_cols + (uint32_t)c, w2);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) + __uint_as_float(w2[e]));  // the two chains
+        uint32_t v[16];
+        tmem_ld16(trow + (uint32_t)c, v);
         const int ncol = min(16, cs - c);  // 16, 8 (cout_store an odd multiple of 8) or none
         if (m >= nrows || ncol <= 0) continue;
         if (out_bf16) {
@@ -3065,8 +3052,8 @@ fvx_status launch_conv_halo(const char* who, fvx_grid gin, fvx_kmap m, fvx_dtype
   a.out_bf16 = (dt == FVX_BF16_OUT_BF16) ? 1 : 0;
   int cols = 32;
   while (cols < cout) cols <<= 1;
-  a.acc_cols = cols;                                          // per accumulator: two tiles x two chains
-  a.stages = kHaloRing;  // A stages of 32 columns: 224 beside the four accumulators
+  a.acc_cols = cols;                                          // one accumulator per tile, two tiles
+  a.stages = std::min((512 - 2 * cols) / 64, kHaloMaxPairs);  // A slots of 64 columns beside the two accumulators
   a.w_bytes = (int)((27 * cout * kHaloRowB + 1023) & ~(int64_t)1023);  // a multiple of 1024 already
   const size_t smem = 1024 + (size_t)a.w_bytes + (size_t)kHaloPoolRows * kHaloRowB + sizeof(HaloHead);
   int optin = 0, dev = 0;
