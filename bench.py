@@ -451,9 +451,11 @@ def time_forward(fvx, torch, wl, K, warmup, flush, peaks, peak_kind, sm_count, w
         durs = each[kn]
         per_step = len(durs) // K if K else 0
         mine = []
-        if per_step == len(same):
+        L = 1  # launches per conv (the halo-staged kernel runs one per 32 input channels)
+        if per_step and per_step % len(same) == 0:
+            L = per_step // len(same)
             pos = same.index(i)
-            mine = durs[pos::per_step]
+            mine = [sum(durs[k * per_step + pos * L:k * per_step + (pos + 1) * L]) for k in range(K)]
         sec = sum(mine) / 1e3 if mine else t[f"conv{i}"]
         nk = len(mine) if mine else K
         # algorithmic bytes: feats read once, output written once (4 B fp32 /
@@ -468,7 +470,7 @@ def time_forward(fvx, torch, wl, K, warmup, flush, peaks, peak_kind, sm_count, w
         rl = conv_roofline(flops_i[i] * nk, alg * nk, sec, wl.fp32, peaks, peak_kind, sm_count)
         per_conv.append(dict(conv=f"{c['cin']}->{c['cout']} stride {c['stride']}", kernel=kn, pairs=int(p),
                              mean_pairs_per_output=round(p / wl.n_out[i], 3),
-                             kernel_ms=round(sec / nk * 1e3, 5), call_ms=round(t[f"conv{i}"] / K * 1e3, 5),
+                             kernel_ms=round(sec / nk * 1e3, 5), launches=L, call_ms=round(t[f"conv{i}"] / K * 1e3, 5),
                              active_pair_tflops=round(flops_i[i] * nk / sec / 1e12, 3),
                              algorithmic_bytes=int(alg), flops=int(flops_i[i]), roofline=rl,
                              kernel_timing="CUDA events around each launch" if mine else "call events"))
@@ -666,8 +668,9 @@ def bench_fvx(args, world, rank, local):
     same = [c for c in entry["convs"] if c["kernel"] == cv["kernel"]]
     roofline.update(kernel=cv["kernel"], conv=cv["conv"],
                     traffic=profiled_traffic(cv["kernel"], w["name"]) if len(same) == 1 else None,
-                    algorithmic_bytes=cv["algorithmic_bytes"], flops=cv["flops"], avg_launch_ms=cv["kernel_ms"],
-                    launches_per_step=1)
+                    algorithmic_bytes=cv["algorithmic_bytes"], flops=cv["flops"],
+                    avg_launch_ms=round(cv["kernel_ms"] / cv["launches"], 5), launches_per_step=cv["launches"],
+                    per="conv call (all its launches)")
     e2e = e2e_forward(fvx, torch, wl, K, world)
     del wl
 

@@ -226,9 +226,10 @@ fvx_status fvx_sparse_conv(fvx_grid gin, fvx_grid gout, fvx_kmap m, fvx_dtype dt
  *   FVX_CONV_AUTO    (default) leaf-densified when the map has stride 1,
  *                    cin is 8 or 16, cout <= 64 and the output grid's leaves
  *                    are at least 20% occupied on average; halo-staged when
- *                    the map has stride 1, cin is 32, cout <= 64 and the
- *                    output leaves hold at least 48 active voxels on
- *                    average; pair-list gather otherwise.
+ *                    the map has stride 1, cin is 32 (or a larger multiple
+ *                    of 32 with fp32 output), cout <= 64 and the output
+ *                    leaves hold at least 48 active voxels on average;
+ *                    pair-list gather otherwise.
  *   FVX_CONV_GATHER  always the pair-list kernels (128 consecutive outputs
  *                    per tile), direct (below).
  *   FVX_CONV_DIRECT  the pair-list kernel that fetches every pair's input row
@@ -245,8 +246,10 @@ fvx_status fvx_sparse_conv(fvx_grid gin, fvx_grid gout, fvx_kmap m, fvx_dtype dt
  *                    that hold an input voxel; the operands of the leaf's
  *                    active outputs, 128 per tile, built from there in tensor
  *                    memory; the pair lists are not read, the map's leaf table
- *                    is); a call it cannot serve (stride 2, a transposed map,
- *                    cin other than 32, cout > 64) fails with
+ *                    is); one pass per 32 input channels, the passes after
+ *                    the first adding to the fp32 output; a call it cannot
+ *                    serve (stride 2, a transposed map, cin not a multiple
+ *                    of 32, cin > 32 with bf16 output, cout > 64) fails with
  *                    FVX_ERR_INVALID_ARG.
  *   FVX_CONV_LEAF    always leaf-densified (each output leaf's 10^3 input
  *                    window staged densely in shared memory; the pair lists

@@ -1896,8 +1896,8 @@ struct HaloHead {
 };
 
 struct HaloArgs {
-  const __nv_bfloat16* x;   // feats [n_in][32] bf16
-  const __nv_bfloat16* wt;  // [27][cout][32] bf16
+  const __nv_bfloat16* x;   // feats: 32 bf16 channels of each row, rows x_stride elements apart
+  const __nv_bfloat16* wt;  // [27][cout][32] bf16, rows w_stride elements apart
   const uint64_t* in_rec;   // input grid leaf records [L][10]
   const int32_t* nbr;       // [L_out][27] input leaf per leaf offset, -1 absent
   const uint64_t* out_rec;  // output grid leaf records [L_out][10]
@@ -1905,6 +1905,8 @@ struct HaloArgs {
   uint32_t* status;
   int64_t n_leaf_out;
   int cout, cout_store, out_bf16, stages, acc_cols, w_bytes;
+  int x_stride, w_stride;  // cin of the layer: this launch takes 32 of its channels
+  int accumulate;          // add to the fp32 output (the passes after the first)
 };
 
 // A operand from tensor memory (row m in lane m, bf16 pairs along the columns).
@@ -2027,7 +2029,7 @@ __device__ void halo_loader(HaloHead& h, const HaloArgs& a, unsigned char* pool,
           const int prow = (ucur + base) % kHaloPoolRows;
           v = (int16_t)prow;
           const uint32_t row = e == 0 ? r_lo : e == 9 ? r_hi : r_mid + (uint32_t)__popc((act >> 1) & ((1u << (e - 1)) - 1u));
-          const __nv_bfloat16* src = a.x + (size_t)row * 32;
+          const __nv_bfloat16* src = a.x + (size_t)row * a.x_stride;
 #pragma unroll
           for (int p = 0; p < 4; ++p) cp_async16_row(pbase + swz_off(prow, p, kHaloRowB), src + 8 * p);
           ++base;
@@ -2253,7 +2255,7 @@ __global__ void __launch_bounds__(kUnThreads, 1) k_conv_halo(const __grid_consta
   // weights, once: row s*cout + co holds wt[s][co][0..31] (64 B, 64-byte swizzle)
   for (int e = tid; e < 27 * cout * 4; e += kUnThreads) {
     const int rr = e >> 2, p = e & 3;
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.wt + (size_t)rr * 32 + 8 * p));
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.wt + (size_t)rr * a.w_stride + 8 * p));
     *reinterpret_cast<uint4*>(wsm + swz_off(rr, p, kHaloRowB)) = v;
   }
   fence_proxy_async();  // the tensor core reads what the generic proxy wrote
@@ -2356,12 +2358,28 @@ __global__ void __launch_bounds__(kUnThreads, 1) k_conv_halo(const __grid_consta
           dst[0] = v0;
           if (ncol == 16) dst[1] = v1;
         } else {
-          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<float*>(a.y) + q * cs + c);
-          dst[0] = make_uint4(v[0], v[1], v[2], v[3]);
-          dst[1] = make_uint4(v[4], v[5], v[6], v[7]);
+          float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.y) + q * cs + c);
+          float4 f[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            f[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]), __uint_as_float(v[4 * e + 2]),
+                               __uint_as_float(v[4 * e + 3]));
+          if (a.accumulate) {  // the earlier passes' sums over other input channels
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              if (e >= 2 && ncol != 16) break;
+              const float4 o = dst[e];
+              f[e].x += o.x;
+              f[e].y += o.y;
+              f[e].z += o.z;
+              f[e].w += o.w;
+            }
+          }
+          dst[0] = f[0];
+          dst[1] = f[1];
           if (ncol == 16) {
-            dst[2] = make_uint4(v[8], v[9], v[10], v[11]);
-            dst[3] = make_uint4(v[12], v[13], v[14], v[15]);
+            dst[2] = f[2];
+            dst[3] = f[3];
           }
         }
       }
@@ -3031,16 +3049,22 @@ fvx_status launch_conv_leaf(const char* who, fvx_grid gin, fvx_kmap m, const int
   return FVX_OK;
 }
 
-// Halo-staged launch (stride-1 forward map with its leaf table, cin 32, MMA N
-// = cout <= 64): persistent, one block per SM; the weights resident in shared
-// memory beside the window pool, the A ring in the tensor memory the four
-// accumulators (two tiles x two chains) leave free.
-fvx_status launch_conv_halo(const char* who, fvx_grid gin, fvx_kmap m, fvx_dtype dt, const void* feats, int64_t cout,
-                            int64_t cout_store, void* out, const __nv_bfloat16* wt, uint32_t* status, cudaStream_t s) {
+// Halo-staged launch (stride-1 forward map with its leaf table, cin a multiple
+// of 32, MMA N = cout <= 64): persistent, one block per SM; the weights
+// resident in shared memory beside the window pool, the A ring in the tensor
+// memory the two accumulators leave free.  One launch per 32 input channels:
+// the first writes the output, the others add to it (fp32 output only when
+// cin > 32).
+fvx_status launch_conv_halo(const char* who, fvx_grid gin, fvx_kmap m, fvx_dtype dt, const void* feats, int64_t cin,
+                            int64_t cout, int64_t cout_store, void* out, const __nv_bfloat16* wt, uint32_t* status,
+                            cudaStream_t s) {
   const fvx_grid_s* go = m->gout;
   HaloArgs a;
   a.x = (const __nv_bfloat16*)feats;
   a.wt = wt;
+  a.x_stride = (int)cin;
+  a.w_stride = (int)cin;
+  a.accumulate = 0;
   a.in_rec = gin->leaf_rec;
   a.nbr = m->leaf_nbr;
   a.out_rec = go->leaf_rec;
@@ -3067,11 +3091,16 @@ fvx_status launch_conv_halo(const char* who, fvx_grid gin, fvx_kmap m, fvx_dtype
   int sms = 0;
   FVX_TRY(device_sm_count(&sms));
   const int64_t grid = std::min<int64_t>(go->n_leaf, (int64_t)sms);
-  {
-    LaunchScope ls("conv_halo", s);
-    k_conv_halo<<<(unsigned)grid, kUnThreads, smem, s>>>(a);
+  for (int64_t c0 = 0; c0 < cin; c0 += 32) {
+    a.x = (const __nv_bfloat16*)feats + c0;
+    a.wt = wt + c0;
+    a.accumulate = c0 > 0 ? 1 : 0;
+    {
+      LaunchScope ls("conv_halo", s);
+      k_conv_halo<<<(unsigned)grid, kUnThreads, smem, s>>>(a);
+    }
+    FVX_TRY(check_launch("conv_halo"));
   }
-  FVX_TRY(check_launch("conv_halo"));
   t_last_algo = FVX_CONV_HALO;
   t_last_kernel = "conv_halo";
   return FVX_OK;
@@ -3151,21 +3180,22 @@ fvx_status launch_conv_bf16(const char* who, fvx_grid gin, fvx_kmap m, fvx_dtype
   const bool dense_leaves = go->n_leaf > 0 && (double)go->n_active >= 0.2 * 512.0 * (double)go->n_leaf;
   if (leaf_ok && (algo == FVX_CONV_LEAF || (algo == FVX_CONV_AUTO && dense_leaves)))
     return launch_conv_leaf(who, gin, m, m->leaf_nbr, dt, feats, cin, cout, cout, out, wt, status, s);
-  // halo-staged: stride 1, cin 32; automatic when the output leaves hold at
-  // least kHaloAutoPerLeaf active voxels on average (sparser leaves leave
-  // most of each 128-row tile empty)
-  const bool halo_ok =
-      m->stride == 1 && m->leaf_nbr != nullptr && cin == 32 && cout <= kHaloMaxCout && gin->n_active > 0;
+  // halo-staged: stride 1, cin a multiple of 32 (32 channels per launch;
+  // more than 32 only with fp32 output, which the later launches add to);
+  // automatic when the output leaves hold at least kHaloAutoPerLeaf active
+  // voxels on average (sparser leaves leave most of each 128-row tile empty)
+  const bool halo_ok = m->stride == 1 && m->leaf_nbr != nullptr && cin % 32 == 0 &&
+                       (cin == 32 || dt == FVX_BF16) && cout <= kHaloMaxCout && gin->n_active > 0;
   if (algo == FVX_CONV_HALO && !halo_ok) {
-    set_error("%s: the halo-staged convolution needs a forward stride-1 map, cin 32 and cout <= %d (got stride "
-              "%d%s, %lld, %lld)",
+    set_error("%s: the halo-staged convolution needs a forward stride-1 map, cin a multiple of 32 (fp32 output "
+              "when cin > 32) and cout <= %d (got stride %d%s, %lld, %lld)",
               who, kHaloMaxCout, (int)m->stride, m->transposed ? " transposed" : "", (long long)cin,
               (long long)cout_real);
     return FVX_ERR_INVALID_ARG;
   }
   const bool halo_auto = go->n_leaf > 0 && (double)go->n_active >= kHaloAutoPerLeaf * (double)go->n_leaf;
   if (halo_ok && (algo == FVX_CONV_HALO || (algo == FVX_CONV_AUTO && halo_auto))) {
-    const fvx_status st = launch_conv_halo(who, gin, m, dt, feats, cout, cout_real, out, wt, status, s);
+    const fvx_status st = launch_conv_halo(who, gin, m, dt, feats, cin, cout, cout_real, out, wt, status, s);
     if (st != FVX_ERR_CAPACITY || algo == FVX_CONV_HALO) return st;
   }
   ConvArgs a;

@@ -1,8 +1,9 @@
-"""The halo-staged bf16 convolution (stride 1, cin 32: each output leaf's
-10^3 input window fetched once into shared memory at the positions that hold
-an input voxel, the operands of the leaf's active outputs built from there, 128
-outputs per tile) against the CPU oracle and against the direct pair-list
-kernel, forced through fvx_set_conv_algo.
+"""The halo-staged bf16 convolution (stride 1, 32 input channels per pass:
+each output leaf's 10^3 input window fetched once into shared memory at the
+positions that hold an input voxel, the operands of the leaf's active outputs
+built from there, 128 outputs per tile; wider inputs in several passes that
+add to the fp32 output) against the CPU oracle and against the direct
+pair-list kernel, forced through fvx_set_conv_algo.
 
 Narrow-band, random-sparse and solid grids (one to four tiles per leaf, tiles
 that take the tail of one leaf and the head of the next, the persistent loop
@@ -81,12 +82,43 @@ def test_halo_matches_oracle_and_direct(cuda_device, case, cout):
     yd, kd = _conv_with(fvx.FVX_CONV_DIRECT, g, g, km, x, W)
     assert kd == "conv_bf16_tma"
     G.assert_conv_close(G.np_(yd), yo, ao, G.BF16_TOL)
-    # the same products; the halo kernel sums input channels 0-15 and 16-31 in
-    # two fp32 chains and adds them, the direct kernel in one: equal up to
-    # fp32 rounding (relative to sum|w*x|)
+    # the same products, summed in fp32 in offset order by both kernels (the
+    # direct kernel skips offsets absent from a whole tile): equal up to fp32
+    # rounding (relative to sum|w*x|)
     assert np.all(np.abs(G.np_(y) - G.np_(yd)) <= 1e-5 * ao + 1e-30)
     yb, _ = _conv_with(fvx.FVX_CONV_HALO, g, g, km, x, W, out_dtype=torch.bfloat16)
     assert torch.equal(yb, y.bfloat16())
+
+
+@pytest.mark.parametrize("case,cin,cout", [("band", 64, 64), ("dense", 64, 32), ("solid", 96, 64), ("sparse", 64, 48),
+                                            ("band", 128, 16)])
+def test_halo_passes_match_oracle_and_direct(cuda_device, case, cin, cout):
+    """cin a multiple of 32 above 32: one pass per 32 input channels, the later
+    passes adding to the fp32 output."""
+    import torch
+
+    import sparse_convolution_gb300 as fvx
+
+    coords, offs = _coords(case)
+    g = G.gpu_grid(coords, offs)
+    og = oracle.Grid.build(coords, offs)
+    km = fvx.KernelMap(g, g, 1)
+    okm = oracle.KernelMap(og, og, 1)
+    x, W = G.bf16_inputs(7 + cin + cout, g.n_active, cin, cout)
+    y, kern = _conv_with(fvx.FVX_CONV_HALO, g, g, km, x, W)
+    assert kern == "conv_halo" and y.dtype == torch.float32
+    yo, ao = oracle.conv(okm, G.as_f64(x), G.as_f64(W))
+    G.assert_conv_close(G.np_(y), yo, ao, G.BF16_TOL)
+    yd, kd = _conv_with(fvx.FVX_CONV_DIRECT, g, g, km, x, W)
+    assert kd == "conv_bf16_tma"
+    assert np.all(np.abs(G.np_(y) - G.np_(yd)) <= 1e-5 * ao + 1e-30)
+    # the sum of the 32-channel passes, each run on its own
+    parts = [_conv_with(fvx.FVX_CONV_HALO, g, g, km, x[:, c:c + 32].contiguous(), W[:, c:c + 32].contiguous())[0]
+             for c in range(0, cin, 32)]
+    acc = parts[0].clone()
+    for p_ in parts[1:]:
+        acc += p_
+    assert torch.equal(acc, y)
 
 
 def test_halo_unrelated_grids_and_identity(cuda_device):
@@ -143,6 +175,8 @@ def test_halo_single_voxel_shift_stencils(cuda_device):
 
 
 def test_halo_auto_choice(cuda_device):
+    import torch
+
     import sparse_convolution_gb300 as fvx
 
     w = synth.narrow_band(scale=0.06)
@@ -153,6 +187,8 @@ def test_halo_auto_choice(cuda_device):
     assert kern == "conv_halo"  # about 100 outputs per leaf
     x64, W64 = G.bf16_inputs(1, g.n_active, 64, 64)
     _, kern = _conv_with(fvx.FVX_CONV_AUTO, g, g, km, x64, W64)
+    assert kern == "conv_halo"  # two 32-channel passes, fp32 output
+    _, kern = _conv_with(fvx.FVX_CONV_AUTO, g, g, km, x64, W64, out_dtype=torch.bfloat16)
     assert kern == "conv_bf16_tma"
     _, kern = _conv_with(fvx.FVX_CONV_GATHER, g, g, km, x, W)
     assert kern == "conv_bf16_tma"
@@ -165,15 +201,18 @@ def test_halo_auto_choice(cuda_device):
 
 
 def test_halo_refusals(cuda_device):
+    import torch
+
     import sparse_convolution_gb300 as fvx
 
     coords, offs = _grid(6, 3000, 20, B=1)
     g = G.gpu_grid(coords, offs)
     km = fvx.KernelMap(g, g, 1)
-    for cin, cout in [(16, 32), (64, 64), (32, 128), (32, 256)]:
+    for cin, cout, od in [(16, 32, None), (48, 64, None), (32, 128, None), (32, 256, None),
+                          (64, 64, torch.bfloat16)]:
         x, W = G.bf16_inputs(1, g.n_active, cin, cout)
         with pytest.raises(fvx.FvxError) as e:
-            _conv_with(fvx.FVX_CONV_HALO, g, g, km, x, W)
+            _conv_with(fvx.FVX_CONV_HALO, g, g, km, x, W, out_dtype=od)
         assert e.value.status == "FVX_ERR_INVALID_ARG"
     x, W = G.bf16_inputs(1, g.n_active, 32, 32)
     coarse = g.coarsen(2)
