@@ -28,6 +28,9 @@ namespace {
 
 constexpr int kKmThreads = 256;
 constexpr int kKmWarps = kKmThreads / 32;
+constexpr int kKm1WriteThreads = 128;  // stride-1 pair writer: a narrow band's leaf holds about 113 voxels
+static_assert(512 % kKm1WriteThreads == 0 && kKm1WriteThreads % 32 == 0 && kKm1WriteThreads >= 64,
+              "the writer's loops over 512 positions and 256 (offset, slice) entries");
 
 struct KmSmem {
   unsigned long long mask[27][8];
@@ -325,7 +328,7 @@ struct Km1WriteSmem {
 // its rank among the leaf's voxels with that neighbour, so the lanes of a
 // warp write consecutive entries of one list at a time.  Work scales with the
 // leaf's active voxels, not with its 512 positions.
-__global__ void __launch_bounds__(kKmThreads) k_kmap1_write(GridDev gin, const int32_t* __restrict__ out_origin,
+__global__ void __launch_bounds__(kKm1WriteThreads) k_kmap1_write(GridDev gin, const int32_t* __restrict__ out_origin,
                                                             const int32_t* __restrict__ out_batch,
                                                             const uint64_t* __restrict__ out_rec, int64_t n_out_leaf,
                                                             const uint32_t* __restrict__ starts,
@@ -336,7 +339,7 @@ __global__ void __launch_bounds__(kKmThreads) k_kmap1_write(GridDev gin, const i
   Km1Smem& sm = sw.k;
   const int lo = blockIdx.x, tid = threadIdx.x;
   km1_load(sm, gin, out_origin, out_batch, out_rec, lo, nbr_in, nullptr);
-  for (int h = tid; h < 1000; h += kKmThreads) {
+  for (int h = tid; h < 1000; h += kKm1WriteThreads) {
     const int hx = h / 100 - 1, hy = (h / 10) % 10 - 1, hz = h % 10 - 1;
     const int slot = ((hx + 8) >> 3) * 9 + ((hy + 8) >> 3) * 3 + ((hz + 8) >> 3);
     const int w = hx & 7, bit = ((hy & 7) << 3) | (hz & 7);
@@ -348,11 +351,12 @@ __global__ void __launch_bounds__(kKmThreads) k_kmap1_write(GridDev gin, const i
     }
     sw.hidx[h] = v;
   }
-  {
-    // the neighbour words of every (offset, slice), as the count pass had
-    // them; thread s * 8 + x, so the eight slices of an offset are eight
-    // consecutive lanes and their running pair counts one segmented scan
-    const int s = tid >> 3, x = tid & 7;
+  // the neighbour words of every (offset, slice), as the count pass had
+  // them; entry e = s * 8 + x, so the eight slices of an offset are eight
+  // consecutive lanes and their running pair counts one segmented scan
+#pragma unroll
+  for (int e0 = 0; e0 < 256; e0 += kKm1WriteThreads) {
+    const int s = (e0 + tid) >> 3, x = tid & 7;
     const unsigned long long R = (s < 27) ? km1_word(sm, s, x) : 0ull;
     const uint32_t c = (uint32_t)__popcll(R);
     uint32_t incl = c;
@@ -368,8 +372,8 @@ __global__ void __launch_bounds__(kKmThreads) k_kmap1_write(GridDev gin, const i
   }
   // active output voxels in index order
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int n = tid + h * 256;
+  for (int h = 0; h < 512 / kKm1WriteThreads; ++h) {
+    const int n = tid + h * kKm1WriteThreads;
     const int w = n >> 6, bit = n & 63;
     const unsigned long long m = sm.om[w];
     if ((m >> bit) & 1ull) {
@@ -379,7 +383,7 @@ __global__ void __launch_bounds__(kKmThreads) k_kmap1_write(GridDev gin, const i
   }
   const int nvox = (int)(((sm.opre9 >> 54) & 511ull) + (unsigned long long)__popcll(sm.om[7]));
   __syncthreads();
-  for (int idx = tid; idx < nvox; idx += kKmThreads) {
+  for (int idx = tid; idx < nvox; idx += kKm1WriteThreads) {
     const int n = sm.vox[idx], x = n >> 6, b = n & 63;
     const unsigned long long below = (1ull << b) - 1ull;
     const int h0 = (x + 1) * 100 + ((b >> 3) + 1) * 10 + (b & 7) + 1;  // the voxel's own halo position
@@ -570,7 +574,7 @@ fvx_status kernel_map_impl(const char* who, fvx_grid gin, fvx_grid gout, int32_t
   if (Lo > 0 && m->pair_capacity > 0) {
     LaunchScope ls("kmap_write", s);
     if (bitpar)
-      k_kmap1_write<<<(unsigned)Lo, kKmThreads, 0, s>>>(gd, gout->leaf_origin, gout->leaf_batch, gout->leaf_rec, Lo,
+      k_kmap1_write<<<(unsigned)Lo, kKm1WriteThreads, 0, s>>>(gd, gout->leaf_origin, gout->leaf_batch, gout->leaf_rec, Lo,
                                                         counts, nbr, m->in_idx, m->out_idx, transposed ? 1 : 0);
     else
       k_kmap_write<<<(unsigned)Lo, kKmThreads, 0, s>>>(gd, gout->leaf_origin, gout->leaf_batch, gout->leaf_rec, Lo,
