@@ -28,9 +28,7 @@ namespace {
 
 constexpr int kKmThreads = 256;
 constexpr int kKmWarps = kKmThreads / 32;
-constexpr int kKm1WriteThreads = 128;  // stride-1 pair writer: a narrow band's leaf holds about 113 voxels
-static_assert(512 % kKm1WriteThreads == 0 && kKm1WriteThreads % 32 == 0 && kKm1WriteThreads >= 64,
-              "the writer's loops over 512 positions and 256 (offset, slice) entries");
+
 
 struct KmSmem {
   unsigned long long mask[27][8];
@@ -328,6 +326,10 @@ struct Km1WriteSmem {
 // its rank among the leaf's voxels with that neighbour, so the lanes of a
 // warp write consecutive entries of one list at a time.  Work scales with the
 // leaf's active voxels, not with its 512 positions.
+// kKm1WriteThreads: 128 for sparse leaves (a narrow band's leaf holds about
+// 113 voxels, so a 256-thread block would idle half its warps in the voxel
+// loop), 256 for leaves with more than 200 voxels on average.
+template <int kKm1WriteThreads>
 __global__ void __launch_bounds__(kKm1WriteThreads) k_kmap1_write(GridDev gin, const int32_t* __restrict__ out_origin,
                                                             const int32_t* __restrict__ out_batch,
                                                             const uint64_t* __restrict__ out_rec, int64_t n_out_leaf,
@@ -335,6 +337,8 @@ __global__ void __launch_bounds__(kKm1WriteThreads) k_kmap1_write(GridDev gin, c
                                                             const int32_t* __restrict__ nbr_in,
                                                             int32_t* __restrict__ in_idx,
                                                             int32_t* __restrict__ out_idx, int mirror) {
+  static_assert(512 % kKm1WriteThreads == 0 && kKm1WriteThreads % 32 == 0 && kKm1WriteThreads >= 64,
+                "the writer's loops over 512 positions and 256 (offset, slice) entries");
   __shared__ Km1WriteSmem sw;
   Km1Smem& sm = sw.k;
   const int lo = blockIdx.x, tid = threadIdx.x;
@@ -573,12 +577,17 @@ fvx_status kernel_map_impl(const char* who, fvx_grid gin, fvx_grid gout, int32_t
   }
   if (Lo > 0 && m->pair_capacity > 0) {
     LaunchScope ls("kmap_write", s);
-    if (bitpar)
-      k_kmap1_write<<<(unsigned)Lo, kKm1WriteThreads, 0, s>>>(gd, gout->leaf_origin, gout->leaf_batch, gout->leaf_rec, Lo,
+    if (bitpar) {
+      if ((double)Nout > 200.0 * (double)Lo)
+        k_kmap1_write<256><<<(unsigned)Lo, 256, 0, s>>>(gd, gout->leaf_origin, gout->leaf_batch, gout->leaf_rec, Lo,
                                                         counts, nbr, m->in_idx, m->out_idx, transposed ? 1 : 0);
-    else
+      else
+        k_kmap1_write<128><<<(unsigned)Lo, 128, 0, s>>>(gd, gout->leaf_origin, gout->leaf_batch, gout->leaf_rec, Lo,
+                                                        counts, nbr, m->in_idx, m->out_idx, transposed ? 1 : 0);
+    } else {
       k_kmap_write<<<(unsigned)Lo, kKmThreads, 0, s>>>(gd, gout->leaf_origin, gout->leaf_batch, gout->leaf_rec, Lo,
                                                        stride, transposed ? 1 : 0, counts, m->in_idx, m->out_idx);
+    }
   }
   FVX_TRY(check_launch("kmap_write"));
   // conv tiling: where each tile's pairs start in every list

@@ -179,6 +179,8 @@ def test_leaf_between_unrelated_grids(cuda_device):
 
 
 def test_auto_choice(cuda_device, dense_case, sparse_case):
+    import torch
+
     import sparse_convolution_gb300 as fvx
 
     for case, want in ((dense_case, fvx.FVX_CONV_LEAF), (sparse_case, fvx.FVX_CONV_GATHER)):
@@ -190,8 +192,10 @@ def test_auto_choice(cuda_device, dense_case, sparse_case):
     x, W = G.bf16_inputs(3, g.n_active, 32, 32)  # too many channels for the leaf kernel: the halo-staged one
     fvx.sparse_conv(g, g, km, x, W)
     assert fvx.last_conv_algo() == fvx.FVX_CONV_HALO
-    x, W = G.bf16_inputs(3, g.n_active, 64, 32)  # neither leaf kernel: pair lists
+    x, W = G.bf16_inputs(3, g.n_active, 64, 32)  # fp32 output: two halo-staged passes of 32 channels
     fvx.sparse_conv(g, g, km, x, W)
+    assert fvx.last_conv_algo() == fvx.FVX_CONV_HALO
+    fvx.sparse_conv(g, g, km, x, W, out_dtype=torch.bfloat16)  # bf16 output: pair lists
     assert fvx.last_conv_algo() == fvx.FVX_CONV_GATHER
 
 
