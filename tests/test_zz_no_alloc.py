@@ -118,6 +118,35 @@ def test_noalloc_leaf_kernel(cuda_device):
         fvx.set_conv_algo(fvx.FVX_CONV_AUTO)
 
 
+def test_noalloc_halo_passes(cuda_device):
+    """The halo-staged kernel through the allocation-free entry point, on a
+    grid whose leaves hold enough outputs for the automatic choice to take
+    it, with 64 input channels: two 32-channel launches, the second adding to
+    the fp32 output; equal to the allocating call, twice in a row."""
+    import torch
+
+    import sparse_convolution_gb300 as fvx
+
+    lib = fvx.load()
+    rng = np.random.default_rng(11)
+    c = rng.integers(-12, 12, size=(14000, 3)).astype(np.int32)  # about 64% of a 24^3 box
+    g = fvx.Grid.build(torch.from_numpy(c).cuda(), [0, len(c)])
+    km = fvx.KernelMap(g, g, 1)
+    for call in range(2):
+        gen = torch.Generator(device="cuda").manual_seed(300 + call)
+        x = torch.randn(g.n_active, 64, device="cuda", generator=gen).bfloat16()
+        W = (torch.randn(27, 64, 64, device="cuda", generator=gen) / 40.0).bfloat16()
+        ref = torch.empty(g.n_active, 64, device="cuda")
+        got = torch.full((g.n_active, 64), float("nan"), device="cuda")
+        assert _call(lib.fvx_sparse_conv, g, km, fvx.FVX_BF16, x, W, ref) == 0, lib.fvx_last_error()
+        assert fvx.last_conv_kernel() == "conv_halo"
+        assert _call(lib.fvx_sparse_conv_noalloc, g, km, fvx.FVX_BF16, x, W, got) == 0, lib.fvx_last_error()
+        assert fvx.last_conv_kernel() == "conv_halo"
+        assert lib.fvx_noalloc_status(ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)) == 0
+        torch.cuda.synchronize()
+        assert torch.equal(got, ref)
+
+
 ALLOC_FN = ctypes.CFUNCTYPE(ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p)
 FREE_FN = ctypes.CFUNCTYPE(None, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p)
 
