@@ -29,7 +29,6 @@ namespace {
 constexpr int kKmThreads = 256;
 constexpr int kKmWarps = kKmThreads / 32;
 
-
 struct KmSmem {
   unsigned long long mask[27][8];
   unsigned long long pre9[27];
