@@ -1937,14 +1937,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Window loader (warps 0-3, thread lt = 0..127).  Thread c < 100 owns window
 // column c = (hx+1)*10 + hy+1: the ten positions hz = -1..8 above (hx, hy),
@@ -2085,10 +2077,11 @@ __device__ void halo_loader(HaloHead& h, const HaloArgs& a, unsigned char* pool,
 
 // Operand-row warps (ct = thread 0.. of warps 4 .. 4 + kHaloRowWarps - 1).
 // Warp group g = ct / 128 writes offsets 4i + g, 4i + g + kHaloGroups, .. of
-// ring slot i; thread = tile row m in its warp's TMEM lane quarter.  Tiles are packed here: 128 rows from the current leaf, or
-// its remaining rows and then the head of the block's next leaf (when the
-// current window is small enough that the next one always fits in the pool
-// beside it).  Returns the number of stages produced.
+// ring slot i; thread = tile row m in its warp's TMEM lane quarter.  Tiles
+// are packed here: 128 rows from the current leaf, or its remaining rows and
+// then the head of the block's next leaf (when the current window is small
+// enough that the next one always fits in the pool beside it).  Returns the
+// number of ring slots filled.
 __device__ int64_t halo_rows(HaloHead& h, const HaloArgs& a, const unsigned char* pool, uint32_t tmem, int ct) {
   const int64_t G = gridDim.x, nL = a.n_leaf_out;
   const int64_t nW = ((int64_t)blockIdx.x < nL) ? (nL - 1 - (int64_t)blockIdx.x) / G + 1 : 0;  // this block's leaves
