@@ -253,14 +253,6 @@ def cpu_baseline(w):
 
 
 # ---------------------------------------------------------------- GPU arm
-def conv_kernel_name(fvx, algo, fp32, cin):
-    if fp32:
-        return "conv_f32"
-    if algo == fvx.FVX_CONV_LEAF:
-        return "conv_leaf"
-    return "conv_bf16_tma" if cin % 16 == 0 else "conv_bf16_tc"
-
-
 def ffma_peak(sm_count, peaks):
     """FP32 FFMA peak: SMs x 128 FP32 lanes x 2 flops x the maximum SM clock."""
     mhz = float(peaks.get("sm_max_mhz", 2070.0))

@@ -187,3 +187,44 @@ int main(void) {
     assert r.returncode == 0, r.stderr
     r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
     assert r.returncode == 0 and r.stdout.strip() == "ok", (r.returncode, r.stdout, r.stderr)
+
+
+def test_bench_roofline_arithmetic(tmp_path, monkeypatch):
+    """The bench line's roofline: tensor above the measured ridge, HBM below,
+    FFMA for fp32; achieved = algorithmic flops or bytes over the time; and
+    a kernel's DRAM traffic read from an ncu summary only while the source
+    hash the summary records matches the kernel's file."""
+    import hashlib
+    import sys
+
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+
+    peaks = {"hbm_gbs": 6785.2, "bf16_tflops": 1917.5, "sm_max_mhz": 2070.0}
+    ridge = 1917.5e12 / 6785.2e9  # flop per byte
+    r = bench.conv_roofline(flops=1e12, alg_bytes=1e12 / (2 * ridge), sec=1e-3, fp32=False, peaks=peaks,
+                            peak_kind="measured", sm_count=152)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and r["achieved"] == 1000.0
+    assert r["frac"] == round(1000.0 / 1917.5, 4)
+    r = bench.conv_roofline(flops=1e12, alg_bytes=2e12 / ridge, sec=1e-3, fp32=False, peaks=peaks,
+                            peak_kind="measured", sm_count=152)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert abs(r["achieved"] - 2e12 / ridge / 1e-3 / 1e9) < 0.1
+    r = bench.conv_roofline(flops=8.05e13, alg_bytes=1e9, sec=1.0, fp32=True, peaks=peaks, peak_kind="measured",
+                            sm_count=152)
+    assert r["bound"] == "alu" and abs(r["peak"] - 152 * 128 * 2 * 2070e6 / 1e12) < 0.1
+    # a summary in the committed format, over a stand-in source tree
+    src = tmp_path / "sparse_convolution_gb300" / "csrc"
+    src.mkdir(parents=True)
+    (src / "conv.cu").write_text("// kernel source\n")
+    sha = hashlib.sha256((src / "conv.cu").read_bytes()).hexdigest()
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "conv_halo_w.md").write_text(
+        f"source_sha256: {sha} (sparse_convolution_gb300/csrc/conv.cu)\n"
+        "| dram__bytes_read.sum | 100.0 | MB |\n"
+        "full launch: dram__bytes_read.sum 801.1 MB, dram__bytes_write.sum 2907.5 MB\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.profiled_traffic("conv_halo", "w") == int((801.1 + 2907.5) * 1e6)
+    assert bench.profiled_traffic("conv_halo", "other") is None
+    (src / "conv.cu").write_text("// kernel source, changed\n")
+    assert bench.profiled_traffic("conv_halo", "w") is None
